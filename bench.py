@@ -1,0 +1,343 @@
+#!/usr/bin/env python
+"""Benchmark of the DSA indexer decode step on GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic input
+(DecodePlan): paged MQA logits with the fused coarse histogram, the
+histogram-driven exact top-2048, block amax8, block top-512, the sorted block
+table, sparse logits over the chosen blocks (FP16) and the FP16 top-2048.
+
+Default workload: B=32 requests, next_n=1, L=131072 keys each, page size 64,
+'mixed' score distribution (heads 16..31 weighted x20) -- the configuration
+the >= 70 % HBM target of the logits kernel is stated on.  Inputs are resident
+in HBM; L2 (129 MB) is flushed by a 256 MiB write between timed steps.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the plain CPU
+oracle on the host cores instead (the reference arm of this comparison).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "indexer decode keys scored/s and HBM GB/s (% of peak); top-2048 rows/s"
+KEY_BYTES = 132  # 128 FP8 bytes of K + 4 bytes of kscale per key
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="c2")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget", type=float, default=12.0)
+    return p.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    lrank = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, lrank
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def traffic_record(kernel_src):
+    """Per-launch DRAM bytes of the logits kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged (sha256 recorded there)."""
+    path = os.path.join(ROOT, "profiles", "logits_fused_hist_c2.md")
+    try:
+        sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+        rec = {}
+        for line in open(path):
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                rec[k.strip()] = v.strip().strip("`")
+        if rec.get("source_sha256") == sha:
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class Clocks:
+    Q = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            if self.uuid and self.uuid not in f[0]:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_step_sample(case, nn, ps, b, k=2048, kb=512):
+    """The oracle's whole step for request b (all its rows): returns keys scored."""
+    from oracle import oracle as O
+    r0, r1 = b * nn, (b + 1) * nn
+    ctx = case["context_lens"][b:b + 1]
+    pt = case["page_table"][b:b + 1]
+    q = case["q"][r0:r1]
+    w = case["weights"][r0:r1]
+    L = O.paged_mqa_logits(q, case["kv"], case["kscale"], w, pt, ctx, nn, ps)
+    rl = O.row_lens(ctx, nn)
+    O.histogram(L, rl)
+    O.topk(L, rl, k)
+    A = O.block_amax8(L, rl, skip_le=kb)
+    t, _, vl = O.block_table(A, rl, np.zeros(nn, np.int32), kb, pt, ps)
+    sp = O.sparse_logits(q, case["kv"], case["kscale"], w, pt, rl, np.zeros(nn, np.int32), ps, t)
+    O.topk_fp16(O.fp16_rn_array(sp), vl, k, t)
+    return int(rl.sum())
+
+
+def run_reference(args, ws_, rank):
+    import synthetic as S
+    if rank != 0:
+        return
+    w = S.named(args.workload)
+    case = S.generate(w)
+    for i in range(args.warmup):
+        oracle_step_sample(case, w.next_n, w.page_size, i % w.B)
+    t0 = time.perf_counter()
+    keys = 0
+    for i in range(args.steps):
+        keys += oracle_step_sample(case, w.next_n, w.page_size, i % w.B)
+    dt = time.perf_counter() - t0
+    v = keys / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "keys/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample": "one request (all its rows) per step"},
+            "cpu_baseline": {"value": v, "unit": "keys/s", "cores": 1, "kind": "oracle",
+                             "sample": "each step: one request of the workload through the "
+                                       "whole oracle step (logits, histogram, top-2048, "
+                                       "amax8, block table, sparse logits, FP16 top-2048)"},
+            "e2e": {"value": v, "unit": "keys/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(case, w, budget):
+    t0 = time.perf_counter()
+    keys, n = 0, 0
+    while time.perf_counter() - t0 < budget and n < w.B:
+        keys += oracle_step_sample(case, w.next_n, w.page_size, n)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": keys / dt, "unit": "keys/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} request(s) of the workload ({keys} keys) through the whole "
+                      f"oracle step, {dt:.1f} s single-threaded"}
+
+
+def main():
+    args = parse()
+    world, rank, lrank = dist_env()
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    import synthetic as S
+    import dsa_sparse_attention_paged_gb300 as D
+    from dsa_sparse_attention_paged_gb300.pipeline import DecodePlan
+
+    torch.cuda.set_device(lrank)
+    dev = torch.device("cuda", lrank)
+    w = S.named(args.workload)
+    case = S.generate(w)
+    nn, ps = w.next_n, w.page_size
+    d = {k: (torch.from_numpy(v).to(dev) if isinstance(v, np.ndarray) else v)
+         for k, v in case.items()}
+    plan = DecodePlan(w.B, nn, max(w.context_lens), ps, k=2048, kb=512, two_level=True,
+                      device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    inputs = (d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"], d["context_lens"])
+
+    ctx = np.asarray(w.context_lens, dtype=np.int64)
+    rl = ctx[:, None] - (nn - 1 - np.arange(nn))[None, :]
+    keys_per_step = int(rl.sum())
+    logits_bytes = int(ctx.sum()) * KEY_BYTES + keys_per_step * 4 + w.R * 32 * (128 + 4)
+
+    for _ in range(args.warmup):
+        plan.step(*inputs)
+    torch.cuda.synchronize()
+    if plan.ws.status() != 0:
+        raise RuntimeError(f"device status {plan.ws.status():#x} after warm-up")
+
+    names = ["logits", "topk", "publish", "consume"]
+    K = args.steps
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    ev_k = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for n in names} for _ in range(K)]
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clk = Clocks(uuid)
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk.start()
+    time.sleep(0.2)
+    for i in range(K):
+        flush.fill_(i & 0xFF)  # evict the previous step's lines from L2
+        ev_step[i][0].record()
+        plan.step(*inputs, events=ev_k[i])
+        ev_step[i][1].record()
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    if dist is not None:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev_step]
+    kern_ms = {n: [e[n][0].elapsed_time(e[n][1]) for e in ev_k] for n in names}
+    t_total = sum(step_ms) / 1e3
+    if dist is not None:
+        t = torch.tensor([t_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_total = float(t.item())
+    if plan.ws.status() != 0:
+        raise RuntimeError(f"device status {plan.ws.status():#x} after timing")
+
+    # e2e through the public API with host buffers: per step, H2D of the
+    # step's decode inputs (q, weights, context lens, page table) from pinned
+    # memory, the step, D2H of both top-2048 index sets
+    host_in = {k: torch.from_numpy(case[k]).pin_memory()
+               for k in ("q", "weights", "context_lens", "page_table")}
+    host_out = [torch.empty_like(plan.topk_idx, device="cpu").pin_memory(),
+                torch.empty_like(plan.sparse_idx, device="cpu").pin_memory()]
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out)
+    Ke = max(1, min(K, 500))
+    ev_e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(Ke)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(Ke):
+        flush.fill_(i & 0xFF)
+        ev_e[i][0].record()
+        for k2, v in host_in.items():
+            d[k2].copy_(v, non_blocking=True)
+        a, b = plan.step(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"],
+                         d["context_lens"])
+        host_out[0].copy_(a, non_blocking=True)
+        host_out[1].copy_(b, non_blocking=True)
+        ev_e[i][1].record()
+    torch.cuda.synchronize()
+    e2e_s = sum(a.elapsed_time(b) for a, b in ev_e) / 1e3
+    if dist is not None:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = peaks()
+    lg_ms = statistics.mean(kern_ms["logits"])
+    achieved = logits_bytes / (lg_ms * 1e-3) / 1e9
+    ms_step = 1e3 * t_total / K
+    value = world * keys_per_step * K / t_total
+    cb = None
+    if not args.no_cpu_baseline:
+        cb = cpu_baseline(case, w, args.cpu_budget)
+    line = {
+        "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8e4m3 x fp8e4m3 -> f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "next_n": nn, "context_len": int(ctx.max()),
+                   "page_size": ps, "H": 32, "D": 128, "k": 2048, "k_blocks": 512,
+                   "dist": w.dist, "seed": w.seed, "parallelism": f"replicas x{world}",
+                   "l2": "flushed between timed steps (256 MiB write, outside the events)"},
+        "hbm_gbs_logits": achieved,
+        "top2048_rows_per_s": world * 2 * w.R * K / t_total,
+        "kernel_us": {n: 1e3 * statistics.mean(v) for n, v in kern_ms.items()},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "kernel": "logits_kernel<next_n=1, histogram>",
+                     "algorithmic_bytes_per_launch": logits_bytes,
+                     "traffic": traffic_record(os.path.join(
+                         ROOT, "dsa_sparse_attention_paged_gb300", "csrc", "logits.cu"))},
+        "cpu_baseline": cb,
+        "e2e": {"value": world * keys_per_step * Ke / e2e_s, "unit": "keys/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": 1e3 * e2e_s / Ke, "steps": Ke},
+        "gpu_launches": plan.launches_per_step * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,264 @@
+"""Python binding of the GB300 DSA indexer decode library (``include/dsa.h``).
+
+Argument marshalling only: every function here checks tensor dtypes, devices
+and shapes, turns tensors into device pointers and calls the C ABI of
+``_build/libdsa_gb300.so`` with the current CUDA stream.  All computation runs
+in the library's sm_103a kernels; there is no Python or CPU fallback, and
+importing this module fails loudly when the library has not been built.
+
+Functions have the C names without the ``dsa_`` prefix.  Row r = b*next_n + j
+of request b sees n_r = context_lens[b] - (next_n - 1 - j) keys.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libdsa_gb300.so")
+
+NUM_BINS = 1024
+MAX_TOPK = 2048
+CAND_CAP = 8192
+OUT_F32 = 0
+OUT_F16 = 1
+DEV_TIMEOUT = 0x1
+DEV_BOUNDS = 0x2
+INT32_MAX = 2**31 - 1
+
+_STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
+           3: "DSA_ERR_MISALIGNED", 4: "DSA_ERR_CUDA", 5: "DSA_ERR_WORKSPACE"}
+
+
+class DSAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        cuda = lib.dsa_last_cuda_error() if lib is not None else 0
+        super().__init__(f"{what}: {_STATUS.get(status, status)}"
+                         + (f" (cuda error {cuda})" if status == 4 else ""))
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"CUDA library not built: {LIB_PATH} is missing. Build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` or "
+            "`python -m dsa_sparse_attention_paged_gb300.build`.")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, sz, u32, u64 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                 ctypes.c_size_t, ctypes.c_uint32, ctypes.c_uint64)
+    sig = {
+        "dsa_status_string": (ctypes.c_char_p, [i32]),
+        "dsa_last_cuda_error": (i32, []),
+        "dsa_version": (i32, []),
+        "dsa_workspace_size": (sz, [i32]),
+        "dsa_workspace_init": (i32, [P, sz, P]),
+        "dsa_read_device_status": (i32, [P, P, ctypes.POINTER(u32)]),
+        "dsa_paged_mqa_logits": (i32, [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, i32, P,
+                                       i64, P, P, sz, P]),
+        "dsa_coarse_hist_topk": (i32, [P, i64, P, i32, i32, i32, P, i32, i32, P, P, P, sz, P]),
+        "dsa_block_amax8": (i32, [P, i64, P, i32, i32, i32, P, i64, P, sz, P]),
+        "dsa_sort_candidate_blocks": (i32, [P, i32, P, i32, i32, P, i64, i32, P, P, P, sz, P]),
+        "dsa_sparse_mqa_logits": (i32, [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, i32, P,
+                                        i32, P, i32, i64, P, sz, P]),
+        "dsa_topk_fp16": (i32, [P, i64, P, i32, i32, P, i32, P, P, sz, P]),
+        "dsa_coarse_bins_range": (i32, [u32, i64, P, P]),
+        "dsa_fp16_order_keys": (i32, [P, P, i64, P]),
+        "dsa_wait_timeout_selftest": (i32, [u64, P, sz, P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+lib = _load()
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise DSAError(st, what)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _req(t, dtype, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+
+
+def _u8(t):
+    return t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t
+
+
+class Workspace:
+    """Caller-owned scratch buffer shared by all calls (zero-filled at creation;
+    every completed call leaves it zeroed again)."""
+
+    def __init__(self, max_rows: int, device=None):
+        self.max_rows = int(max_rows)
+        self.nbytes = int(lib.dsa_workspace_size(self.max_rows))
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8,
+                               device=device if device is not None else "cuda")
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+    def init(self, stream=None):
+        _check(lib.dsa_workspace_init(self.ptr, self.nbytes, _stream(stream)), "workspace_init")
+
+    def status(self, stream=None) -> int:
+        out = ctypes.c_uint32(0)
+        _check(lib.dsa_read_device_status(self.ptr, _stream(stream), ctypes.byref(out)),
+               "read_device_status")
+        return int(out.value)
+
+
+def workspace_size(max_rows: int) -> int:
+    return int(lib.dsa_workspace_size(int(max_rows)))
+
+
+def paged_mqa_logits(q, kv_pages, kscale, weights, page_table, context_lens, next_n, ws,
+                     logits=None, logits_stride=None, histogram=None, stream=None):
+    """Dense logits [B*next_n][stride] (dead columns untouched) and, when
+    ``histogram`` is given, accumulate its coarse bins.  Returns logits."""
+    q, kv_pages = _u8(q), _u8(kv_pages)
+    _req(q, torch.uint8, "q")
+    _req(kv_pages, torch.uint8, "kv_pages")
+    _req(kscale, torch.float32, "kscale")
+    _req(weights, torch.float32, "weights")
+    _req(page_table, torch.int32, "page_table")
+    _req(context_lens, torch.int32, "context_lens")
+    R, H, D = q.shape
+    P, ps, D2 = kv_pages.shape
+    B = context_lens.shape[0]
+    if R != B * next_n or D2 != D:
+        raise ValueError("shape mismatch between q, kv_pages and context_lens")
+    if logits is None:
+        stride = int(logits_stride) if logits_stride is not None else None
+        if stride is None:
+            raise ValueError("give logits or logits_stride")
+        logits = torch.empty((R, stride), dtype=torch.float32, device=q.device)
+    _req(logits, torch.float32, "logits")
+    if histogram is not None:
+        _req(histogram, torch.int32, "histogram")
+    for t in (q, kv_pages, kscale, weights, page_table, context_lens):
+        assert t.is_contiguous()
+    _check(lib.dsa_paged_mqa_logits(
+        _p(q), _p(kv_pages), _p(kscale), _p(weights), _p(page_table), page_table.stride(0),
+        _p(context_lens), B, next_n, H, D, ps, P, _p(logits), logits.stride(0), _p(histogram),
+        ws.ptr, ws.nbytes, _stream(stream)), "paged_mqa_logits")
+    return logits
+
+
+def coarse_hist_topk(logits, context_lens, next_n, k, ws, histogram=None, reset_histogram=False,
+                     len_div=1, out=None, fallback_flags=None, R=None, stream=None):
+    """Exact top-k columns per row ([R][k] int32, -1 padded, order unspecified)."""
+    _req(logits, torch.float32, "logits")
+    _req(context_lens, torch.int32, "context_lens")
+    R = logits.shape[0] if R is None else R
+    if out is None:
+        out = torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    _req(out, torch.int32, "out")
+    if histogram is not None:
+        _req(histogram, torch.int32, "histogram")
+    if fallback_flags is not None:
+        _req(fallback_flags, torch.int32, "fallback_flags")
+    _check(lib.dsa_coarse_hist_topk(
+        _p(logits), logits.stride(0), _p(context_lens), next_n, len_div, R, _p(histogram),
+        1 if reset_histogram else 0, k, _p(out), _p(fallback_flags), ws.ptr, ws.nbytes,
+        _stream(stream)), "coarse_hist_topk")
+    return out
+
+
+def block_amax8(logits, context_lens, next_n, ws, skip_if_blocks_le=0, amax=None,
+                amax_stride=None, stream=None):
+    _req(logits, torch.float32, "logits")
+    _req(context_lens, torch.int32, "context_lens")
+    R = logits.shape[0]
+    if amax is None:
+        amax_stride = (logits.stride(0) + 7) // 8 if amax_stride is None else amax_stride
+        amax = torch.empty((R, amax_stride), dtype=torch.float32, device=logits.device)
+    _req(amax, torch.float32, "amax")
+    _check(lib.dsa_block_amax8(_p(logits), logits.stride(0), _p(context_lens), next_n, R,
+                               skip_if_blocks_le, _p(amax), amax.stride(0), ws.ptr, ws.nbytes,
+                               _stream(stream)), "block_amax8")
+    return amax
+
+
+def sort_candidate_blocks(block_ids, context_lens, next_n, page_table, page_size, ws,
+                          phys_blocks=None, valid_lens=None, stream=None):
+    """In place: block_ids [R][kb] -> ascending INT32_MAX-padded table."""
+    _req(block_ids, torch.int32, "block_ids")
+    R, kb = block_ids.shape
+    _check(lib.dsa_sort_candidate_blocks(
+        _p(block_ids), kb, _p(context_lens), next_n, R, _p(page_table), page_table.stride(0),
+        page_size, _p(phys_blocks), _p(valid_lens), ws.ptr, ws.nbytes, _stream(stream)),
+        "sort_candidate_blocks")
+    return block_ids
+
+
+def sparse_mqa_logits(q, kv_pages, kscale, weights, page_table, context_lens, next_n,
+                      block_table, ws, out=None, out_dtype=OUT_F32, stream=None):
+    q, kv_pages = _u8(q), _u8(kv_pages)
+    R, H, D = q.shape
+    P, ps, _ = kv_pages.shape
+    B = context_lens.shape[0]
+    kb = block_table.shape[1]
+    if out is None:
+        dt = torch.float32 if out_dtype == OUT_F32 else torch.float16
+        out = torch.empty((R, kb * 8), dtype=dt, device=q.device)
+    _req(block_table, torch.int32, "block_table")
+    _check(lib.dsa_sparse_mqa_logits(
+        _p(q), _p(kv_pages), _p(kscale), _p(weights), _p(page_table), page_table.stride(0),
+        _p(context_lens), B, next_n, H, D, ps, P, _p(block_table), kb, _p(out), out_dtype,
+        out.stride(0), ws.ptr, ws.nbytes, _stream(stream)), "sparse_mqa_logits")
+    return out
+
+
+def topk_fp16(scores, valid_lens, k, ws, block_table=None, out=None, stream=None):
+    """Top-k over FP16 scores (torch.float16 or raw uint16 bits)."""
+    s = scores.view(torch.uint16) if scores.dtype == torch.float16 else scores
+    _req(s, torch.uint16, "scores")
+    R = s.shape[0]
+    if out is None:
+        out = torch.empty((R, k), dtype=torch.int32, device=s.device)
+    kb = 0 if block_table is None else block_table.shape[1]
+    _check(lib.dsa_topk_fp16(_p(s), s.stride(0), _p(valid_lens), R, k, _p(block_table), kb,
+                             _p(out), ws.ptr, ws.nbytes, _stream(stream)), "topk_fp16")
+    return out
+
+
+def coarse_bins_range(start: int, count: int, out=None, stream=None):
+    if out is None:
+        out = torch.empty(count, dtype=torch.int16, device="cuda")
+    _check(lib.dsa_coarse_bins_range(ctypes.c_uint32(start), count, _p(out), _stream(stream)),
+           "coarse_bins_range")
+    return out
+
+
+def fp16_order_keys(x, out=None, stream=None):
+    s = x.view(torch.uint16) if x.dtype == torch.float16 else x
+    if out is None:
+        out = torch.empty_like(s)
+    _check(lib.dsa_fp16_order_keys(_p(s), _p(out), s.numel(), _stream(stream)),
+           "fp16_order_keys")
+    return out
+
+
+def wait_timeout_selftest(limit_cycles: int, ws, stream=None):
+    _check(lib.dsa_wait_timeout_selftest(ctypes.c_uint64(limit_cycles), ws.ptr, ws.nbytes,
+                                         _stream(stream)), "wait_timeout_selftest")

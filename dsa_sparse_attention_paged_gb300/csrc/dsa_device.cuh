@@ -1,0 +1,276 @@
+// dsa_device.cuh -- device-side building blocks shared by the sm_103a kernels:
+// inline-PTX wrappers for mbarriers, TMA (cp.async.bulk[.tensor]), the
+// tcgen05 tensor-core/TMEM instructions, bounded waits that record a status
+// bit instead of hanging, and the coarse score bin / order-key functions.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+// ---------------------------------------------------------------- workspace
+// Byte layout of the caller's workspace (see dsa_workspace_size).
+struct WsLayout {
+  static constexpr size_t kStatusOff = 0;         // uint32 status word (+ padding)
+  static constexpr size_t kHeader = 256;
+  // per row: 4 x int32 counters {emitted, candidates, done CTAs, spare}
+  static size_t counters_off() { return kHeader; }
+  static size_t counters_bytes(int64_t R) { return (size_t)R * 16; }
+  // per row: DSA_CAND_CAP x uint64 (key << 32 | ~column) candidates
+  static size_t cand_off(int64_t R) { return align(counters_off() + counters_bytes(R)); }
+  static size_t cand_bytes(int64_t R) { return (size_t)R * DSA_CAND_CAP * 8; }
+  // per row: 1024 int32 histogram for selects given no histogram
+  static size_t hist_off(int64_t R) { return align(cand_off(R) + cand_bytes(R)); }
+  static size_t hist_bytes(int64_t R) { return (size_t)R * DSA_NUM_BINS * 4; }
+  static size_t total(int64_t R) { return align(hist_off(R) + hist_bytes(R)); }
+  static size_t align(size_t x) { return (x + 255) & ~(size_t)255; }
+};
+
+__device__ __forceinline__ void set_status(uint32_t *status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------- smem / sync
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lane_id() {
+  uint32_t l;
+  asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
+  return l;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Shared abort flag + global status for one CTA's bounded waits.
+struct WaitCtl {
+  volatile int *abort_flag;  // shared memory
+  uint32_t *status;          // global
+  long long limit;           // clock64 cycles
+};
+
+// Wait for the phase with `parity` to complete.  Gives up (returns false) when
+// another role of the CTA aborted, or after ctl.limit cycles, in which case it
+// records DSA_DEV_TIMEOUT and raises the CTA's abort flag.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*ctl.abort_flag) return false;
+    if (clock64() - t0 > ctl.limit) {
+      *ctl.abort_flag = 1;
+      set_status(ctl.status, DSA_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Same, without abort propagation: used while draining after an abort.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, long long limit) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit) return false;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar, int32_t x, int32_t y,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// Plain bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, FP8 E4M3 x E4M3 -> FP32, issued by one thread.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05.mma issued so far by this thread completes.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// Instruction descriptor for kind::f8f6f4: D = FP32, A = B = E4M3, both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
+// layout TMA writes (rows of 128 bytes, 8-row groups 1024 bytes apart).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                    // leading byte offset (unused for SW128 K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                    // descriptor version (sm_100 family)
+  d |= (uint64_t)2 << 61;                    // swizzle mode: 128 B
+  return d;
+}
+
+// 32 lanes x 32 columns of 32-bit TMEM data: thread i of the warp receives
+// the 32 consecutive columns of TMEM lane (warp's lane base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- scores
+// Coarse bin of one score ([DG94] "What this adds"): 1024 descending bins,
+// bin 0 = largest.  |x| >= 223 -> magnitude code 511; 16 <= |x| < 223 ->
+// 304 + floor(|x|) - 16; |x| < 16 -> FP16-RN(|x|) >> 6.  bin = 511 - m for a
+// clear sign bit, 512 + m otherwise; -1 for NaN.
+__device__ __forceinline__ int coarse_bin(float x) {
+  if (isnan(x)) return -1;
+  const float a = fabsf(x);
+  int m;
+  if (a >= 223.0f) {
+    m = 511;
+  } else if (a >= 16.0f) {
+    m = 288 + static_cast<int>(a);  // 304 + floor(a) - 16; a > 0 so truncation is floor
+  } else {
+    m = static_cast<int>(__half_as_ushort(__float2half_rn(a)) >> 6);
+  }
+  return (__float_as_uint(x) >> 31) ? 512 + m : 511 - m;
+}
+
+// Ascending order key of an FP32 value: unsigned compare == value compare,
+// -inf lowest, -0 just below +0.
+__device__ __forceinline__ uint32_t f32_order_key(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Order keys of the two FP16 halves of a 32-bit word at once ([VL52696]
+// "Why": both packed halves are transformed with one 32-bit operation).  A
+// set sign bit flips all 16 bits, a clear one flips only the sign bit.  NaN
+// halves become key 0, below every non-NaN key (-inf has key 0x03FF).
+__device__ __forceinline__ uint32_t f16x2_order_keys(uint32_t w) {
+  const uint32_t sign = (w >> 15) & 0x00010001u;
+  uint32_t k = w ^ ((sign * 0x7FFFu) | 0x80008000u);
+  // |h| > 0x7C00 (NaN) iff (h & 0x7FFF) + 0x03FF carries into bit 15
+  const uint32_t nan_bits = ((w & 0x7FFF7FFFu) + 0x03FF03FFu) & 0x80008000u;
+  const uint32_t nan_mask = (nan_bits >> 15) * 0xFFFFu;
+  return k & ~nan_mask;
+}
+
+}  // namespace dsa

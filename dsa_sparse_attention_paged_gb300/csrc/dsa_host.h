@@ -1,0 +1,88 @@
+// dsa_host.h -- host-side helpers shared by the library's translation units
+// (tensor-map encoding, launch checks, device queries, call descriptors).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+// Default bound of every spin-wait inside a kernel, in SM clock cycles (about
+// two seconds at GB300 clocks); a wait that runs out sets DSA_DEV_TIMEOUT.
+constexpr long long kDefaultWaitLimit = 4000000000LL;
+
+struct LogitsCall {
+  const uint8_t *q;
+  const uint8_t *kv;
+  const float *kscale;
+  const float *weights;
+  const int32_t *page_table;
+  int64_t pt_stride;
+  const int32_t *context_lens;
+  int32_t B, next_n, page_size, num_pages;
+  void *out;
+  int64_t out_stride;
+  int32_t *histogram;
+  bool sparse;
+  bool out_f16;
+  const int32_t *block_table;
+  int32_t kb;
+  uint32_t *status;
+  long long wait_limit;
+};
+
+dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st);
+int logits_stages_for(int next_n, bool hist);
+
+struct TopkCall {
+  const float *logits;
+  int64_t stride;
+  const int32_t *context_lens;
+  int32_t next_n, len_div, R;
+  int32_t *histogram;        // caller's, or NULL
+  bool reset_histogram;
+  int32_t k;
+  int32_t *out_idx;
+  int32_t *fallback_flags;
+  void *workspace;
+  int32_t ws_rows;           // rows the workspace was sized for
+};
+dsa_status_t run_topk(const TopkCall &c, cudaStream_t st);
+
+struct Fp16TopkCall {
+  const uint16_t *scores;
+  int64_t stride;
+  const int32_t *valid_lens;
+  int32_t R, k;
+  const int32_t *block_table;
+  int32_t kb;
+  int32_t *out_idx;
+  uint32_t *status;
+};
+dsa_status_t run_topk_fp16(const Fp16TopkCall &c, cudaStream_t st);
+
+dsa_status_t run_block_amax8(const float *logits, int64_t stride, const int32_t *context_lens,
+                             int32_t next_n, int32_t R, int32_t skip_le, float *amax,
+                             int64_t amax_stride, uint32_t *status, cudaStream_t st);
+
+dsa_status_t run_sort_blocks(int32_t *ids, int32_t kb, const int32_t *context_lens,
+                             int32_t next_n, int32_t R, const int32_t *page_table,
+                             int64_t pt_stride, int32_t page_size, int32_t *phys,
+                             int32_t *valid_lens, uint32_t *status, cudaStream_t st);
+
+dsa_status_t run_bins_range(uint32_t start, int64_t count, int16_t *out, cudaStream_t st);
+dsa_status_t run_fp16_keys(const uint16_t *in, uint16_t *out, int64_t n, cudaStream_t st);
+dsa_status_t run_wait_selftest(uint64_t limit, uint32_t *status, cudaStream_t st);
+
+// --- utilities (api.cu) ---
+dsa_status_t make_tmap_rows128(CUtensorMap *map, const void *base, uint64_t rows,
+                               uint32_t box_rows);
+int num_sms();
+bool ensure_smem_attr(const void *fn, int bytes);
+dsa_status_t check_launch();
+void record_cuda_error(cudaError_t e);
+
+}  // namespace dsa

@@ -1,0 +1,634 @@
+// logits.cu -- paged MQA logits on sm_103a tensor cores, with the coarse
+// score histogram fused into the epilogue, and the sparse variant that scores
+// only the blocks of a candidate block table.
+//
+// [DG94] DeepGEMM PR #94 "What this adds": logits[r,t] = sum_h w[r,h] *
+// ReLU(q[r,h].k[t] * kscale[t]) over an FP8 paged K cache, H = 32, D = 128,
+// every live non-NaN score binned into 1024 descending bins while it is still
+// in registers; verify rows (next_n > 1) share one K pass of their request
+// (token Q tile, UMMA_N = 32 * next_n).
+// [SG38944] SGLang PR #38944 "What this enables": the sparse logits score only
+// the published 8-token blocks.
+//
+// One persistent CTA per SM, six warps:
+//   warp 0      TMA producer: gathers K pages through the page table into a
+//               ring of 128-token stages (16 KiB K + 512 B kscale each), and
+//               each request's Q tile + head weights into one of two buffers
+//   warp 1      allocates TMEM and issues tcgen05.mma (one thread):
+//               D[128 tokens x 32*next_n] = K[128 x 128] . Q[32*next_n x 128]^T,
+//               FP8 x FP8 -> FP32, with 4-8 accumulator buffers in TMEM
+//   warps 2..5  epilogue: each thread owns one TMEM lane = one token, loads
+//               its 32 head dots per row, applies kscale, ReLU and the head
+//               weights in registers, stores the logit (coalesced across the
+//               warp), and counts its bin in a per-warp shared histogram
+//               slot; the slots are summed and flushed with packed 64-bit
+//               global atomics whenever the CTA moves on to another request.
+// Work split: the flattened (request, 128-token tile) sequence is cut into
+// gridDim.x contiguous ranges, one per CTA; each CTA derives its range from a
+// prefix sum over context_lens (no separate metadata kernel).
+#include <algorithm>
+#include <mutex>
+
+#include "dsa_device.cuh"
+#include "dsa_host.h"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kTileTok = 128;
+constexpr int kStageK = kTileTok * 128;      // bytes of K per stage
+constexpr int kStageKs = kTileTok * 4;       // bytes of kscale per stage
+constexpr int kMaxStages = 16;
+constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kSmemLimit = 232448;           // 227 KiB opt-in per CTA
+
+struct LogitsArgs {
+  const int32_t *context_lens;
+  const int32_t *page_table;
+  int64_t pt_stride;
+  const float *kscale;
+  const float *weights;
+  int32_t B;
+  int32_t req_next_n;   // rows per request
+  int32_t page_size;
+  int32_t num_pages;
+  int32_t num_units;    // dense: requests; sparse: rows
+  int32_t sparse_tpu;   // sparse: tiles per row (kb / 16)
+  const int32_t *block_table;
+  int32_t kb;
+  void *out;
+  int64_t out_stride;
+  int32_t *histogram;
+  uint32_t *status;
+  int32_t num_stages;
+  int32_t num_acc;
+  uint32_t tmem_cols;
+  long long wait_limit;
+};
+
+struct SmemPlan {
+  int kst, q, ks, w, hist, bar, misc, total;
+};
+
+__host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, int stages, int nacc) {
+  SmemPlan p;
+  int off = 0;
+  p.kst = off;
+  off += stages * kStageK;
+  p.q = off;
+  off += 2 * nn * 32 * 128;
+  p.ks = off;
+  off += stages * kStageKs;
+  p.w = off;
+  off += 2 * nn * 32 * 4;
+  p.hist = off;
+  off += hist ? kEpiWarps * nn * DSA_NUM_BINS * 4 : 0;
+  off = (off + 7) & ~7;
+  p.bar = off;
+  off += (2 * stages + 4 + 2 * nacc + 2) * 8;
+  p.misc = off;
+  off += 64;
+  p.total = off + 1024;  // slack to align the base to 1024 bytes
+  return p;
+}
+
+__device__ __forceinline__ int64_t eff_ctx(const LogitsArgs &a, int b) {
+  int64_t c = a.context_lens[b];
+  const int64_t cap = a.pt_stride * a.page_size;
+  if (c < 0) c = 0;
+  if (c > cap) c = cap;
+  return c;
+}
+
+template <bool SPARSE>
+__device__ __forceinline__ int unit_tiles(const LogitsArgs &a, int u) {
+  if (SPARSE) return a.sparse_tpu;
+  return static_cast<int>((eff_ctx(a, u) + kTileTok - 1) / kTileTok);
+}
+
+template <bool SPARSE>
+struct TileIter {
+  int u, i, tiles;
+  __device__ void init(const LogitsArgs &a, int u0, int i0) {
+    u = u0;
+    i = i0;
+    tiles = (u < a.num_units) ? unit_tiles<SPARSE>(a, u) : 1;
+  }
+  __device__ void next(const LogitsArgs &a) {
+    if (++i >= tiles) {
+      i = 0;
+      do {
+        ++u;
+        tiles = (u < a.num_units) ? unit_tiles<SPARSE>(a, u) : 1;
+      } while (tiles == 0);
+    }
+  }
+};
+
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// One warp: this CTA's contiguous range [g0, g1) of the flattened tile
+// sequence, as (first unit, first tile in it, tile count).
+template <bool SPARSE>
+__device__ void compute_sched(const LogitsArgs &a, int *out_u0, int *out_i0, long long *out_cnt) {
+  const int lane = threadIdx.x & 31;
+  long long T = 0;
+  if (SPARSE) {
+    T = (long long)a.num_units * a.sparse_tpu;
+  } else {
+    for (int base = 0; base < a.num_units; base += 32) {
+      const int b = base + lane;
+      int t = (b < a.num_units) ? unit_tiles<false>(a, b) : 0;
+      if (b < a.num_units && a.context_lens[b] > a.pt_stride * a.page_size)
+        set_status(a.status, DSA_DEV_BOUNDS);
+      T += __shfl_sync(0xffffffffu, warp_incl_scan(t), 31);
+    }
+  }
+  const long long g0 = (long long)blockIdx.x * T / gridDim.x;
+  const long long g1 = (long long)(blockIdx.x + 1) * T / gridDim.x;
+  int u0 = a.num_units, i0 = 0;
+  if (g1 > g0) {
+    if (SPARSE) {
+      u0 = (int)(g0 / a.sparse_tpu);
+      i0 = (int)(g0 % a.sparse_tpu);
+    } else {
+      long long acc = 0;
+      for (int base = 0; base < a.num_units; base += 32) {
+        const int b = base + lane;
+        const int t = (b < a.num_units) ? unit_tiles<false>(a, b) : 0;
+        const int incl = warp_incl_scan(t);
+        const int tot = __shfl_sync(0xffffffffu, incl, 31);
+        if (g0 < acc + tot) {
+          const unsigned m = __ballot_sync(0xffffffffu, acc + incl > g0);
+          const int l = __ffs(m) - 1;
+          const int excl_l = __shfl_sync(0xffffffffu, incl - t, l);
+          u0 = base + l;
+          i0 = (int)(g0 - acc - excl_l);
+          break;
+        }
+        acc += tot;
+      }
+    }
+  }
+  *out_u0 = u0;
+  *out_i0 = i0;
+  *out_cnt = g1 - g0;
+}
+
+// Sum over the 32 heads of one row: kscale, ReLU, head weight, in a fixed
+// order (dense and sparse share it, so their logits are bitwise equal).
+__device__ __forceinline__ float head_sum(const uint32_t (&v)[32], float ks, const float *w) {
+  float acc = 0.0f;
+#pragma unroll
+  for (int h = 0; h < 32; h += 4) {
+    const float4 wv = *reinterpret_cast<const float4 *>(w + h);
+    acc = fmaf(wv.x, fmaxf(__uint_as_float(v[h + 0]) * ks, 0.0f), acc);
+    acc = fmaf(wv.y, fmaxf(__uint_as_float(v[h + 1]) * ks, 0.0f), acc);
+    acc = fmaf(wv.z, fmaxf(__uint_as_float(v[h + 2]) * ks, 0.0f), acc);
+    acc = fmaf(wv.w, fmaxf(__uint_as_float(v[h + 3]) * ks, 0.0f), acc);
+  }
+  return acc;
+}
+
+template <int NN, bool SPARSE, bool OUT_F16, bool HIST>
+__global__ void __launch_bounds__(kThreads, 1)
+    logits_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                  const LogitsArgs a) {
+  constexpr int N = 32 * NN;
+  constexpr uint32_t IDESC = idesc_e4m3_f32(128, N);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int S = a.num_stages;
+  const int A = a.num_acc;
+  const SmemPlan P = smem_plan(NN, HIST, S, A);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const uint32_t kst = smem_u32(smem + P.kst);
+  const uint32_t qst = smem_u32(smem + P.q);
+  float *ks_s = reinterpret_cast<float *>(smem + P.ks);
+  float *w_s = reinterpret_cast<float *>(smem + P.w);
+  int *hist_s = reinterpret_cast<int *>(smem + P.hist);
+  const uint32_t bar0 = smem_u32(smem + P.bar);
+  auto FULL = [&](int s) { return bar0 + 8u * s; };
+  auto EMPTY = [&](int s) { return bar0 + 8u * (S + s); };
+  auto QFULL = [&](int q) { return bar0 + 8u * (2 * S + q); };
+  auto QEMPTY = [&](int q) { return bar0 + 8u * (2 * S + 2 + q); };
+  auto AFULL = [&](int x) { return bar0 + 8u * (2 * S + 4 + x); };
+  auto AEMPTY = [&](int x) { return bar0 + 8u * (2 * S + 4 + A + x); };
+  const uint32_t DRAIN = bar0 + 8u * (2 * S + 4 + 2 * A);
+  const uint32_t GSYNC = bar0 + 8u * (2 * S + 4 + 2 * A + 1);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P.misc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P.misc + 4);
+  int *sched = reinterpret_cast<int *>(smem + P.misc + 16);
+  long long *sched_cnt = reinterpret_cast<long long *>(smem + P.misc + 32);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(FULL(s), 1);
+      mbar_init(EMPTY(s), 1 + kEpiWarps);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(QFULL(q), 1);
+      mbar_init(QEMPTY(q), 1 + kEpiWarps);
+    }
+    for (int x = 0; x < A; ++x) {
+      mbar_init(AFULL(x), 1);
+      mbar_init(AEMPTY(x), kEpiWarps);
+    }
+    mbar_init(DRAIN, 1);
+    mbar_init(GSYNC, kEpiWarps);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) compute_sched<SPARSE>(a, &sched[0], &sched[1], sched_cnt);
+  if (HIST) {
+    for (int i = threadIdx.x; i < kEpiWarps * NN * DSA_NUM_BINS; i += kThreads) hist_s[i] = 0;
+  }
+  __syncthreads();
+  const long long count = *sched_cnt;
+  if (count <= 0) return;  // uniform across the CTA: nothing to do, no TMEM taken
+  const int u_start = sched[0], i_start = sched[1];
+
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_q);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl ctl{abort_flag, a.status, a.wait_limit};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = policy_evict_first();
+    TileIter<SPARSE> it;
+    it.init(a, u_start, i_start);
+    int prev_u = -1, unit_ord = -1;
+    long long issued = 0;
+    int q_issued = 0;
+    bool ok = true;
+    for (long long n = 0; n < count && ok; ++n, it.next(a)) {
+      const int u = it.u, i = it.i;
+      int b, qrow0;
+      int64_t n_live;  // dense: tokens of the request; sparse: live keys of the row
+      if (SPARSE) {
+        b = u / a.req_next_n;
+        const int j = u % a.req_next_n;
+        n_live = eff_ctx(a, b) - (a.req_next_n - 1 - j);
+        qrow0 = u * 32;
+      } else {
+        b = u;
+        n_live = eff_ctx(a, b);
+        qrow0 = u * N;
+      }
+      // Physical rows for this tile, read before waiting for the slot.
+      int row = -1;
+      if (SPARSE) {
+        if (lane < 16) {
+          const int32_t id = a.block_table[(int64_t)u * a.kb + (int64_t)i * 16 + lane];
+          if (id != INT32_MAX && id >= 0 && (int64_t)id * 8 < n_live) {
+            const int64_t tok = (int64_t)id * 8;
+            int32_t pg = a.page_table[(int64_t)b * a.pt_stride + tok / a.page_size];
+            if (pg < 0 || pg >= a.num_pages) {
+              set_status(a.status, DSA_DEV_BOUNDS);
+              pg = 0;
+            }
+            row = pg * a.page_size + (int)(tok % a.page_size);
+          }
+        }
+      } else {
+        const int ppt = kTileTok / a.page_size;  // pages per tile: 2 or 1
+        if (lane < ppt) {
+          const int64_t p = (int64_t)i * ppt + lane;
+          if (p * a.page_size < n_live) {
+            int32_t pg = a.page_table[(int64_t)b * a.pt_stride + p];
+            if (pg < 0 || pg >= a.num_pages) {
+              set_status(a.status, DSA_DEV_BOUNDS);
+              pg = 0;
+            }
+            row = pg * a.page_size;
+          }
+        }
+      }
+      if (u != prev_u) {
+        ++unit_ord;
+        prev_u = u;
+        const int qb = unit_ord & 1;
+        const uint32_t qph = (unit_ord >> 1) & 1;
+        if (lane == 0) {
+          ok = mbar_wait(QEMPTY(qb), qph ^ 1, ctl);
+          if (ok) {
+            mbar_arrive_expect_tx(QFULL(qb), N * 128 + N * 4);
+            tma_load_2d(qst + qb * (N * 128), &tm_q, QFULL(qb), 0, qrow0);
+            bulk_load(smem_u32(w_s + qb * N), a.weights + (int64_t)qrow0, N * 4, QFULL(qb));
+            ++q_issued;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+      const int s = (int)(n % S);
+      const uint32_t ph = (uint32_t)((n / S) & 1);
+      if (lane == 0) ok = mbar_wait(EMPTY(s), ph ^ 1, ctl);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      const unsigned loads = __ballot_sync(0xffffffffu, row >= 0);
+      const int blk_rows = SPARSE ? 8 : a.page_size;
+      const uint32_t bytes = (uint32_t)__popc(loads) * (uint32_t)(blk_rows * 132);
+      if (lane == 0) mbar_arrive_expect_tx(FULL(s), bytes);
+      __syncwarp();
+      if (row >= 0) {
+        tma_load_2d_hint(kst + s * kStageK + lane * blk_rows * 128, &tm_k, FULL(s), 0, row, pol);
+        bulk_load(smem_u32(ks_s + s * kTileTok + lane * blk_rows), a.kscale + (int64_t)row,
+                  blk_rows * 4, FULL(s));
+      }
+      ++issued;
+    }
+    if (!ok && lane == 0) {
+      // drain our own copies still in flight before the CTA exits
+      const long long lim = a.wait_limit;
+      for (long long n = (issued > S ? issued - S : 0); n < issued; ++n)
+        mbar_wait_drain(FULL((int)(n % S)), (uint32_t)((n / S) & 1), lim);
+      for (int k2 = (q_issued > 2 ? q_issued - 2 : 0); k2 < q_issued; ++k2)
+        mbar_wait_drain(QFULL(k2 & 1), (uint32_t)((k2 >> 1) & 1), lim);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      TileIter<SPARSE> it;
+      it.init(a, u_start, i_start);
+      int prev_u = -1, unit_ord = -1, qb = 0;
+      bool ok = true;
+      long long mmas = 0;
+      for (long long n = 0; n < count; ++n, it.next(a)) {
+        if (it.u != prev_u) {
+          ++unit_ord;
+          prev_u = it.u;
+          qb = unit_ord & 1;
+          if (!(ok = mbar_wait(QFULL(qb), (unit_ord >> 1) & 1, ctl))) break;
+        }
+        const int s = (int)(n % S);
+        const int x = (int)(n % A);
+        if (!(ok = mbar_wait(AEMPTY(x), (uint32_t)(((n / A) & 1) ^ 1), ctl))) break;
+        if (!(ok = mbar_wait(FULL(s), (uint32_t)((n / S) & 1), ctl))) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(x * N);
+        const uint64_t ad = sdesc_sw128(kst + s * kStageK);
+        const uint64_t bd = sdesc_sw128(qst + qb * (N * 128));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // K = 128 FP8 = 4 steps of 32 bytes
+          mma_f8(d, ad + 2 * kk, bd + 2 * kk, IDESC, kk > 0 ? 1u : 0u);
+        ++mmas;
+        mma_commit(EMPTY(s));
+        mma_commit(AFULL(x));
+        if (it.i == it.tiles - 1 || n == count - 1) mma_commit(QEMPTY(qb));
+      }
+      if (!ok && mmas > 0) {
+        mma_commit(DRAIN);
+        mbar_wait_drain(DRAIN, 0, a.wait_limit);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;                 // 0..3: histogram slot
+    const int lane_base = 32 * (warp & 3);   // TMEM lanes this warp may read
+    const int tok = lane_base + lane;        // token (row of D) owned by this thread
+    int *my_hist = hist_s + ew * NN * DSA_NUM_BINS;
+    TileIter<SPARSE> it;
+    it.init(a, u_start, i_start);
+    int prev_u = -1, unit_ord = -1, qb = 0;
+    uint32_t gsync_ph = 0;
+    int64_t ctx_b = 0, n_row = 0;
+    int row_base = 0;
+    bool ok = true;
+
+    // warp-uniform bounded wait: every lane polls, the warp leaves together
+    auto ewait = [&](uint32_t bar, uint32_t parity) -> bool {
+      const bool r = mbar_wait(bar, parity, ctl);
+      return __all_sync(0xffffffffu, r) != 0;
+    };
+    // all four epilogue warps meet (bounded wait on an mbarrier)
+    auto group_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(GSYNC);
+      const bool r = ewait(GSYNC, gsync_ph);
+      gsync_ph ^= 1;
+      return r;
+    };
+    // sum the four warps' slots for the finished request, add them to the
+    // global histogram with packed 64-bit atomics, and clear the slots
+    auto flush = [&](int rb) -> bool {
+      if (!group_sync()) return false;
+      const int t128 = threadIdx.x - 64;
+      for (int j = 0; j < NN; ++j) {
+        for (int p = t128; p < DSA_NUM_BINS / 2; p += 128) {
+          uint32_t c0 = 0, c1 = 0;
+#pragma unroll
+          for (int w = 0; w < kEpiWarps; ++w) {
+            int *sl = hist_s + (w * NN + j) * DSA_NUM_BINS + 2 * p;
+            c0 += sl[0];
+            c1 += sl[1];
+            sl[0] = 0;
+            sl[1] = 0;
+          }
+          if (c0 | c1) {
+            unsigned long long *g = reinterpret_cast<unsigned long long *>(
+                a.histogram + (int64_t)(rb + j) * DSA_NUM_BINS + 2 * p);
+            atomicAdd(g, ((unsigned long long)c1 << 32) | c0);
+          }
+        }
+      }
+      return group_sync();
+    };
+
+    for (long long n = 0; n < count; ++n, it.next(a)) {
+      const int u = it.u, i = it.i;
+      if (u != prev_u) {
+        if (HIST && prev_u >= 0) {
+          if (!(ok = flush(row_base))) break;
+        }
+        ++unit_ord;
+        prev_u = u;
+        qb = unit_ord & 1;
+        if (SPARSE) {
+          const int b = u / a.req_next_n;
+          const int j = u % a.req_next_n;
+          n_row = eff_ctx(a, b) - (a.req_next_n - 1 - j);
+          if (n_row < 0) n_row = 0;
+        } else {
+          ctx_b = eff_ctx(a, u);
+          row_base = u * NN;
+        }
+        if (!(ok = ewait(QFULL(qb), (unit_ord >> 1) & 1))) break;
+      }
+      const int s = (int)(n % S);
+      const int x = (int)(n % A);
+      const int64_t pos = (int64_t)i * kTileTok + tok;
+      int32_t blk = 0;
+      if (SPARSE) blk = a.block_table[(int64_t)u * a.kb + pos / 8];
+      if (!(ok = ewait(FULL(s), (uint32_t)((n / S) & 1)))) break;
+      const float ks = ks_s[s * kTileTok + tok];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(EMPTY(s));
+      if (!(ok = ewait(AFULL(x), (uint32_t)((n / A) & 1)))) break;
+      tc_fence_after();
+      float acc[NN];
+#pragma unroll
+      for (int j = 0; j < NN; ++j) {
+        uint32_t v[32];
+        tmem_ld32(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(x * N + j * 32), v);
+        tmem_ld_wait();
+        acc[j] = head_sum(v, ks, w_s + qb * N + j * 32);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(AEMPTY(x));
+
+      if (SPARSE) {
+        const int64_t t = (int64_t)blk * 8 + (pos & 7);
+        const bool live = blk != INT32_MAX && blk >= 0 && t < n_row;
+        const float val = live ? acc[0] : -INFINITY;
+        if (OUT_F16) {
+          reinterpret_cast<__half *>(a.out)[(int64_t)u * a.out_stride + pos] = __float2half_rn(val);
+        } else {
+          reinterpret_cast<float *>(a.out)[(int64_t)u * a.out_stride + pos] = val;
+        }
+      } else {
+        const int64_t t = pos;
+#pragma unroll
+        for (int j = 0; j < NN; ++j) {
+          int64_t n_rj = ctx_b - (NN - 1 - j);
+          if (n_rj > a.out_stride) {
+            n_rj = a.out_stride;
+            if (t == a.out_stride) set_status(a.status, DSA_DEV_BOUNDS);
+          }
+          if (t < n_rj) {
+            reinterpret_cast<float *>(a.out)[(int64_t)(row_base + j) * a.out_stride + t] = acc[j];
+            if (HIST) {
+              const int bin = coarse_bin(acc[j]);
+              if (bin >= 0) atomicAdd(&my_hist[j * DSA_NUM_BINS + bin], 1);
+            }
+          }
+        }
+      }
+      if (i == it.tiles - 1 || n == count - 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(QEMPTY(qb));
+      }
+    }
+    if (HIST && ok && prev_u >= 0) flush(row_base);
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, a.tmem_cols);
+  }
+}
+
+template <int NN, bool SPARSE, bool OUT_F16, bool HIST>
+dsa_status_t launch_one(const CUtensorMap &tk, const CUtensorMap &tq, const LogitsArgs &a0,
+                        int grid, cudaStream_t st) {
+  LogitsArgs a = a0;
+  const int N = 32 * NN;
+  a.num_acc = std::min(8, 512 / N);
+  int cols = 32;
+  while (cols < a.num_acc * N) cols <<= 1;
+  a.tmem_cols = (uint32_t)cols;
+  int S = kMaxStages;
+  while (S > 2 && smem_plan(NN, HIST, S, a.num_acc).total > kSmemLimit) --S;
+  a.num_stages = S;
+  const int smem = smem_plan(NN, HIST, S, a.num_acc).total;
+  auto kfn = logits_kernel<NN, SPARSE, OUT_F16, HIST>;
+  if (!ensure_smem_attr(reinterpret_cast<const void *>(kfn), smem)) return DSA_ERR_CUDA;
+  kfn<<<grid, kThreads, smem, st>>>(tk, tq, a);
+  return check_launch();
+}
+
+}  // namespace
+
+int logits_stages_for(int next_n, bool hist) {
+  const int N = 32 * next_n;
+  const int nacc = std::min(8, 512 / N);
+  int S = kMaxStages;
+  while (S > 2 && smem_plan(next_n, hist, S, nacc).total > kSmemLimit) --S;
+  return S;
+}
+
+dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
+  CUtensorMap tk, tq;
+  dsa_status_t e = make_tmap_rows128(&tk, c.kv, (uint64_t)c.num_pages * c.page_size,
+                                     c.sparse ? 8 : c.page_size);
+  if (e != DSA_OK) return e;
+  const int nn = c.sparse ? 1 : c.next_n;
+  e = make_tmap_rows128(&tq, c.q, (uint64_t)c.B * c.next_n * 32, 32 * nn);
+  if (e != DSA_OK) return e;
+  LogitsArgs a{};
+  a.context_lens = c.context_lens;
+  a.page_table = c.page_table;
+  a.pt_stride = c.pt_stride;
+  a.kscale = c.kscale;
+  a.weights = c.weights;
+  a.B = c.B;
+  a.req_next_n = c.next_n;
+  a.page_size = c.page_size;
+  a.num_pages = c.num_pages;
+  a.block_table = c.block_table;
+  a.kb = c.kb;
+  a.out = c.out;
+  a.out_stride = c.out_stride;
+  a.histogram = c.histogram;
+  a.status = c.status;
+  a.wait_limit = c.wait_limit;
+  const int sms = num_sms();
+  if (sms <= 0) return DSA_ERR_CUDA;
+  if (c.sparse) {
+    a.num_units = c.B * c.next_n;
+    a.sparse_tpu = c.kb / 16;
+    const long long tiles = (long long)a.num_units * a.sparse_tpu;
+    const int grid = (int)std::max<long long>(1, std::min<long long>(sms, tiles));
+    if (c.out_f16) return launch_one<1, true, true, false>(tk, tq, a, grid, st);
+    return launch_one<1, true, false, false>(tk, tq, a, grid, st);
+  }
+  a.num_units = c.B;
+  a.sparse_tpu = 0;
+  const int grid = sms;
+  const bool h = c.histogram != nullptr;
+  switch (c.next_n) {
+    case 1:
+      return h ? launch_one<1, false, false, true>(tk, tq, a, grid, st)
+               : launch_one<1, false, false, false>(tk, tq, a, grid, st);
+    case 2:
+      return h ? launch_one<2, false, false, true>(tk, tq, a, grid, st)
+               : launch_one<2, false, false, false>(tk, tq, a, grid, st);
+    case 3:
+      return h ? launch_one<3, false, false, true>(tk, tq, a, grid, st)
+               : launch_one<3, false, false, false>(tk, tq, a, grid, st);
+    case 4:
+      return h ? launch_one<4, false, false, true>(tk, tq, a, grid, st)
+               : launch_one<4, false, false, false>(tk, tq, a, grid, st);
+    default:
+      return DSA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace dsa

@@ -1,0 +1,89 @@
+"""One indexer decode step as a fixed sequence of C-ABI calls.
+
+``DecodePlan`` plays the role of SGLang's ``FusedDecodePlan`` (DeepGEMM PR #94,
+cross-referenced SGLang commit 7e252c5): it is built once per shape, owns the
+step's device buffers and the workspace, and each ``step`` runs
+
+  source layer   paged MQA logits + fused coarse histogram        (1 launch)
+                 histogram-driven exact top-k (resets the hist)   (1 launch)
+  level one      block amax8 (rows with nb <= kb skipped)          (1 launch)
+  (two-level)    block top-kb of the maxima                         (2 launches)
+                 sort_candidate_blocks -> table, phys, valid lens   (1 launch)
+  consumer       sparse MQA logits over the table, FP16 output      (1 launch)
+                 FP16 top-k with the fused table transform          (1 launch)
+
+following SGLang PR #38944 ("What this enables": the source layer publishes an
+ascending block table; the consumer scores only those blocks and selects
+inside that row).  Everything runs in the library's kernels on one stream.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (OUT_F16, Workspace, block_amax8, coarse_hist_topk, paged_mqa_logits,
+               sort_candidate_blocks, sparse_mqa_logits, topk_fp16)
+
+
+class DecodePlan:
+    LAUNCHES_DENSE = 2
+    LAUNCHES_TWO_LEVEL = 6
+
+    def __init__(self, B, next_n, max_context, page_size, k=2048, kb=512, two_level=True,
+                 device="cuda"):
+        self.B, self.next_n, self.page_size = B, next_n, page_size
+        self.R = B * next_n
+        self.k, self.kb, self.two_level = k, kb, two_level
+        self.stride = int(max_context)
+        dev = torch.device(device)
+        R = self.R
+        self.ws = Workspace(R, device=dev)
+        self.logits = torch.empty((R, self.stride), dtype=torch.float32, device=dev)
+        self.hist = torch.zeros((R, 1024), dtype=torch.int32, device=dev)
+        self.topk_idx = torch.empty((R, k), dtype=torch.int32, device=dev)
+        if two_level:
+            self.amax_stride = (self.stride + 7) // 8
+            self.amax = torch.empty((R, self.amax_stride), dtype=torch.float32, device=dev)
+            self.block_ids = torch.empty((R, kb), dtype=torch.int32, device=dev)
+            self.phys = torch.empty((R, kb), dtype=torch.int32, device=dev)
+            self.valid_lens = torch.empty((R,), dtype=torch.int32, device=dev)
+            self.sparse = torch.empty((R, kb * 8), dtype=torch.float16, device=dev)
+            self.sparse_idx = torch.empty((R, k), dtype=torch.int32, device=dev)
+
+    @property
+    def launches_per_step(self) -> int:
+        return self.LAUNCHES_DENSE + (self.LAUNCHES_TWO_LEVEL if self.two_level else 0)
+
+    def step(self, q, kv, kscale, weights, page_table, context_lens, events=None):
+        """Run one decode step.  ``events`` (optional dict name -> (start, end)
+        CUDA events) brackets individual launches for per-kernel timing."""
+        nn, ws = self.next_n, self.ws
+
+        def mark(name, i):
+            if events is not None and name in events:
+                events[name][i].record()
+
+        mark("logits", 0)
+        paged_mqa_logits(q, kv, kscale, weights, page_table, context_lens, nn, ws,
+                         logits=self.logits, histogram=self.hist)
+        mark("logits", 1)
+        mark("topk", 0)
+        coarse_hist_topk(self.logits, context_lens, nn, self.k, ws, histogram=self.hist,
+                         reset_histogram=True, out=self.topk_idx)
+        mark("topk", 1)
+        if not self.two_level:
+            return self.topk_idx, None
+        mark("publish", 0)
+        block_amax8(self.logits, context_lens, nn, ws, skip_if_blocks_le=self.kb,
+                    amax=self.amax)
+        coarse_hist_topk(self.amax, context_lens, nn, self.kb, ws, histogram=None,
+                         len_div=8, out=self.block_ids)
+        sort_candidate_blocks(self.block_ids, context_lens, nn, page_table, self.page_size, ws,
+                              phys_blocks=self.phys, valid_lens=self.valid_lens)
+        mark("publish", 1)
+        mark("consume", 0)
+        sparse_mqa_logits(q, kv, kscale, weights, page_table, context_lens, nn,
+                          self.block_ids, ws, out=self.sparse, out_dtype=OUT_F16)
+        topk_fp16(self.sparse, self.valid_lens, self.k, ws, block_table=self.block_ids,
+                  out=self.sparse_idx)
+        mark("consume", 1)
+        return self.topk_idx, self.sparse_idx

@@ -1,0 +1,250 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DSA indexer decode library.
+ *
+ * The library scores a paged FP8 index-K cache against FP8 queries (paged MQA
+ * logits), bins every live score into a 1024-bin coarse histogram inside the
+ * same kernel, selects the exact top-k columns per row from that histogram,
+ * and builds the two-level candidate path (block maxima over 8-score blocks,
+ * block top-k, an ascending padded block table, sparse logits over the chosen
+ * blocks, and a top-k over FP16 scores).
+ *
+ * Sources, cited by page title and section:
+ *   [DG94]   DeepGEMM PR #94 "[SM100] Paged MQA logits: fused coarse score
+ *            histogram for LiteTopK decode" -- "What this adds", "Producer
+ *            cost", commit 2d3b1c1, cross-referenced SGLang commit 7e252c5.
+ *   [SG38944] SGLang PR #38944 "[DSV4.1] Enable the two-level candidate indexer
+ *            on DeepGEMM's paged sparse MQA logits" -- squashed commit texts,
+ *            "What this enables", "Structure", "Tests".
+ *   [VL52696] vLLM PR #52696 "[Performance][MLA] Use FP16 logits for sparse
+ *            indexer" -- "Summary", "Why".
+ *
+ * Conventions for every entry point:
+ *   - Data pointers are DEVICE pointers owned by the caller unless a comment
+ *     says otherwise; the library never frees or retains them past the call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  The library allocates no device memory: scratch space comes
+ *     from a caller-owned workspace sized by dsa_workspace_size().
+ *   - Host-side argument checks run before anything is launched and return a
+ *     status synchronously; nothing is launched when the status is not DSA_OK.
+ *   - Problems only the device can see (a page id outside the pool, a context
+ *     length beyond the page table or the output stride, a wait that ran out)
+ *     are recorded as bits in the workspace's device status word and the
+ *     kernel skips or clamps the offending access; they never trap.  Read the
+ *     word with dsa_read_device_status().
+ *   - Row r = b * next_n + j belongs to request b; it sees
+ *     n_r = context_lens[b] - (next_n - 1 - j) keys ("token j of a request
+ *     sees L + j keys", [DG94] "Producer cost", with context_lens[b] = L +
+ *     next_n - 1).
+ *   - Supported shapes follow [DG94] "What this adds": H = 32 heads, D = 128,
+ *     FP8 E4M3 q and K, FP32 kscale, weights and logits, next_n in 1..4,
+ *     page size 64 or 128 ([SG38944]: the metadata builder takes 64 or 128).
+ *     Anything else returns DSA_ERR_UNSUPPORTED.
+ */
+#ifndef DSA_GB300_H
+#define DSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes returned by every entry point ------------------------- */
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,   /* NULL pointer, negative size, bad stride        */
+  DSA_ERR_UNSUPPORTED = 2,   /* shape outside the supported set                */
+  DSA_ERR_MISALIGNED = 3,    /* pointer or stride breaks an alignment rule     */
+  DSA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed              */
+  DSA_ERR_WORKSPACE = 5      /* workspace NULL or smaller than required        */
+} dsa_status_t;
+
+/* ---- device status word bits (sticky; see dsa_read_device_status) ------- */
+#define DSA_DEV_TIMEOUT 0x1u  /* a bounded wait in a kernel ran out; the kernel
+                                 drained its copies and returned early        */
+#define DSA_DEV_BOUNDS 0x2u   /* a page id outside [0, num_pages), a context
+                                 length beyond page_table_stride * page_size or
+                                 the output stride, or a block id beyond the
+                                 row; the access was skipped or clamped        */
+
+#define DSA_NUM_BINS 1024     /* coarse histogram bins per row ([DG94])        */
+#define DSA_MAX_TOPK 2048     /* largest k of the selects                      */
+#define DSA_CAND_CAP 8192     /* threshold-bin candidates kept per row, the
+                                 default capacity of FusedDecodePlan ([DG94],
+                                 SGLang commit 7e252c5)                        */
+#define DSA_OUT_F32 0
+#define DSA_OUT_F16 1
+
+/* Human-readable name of a dsa_status_t (static storage). */
+const char *dsa_status_string(int32_t status);
+
+/* Last CUDA error code seen by the library in this thread (0 if none). */
+int32_t dsa_last_cuda_error(void);
+
+/* Library version, as an integer major*10000 + minor*100 + patch. */
+int32_t dsa_version(void);
+
+/* ---- workspace ----------------------------------------------------------
+ * One caller-owned device buffer serves every entry point.  It holds the
+ * device status word, per-row select counters, the threshold-bin candidate
+ * buffer (DSA_CAND_CAP entries per row) and a histogram for selects that are
+ * not given one.  `max_rows` is the largest row count any call will use.
+ * The buffer must be zero-filled once before first use (dsa_workspace_init);
+ * every completed call leaves its counters at zero again, so no per-call
+ * clearing is needed.  Calls that share a workspace must be ordered on one
+ * stream (or otherwise serialised): concurrent calls on one workspace race. */
+size_t dsa_workspace_size(int32_t max_rows);
+
+/* Zero-fill the workspace on `stream` (also clears the device status word). */
+int32_t dsa_workspace_init(void *workspace, size_t ws_bytes, void *stream);
+
+/* Copy the device status word to *out_host (synchronises `stream`). */
+int32_t dsa_read_device_status(const void *workspace, void *stream, uint32_t *out_host);
+
+/* ---- paged MQA logits with the fused coarse histogram -------------------
+ * [DG94] "What this adds" and the indexer logits formula:
+ *   logits[r, t] = sum_h weights[r, h] * ReLU( (sum_d q[r, h, d] * k[t, d]) * kscale[t] )
+ * for every live column t < n_r; dead columns are not written.  K token t of
+ * request b is read from physical slot s = page_table[b * page_table_stride +
+ * t / page_size] * page_size + t % page_size.
+ *
+ *   q            [B*next_n][num_heads][head_dim] FP8 E4M3 bytes, 16-byte aligned
+ *   kv_pages     [num_pages][page_size][head_dim] FP8 E4M3 bytes, 16-byte aligned
+ *   kscale       [num_pages][page_size] float, 16-byte aligned
+ *   weights      [B*next_n][num_heads] float, 16-byte aligned
+ *   page_table   [B][page_table_stride] int32 physical page ids
+ *   context_lens [B] int32
+ *   logits       [B*next_n][logits_stride] float
+ *   histogram    NULL, or [B*next_n][1024] int32, 8-byte aligned: every live,
+ *                non-NaN score adds 1 to bin(score) of its row.  Counts are
+ *                ADDED to what is there (zero it before the first call; the
+ *                consumer resets it -- see dsa_coarse_hist_topk).  Bins
+ *                descend: bin 0 holds the largest scores; |x| < 16 uses the
+ *                FP16-RN exponent and 4 mantissa bits, 16 <= |x| < 223 unit
+ *                bins, |x| >= 223 one saturating bin at each end.
+ * With or without the histogram the logits are bitwise identical. */
+int32_t dsa_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const float *kscale,
+                             const float *weights, const int32_t *page_table,
+                             int64_t page_table_stride, const int32_t *context_lens, int32_t B,
+                             int32_t next_n, int32_t num_heads, int32_t head_dim,
+                             int32_t page_size, int32_t num_pages, float *logits,
+                             int64_t logits_stride, int32_t *histogram, void *workspace,
+                             size_t ws_bytes, void *stream);
+
+/* ---- histogram-driven exact top-k ---------------------------------------
+ * SGLang commit 7e252c5 (select.cuh, cross-referenced from [DG94]): per row,
+ * find the threshold bin T from the coarse histogram (the bins above T hold
+ * fewer than k scores, T completes k), emit every score in a bin above T,
+ * collect the scores of bin T (at most DSA_CAND_CAP) and refine them exactly.
+ * A histogram that does not match the row (stale) or a bin T with more than
+ * DSA_CAND_CAP scores falls back to an exact whole-row radix select instead of
+ * raising a device error.
+ *
+ * Rows: r in [0, R); row r has n_r = ceil_div(context_lens[r / next_n] -
+ * (next_n - 1 - r % next_n), len_div) live scores (len_div = 1 for logits
+ * rows, 8 for rows of block maxima).
+ *   logits       [R][stride] float; dead columns are never read
+ *   histogram    [R][1024] int32 built by dsa_paged_mqa_logits for these rows,
+ *                or NULL: the library builds it in the workspace first
+ *   reset_histogram  nonzero: zero the caller's histogram rows after use (the
+ *                consumer reset the histogram contract asks for)
+ *   out_idx      [R][k] int32: the k columns with the largest scores, ties
+ *                to the lower column, NaN never selected; order within a row
+ *                is unspecified; rows with fewer than k live non-NaN scores
+ *                are padded with -1
+ *   fallback_flags NULL or [R] int32: 0 = histogram path, 1 = stale
+ *                histogram, 2 = threshold bin over capacity
+ * k <= DSA_MAX_TOPK. */
+int32_t dsa_coarse_hist_topk(const float *logits, int64_t stride, const int32_t *context_lens,
+                             int32_t next_n, int32_t len_div, int32_t R, int32_t *histogram,
+                             int32_t reset_histogram, int32_t k, int32_t *out_idx,
+                             int32_t *fallback_flags, void *workspace, size_t ws_bytes,
+                             void *stream);
+
+/* ---- block maxima over 8-score blocks ------------------------------------
+ * [SG38944] amax8_varlen: for row r with n_r live scores and
+ * nb = ceil(n_r / 8) blocks, amax[r][i] = max(logits[r][8i .. 8i+7]) for
+ * i < nb - 1 (NaN ignored; an all-NaN block stays NaN), amax[r][nb-1] = +inf
+ * (the newest block is always chosen), nothing written past nb.  Rows with
+ * nb <= skip_if_blocks_le are skipped when skip_if_blocks_le > 0 (their block
+ * table is the identity anyway).
+ *   logits [R][stride] float, 16-byte aligned, stride % 4 == 0
+ *   amax   [R][amax_stride] float */
+int32_t dsa_block_amax8(const float *logits, int64_t stride, const int32_t *context_lens,
+                        int32_t next_n, int32_t R, int32_t skip_if_blocks_le, float *amax,
+                        int64_t amax_stride, void *workspace, size_t ws_bytes, void *stream);
+
+/* ---- candidate block table ----------------------------------------------
+ * [SG38944] sort_candidate_blocks: in place, the selected block ids of each
+ * row (any order, -1 padded) become the ascending INT32_MAX-padded table that
+ * the sparse logits read; rows with nb <= kb get the identity table
+ * 0 .. nb-1.  Also emits, when the pointers are not NULL:
+ *   phys_blocks [R][kb]: the same blocks as pool slot / 8 through the row's
+ *               page table (INT32_MAX for padding; needs page_size % 8 == 0)
+ *   valid_lens  [R]: live tokens covered by the table ([SG38944]
+ *               candidate_row_lens); the live positions form a prefix of the
+ *               sparse row because the newest (possibly partial) block has the
+ *               largest id.
+ * Row r uses page-table row r / next_n.  Ids outside [0, nb) are dropped and
+ * flagged DSA_DEV_BOUNDS.  kb <= 4096. */
+int32_t dsa_sort_candidate_blocks(int32_t *block_ids, int32_t kb, const int32_t *context_lens,
+                                  int32_t next_n, int32_t R, const int32_t *page_table,
+                                  int64_t page_table_stride, int32_t page_size,
+                                  int32_t *phys_blocks, int32_t *valid_lens, void *workspace,
+                                  size_t ws_bytes, void *stream);
+
+/* ---- sparse MQA logits over the chosen blocks ----------------------------
+ * [SG38944] "What this enables" (fp8_fp4_paged_sparse_mqa_logits scores only
+ * the published blocks): position i < kb*8 of row r is token
+ * t = block_table[r][i / 8] * 8 + i % 8 and gets the paged MQA logit of
+ * (r, t) -- bitwise equal to dsa_paged_mqa_logits at (r, t) -- or -inf when
+ * the table entry is padding (INT32_MAX) or t >= n_r.  Inputs as for
+ * dsa_paged_mqa_logits; kb % 16 == 0.
+ *   out        [R][out_stride] float (DSA_OUT_F32) or FP16 bits (DSA_OUT_F16,
+ *              round-to-nearest-even of the float logit, [VL52696] "Why":
+ *              the logits kernel writes FP16 directly), out_stride >= kb*8 */
+int32_t dsa_sparse_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const float *kscale,
+                              const float *weights, const int32_t *page_table,
+                              int64_t page_table_stride, const int32_t *context_lens, int32_t B,
+                              int32_t next_n, int32_t num_heads, int32_t head_dim,
+                              int32_t page_size, int32_t num_pages, const int32_t *block_table,
+                              int32_t kb, void *out, int32_t out_dtype, int64_t out_stride,
+                              void *workspace, size_t ws_bytes, void *stream);
+
+/* ---- top-k over FP16 scores ---------------------------------------------
+ * [VL52696] "Why": select on the packed FP16 score bits directly (both halves
+ * of a 32-bit word are turned into order keys with one 32-bit operation), a
+ * 10-bit coarse pass, then one exact refine pass over the remaining 6 key
+ * bits.  Positions i < valid_lens[r] take part unless NaN; ties go to the
+ * lower position (= lower column, the table being ascending).
+ *   scores      [R][stride] uint16 FP16 bits, 4-byte aligned rows (stride even)
+ *   block_table NULL: out_idx holds positions i; else [R][kb] and out_idx holds
+ *               the logical column block_table[r][i/8]*8 + i%8 (the fused
+ *               page-table transform of [SG38944] topk_bf16_small)
+ *   out_idx     [R][k] int32, order unspecified, -1 padded
+ * valid_lens[r] <= 16384, k <= DSA_MAX_TOPK. */
+int32_t dsa_topk_fp16(const uint16_t *scores, int64_t stride, const int32_t *valid_lens,
+                      int32_t R, int32_t k, const int32_t *block_table, int32_t kb,
+                      int32_t *out_idx, void *workspace, size_t ws_bytes, void *stream);
+
+/* ---- diagnostics (same device functions as the kernels above) ------------
+ * dsa_coarse_bins_range: out[i] = coarse bin of the float whose bit pattern is
+ *   start + i (-1 for NaN), for i < count; out is int16 on the device.  Used
+ *   to sweep all 2^32 patterns against an independent reference.
+ * dsa_fp16_order_keys: out[i] = 16-bit order key of the FP16 pattern in[i]
+ *   computed two halves per 32-bit word, as the FP16 select does (NaN -> 0);
+ *   n even, both arrays device-resident.
+ * dsa_wait_timeout_selftest: launches a kernel whose only wait is on a
+ *   barrier nothing arrives on, bounded by `limit_cycles`; the kernel records
+ *   DSA_DEV_TIMEOUT in the workspace status word and returns. */
+int32_t dsa_coarse_bins_range(uint32_t start, int64_t count, int16_t *out, void *stream);
+int32_t dsa_fp16_order_keys(const uint16_t *in, uint16_t *out, int64_t n, void *stream);
+int32_t dsa_wait_timeout_selftest(uint64_t limit_cycles, void *workspace, size_t ws_bytes,
+                                  void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_GB300_H */

@@ -35,8 +35,9 @@
  *       low 6 bits of the half are dropped.
  *   R6  Top-k orders by value, ties go to the lower column, NaN is never
  *       selected, short rows are padded with -1.
- *   R7  amax8: NaN is ignored inside a block, an all-NaN block stays NaN; the
- *       newest block (index ceil(n/8)-1) is +inf.
+ *   R7  amax8: the block maximum follows the same value order as the top-k
+ *       (-0 below +0), NaN is ignored inside a block, an all-NaN block stays
+ *       NaN; the newest block (index ceil(n/8)-1) is +inf.
  *   R8  Block-table padding (ids and physical blocks) is INT32_MAX; the live
  *       length of a sparse row counts the live tokens of the chosen blocks.
  *   R9  Sparse positions that are padding or past the row's live length are
@@ -298,13 +299,13 @@ void o_block_amax8(const float *logits, int64_t stride, const int64_t *row_lens,
         int64_t nb = (n + 7) / 8;
         if (skip_le > 0 && nb <= skip_le) continue;
         for (int64_t i = 0; i + 1 < nb; ++i) {
-            double m = NAN;
+            float m = NAN;
             for (int e = 0; e < 8; ++e) {
                 float v = logits[(int64_t)r * stride + 8 * i + e];
                 if (isnan(v)) continue;
-                if (isnan(m) || (double)v > m) m = (double)v;
+                if (isnan(m) || o_f32_order_key(v) > o_f32_order_key(m)) m = v;
             }
-            amax[(int64_t)r * amax_stride + i] = (float)m;
+            amax[(int64_t)r * amax_stride + i] = m;
         }
         amax[(int64_t)r * amax_stride + nb - 1] = INFINITY;
     }

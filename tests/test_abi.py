@@ -1,0 +1,98 @@
+"""CPU-side checks of the C ABI: the library loads and exports every function
+include/dsa.h declares, and host-side argument checks reject bad calls with
+the documented status before anything touches the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HDR = os.path.join(ROOT, "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dsa_sparse_attention_paged_gb300 import build
+    build.build()
+    import dsa_sparse_attention_paged_gb300 as D
+    return D.lib
+
+
+def declared():
+    src = open(HDR).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_sizes(lib):
+    assert lib.dsa_status_string(0) == b"DSA_OK"
+    assert lib.dsa_status_string(2) == b"DSA_ERR_UNSUPPORTED"
+    assert lib.dsa_version() >= 10000
+    s1, s32 = lib.dsa_workspace_size(1), lib.dsa_workspace_size(32)
+    assert s32 > s1 > 0 and s32 % 256 == 0
+    # per row: 16 B counters + 8192 x 8 B candidates + 4 KiB histogram
+    assert s32 - s1 >= 31 * (16 + 8192 * 8 + 4096) - 512
+
+
+A16 = ctypes.c_void_p(0x10000)     # aligned, never dereferenced: checks fail first
+MIS = ctypes.c_void_p(0x10004)
+
+
+def paged(lib, **kw):
+    a = dict(q=A16, kv=A16, ks=A16, w=A16, pt=A16, pts=4, ctx=A16, B=2, nn=1, H=32, D=128,
+             ps=64, P=10, out=A16, ostride=256, hist=None, ws=ctypes.c_void_p(0x20000),
+             wsb=4096, st=None)
+    a.update(kw)
+    return lib.dsa_paged_mqa_logits(a["q"], a["kv"], a["ks"], a["w"], a["pt"], a["pts"], a["ctx"],
+                                    a["B"], a["nn"], a["H"], a["D"], a["ps"], a["P"], a["out"],
+                                    a["ostride"], a["hist"], a["ws"], a["wsb"], a["st"])
+
+
+def test_paged_logits_argument_checks(lib):
+    assert paged(lib, nn=5) == 2
+    assert paged(lib, nn=0) == 2
+    assert paged(lib, H=64) == 2
+    assert paged(lib, D=64) == 2
+    assert paged(lib, ps=32) == 2
+    assert paged(lib, q=MIS) == 3
+    assert paged(lib, kv=MIS) == 3
+    assert paged(lib, hist=ctypes.c_void_p(0x10004)) == 3
+    assert paged(lib, ws=None) == 5
+    assert paged(lib, wsb=16) == 5
+    assert paged(lib, q=None) == 1
+    assert paged(lib, B=-1) == 1
+    assert paged(lib, ostride=0) == 1
+    assert paged(lib, B=0) == 0          # nothing to do, nothing launched
+
+
+def test_topk_and_block_argument_checks(lib):
+    ws = ctypes.c_void_p(0x20000)
+    big = lib.dsa_workspace_size(4)
+    f = lib.dsa_coarse_hist_topk
+    assert f(A16, 128, A16, 1, 1, 4, None, 0, 0, A16, None, ws, big, None) == 2      # k = 0
+    assert f(A16, 128, A16, 1, 1, 4, None, 0, 4096, A16, None, ws, big, None) == 2   # k > 2048
+    assert f(A16, 128, A16, 1, 1, 4, None, 0, 16, A16, None, ws, 1024, None) == 5    # too small
+    assert f(A16, 128, A16, 1, 1, 0, None, 0, 16, A16, None, ws, big, None) == 0     # R = 0
+    assert f(A16, 128, A16, 1, 0, 4, None, 0, 16, A16, None, ws, big, None) == 1     # len_div
+    g = lib.dsa_block_amax8
+    assert g(MIS, 128, A16, 1, 2, 0, A16, 16, ws, 4096, None) == 3
+    assert g(A16, 130, A16, 1, 2, 0, A16, 16, ws, 4096, None) == 3
+    h = lib.dsa_sort_candidate_blocks
+    assert h(A16, 8192, A16, 1, 2, A16, 4, 64, None, None, ws, 4096, None) == 2
+    assert h(A16, 512, A16, 1, 2, A16, 4, 12, None, None, ws, 4096, None) == 2
+    s = lib.dsa_sparse_mqa_logits
+    assert s(A16, A16, A16, A16, A16, 4, A16, 2, 1, 32, 128, 64, 10, A16, 500, A16, 0, 4000,
+             ws, 4096, None) == 2  # kb not a multiple of 16
+    assert s(A16, A16, A16, A16, A16, 4, A16, 2, 1, 32, 128, 64, 10, A16, 512, A16, 0, 100,
+             ws, 4096, None) == 1  # out_stride < kb * 8
+    t = lib.dsa_topk_fp16
+    assert t(A16, 4097, A16, 2, 16, None, 0, A16, ws, 4096, None) == 3  # odd stride
+    assert t(A16, 4096, A16, 2, 0, None, 0, A16, ws, 4096, None) == 2

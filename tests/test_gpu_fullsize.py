@@ -1,0 +1,82 @@
+"""Full-size parity on the five named workloads, in the launch configuration
+the bench times (DecodePlan): logits on sampled (row, column) pairs against
+the oracle one by one; histograms, top-k sets, block tables and the FP16
+select exactly, on the GPU's own logits; sparse logits bitwise against the
+dense logits at the chosen positions."""
+import numpy as np
+import pytest
+import torch
+
+import synthetic as S
+from oracle import oracle as O
+from tests.helpers import assert_close, sets_equal, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", ["c0", "c1", "c2", "c3", "c3u", "c4"])
+def test_full_size_workload(name):
+    from dsa_sparse_attention_paged_gb300.pipeline import DecodePlan
+    w = S.named(name)
+    case = S.generate(w)
+    d = to_dev(case)
+    nn, ps = w.next_n, w.page_size
+    plan = DecodePlan(w.B, nn, max(w.context_lens), ps, k=2048, kb=512, two_level=True)
+    dense_idx, sparse_idx = plan.step(d["q"], d["kv"], d["kscale"], d["weights"],
+                                      d["page_table"], d["context_lens"])
+    torch.cuda.synchronize()
+    assert plan.ws.status() == 0
+    R = w.R
+    rl = O.row_lens(case["context_lens"], nn)
+    L = plan.logits.cpu().numpy()
+
+    # logits: 8192 sampled live positions (plus every row's first and last column)
+    rng = np.random.default_rng(1)
+    rows = rng.integers(0, R, 8192)
+    cols = (rng.random(8192) * rl[rows]).astype(np.int64)
+    rows = np.concatenate([rows, np.arange(R), np.arange(R)])
+    cols = np.concatenate([cols, np.zeros(R, np.int64), rl - 1])
+    ref = O.logits_at(case["q"], case["kv"], case["kscale"], case["weights"],
+                      case["page_table"], nn, ps, rows, cols)
+    assert_close(L[rows, cols], ref, f"{name} logits")
+
+    # histogram of the GPU's own logits (the plan's top-k reset it, so rerun)
+    hist = torch.zeros((R, 1024), dtype=torch.int32, device="cuda")
+    import dsa_sparse_attention_paged_gb300 as D
+    L2 = D.paged_mqa_logits(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"],
+                            d["context_lens"], nn, plan.ws, logits_stride=plan.stride,
+                            histogram=hist)
+    torch.cuda.synchronize()
+    live = np.arange(plan.stride)[None, :] < rl[:, None]
+    Lm = np.where(live, L, np.nan).astype(np.float32)
+    np.testing.assert_array_equal(L2.cpu().numpy()[live], L[live])
+    np.testing.assert_array_equal(hist.cpu().numpy(), O.histogram(Lm, rl))
+    if name == "c2":  # 'mixed' spans fine, unit and saturating bins
+        h = hist.cpu().numpy().sum(0)
+        assert h[0] + h[1023] > 0 and h[1:207].sum() + h[817:1023].sum() > 0
+        assert h[208:816].sum() > 0
+
+    # dense top-2048
+    assert sets_equal(dense_idx.cpu().numpy(), O.topk(Lm, rl, 2048))
+
+    # two-level chain
+    A = plan.amax.cpu().numpy()
+    kb = plan.kb
+    nb = (rl + 7) // 8
+    refA = O.block_amax8(Lm, rl, skip_le=kb, amax_stride=plan.amax_stride, fill=0.0)
+    for r in range(R):
+        if nb[r] > kb:
+            np.testing.assert_array_equal(A[r, :nb[r]], refA[r, :nb[r]])
+    rtr = np.arange(R, dtype=np.int32) // nn
+    t_ref, p_ref, v_ref = O.block_table(A, rl, rtr, kb, case["page_table"], ps)
+    np.testing.assert_array_equal(plan.block_ids.cpu().numpy(), t_ref)
+    np.testing.assert_array_equal(plan.phys.cpu().numpy(), p_ref)
+    np.testing.assert_array_equal(plan.valid_lens.cpu().numpy(), v_ref)
+    SP16 = plan.sparse.cpu().numpy().view(np.uint16)
+    pos = np.arange(kb * 8)
+    for r in range(R):
+        tok = t_ref[r, pos // 8].astype(np.int64) * 8 + pos % 8
+        n_live = v_ref[r]
+        np.testing.assert_array_equal(SP16[r, :n_live], O.fp16_rn_array(L[r, tok[:n_live]]))
+        assert (SP16[r, n_live:] == 0xFC00).all()
+    assert sets_equal(sparse_idx.cpu().numpy(), O.topk_fp16(SP16, v_ref, 2048, t_ref))

@@ -1,0 +1,135 @@
+"""Parity of the two-level candidate path with the oracle: block amax8, block
+top-k, the ascending padded block table, sparse logits (bitwise equal to the
+dense logits at the chosen positions) and the FP16 packed top-k."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from tests.helpers import assert_close, make, sets_equal, to_dev
+
+pytestmark = pytest.mark.gpu
+IMAX = 2**31 - 1
+
+
+def _dense(case, stride):
+    import dsa_sparse_attention_paged_gb300 as D
+    d = to_dev(case)
+    R = d["q"].shape[0]
+    ws = D.Workspace(R)
+    logits = torch.full((R, stride), float("nan"), dtype=torch.float32, device="cuda")
+    D.paged_mqa_logits(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"],
+                       d["context_lens"], case["next_n"], ws, logits=logits)
+    return d, ws, logits
+
+
+@pytest.mark.parametrize("ctx,kb,ps,nn", [
+    ([40000, 3000, 20001], 512, 128, 1),
+    ([9000, 17], 256, 64, 1),
+    ([12000, 5000], 512, 64, 2),
+])
+def test_two_level_chain(ctx, kb, ps, nn):
+    import dsa_sparse_attention_paged_gb300 as D
+    B = len(ctx)
+    R = B * nn
+    case = make(B, nn, ctx, ps, "normal", seed=400 + kb)
+    stride = max(ctx) + 16
+    d, ws, logits = _dense(case, stride)
+    rl = O.row_lens(case["context_lens"], nn)
+    L = logits.cpu().numpy()
+
+    # amax8 (rows with nb <= kb skipped)
+    amax_stride = (stride + 7) // 8
+    amax = torch.full((R, amax_stride), -5.0, dtype=torch.float32, device="cuda")
+    D.block_amax8(logits, d["context_lens"], nn, ws, skip_if_blocks_le=kb, amax=amax)
+    A = amax.cpu().numpy()
+    refA = O.block_amax8(L, rl, skip_le=kb, amax_stride=amax_stride, fill=-5.0)
+    np.testing.assert_array_equal(A, refA)
+
+    # block top-k on the GPU's amax, rows with nb > kb compared
+    ids = D.coarse_hist_topk(amax, d["context_lens"], nn, kb, ws, len_div=8)
+    nb = (rl + 7) // 8
+    ref_ids = O.topk(A, nb, kb)
+    got_ids = ids.cpu().numpy()
+    for r in range(R):
+        if nb[r] > kb:
+            assert sets_equal(got_ids[r:r + 1], ref_ids[r:r + 1]), r
+
+    # sort -> table, phys, valid lens
+    phys = torch.empty((R, kb), dtype=torch.int32, device="cuda")
+    vl = torch.empty((R,), dtype=torch.int32, device="cuda")
+    D.sort_candidate_blocks(ids, d["context_lens"], nn, d["page_table"], ps, ws,
+                            phys_blocks=phys, valid_lens=vl)
+    rtr = np.arange(R, dtype=np.int32) // nn
+    t_ref, p_ref, v_ref = O.block_table(A, rl, rtr, kb, case["page_table"], ps)
+    np.testing.assert_array_equal(ids.cpu().numpy(), t_ref)
+    np.testing.assert_array_equal(phys.cpu().numpy(), p_ref)
+    np.testing.assert_array_equal(vl.cpu().numpy(), v_ref)
+
+    # sparse logits: oracle tolerance, and bitwise equal to the dense logits
+    sp = D.sparse_mqa_logits(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"],
+                             d["context_lens"], nn, ids, ws, out_dtype=D.OUT_F32)
+    sp16 = D.sparse_mqa_logits(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"],
+                               d["context_lens"], nn, ids, ws, out_dtype=D.OUT_F16)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    SP = sp.cpu().numpy()
+    ref_sp = O.sparse_logits(case["q"], case["kv"], case["kscale"], case["weights"],
+                             case["page_table"], rl, rtr, ps, t_ref)
+    masked = np.isneginf(ref_sp)
+    np.testing.assert_array_equal(np.isneginf(SP), masked)
+    assert_close(SP[~masked], ref_sp[~masked], "sparse logits")
+    pos = np.arange(kb * 8)
+    for r in range(R):
+        tok = t_ref[r, pos // 8].astype(np.int64) * 8 + pos % 8
+        ok = ~masked[r]
+        np.testing.assert_array_equal(SP[r, ok], L[r, tok[ok]])
+    # live positions are a prefix of length valid_len
+    for r in range(R):
+        assert (~masked[r, :v_ref[r]]).all() and masked[r, v_ref[r]:].all()
+    # FP16 output is the RN-even rounding of the FP32 one
+    np.testing.assert_array_equal(sp16.cpu().numpy().view(np.uint16), O.fp16_rn_array(SP))
+
+    # FP16 top-2048 with the fused table transform, on the GPU's own FP16 scores
+    k = 2048
+    top = D.topk_fp16(sp16, vl, k, ws, block_table=ids)
+    torch.cuda.synchronize()
+    ref_top = O.topk_fp16(sp16.cpu().numpy().view(np.uint16), v_ref, k, t_ref)
+    assert sets_equal(top.cpu().numpy(), ref_top)
+
+
+def test_fp16_topk_ties_nan_and_positions():
+    import dsa_sparse_attention_paged_gb300 as D
+    rng = np.random.default_rng(3)
+    R, n = 4, 6000
+    vals = rng.normal(0, 4, (R, n)).astype(np.float16)
+    vals[0, :] = np.float16(1.0)                      # all ties
+    vals[1, ::3] = np.float16(np.nan)
+    vals[2, :50] = np.float16(np.inf)
+    vals[2, 50:60] = np.float16(-np.inf)
+    vals[3, 100:200] = np.float16(-0.0)
+    s = torch.from_numpy(vals.view(np.uint16).copy()).cuda()
+    ws = D.Workspace(R)
+    for vl_list, k in (([n, n, n, n], 2048), ([5999, 17, 2048, 1], 2048), ([n, 4001, 3, 0], 1)):
+        vl = torch.tensor(vl_list, dtype=torch.int32, device="cuda")
+        out = D.topk_fp16(s, vl, k, ws)
+        torch.cuda.synchronize()
+        ref = O.topk_fp16(vals.view(np.uint16), np.array(vl_list, np.int32), k)
+        assert sets_equal(out.cpu().numpy(), ref), (vl_list, k)
+
+
+def test_fp16_order_keys_all_65536_encodings():
+    import dsa_sparse_attention_paged_gb300 as D
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    keys = D.fp16_order_keys(torch.from_numpy(codes.copy()).cuda()).cpu().numpy()
+    vals = codes.view(np.float16).astype(np.float64)
+    nan = np.isnan(vals)
+    assert (keys[nan] == 0).all()
+    kk = keys[~nan].astype(np.int64)
+    v = vals[~nan]
+    assert len(np.unique(kk)) == kk.size  # one key per encoding
+    order = np.argsort(kk)
+    assert np.all(np.diff(v[order]) >= 0)  # key order == value order
+    # +0 above -0
+    assert keys[0x0000] > keys[0x8000]
+    assert (kk > 0).all()

@@ -356,10 +356,14 @@ def test_amax8_closed_form_on_arange_rows():
     assert (a[:4] == -7.0).all() and a[4, 9] == np.inf  # nb = 1, 1, 2, 8 skipped; 10 kept
 
 
-def test_amax8_nan_handling():
-    x = np.array([[np.nan, 1.0, np.nan, -3.0, 0, 0, 0, 0] + [np.nan] * 8 + [1.0]], np.float32)
-    a = O.block_amax8(x, np.array([17]), amax_stride=3)
-    assert a[0, 0] == 1.0 and np.isnan(a[0, 1]) and a[0, 2] == np.inf
+def test_amax8_nan_and_signed_zero_handling():
+    x = np.array([[np.nan, 1.0, np.nan, -3.0, 0, 0, 0, 0] + [np.nan] * 8 +
+                  [-0.0, 0.0, -0.0, -1.0, -0.0, -2.0, -0.0, -0.0] +
+                  [-0.0, -0.0, -5.0, -0.0, -0.0, -0.0, -0.0, -0.0] + [1.0]], np.float32)
+    a = O.block_amax8(x, np.array([33]), amax_stride=5)
+    assert a[0, 0] == 1.0 and np.isnan(a[0, 1]) and a[0, 4] == np.inf
+    assert a[0, 2] == 0.0 and not np.signbit(a[0, 2])  # +0 is above -0
+    assert a[0, 3] == 0.0 and np.signbit(a[0, 3])
 
 
 def test_block_table_closed_form():
