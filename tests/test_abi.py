@@ -13,8 +13,8 @@ HDR = os.path.join(ROOT, "include", "dsa.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from dsa_sparse_attention_paged_gb300 import build
-    build.build()
+    import __graft_entry__ as g
+    g.build()
     import dsa_sparse_attention_paged_gb300 as D
     return D.lib
 
