@@ -33,7 +33,8 @@ class DecodePlan:
         self.B, self.next_n, self.page_size = B, next_n, page_size
         self.R = B * next_n
         self.k, self.kb, self.two_level = k, kb, two_level
-        self.stride = int(max_context)
+        # row stride padded to 8 floats: 32-byte aligned rows for the vector loads
+        self.stride = (int(max_context) + 7) // 8 * 8
         dev = torch.device(device)
         R = self.R
         self.ws = Workspace(R, device=dev)
