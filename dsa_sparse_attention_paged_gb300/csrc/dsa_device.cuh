@@ -27,7 +27,10 @@ struct WsLayout {
   // per row: 1024 int32 histogram for selects given no histogram
   static size_t hist_off(int64_t R) { return align(cand_off(R) + cand_bytes(R)); }
   static size_t hist_bytes(int64_t R) { return (size_t)R * DSA_NUM_BINS * 4; }
-  static size_t total(int64_t R) { return align(hist_off(R) + hist_bytes(R)); }
+  // per row: 4096 int32 fine histogram of a threshold bin over capacity
+  static size_t fine_off(int64_t R) { return align(hist_off(R) + hist_bytes(R)); }
+  static size_t fine_bytes(int64_t R) { return (size_t)R * 4096 * 4; }
+  static size_t total(int64_t R) { return align(fine_off(R) + fine_bytes(R)); }
   static size_t align(size_t x) { return (x + 255) & ~(size_t)255; }
 };
 

@@ -27,7 +27,6 @@
 // gridDim.x contiguous ranges, one per CTA; each CTA derives its range from a
 // prefix sum over context_lens (no separate metadata kernel).
 #include <algorithm>
-#include <mutex>
 
 #include "dsa_device.cuh"
 #include "dsa_host.h"
@@ -40,8 +39,8 @@ constexpr int kTileTok = 128;
 constexpr int kStageK = kTileTok * 128;      // bytes of K per stage
 constexpr int kStageKs = kTileTok * 4;       // bytes of kscale per stage
 constexpr int kMaxStages = 16;
-constexpr int kThreads = 192;
-constexpr int kEpiWarps = 4;
+constexpr int kThreads = 320;       // producer, MMA, 2 x 4 epilogue warps
+constexpr int kEpiWarps = 8;
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in per CTA
 
 struct LogitsArgs {
@@ -64,6 +63,7 @@ struct LogitsArgs {
   uint32_t *status;
   int32_t num_stages;
   int32_t num_acc;
+  int32_t num_ks;       // kscale ring depth
   uint32_t tmem_cols;
   long long wait_limit;
 };
@@ -72,7 +72,11 @@ struct SmemPlan {
   int kst, q, ks, w, hist, bar, misc, total;
 };
 
-__host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, int stages, int nacc) {
+// Histogram slots per epilogue warpgroup: one per warp at next_n = 1, one
+// shared by the group's four warps otherwise (shared memory goes to stages).
+__host__ __device__ constexpr int hist_slots_per_group(int nn) { return nn == 1 ? 4 : 1; }
+
+__host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, int stages, int nacc, int nks) {
   SmemPlan p;
   int off = 0;
   p.kst = off;
@@ -80,14 +84,14 @@ __host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, int stages, int
   p.q = off;
   off += 2 * nn * 32 * 128;
   p.ks = off;
-  off += stages * kStageKs;
+  off += nks * kStageKs;
   p.w = off;
   off += 2 * nn * 32 * 4;
   p.hist = off;
-  off += hist ? kEpiWarps * nn * DSA_NUM_BINS * 4 : 0;
+  off += hist ? 2 * hist_slots_per_group(nn) * nn * DSA_NUM_BINS * 4 : 0;
   off = (off + 7) & ~7;
   p.bar = off;
-  off += (2 * stages + 4 + 2 * nacc + 2) * 8;
+  off += (2 * stages + 2 * nks + 4 + 2 * nacc + 3) * 8;
   p.misc = off;
   off += 64;
   p.total = off + 1024;  // slack to align the base to 1024 bytes
@@ -185,19 +189,46 @@ __device__ void compute_sched(const LogitsArgs &a, int *out_u0, int *out_i0, lon
   *out_cnt = g1 - g0;
 }
 
-// Sum over the 32 heads of one row: kscale, ReLU, head weight, in a fixed
-// order (dense and sparse share it, so their logits are bitwise equal).
+// Packed FP32 pairs (sm_100 family): two lanes of arithmetic per instruction.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// Sum over the 32 heads of one row: kscale, ReLU, head weight.  Four
+// independent accumulation chains (heads h = 4i + c go to chain c), combined
+// as (c0 + c1) + (c2 + c3).  Dense and sparse logits share this function, so
+// they are bitwise equal.
 __device__ __forceinline__ float head_sum(const uint32_t (&v)[32], float ks, const float *w) {
-  float acc = 0.0f;
+  const uint64_t ks2 = pk2(ks, ks);
+  uint64_t a01 = pk2(0.0f, 0.0f), a23 = pk2(0.0f, 0.0f);
 #pragma unroll
   for (int h = 0; h < 32; h += 4) {
     const float4 wv = *reinterpret_cast<const float4 *>(w + h);
-    acc = fmaf(wv.x, fmaxf(__uint_as_float(v[h + 0]) * ks, 0.0f), acc);
-    acc = fmaf(wv.y, fmaxf(__uint_as_float(v[h + 1]) * ks, 0.0f), acc);
-    acc = fmaf(wv.z, fmaxf(__uint_as_float(v[h + 2]) * ks, 0.0f), acc);
-    acc = fmaf(wv.w, fmaxf(__uint_as_float(v[h + 3]) * ks, 0.0f), acc);
+    float p0, p1, p2, p3;
+    upk2(mul2(pk2(__uint_as_float(v[h + 0]), __uint_as_float(v[h + 1])), ks2), p0, p1);
+    upk2(mul2(pk2(__uint_as_float(v[h + 2]), __uint_as_float(v[h + 3])), ks2), p2, p3);
+    a01 = fma2(pk2(wv.x, wv.y), pk2(fmaxf(p0, 0.0f), fmaxf(p1, 0.0f)), a01);
+    a23 = fma2(pk2(wv.z, wv.w), pk2(fmaxf(p2, 0.0f), fmaxf(p3, 0.0f)), a23);
   }
-  return acc;
+  float c0, c1, c2, c3;
+  upk2(a01, c0, c1);
+  upk2(a23, c2, c3);
+  return (c0 + c1) + (c2 + c3);
 }
 
 template <int NN, bool SPARSE, bool OUT_F16, bool HIST>
@@ -206,13 +237,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const LogitsArgs a) {
   constexpr int N = 32 * NN;
   constexpr uint32_t IDESC = idesc_e4m3_f32(128, N);
+  constexpr int HS = hist_slots_per_group(NN);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int S = a.num_stages;
   const int A = a.num_acc;
-  const SmemPlan P = smem_plan(NN, HIST, S, A);
+  const int KS = a.num_ks;
+  const SmemPlan P = smem_plan(NN, HIST, S, A, KS);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -222,14 +255,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *w_s = reinterpret_cast<float *>(smem + P.w);
   int *hist_s = reinterpret_cast<int *>(smem + P.hist);
   const uint32_t bar0 = smem_u32(smem + P.bar);
-  auto FULL = [&](int s) { return bar0 + 8u * s; };
-  auto EMPTY = [&](int s) { return bar0 + 8u * (S + s); };
-  auto QFULL = [&](int q) { return bar0 + 8u * (2 * S + q); };
-  auto QEMPTY = [&](int q) { return bar0 + 8u * (2 * S + 2 + q); };
-  auto AFULL = [&](int x) { return bar0 + 8u * (2 * S + 4 + x); };
-  auto AEMPTY = [&](int x) { return bar0 + 8u * (2 * S + 4 + A + x); };
-  const uint32_t DRAIN = bar0 + 8u * (2 * S + 4 + 2 * A);
-  const uint32_t GSYNC = bar0 + 8u * (2 * S + 4 + 2 * A + 1);
+  // barrier map
+  auto FULL = [&](int s) { return bar0 + 8u * s; };                       // K landed
+  auto EMPTY = [&](int s) { return bar0 + 8u * (S + s); };                // MMA done with K
+  auto KSF = [&](int k) { return bar0 + 8u * (2 * S + k); };              // kscale landed
+  auto KSE = [&](int k) { return bar0 + 8u * (2 * S + KS + k); };         // epilogue done
+  const uint32_t qb0 = bar0 + 8u * (2 * S + 2 * KS);
+  auto QFULL = [&](int q) { return qb0 + 8u * q; };
+  auto QEMPTY = [&](int q) { return qb0 + 8u * (2 + q); };
+  auto AFULL = [&](int x) { return qb0 + 8u * (4 + x); };
+  auto AEMPTY = [&](int x) { return qb0 + 8u * (4 + A + x); };
+  const uint32_t DRAIN = qb0 + 8u * (4 + 2 * A);
+  auto GSYNC = [&](int g) { return qb0 + 8u * (5 + 2 * A + g); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P.misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P.misc + 4);
   int *sched = reinterpret_cast<int *>(smem + P.misc + 16);
@@ -238,7 +275,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(FULL(s), 1);
-      mbar_init(EMPTY(s), 1 + kEpiWarps);
+      mbar_init(EMPTY(s), 1);
+    }
+    for (int k = 0; k < KS; ++k) {
+      mbar_init(KSF(k), 1);
+      mbar_init(KSE(k), 4);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(QFULL(q), 1);
@@ -246,16 +287,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < A; ++x) {
       mbar_init(AFULL(x), 1);
-      mbar_init(AEMPTY(x), kEpiWarps);
+      mbar_init(AEMPTY(x), 4);
     }
     mbar_init(DRAIN, 1);
-    mbar_init(GSYNC, kEpiWarps);
+    mbar_init(GSYNC(0), 4);
+    mbar_init(GSYNC(1), 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) compute_sched<SPARSE>(a, &sched[0], &sched[1], sched_cnt);
   if (HIST) {
-    for (int i = threadIdx.x; i < kEpiWarps * NN * DSA_NUM_BINS; i += kThreads) hist_s[i] = 0;
+    for (int i = threadIdx.x; i < 2 * HS * NN * DSA_NUM_BINS; i += kThreads) hist_s[i] = 0;
   }
   __syncthreads();
   const long long count = *sched_cnt;
@@ -299,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         n_live = eff_ctx(a, b);
         qrow0 = u * N;
       }
-      // Physical rows for this tile, read before waiting for the slot.
+      // physical rows of this tile, read before waiting for a free stage
       int row = -1;
       if (SPARSE) {
         if (lane < 16) {
@@ -346,19 +388,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
       }
       const int s = (int)(n % S);
-      const uint32_t ph = (uint32_t)((n / S) & 1);
-      if (lane == 0) ok = mbar_wait(EMPTY(s), ph ^ 1, ctl);
+      const int kx = (int)(n % KS);
+      if (lane == 0) {
+        ok = mbar_wait(EMPTY(s), (uint32_t)(((n / S) & 1) ^ 1), ctl) &&
+             mbar_wait(KSE(kx), (uint32_t)(((n / KS) & 1) ^ 1), ctl);
+      }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       const unsigned loads = __ballot_sync(0xffffffffu, row >= 0);
       const int blk_rows = SPARSE ? 8 : a.page_size;
-      const uint32_t bytes = (uint32_t)__popc(loads) * (uint32_t)(blk_rows * 132);
-      if (lane == 0) mbar_arrive_expect_tx(FULL(s), bytes);
+      const uint32_t nload = (uint32_t)__popc(loads);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(FULL(s), nload * (uint32_t)(blk_rows * 128));
+        mbar_arrive_expect_tx(KSF(kx), nload * (uint32_t)(blk_rows * 4));
+      }
       __syncwarp();
       if (row >= 0) {
         tma_load_2d_hint(kst + s * kStageK + lane * blk_rows * 128, &tm_k, FULL(s), 0, row, pol);
-        bulk_load(smem_u32(ks_s + s * kTileTok + lane * blk_rows), a.kscale + (int64_t)row,
-                  blk_rows * 4, FULL(s));
+        bulk_load(smem_u32(ks_s + kx * kTileTok + lane * blk_rows), a.kscale + (int64_t)row,
+                  blk_rows * 4, KSF(kx));
       }
       ++issued;
     }
@@ -367,6 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long lim = a.wait_limit;
       for (long long n = (issued > S ? issued - S : 0); n < issued; ++n)
         mbar_wait_drain(FULL((int)(n % S)), (uint32_t)((n / S) & 1), lim);
+      for (long long n = (issued > KS ? issued - KS : 0); n < issued; ++n)
+        mbar_wait_drain(KSF((int)(n % KS)), (uint32_t)((n / KS) & 1), lim);
       for (int k2 = (q_issued > 2 ? q_issued - 2 : 0); k2 < q_issued; ++k2)
         mbar_wait_drain(QFULL(k2 & 1), (uint32_t)((k2 >> 1) & 1), lim);
     }
@@ -409,51 +459,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;                 // 0..3: histogram slot
-    const int lane_base = 32 * (warp & 3);   // TMEM lanes this warp may read
-    const int tok = lane_base + lane;        // token (row of D) owned by this thread
-    int *my_hist = hist_s + ew * NN * DSA_NUM_BINS;
+    // two warpgroups take alternate tiles; in each, warp w reads TMEM lanes
+    // 32*(w%4) .. +31, i.e. one token per thread
+    const int g = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const int lane_base = 32 * quarter;
+    const int tok = lane_base + lane;
+    const int gtid = ((warp - 2) & 3) * 32 + lane;  // 0..127 within the group
+    int *grp_hist = hist_s + g * HS * NN * DSA_NUM_BINS;
+    int *my_hist = grp_hist + (HS == 4 ? quarter : 0) * NN * DSA_NUM_BINS;
     TileIter<SPARSE> it;
     it.init(a, u_start, i_start);
     int prev_u = -1, unit_ord = -1, qb = 0;
     uint32_t gsync_ph = 0;
     int64_t ctx_b = 0, n_row = 0;
     int row_base = 0;
-    bool ok = true;
+    bool ok = true, touched = false;
 
-    // warp-uniform bounded wait: every lane polls, the warp leaves together
     auto ewait = [&](uint32_t bar, uint32_t parity) -> bool {
       const bool r = mbar_wait(bar, parity, ctl);
       return __all_sync(0xffffffffu, r) != 0;
     };
-    // all four epilogue warps meet (bounded wait on an mbarrier)
     auto group_sync = [&]() -> bool {
       __syncwarp();
-      if (lane == 0) mbar_arrive(GSYNC);
-      const bool r = ewait(GSYNC, gsync_ph);
+      if (lane == 0) mbar_arrive(GSYNC(g));
+      const bool r = ewait(GSYNC(g), gsync_ph);
       gsync_ph ^= 1;
       return r;
     };
-    // sum the four warps' slots for the finished request, add them to the
-    // global histogram with packed 64-bit atomics, and clear the slots
+    // add this group's counts for the finished request to the global
+    // histogram (packed 64-bit atomics on bin pairs) and clear its slots
     auto flush = [&](int rb) -> bool {
       if (!group_sync()) return false;
-      const int t128 = threadIdx.x - 64;
       for (int j = 0; j < NN; ++j) {
-        for (int p = t128; p < DSA_NUM_BINS / 2; p += 128) {
+        for (int p = gtid; p < DSA_NUM_BINS / 2; p += 128) {
           uint32_t c0 = 0, c1 = 0;
 #pragma unroll
-          for (int w = 0; w < kEpiWarps; ++w) {
-            int *sl = hist_s + (w * NN + j) * DSA_NUM_BINS + 2 * p;
+          for (int w = 0; w < HS; ++w) {
+            int *sl = grp_hist + (w * NN + j) * DSA_NUM_BINS + 2 * p;
             c0 += sl[0];
             c1 += sl[1];
             sl[0] = 0;
             sl[1] = 0;
           }
           if (c0 | c1) {
-            unsigned long long *g = reinterpret_cast<unsigned long long *>(
+            unsigned long long *gp = reinterpret_cast<unsigned long long *>(
                 a.histogram + (int64_t)(rb + j) * DSA_NUM_BINS + 2 * p);
-            atomicAdd(g, ((unsigned long long)c1 << 32) | c0);
+            atomicAdd(gp, ((unsigned long long)c1 << 32) | c0);
           }
         }
       }
@@ -463,9 +515,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (long long n = 0; n < count; ++n, it.next(a)) {
       const int u = it.u, i = it.i;
       if (u != prev_u) {
-        if (HIST && prev_u >= 0) {
+        if (HIST && touched) {
           if (!(ok = flush(row_base))) break;
         }
+        touched = false;
         ++unit_ord;
         prev_u = u;
         qb = unit_ord & 1;
@@ -480,62 +533,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!(ok = ewait(QFULL(qb), (unit_ord >> 1) & 1))) break;
       }
-      const int s = (int)(n % S);
-      const int x = (int)(n % A);
-      const int64_t pos = (int64_t)i * kTileTok + tok;
-      int32_t blk = 0;
-      if (SPARSE) blk = a.block_table[(int64_t)u * a.kb + pos / 8];
-      if (!(ok = ewait(FULL(s), (uint32_t)((n / S) & 1)))) break;
-      const float ks = ks_s[s * kTileTok + tok];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(EMPTY(s));
-      if (!(ok = ewait(AFULL(x), (uint32_t)((n / A) & 1)))) break;
-      tc_fence_after();
-      float acc[NN];
-#pragma unroll
-      for (int j = 0; j < NN; ++j) {
-        uint32_t v[32];
-        tmem_ld32(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(x * N + j * 32), v);
-        tmem_ld_wait();
-        acc[j] = head_sum(v, ks, w_s + qb * N + j * 32);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(AEMPTY(x));
-
-      if (SPARSE) {
-        const int64_t t = (int64_t)blk * 8 + (pos & 7);
-        const bool live = blk != INT32_MAX && blk >= 0 && t < n_row;
-        const float val = live ? acc[0] : -INFINITY;
-        if (OUT_F16) {
-          reinterpret_cast<__half *>(a.out)[(int64_t)u * a.out_stride + pos] = __float2half_rn(val);
-        } else {
-          reinterpret_cast<float *>(a.out)[(int64_t)u * a.out_stride + pos] = val;
-        }
-      } else {
-        const int64_t t = pos;
+      const bool last_of_unit = (i == it.tiles - 1 || n == count - 1);
+      if ((int)(n & 1) == g) {
+        touched = true;
+        const int x = (int)(n % A);
+        const int kx = (int)(n % KS);
+        const int64_t pos = (int64_t)i * kTileTok + tok;
+        int32_t blk = 0;
+        if (SPARSE) blk = a.block_table[(int64_t)u * a.kb + pos / 8];
+        if (!(ok = ewait(KSF(kx), (uint32_t)((n / KS) & 1)))) break;
+        const float ks = ks_s[kx * kTileTok + tok];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(KSE(kx));
+        if (!(ok = ewait(AFULL(x), (uint32_t)((n / A) & 1)))) break;
+        tc_fence_after();
+        float acc[NN];
 #pragma unroll
         for (int j = 0; j < NN; ++j) {
-          int64_t n_rj = ctx_b - (NN - 1 - j);
-          if (n_rj > a.out_stride) {
-            n_rj = a.out_stride;
-            if (t == a.out_stride) set_status(a.status, DSA_DEV_BOUNDS);
+          uint32_t v[32];
+          tmem_ld32(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(x * N + j * 32), v);
+          tmem_ld_wait();
+          acc[j] = head_sum(v, ks, w_s + qb * N + j * 32);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(AEMPTY(x));
+
+        if (SPARSE) {
+          const int64_t t = (int64_t)blk * 8 + (pos & 7);
+          const bool live = blk != INT32_MAX && blk >= 0 && t < n_row;
+          const float val = live ? acc[0] : -INFINITY;
+          if (OUT_F16) {
+            reinterpret_cast<__half *>(a.out)[(int64_t)u * a.out_stride + pos] = __float2half_rn(val);
+          } else {
+            reinterpret_cast<float *>(a.out)[(int64_t)u * a.out_stride + pos] = val;
           }
-          if (t < n_rj) {
-            reinterpret_cast<float *>(a.out)[(int64_t)(row_base + j) * a.out_stride + t] = acc[j];
-            if (HIST) {
-              const int bin = coarse_bin(acc[j]);
-              if (bin >= 0) atomicAdd(&my_hist[j * DSA_NUM_BINS + bin], 1);
+        } else {
+          const int64_t t = pos;
+#pragma unroll
+          for (int j = 0; j < NN; ++j) {
+            int64_t n_rj = ctx_b - (NN - 1 - j);
+            if (n_rj > a.out_stride) {
+              n_rj = a.out_stride;
+              if (t == a.out_stride) set_status(a.status, DSA_DEV_BOUNDS);
+            }
+            if (t < n_rj) {
+              reinterpret_cast<float *>(a.out)[(int64_t)(row_base + j) * a.out_stride + t] = acc[j];
+              if (HIST) {
+                const int bin = coarse_bin(acc[j]);
+                if (bin >= 0) atomicAdd(&my_hist[j * DSA_NUM_BINS + bin], 1);
+              }
             }
           }
         }
       }
-      if (i == it.tiles - 1 || n == count - 1) {
+      if (last_of_unit) {
         __syncwarp();
         if (lane == 0) mbar_arrive(QEMPTY(qb));
       }
     }
-    if (HIST && ok && prev_u >= 0) flush(row_base);
+    if (HIST && ok && touched) flush(row_base);
   }
 
   __syncthreads();
@@ -545,34 +602,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Stage count and ring depths for one instantiation: as many 16 KiB K stages
+// as fit next to the Q/weight buffers, the histogram slots and a kscale ring
+// deep enough (stages + accumulators + 2) never to hold the producer back.
+struct LaunchPlan {
+  int stages, nacc, nks, cols, smem;
+};
+
+inline LaunchPlan plan_for(int nn, bool hist) {
+  LaunchPlan L;
+  const int N = 32 * nn;
+  L.nacc = std::min(8, 512 / N);
+  L.cols = 32;
+  while (L.cols < L.nacc * N) L.cols <<= 1;
+  L.stages = kMaxStages;
+  while (L.stages > 2 &&
+         smem_plan(nn, hist, L.stages, L.nacc, L.stages + L.nacc + 2).total > kSmemLimit)
+    --L.stages;
+  L.nks = L.stages + L.nacc + 2;
+  L.smem = smem_plan(nn, hist, L.stages, L.nacc, L.nks).total;
+  return L;
+}
+
 template <int NN, bool SPARSE, bool OUT_F16, bool HIST>
 dsa_status_t launch_one(const CUtensorMap &tk, const CUtensorMap &tq, const LogitsArgs &a0,
                         int grid, cudaStream_t st) {
   LogitsArgs a = a0;
-  const int N = 32 * NN;
-  a.num_acc = std::min(8, 512 / N);
-  int cols = 32;
-  while (cols < a.num_acc * N) cols <<= 1;
-  a.tmem_cols = (uint32_t)cols;
-  int S = kMaxStages;
-  while (S > 2 && smem_plan(NN, HIST, S, a.num_acc).total > kSmemLimit) --S;
-  a.num_stages = S;
-  const int smem = smem_plan(NN, HIST, S, a.num_acc).total;
+  const LaunchPlan L = plan_for(NN, HIST);
+  a.num_acc = L.nacc;
+  a.num_ks = L.nks;
+  a.tmem_cols = (uint32_t)L.cols;
+  a.num_stages = L.stages;
   auto kfn = logits_kernel<NN, SPARSE, OUT_F16, HIST>;
-  if (!ensure_smem_attr(reinterpret_cast<const void *>(kfn), smem)) return DSA_ERR_CUDA;
-  kfn<<<grid, kThreads, smem, st>>>(tk, tq, a);
+  if (!ensure_smem_attr(reinterpret_cast<const void *>(kfn), L.smem)) return DSA_ERR_CUDA;
+  kfn<<<grid, kThreads, L.smem, st>>>(tk, tq, a);
   return check_launch();
 }
 
 }  // namespace
 
-int logits_stages_for(int next_n, bool hist) {
-  const int N = 32 * next_n;
-  const int nacc = std::min(8, 512 / N);
-  int S = kMaxStages;
-  while (S > 2 && smem_plan(next_n, hist, S, nacc).total > kSmemLimit) --S;
-  return S;
-}
+int logits_stages_for(int next_n, bool hist) { return plan_for(next_n, hist).stages; }
 
 dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   CUtensorMap tk, tq;

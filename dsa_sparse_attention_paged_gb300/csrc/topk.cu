@@ -127,14 +127,127 @@ struct SelArgs {
   int k;
   int32_t *out;
   int32_t *flags;
-  int32_t *counters;              // [R][4]
+  int32_t *counters;              // [R][4]: emitted, candidates, done CTAs, level-1 state
   unsigned long long *cand;       // [R][DSA_CAND_CAP]
+  int32_t *fine;                  // [R][kFineBins] fine histogram of an overflowing bin
   uint32_t *status;
   int64_t chunk;
 };
 
+constexpr int kFineBits = 12;
+constexpr int kFineBins = 1 << kFineBits;
+constexpr int kSelSmem = DSA_CAND_CAP * 8;  // candidates (refine) / fine histogram (pass)
+
 __device__ __forceinline__ unsigned long long cand_key(float x, int64_t t) {
   return ((unsigned long long)f32_order_key(x) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
+}
+
+// Coarse bin as a function of the FP32 order key, extended to NaN patterns so
+// it stays monotone: NaNs above +inf count as bin -1, NaNs below -inf as 1024.
+__device__ __forceinline__ int bin_of_key(uint32_t key) {
+  const uint32_t bits = (key & 0x80000000u) ? (key ^ 0x80000000u) : ~key;
+  const float x = __uint_as_float(bits);
+  if (isnan(x)) return (key & 0x80000000u) ? -1 : DSA_NUM_BINS;
+  return coarse_bin(x);
+}
+
+// Smallest order key whose bin is <= b (bins never increase with the key).
+__device__ uint32_t first_key_with_bin_le(int b) {
+  uint64_t lo = 0, hi = 0x100000000ull;  // answer in [lo, hi]
+  while (lo < hi) {
+    const uint64_t mid = (lo + hi) >> 1;
+    if (bin_of_key((uint32_t)mid) <= b) hi = mid;
+    else lo = mid + 1;
+  }
+  return (uint32_t)lo;
+}
+
+// Key range of bin T -> (first key, shift) so that (key - first) >> shift
+// spreads the bin over at most kFineBins fine bins, monotonically (see
+// fine_bin for the descending index).
+__device__ void fine_map(int T, uint32_t *klo, int *shift) {
+  const uint64_t lo = first_key_with_bin_le(T);
+  const uint64_t hi = (uint64_t)first_key_with_bin_le(T - 1) - 1;  // last key of bin T
+  const uint64_t span = hi - lo + 1;
+  int bits = 0;
+  while (bits < 33 && (1ull << bits) < span) ++bits;
+  *klo = (uint32_t)lo;
+  *shift = bits > kFineBits ? bits - kFineBits : 0;
+}
+
+// Fine bin of a key inside bin T, descending like the coarse bins: fine bin 0
+// holds the largest keys of the bin.
+__device__ __forceinline__ int fine_bin(uint32_t key, uint32_t klo, int shift) {
+  return (kFineBins - 1) - (int)((key - klo) >> shift);
+}
+
+// Exact top-m of n unique 64-bit keys held in shared memory, emitted (as the
+// column in their low 32 bits, inverted) to out[0..m).  MSB radix select that
+// skips the bits all keys share and stops once a whole bucket is taken.
+__device__ void smem_refine(const unsigned long long *sc, int n, int m, int32_t *out,
+                            int *sm_h, int *sm_misc, unsigned long long *sm_u64) {
+  if (threadIdx.x == 0) {
+    sm_u64[0] = ~0ull;
+    sm_u64[1] = 0ull;
+  }
+  __syncthreads();
+  unsigned long long a = ~0ull, o = 0ull;
+  for (int i = threadIdx.x; i < n; i += kSelThreads) {
+    a &= sc[i];
+    o |= sc[i];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    a &= __shfl_xor_sync(0xffffffffu, a, off);
+    o |= __shfl_xor_sync(0xffffffffu, o, off);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicAnd(&sm_u64[0], a);
+    atomicOr(&sm_u64[1], o);
+  }
+  __syncthreads();
+  const unsigned long long diff = sm_u64[0] ^ sm_u64[1];
+  unsigned long long prefix = 0, mask = 0;
+  int need = m;
+  if (diff != 0 && m < n) {
+    const int hb = 63 - __clzll((long long)diff);
+    mask = (hb >= 63) ? 0ull : ~((2ull << hb) - 1);
+    prefix = sm_u64[0] & mask;
+    for (int top = hb; top >= 0; top -= 8) {
+      const int shift = top >= 7 ? top - 7 : 0;
+      const int width = top - shift + 1;
+      const unsigned long long dmask = ((1ull << width) - 1) << shift;
+      for (int i = threadIdx.x; i < 256; i += kSelThreads) sm_h[i] = 0;
+      __syncthreads();
+      for (int i = threadIdx.x; i < n; i += kSelThreads) {
+        const unsigned long long v = sc[i];
+        if ((v & mask) == prefix) atomicAdd(&sm_h[(int)((v & dmask) >> shift)], 1);
+      }
+      __syncthreads();
+      if (threadIdx.x < 32) find_digit_desc(sm_h, need, &sm_misc[4], &sm_misc[5]);
+      __syncthreads();
+      const int d = sm_misc[4];
+      if (d < 0) break;  // cannot happen for consistent inputs; take what is left
+      const int hd = sm_h[d];
+      need -= sm_misc[5];
+      prefix |= (unsigned long long)d << shift;
+      mask |= dmask;
+      __syncthreads();
+      if (need == hd) break;
+    }
+  } else {
+    prefix = 0;  // m >= n: take every candidate
+  }
+  if (threadIdx.x == 0) sm_misc[6] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += kSelThreads) {
+    const unsigned long long v = sc[i];
+    if (v >= prefix) {
+      const int p = atomicAdd(&sm_misc[6], 1);
+      if (p < m) out[p] = (int32_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
+    }
+  }
+  __syncthreads();
 }
 
 // Exact top-k of one FP32 row by MSB radix select over 32-bit order keys, run
@@ -242,57 +355,116 @@ __global__ void __launch_bounds__(kSelThreads)
   }
 }
 
+// Threshold search over a histogram held in global memory: bin T with
+// cnt(bins < T) < need <= cnt(bins <= T), bins taken in increasing index
+// order (index 0 = largest scores).  Every thread calls it.  Writes
+// sm_misc[0..2] = (T, count above T, count in T); T = nb when the histogram
+// holds fewer than `need`, and (nb, -1, 0) when no bin qualifies (a corrupt
+// histogram).
+template <int NB>
+__device__ void threshold_from_hist(const int32_t *h, int need, int *sm_scan, int *sm_misc) {
+  constexpr int PER = NB / kSelThreads;
+  int c[PER];
+  int sum = 0;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    c[e] = h[threadIdx.x * PER + e];
+    sum += c[e];
+  }
+  if (threadIdx.x == 0) {
+    sm_misc[0] = NB;
+    sm_misc[1] = -1;
+    sm_misc[2] = 0;
+  }
+  int tot;
+  const int ex = block_excl_scan(sum, sm_scan, &tot);
+  if (threadIdx.x == 0 && tot < need) {
+    sm_misc[0] = NB;
+    sm_misc[1] = tot;
+    sm_misc[2] = 0;
+  }
+  if (ex < need && ex + sum >= need) {
+    int acc = ex;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      if (acc + c[e] >= need) {
+        sm_misc[0] = threadIdx.x * PER + e;
+        sm_misc[1] = acc;
+        sm_misc[2] = c[e];
+        break;
+      }
+      acc += c[e];
+    }
+  }
+  __syncthreads();
+}
+
+// One pass of the select over this CTA's chunk of the row.
+//   level 0: emit coarse bins above T; collect bin T, or -- when the
+//            histogram already says bin T holds more than the candidate
+//            capacity -- build a fine histogram of bin T instead
+//   level 1: (rows flagged by level 0 only) emit the fine bins of bin T above
+//            the fine threshold S, collect fine bin S
+// The last CTA of the row checks every count against the histograms, then
+// refines the candidates exactly, or flags level 1, or (stale histogram /
+// fine bin over capacity) runs the exact whole-row fallback.
+template <int LEVEL>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
+  extern __shared__ unsigned long long sm_dyn[];  // fine hist (pass) / candidates (refine)
   __shared__ int sm_h[256];
   __shared__ int sm_scan[kSelWarps + 1];
-  __shared__ int sm_misc[8];
+  __shared__ int sm_misc[16];
+  __shared__ unsigned long long sm_u64[2];
   __shared__ int sm_last;
   const int r = blockIdx.y;
   const int k = a.k;
   const int lane = threadIdx.x & 31;
+  int32_t *cnt = a.counters + (int64_t)r * 4;
+  if (LEVEL == 1 && *reinterpret_cast<volatile int *>(&cnt[3]) == 0) return;
   const int64_t n = row_len(a.ctx, a.next_n, a.len_div, r, a.stride, a.status);
   const float *row = a.logits + (int64_t)r * a.stride;
-  const int32_t *hr = a.hist + (int64_t)r * DSA_NUM_BINS;
   int32_t *outr = a.out + (int64_t)r * k;
-  int32_t *cnt = a.counters + (int64_t)r * 4;
   unsigned long long *cr = a.cand + (int64_t)r * DSA_CAND_CAP;
+  int32_t *finer = a.fine + (int64_t)r * kFineBins;
+  int *fine_s = reinterpret_cast<int *>(sm_dyn);
 
-  // ---- threshold bin from the histogram (every CTA of the row, redundantly)
-  {
-    const int c0 = hr[2 * threadIdx.x], c1 = hr[2 * threadIdx.x + 1];
-    if (threadIdx.x == 0) {  // sentinel: a histogram that yields no threshold is stale
-      sm_misc[0] = DSA_NUM_BINS;
-      sm_misc[1] = -1;
-      sm_misc[2] = 0;
-    }
-    int tot;
-    const int ex = block_excl_scan(c0 + c1, sm_scan, &tot);
-    if (threadIdx.x == 0 && tot < k) {
-      sm_misc[0] = DSA_NUM_BINS;  // every bin is "above": take all
-      sm_misc[1] = tot;
-      sm_misc[2] = 0;
-    }
-    if (ex < k && ex + c0 + c1 >= k) {
-      if (ex + c0 >= k) {
-        sm_misc[0] = 2 * threadIdx.x;
-        sm_misc[1] = ex;
-        sm_misc[2] = c0;
-      } else {
-        sm_misc[0] = 2 * threadIdx.x + 1;
-        sm_misc[1] = ex + c0;
-        sm_misc[2] = c1;
-      }
-    }
-    __syncthreads();
-  }
+  // ---- coarse threshold bin (every CTA, redundantly)
+  threshold_from_hist<DSA_NUM_BINS>(a.hist + (int64_t)r * DSA_NUM_BINS, k, sm_scan, sm_misc);
   const int T = sm_misc[0];
   const int above = sm_misc[1];
   const int histT = sm_misc[2];
+  __syncthreads();
+  const bool overflow0 = (T < DSA_NUM_BINS) && histT > DSA_CAND_CAP;
 
-  // ---- one pass over this CTA's chunk: emit bins above T, collect bin T
+  uint32_t klo = 0;
+  int fshift = 0, S = 0, above1 = 0, fineS = 0;
+  if (overflow0 && LEVEL == 0) {
+    for (int i = threadIdx.x; i < kFineBins; i += kSelThreads) fine_s[i] = 0;
+  }
+  if (overflow0) {
+    if (threadIdx.x == 0) {
+      fine_map(T, &klo, &fshift);
+      sm_misc[8] = (int)klo;
+      sm_misc[9] = fshift;
+    }
+    __syncthreads();
+    klo = (uint32_t)sm_misc[8];
+    fshift = sm_misc[9];
+  }
+  if (LEVEL == 1) {
+    threshold_from_hist<kFineBins>(finer, k - above, sm_scan, sm_misc + 10);
+    S = sm_misc[10];
+    above1 = sm_misc[11];
+    fineS = sm_misc[12];
+    __syncthreads();
+  }
+
+  // ---- the pass
   const int64_t c0 = blockIdx.x * a.chunk;
   const int64_t c1 = min(n, c0 + a.chunk);
   const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
+  int *cnt_e = &cnt[0];
+  int *cnt_c = &cnt[1];
   for (int64_t base = c0; base < c1; base += (int64_t)kSelThreads * 4) {
     const int64_t t0 = base + threadIdx.x * 4;
     float x[4];
@@ -303,14 +475,25 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) x[e] = (t0 + e < c1) ? row[t0 + e] : __int_as_float(0x7fffffff);
     }
-    int ne = 0, nc = 0, bins[4];
+    // kind: 1 = emit, 2 = candidate, 3 = count into the fine histogram
+    int kind[4];
+    int ne = 0, nc = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      bins[e] = coarse_bin(x[e]);
-      ne += (bins[e] >= 0 && bins[e] < T);
-      nc += (bins[e] == T);
+      const int b = coarse_bin(x[e]);
+      kind[e] = 0;
+      if (b < 0) continue;
+      if (LEVEL == 0) {
+        if (b < T) kind[e] = 1;
+        else if (b == T) kind[e] = overflow0 ? 3 : 2;
+      } else if (b == T) {
+        const int f = fine_bin(f32_order_key(x[e]), klo, fshift);
+        if (f < S) kind[e] = 1;
+        else if (f == S) kind[e] = 2;
+      }
+      ne += (kind[e] == 1);
+      nc += (kind[e] == 2 || kind[e] == 3);
     }
-    // warp-aggregated reservations: one atomic per warp and kind
     int ie = ne, ic = nc;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -324,21 +507,32 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
     const int te = __shfl_sync(0xffffffffu, ie, 31), tc = __shfl_sync(0xffffffffu, ic, 31);
     int be = 0, bc = 0;
     if (lane == 31) {
-      if (te) be = atomicAdd(&cnt[0], te);
-      if (tc) bc = atomicAdd(&cnt[1], tc);
+      if (te) be = atomicAdd(cnt_e, te);
+      if (tc) bc = atomicAdd(cnt_c, tc);
     }
     be = __shfl_sync(0xffffffffu, be, 31) + ie - ne;
     bc = __shfl_sync(0xffffffffu, bc, 31) + ic - nc;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      if (bins[e] < 0) continue;
-      if (bins[e] < T) {
+      if (kind[e] == 1) {
         if (be < k) outr[be] = (int32_t)(t0 + e);
         ++be;
-      } else if (bins[e] == T) {
+      } else if (kind[e] == 2) {
         if (bc < DSA_CAND_CAP) cr[bc] = cand_key(x[e], t0 + e);
         ++bc;
+      } else if (kind[e] == 3) {
+        atomicAdd(&fine_s[fine_bin(f32_order_key(x[e]), klo, fshift)], 1);
+        ++bc;
       }
+    }
+  }
+  if (LEVEL == 0 && overflow0) {
+    __syncthreads();
+    for (int p = threadIdx.x; p < kFineBins / 2; p += kSelThreads) {
+      const uint32_t f0 = fine_s[2 * p], f1 = fine_s[2 * p + 1];
+      if (f0 | f1)
+        atomicAdd(reinterpret_cast<unsigned long long *>(finer + 2 * p),
+                  ((unsigned long long)f1 << 32) | f0);
     }
   }
 
@@ -354,63 +548,62 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
   __threadfence();
   const int emitted = *reinterpret_cast<volatile int *>(&cnt[0]);
   const int ncand = *reinterpret_cast<volatile int *>(&cnt[1]);
-  const bool sane = (T < DSA_NUM_BINS) ? (above >= 0 && above < k && histT >= k - above)
+  const bool sane0 = (T < DSA_NUM_BINS) ? (above >= 0 && above < k && histT >= k - above)
                                         : (above >= 0 && above < k);
-  const bool stale = !sane || (emitted != above) || (T < DSA_NUM_BINS && ncand != histT);
-  const bool over = !stale && T < DSA_NUM_BINS && ncand > DSA_CAND_CAP;
-  if (!stale && !over) {
-    if (T >= DSA_NUM_BINS) {
-      for (int i = emitted + threadIdx.x; i < k; i += kSelThreads) outr[i] = -1;
+  int flag = 0;           // 0 histogram path, 1 stale, 2 over capacity
+  bool done = true;       // false: level 1 continues this row
+  int base_out = 0, m = 0;
+  if (LEVEL == 0) {
+    const bool stale = !sane0 || emitted != above || (T < DSA_NUM_BINS && ncand != histT);
+    if (stale) {
+      flag = 1;
+    } else if (overflow0) {
+      done = false;       // fine histogram complete: level 1 collects bin S
     } else {
-      // exact top-m of the candidates (64-bit keys are unique per row)
-      const int m = k - above;
-      unsigned long long prefix = 0, mask = 0;
-      int need = m;
-      for (int shift = 56; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += kSelThreads) sm_h[i] = 0;
-        __syncthreads();
-        for (int i = threadIdx.x; i < ncand; i += kSelThreads) {
-          const unsigned long long v = cr[i];
-          if ((v & mask) == prefix) atomicAdd(&sm_h[(int)((v >> shift) & 255)], 1);
-        }
-        __syncthreads();
-        if (threadIdx.x < 32) find_digit_desc(sm_h, need, &sm_misc[4], &sm_misc[5]);
-        __syncthreads();
-        const int d = sm_misc[4];
-        if (d < 0) {  // fewer candidates than needed: take them all
-          prefix = 0;
-          break;
-        }
-        const int hd = sm_h[d];
-        need -= sm_misc[5];
-        prefix |= (unsigned long long)d << shift;
-        mask |= 0xFFull << shift;
-        __syncthreads();
-        if (need == hd) break;
-      }
-      if (threadIdx.x == 0) sm_misc[6] = 0;
-      __syncthreads();
-      for (int i = threadIdx.x; i < ncand; i += kSelThreads) {
-        const unsigned long long v = cr[i];
-        if (v >= prefix) {
-          const int p = atomicAdd(&sm_misc[6], 1);
-          if (p < m) outr[above + p] = (int32_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
-        }
-      }
+      base_out = above;
+      m = (T < DSA_NUM_BINS) ? k - above : 0;
     }
-    if (a.flags && threadIdx.x == 0) a.flags[r] = 0;
   } else {
-    if (a.flags && threadIdx.x == 0) a.flags[r] = stale ? 1 : 2;
+    const bool sane1 = S < kFineBins && above1 >= 0 && above1 < k - above;
+    const bool stale = !sane1 || emitted != above + above1 || ncand != fineS;
+    if (stale) flag = 1;
+    else if (ncand > DSA_CAND_CAP) flag = 2;
+    else {
+      base_out = above + above1;
+      m = k - base_out;
+    }
+  }
+  if (!done) {
+    if (threadIdx.x == 0) {
+      cnt[1] = 0;
+      cnt[2] = 0;
+      cnt[3] = 1;
+    }
+    return;
+  }
+  if (flag == 0) {
+    if (m > 0) {
+      for (int i = threadIdx.x; i < ncand; i += kSelThreads) sm_dyn[i] = cr[i];
+      __syncthreads();
+      smem_refine(sm_dyn, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
+    } else {
+      for (int i = emitted + threadIdx.x; i < k; i += kSelThreads) outr[i] = -1;
+    }
+  } else {
     __syncthreads();
     block_radix_topk_row(row, n, k, outr, sm_h, sm_scan, sm_misc);
   }
-  // leave the row's counters (and, when asked, its histogram) at zero
+  if (a.flags && threadIdx.x == 0) a.flags[r] = flag;
+  // leave the row's counters, fine histogram and (when asked) histogram at zero
   __syncthreads();
   if (threadIdx.x == 0) {
     cnt[0] = 0;
     cnt[1] = 0;
     cnt[2] = 0;
+    cnt[3] = 0;
   }
+  if (LEVEL == 1 || overflow0)
+    for (int i = threadIdx.x; i < kFineBins; i += kSelThreads) finer[i] = 0;
   if (a.reset_hist) {
     int32_t *hw = a.hist + (int64_t)r * DSA_NUM_BINS;
     for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kSelThreads) hw[i] = 0;
@@ -557,6 +750,7 @@ dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
   int32_t *counters = reinterpret_cast<int32_t *>(ws + WsLayout::counters_off());
   unsigned long long *cand = reinterpret_cast<unsigned long long *>(ws + WsLayout::cand_off(c.ws_rows));
   int32_t *ws_hist = reinterpret_cast<int32_t *>(ws + WsLayout::hist_off(c.ws_rows));
+  int32_t *fine = reinterpret_cast<int32_t *>(ws + WsLayout::fine_off(c.ws_rows));
   const int sms = num_sms();
   if (sms <= 0) return DSA_ERR_CUDA;
   const int64_t total = c.stride * (int64_t)c.R;
@@ -588,9 +782,17 @@ dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
   a.flags = c.fallback_flags;
   a.counters = counters;
   a.cand = cand;
+  a.fine = fine;
   a.status = status;
   a.chunk = chunk;
-  select_kernel<<<dim3((unsigned)nchunks, (unsigned)c.R), kSelThreads, 0, st>>>(a);
+  if (!ensure_smem_attr(reinterpret_cast<const void *>(select_kernel<0>), kSelSmem) ||
+      !ensure_smem_attr(reinterpret_cast<const void *>(select_kernel<1>), kSelSmem))
+    return DSA_ERR_CUDA;
+  const dim3 grid((unsigned)nchunks, (unsigned)c.R);
+  select_kernel<0><<<grid, kSelThreads, kSelSmem, st>>>(a);
+  dsa_status_t e = check_launch();
+  if (e != DSA_OK) return e;
+  select_kernel<1><<<grid, kSelThreads, kSelSmem, st>>>(a);
   return check_launch();
 }
 

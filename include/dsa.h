@@ -88,9 +88,11 @@ int32_t dsa_version(void);
 /* ---- workspace ----------------------------------------------------------
  * One caller-owned device buffer serves every entry point.  It holds the
  * device status word, per-row select counters, the threshold-bin candidate
- * buffer (DSA_CAND_CAP entries per row) and a histogram for selects that are
- * not given one.  `max_rows` is the largest row count any call will use.
- * The buffer must be zero-filled once before first use (dsa_workspace_init);
+ * buffer (DSA_CAND_CAP entries per row), a histogram for selects that are not
+ * given one, and a 4096-bin fine histogram per row for a threshold bin that
+ * holds more than DSA_CAND_CAP scores (about 86 KiB per row in all).
+ * `max_rows` is the largest row count any call will use.  The buffer must be
+ * zero-filled once before first use (dsa_workspace_init);
  * every completed call leaves its counters at zero again, so no per-call
  * clearing is needed.  Calls that share a workspace must be ordered on one
  * stream (or otherwise serialised): concurrent calls on one workspace race. */
@@ -137,9 +139,11 @@ int32_t dsa_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const fl
  * find the threshold bin T from the coarse histogram (the bins above T hold
  * fewer than k scores, T completes k), emit every score in a bin above T,
  * collect the scores of bin T (at most DSA_CAND_CAP) and refine them exactly.
- * A histogram that does not match the row (stale) or a bin T with more than
- * DSA_CAND_CAP scores falls back to an exact whole-row radix select instead of
- * raising a device error.
+ * When the histogram shows bin T holding more than DSA_CAND_CAP scores, the
+ * pass builds a 4096-bin fine histogram of bin T instead and a second pass
+ * collects inside its threshold fine bin.  A histogram that does not match
+ * the row (stale), or a fine bin still over capacity, falls back to an exact
+ * whole-row radix select instead of raising a device error.
  *
  * Rows: r in [0, R); row r has n_r = ceil_div(context_lens[r / next_n] -
  * (next_n - 1 - r % next_n), len_div) live scores (len_div = 1 for logits
@@ -153,8 +157,9 @@ int32_t dsa_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const fl
  *                to the lower column, NaN never selected; order within a row
  *                is unspecified; rows with fewer than k live non-NaN scores
  *                are padded with -1
- *   fallback_flags NULL or [R] int32: 0 = histogram path, 1 = stale
- *                histogram, 2 = threshold bin over capacity
+ *   fallback_flags NULL or [R] int32: 0 = histogram path (with or without
+ *                the fine pass), 1 = stale histogram, 2 = threshold bin over
+ *                capacity even after the fine pass
  * k <= DSA_MAX_TOPK. */
 int32_t dsa_coarse_hist_topk(const float *logits, int64_t stride, const int32_t *context_lens,
                              int32_t next_n, int32_t len_div, int32_t R, int32_t *histogram,

@@ -38,8 +38,8 @@ def test_status_strings_and_sizes(lib):
     assert lib.dsa_version() >= 10000
     s1, s32 = lib.dsa_workspace_size(1), lib.dsa_workspace_size(32)
     assert s32 > s1 > 0 and s32 % 256 == 0
-    # per row: 16 B counters + 8192 x 8 B candidates + 4 KiB histogram
-    assert s32 - s1 >= 31 * (16 + 8192 * 8 + 4096) - 512
+    # per row: 16 B counters + 8192 x 8 B candidates + 4 KiB histogram + 16 KiB fine histogram
+    assert s32 - s1 >= 31 * (16 + 8192 * 8 + 4096 + 16384) - 1024
 
 
 A16 = ctypes.c_void_p(0x10000)     # aligned, never dereferenced: checks fail first

@@ -103,6 +103,31 @@ def test_threshold_bin_over_capacity_falls_back_to_exact():
     assert (flags.cpu().numpy() == 2).all()
 
 
+@pytest.mark.parametrize("lo,hi", [(223.0, 1000.0), (17.0, 17.9), (0.5, 0.53)])
+def test_overflowing_bin_resolved_by_fine_histogram(lo, hi):
+    """30000 distinct scores inside one coarse bin (the saturating bin, a unit
+    bin, an FP16 bin): the histogram predicts the overflow, the fine pass
+    resolves it exactly, no fallback."""
+    import dsa_sparse_attention_paged_gb300 as D
+    R, n = 3, 40000
+    rng = np.random.default_rng(11)
+    x = rng.normal(0, 1, (R, n)).astype(np.float32)
+    x[:, 1000:31000] = rng.uniform(lo, hi, (R, 30000)).astype(np.float32)
+    x[2, 5000:5100] = np.float32(lo)  # some exact ties as well
+    L = torch.from_numpy(x).cuda()
+    ctx = torch.full((R,), n, dtype=torch.int32, device="cuda")
+    hist = torch.from_numpy(O.histogram(x, np.full(R, n))).cuda()
+    ws = D.Workspace(R)
+    flags = torch.full((R,), 9, dtype=torch.int32, device="cuda")
+    for rep in range(2):
+        out = D.coarse_hist_topk(L, ctx, 1, 2048, ws, histogram=hist, fallback_flags=flags)
+        torch.cuda.synchronize()
+        ref = O.topk(x, np.full(R, n), 2048)
+        assert sets_equal(out.cpu().numpy(), ref), rep
+        assert (flags.cpu().numpy() == 0).all(), flags
+    assert ws.status() == 0
+
+
 def test_nan_inf_and_short_rows():
     import dsa_sparse_attention_paged_gb300 as D
     R, n = 3, 5000
