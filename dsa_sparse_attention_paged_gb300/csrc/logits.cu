@@ -99,7 +99,7 @@ __host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, int stages, int
 }
 
 __device__ __forceinline__ int64_t eff_ctx(const LogitsArgs &a, int b) {
-  int64_t c = a.context_lens[b];
+  int64_t c = __ldg(&a.context_lens[b]);
   const int64_t cap = a.pt_stride * a.page_size;
   if (c < 0) c = 0;
   if (c > cap) c = cap;
@@ -320,61 +320,77 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // The page-table (and block-table) reads for a group of tiles are issued
+    // one group ahead, one entry per lane, so no tile waits on a dependent
+    // global load: ppt load slots per tile (2 or 1 pages, or 16 blocks),
+    // tpg = 32 / ppt tiles per group.
     const uint64_t pol = policy_evict_first();
+    const int ppt = SPARSE ? 16 : (kTileTok / a.page_size);
+    const int tpg = 32 / ppt;
+    const int my_o = lane / ppt, my_sl = lane % ppt;
+    constexpr int kNone = INT32_MIN;
     TileIter<SPARSE> it;
     it.init(a, u_start, i_start);
+    TileIter<SPARSE> git = it;  // first tile of the group being prefetched
+    long long gn = 0;
+    // raw table entry of this lane's slot in the group starting at (g0, n0)
+    auto fetch = [&](TileIter<SPARSE> g0, long long n0, int &unit) -> int {
+      unit = -1;
+      if (n0 + my_o >= count) return kNone;
+      for (int k = 0; k < my_o; ++k) g0.next(a);
+      unit = g0.u;
+      if (SPARSE) return __ldg(&a.block_table[(int64_t)g0.u * a.kb + (int64_t)g0.i * 16 + my_sl]);
+      const int64_t p = (int64_t)g0.i * ppt + my_sl;
+      if (p * a.page_size >= eff_ctx(a, g0.u)) return kNone;
+      return __ldg(&a.page_table[(int64_t)g0.u * a.pt_stride + p]);
+    };
+    // physical row of this lane's slot (or -1 when nothing is loaded)
+    auto to_row = [&](int raw, int unit) -> int {
+      if (raw == kNone || unit < 0) return -1;
+      if (SPARSE) {
+        const int b = unit / a.req_next_n;
+        const int j = unit % a.req_next_n;
+        const int64_t n_live = eff_ctx(a, b) - (a.req_next_n - 1 - j);
+        if (raw == INT32_MAX || raw < 0 || (int64_t)raw * 8 >= n_live) return -1;
+        const int64_t tok = (int64_t)raw * 8;
+        int32_t pg = __ldg(&a.page_table[(int64_t)b * a.pt_stride + tok / a.page_size]);
+        if (pg < 0 || pg >= a.num_pages) {
+          set_status(a.status, DSA_DEV_BOUNDS);
+          pg = 0;
+        }
+        return pg * a.page_size + (int)(tok % a.page_size);
+      }
+      int32_t pg = raw;
+      if (pg < 0 || pg >= a.num_pages) {
+        set_status(a.status, DSA_DEV_BOUNDS);
+        pg = 0;
+      }
+      return pg * a.page_size;
+    };
+    int nxt_unit;
+    int nxt = fetch(git, gn, nxt_unit);
+    int cur_row = -1;
     int prev_u = -1, unit_ord = -1;
     long long issued = 0;
     int q_issued = 0;
     bool ok = true;
     for (long long n = 0; n < count && ok; ++n, it.next(a)) {
-      const int u = it.u, i = it.i;
-      int b, qrow0;
-      int64_t n_live;  // dense: tokens of the request; sparse: live keys of the row
-      if (SPARSE) {
-        b = u / a.req_next_n;
-        const int j = u % a.req_next_n;
-        n_live = eff_ctx(a, b) - (a.req_next_n - 1 - j);
-        qrow0 = u * 32;
-      } else {
-        b = u;
-        n_live = eff_ctx(a, b);
-        qrow0 = u * N;
+      const int u = it.u;
+      const int o = (int)(n % tpg);
+      if (o == 0) {
+        cur_row = to_row(nxt, nxt_unit);
+        for (int k = 0; k < tpg; ++k) git.next(a);
+        gn += tpg;
+        nxt = fetch(git, gn, nxt_unit);
       }
-      // physical rows of this tile, read before waiting for a free stage
-      int row = -1;
-      if (SPARSE) {
-        if (lane < 16) {
-          const int32_t id = a.block_table[(int64_t)u * a.kb + (int64_t)i * 16 + lane];
-          if (id != INT32_MAX && id >= 0 && (int64_t)id * 8 < n_live) {
-            const int64_t tok = (int64_t)id * 8;
-            int32_t pg = a.page_table[(int64_t)b * a.pt_stride + tok / a.page_size];
-            if (pg < 0 || pg >= a.num_pages) {
-              set_status(a.status, DSA_DEV_BOUNDS);
-              pg = 0;
-            }
-            row = pg * a.page_size + (int)(tok % a.page_size);
-          }
-        }
-      } else {
-        const int ppt = kTileTok / a.page_size;  // pages per tile: 2 or 1
-        if (lane < ppt) {
-          const int64_t p = (int64_t)i * ppt + lane;
-          if (p * a.page_size < n_live) {
-            int32_t pg = a.page_table[(int64_t)b * a.pt_stride + p];
-            if (pg < 0 || pg >= a.num_pages) {
-              set_status(a.status, DSA_DEV_BOUNDS);
-              pg = 0;
-            }
-            row = pg * a.page_size;
-          }
-        }
-      }
+      int row = __shfl_sync(0xffffffffu, cur_row, (o * ppt + my_sl) & 31);
+      if (lane >= ppt) row = -1;
       if (u != prev_u) {
         ++unit_ord;
         prev_u = u;
         const int qb = unit_ord & 1;
         const uint32_t qph = (unit_ord >> 1) & 1;
+        const int qrow0 = SPARSE ? u * 32 : u * N;
         if (lane == 0) {
           ok = mbar_wait(QEMPTY(qb), qph ^ 1, ctl);
           if (ok) {

@@ -136,7 +136,10 @@ struct SelArgs {
 
 constexpr int kFineBits = 12;
 constexpr int kFineBins = 1 << kFineBits;
-constexpr int kSelSmem = DSA_CAND_CAP * 8;  // candidates (refine) / fine histogram (pass)
+constexpr int kSelSmem = kFineBins * 4;      // fine histogram (pass) / candidates (refine)
+constexpr int kSmemCand = kSelSmem / 8;      // candidates refined from shared memory
+constexpr int kPerThread = 16;               // elements per thread per pass iteration
+constexpr int kIter = kSelThreads * kPerThread;
 
 __device__ __forceinline__ unsigned long long cand_key(float x, int64_t t) {
   return ((unsigned long long)f32_order_key(x) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
@@ -151,28 +154,48 @@ __device__ __forceinline__ int bin_of_key(uint32_t key) {
   return coarse_bin(x);
 }
 
-// Smallest order key whose bin is <= b (bins never increase with the key).
-__device__ uint32_t first_key_with_bin_le(int b) {
-  uint64_t lo = 0, hi = 0x100000000ull;  // answer in [lo, hi]
-  while (lo < hi) {
-    const uint64_t mid = (lo + hi) >> 1;
-    if (bin_of_key((uint32_t)mid) <= b) hi = mid;
-    else lo = mid + 1;
+// Smallest order key whose bin is <= b (bins never increase with the key),
+// found by one warp with a 32-way search (about seven rounds).  Key 2^32
+// stands for "past the last key" and counts as satisfying the predicate.
+__device__ uint64_t first_key_with_bin_le(int b) {
+  const int lane = threadIdx.x & 31;
+  uint64_t lo = 0, hi = 1ull << 32;  // answer in [lo, hi]; hi satisfies the predicate
+  while (hi > lo) {
+    const uint64_t span = hi - lo;
+    uint64_t probe;
+    if (span <= 32) {
+      probe = lo + (uint64_t)lane;  // probe every key of [lo, hi)
+      if (probe > hi) probe = hi;
+    } else {
+      const uint64_t step = span / 32;
+      probe = (lane == 31) ? hi : lo + (uint64_t)(lane + 1) * step;
+    }
+    const bool t = (probe >= (1ull << 32)) || bin_of_key((uint32_t)probe) <= b;
+    const unsigned m = __ballot_sync(0xffffffffu, t);
+    const int f = __ffs(m) - 1;  // lane 31 (or the last probe) is always true
+    const uint64_t pf = __shfl_sync(0xffffffffu, probe, f);
+    if (span <= 32) return pf;
+    const uint64_t pprev = __shfl_sync(0xffffffffu, probe, f > 0 ? f - 1 : 0);
+    lo = (f == 0) ? lo : pprev + 1;
+    hi = pf;
   }
-  return (uint32_t)lo;
+  return lo;
 }
 
 // Key range of bin T -> (first key, shift) so that (key - first) >> shift
 // spreads the bin over at most kFineBins fine bins, monotonically (see
 // fine_bin for the descending index).
+// Called by one full warp.
 __device__ void fine_map(int T, uint32_t *klo, int *shift) {
   const uint64_t lo = first_key_with_bin_le(T);
-  const uint64_t hi = (uint64_t)first_key_with_bin_le(T - 1) - 1;  // last key of bin T
+  const uint64_t hi = first_key_with_bin_le(T - 1) - 1;  // last key of bin T
   const uint64_t span = hi - lo + 1;
   int bits = 0;
   while (bits < 33 && (1ull << bits) < span) ++bits;
-  *klo = (uint32_t)lo;
-  *shift = bits > kFineBits ? bits - kFineBits : 0;
+  if ((threadIdx.x & 31) == 0) {
+    *klo = (uint32_t)lo;
+    *shift = bits > kFineBits ? bits - kFineBits : 0;
+  }
 }
 
 // Fine bin of a key inside bin T, descending like the coarse bins: fine bin 0
@@ -428,6 +451,27 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
   int32_t *finer = a.fine + (int64_t)r * kFineBins;
   int *fine_s = reinterpret_cast<int *>(sm_dyn);
 
+  // ---- issue this CTA's first loads, then read the histogram while they fly
+  const int64_t c0 = blockIdx.x * a.chunk;
+  const int64_t c1 = min(n, c0 + a.chunk);
+  const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
+  float x[kPerThread];
+  auto load = [&](int64_t base) {
+#pragma unroll
+    for (int q = 0; q < kPerThread / 4; ++q) {
+      const int64_t t0 = base + (int64_t)q * kSelThreads * 4 + threadIdx.x * 4;
+      if (vec && t0 + 3 < c1) {
+        const float4 v = *reinterpret_cast<const float4 *>(row + t0);
+        x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          x[4 * q + e] = (t0 + e < c1) ? row[t0 + e] : __int_as_float(0x7fffffff);
+      }
+    }
+  };
+  if (c0 < c1) load(c0);
+
   // ---- coarse threshold bin (every CTA, redundantly)
   threshold_from_hist<DSA_NUM_BINS>(a.hist + (int64_t)r * DSA_NUM_BINS, k, sm_scan, sm_misc);
   const int T = sm_misc[0];
@@ -442,10 +486,14 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
     for (int i = threadIdx.x; i < kFineBins; i += kSelThreads) fine_s[i] = 0;
   }
   if (overflow0) {
-    if (threadIdx.x == 0) {
-      fine_map(T, &klo, &fshift);
-      sm_misc[8] = (int)klo;
-      sm_misc[9] = fshift;
+    if (threadIdx.x < 32) {
+      uint32_t kl;
+      int sh;
+      fine_map(T, &kl, &sh);
+      if (threadIdx.x == 0) {
+        sm_misc[8] = (int)kl;
+        sm_misc[9] = sh;
+      }
     }
     __syncthreads();
     klo = (uint32_t)sm_misc[8];
@@ -460,40 +508,33 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
   }
 
   // ---- the pass
-  const int64_t c0 = blockIdx.x * a.chunk;
-  const int64_t c1 = min(n, c0 + a.chunk);
-  const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
   int *cnt_e = &cnt[0];
   int *cnt_c = &cnt[1];
-  for (int64_t base = c0; base < c1; base += (int64_t)kSelThreads * 4) {
-    const int64_t t0 = base + threadIdx.x * 4;
-    float x[4];
-    if (vec && t0 + 3 < c1) {
-      const float4 v = *reinterpret_cast<const float4 *>(row + t0);
-      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) x[e] = (t0 + e < c1) ? row[t0 + e] : __int_as_float(0x7fffffff);
-    }
+  for (int64_t base = c0; base < c1; base += kIter) {
+    if (base != c0) load(base);
     // kind: 1 = emit, 2 = candidate, 3 = count into the fine histogram
-    int kind[4];
+    uint32_t kinds = 0;
     int ne = 0, nc = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < kPerThread; ++e) {
       const int b = coarse_bin(x[e]);
-      kind[e] = 0;
-      if (b < 0) continue;
-      if (LEVEL == 0) {
-        if (b < T) kind[e] = 1;
-        else if (b == T) kind[e] = overflow0 ? 3 : 2;
-      } else if (b == T) {
-        const int f = fine_bin(f32_order_key(x[e]), klo, fshift);
-        if (f < S) kind[e] = 1;
-        else if (f == S) kind[e] = 2;
+      uint32_t kd = 0;
+      if (b >= 0) {
+        if (LEVEL == 0) {
+          if (b < T) kd = 1;
+          else if (b == T) kd = overflow0 ? 3 : 2;
+        } else if (b == T) {
+          const int f = fine_bin(f32_order_key(x[e]), klo, fshift);
+          if (f < S) kd = 1;
+          else if (f == S) kd = 2;
+        }
       }
-      ne += (kind[e] == 1);
-      nc += (kind[e] == 2 || kind[e] == 3);
+      kinds |= kd << (2 * e);
+      ne += (kd == 1);
+      nc += (kd >= 2);
     }
+    const unsigned any = __ballot_sync(0xffffffffu, (ne | nc) != 0);
+    if (any == 0) continue;  // warp-uniform: nothing to emit or collect here
     int ie = ne, ic = nc;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -513,14 +554,17 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
     be = __shfl_sync(0xffffffffu, be, 31) + ie - ne;
     bc = __shfl_sync(0xffffffffu, bc, 31) + ic - nc;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (kind[e] == 1) {
-        if (be < k) outr[be] = (int32_t)(t0 + e);
+    for (int e = 0; e < kPerThread; ++e) {
+      const uint32_t kd = (kinds >> (2 * e)) & 3u;
+      if (!kd) continue;
+      const int64_t t = base + (int64_t)(e >> 2) * kSelThreads * 4 + threadIdx.x * 4 + (e & 3);
+      if (kd == 1) {
+        if (be < k) outr[be] = (int32_t)t;
         ++be;
-      } else if (kind[e] == 2) {
-        if (bc < DSA_CAND_CAP) cr[bc] = cand_key(x[e], t0 + e);
+      } else if (kd == 2) {
+        if (bc < DSA_CAND_CAP) cr[bc] = cand_key(x[e], t);
         ++bc;
-      } else if (kind[e] == 3) {
+      } else {
         atomicAdd(&fine_s[fine_bin(f32_order_key(x[e]), klo, fshift)], 1);
         ++bc;
       }
@@ -583,9 +627,15 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
   }
   if (flag == 0) {
     if (m > 0) {
-      for (int i = threadIdx.x; i < ncand; i += kSelThreads) sm_dyn[i] = cr[i];
-      __syncthreads();
-      smem_refine(sm_dyn, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
+      // small candidate sets are refined from shared memory, larger ones
+      // straight from the (L2-resident) workspace buffer
+      const unsigned long long *src = cr;
+      if (ncand <= kSmemCand) {
+        for (int i = threadIdx.x; i < ncand; i += kSelThreads) sm_dyn[i] = cr[i];
+        __syncthreads();
+        src = sm_dyn;
+      }
+      smem_refine(src, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
     } else {
       for (int i = emitted + threadIdx.x; i < k; i += kSelThreads) outr[i] = -1;
     }
@@ -753,9 +803,10 @@ dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
   int32_t *fine = reinterpret_cast<int32_t *>(ws + WsLayout::fine_off(c.ws_rows));
   const int sms = num_sms();
   if (sms <= 0) return DSA_ERR_CUDA;
-  const int64_t total = c.stride * (int64_t)c.R;
-  int64_t chunk = (total + 2LL * sms - 1) / (2LL * sms);
-  chunk = std::max<int64_t>(2048, (chunk + 2047) / 2048 * 2048);
+  // one pass iteration (8192 scores) per CTA; longer chunks only when the
+  // grid would exceed the launch limit
+  int64_t chunk = kIter;
+  while ((c.stride + chunk - 1) / chunk > 65535) chunk *= 2;
   const int64_t nchunks = std::max<int64_t>(1, (c.stride + chunk - 1) / chunk);
   if (nchunks > 65535 || c.R > 65535) return DSA_ERR_UNSUPPORTED;
   int32_t *hist = c.histogram;
