@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/dsa.h"
+#include "dsa.h"  // include/ is on the include path
 
 namespace dsa {
 

@@ -52,6 +52,7 @@ struct LogitsArgs {
   int32_t B;
   int32_t req_next_n;   // rows per request
   int32_t page_size;
+  int32_t log2_ps;      // page_size is 64 or 128
   int32_t num_pages;
   int32_t num_units;    // dense: requests; sparse: rows
   int32_t sparse_tpu;   // sparse: tiles per row (kb / 16)
@@ -140,6 +141,34 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
   }
   return v;
 }
+
+// Position in a ring of `size` slots with the mbarrier phase bit of the
+// current lap: advanced by one per tile (no division in the loops).
+struct Ring {
+  int idx;
+  uint32_t ph;
+  int size;
+  __device__ __forceinline__ void init(int n) {
+    idx = 0;
+    ph = 0;
+    size = n;
+  }
+  __device__ __forceinline__ void next() {
+    if (++idx == size) {
+      idx = 0;
+      ph ^= 1;
+    }
+  }
+  // slot and phase of the tile `back` positions before the current one (back <= size)
+  __device__ __forceinline__ void prev(int back, int &i, uint32_t &p) const {
+    i = idx - back;
+    p = ph;
+    if (i < 0) {
+      i += size;
+      p ^= 1;
+    }
+  }
+};
 
 // One warp: this CTA's contiguous range [g0, g1) of the flattened tile
 // sequence, as (first unit, first tile in it, tile count).
@@ -278,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(EMPTY(s), 1);
     }
     for (int k = 0; k < KS; ++k) {
-      mbar_init(KSF(k), 1);
+      mbar_init(KSF(k), 32);  // one cp.async completion arrival per producer lane
       mbar_init(KSE(k), 4);
     }
     for (int q = 0; q < 2; ++q) {
@@ -353,12 +382,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t n_live = eff_ctx(a, b) - (a.req_next_n - 1 - j);
         if (raw == INT32_MAX || raw < 0 || (int64_t)raw * 8 >= n_live) return -1;
         const int64_t tok = (int64_t)raw * 8;
-        int32_t pg = __ldg(&a.page_table[(int64_t)b * a.pt_stride + tok / a.page_size]);
+        int32_t pg = __ldg(&a.page_table[(int64_t)b * a.pt_stride + (tok >> a.log2_ps)]);
         if (pg < 0 || pg >= a.num_pages) {
           set_status(a.status, DSA_DEV_BOUNDS);
           pg = 0;
         }
-        return pg * a.page_size + (int)(tok % a.page_size);
+        return pg * a.page_size + (int)(tok & (a.page_size - 1));
       }
       int32_t pg = raw;
       if (pg < 0 || pg >= a.num_pages) {
@@ -374,9 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long issued = 0;
     int q_issued = 0;
     bool ok = true;
-    for (long long n = 0; n < count && ok; ++n, it.next(a)) {
+    Ring rs, rk;
+    rs.init(S);
+    rk.init(KS);
+    int o = 0;
+    for (long long n = 0; n < count && ok; ++n, it.next(a), rs.next(), rk.next(),
+                   o = (o + 1 == tpg) ? 0 : o + 1) {
       const int u = it.u;
-      const int o = (int)(n % tpg);
       if (o == 0) {
         cur_row = to_row(nxt, nxt_unit);
         for (int k = 0; k < tpg; ++k) git.next(a);
@@ -403,36 +436,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
       }
-      const int s = (int)(n % S);
-      const int kx = (int)(n % KS);
+      const int s = rs.idx;
+      const int kx = rk.idx;
       if (lane == 0) {
-        ok = mbar_wait(EMPTY(s), (uint32_t)(((n / S) & 1) ^ 1), ctl) &&
-             mbar_wait(KSE(kx), (uint32_t)(((n / KS) & 1) ^ 1), ctl);
+        ok = mbar_wait(EMPTY(s), rs.ph ^ 1, ctl) && mbar_wait(KSE(kx), rk.ph ^ 1, ctl);
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       const unsigned loads = __ballot_sync(0xffffffffu, row >= 0);
       const int blk_rows = SPARSE ? 8 : a.page_size;
       const uint32_t nload = (uint32_t)__popc(loads);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(FULL(s), nload * (uint32_t)(blk_rows * 128));
-        mbar_arrive_expect_tx(KSF(kx), nload * (uint32_t)(blk_rows * 4));
-      }
+      if (lane == 0) mbar_arrive_expect_tx(FULL(s), nload * (uint32_t)(blk_rows * 128));
       __syncwarp();
-      if (row >= 0) {
+      if (row >= 0)
         tma_load_2d_hint(kst + s * kStageK + lane * blk_rows * 128, &tm_k, FULL(s), 0, row, pol);
-        bulk_load(smem_u32(ks_s + kx * kTileTok + lane * blk_rows), a.kscale + (int64_t)row,
-                  blk_rows * 4, KSF(kx));
+      // kscale of the tile (128 floats = 512 bytes): 16 bytes per lane by
+      // cp.async; lane l covers tokens 4l .. 4l+3 of the tile
+      {
+        const int tk = lane * 4;                      // first token of this lane
+        const int src_lane = tk / blk_rows;           // load slot holding those tokens
+        const int srow = __shfl_sync(0xffffffffu, row, src_lane);
+        const bool have = srow >= 0;
+        const float *src = a.kscale + (have ? (int64_t)srow + (tk % blk_rows) : 0);
+        cp_async16(smem_u32(ks_s + kx * kTileTok + tk), src, have ? 16u : 0u);
+        cp_async_arrive_noinc(KSF(kx));
       }
       ++issued;
     }
     if (!ok && lane == 0) {
       // drain our own copies still in flight before the CTA exits
       const long long lim = a.wait_limit;
-      for (long long n = (issued > S ? issued - S : 0); n < issued; ++n)
-        mbar_wait_drain(FULL((int)(n % S)), (uint32_t)((n / S) & 1), lim);
-      for (long long n = (issued > KS ? issued - KS : 0); n < issued; ++n)
-        mbar_wait_drain(KSF((int)(n % KS)), (uint32_t)((n / KS) & 1), lim);
+      // the break left the rings one past the last issued tile only when
+      // the tile's copies were issued; count back from the issued total
+      Ring ds = rs, dk = rk;
+      ds.idx = (int)(issued % S);
+      ds.ph = (uint32_t)((issued / S) & 1);
+      dk.idx = (int)(issued % KS);
+      dk.ph = (uint32_t)((issued / KS) & 1);
+      for (int back = 1; back <= S && back <= issued; ++back) {
+        int i2;
+        uint32_t p2;
+        ds.prev(back, i2, p2);
+        mbar_wait_drain(FULL(i2), p2, lim);
+      }
+      for (int back = 1; back <= KS && back <= issued; ++back) {
+        int i2;
+        uint32_t p2;
+        dk.prev(back, i2, p2);
+        mbar_wait_drain(KSF(i2), p2, lim);
+      }
       for (int k2 = (q_issued > 2 ? q_issued - 2 : 0); k2 < q_issued; ++k2)
         mbar_wait_drain(QFULL(k2 & 1), (uint32_t)((k2 >> 1) & 1), lim);
     }
@@ -444,17 +496,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       int prev_u = -1, unit_ord = -1, qb = 0;
       bool ok = true;
       long long mmas = 0;
-      for (long long n = 0; n < count; ++n, it.next(a)) {
+      Ring rs, ra;
+      rs.init(S);
+      ra.init(A);
+      for (long long n = 0; n < count; ++n, it.next(a), rs.next(), ra.next()) {
         if (it.u != prev_u) {
           ++unit_ord;
           prev_u = it.u;
           qb = unit_ord & 1;
           if (!(ok = mbar_wait(QFULL(qb), (unit_ord >> 1) & 1, ctl))) break;
         }
-        const int s = (int)(n % S);
-        const int x = (int)(n % A);
-        if (!(ok = mbar_wait(AEMPTY(x), (uint32_t)(((n / A) & 1) ^ 1), ctl))) break;
-        if (!(ok = mbar_wait(FULL(s), (uint32_t)((n / S) & 1), ctl))) break;
+        const int s = rs.idx;
+        const int x = ra.idx;
+        if (!(ok = mbar_wait(AEMPTY(x), ra.ph ^ 1, ctl))) break;
+        if (!(ok = mbar_wait(FULL(s), rs.ph, ctl))) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(x * N);
         const uint64_t ad = sdesc_sw128(kst + s * kStageK);
@@ -528,7 +583,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       return group_sync();
     };
 
-    for (long long n = 0; n < count; ++n, it.next(a)) {
+    Ring ra, rk;
+    ra.init(A);
+    rk.init(KS);
+    int par = 0;  // parity of n: which group owns the tile
+    for (long long n = 0; n < count; ++n, it.next(a), ra.next(), rk.next(), par ^= 1) {
       const int u = it.u, i = it.i;
       if (u != prev_u) {
         if (HIST && touched) {
@@ -550,18 +609,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = ewait(QFULL(qb), (unit_ord >> 1) & 1))) break;
       }
       const bool last_of_unit = (i == it.tiles - 1 || n == count - 1);
-      if ((int)(n & 1) == g) {
+      if (par == g) {
         touched = true;
-        const int x = (int)(n % A);
-        const int kx = (int)(n % KS);
+        const int x = ra.idx;
+        const int kx = rk.idx;
         const int64_t pos = (int64_t)i * kTileTok + tok;
         int32_t blk = 0;
         if (SPARSE) blk = a.block_table[(int64_t)u * a.kb + pos / 8];
-        if (!(ok = ewait(KSF(kx), (uint32_t)((n / KS) & 1)))) break;
+        if (!(ok = ewait(KSF(kx), rk.ph))) break;
         const float ks = ks_s[kx * kTileTok + tok];
         __syncwarp();
         if (lane == 0) mbar_arrive(KSE(kx));
-        if (!(ok = ewait(AFULL(x), (uint32_t)((n / A) & 1)))) break;
+        if (!(ok = ewait(AFULL(x), ra.ph))) break;
         tc_fence_after();
         float acc[NN];
 #pragma unroll
@@ -676,6 +735,7 @@ dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   a.B = c.B;
   a.req_next_n = c.next_n;
   a.page_size = c.page_size;
+  a.log2_ps = (c.page_size == 128) ? 7 : 6;
   a.num_pages = c.num_pages;
   a.block_table = c.block_table;
   a.kb = c.kb;
