@@ -94,7 +94,7 @@ __host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, int stages, int
   p.bar = off;
   off += (2 * stages + 2 * nks + 4 + 2 * nacc + 3) * 8;
   p.misc = off;
-  off += 64;
+  off += 64 + 2 * 32 * 4;  // flags/schedule + the producer's two row tables
   p.total = off + 1024;  // slack to align the base to 1024 bytes
   return p;
 }
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(EMPTY(s), 1);
     }
     for (int k = 0; k < KS; ++k) {
-      mbar_init(KSF(k), 32);  // one cp.async completion arrival per producer lane
+      mbar_init(KSF(k), 1);
       mbar_init(KSE(k), 4);
     }
     for (int q = 0; q < 2; ++q) {
@@ -349,19 +349,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // The page-table (and block-table) reads for a group of tiles are issued
-    // one group ahead, one entry per lane, so no tile waits on a dependent
-    // global load: ppt load slots per tile (2 or 1 pages, or 16 blocks),
-    // tpg = 32 / ppt tiles per group.
-    const uint64_t pol = policy_evict_first();
+    // The whole warp reads the page-table (or block-table) entries of a group
+    // of tpg tiles, one entry per lane, one group ahead of use, into a small
+    // shared table; lane 0 alone then walks the group's tiles: waits for the
+    // slots, arms the barriers and issues the copies (no warp-collective
+    // operation per tile).  ppt = load slots per tile (2 or 1 pages, or 16
+    // blocks of 8 tokens).
     const int ppt = SPARSE ? 16 : (kTileTok / a.page_size);
     const int tpg = 32 / ppt;
     const int my_o = lane / ppt, my_sl = lane % ppt;
     constexpr int kNone = INT32_MIN;
-    TileIter<SPARSE> it;
-    it.init(a, u_start, i_start);
-    TileIter<SPARSE> git = it;  // first tile of the group being prefetched
-    long long gn = 0;
+    int *rows_s = reinterpret_cast<int *>(smem + P.misc + 64);  // [2][32]
+    TileIter<SPARSE> git;
+    git.init(a, u_start, i_start);
     // raw table entry of this lane's slot in the group starting at (g0, n0)
     auto fetch = [&](TileIter<SPARSE> g0, long long n0, int &unit) -> int {
       unit = -1;
@@ -373,12 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p * a.page_size >= eff_ctx(a, g0.u)) return kNone;
       return __ldg(&a.page_table[(int64_t)g0.u * a.pt_stride + p]);
     };
-    // physical row of this lane's slot (or -1 when nothing is loaded)
+    // physical row of a slot (or -1 when nothing is loaded)
     auto to_row = [&](int raw, int unit) -> int {
       if (raw == kNone || unit < 0) return -1;
       if (SPARSE) {
         const int b = unit / a.req_next_n;
-        const int j = unit % a.req_next_n;
+        const int j = unit - b * a.req_next_n;
         const int64_t n_live = eff_ctx(a, b) - (a.req_next_n - 1 - j);
         if (raw == INT32_MAX || raw < 0 || (int64_t)raw * 8 >= n_live) return -1;
         const int64_t tok = (int64_t)raw * 8;
@@ -396,9 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return pg * a.page_size;
     };
+    const uint64_t pol = policy_evict_first();
     int nxt_unit;
-    int nxt = fetch(git, gn, nxt_unit);
-    int cur_row = -1;
+    int nxt = fetch(git, 0, nxt_unit);
+    TileIter<SPARSE> it = git;  // lane 0's walk over the tiles
     int prev_u = -1, unit_ord = -1;
     long long issued = 0;
     int q_issued = 0;
@@ -406,68 +407,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ring rs, rk;
     rs.init(S);
     rk.init(KS);
-    int o = 0;
-    for (long long n = 0; n < count && ok; ++n, it.next(a), rs.next(), rk.next(),
-                   o = (o + 1 == tpg) ? 0 : o + 1) {
-      const int u = it.u;
-      if (o == 0) {
-        cur_row = to_row(nxt, nxt_unit);
-        for (int k = 0; k < tpg; ++k) git.next(a);
-        gn += tpg;
-        nxt = fetch(git, gn, nxt_unit);
-      }
-      int row = __shfl_sync(0xffffffffu, cur_row, (o * ppt + my_sl) & 31);
-      if (lane >= ppt) row = -1;
-      if (u != prev_u) {
-        ++unit_ord;
-        prev_u = u;
-        const int qb = unit_ord & 1;
-        const uint32_t qph = (unit_ord >> 1) & 1;
-        const int qrow0 = SPARSE ? u * 32 : u * N;
-        if (lane == 0) {
-          ok = mbar_wait(QEMPTY(qb), qph ^ 1, ctl);
-          if (ok) {
+    int buf = 0;
+    for (long long g0n = 0; g0n < count && ok; g0n += tpg, buf ^= 1) {
+      // publish this group's rows, start fetching the next group's entries
+      rows_s[buf * 32 + lane] = to_row(nxt, nxt_unit);
+      for (int k = 0; k < tpg; ++k) git.next(a);
+      nxt = fetch(git, g0n + tpg, nxt_unit);
+      __syncwarp();
+      if (lane == 0) {
+        const long long gend = min(count, g0n + tpg);
+        for (long long n = g0n; n < gend; ++n, it.next(a), rs.next(), rk.next()) {
+          const int u = it.u;
+          if (u != prev_u) {
+            ++unit_ord;
+            prev_u = u;
+            const int qb = unit_ord & 1;
+            const int qrow0 = SPARSE ? u * 32 : u * N;
+            if (!(ok = mbar_wait(QEMPTY(qb), ((unit_ord >> 1) & 1) ^ 1, ctl))) break;
             mbar_arrive_expect_tx(QFULL(qb), N * 128 + N * 4);
             tma_load_2d(qst + qb * (N * 128), &tm_q, QFULL(qb), 0, qrow0);
             bulk_load(smem_u32(w_s + qb * N), a.weights + (int64_t)qrow0, N * 4, QFULL(qb));
             ++q_issued;
           }
+          const int s = rs.idx;
+          const int kx = rk.idx;
+          if (!(ok = mbar_wait(EMPTY(s), rs.ph ^ 1, ctl))) break;
+          if (!(ok = mbar_wait(KSE(kx), rk.ph ^ 1, ctl))) break;
+          const int *rw = rows_s + buf * 32 + (int)(n - g0n) * ppt;
+          const int blk_rows = SPARSE ? 8 : a.page_size;
+          uint32_t nload = 0;
+          for (int q = 0; q < ppt; ++q) nload += (rw[q] >= 0);
+          mbar_arrive_expect_tx(FULL(s), nload * (uint32_t)(blk_rows * 128));
+          mbar_arrive_expect_tx(KSF(kx), nload * (uint32_t)(blk_rows * 4));
+          for (int q = 0; q < ppt; ++q) {
+            const int row = rw[q];
+            if (row < 0) continue;
+            tma_load_2d_hint(kst + s * kStageK + q * blk_rows * 128, &tm_k, FULL(s), 0, row, pol);
+            bulk_load(smem_u32(ks_s + kx * kTileTok + q * blk_rows), a.kscale + (int64_t)row,
+                      blk_rows * 4, KSF(kx));
+          }
+          ++issued;
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-      }
-      const int s = rs.idx;
-      const int kx = rk.idx;
-      if (lane == 0) {
-        ok = mbar_wait(EMPTY(s), rs.ph ^ 1, ctl) && mbar_wait(KSE(kx), rk.ph ^ 1, ctl);
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
-      const unsigned loads = __ballot_sync(0xffffffffu, row >= 0);
-      const int blk_rows = SPARSE ? 8 : a.page_size;
-      const uint32_t nload = (uint32_t)__popc(loads);
-      if (lane == 0) mbar_arrive_expect_tx(FULL(s), nload * (uint32_t)(blk_rows * 128));
       __syncwarp();
-      if (row >= 0)
-        tma_load_2d_hint(kst + s * kStageK + lane * blk_rows * 128, &tm_k, FULL(s), 0, row, pol);
-      // kscale of the tile (128 floats = 512 bytes): 16 bytes per lane by
-      // cp.async; lane l covers tokens 4l .. 4l+3 of the tile
-      {
-        const int tk = lane * 4;                      // first token of this lane
-        const int src_lane = tk / blk_rows;           // load slot holding those tokens
-        const int srow = __shfl_sync(0xffffffffu, row, src_lane);
-        const bool have = srow >= 0;
-        const float *src = a.kscale + (have ? (int64_t)srow + (tk % blk_rows) : 0);
-        cp_async16(smem_u32(ks_s + kx * kTileTok + tk), src, have ? 16u : 0u);
-        cp_async_arrive_noinc(KSF(kx));
-      }
-      ++issued;
     }
     if (!ok && lane == 0) {
       // drain our own copies still in flight before the CTA exits
       const long long lim = a.wait_limit;
-      // the break left the rings one past the last issued tile only when
-      // the tile's copies were issued; count back from the issued total
       Ring ds = rs, dk = rk;
       ds.idx = (int)(issued % S);
       ds.ph = (uint32_t)((issued / S) & 1);
