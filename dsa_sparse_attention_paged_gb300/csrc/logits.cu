@@ -10,22 +10,27 @@
 // [SG38944] SGLang PR #38944 "What this enables": the sparse logits score only
 // the published 8-token blocks.
 //
-// One persistent CTA per SM, six warps:
-//   warp 0      TMA producer: gathers K pages through the page table into a
-//               ring of 128-token stages (16 KiB K + 512 B kscale each), and
-//               each request's Q tile + head weights into one of two buffers
-//   warp 1      allocates TMEM and issues tcgen05.mma (one thread):
-//               D[128 tokens x 32*next_n] = K[128 x 128] . Q[32*next_n x 128]^T,
-//               FP8 x FP8 -> FP32, with 4-8 accumulator buffers in TMEM
-//   warps 2..5  epilogue: each thread owns one TMEM lane = one token, loads
-//               its 32 head dots per row, applies kscale, ReLU and the head
-//               weights in registers, stores the logit (coalesced across the
-//               warp), and counts its bin in a per-warp shared histogram
-//               slot; the slots are summed and flushed with packed 64-bit
-//               global atomics whenever the CTA moves on to another request.
-// Work split: the flattened (request, 128-token tile) sequence is cut into
-// gridDim.x contiguous ranges, one per CTA; each CTA derives its range from a
-// prefix sum over context_lens (no separate metadata kernel).
+// One persistent CTA per SM, ten warps, over a ring of 256-token stages
+// (32 KiB of K, 1 KiB of kscale each):
+//   warp 0      producer: gathers the stage's K pages (or 8-token blocks)
+//               through the page table with one multi-lane TMA instruction,
+//               the matching kscale with one multi-lane bulk copy, and each
+//               request's Q tile and head weights into one of two buffers;
+//               page-table entries are read one group of stages ahead
+//   warp 1      allocates TMEM and issues tcgen05.mma (one thread): per stage
+//               two sub-tiles D[128 tokens x 32*next_n] = K[128 x 128] .
+//               Q[32*next_n x 128]^T, FP8 x FP8 -> FP32, into a TMEM pair
+//   warps 2..9  epilogue, two warpgroups, one per 128-token sub-tile: each
+//               thread owns one TMEM lane = one token, loads its 32 head dots
+//               per row, applies kscale, ReLU and the head weights in
+//               registers, stores the logit (coalesced across the warp) and
+//               counts its bin in a shared histogram slot; the slots are
+//               flushed with packed 64-bit global atomics whenever the CTA
+//               moves on to another request.
+// Work split: the flattened (request, stage) sequence is cut into gridDim.x
+// contiguous ranges, one per CTA; each CTA derives its range from a prefix sum
+// over context_lens (no separate metadata kernel).  Ring positions advance
+// by counters (no division per stage).
 #include <algorithm>
 
 #include "dsa_device.cuh"
@@ -35,11 +40,13 @@ namespace dsa {
 
 namespace {
 
-constexpr int kTileTok = 128;
-constexpr int kStageK = kTileTok * 128;      // bytes of K per stage
-constexpr int kStageKs = kTileTok * 4;       // bytes of kscale per stage
-constexpr int kMaxStages = 16;
-constexpr int kThreads = 320;       // producer, MMA, 2 x 4 epilogue warps
+constexpr int kStageTok = 256;               // tokens per pipeline stage
+constexpr int kSubTok = 128;                 // tokens per MMA sub-tile (TMEM lanes)
+constexpr int kStageK = kStageTok * 128;     // bytes of K per stage
+constexpr int kSubK = kSubTok * 128;
+constexpr int kStageKs = kStageTok * 4;      // bytes of kscale per stage
+constexpr int kMaxStages = 8;
+constexpr int kThreads = 320;                // producer, MMA, 2 x 4 epilogue warps
 constexpr int kEpiWarps = 8;
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in per CTA
 
@@ -55,7 +62,7 @@ struct LogitsArgs {
   int32_t log2_ps;      // page_size is 64 or 128
   int32_t num_pages;
   int32_t num_units;    // dense: requests; sparse: rows
-  int32_t sparse_tpu;   // sparse: tiles per row (kb / 16)
+  int32_t sparse_tpu;   // sparse: stages per row (ceil(kb / 32))
   const int32_t *block_table;
   int32_t kb;
   void *out;
@@ -110,7 +117,7 @@ __device__ __forceinline__ int64_t eff_ctx(const LogitsArgs &a, int b) {
 template <bool SPARSE>
 __device__ __forceinline__ int unit_tiles(const LogitsArgs &a, int u) {
   if (SPARSE) return a.sparse_tpu;
-  return static_cast<int>((eff_ctx(a, u) + kTileTok - 1) / kTileTok);
+  return static_cast<int>((eff_ctx(a, u) + kStageTok - 1) / kStageTok);
 }
 
 template <bool SPARSE>
@@ -308,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int k = 0; k < KS; ++k) {
       mbar_init(KSF(k), 1);
-      mbar_init(KSE(k), 4);
+      mbar_init(KSE(k), kEpiWarps);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(QFULL(q), 1);
@@ -316,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < A; ++x) {
       mbar_init(AFULL(x), 1);
-      mbar_init(AEMPTY(x), 4);
+      mbar_init(AEMPTY(x), kEpiWarps);
     }
     mbar_init(DRAIN, 1);
     mbar_init(GSYNC(0), 4);
@@ -349,26 +356,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // The whole warp reads the page-table (or block-table) entries of a group
-    // of tpg tiles, one entry per lane, one group ahead of use, into a small
-    // shared table; lane 0 alone then walks the group's tiles: waits for the
-    // slots, arms the barriers and issues the copies (no warp-collective
-    // operation per tile).  ppt = load slots per tile (2 or 1 pages, or 16
-    // blocks of 8 tokens).
-    const int ppt = SPARSE ? 16 : (kTileTok / a.page_size);
+    // ppt load slots per stage (4 or 2 pages, or 32 blocks of 8 tokens), one
+    // per lane; tpg = 32 / ppt stages per prefetch group.  Each lane reads its
+    // slot's table entry one group ahead of use.
+    const int ppt = SPARSE ? 32 : (kStageTok / a.page_size);
     const int tpg = 32 / ppt;
     const int my_o = lane / ppt, my_sl = lane % ppt;
     constexpr int kNone = INT32_MIN;
-    int *rows_s = reinterpret_cast<int *>(smem + P.misc + 64);  // [2][32]
-    TileIter<SPARSE> git;
-    git.init(a, u_start, i_start);
+    TileIter<SPARSE> it;
+    it.init(a, u_start, i_start);
+    TileIter<SPARSE> git = it;  // first stage of the group being prefetched
     // raw table entry of this lane's slot in the group starting at (g0, n0)
     auto fetch = [&](TileIter<SPARSE> g0, long long n0, int &unit) -> int {
       unit = -1;
       if (n0 + my_o >= count) return kNone;
       for (int k = 0; k < my_o; ++k) g0.next(a);
       unit = g0.u;
-      if (SPARSE) return __ldg(&a.block_table[(int64_t)g0.u * a.kb + (int64_t)g0.i * 16 + my_sl]);
+      if (SPARSE) {
+        const int blk = g0.i * 32 + my_sl;
+        if (blk >= a.kb) return kNone;
+        return __ldg(&a.block_table[(int64_t)g0.u * a.kb + blk]);
+      }
       const int64_t p = (int64_t)g0.i * ppt + my_sl;
       if (p * a.page_size >= eff_ctx(a, g0.u)) return kNone;
       return __ldg(&a.page_table[(int64_t)g0.u * a.pt_stride + p]);
@@ -397,9 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       return pg * a.page_size;
     };
     const uint64_t pol = policy_evict_first();
+    const int blk_rows = SPARSE ? 8 : a.page_size;
     int nxt_unit;
     int nxt = fetch(git, 0, nxt_unit);
-    TileIter<SPARSE> it = git;  // lane 0's walk over the tiles
+    int cur_row = -1;
     int prev_u = -1, unit_ord = -1;
     long long issued = 0;
     int q_issued = 0;
@@ -407,50 +416,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ring rs, rk;
     rs.init(S);
     rk.init(KS);
-    int buf = 0;
-    for (long long g0n = 0; g0n < count && ok; g0n += tpg, buf ^= 1) {
-      // publish this group's rows, start fetching the next group's entries
-      rows_s[buf * 32 + lane] = to_row(nxt, nxt_unit);
-      for (int k = 0; k < tpg; ++k) git.next(a);
-      nxt = fetch(git, g0n + tpg, nxt_unit);
-      __syncwarp();
-      if (lane == 0) {
-        const long long gend = min(count, g0n + tpg);
-        for (long long n = g0n; n < gend; ++n, it.next(a), rs.next(), rk.next()) {
-          const int u = it.u;
-          if (u != prev_u) {
-            ++unit_ord;
-            prev_u = u;
-            const int qb = unit_ord & 1;
-            const int qrow0 = SPARSE ? u * 32 : u * N;
-            if (!(ok = mbar_wait(QEMPTY(qb), ((unit_ord >> 1) & 1) ^ 1, ctl))) break;
+    int o = 0;
+    for (long long n = 0; n < count && ok; ++n, it.next(a), rs.next(), rk.next(),
+                   o = (o + 1 == tpg) ? 0 : o + 1) {
+      const int u = it.u;
+      if (o == 0) {
+        cur_row = to_row(nxt, nxt_unit);
+        for (int k = 0; k < tpg; ++k) git.next(a);
+        nxt = fetch(git, n + tpg, nxt_unit);
+      }
+      int row = __shfl_sync(0xffffffffu, cur_row, (o * ppt + my_sl) & 31);
+      if (lane >= ppt) row = -1;
+      if (u != prev_u) {
+        ++unit_ord;
+        prev_u = u;
+        const int qb = unit_ord & 1;
+        const int qrow0 = SPARSE ? u * 32 : u * N;
+        if (lane == 0) {
+          ok = mbar_wait(QEMPTY(qb), ((unit_ord >> 1) & 1) ^ 1, ctl);
+          if (ok) {
             mbar_arrive_expect_tx(QFULL(qb), N * 128 + N * 4);
             tma_load_2d(qst + qb * (N * 128), &tm_q, QFULL(qb), 0, qrow0);
             bulk_load(smem_u32(w_s + qb * N), a.weights + (int64_t)qrow0, N * 4, QFULL(qb));
             ++q_issued;
           }
-          const int s = rs.idx;
-          const int kx = rk.idx;
-          if (!(ok = mbar_wait(EMPTY(s), rs.ph ^ 1, ctl))) break;
-          if (!(ok = mbar_wait(KSE(kx), rk.ph ^ 1, ctl))) break;
-          const int *rw = rows_s + buf * 32 + (int)(n - g0n) * ppt;
-          const int blk_rows = SPARSE ? 8 : a.page_size;
-          uint32_t nload = 0;
-          for (int q = 0; q < ppt; ++q) nload += (rw[q] >= 0);
-          mbar_arrive_expect_tx(FULL(s), nload * (uint32_t)(blk_rows * 128));
-          mbar_arrive_expect_tx(KSF(kx), nload * (uint32_t)(blk_rows * 4));
-          for (int q = 0; q < ppt; ++q) {
-            const int row = rw[q];
-            if (row < 0) continue;
-            tma_load_2d_hint(kst + s * kStageK + q * blk_rows * 128, &tm_k, FULL(s), 0, row, pol);
-            bulk_load(smem_u32(ks_s + kx * kTileTok + q * blk_rows), a.kscale + (int64_t)row,
-                      blk_rows * 4, KSF(kx));
-          }
-          ++issued;
         }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
       }
+      const int s = rs.idx;
+      const int kx = rk.idx;
+      if (lane == 0) ok = mbar_wait(EMPTY(s), rs.ph ^ 1, ctl) && mbar_wait(KSE(kx), rk.ph ^ 1, ctl);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      const uint32_t nload = (uint32_t)__popc(__ballot_sync(0xffffffffu, row >= 0));
+      if (lane == 0) {
+        mbar_arrive_expect_tx(FULL(s), nload * (uint32_t)(blk_rows * 128));
+        mbar_arrive_expect_tx(KSF(kx), nload * (uint32_t)(blk_rows * 4));
+      }
       __syncwarp();
+      if (row >= 0) {
+        tma_load_2d_hint(kst + s * kStageK + lane * blk_rows * 128, &tm_k, FULL(s), 0, row, pol);
+        bulk_load(smem_u32(ks_s + kx * kStageTok + lane * blk_rows), a.kscale + (int64_t)row,
+                  blk_rows * 4, KSF(kx));
+      }
+      ++issued;
     }
     if (!ok && lane == 0) {
       // drain our own copies still in flight before the CTA exits
@@ -498,12 +508,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(AEMPTY(x), ra.ph ^ 1, ctl))) break;
         if (!(ok = mbar_wait(FULL(s), rs.ph, ctl))) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(x * N);
-        const uint64_t ad = sdesc_sw128(kst + s * kStageK);
         const uint64_t bd = sdesc_sw128(qst + qb * (N * 128));
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // K = 128 FP8 = 4 steps of 32 bytes
-          mma_f8(d, ad + 2 * kk, bd + 2 * kk, IDESC, kk > 0 ? 1u : 0u);
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t d = tmem_base + (uint32_t)((2 * x + h) * N);
+          const uint64_t ad = sdesc_sw128(kst + s * kStageK + h * kSubK);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // K = 128 FP8 = 4 steps of 32 bytes
+            mma_f8(d, ad + 2 * kk, bd + 2 * kk, IDESC, kk > 0 ? 1u : 0u);
+        }
         ++mmas;
         mma_commit(EMPTY(s));
         mma_commit(AFULL(x));
@@ -517,13 +530,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    // two warpgroups take alternate tiles; in each, warp w reads TMEM lanes
+    // warpgroup g takes sub-tile g of every stage; warp w reads TMEM lanes
     // 32*(w%4) .. +31, i.e. one token per thread
     const int g = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int lane_base = 32 * quarter;
-    const int tok = lane_base + lane;
-    const int gtid = ((warp - 2) & 3) * 32 + lane;  // 0..127 within the group
+    const int tok = g * kSubTok + lane_base + lane;   // token within the stage
+    const int gtid = ((warp - 2) & 3) * 32 + lane;    // 0..127 within the group
     int *grp_hist = hist_s + g * HS * NN * DSA_NUM_BINS;
     int *my_hist = grp_hist + (HS == 4 ? quarter : 0) * NN * DSA_NUM_BINS;
     TileIter<SPARSE> it;
@@ -532,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t gsync_ph = 0;
     int64_t ctx_b = 0, n_row = 0;
     int row_base = 0;
-    bool ok = true, touched = false;
+    bool ok = true;
 
     auto ewait = [&](uint32_t bar, uint32_t parity) -> bool {
       const bool r = mbar_wait(bar, parity, ctl);
@@ -573,20 +586,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ring ra, rk;
     ra.init(A);
     rk.init(KS);
-    int par = 0;  // parity of n: which group owns the tile
-    for (long long n = 0; n < count; ++n, it.next(a), ra.next(), rk.next(), par ^= 1) {
+    for (long long n = 0; n < count; ++n, it.next(a), ra.next(), rk.next()) {
       const int u = it.u, i = it.i;
       if (u != prev_u) {
-        if (HIST && touched) {
+        if (HIST && prev_u >= 0) {
           if (!(ok = flush(row_base))) break;
         }
-        touched = false;
         ++unit_ord;
         prev_u = u;
         qb = unit_ord & 1;
         if (SPARSE) {
           const int b = u / a.req_next_n;
-          const int j = u % a.req_next_n;
+          const int j = u - b * a.req_next_n;
           n_row = eff_ctx(a, b) - (a.req_next_n - 1 - j);
           if (n_row < 0) n_row = 0;
         } else {
@@ -595,33 +606,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!(ok = ewait(QFULL(qb), (unit_ord >> 1) & 1))) break;
       }
-      const bool last_of_unit = (i == it.tiles - 1 || n == count - 1);
-      if (par == g) {
-        touched = true;
-        const int x = ra.idx;
-        const int kx = rk.idx;
-        const int64_t pos = (int64_t)i * kTileTok + tok;
-        int32_t blk = 0;
-        if (SPARSE) blk = a.block_table[(int64_t)u * a.kb + pos / 8];
-        if (!(ok = ewait(KSF(kx), rk.ph))) break;
-        const float ks = ks_s[kx * kTileTok + tok];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(KSE(kx));
-        if (!(ok = ewait(AFULL(x), ra.ph))) break;
-        tc_fence_after();
-        float acc[NN];
+      const int x = ra.idx;
+      const int kx = rk.idx;
+      const int64_t pos = (int64_t)i * kStageTok + tok;
+      int32_t blk = INT32_MAX;
+      if (SPARSE && pos < (int64_t)a.kb * 8) blk = __ldg(&a.block_table[(int64_t)u * a.kb + pos / 8]);
+      if (!(ok = ewait(KSF(kx), rk.ph))) break;
+      const float ks = ks_s[kx * kStageTok + tok];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(KSE(kx));
+      if (!(ok = ewait(AFULL(x), ra.ph))) break;
+      tc_fence_after();
+      float acc[NN];
 #pragma unroll
-        for (int j = 0; j < NN; ++j) {
-          uint32_t v[32];
-          tmem_ld32(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(x * N + j * 32), v);
-          tmem_ld_wait();
-          acc[j] = head_sum(v, ks, w_s + qb * N + j * 32);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(AEMPTY(x));
+      for (int j = 0; j < NN; ++j) {
+        uint32_t v[32];
+        tmem_ld32(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)((2 * x + g) * N + j * 32), v);
+        tmem_ld_wait();
+        acc[j] = head_sum(v, ks, w_s + qb * N + j * 32);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(AEMPTY(x));
 
-        if (SPARSE) {
+      if (SPARSE) {
+        if (pos < (int64_t)a.kb * 8) {
           const int64_t t = (int64_t)blk * 8 + (pos & 7);
           const bool live = blk != INT32_MAX && blk >= 0 && t < n_row;
           const float val = live ? acc[0] : -INFINITY;
@@ -630,31 +639,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             reinterpret_cast<float *>(a.out)[(int64_t)u * a.out_stride + pos] = val;
           }
-        } else {
-          const int64_t t = pos;
+        }
+      } else {
+        const int64_t t = pos;
 #pragma unroll
-          for (int j = 0; j < NN; ++j) {
-            int64_t n_rj = ctx_b - (NN - 1 - j);
-            if (n_rj > a.out_stride) {
-              n_rj = a.out_stride;
-              if (t == a.out_stride) set_status(a.status, DSA_DEV_BOUNDS);
-            }
-            if (t < n_rj) {
-              reinterpret_cast<float *>(a.out)[(int64_t)(row_base + j) * a.out_stride + t] = acc[j];
-              if (HIST) {
-                const int bin = coarse_bin(acc[j]);
-                if (bin >= 0) atomicAdd(&my_hist[j * DSA_NUM_BINS + bin], 1);
-              }
+        for (int j = 0; j < NN; ++j) {
+          int64_t n_rj = ctx_b - (NN - 1 - j);
+          if (n_rj > a.out_stride) {
+            n_rj = a.out_stride;
+            if (t == a.out_stride) set_status(a.status, DSA_DEV_BOUNDS);
+          }
+          if (t < n_rj) {
+            reinterpret_cast<float *>(a.out)[(int64_t)(row_base + j) * a.out_stride + t] = acc[j];
+            if (HIST) {
+              const int bin = coarse_bin(acc[j]);
+              if (bin >= 0) atomicAdd(&my_hist[j * DSA_NUM_BINS + bin], 1);
             }
           }
         }
       }
-      if (last_of_unit) {
+      if (i == it.tiles - 1 || n == count - 1) {
         __syncwarp();
         if (lane == 0) mbar_arrive(QEMPTY(qb));
       }
     }
-    if (HIST && ok && touched) flush(row_base);
+    if (HIST && ok && prev_u >= 0) flush(row_base);
   }
 
   __syncthreads();
@@ -664,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Stage count and ring depths for one instantiation: as many 16 KiB K stages
+// Stage count and ring depths for one instantiation: as many 32 KiB K stages
 // as fit next to the Q/weight buffers, the histogram slots and a kscale ring
 // deep enough (stages + accumulators + 2) never to hold the producer back.
 struct LaunchPlan {
@@ -674,9 +683,9 @@ struct LaunchPlan {
 inline LaunchPlan plan_for(int nn, bool hist) {
   LaunchPlan L;
   const int N = 32 * nn;
-  L.nacc = std::min(8, 512 / N);
+  L.nacc = std::min(4, 512 / (2 * N));  // TMEM pairs (two 128-lane sub-tiles each)
   L.cols = 32;
-  while (L.cols < L.nacc * N) L.cols <<= 1;
+  while (L.cols < 2 * L.nacc * N) L.cols <<= 1;
   L.stages = kMaxStages;
   while (L.stages > 2 &&
          smem_plan(nn, hist, L.stages, L.nacc, L.stages + L.nacc + 2).total > kSmemLimit)
@@ -735,7 +744,7 @@ dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   if (sms <= 0) return DSA_ERR_CUDA;
   if (c.sparse) {
     a.num_units = c.B * c.next_n;
-    a.sparse_tpu = c.kb / 16;
+    a.sparse_tpu = (c.kb + 31) / 32;
     const long long tiles = (long long)a.num_units * a.sparse_tpu;
     const int grid = (int)std::max<long long>(1, std::min<long long>(sms, tiles));
     if (c.out_f16) return launch_one<1, true, true, false>(tk, tq, a, grid, st);
