@@ -1,0 +1,53 @@
+"""Bench host logic with two gloo ranks on CPU: replicas report the slowest
+rank's time and the whole-job rate; the reference arm prints on rank 0 only."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    t = bench.max_over_ranks(1.0 + rank, dist, "cpu")
+    env = bench.dist_env()
+    q.put((rank, t, env))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [2.0, 2.0]
+    assert res[1][2] == (2, 1, 1)
+
+
+def test_whole_job_rate_is_weak_scaling():
+    import bench
+    assert bench.whole_job_rate(1000, 1, 10, 2.0) == 5000.0
+    assert bench.whole_job_rate(1000, 4, 10, 2.0) == 20000.0
+    assert bench.max_over_ranks(3.5, None, "cpu") == 3.5
