@@ -27,6 +27,7 @@ OUT_F16 = 1
 DEV_TIMEOUT = 0x1
 DEV_BOUNDS = 0x2
 INT32_MAX = 2**31 - 1
+NOALLOC_MAX_ROWS = 64
 
 _STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
            3: "DSA_ERR_MISALIGNED", 4: "DSA_ERR_CUDA", 5: "DSA_ERR_WORKSPACE"}
@@ -45,7 +46,7 @@ def _load():
         raise ImportError(
             f"CUDA library not built: {LIB_PATH} is missing. Build it with "
             "`python -c 'import __graft_entry__ as g; g.build()'` or "
-            "`python -m dsa_sparse_attention_paged_gb300.build`.")
+            "`python dsa_sparse_attention_paged_gb300/build.py`.")
     L = ctypes.CDLL(LIB_PATH)
     P, i32, i64, sz, u32, u64 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                  ctypes.c_size_t, ctypes.c_uint32, ctypes.c_uint64)
@@ -64,6 +65,7 @@ def _load():
         "dsa_sparse_mqa_logits": (i32, [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, i32, P,
                                         i32, P, i32, i64, P, sz, P]),
         "dsa_topk_fp16": (i32, [P, i64, P, i32, i32, P, i32, P, P, sz, P]),
+        "dsa_coarse_hist_topk_noalloc": (i32, [P, i64, P, i32, i32, i32, P, i32, i32, P, P, P]),
         "dsa_coarse_bins_range": (i32, [u32, i64, P, P]),
         "dsa_fp16_order_keys": (i32, [P, P, i64, P]),
         "dsa_wait_timeout_selftest": (i32, [u64, P, sz, P]),
@@ -262,3 +264,23 @@ def fp16_order_keys(x, out=None, stream=None):
 def wait_timeout_selftest(limit_cycles: int, ws, stream=None):
     _check(lib.dsa_wait_timeout_selftest(ctypes.c_uint64(limit_cycles), ws.ptr, ws.nbytes,
                                          _stream(stream)), "wait_timeout_selftest")
+
+
+def coarse_hist_topk_noalloc(logits, context_lens, next_n, k, histogram=None,
+                             reset_histogram=False, len_div=1, out=None, fallback_flags=None,
+                             R=None, stream=None):
+    """coarse_hist_topk for callers that cannot allocate device memory: the
+    scratch lives in a fixed array inside the library (at most NOALLOC_MAX_ROWS
+    rows; calls that overlap on the GPU race on it).  ``out`` and
+    ``fallback_flags`` are the caller's own buffers."""
+    _req(logits, torch.float32, "logits")
+    _req(context_lens, torch.int32, "context_lens")
+    R = logits.shape[0] if R is None else R
+    if out is None:
+        out = torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    _req(out, torch.int32, "out")
+    _check(lib.dsa_coarse_hist_topk_noalloc(
+        _p(logits), logits.stride(0), _p(context_lens), next_n, len_div, R, _p(histogram),
+        1 if reset_histogram else 0, k, _p(out), _p(fallback_flags), _stream(stream)),
+        "coarse_hist_topk_noalloc")
+    return out

@@ -167,6 +167,35 @@ int32_t dsa_coarse_hist_topk(const float *logits, int64_t stride, const int32_t 
                              int32_t *fallback_flags, void *workspace, size_t ws_bytes,
                              void *stream);
 
+/* ---- top-k without a caller workspace --------------------------------------
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory at the point where they select -- for
+ * example code running inside a framework that owns every allocation, or a
+ * host callback that must not call cudaMalloc -- and so cannot provide the
+ * workspace dsa_coarse_hist_topk needs.
+ *
+ * Same arguments, results and fallbacks as dsa_coarse_hist_topk, minus the
+ * workspace: the scratch (counters, candidates, histograms) lives in one
+ * static device array inside the library, sized for DSA_NOALLOC_MAX_ROWS rows
+ * (about 5.3 MB, held on every GPU that loads the library until the process
+ * exits).  R > DSA_NOALLOC_MAX_ROWS returns DSA_ERR_UNSUPPORTED.  The call
+ * allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make this first call
+ *     before any stream capture.
+ *   - Every call shares the one array and clears the parts that must start at
+ *     zero itself.  Calls whose kernels overlap on the GPU (other streams,
+ *     other host threads) race on it and give wrong results: serialise them.
+ *   - Device-side anomaly bits of this variant stay in the library's array and
+ *     are not reported; fallback_flags still reports per-row fallbacks. */
+#define DSA_NOALLOC_MAX_ROWS 64
+int32_t dsa_coarse_hist_topk_noalloc(const float *logits, int64_t stride,
+                                     const int32_t *context_lens, int32_t next_n,
+                                     int32_t len_div, int32_t R, int32_t *histogram,
+                                     int32_t reset_histogram, int32_t k, int32_t *out_idx,
+                                     int32_t *fallback_flags, void *stream);
+
 /* ---- block maxima over 8-score blocks ------------------------------------
  * [SG38944] amax8_varlen: for row r with n_r live scores and
  * nb = ceil(n_r / 8) blocks, amax[r][i] = max(logits[r][8i .. 8i+7]) for

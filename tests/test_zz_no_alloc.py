@@ -1,0 +1,64 @@
+"""The allocation-free top-k entry point (for callers that cannot allocate a
+workspace) gives the same results as the workspace entry point, on two calls
+in a row, through the C ABI.  Collected last on purpose."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+def _case():
+    import synthetic as S
+    from tests.helpers import make, to_dev
+    import dsa_sparse_attention_paged_gb300 as D
+    case = make(4, 1, [20000, 9000, 130, 16000], 64, "mixed", seed=606)
+    d = to_dev(case)
+    ws = D.Workspace(4)
+    stride = 20008
+    logits = torch.full((4, stride), float("nan"), dtype=torch.float32, device="cuda")
+    hist = torch.zeros((4, 1024), dtype=torch.int32, device="cuda")
+    D.paged_mqa_logits(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"],
+                       d["context_lens"], 1, ws, logits=logits, histogram=hist)
+    torch.cuda.synchronize()
+    return D, d, ws, logits, hist
+
+
+def _sorted(t):
+    return np.sort(t.cpu().numpy(), axis=1)
+
+
+def test_noalloc_topk_matches_workspace_topk_twice():
+    D, d, ws, logits, hist = _case()
+    ctx = d["context_lens"]
+    ref = D.coarse_hist_topk(logits, ctx, 1, 2048, ws, histogram=hist)
+    ref_nohist = D.coarse_hist_topk(logits, ctx, 1, 2048, ws, histogram=None)
+    torch.cuda.synchronize()
+    for call in range(2):
+        flags = torch.full((4,), -1, dtype=torch.int32, device="cuda")
+        out = torch.full((4, 2048), -7, dtype=torch.int32, device="cuda")
+        st = D.lib.dsa_coarse_hist_topk_noalloc(
+            ctypes.c_void_p(logits.data_ptr()), logits.stride(0), ctypes.c_void_p(ctx.data_ptr()),
+            1, 1, 4, ctypes.c_void_p(hist.data_ptr()), 0, 2048,
+            ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(flags.data_ptr()),
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert st == 0, D.lib.dsa_status_string(st)
+        out2 = D.coarse_hist_topk_noalloc(logits, ctx, 1, 2048, histogram=None)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(_sorted(out), _sorted(ref))
+        np.testing.assert_array_equal(_sorted(out2), _sorted(ref_nohist))
+        assert (flags.cpu().numpy() >= 0).all()
+
+
+def test_noalloc_rejects_rows_beyond_its_maximum():
+    import dsa_sparse_attention_paged_gb300 as D
+    n = D.NOALLOC_MAX_ROWS + 1
+    x = torch.zeros((n, 64), dtype=torch.float32, device="cuda")
+    c = torch.full((n,), 64, dtype=torch.int32, device="cuda")
+    o = torch.zeros((n, 8), dtype=torch.int32, device="cuda")
+    st = D.lib.dsa_coarse_hist_topk_noalloc(
+        ctypes.c_void_p(x.data_ptr()), 64, ctypes.c_void_p(c.data_ptr()), 1, 1, n, None, 0, 8,
+        ctypes.c_void_p(o.data_ptr()), None, None)
+    assert st == 2  # DSA_ERR_UNSUPPORTED
