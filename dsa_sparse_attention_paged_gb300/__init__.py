@@ -58,7 +58,7 @@ def _load():
         "dsa_workspace_init": (i32, [P, sz, P]),
         "dsa_read_device_status": (i32, [P, P, ctypes.POINTER(u32)]),
         "dsa_paged_mqa_logits": (i32, [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, i32, P,
-                                       i64, P, P, sz, P]),
+                                       i64, P, P, i64, i32, P, sz, P]),
         "dsa_coarse_hist_topk": (i32, [P, i64, P, i32, i32, i32, P, i32, i32, P, P, P, sz, P]),
         "dsa_block_amax8": (i32, [P, i64, P, i32, i32, i32, P, i64, P, sz, P]),
         "dsa_sort_candidate_blocks": (i32, [P, i32, P, i32, i32, P, i64, i32, P, P, P, sz, P]),
@@ -134,9 +134,11 @@ def workspace_size(max_rows: int) -> int:
 
 
 def paged_mqa_logits(q, kv_pages, kscale, weights, page_table, context_lens, next_n, ws,
-                     logits=None, logits_stride=None, histogram=None, stream=None):
-    """Dense logits [B*next_n][stride] (dead columns untouched) and, when
-    ``histogram`` is given, accumulate its coarse bins.  Returns logits."""
+                     logits=None, logits_stride=None, histogram=None, amax=None,
+                     amax_skip_if_blocks_le=0, stream=None):
+    """Dense logits [B*next_n][stride] (dead columns untouched); when given,
+    accumulate the coarse histogram and write the block maxima over 8 scores
+    in the same pass.  Returns logits."""
     q, kv_pages = _u8(q), _u8(kv_pages)
     _req(q, torch.uint8, "q")
     _req(kv_pages, torch.uint8, "kv_pages")
@@ -157,11 +159,14 @@ def paged_mqa_logits(q, kv_pages, kscale, weights, page_table, context_lens, nex
     _req(logits, torch.float32, "logits")
     if histogram is not None:
         _req(histogram, torch.int32, "histogram")
+    if amax is not None:
+        _req(amax, torch.float32, "amax")
     for t in (q, kv_pages, kscale, weights, page_table, context_lens):
         assert t.is_contiguous()
     _check(lib.dsa_paged_mqa_logits(
         _p(q), _p(kv_pages), _p(kscale), _p(weights), _p(page_table), page_table.stride(0),
         _p(context_lens), B, next_n, H, D, ps, P, _p(logits), logits.stride(0), _p(histogram),
+        _p(amax), amax.stride(0) if amax is not None else 0, int(amax_skip_if_blocks_le),
         ws.ptr, ws.nbytes, _stream(stream)), "paged_mqa_logits")
     return logits
 

@@ -203,14 +203,16 @@ int32_t dsa_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const fl
                              int64_t page_table_stride, const int32_t *context_lens, int32_t B,
                              int32_t next_n, int32_t num_heads, int32_t head_dim,
                              int32_t page_size, int32_t num_pages, float *logits,
-                             int64_t logits_stride, int32_t *histogram, void *workspace,
-                             size_t ws_bytes, void *stream) {
+                             int64_t logits_stride, int32_t *histogram, float *amax,
+                             int64_t amax_stride, int32_t amax_skip_if_blocks_le,
+                             void *workspace, size_t ws_bytes, void *stream) {
   int32_t e = check_paged_common(q, kv_pages, kscale, weights, page_table, page_table_stride,
                                  context_lens, B, next_n, num_heads, head_dim, page_size,
                                  num_pages, workspace, ws_bytes);
   if (e != DSA_OK) return e;
   if (!logits || logits_stride < 1) return DSA_ERR_INVALID_ARG;
   if (histogram && !aligned(histogram, 8)) return DSA_ERR_MISALIGNED;
+  if (amax && amax_stride < 1) return DSA_ERR_INVALID_ARG;
   if (B == 0) return DSA_OK;
   LogitsCall c{};
   c.q = q;
@@ -227,6 +229,9 @@ int32_t dsa_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const fl
   c.out = logits;
   c.out_stride = logits_stride;
   c.histogram = histogram;
+  c.amax = amax;
+  c.amax_stride = amax_stride;
+  c.amax_skip = amax_skip_if_blocks_le;
   c.sparse = false;
   c.out_f16 = false;
   c.block_table = nullptr;
@@ -267,6 +272,9 @@ int32_t dsa_sparse_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const f
   c.out = out;
   c.out_stride = out_stride;
   c.histogram = nullptr;
+  c.amax = nullptr;
+  c.amax_stride = 0;
+  c.amax_skip = 0;
   c.sparse = true;
   c.out_f16 = (out_dtype == DSA_OUT_F16);
   c.block_table = block_table;

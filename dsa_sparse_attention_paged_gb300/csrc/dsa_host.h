@@ -26,6 +26,9 @@ struct LogitsCall {
   void *out;
   int64_t out_stride;
   int32_t *histogram;
+  float *amax;
+  int64_t amax_stride;
+  int32_t amax_skip;
   bool sparse;
   bool out_f16;
   const int32_t *block_table;

@@ -68,6 +68,9 @@ struct LogitsArgs {
   void *out;
   int64_t out_stride;
   int32_t *histogram;
+  float *amax;          // dense only: block maxima over 8 scores, or NULL
+  int64_t amax_stride;
+  int32_t amax_skip;    // rows with at most this many blocks are skipped (0: none)
   uint32_t *status;
   int32_t num_stages;
   int32_t num_acc;
@@ -656,6 +659,28 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (bin >= 0) atomicAdd(&my_hist[j * DSA_NUM_BINS + bin], 1);
             }
           }
+          if (a.amax != nullptr) {
+            // block maximum of 8 consecutive scores (8 consecutive lanes), in
+            // the value order of the select (-0 below +0, NaN ignored); the
+            // newest block is +inf, nothing is written past the block count
+            const int64_t nb = n_rj > 0 ? (n_rj + 7) >> 3 : 0;
+            uint32_t key = (t < n_rj && !isnan(acc[j])) ? f32_order_key(acc[j]) : 0u;
+            key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
+            key = max(key, __shfl_xor_sync(0xffffffffu, key, 2));
+            key = max(key, __shfl_xor_sync(0xffffffffu, key, 4));
+            const int64_t blk = t >> 3;
+            if ((lane & 7) == 0 && blk < nb && (a.amax_skip <= 0 || nb > a.amax_skip)) {
+              float m;
+              if (blk == nb - 1) {
+                m = INFINITY;
+              } else {
+                const uint32_t bits = (key & 0x80000000u) ? (key ^ 0x80000000u) : ~key;
+                m = key ? __uint_as_float(bits) : __int_as_float(0x7fc00000);
+              }
+              if (blk < a.amax_stride) a.amax[(int64_t)(row_base + j) * a.amax_stride + blk] = m;
+              else set_status(a.status, DSA_DEV_BOUNDS);
+            }
+          }
         }
       }
       if (i == it.tiles - 1 || n == count - 1) {
@@ -738,6 +763,9 @@ dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   a.out = c.out;
   a.out_stride = c.out_stride;
   a.histogram = c.histogram;
+  a.amax = c.sparse ? nullptr : c.amax;
+  a.amax_stride = c.amax_stride;
+  a.amax_skip = c.amax_skip;
   a.status = c.status;
   a.wait_limit = c.wait_limit;
   const int sms = num_sms();

@@ -660,6 +660,141 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- short rows
+// Rows of at most kSmemRow scores with no histogram given (the block maxima
+// of the two-level path): one CTA per row holds the row as FP32 order keys in
+// shared memory and runs an exact MSB radix select there -- no global
+// counters, no second launch.  Digit counts are aggregated per warp with
+// __match_any_sync, so skewed rows (many equal leading bytes) do not
+// serialise on one shared counter.
+constexpr int kSmemRow = 16384;
+constexpr int kRowThreads = 1024;
+constexpr int kRowWarps = kRowThreads / 32;
+
+__device__ __forceinline__ int block_excl_scan_1024(int v, int *ws, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) ws[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = ws[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    ws[lane] = wi - w;
+    if (lane == 31) ws[kRowWarps] = wi;
+  }
+  __syncthreads();
+  const int res = ws[warp] + incl - v;
+  *total = ws[kRowWarps];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(kRowThreads)
+    row_topk_kernel(const float *logits, int64_t stride, const int32_t *ctx, int next_n,
+                    int len_div, int k, int32_t *out, uint32_t *status) {
+  extern __shared__ uint32_t keys[];  // [kSmemRow]
+  __shared__ int h[256];
+  __shared__ int sm_scan[kRowWarps + 1];
+  __shared__ int sm_misc[8];
+  const int r = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  int64_t n = row_len(ctx, next_n, len_div, r, stride, status);
+  if (n > kSmemRow) {
+    if (threadIdx.x == 0) set_status(status, DSA_DEV_BOUNDS);
+    n = kSmemRow;
+  }
+  const float *row = logits + (int64_t)r * stride;
+  int32_t *outr = out + (int64_t)r * k;
+  // order keys; NaN and positions past the row become key 0 (never chosen)
+  const int nn = (int)n;
+  for (int t = threadIdx.x; t < kSmemRow; t += kRowThreads) {
+    uint32_t kk = 0;
+    if (t < nn) {
+      const float x = row[t];
+      kk = isnan(x) ? 0u : f32_order_key(x);
+    }
+    keys[t] = kk;
+  }
+  constexpr int PER = kSmemRow / kRowThreads;  // keys per thread, contiguous
+  const int t0 = threadIdx.x * PER;
+  __syncthreads();
+  // valid count (key 0 is only ever NaN or padding: -inf has key 0x007FFFFF)
+  int valid = 0;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) valid += (keys[t0 + e] != 0);
+  int nvalid;
+  (void)block_excl_scan_1024(valid, sm_scan, &nvalid);
+  uint32_t prefix = 0, mask = 0;
+  int need = k;
+  bool take_all = nvalid <= k, early = false;
+  if (!take_all) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      if (threadIdx.x < 256) h[threadIdx.x] = 0;
+      __syncthreads();
+#pragma unroll 4
+      for (int e = 0; e < PER; ++e) {
+        const uint32_t kk = keys[t0 + e];
+        const bool in = kk != 0 && (kk & mask) == prefix;
+        const int d = in ? (int)((kk >> shift) & 255u) : 256;
+        const unsigned grp = __match_any_sync(0xffffffffu, d);
+        if (in && lane == __ffs(grp) - 1) atomicAdd(&h[d], __popc(grp));
+      }
+      __syncthreads();
+      if (threadIdx.x < 32) find_digit_desc(h, need, &sm_misc[0], &sm_misc[1]);
+      __syncthreads();
+      const int d = sm_misc[0];
+      const int hd = h[d];
+      need -= sm_misc[1];
+      prefix |= (uint32_t)d << shift;
+      mask |= 0xFFu << shift;
+      __syncthreads();
+      if (need == hd) {
+        early = true;
+        break;
+      }
+    }
+  }
+  // emit: above the threshold in any order, ties by position (ordered scan)
+  if (threadIdx.x == 0) sm_misc[2] = 0;
+  __syncthreads();
+  const int n_gt = (take_all || early) ? 0 : k - need;
+  int eqc = 0;
+#pragma unroll 4
+  for (int e = 0; e < PER; ++e) {
+    const uint32_t kk = keys[t0 + e];
+    if (kk == 0) continue;
+    const bool sel = take_all ? true : (early ? kk >= prefix : kk > prefix);
+    if (sel) {
+      const int p = atomicAdd(&sm_misc[2], 1);
+      if (p < k) outr[p] = t0 + e;
+    } else if (!take_all && !early && kk == prefix) {
+      ++eqc;
+    }
+  }
+  int tot;
+  int rank = block_excl_scan_1024(eqc, sm_scan, &tot);
+  if (!take_all && !early && eqc) {
+    for (int e = 0; e < PER; ++e) {
+      if (keys[t0 + e] != prefix) continue;
+      if (rank < need) outr[n_gt + rank] = t0 + e;
+      ++rank;
+    }
+  }
+  __syncthreads();
+  const int written = (take_all || early) ? sm_misc[2] : k;
+  for (int i = written + threadIdx.x; i < k; i += kRowThreads) outr[i] = -1;
+}
+
 // ---------------------------------------------------------------- FP16 select
 constexpr int kF16MaxRow = 16384;
 
@@ -809,6 +944,19 @@ dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
   while ((c.stride + chunk - 1) / chunk > 65535) chunk *= 2;
   const int64_t nchunks = std::max<int64_t>(1, (c.stride + chunk - 1) / chunk);
   if (nchunks > 65535 || c.R > 65535) return DSA_ERR_UNSUPPORTED;
+  if (!c.histogram && c.stride <= kSmemRow) {
+    // short rows, no histogram: one CTA per row, the row held in shared memory
+    const int smem = kSmemRow * 4;
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(row_topk_kernel), smem))
+      return DSA_ERR_CUDA;
+    row_topk_kernel<<<c.R, kRowThreads, smem, st>>>(c.logits, c.stride, c.context_lens, c.next_n,
+                                                    c.len_div, c.k, c.out_idx, status);
+    dsa_status_t e = check_launch();
+    if (e == DSA_OK && c.fallback_flags)
+      e = cudaMemsetAsync(c.fallback_flags, 0, sizeof(int32_t) * c.R, st) == cudaSuccess
+              ? DSA_OK : DSA_ERR_CUDA;
+    return e;
+  }
   int32_t *hist = c.histogram;
   bool reset = c.reset_histogram;
   if (!hist) {

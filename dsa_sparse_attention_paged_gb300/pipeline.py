@@ -4,10 +4,11 @@
 cross-referenced SGLang commit 7e252c5): it is built once per shape, owns the
 step's device buffers and the workspace, and each ``step`` runs
 
-  source layer   paged MQA logits + fused coarse histogram        (1 launch)
-                 histogram-driven exact top-k (resets the hist)   (1 launch)
-  level one      block amax8 (rows with nb <= kb skipped)          (1 launch)
-  (two-level)    block top-kb of the maxima                         (2 launches)
+  source layer   paged MQA logits + fused coarse histogram + fused
+                 block maxima over 8 scores                        (1 launch)
+                 histogram-driven exact top-k (resets the hist)   (2 launches)
+  level one      top-kb of the block maxima                        (1 launch,
+                 3 when a row has more than 16384 blocks)
                  sort_candidate_blocks -> table, phys, valid lens   (1 launch)
   consumer       sparse MQA logits over the table, FP16 output      (1 launch)
                  FP16 top-k with the fused table transform          (1 launch)
@@ -20,13 +21,11 @@ from __future__ import annotations
 
 import torch
 
-from . import (OUT_F16, Workspace, block_amax8, coarse_hist_topk, paged_mqa_logits,
-               sort_candidate_blocks, sparse_mqa_logits, topk_fp16)
+from . import (OUT_F16, Workspace, coarse_hist_topk, paged_mqa_logits, sort_candidate_blocks,
+               sparse_mqa_logits, topk_fp16)
 
 
 class DecodePlan:
-    LAUNCHES_DENSE = 2
-    LAUNCHES_TWO_LEVEL = 6
 
     def __init__(self, B, next_n, max_context, page_size, k=2048, kb=512, two_level=True,
                  device="cuda"):
@@ -52,7 +51,11 @@ class DecodePlan:
 
     @property
     def launches_per_step(self) -> int:
-        return self.LAUNCHES_DENSE + (self.LAUNCHES_TWO_LEVEL if self.two_level else 0)
+        """Kernels of this library launched by one step."""
+        n = 1 + 2  # logits (+ histogram, + block maxima), top-k levels 0 and 1
+        if self.two_level:
+            n += (1 if self.amax_stride <= 16384 else 3) + 1 + 1 + 1
+        return n
 
     def step(self, q, kv, kscale, weights, page_table, context_lens, events=None):
         """Run one decode step.  ``events`` (optional dict name -> (start, end)
@@ -65,7 +68,9 @@ class DecodePlan:
 
         mark("logits", 0)
         paged_mqa_logits(q, kv, kscale, weights, page_table, context_lens, nn, ws,
-                         logits=self.logits, histogram=self.hist)
+                         logits=self.logits, histogram=self.hist,
+                         amax=self.amax if self.two_level else None,
+                         amax_skip_if_blocks_le=self.kb)
         mark("logits", 1)
         mark("topk", 0)
         coarse_hist_topk(self.logits, context_lens, nn, self.k, ws, histogram=self.hist,
@@ -74,8 +79,6 @@ class DecodePlan:
         if not self.two_level:
             return self.topk_idx, None
         mark("publish", 0)
-        block_amax8(self.logits, context_lens, nn, ws, skip_if_blocks_le=self.kb,
-                    amax=self.amax)
         coarse_hist_topk(self.amax, context_lens, nn, self.kb, ws, histogram=None,
                          len_div=8, out=self.block_ids)
         sort_candidate_blocks(self.block_ids, context_lens, nn, page_table, self.page_size, ws,

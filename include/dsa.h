@@ -125,14 +125,21 @@ int32_t dsa_read_device_status(const void *workspace, void *stream, uint32_t *ou
  *                descend: bin 0 holds the largest scores; |x| < 16 uses the
  *                FP16-RN exponent and 4 mantissa bits, 16 <= |x| < 223 unit
  *                bins, |x| >= 223 one saturating bin at each end.
- * With or without the histogram the logits are bitwise identical. */
+ *   amax         NULL, or [B*next_n][amax_stride] float: the block maxima of
+ *                dsa_block_amax8 computed in the same pass ([SG38944]
+ *                amax8_varlen), bitwise equal to that entry point's output;
+ *                rows with at most amax_skip_if_blocks_le blocks are skipped
+ *                when that is > 0.
+ * With or without the histogram and block maxima the logits are bitwise
+ * identical. */
 int32_t dsa_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const float *kscale,
                              const float *weights, const int32_t *page_table,
                              int64_t page_table_stride, const int32_t *context_lens, int32_t B,
                              int32_t next_n, int32_t num_heads, int32_t head_dim,
                              int32_t page_size, int32_t num_pages, float *logits,
-                             int64_t logits_stride, int32_t *histogram, void *workspace,
-                             size_t ws_bytes, void *stream);
+                             int64_t logits_stride, int32_t *histogram, float *amax,
+                             int64_t amax_stride, int32_t amax_skip_if_blocks_le,
+                             void *workspace, size_t ws_bytes, void *stream);
 
 /* ---- histogram-driven exact top-k ---------------------------------------
  * SGLang commit 7e252c5 (select.cuh, cross-referenced from [DG94]): per row,

@@ -48,12 +48,13 @@ MIS = ctypes.c_void_p(0x10004)
 
 def paged(lib, **kw):
     a = dict(q=A16, kv=A16, ks=A16, w=A16, pt=A16, pts=4, ctx=A16, B=2, nn=1, H=32, D=128,
-             ps=64, P=10, out=A16, ostride=256, hist=None, ws=ctypes.c_void_p(0x20000),
-             wsb=4096, st=None)
+             ps=64, P=10, out=A16, ostride=256, hist=None, amax=None, astride=0, askip=0,
+             ws=ctypes.c_void_p(0x20000), wsb=4096, st=None)
     a.update(kw)
     return lib.dsa_paged_mqa_logits(a["q"], a["kv"], a["ks"], a["w"], a["pt"], a["pts"], a["ctx"],
                                     a["B"], a["nn"], a["H"], a["D"], a["ps"], a["P"], a["out"],
-                                    a["ostride"], a["hist"], a["ws"], a["wsb"], a["st"])
+                                    a["ostride"], a["hist"], a["amax"], a["astride"], a["askip"],
+                                    a["ws"], a["wsb"], a["st"])
 
 
 def test_paged_logits_argument_checks(lib):
@@ -70,6 +71,7 @@ def test_paged_logits_argument_checks(lib):
     assert paged(lib, q=None) == 1
     assert paged(lib, B=-1) == 1
     assert paged(lib, ostride=0) == 1
+    assert paged(lib, amax=A16, astride=0) == 1
     assert paged(lib, B=0) == 0          # nothing to do, nothing launched
 
 

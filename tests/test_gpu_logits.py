@@ -109,3 +109,33 @@ def test_bad_page_id_is_flagged_not_faulted():
     assert ws.status() & D.DEV_BOUNDS
     ws.init()
     assert ws.status() == 0
+
+
+@pytest.mark.parametrize("B,nn,ctx,ps,skip", [
+    (3, 1, [4097, 9000, 130], 64, 0),
+    (3, 1, [4097, 9000, 130], 64, 512),
+    (2, 4, [3001, 700], 128, 64),
+])
+def test_fused_block_maxima_equal_block_amax8(B, nn, ctx, ps, skip):
+    """Block maxima written by the logits kernel are bitwise those of
+    dsa_block_amax8 on the same logits, and of the oracle."""
+    import dsa_sparse_attention_paged_gb300 as D
+    case = make(B, nn, ctx, ps, "mixed", seed=55 + skip)
+    d = to_dev(case)
+    R = B * nn
+    stride = (max(ctx) + 7) // 8 * 8
+    ws = D.Workspace(R)
+    logits = torch.full((R, stride), float("nan"), dtype=torch.float32, device="cuda")
+    fused = torch.full((R, stride // 8), -3.0, dtype=torch.float32, device="cuda")
+    D.paged_mqa_logits(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"],
+                       d["context_lens"], nn, ws, logits=logits, amax=fused,
+                       amax_skip_if_blocks_le=skip)
+    sep = torch.full((R, stride // 8), -3.0, dtype=torch.float32, device="cuda")
+    D.block_amax8(logits, d["context_lens"], nn, ws, skip_if_blocks_le=skip, amax=sep)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    np.testing.assert_array_equal(fused.cpu().numpy(), sep.cpu().numpy())
+    live, rl = live_mask(case["context_lens"], nn, stride)
+    L = np.where(live, logits.cpu().numpy(), np.nan).astype(np.float32)
+    ref = O.block_amax8(L, rl, skip_le=skip, amax_stride=stride // 8, fill=-3.0)
+    np.testing.assert_array_equal(fused.cpu().numpy(), ref)

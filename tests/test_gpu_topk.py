@@ -50,10 +50,13 @@ def test_topk_matches_oracle(B, nn, ctx, ps, dist, k):
     assert (hist.cpu().numpy() == 0).all(), "reset_histogram left counts behind"
 
 
-def test_topk_without_histogram_builds_its_own():
+@pytest.mark.parametrize("longest", [12000, 20000])
+def test_topk_without_histogram_builds_its_own(longest):
+    """Rows that fit in shared memory take the one-CTA select; longer rows
+    build their histogram in the workspace first."""
     import dsa_sparse_attention_paged_gb300 as D
-    case = make(3, 1, [7000, 12000, 300], 64, "mixed", seed=5)
-    d, ws, logits, hist = _logits_and_hist(case, 12000)
+    case = make(3, 1, [7000, longest, 300], 64, "mixed", seed=5)
+    d, ws, logits, hist = _logits_and_hist(case, longest)
     out = D.coarse_hist_topk(logits, d["context_lens"], 1, 2048, ws, histogram=None)
     out2 = D.coarse_hist_topk(logits, d["context_lens"], 1, 2048, ws, histogram=None)
     torch.cuda.synchronize()
