@@ -36,6 +36,8 @@ __device__ __forceinline__ float key_to_f32(uint32_t key) {
 __global__ void __launch_bounds__(kAmaxThreads)
     amax8_kernel(const float *logits, int64_t stride, const int32_t *ctx, int next_n,
                  int skip_le, float *amax, int64_t amax_stride, uint32_t *status) {
+  pdl_wait();  // predecessor grids complete before any global access
+  pdl_launch_dependents();
   const int r = blockIdx.y;
   int64_t n = live_len(ctx, next_n, r);
   if (n > stride) {
@@ -97,6 +99,8 @@ __global__ void __launch_bounds__(kSortThreads)
     sort_blocks_kernel(int32_t *ids, int kb, const int32_t *ctx, int next_n,
                        const int32_t *page_table, int64_t pt_stride, int page_size,
                        int32_t *phys, int32_t *valid_lens, uint32_t *status) {
+  pdl_wait();  // predecessor grids complete before any global access
+  pdl_launch_dependents();
   __shared__ uint32_t bm[kMaxBitmapWords];
   __shared__ int sm_scan[kSortThreads / 32 + 1];
   __shared__ long long sm_live[kSortThreads / 32];
@@ -195,18 +199,17 @@ dsa_status_t run_block_amax8(const float *logits, int64_t stride, const int32_t 
   const int64_t nbmax = (stride + 7) / 8;
   const int64_t gx = (nbmax + kAmaxThreads - 1) / kAmaxThreads;
   if (gx > 0x7fffffff || R > 65535) return DSA_ERR_UNSUPPORTED;
-  amax8_kernel<<<dim3((unsigned)std::max<int64_t>(1, gx), (unsigned)R), kAmaxThreads, 0, st>>>(
-      logits, stride, context_lens, next_n, skip_le, amax, amax_stride, status);
-  return check_launch();
+  return launch_pdl(amax8_kernel, dim3((unsigned)std::max<int64_t>(1, gx), (unsigned)R),
+                    dim3(kAmaxThreads), 0, st, logits, stride, context_lens, next_n, skip_le, amax,
+                    amax_stride, status);
 }
 
 dsa_status_t run_sort_blocks(int32_t *ids, int32_t kb, const int32_t *context_lens,
                              int32_t next_n, int32_t R, const int32_t *page_table,
                              int64_t pt_stride, int32_t page_size, int32_t *phys,
                              int32_t *valid_lens, uint32_t *status, cudaStream_t st) {
-  sort_blocks_kernel<<<R, kSortThreads, 0, st>>>(ids, kb, context_lens, next_n, page_table,
-                                                  pt_stride, page_size, phys, valid_lens, status);
-  return check_launch();
+  return launch_pdl(sort_blocks_kernel, dim3(R), dim3(kSortThreads), 0, st, ids, kb, context_lens,
+                    next_n, page_table, pt_stride, page_size, phys, valid_lens, status);
 }
 
 }  // namespace dsa

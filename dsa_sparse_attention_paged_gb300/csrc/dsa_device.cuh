@@ -53,6 +53,17 @@ __device__ __forceinline__ uint32_t lane_id() {
   return l;
 }
 
+// ---------------------------------------------------------------- launches
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while its predecessor on the stream finishes.
+// pdl_wait() blocks until every predecessor grid has completed and its memory
+// is visible; each kernel calls it before touching global memory.
+// pdl_launch_dependents() lets the next kernel on the stream start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

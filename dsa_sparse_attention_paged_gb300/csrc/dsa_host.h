@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "dsa.h"  // include/ is on the include path
 
 namespace dsa {
@@ -80,12 +82,38 @@ dsa_status_t run_bins_range(uint32_t start, int64_t count, int16_t *out, cudaStr
 dsa_status_t run_fp16_keys(const uint16_t *in, uint16_t *out, int64_t n, cudaStream_t st);
 dsa_status_t run_wait_selftest(uint64_t limit, uint32_t *status, cudaStream_t st);
 
+void record_cuda_error(cudaError_t e);
+
+// Launch with programmatic stream serialisation (see pdl_wait in
+// dsa_device.cuh): the kernel may be scheduled while the previous kernel on
+// the stream drains; it waits for it before reading or writing memory.
+template <typename... KArgs, typename... Args>
+dsa_status_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                        cudaStream_t st, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    (void)cudaGetLastError();
+    return DSA_ERR_CUDA;
+  }
+  return DSA_OK;
+}
+
 // --- utilities (api.cu) ---
 dsa_status_t make_tmap_rows128(CUtensorMap *map, const void *base, uint64_t rows,
                                uint32_t box_rows);
 int num_sms();
 bool ensure_smem_attr(const void *fn, int bytes);
 dsa_status_t check_launch();
-void record_cuda_error(cudaError_t e);
 
 }  // namespace dsa

@@ -274,6 +274,8 @@ template <int NN, bool SPARSE, bool OUT_F16, bool HIST>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const LogitsArgs a) {
+  pdl_wait();  // predecessor grids complete before any global access
+  pdl_launch_dependents();
   constexpr int N = 32 * NN;
   constexpr uint32_t IDESC = idesc_e4m3_f32(128, N);
   constexpr int HS = hist_slots_per_group(NN);
@@ -731,8 +733,7 @@ dsa_status_t launch_one(const CUtensorMap &tk, const CUtensorMap &tq, const Logi
   a.num_stages = L.stages;
   auto kfn = logits_kernel<NN, SPARSE, OUT_F16, HIST>;
   if (!ensure_smem_attr(reinterpret_cast<const void *>(kfn), L.smem)) return DSA_ERR_CUDA;
-  kfn<<<grid, kThreads, L.smem, st>>>(tk, tq, a);
-  return check_launch();
+  return launch_pdl(kfn, dim3(grid), dim3(kThreads), (size_t)L.smem, st, tk, tq, a);
 }
 
 }  // namespace

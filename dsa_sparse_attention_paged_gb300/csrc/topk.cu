@@ -358,6 +358,8 @@ __device__ void block_radix_topk_row(const float *row, int64_t n, int k, int32_t
 __global__ void __launch_bounds__(kSelThreads)
     hist_build_kernel(const float *logits, int64_t stride, const int32_t *ctx, int next_n,
                       int len_div, int64_t chunk, int32_t *hist, uint32_t *status) {
+  pdl_wait();  // predecessor grids complete before any global access
+  pdl_launch_dependents();
   __shared__ int h[DSA_NUM_BINS];
   const int r = blockIdx.y;
   for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kSelThreads) h[i] = 0;
@@ -433,6 +435,8 @@ __device__ void threshold_from_hist(const int32_t *h, int need, int *sm_scan, in
 // fine bin over capacity) runs the exact whole-row fallback.
 template <int LEVEL>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
+  pdl_wait();  // predecessor grids complete before any global access
+  pdl_launch_dependents();
   extern __shared__ unsigned long long sm_dyn[];  // fine hist (pass) / candidates (refine)
   __shared__ int sm_h[256];
   __shared__ int sm_scan[kSelWarps + 1];
@@ -702,6 +706,8 @@ __device__ __forceinline__ int block_excl_scan_1024(int v, int *ws, int *total) 
 __global__ void __launch_bounds__(kRowThreads)
     row_topk_kernel(const float *logits, int64_t stride, const int32_t *ctx, int next_n,
                     int len_div, int k, int32_t *out, uint32_t *status) {
+  pdl_wait();  // predecessor grids complete before any global access
+  pdl_launch_dependents();
   extern __shared__ uint32_t keys[];  // [kSmemRow]
   __shared__ int h[256];
   __shared__ int sm_scan[kRowWarps + 1];
@@ -715,23 +721,27 @@ __global__ void __launch_bounds__(kRowThreads)
   }
   const float *row = logits + (int64_t)r * stride;
   int32_t *outr = out + (int64_t)r * k;
-  // order keys; NaN and positions past the row become key 0 (never chosen)
+  // order keys; NaN and positions past the row become key 0 (never chosen).
+  // Thread tid owns positions e * kRowThreads + tid: all loads in flight at
+  // once, and conflict-free shared-memory access in the radix passes.
+  constexpr int PER = kSmemRow / kRowThreads;
   const int nn = (int)n;
-  for (int t = threadIdx.x; t < kSmemRow; t += kRowThreads) {
-    uint32_t kk = 0;
-    if (t < nn) {
-      const float x = row[t];
-      kk = isnan(x) ? 0u : f32_order_key(x);
+  {
+    float xv[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int t = e * kRowThreads + threadIdx.x;
+      xv[e] = (t < nn) ? row[t] : __int_as_float(0x7fffffff);
     }
-    keys[t] = kk;
+#pragma unroll
+    for (int e = 0; e < PER; ++e)
+      keys[e * kRowThreads + threadIdx.x] = isnan(xv[e]) ? 0u : f32_order_key(xv[e]);
   }
-  constexpr int PER = kSmemRow / kRowThreads;  // keys per thread, contiguous
-  const int t0 = threadIdx.x * PER;
   __syncthreads();
   // valid count (key 0 is only ever NaN or padding: -inf has key 0x007FFFFF)
   int valid = 0;
 #pragma unroll
-  for (int e = 0; e < PER; ++e) valid += (keys[t0 + e] != 0);
+  for (int e = 0; e < PER; ++e) valid += (keys[e * kRowThreads + threadIdx.x] != 0);
   int nvalid;
   (void)block_excl_scan_1024(valid, sm_scan, &nvalid);
   uint32_t prefix = 0, mask = 0;
@@ -743,7 +753,7 @@ __global__ void __launch_bounds__(kRowThreads)
       __syncthreads();
 #pragma unroll 4
       for (int e = 0; e < PER; ++e) {
-        const uint32_t kk = keys[t0 + e];
+        const uint32_t kk = keys[e * kRowThreads + threadIdx.x];
         const bool in = kk != 0 && (kk & mask) == prefix;
         const int d = in ? (int)((kk >> shift) & 255u) : 256;
         const unsigned grp = __match_any_sync(0xffffffffu, d);
@@ -771,19 +781,28 @@ __global__ void __launch_bounds__(kRowThreads)
   int eqc = 0;
 #pragma unroll 4
   for (int e = 0; e < PER; ++e) {
-    const uint32_t kk = keys[t0 + e];
+    const int t = e * kRowThreads + threadIdx.x;
+    const uint32_t kk = keys[t];
     if (kk == 0) continue;
     const bool sel = take_all ? true : (early ? kk >= prefix : kk > prefix);
     if (sel) {
       const int p = atomicAdd(&sm_misc[2], 1);
-      if (p < k) outr[p] = t0 + e;
+      if (p < k) outr[p] = t;
     } else if (!take_all && !early && kk == prefix) {
       ++eqc;
     }
   }
+  // ties at the threshold key, lowest positions first: here each thread
+  // takes a contiguous run of positions so a block scan orders them
+  const bool ties = !take_all && !early;
+  const int t0 = threadIdx.x * PER;
+  eqc = 0;
+  if (ties) {
+    for (int e = 0; e < PER; ++e) eqc += (keys[t0 + e] == prefix);
+  }
   int tot;
   int rank = block_excl_scan_1024(eqc, sm_scan, &tot);
-  if (!take_all && !early && eqc) {
+  if (ties && eqc) {
     for (int e = 0; e < PER; ++e) {
       if (keys[t0 + e] != prefix) continue;
       if (rank < need) outr[n_gt + rank] = t0 + e;
@@ -801,6 +820,8 @@ constexpr int kF16MaxRow = 16384;
 __global__ void __launch_bounds__(kSelThreads)
     topk_fp16_kernel(const uint16_t *scores, int64_t stride, const int32_t *valid_lens, int k,
                      const int32_t *table, int kb, int32_t *out, uint32_t *status) {
+  pdl_wait();  // predecessor grids complete before any global access
+  pdl_launch_dependents();
   __shared__ uint32_t keys2[kF16MaxRow / 2];  // two 16-bit keys per word
   __shared__ int h[DSA_NUM_BINS];
   __shared__ int sm_scan[kSelWarps + 1];
@@ -816,14 +837,32 @@ __global__ void __launch_bounds__(kSelThreads)
   const int nw = (int)((n + 1) / 2);
   for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kSelThreads) h[i] = 0;
   __syncthreads();
-  // keys, with positions >= n masked to the invalid key 0; coarse histogram
-  for (int w = threadIdx.x; w < nw; w += kSelThreads) {
-    uint32_t kk = f16x2_order_keys(row[w]);
-    if (2 * w + 1 >= n) kk &= 0x0000FFFFu;
-    keys2[w] = kk;
-    const uint32_t lo = kk & 0xFFFFu, hi = kk >> 16;
-    if (lo) atomicAdd(&h[lo >> 6], 1);
-    if (hi) atomicAdd(&h[hi >> 6], 1);
+  // keys, with positions >= n masked to the invalid key 0 (all loads issued
+  // first); coarse histogram with per-warp aggregation of equal bins
+  constexpr int WPT = kF16MaxRow / 2 / kSelThreads;  // words per thread
+  {
+    uint32_t wv[WPT];
+#pragma unroll
+    for (int e = 0; e < WPT; ++e) {
+      const int w = e * kSelThreads + threadIdx.x;
+      wv[e] = (w < nw) ? row[w] : 0u;
+    }
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int e = 0; e < WPT; ++e) {
+      const int w = e * kSelThreads + threadIdx.x;
+      uint32_t kk = (w < nw) ? f16x2_order_keys(wv[e]) : 0u;
+      if (2 * w + 1 >= n) kk &= 0x0000FFFFu;
+      if (w >= nw) kk = 0;
+      keys2[w] = kk;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t key = hh ? (kk >> 16) : (kk & 0xFFFFu);
+        const int b = key ? (int)(key >> 6) : DSA_NUM_BINS;
+        const unsigned grp = __match_any_sync(0xffffffffu, b);
+        if (key && lane == __ffs(grp) - 1) atomicAdd(&h[b], __popc(grp));
+      }
+    }
   }
   __syncthreads();
   // threshold among 1024 coarse bins, searching from the top (bin 1023)
@@ -856,11 +895,17 @@ __global__ void __launch_bounds__(kSelThreads)
     // refine the remaining 6 bits inside bin T10
     if (threadIdx.x < 64) h[threadIdx.x] = 0;
     __syncthreads();
-    for (int w = threadIdx.x; w < nw; w += kSelThreads) {
-      const uint32_t kk = keys2[w];
-      const uint32_t lo = kk & 0xFFFFu, hi = kk >> 16;
-      if (lo && (int)(lo >> 6) == T10) atomicAdd(&h[lo & 63], 1);
-      if (hi && (int)(hi >> 6) == T10) atomicAdd(&h[hi & 63], 1);
+    const int lane = threadIdx.x & 31;
+#pragma unroll 4
+    for (int e = 0; e < WPT; ++e) {
+      const uint32_t kk = keys2[e * kSelThreads + threadIdx.x];  // 0 past the row
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t key = hh ? (kk >> 16) : (kk & 0xFFFFu);
+        const int d = (key && (int)(key >> 6) == T10) ? (int)(key & 63) : 64;
+        const unsigned grp = __match_any_sync(0xffffffffu, d);
+        if (d < 64 && lane == __ffs(grp) - 1) atomicAdd(&h[d], __popc(grp));
+      }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -949,9 +994,9 @@ dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
     const int smem = kSmemRow * 4;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(row_topk_kernel), smem))
       return DSA_ERR_CUDA;
-    row_topk_kernel<<<c.R, kRowThreads, smem, st>>>(c.logits, c.stride, c.context_lens, c.next_n,
-                                                    c.len_div, c.k, c.out_idx, status);
-    dsa_status_t e = check_launch();
+    dsa_status_t e = launch_pdl(row_topk_kernel, dim3(c.R), dim3(kRowThreads), (size_t)smem, st,
+                                c.logits, c.stride, c.context_lens, c.next_n, c.len_div, c.k,
+                                c.out_idx, status);
     if (e == DSA_OK && c.fallback_flags)
       e = cudaMemsetAsync(c.fallback_flags, 0, sizeof(int32_t) * c.R, st) == cudaSuccess
               ? DSA_OK : DSA_ERR_CUDA;
@@ -962,9 +1007,9 @@ dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
   if (!hist) {
     hist = ws_hist;  // zero by contract; the select below clears it again
     reset = true;
-    hist_build_kernel<<<dim3((unsigned)nchunks, (unsigned)c.R), kSelThreads, 0, st>>>(
-        c.logits, c.stride, c.context_lens, c.next_n, c.len_div, chunk, hist, status);
-    dsa_status_t e = check_launch();
+    dsa_status_t e = launch_pdl(hist_build_kernel, dim3((unsigned)nchunks, (unsigned)c.R),
+                                dim3(kSelThreads), 0, st, c.logits, c.stride, c.context_lens,
+                                c.next_n, c.len_div, chunk, hist, status);
     if (e != DSA_OK) return e;
   }
   SelArgs a;
@@ -988,17 +1033,14 @@ dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
       !ensure_smem_attr(reinterpret_cast<const void *>(select_kernel<1>), kSelSmem))
     return DSA_ERR_CUDA;
   const dim3 grid((unsigned)nchunks, (unsigned)c.R);
-  select_kernel<0><<<grid, kSelThreads, kSelSmem, st>>>(a);
-  dsa_status_t e = check_launch();
+  dsa_status_t e = launch_pdl(select_kernel<0>, grid, dim3(kSelThreads), (size_t)kSelSmem, st, a);
   if (e != DSA_OK) return e;
-  select_kernel<1><<<grid, kSelThreads, kSelSmem, st>>>(a);
-  return check_launch();
+  return launch_pdl(select_kernel<1>, grid, dim3(kSelThreads), (size_t)kSelSmem, st, a);
 }
 
 dsa_status_t run_topk_fp16(const Fp16TopkCall &c, cudaStream_t st) {
-  topk_fp16_kernel<<<c.R, kSelThreads, 0, st>>>(c.scores, c.stride, c.valid_lens, c.k,
-                                                c.block_table, c.kb, c.out_idx, c.status);
-  return check_launch();
+  return launch_pdl(topk_fp16_kernel, dim3(c.R), dim3(kSelThreads), 0, st, c.scores, c.stride,
+                    c.valid_lens, c.k, c.block_table, c.kb, c.out_idx, c.status);
 }
 
 }  // namespace dsa
