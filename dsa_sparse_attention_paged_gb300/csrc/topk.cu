@@ -839,21 +839,23 @@ __global__ void __launch_bounds__(kSelThreads)
   __syncthreads();
   // keys, with positions >= n masked to the invalid key 0 (all loads issued
   // first); coarse histogram with per-warp aggregation of equal bins
-  constexpr int WPT = kF16MaxRow / 2 / kSelThreads;  // words per thread
-  {
-    uint32_t wv[WPT];
+  // words are handled in rounds of 4 per thread (all 4 loads in flight);
+  // the round count depends only on the row, so every lane runs it
+  constexpr int WR = 4;
+  const int rounds = (nw + WR * kSelThreads - 1) / (WR * kSelThreads);
+  const int lane = threadIdx.x & 31;
+  for (int rd = 0; rd < rounds; ++rd) {
+    uint32_t wv[WR];
 #pragma unroll
-    for (int e = 0; e < WPT; ++e) {
-      const int w = e * kSelThreads + threadIdx.x;
+    for (int e = 0; e < WR; ++e) {
+      const int w = (rd * WR + e) * kSelThreads + threadIdx.x;
       wv[e] = (w < nw) ? row[w] : 0u;
     }
-    const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int e = 0; e < WPT; ++e) {
-      const int w = e * kSelThreads + threadIdx.x;
+    for (int e = 0; e < WR; ++e) {
+      const int w = (rd * WR + e) * kSelThreads + threadIdx.x;
       uint32_t kk = (w < nw) ? f16x2_order_keys(wv[e]) : 0u;
       if (2 * w + 1 >= n) kk &= 0x0000FFFFu;
-      if (w >= nw) kk = 0;
       keys2[w] = kk;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -864,6 +866,7 @@ __global__ void __launch_bounds__(kSelThreads)
       }
     }
   }
+  const int nw_r = rounds * WR * kSelThreads;  // words written above (zero past the row)
   __syncthreads();
   // threshold among 1024 coarse bins, searching from the top (bin 1023)
   {
@@ -895,10 +898,8 @@ __global__ void __launch_bounds__(kSelThreads)
     // refine the remaining 6 bits inside bin T10
     if (threadIdx.x < 64) h[threadIdx.x] = 0;
     __syncthreads();
-    const int lane = threadIdx.x & 31;
-#pragma unroll 4
-    for (int e = 0; e < WPT; ++e) {
-      const uint32_t kk = keys2[e * kSelThreads + threadIdx.x];  // 0 past the row
+    for (int w0 = 0; w0 < nw_r; w0 += kSelThreads) {
+      const uint32_t kk = keys2[w0 + threadIdx.x];  // 0 past the row
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const uint32_t key = hh ? (kk >> 16) : (kk & 0xFFFFu);
