@@ -136,7 +136,7 @@ struct SelArgs {
 
 constexpr int kFineBits = 12;
 constexpr int kFineBins = 1 << kFineBits;
-constexpr int kSelSmem = kFineBins * 4;      // fine histogram (pass) / candidates (refine)
+constexpr int kSelSmem = 32768;              // fine histogram (pass) / candidates (refine)
 constexpr int kSmemCand = kSelSmem / 8;      // candidates refined from shared memory
 constexpr int kPerThread = 16;               // elements per thread per pass iteration
 constexpr int kIter = kSelThreads * kPerThread;
@@ -145,127 +145,151 @@ __device__ __forceinline__ unsigned long long cand_key(float x, int64_t t) {
   return ((unsigned long long)f32_order_key(x) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
 }
 
-// Coarse bin as a function of the FP32 order key, extended to NaN patterns so
-// it stays monotone: NaNs above +inf count as bin -1, NaNs below -inf as 1024.
-__device__ __forceinline__ int bin_of_key(uint32_t key) {
-  const uint32_t bits = (key & 0x80000000u) ? (key ^ 0x80000000u) : ~key;
-  const float x = __uint_as_float(bits);
-  if (isnan(x)) return (key & 0x80000000u) ? -1 : DSA_NUM_BINS;
-  return coarse_bin(x);
-}
-
-// Smallest order key whose bin is <= b (bins never increase with the key),
-// found by one warp with a 32-way search (about seven rounds).  Key 2^32
-// stands for "past the last key" and counts as satisfying the predicate.
-__device__ uint64_t first_key_with_bin_le(int b) {
-  const int lane = threadIdx.x & 31;
-  uint64_t lo = 0, hi = 1ull << 32;  // answer in [lo, hi]; hi satisfies the predicate
-  while (hi > lo) {
-    const uint64_t span = hi - lo;
-    uint64_t probe;
-    if (span <= 32) {
-      probe = lo + (uint64_t)lane;  // probe every key of [lo, hi)
-      if (probe > hi) probe = hi;
-    } else {
-      const uint64_t step = span / 32;
-      probe = (lane == 31) ? hi : lo + (uint64_t)(lane + 1) * step;
-    }
-    const bool t = (probe >= (1ull << 32)) || bin_of_key((uint32_t)probe) <= b;
-    const unsigned m = __ballot_sync(0xffffffffu, t);
-    const int f = __ffs(m) - 1;  // lane 31 (or the last probe) is always true
-    const uint64_t pf = __shfl_sync(0xffffffffu, probe, f);
-    if (span <= 32) return pf;
-    const uint64_t pprev = __shfl_sync(0xffffffffu, probe, f > 0 ? f - 1 : 0);
-    lo = (f == 0) ? lo : pprev + 1;
-    hi = pf;
-  }
-  return lo;
-}
-
-// Key range of bin T -> (first key, shift) so that (key - first) >> shift
-// spreads the bin over at most kFineBins fine bins, monotonically (see
-// fine_bin for the descending index).
-// Called by one full warp.
+// Fine bins of a coarse bin T: an enclosing range of |x| is known in closed
+// form from the bin rules (saturating: resolution spent on 223 <= |x| < 2^16;
+// unit bins: [n, n+1); FP16 bins: between the neighbouring half codes); the
+// range is mapped to order keys and spread over kFineBins fine bins.  The map
+// is clamped, so it stays monotone (and the select exact) whatever the range.
 __device__ void fine_map(int T, uint32_t *klo, int *shift) {
-  const uint64_t lo = first_key_with_bin_le(T);
-  const uint64_t hi = first_key_with_bin_le(T - 1) - 1;  // last key of bin T
-  const uint64_t span = hi - lo + 1;
+  const bool neg = T >= 512;
+  const int m = neg ? T - 512 : 511 - T;  // magnitude code
+  float alo, ahi;
+  if (m >= 511) {
+    alo = 223.0f;
+    ahi = 65536.0f;
+  } else if (m >= 304) {
+    alo = (m == 304) ? 15.99f : (float)(m - 288);
+    ahi = (float)(m - 287);
+  } else {
+    alo = (m == 0) ? 0.0f : __half2float(__ushort_as_half((unsigned short)(64 * m - 1)));
+    ahi = __half2float(__ushort_as_half((unsigned short)(64 * m + 64)));
+  }
+  const uint32_t k1 = f32_order_key(neg ? -ahi : alo);
+  const uint32_t k2 = f32_order_key(neg ? -alo : ahi);
+  const uint32_t lo = min(k1, k2), hi = max(k1, k2);
+  const uint64_t span = (uint64_t)(hi - lo) + 1;
   int bits = 0;
   while (bits < 33 && (1ull << bits) < span) ++bits;
-  if ((threadIdx.x & 31) == 0) {
-    *klo = (uint32_t)lo;
-    *shift = bits > kFineBits ? bits - kFineBits : 0;
-  }
+  *klo = lo;
+  *shift = bits > kFineBits ? bits - kFineBits : 0;
 }
 
 // Fine bin of a key inside bin T, descending like the coarse bins: fine bin 0
 // holds the largest keys of the bin.
 __device__ __forceinline__ int fine_bin(uint32_t key, uint32_t klo, int shift) {
-  return (kFineBins - 1) - (int)((key - klo) >> shift);
+  const int64_t off = (int64_t)key - (int64_t)klo;
+  const int64_t f = off <= 0 ? 0 : min((int64_t)(kFineBins - 1), off >> shift);
+  return (kFineBins - 1) - (int)f;
 }
 
-// Exact top-m of n unique 64-bit keys held in shared memory, emitted (as the
-// column in their low 32 bits, inverted) to out[0..m).  MSB radix select that
-// skips the bits all keys share and stops once a whole bucket is taken.
-__device__ void smem_refine(const unsigned long long *sc, int n, int m, int32_t *out,
-                            int *sm_h, int *sm_misc, unsigned long long *sm_u64) {
+__device__ __forceinline__ int bitlen64(unsigned long long v) { return v ? 64 - __clzll((long long)v) : 0; }
+
+// Threshold of the top m of the n keys keys[0..n) (key 0 = invalid), found by
+// a range-adaptive MSB radix select run by the whole block: every pass spreads
+// the active key range [lo, hi] over 256 digits, so bits all keys share cost
+// nothing and smooth data does not pile onto one counter.  Result:
+//   inclusive  -> the top m are exactly the valid keys >= thr
+//   !inclusive -> they are the n_gt keys > thr plus need_eq keys == thr
+// Scratch: h[256], red[2] (same type as the keys), imisc[8].
+template <typename K, int NT>
+__device__ void adaptive_threshold(const K *keys, int n, int m, int *h, K *red, int *imisc,
+                                   K &thr, int &n_gt, int &need_eq, bool &inclusive) {
+  const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    sm_u64[0] = ~0ull;
-    sm_u64[1] = 0ull;
+    red[0] = ~(K)0;
+    red[1] = 0;
+    imisc[0] = 0;
   }
   __syncthreads();
-  unsigned long long a = ~0ull, o = 0ull;
-  for (int i = threadIdx.x; i < n; i += kSelThreads) {
-    a &= sc[i];
-    o |= sc[i];
+  K lo = ~(K)0, hi = 0;
+  int cnt = 0;
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const K kk = keys[i];
+    if (kk == 0) continue;
+    lo = min(lo, kk);
+    hi = max(hi, kk);
+    ++cnt;
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    a &= __shfl_xor_sync(0xffffffffu, a, off);
-    o |= __shfl_xor_sync(0xffffffffu, o, off);
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, (K)__shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, (K)__shfl_xor_sync(0xffffffffu, hi, o));
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
   }
-  if ((threadIdx.x & 31) == 0) {
-    atomicAnd(&sm_u64[0], a);
-    atomicOr(&sm_u64[1], o);
+  if (lane == 0) {
+    atomicMin(&red[0], lo);
+    atomicMax(&red[1], hi);
+    atomicAdd(&imisc[0], cnt);
   }
   __syncthreads();
-  const unsigned long long diff = sm_u64[0] ^ sm_u64[1];
-  unsigned long long prefix = 0, mask = 0;
-  int need = m;
-  if (diff != 0 && m < n) {
-    const int hb = 63 - __clzll((long long)diff);
-    mask = (hb >= 63) ? 0ull : ~((2ull << hb) - 1);
-    prefix = sm_u64[0] & mask;
-    for (int top = hb; top >= 0; top -= 8) {
-      const int shift = top >= 7 ? top - 7 : 0;
-      const int width = top - shift + 1;
-      const unsigned long long dmask = ((1ull << width) - 1) << shift;
-      for (int i = threadIdx.x; i < 256; i += kSelThreads) sm_h[i] = 0;
-      __syncthreads();
-      for (int i = threadIdx.x; i < n; i += kSelThreads) {
-        const unsigned long long v = sc[i];
-        if ((v & mask) == prefix) atomicAdd(&sm_h[(int)((v & dmask) >> shift)], 1);
-      }
-      __syncthreads();
-      if (threadIdx.x < 32) find_digit_desc(sm_h, need, &sm_misc[4], &sm_misc[5]);
-      __syncthreads();
-      const int d = sm_misc[4];
-      if (d < 0) break;  // cannot happen for consistent inputs; take what is left
-      const int hd = sm_h[d];
-      need -= sm_misc[5];
-      prefix |= (unsigned long long)d << shift;
-      mask |= dmask;
-      __syncthreads();
-      if (need == hd) break;
-    }
-  } else {
-    prefix = 0;  // m >= n: take every candidate
+  lo = red[0];
+  hi = red[1];
+  const int nvalid = imisc[0];
+  __syncthreads();
+  n_gt = 0;
+  need_eq = 0;
+  if (nvalid <= m) {  // every valid key is taken
+    thr = 1;
+    inclusive = true;
+    return;
   }
+  int need = m;
+  while (true) {
+    if (lo == hi) {
+      thr = lo;
+      need_eq = need;
+      inclusive = false;
+      return;
+    }
+    const int shift = max(0, bitlen64((unsigned long long)(hi - lo)) - 8);
+    for (int i = threadIdx.x; i < 256; i += NT) h[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += NT) {
+      const K kk = keys[i];
+      if (kk == 0 || kk < lo || kk > hi) continue;
+      atomicAdd(&h[(int)((kk - lo) >> shift)], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) find_digit_desc(h, need, &imisc[1], &imisc[2]);
+    __syncthreads();
+    const int d = imisc[1];
+    const int hd = h[d];
+    n_gt += imisc[2];
+    need -= imisc[2];
+    const K nlo = lo + ((K)d << shift);
+    const K nhi = (shift >= (int)(8 * sizeof(K))) ? hi : min(hi, (K)(nlo + (((K)1 << shift) - 1)));
+    __syncthreads();
+    if (need == hd) {  // the whole digit is taken
+      thr = nlo;
+      inclusive = true;
+      return;
+    }
+    if (shift == 0) {  // one key value: ties
+      thr = nlo;
+      need_eq = need;
+      inclusive = false;
+      return;
+    }
+    lo = nlo;
+    hi = nhi;
+  }
+}
+
+// Exact top-m of n unique 64-bit keys (candidates: value order key << 32 |
+// inverted column), emitted as columns to out[0..m).
+__device__ void refine_candidates(const unsigned long long *sc, int n, int m, int32_t *out,
+                                  int *sm_h, int *sm_misc, unsigned long long *sm_u64) {
+  unsigned long long thr;
+  int n_gt, need_eq;
+  bool incl;
+  adaptive_threshold<unsigned long long, kSelThreads>(sc, n, m, sm_h, sm_u64, sm_misc, thr, n_gt,
+                                                      need_eq, incl);
   if (threadIdx.x == 0) sm_misc[6] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += kSelThreads) {
     const unsigned long long v = sc[i];
-    if (v >= prefix) {
+    if (v == 0) continue;
+    if (incl ? v >= thr : (v > thr || (v == thr && need_eq > 0))) {
       const int p = atomicAdd(&sm_misc[6], 1);
       if (p < m) out[p] = (int32_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
     }
@@ -490,14 +514,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
     for (int i = threadIdx.x; i < kFineBins; i += kSelThreads) fine_s[i] = 0;
   }
   if (overflow0) {
-    if (threadIdx.x < 32) {
+    if (threadIdx.x == 0) {
       uint32_t kl;
       int sh;
       fine_map(T, &kl, &sh);
-      if (threadIdx.x == 0) {
-        sm_misc[8] = (int)kl;
-        sm_misc[9] = sh;
-      }
+      sm_misc[8] = (int)kl;
+      sm_misc[9] = sh;
     }
     __syncthreads();
     klo = (uint32_t)sm_misc[8];
@@ -639,7 +661,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
         __syncthreads();
         src = sm_dyn;
       }
-      smem_refine(src, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
+      refine_candidates(src, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
     } else {
       for (int i = emitted + threadIdx.x; i < k; i += kSelThreads) outr[i] = -1;
     }
@@ -667,10 +689,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
 // ---------------------------------------------------------------- short rows
 // Rows of at most kSmemRow scores with no histogram given (the block maxima
 // of the two-level path): one CTA per row holds the row as FP32 order keys in
-// shared memory and runs an exact MSB radix select there -- no global
-// counters, no second launch.  Digit counts are aggregated per warp with
-// __match_any_sync, so skewed rows (many equal leading bytes) do not
-// serialise on one shared counter.
+// shared memory and runs the range-adaptive radix select there -- no global
+// counters, no second launch.
 constexpr int kSmemRow = 16384;
 constexpr int kRowThreads = 1024;
 constexpr int kRowWarps = kRowThreads / 32;
@@ -712,6 +732,7 @@ __global__ void __launch_bounds__(kRowThreads)
   __shared__ int h[256];
   __shared__ int sm_scan[kRowWarps + 1];
   __shared__ int sm_misc[8];
+  __shared__ uint32_t sm_red[2];
   const int r = blockIdx.x;
   const int lane = threadIdx.x & 31;
   int64_t n = row_len(ctx, next_n, len_div, r, stride, status);
@@ -738,79 +759,45 @@ __global__ void __launch_bounds__(kRowThreads)
       keys[e * kRowThreads + threadIdx.x] = isnan(xv[e]) ? 0u : f32_order_key(xv[e]);
   }
   __syncthreads();
-  // valid count (key 0 is only ever NaN or padding: -inf has key 0x007FFFFF)
-  int valid = 0;
-#pragma unroll
-  for (int e = 0; e < PER; ++e) valid += (keys[e * kRowThreads + threadIdx.x] != 0);
-  int nvalid;
-  (void)block_excl_scan_1024(valid, sm_scan, &nvalid);
-  uint32_t prefix = 0, mask = 0;
-  int need = k;
-  bool take_all = nvalid <= k, early = false;
-  if (!take_all) {
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      if (threadIdx.x < 256) h[threadIdx.x] = 0;
-      __syncthreads();
-#pragma unroll 4
-      for (int e = 0; e < PER; ++e) {
-        const uint32_t kk = keys[e * kRowThreads + threadIdx.x];
-        const bool in = kk != 0 && (kk & mask) == prefix;
-        const int d = in ? (int)((kk >> shift) & 255u) : 256;
-        const unsigned grp = __match_any_sync(0xffffffffu, d);
-        if (in && lane == __ffs(grp) - 1) atomicAdd(&h[d], __popc(grp));
-      }
-      __syncthreads();
-      if (threadIdx.x < 32) find_digit_desc(h, need, &sm_misc[0], &sm_misc[1]);
-      __syncthreads();
-      const int d = sm_misc[0];
-      const int hd = h[d];
-      need -= sm_misc[1];
-      prefix |= (uint32_t)d << shift;
-      mask |= 0xFFu << shift;
-      __syncthreads();
-      if (need == hd) {
-        early = true;
-        break;
-      }
-    }
-  }
+  // threshold of the top k (key 0 is only ever NaN or padding: -inf has key
+  // 0x007FFFFF)
+  uint32_t thr;
+  int n_gt, need_eq;
+  bool incl;
+  adaptive_threshold<uint32_t, kRowThreads>(keys, kSmemRow, k, h, sm_red, sm_misc, thr, n_gt,
+                                            need_eq, incl);
   // emit: above the threshold in any order, ties by position (ordered scan)
-  if (threadIdx.x == 0) sm_misc[2] = 0;
+  if (threadIdx.x == 0) sm_misc[3] = 0;
   __syncthreads();
-  const int n_gt = (take_all || early) ? 0 : k - need;
-  int eqc = 0;
 #pragma unroll 4
   for (int e = 0; e < PER; ++e) {
     const int t = e * kRowThreads + threadIdx.x;
     const uint32_t kk = keys[t];
     if (kk == 0) continue;
-    const bool sel = take_all ? true : (early ? kk >= prefix : kk > prefix);
-    if (sel) {
-      const int p = atomicAdd(&sm_misc[2], 1);
+    if (incl ? kk >= thr : kk > thr) {
+      const int p = atomicAdd(&sm_misc[3], 1);
       if (p < k) outr[p] = t;
-    } else if (!take_all && !early && kk == prefix) {
-      ++eqc;
     }
   }
   // ties at the threshold key, lowest positions first: here each thread
   // takes a contiguous run of positions so a block scan orders them
-  const bool ties = !take_all && !early;
+  const bool ties = !incl && need_eq > 0;
   const int t0 = threadIdx.x * PER;
-  eqc = 0;
+  int eqc = 0;
   if (ties) {
-    for (int e = 0; e < PER; ++e) eqc += (keys[t0 + e] == prefix);
+    for (int e = 0; e < PER; ++e) eqc += (keys[t0 + e] == thr);
   }
   int tot;
   int rank = block_excl_scan_1024(eqc, sm_scan, &tot);
   if (ties && eqc) {
     for (int e = 0; e < PER; ++e) {
-      if (keys[t0 + e] != prefix) continue;
-      if (rank < need) outr[n_gt + rank] = t0 + e;
+      if (keys[t0 + e] != thr) continue;
+      if (rank < need_eq) outr[n_gt + rank] = t0 + e;
       ++rank;
     }
   }
   __syncthreads();
-  const int written = (take_all || early) ? sm_misc[2] : k;
+  const int written = incl ? sm_misc[3] : k;
   for (int i = written + threadIdx.x; i < k; i += kRowThreads) outr[i] = -1;
 }
 
@@ -838,12 +825,11 @@ __global__ void __launch_bounds__(kSelThreads)
   for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kSelThreads) h[i] = 0;
   __syncthreads();
   // keys, with positions >= n masked to the invalid key 0 (all loads issued
-  // first); coarse histogram with per-warp aggregation of equal bins
+  // first); coarse histogram
   // words are handled in rounds of 4 per thread (all 4 loads in flight);
   // the round count depends only on the row, so every lane runs it
   constexpr int WR = 4;
   const int rounds = (nw + WR * kSelThreads - 1) / (WR * kSelThreads);
-  const int lane = threadIdx.x & 31;
   for (int rd = 0; rd < rounds; ++rd) {
     uint32_t wv[WR];
 #pragma unroll
@@ -857,13 +843,9 @@ __global__ void __launch_bounds__(kSelThreads)
       uint32_t kk = (w < nw) ? f16x2_order_keys(wv[e]) : 0u;
       if (2 * w + 1 >= n) kk &= 0x0000FFFFu;
       keys2[w] = kk;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t key = hh ? (kk >> 16) : (kk & 0xFFFFu);
-        const int b = key ? (int)(key >> 6) : DSA_NUM_BINS;
-        const unsigned grp = __match_any_sync(0xffffffffu, b);
-        if (key && lane == __ffs(grp) - 1) atomicAdd(&h[b], __popc(grp));
-      }
+      const uint32_t lo = kk & 0xFFFFu, hi = kk >> 16;
+      if (lo) atomicAdd(&h[lo >> 6], 1);
+      if (hi) atomicAdd(&h[hi >> 6], 1);
     }
   }
   const int nw_r = rounds * WR * kSelThreads;  // words written above (zero past the row)
@@ -900,13 +882,9 @@ __global__ void __launch_bounds__(kSelThreads)
     __syncthreads();
     for (int w0 = 0; w0 < nw_r; w0 += kSelThreads) {
       const uint32_t kk = keys2[w0 + threadIdx.x];  // 0 past the row
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t key = hh ? (kk >> 16) : (kk & 0xFFFFu);
-        const int d = (key && (int)(key >> 6) == T10) ? (int)(key & 63) : 64;
-        const unsigned grp = __match_any_sync(0xffffffffu, d);
-        if (d < 64 && lane == __ffs(grp) - 1) atomicAdd(&h[d], __popc(grp));
-      }
+      const uint32_t lo = kk & 0xFFFFu, hi = kk >> 16;
+      if (lo && (int)(lo >> 6) == T10) atomicAdd(&h[lo & 63], 1);
+      if (hi && (int)(hi >> 6) == T10) atomicAdd(&h[hi & 63], 1);
     }
     __syncthreads();
     if (threadIdx.x == 0) {
