@@ -253,11 +253,18 @@ __device__ void adaptive_threshold(const K *keys, int n, int m, int *h, K *red, 
     if (threadIdx.x < 32) find_digit_desc(h, need, &imisc[1], &imisc[2]);
     __syncthreads();
     const int d = imisc[1];
+    if (d < 0) {  // cannot happen for consistent counts: take what is active
+      __syncthreads();
+      thr = lo;
+      inclusive = true;
+      return;
+    }
     const int hd = h[d];
     n_gt += imisc[2];
     need -= imisc[2];
     const K nlo = lo + ((K)d << shift);
-    const K nhi = (shift >= (int)(8 * sizeof(K))) ? hi : min(hi, (K)(nlo + (((K)1 << shift) - 1)));
+    const K width = ((K)1 << shift) - 1;  // last key of the digit is nlo + width
+    const K nhi = (hi - nlo > width) ? (K)(nlo + width) : hi;  // no wrap-around
     __syncthreads();
     if (need == hd) {  // the whole digit is taken
       thr = nlo;
