@@ -250,11 +250,29 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
 
 // Sum over the 32 heads of one row: kscale, ReLU, head weight.  Four
 // independent accumulation chains (heads h = 4i + c go to chain c), combined
-// as (c0 + c1) + (c2 + c3).  Dense and sparse logits share this function, so
-// they are bitwise equal.
+// as (c0 + c1) + (c2 + c3).  For a finite kscale s >= 0, ReLU(d * s) = s *
+// ReLU(d), so s is applied once to the sum; any other s takes the formula
+// term by term.  Dense and sparse logits share this function, so they are
+// bitwise equal.
 __device__ __forceinline__ float head_sum(const uint32_t (&v)[32], float ks, const float *w) {
-  const uint64_t ks2 = pk2(ks, ks);
   uint64_t a01 = pk2(0.0f, 0.0f), a23 = pk2(0.0f, 0.0f);
+  if (ks >= 0.0f && ks <= 3.4028234e38f) {
+#pragma unroll
+    for (int h = 0; h < 32; h += 4) {
+      const float4 wv = *reinterpret_cast<const float4 *>(w + h);
+      a01 = fma2(pk2(wv.x, wv.y),
+                 pk2(fmaxf(__uint_as_float(v[h + 0]), 0.0f), fmaxf(__uint_as_float(v[h + 1]), 0.0f)),
+                 a01);
+      a23 = fma2(pk2(wv.z, wv.w),
+                 pk2(fmaxf(__uint_as_float(v[h + 2]), 0.0f), fmaxf(__uint_as_float(v[h + 3]), 0.0f)),
+                 a23);
+    }
+    float c0, c1, c2, c3;
+    upk2(a01, c0, c1);
+    upk2(a23, c2, c3);
+    return ks * ((c0 + c1) + (c2 + c3));
+  }
+  const uint64_t ks2 = pk2(ks, ks);
 #pragma unroll
   for (int h = 0; h < 32; h += 4) {
     const float4 wv = *reinterpret_cast<const float4 *>(w + h);
@@ -622,17 +640,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(KSE(kx));
       if (!(ok = ewait(AFULL(x), ra.ph))) break;
       tc_fence_after();
+      // head dots leave TMEM in batches of up to two rows (one wait per
+      // batch, bounded register use); the accumulator goes back to the MMA
+      // as soon as the last batch is in registers
       float acc[NN];
+      const uint32_t tcol = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)((2 * x + g) * N);
 #pragma unroll
-      for (int j = 0; j < NN; ++j) {
-        uint32_t v[32];
-        tmem_ld32(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)((2 * x + g) * N + j * 32), v);
+      for (int j0 = 0; j0 < NN; j0 += 2) {
+        constexpr int kB = 2;
+        uint32_t v[kB][32];
+#pragma unroll
+        for (int jj = 0; jj < kB; ++jj)
+          if (j0 + jj < NN) tmem_ld32(tcol + (uint32_t)((j0 + jj) * 32), v[jj]);
         tmem_ld_wait();
-        acc[j] = head_sum(v, ks, w_s + qb * N + j * 32);
+        if (j0 + kB >= NN) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(AEMPTY(x));
+        }
+#pragma unroll
+        for (int jj = 0; jj < kB; ++jj)
+          if (j0 + jj < NN) acc[j0 + jj] = head_sum(v[jj], ks, w_s + qb * N + (j0 + jj) * 32);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(AEMPTY(x));
 
       if (SPARSE) {
         if (pos < (int64_t)a.kb * 8) {
