@@ -54,6 +54,7 @@ struct TopkCall {
   int32_t *fallback_flags;
   void *workspace;
   int32_t ws_rows;           // rows the workspace was sized for
+  bool allow_cluster = true; // rows up to 131072 may take the cluster kernel
 };
 dsa_status_t run_topk(const TopkCall &c, cudaStream_t st);
 

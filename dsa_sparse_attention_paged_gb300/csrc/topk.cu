@@ -693,6 +693,246 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- cluster select
+// Rows of at most kClRow scores: one cluster of kCl CTAs per row, each CTA
+// holding its share of the row as order keys in registers (the row is read
+// from memory once).  The threshold bin comes from the caller's histogram
+// (or one the cluster builds from its registers); the row's counters and its
+// threshold-bin candidates live in the shared memory of CTA 0 of the
+// cluster and every CTA reaches them through distributed shared memory.  A
+// threshold bin over capacity gets its fine histogram the same way and is
+// resolved from the registers, without reading the row again.  CTA 0 then
+// checks the counts and refines the candidates exactly.  Every cluster-wide
+// decision is taken from data all CTAs share, so all CTAs pass the same
+// cluster barriers.
+constexpr int kCl = 8;
+constexpr int kClThreads = 512;
+constexpr int kClVpt = 32;                       // scores per thread
+constexpr int kClChunk = kClThreads * kClVpt;    // 16384 per CTA
+constexpr int kClRow = kCl * kClChunk;           // 131072
+
+struct ClSmem {
+  unsigned long long cand[DSA_CAND_CAP];  // CTA 0: the row's candidates
+  int chist[DSA_NUM_BINS];                // coarse histogram (local, then the row's)
+  int fine[kFineBins];                    // fine histogram (local, then the row's)
+  int ctr[4];                             // CTA 0: emitted, candidates, bin-T count
+};
+
+struct ClArgs {
+  const float *logits;
+  int64_t stride;
+  const int32_t *ctx;
+  int next_n, len_div;
+  int32_t *hist;  // NULL: the cluster builds it
+  int reset_hist;
+  int k;
+  int32_t *out;
+  int32_t *flags;
+  uint32_t *status;
+};
+
+__global__ void __launch_bounds__(kClThreads, 2) cluster_select_kernel(const ClArgs a) {
+  pdl_wait();  // predecessor grids complete before any global access
+  pdl_launch_dependents();
+  extern __shared__ __align__(16) unsigned char cl_raw[];
+  ClSmem &sm = *reinterpret_cast<ClSmem *>(cl_raw);
+  __shared__ int sm_h[256];
+  __shared__ int sm_scan[kSelWarps + 1];
+  __shared__ int sm_misc[16];
+  __shared__ unsigned long long sm_u64[2];
+  const uint32_t rank = cluster_ctarank();
+  const int r = blockIdx.y;
+  const int k = a.k;
+  const int lane = threadIdx.x & 31;
+  const int64_t n = row_len(a.ctx, a.next_n, a.len_div, r, a.stride, a.status);
+  const float *row = a.logits + (int64_t)r * a.stride;
+  int32_t *outr = a.out + (int64_t)r * k;
+  // this CTA's share: a multiple of 2048 positions
+  const int64_t chunk = ((n + kCl - 1) / kCl + 2047) / 2048 * 2048;
+  const int64_t c0 = (int64_t)rank * chunk;
+  const int64_t c1 = min(n, c0 + chunk);
+
+  for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) sm.chist[i] = 0;
+  for (int i = threadIdx.x; i < kFineBins; i += kClThreads) sm.fine[i] = 0;
+  if (threadIdx.x < 4) sm.ctr[threadIdx.x] = 0;
+  uint32_t key[kClVpt];
+#pragma unroll
+  for (int e = 0; e < kClVpt; ++e) {
+    const int64_t t = c0 + (int64_t)e * kClThreads + threadIdx.x;
+    const float x = (t < c1) ? row[t] : __int_as_float(0x7fffffff);
+    key[e] = isnan(x) ? 0u : f32_order_key(x);
+  }
+  const uint32_t ctr0 = dsmem_map(smem_u32(&sm.ctr[0]), 0);
+  const uint32_t cand0 = dsmem_map(smem_u32(&sm.cand[0]), 0);
+  cluster_sync();  // every CTA's shared state is zeroed before any remote access
+
+  // ---- the row's coarse histogram and its threshold bin
+  const int32_t *hsrc = a.hist ? a.hist + (int64_t)r * DSA_NUM_BINS : sm.chist;
+  if (!a.hist) {
+#pragma unroll
+    for (int e = 0; e < kClVpt; ++e) {
+      if (!key[e]) continue;
+      const uint32_t bits = (key[e] & 0x80000000u) ? (key[e] ^ 0x80000000u) : ~key[e];
+      atomicAdd(&sm.chist[coarse_bin(__uint_as_float(bits))], 1);
+    }
+    __syncthreads();
+    if (rank != 0) {
+      const uint32_t h0 = dsmem_map(smem_u32(&sm.chist[0]), 0);
+      for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads)
+        if (sm.chist[i]) dsmem_red_add(h0 + 4u * i, sm.chist[i]);
+    }
+    cluster_sync();
+    if (rank != 0) {
+      const uint32_t h0 = dsmem_map(smem_u32(&sm.chist[0]), 0);
+      for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) sm.chist[i] = dsmem_ld(h0 + 4u * i);
+    }
+    __syncthreads();
+  }
+  threshold_from_hist<DSA_NUM_BINS>(hsrc, k, sm_scan, sm_misc);
+  const int T = sm_misc[0];
+  const int above = sm_misc[1];
+  const int histT = sm_misc[2];
+  __syncthreads();
+  const bool overflow = (T < DSA_NUM_BINS) && histT > DSA_CAND_CAP;
+
+  // ---- a threshold bin over capacity: the row's fine histogram of bin T
+  uint32_t klo = 0;
+  int fshift = 0, S = 0, above1 = 0, fineS = 0;
+  if (overflow) {
+    if (threadIdx.x == 0) {
+      uint32_t kl;
+      int sh;
+      fine_map(T, &kl, &sh);
+      sm_misc[8] = (int)kl;
+      sm_misc[9] = sh;
+    }
+    __syncthreads();
+    klo = (uint32_t)sm_misc[8];
+    fshift = sm_misc[9];
+#pragma unroll
+    for (int e = 0; e < kClVpt; ++e) {
+      if (!key[e]) continue;
+      const uint32_t bits = (key[e] & 0x80000000u) ? (key[e] ^ 0x80000000u) : ~key[e];
+      if (coarse_bin(__uint_as_float(bits)) == T) atomicAdd(&sm.fine[fine_bin(key[e], klo, fshift)], 1);
+    }
+    __syncthreads();
+    if (rank != 0) {
+      const uint32_t f0 = dsmem_map(smem_u32(&sm.fine[0]), 0);
+      for (int i = threadIdx.x; i < kFineBins; i += kClThreads)
+        if (sm.fine[i]) dsmem_red_add(f0 + 4u * i, sm.fine[i]);
+    }
+    cluster_sync();
+    if (rank != 0) {
+      const uint32_t f0 = dsmem_map(smem_u32(&sm.fine[0]), 0);
+      for (int i = threadIdx.x; i < kFineBins; i += kClThreads) sm.fine[i] = dsmem_ld(f0 + 4u * i);
+    }
+    __syncthreads();
+    threshold_from_hist<kFineBins>(sm.fine, k - above, sm_scan, sm_misc + 10);
+    S = sm_misc[10];
+    above1 = sm_misc[11];
+    fineS = sm_misc[12];
+    __syncthreads();
+  }
+
+  // ---- emit the scores above the threshold, collect the threshold bin
+  // (kind: 1 above, 2 candidate, 4 counted in bin T)
+  uint32_t kinds = 0;
+  int ne = 0, nc = 0, nt = 0;
+#pragma unroll
+  for (int e = 0; e < kClVpt; ++e) {
+    if (!key[e]) continue;
+    const uint32_t bits = (key[e] & 0x80000000u) ? (key[e] ^ 0x80000000u) : ~key[e];
+    const int b = coarse_bin(__uint_as_float(bits));
+    int kd = 0;
+    if (b < T) {
+      kd = 1;
+    } else if (b == T) {
+      ++nt;
+      if (!overflow) {
+        kd = 2;
+      } else {
+        const int f = fine_bin(key[e], klo, fshift);
+        kd = (f < S) ? 1 : (f == S ? 2 : 0);
+      }
+    }
+    kinds |= (uint32_t)kd << (2 * e);
+    ne += (kd == 1);
+    nc += (kd == 2);
+  }
+  int ie = ne, ic = nc, it = nt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a1 = __shfl_up_sync(0xffffffffu, ie, o);
+    const int a2 = __shfl_up_sync(0xffffffffu, ic, o);
+    const int a3 = __shfl_up_sync(0xffffffffu, it, o);
+    if (lane >= o) {
+      ie += a1;
+      ic += a2;
+      it += a3;
+    }
+  }
+  int be = 0, bc = 0;
+  if (lane == 31) {
+    if (ie) be = dsmem_atomic_add(ctr0, ie);
+    if (ic) bc = dsmem_atomic_add(ctr0 + 4, ic);
+    if (it) dsmem_red_add(ctr0 + 8, it);
+  }
+  be = __shfl_sync(0xffffffffu, be, 31) + ie - ne;
+  bc = __shfl_sync(0xffffffffu, bc, 31) + ic - nc;
+#pragma unroll
+  for (int e = 0; e < kClVpt; ++e) {
+    const uint32_t kd = (kinds >> (2 * e)) & 3u;
+    if (!kd) continue;
+    const int64_t t = c0 + (int64_t)e * kClThreads + threadIdx.x;
+    if (kd == 1) {
+      if (be < k) outr[be] = (int32_t)t;
+      ++be;
+    } else {
+      if (bc < DSA_CAND_CAP)
+        dsmem_st64(cand0 + 8u * bc, ((unsigned long long)key[e] << 32) |
+                                        (unsigned long long)(0xFFFFFFFFu - (uint32_t)t));
+      ++bc;
+    }
+  }
+  cluster_sync();  // all emits and candidates are in place
+  if (rank != 0) return;  // nothing reads another CTA's shared memory from here on
+
+  // ---- CTA 0: check the counts, refine, or fall back
+  const int emitted = sm.ctr[0], ncand = sm.ctr[1], n_binT = sm.ctr[2];
+  const bool sane = (T < DSA_NUM_BINS) ? (above >= 0 && above < k && histT >= k - above)
+                                       : (above >= 0 && above < k);
+  int flag = 0, base_out = 0, m = 0;
+  if (!sane) {
+    flag = 1;
+  } else if (!overflow) {
+    if (emitted != above || (T < DSA_NUM_BINS && ncand != histT)) flag = 1;
+    base_out = above;
+    m = (T < DSA_NUM_BINS) ? k - above : 0;
+  } else {
+    const bool sane1 = S < kFineBins && above1 >= 0 && above1 < k - above;
+    if (!sane1 || n_binT != histT || emitted != above + above1 || ncand != fineS) flag = 1;
+    else if (ncand > DSA_CAND_CAP) flag = 2;
+    base_out = above + above1;
+    m = k - base_out;
+  }
+  if (flag == 0) {
+    if (m > 0) {
+      refine_candidates(sm.cand, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
+    } else {
+      for (int i = emitted + threadIdx.x; i < k; i += kClThreads) outr[i] = -1;
+    }
+  } else {
+    __syncthreads();
+    block_radix_topk_row(row, n, k, outr, sm_h, sm_scan, sm_misc);
+  }
+  if (a.flags && threadIdx.x == 0) a.flags[r] = flag;
+  if (a.reset_hist && a.hist) {
+    __syncthreads();
+    int32_t *hw = a.hist + (int64_t)r * DSA_NUM_BINS;
+    for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) hw[i] = 0;
+  }
+}
+
 // ---------------------------------------------------------------- short rows
 // Rows of at most kSmemRow scores with no histogram given (the block maxima
 // of the two-level path): one CTA per row holds the row as FP32 order keys in
@@ -975,6 +1215,45 @@ dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
   while ((c.stride + chunk - 1) / chunk > 65535) chunk *= 2;
   const int64_t nchunks = std::max<int64_t>(1, (c.stride + chunk - 1) / chunk);
   if (nchunks > 65535 || c.R > 65535) return DSA_ERR_UNSUPPORTED;
+  if (c.allow_cluster && c.stride <= kClRow) {
+    // one cluster of kCl CTAs per row, the row held in registers
+    ClArgs ca;
+    ca.logits = c.logits;
+    ca.stride = c.stride;
+    ca.ctx = c.context_lens;
+    ca.next_n = c.next_n;
+    ca.len_div = c.len_div;
+    ca.hist = c.histogram;
+    ca.reset_hist = c.reset_histogram ? 1 : 0;
+    ca.k = c.k;
+    ca.out = c.out_idx;
+    ca.flags = c.fallback_flags;
+    ca.status = status;
+    const int smem = (int)sizeof(ClSmem);
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(cluster_select_kernel), smem))
+      return DSA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kCl, (unsigned)c.R);
+    cfg.blockDim = dim3(kClThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, cluster_select_kernel, ca);
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      (void)cudaGetLastError();
+      return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
+  }
   if (!c.histogram && c.stride <= kSmemRow) {
     // short rows, no histogram: one CTA per row, the row held in shared memory
     const int smem = kSmemRow * 4;

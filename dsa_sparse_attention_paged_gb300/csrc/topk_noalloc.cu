@@ -105,5 +105,6 @@ extern "C" int32_t dsa_coarse_hist_topk_noalloc(const float *logits, int64_t str
   c.fallback_flags = fallback_flags;
   c.workspace = ws;
   c.ws_rows = DSA_NOALLOC_MAX_ROWS;
+  c.allow_cluster = false;  // the scratch-based kernels, whatever the row length
   return run_topk(c, st);
 }

@@ -162,3 +162,26 @@ def test_len_div_rows_of_block_maxima():
     torch.cuda.synchronize()
     ref = O.topk(x, np.array([4000, 700]), 512)
     assert sets_equal(out.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("with_hist,overflow", [(True, False), (False, False), (True, True)])
+def test_rows_longer_than_a_cluster_take_the_multi_cta_select(with_hist, overflow):
+    """Rows over 131072 scores are split over many CTAs with global counters
+    (and a fine pass when the threshold bin is over capacity)."""
+    import dsa_sparse_attention_paged_gb300 as D
+    R, n = 2, 150000
+    rng = np.random.default_rng(21)
+    x = rng.normal(0, 8, (R, n)).astype(np.float32)
+    if overflow:
+        x[:, 5000:45000] = rng.uniform(223.0, 900.0, (R, 40000)).astype(np.float32)
+    L = torch.from_numpy(x).cuda()
+    ctx = torch.full((R,), n, dtype=torch.int32, device="cuda")
+    hist = torch.from_numpy(O.histogram(x, np.full(R, n))).cuda() if with_hist else None
+    ws = D.Workspace(R)
+    flags = torch.full((R,), 9, dtype=torch.int32, device="cuda")
+    out = D.coarse_hist_topk(L, ctx, 1, 2048, ws, histogram=hist, fallback_flags=flags)
+    torch.cuda.synchronize()
+    ref = O.topk(x, np.full(R, n), 2048)
+    assert sets_equal(out.cpu().numpy(), ref)
+    assert (flags.cpu().numpy() == 0).all()
+    assert ws.status() == 0

@@ -52,6 +52,20 @@ def test_noalloc_topk_matches_workspace_topk_twice():
         assert (flags.cpu().numpy() >= 0).all()
 
 
+def test_noalloc_short_rows_without_histogram():
+    import dsa_sparse_attention_paged_gb300 as D
+    from oracle import oracle as O
+    rng = np.random.default_rng(8)
+    x = rng.normal(0, 5, (3, 9000)).astype(np.float32)
+    L = torch.from_numpy(x).cuda()
+    ctx = torch.tensor([8 * 9000 - 5, 8 * 700, 8 * 4000], dtype=torch.int32, device="cuda")
+    for call in range(2):
+        out = D.coarse_hist_topk_noalloc(L, ctx, 1, 512, len_div=8)
+        torch.cuda.synchronize()
+        ref = O.topk(x, np.array([9000, 700, 4000]), 512)
+        np.testing.assert_array_equal(_sorted(out), np.sort(ref, axis=1))
+
+
 def test_noalloc_rejects_rows_beyond_its_maximum():
     import dsa_sparse_attention_paged_gb300 as D
     n = D.NOALLOC_MAX_ROWS + 1
