@@ -835,8 +835,7 @@ __global__ void __launch_bounds__(kClThreads, 2) cluster_select_kernel(const ClA
   }
 
   // ---- emit the scores above the threshold, collect the threshold bin
-  // (kind: 1 above, 2 candidate, 4 counted in bin T)
-  uint32_t kinds = 0;
+  uint64_t kinds = 0;  // 2 bits per score: 1 above, 2 candidate
   int ne = 0, nc = 0, nt = 0;
 #pragma unroll
   for (int e = 0; e < kClVpt; ++e) {
@@ -855,7 +854,7 @@ __global__ void __launch_bounds__(kClThreads, 2) cluster_select_kernel(const ClA
         kd = (f < S) ? 1 : (f == S ? 2 : 0);
       }
     }
-    kinds |= (uint32_t)kd << (2 * e);
+    kinds |= (uint64_t)kd << (2 * e);
     ne += (kd == 1);
     nc += (kd == 2);
   }
@@ -881,7 +880,7 @@ __global__ void __launch_bounds__(kClThreads, 2) cluster_select_kernel(const ClA
   bc = __shfl_sync(0xffffffffu, bc, 31) + ic - nc;
 #pragma unroll
   for (int e = 0; e < kClVpt; ++e) {
-    const uint32_t kd = (kinds >> (2 * e)) & 3u;
+    const uint32_t kd = (uint32_t)(kinds >> (2 * e)) & 3u;
     if (!kd) continue;
     const int64_t t = c0 + (int64_t)e * kClThreads + threadIdx.x;
     if (kd == 1) {
