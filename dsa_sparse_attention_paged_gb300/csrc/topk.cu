@@ -695,28 +695,38 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
 
 // ---------------------------------------------------------------- cluster select
 // Rows of at most kClRow scores: one cluster of kCl CTAs per row, each CTA
-// holding its share of the row as order keys in registers (the row is read
-// from memory once).  The threshold bin comes from the caller's histogram
-// (or one the cluster builds from its registers); the row's counters and its
-// threshold-bin candidates live in the shared memory of CTA 0 of the
-// cluster and every CTA reaches them through distributed shared memory.  A
-// threshold bin over capacity gets its fine histogram the same way and is
-// resolved from the registers, without reading the row again.  CTA 0 then
-// checks the counts and refines the candidates exactly.  Every cluster-wide
-// decision is taken from data all CTAs share, so all CTAs pass the same
-// cluster barriers.
+// holding its share of the row as order keys in shared memory (the row is
+// read from memory once).
+//   1. threshold bin T from the caller's histogram, or from one the CTAs
+//      merge in the workspace (global reductions, resolved in L2)
+//   2. the exact key range [loT, hiT] of bin T (coarse bins descend with the
+//      key, so every bin is one key range), found by a warp-parallel search
+//   3. when bin T holds more than kClDirect scores: a fine histogram of bin T
+//      over its exact key range, merged in the workspace the same way, and
+//      the fine threshold bin S
+//   4. every CTA classifies its scores, reserves its output and candidate
+//      ranges with one atomic per counter on CTA 0, and writes them
+//   5. CTA 0 checks the counts and ranks the candidates (or refines them, or
+//      runs the exact whole-row fallback)
+// Every cluster-wide decision is taken from data all CTAs share, so all CTAs
+// pass the same cluster barriers.  The workspace histograms are zero on entry
+// and are cleared again by CTA 0 after the last barrier.
 constexpr int kCl = 8;
 constexpr int kClThreads = 512;
 constexpr int kClVpt = 32;                       // scores per thread
 constexpr int kClChunk = kClThreads * kClVpt;    // 16384 per CTA
 constexpr int kClRow = kCl * kClChunk;           // 131072
+constexpr int kClDirect = kClThreads;            // candidates ranked directly
+static_assert(kClThreads == kSelThreads, "block scans assume kSelThreads");
 
 struct ClSmem {
-  unsigned long long cand[DSA_CAND_CAP];  // CTA 0: the row's candidates
-  int chist[DSA_NUM_BINS];                // coarse histogram (local, then the row's)
-  int fine[kFineBins];                    // fine histogram (local, then the row's)
+  uint32_t keys[kClChunk];                // this CTA's scores; CTA 0 refines here
+  int hist[kFineBins];                    // local coarse / fine histogram, then the row's
+  unsigned long long cand[kClDirect];     // CTA 0: the first candidates of the row
   int ctr[4];                             // CTA 0: emitted, candidates, bin-T count
 };
+static_assert(sizeof(uint32_t) * kClChunk >= sizeof(unsigned long long) * DSA_CAND_CAP,
+              "CTA 0 refines the candidates in its key buffer");
 
 struct ClArgs {
   const float *logits;
@@ -728,8 +738,58 @@ struct ClArgs {
   int k;
   int32_t *out;
   int32_t *flags;
+  unsigned long long *cand;  // [R][DSA_CAND_CAP] workspace
+  int32_t *ws_hist;          // [R][DSA_NUM_BINS] workspace, zero on entry
+  int32_t *ws_fine;          // [R][kFineBins] workspace, zero on entry
   uint32_t *status;
 };
+
+constexpr uint32_t kKeyNegInf = 0x007FFFFFu;  // order key of -inf (lowest non-NaN)
+constexpr uint32_t kKeyPosInf = 0xFF800000u;  // order key of +inf (highest non-NaN)
+
+__device__ __forceinline__ int coarse_bin_of_key(uint32_t key) {
+  const uint32_t bits = (key & 0x80000000u) ? (key ^ 0x80000000u) : ~key;
+  return coarse_bin(__uint_as_float(bits));
+}
+
+// Largest non-NaN key whose coarse bin is >= X, kKeyNegInf - 1 if none.  The
+// keys with bin >= X are a prefix of the non-NaN keys because the bin never
+// increases with the value.  Run by one full warp (32-way search, 7 rounds);
+// every lane returns the result.
+__device__ uint32_t bin_prefix_end(int X) {
+  const int lane = threadIdx.x & 31;
+  uint32_t lo = kKeyNegInf - 1, hi = kKeyPosInf;  // answer in [lo, hi]
+  while (hi > lo) {
+    const uint32_t step = (hi - lo + 31) / 32;  // >= 1; lo + 32 step <= hi + 31
+    const uint32_t pt = min(hi, lo + step * (uint32_t)(lane + 1));
+    const unsigned bal = __ballot_sync(0xffffffffu, coarse_bin_of_key(pt) >= X);
+    const int nt = __popc(bal);  // the predicate holds on a prefix of the lanes
+    const uint32_t p_last = __shfl_sync(0xffffffffu, pt, max(nt - 1, 0));
+    const uint32_t p_next = __shfl_sync(0xffffffffu, pt, min(nt, 31));
+    if (nt == 0) {
+      hi = p_last - 1;  // p_last is lane 0's point lo + step
+    } else {
+      lo = p_last;
+      if (nt < 32) hi = p_next - 1;
+    }
+  }
+  return lo;
+}
+
+// The CTA's local histogram (nb bins) is added into the row's workspace copy.
+__device__ __forceinline__ void cl_flush(const int *local, int32_t *row_ws, int nb) {
+  for (int i = threadIdx.x; i < nb; i += kClThreads) {
+    const int v = local[i];
+    if (v) atomicAdd(&row_ws[i], v);
+  }
+}
+
+// The row's merged histogram is read back from L2 (no L1: other SMs wrote it).
+__device__ __forceinline__ void cl_fetch(int *local, const int32_t *row_ws, int nb) {
+  const int4 *src = reinterpret_cast<const int4 *>(row_ws);
+  int4 *dst = reinterpret_cast<int4 *>(local);
+  for (int i = threadIdx.x; i < nb / 4; i += kClThreads) dst[i] = __ldcg(src + i);
+}
 
 __global__ void __launch_bounds__(kClThreads, 2) cluster_select_kernel(const ClArgs a) {
   pdl_wait();  // predecessor grids complete before any global access
@@ -739,171 +799,161 @@ __global__ void __launch_bounds__(kClThreads, 2) cluster_select_kernel(const ClA
   __shared__ int sm_h[256];
   __shared__ int sm_scan[kSelWarps + 1];
   __shared__ int sm_misc[16];
+  __shared__ uint32_t sm_key[2];
   __shared__ unsigned long long sm_u64[2];
   const uint32_t rank = cluster_ctarank();
   const int r = blockIdx.y;
   const int k = a.k;
-  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int64_t n = row_len(a.ctx, a.next_n, a.len_div, r, a.stride, a.status);
   const float *row = a.logits + (int64_t)r * a.stride;
   int32_t *outr = a.out + (int64_t)r * k;
-  // this CTA's share: a multiple of 2048 positions
+  unsigned long long *cr = a.cand + (int64_t)r * DSA_CAND_CAP;
+  int32_t *wh = a.ws_hist + (int64_t)r * DSA_NUM_BINS;
+  int32_t *wf = a.ws_fine + (int64_t)r * kFineBins;
+  // this CTA's share: a multiple of 2048 positions; slot (e, tid) holds
+  // position c0 + e * kClThreads + tid
   const int64_t chunk = ((n + kCl - 1) / kCl + 2047) / 2048 * 2048;
   const int64_t c0 = (int64_t)rank * chunk;
   const int64_t c1 = min(n, c0 + chunk);
+  const int vpt = (int)(chunk / kClThreads);  // slots per thread in use (<= kClVpt)
 
-  for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) sm.chist[i] = 0;
-  for (int i = threadIdx.x; i < kFineBins; i += kClThreads) sm.fine[i] = 0;
-  if (threadIdx.x < 4) sm.ctr[threadIdx.x] = 0;
-  uint32_t key[kClVpt];
-#pragma unroll
-  for (int e = 0; e < kClVpt; ++e) {
-    const int64_t t = c0 + (int64_t)e * kClThreads + threadIdx.x;
-    const float x = (t < c1) ? row[t] : __int_as_float(0x7fffffff);
-    key[e] = isnan(x) ? 0u : f32_order_key(x);
-  }
-  const uint32_t ctr0 = dsmem_map(smem_u32(&sm.ctr[0]), 0);
-  const uint32_t cand0 = dsmem_map(smem_u32(&sm.cand[0]), 0);
-  cluster_sync();  // every CTA's shared state is zeroed before any remote access
-
-  // ---- the row's coarse histogram and its threshold bin
-  const int32_t *hsrc = a.hist ? a.hist + (int64_t)r * DSA_NUM_BINS : sm.chist;
-  if (!a.hist) {
+  {
+    float xv[kClVpt];
 #pragma unroll
     for (int e = 0; e < kClVpt; ++e) {
-      if (!key[e]) continue;
-      const uint32_t bits = (key[e] & 0x80000000u) ? (key[e] ^ 0x80000000u) : ~key[e];
-      atomicAdd(&sm.chist[coarse_bin(__uint_as_float(bits))], 1);
+      const int64_t t = c0 + (int64_t)e * kClThreads + threadIdx.x;
+      xv[e] = (e < vpt && t < c1) ? row[t] : __int_as_float(0x7fffffff);
+    }
+    if (!a.hist)
+      for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) sm.hist[i] = 0;
+    if (threadIdx.x < 4) sm.ctr[threadIdx.x] = 0;
+#pragma unroll
+    for (int e = 0; e < kClVpt; ++e)
+      sm.keys[e * kClThreads + threadIdx.x] = isnan(xv[e]) ? 0u : f32_order_key(xv[e]);
+  }
+  __syncthreads();
+
+  // ---- 1. the row's coarse histogram and its threshold bin
+  if (!a.hist) {
+    for (int e = 0; e < vpt; ++e) {
+      const uint32_t kk = sm.keys[e * kClThreads + threadIdx.x];
+      if (kk) atomicAdd(&sm.hist[coarse_bin_of_key(kk)], 1);
     }
     __syncthreads();
-    if (rank != 0) {
-      const uint32_t h0 = dsmem_map(smem_u32(&sm.chist[0]), 0);
-      for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads)
-        if (sm.chist[i]) dsmem_red_add(h0 + 4u * i, sm.chist[i]);
-    }
-    cluster_sync();
-    if (rank != 0) {
-      const uint32_t h0 = dsmem_map(smem_u32(&sm.chist[0]), 0);
-      for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) sm.chist[i] = dsmem_ld(h0 + 4u * i);
-    }
+    cl_flush(sm.hist, wh, DSA_NUM_BINS);
+  }
+  cluster_sync();  // merged histogram complete; every CTA's shared state ready
+  if (!a.hist) {
+    cl_fetch(sm.hist, wh, DSA_NUM_BINS);
     __syncthreads();
   }
-  threshold_from_hist<DSA_NUM_BINS>(hsrc, k, sm_scan, sm_misc);
+  threshold_from_hist<DSA_NUM_BINS>(a.hist ? a.hist + (int64_t)r * DSA_NUM_BINS : sm.hist, k,
+                                    sm_scan, sm_misc);
   const int T = sm_misc[0];
   const int above = sm_misc[1];
   const int histT = sm_misc[2];
+  // ---- 2. key range of bin T (empty, loT > hiT, when T is past the last bin)
+  if (warp < 2) {
+    const uint32_t g = bin_prefix_end(T + warp);
+    if ((threadIdx.x & 31) == 0) sm_key[warp] = g;
+  }
   __syncthreads();
-  const bool overflow = (T < DSA_NUM_BINS) && histT > DSA_CAND_CAP;
+  const uint32_t hiT = sm_key[0];
+  const uint32_t loT = sm_key[1] + 1;
+  const bool fine = (T < DSA_NUM_BINS) && histT > kClDirect;
 
-  // ---- a threshold bin over capacity: the row's fine histogram of bin T
-  uint32_t klo = 0;
+  // ---- 3. fine histogram of bin T over its key range, fine threshold bin S
   int fshift = 0, S = 0, above1 = 0, fineS = 0;
-  if (overflow) {
-    if (threadIdx.x == 0) {
-      uint32_t kl;
-      int sh;
-      fine_map(T, &kl, &sh);
-      sm_misc[8] = (int)kl;
-      sm_misc[9] = sh;
+  if (fine) {
+    const uint32_t span1 = hiT - loT;  // key span - 1; offsets (kk - loT) >> fshift < kFineBins
+    while ((span1 >> fshift) >= (uint32_t)kFineBins) ++fshift;
+    for (int i = threadIdx.x; i < kFineBins; i += kClThreads) sm.hist[i] = 0;
+    __syncthreads();
+    for (int e = 0; e < vpt; ++e) {
+      const uint32_t kk = sm.keys[e * kClThreads + threadIdx.x];
+      if (kk >= loT && kk <= hiT) atomicAdd(&sm.hist[(kFineBins - 1) - (int)((kk - loT) >> fshift)], 1);
     }
     __syncthreads();
-    klo = (uint32_t)sm_misc[8];
-    fshift = sm_misc[9];
-#pragma unroll
-    for (int e = 0; e < kClVpt; ++e) {
-      if (!key[e]) continue;
-      const uint32_t bits = (key[e] & 0x80000000u) ? (key[e] ^ 0x80000000u) : ~key[e];
-      if (coarse_bin(__uint_as_float(bits)) == T) atomicAdd(&sm.fine[fine_bin(key[e], klo, fshift)], 1);
-    }
-    __syncthreads();
-    if (rank != 0) {
-      const uint32_t f0 = dsmem_map(smem_u32(&sm.fine[0]), 0);
-      for (int i = threadIdx.x; i < kFineBins; i += kClThreads)
-        if (sm.fine[i]) dsmem_red_add(f0 + 4u * i, sm.fine[i]);
-    }
+    cl_flush(sm.hist, wf, kFineBins);
     cluster_sync();
-    if (rank != 0) {
-      const uint32_t f0 = dsmem_map(smem_u32(&sm.fine[0]), 0);
-      for (int i = threadIdx.x; i < kFineBins; i += kClThreads) sm.fine[i] = dsmem_ld(f0 + 4u * i);
-    }
+    cl_fetch(sm.hist, wf, kFineBins);
     __syncthreads();
-    threshold_from_hist<kFineBins>(sm.fine, k - above, sm_scan, sm_misc + 10);
+    threshold_from_hist<kFineBins>(sm.hist, k - above, sm_scan, sm_misc + 10);
     S = sm_misc[10];
     above1 = sm_misc[11];
     fineS = sm_misc[12];
-    __syncthreads();
   }
 
-  // ---- emit the scores above the threshold, collect the threshold bin
-  uint64_t kinds = 0;  // 2 bits per score: 1 above, 2 candidate
+  // ---- 4. classify (2 bits per slot: 1 emit, 2 candidate), reserve, write
+  unsigned long long kinds = 0;
   int ne = 0, nc = 0, nt = 0;
 #pragma unroll
   for (int e = 0; e < kClVpt; ++e) {
-    if (!key[e]) continue;
-    const uint32_t bits = (key[e] & 0x80000000u) ? (key[e] ^ 0x80000000u) : ~key[e];
-    const int b = coarse_bin(__uint_as_float(bits));
-    int kd = 0;
-    if (b < T) {
+    if (e >= vpt) break;
+    const uint32_t kk = sm.keys[e * kClThreads + threadIdx.x];
+    uint32_t kd = 0;
+    if (kk > hiT) {
       kd = 1;
-    } else if (b == T) {
+    } else if (kk >= loT) {
       ++nt;
-      if (!overflow) {
+      if (!fine) {
         kd = 2;
       } else {
-        const int f = fine_bin(key[e], klo, fshift);
-        kd = (f < S) ? 1 : (f == S ? 2 : 0);
+        const int f = (kFineBins - 1) - (int)((kk - loT) >> fshift);
+        kd = (f < S) ? 1u : (f == S ? 2u : 0u);
       }
     }
-    kinds |= (uint64_t)kd << (2 * e);
+    kinds |= (unsigned long long)kd << (2 * e);
     ne += (kd == 1);
     nc += (kd == 2);
   }
-  int ie = ne, ic = nc, it = nt;
+  if (threadIdx.x == 0) sm_misc[4] = 0;
+  int tot;
+  const int ex = block_excl_scan((nc << 16) | ne, sm_scan, &tot);  // per CTA < 2^15 each
+  const int ntw = __reduce_add_sync(0xffffffffu, nt);
+  if ((threadIdx.x & 31) == 0 && ntw) atomicAdd(&sm_misc[4], ntw);
+  __syncthreads();
+  const uint32_t ctr0 = dsmem_map(smem_u32(&sm.ctr[0]), 0);
+  if (threadIdx.x == 0) {
+    sm_misc[5] = (tot & 0xFFFF) ? dsmem_atomic_add(ctr0, tot & 0xFFFF) : 0;
+    sm_misc[6] = (tot >> 16) ? dsmem_atomic_add(ctr0 + 4, tot >> 16) : 0;
+    if (sm_misc[4]) dsmem_red_add(ctr0 + 8, sm_misc[4]);
+  }
+  __syncthreads();
+  if (kinds) {
+    int pe = sm_misc[5] + (ex & 0xFFFF);
+    int pc = sm_misc[6] + (ex >> 16);
+    const uint32_t cand0 = dsmem_map(smem_u32(&sm.cand[0]), 0);
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int a1 = __shfl_up_sync(0xffffffffu, ie, o);
-    const int a2 = __shfl_up_sync(0xffffffffu, ic, o);
-    const int a3 = __shfl_up_sync(0xffffffffu, it, o);
-    if (lane >= o) {
-      ie += a1;
-      ic += a2;
-      it += a3;
+    for (int e = 0; e < kClVpt; ++e) {
+      const uint32_t kd = (uint32_t)(kinds >> (2 * e)) & 3u;
+      if (!kd) continue;
+      const int64_t t = c0 + (int64_t)e * kClThreads + threadIdx.x;
+      if (kd == 1) {
+        if (pe < k) outr[pe] = (int32_t)t;
+        ++pe;
+      } else {
+        const unsigned long long v =
+            ((unsigned long long)sm.keys[e * kClThreads + threadIdx.x] << 32) |
+            (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
+        if (pc < kClDirect) dsmem_st64(cand0 + 8u * pc, v);
+        else if (pc < DSA_CAND_CAP) cr[pc] = v;
+        ++pc;
+      }
     }
   }
-  int be = 0, bc = 0;
-  if (lane == 31) {
-    if (ie) be = dsmem_atomic_add(ctr0, ie);
-    if (ic) bc = dsmem_atomic_add(ctr0 + 4, ic);
-    if (it) dsmem_red_add(ctr0 + 8, it);
-  }
-  be = __shfl_sync(0xffffffffu, be, 31) + ie - ne;
-  bc = __shfl_sync(0xffffffffu, bc, 31) + ic - nc;
-#pragma unroll
-  for (int e = 0; e < kClVpt; ++e) {
-    const uint32_t kd = (uint32_t)(kinds >> (2 * e)) & 3u;
-    if (!kd) continue;
-    const int64_t t = c0 + (int64_t)e * kClThreads + threadIdx.x;
-    if (kd == 1) {
-      if (be < k) outr[be] = (int32_t)t;
-      ++be;
-    } else {
-      if (bc < DSA_CAND_CAP)
-        dsmem_st64(cand0 + 8u * bc, ((unsigned long long)key[e] << 32) |
-                                        (unsigned long long)(0xFFFFFFFFu - (uint32_t)t));
-      ++bc;
-    }
-  }
-  cluster_sync();  // all emits and candidates are in place
+  cluster_sync();  // all emits and candidates are in place; histograms read
   if (rank != 0) return;  // nothing reads another CTA's shared memory from here on
 
-  // ---- CTA 0: check the counts, refine, or fall back
+  // ---- 5. CTA 0: check the counts, rank or refine, or fall back
   const int emitted = sm.ctr[0], ncand = sm.ctr[1], n_binT = sm.ctr[2];
   const bool sane = (T < DSA_NUM_BINS) ? (above >= 0 && above < k && histT >= k - above)
                                        : (above >= 0 && above < k);
   int flag = 0, base_out = 0, m = 0;
   if (!sane) {
     flag = 1;
-  } else if (!overflow) {
+  } else if (!fine) {
     if (emitted != above || (T < DSA_NUM_BINS && ncand != histT)) flag = 1;
     base_out = above;
     m = (T < DSA_NUM_BINS) ? k - above : 0;
@@ -915,18 +965,35 @@ __global__ void __launch_bounds__(kClThreads, 2) cluster_select_kernel(const ClA
     m = k - base_out;
   }
   if (flag == 0) {
-    if (m > 0) {
-      refine_candidates(sm.cand, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
-    } else {
+    if (m <= 0) {
       for (int i = emitted + threadIdx.x; i < k; i += kClThreads) outr[i] = -1;
+    } else if (ncand <= kClDirect) {
+      // candidate keys are unique (the column is part of the key): each
+      // thread ranks one against all the others
+      if (threadIdx.x < ncand) {
+        const unsigned long long v = sm.cand[threadIdx.x];
+        int rk = 0;
+        for (int j = 0; j < ncand; ++j) rk += sm.cand[j] > v;
+        if (rk < m) outr[base_out + rk] = (int32_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
+      }
+    } else {
+      unsigned long long *sc = reinterpret_cast<unsigned long long *>(sm.keys);
+      for (int i = threadIdx.x; i < ncand; i += kClThreads)
+        sc[i] = i < kClDirect ? sm.cand[i] : __ldcg(cr + i);
+      __syncthreads();
+      refine_candidates(sc, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
     }
   } else {
     __syncthreads();
     block_radix_topk_row(row, n, k, outr, sm_h, sm_scan, sm_misc);
   }
   if (a.flags && threadIdx.x == 0) a.flags[r] = flag;
+  // restore the zero workspace histograms; clear the caller's on request
+  if (!a.hist)
+    for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) wh[i] = 0;
+  if (fine)
+    for (int i = threadIdx.x; i < kFineBins; i += kClThreads) wf[i] = 0;
   if (a.reset_hist && a.hist) {
-    __syncthreads();
     int32_t *hw = a.hist + (int64_t)r * DSA_NUM_BINS;
     for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) hw[i] = 0;
   }
@@ -1227,6 +1294,9 @@ dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
     ca.k = c.k;
     ca.out = c.out_idx;
     ca.flags = c.fallback_flags;
+    ca.cand = cand;
+    ca.ws_hist = ws_hist;
+    ca.ws_fine = fine;
     ca.status = status;
     const int smem = (int)sizeof(ClSmem);
     if (!ensure_smem_attr(reinterpret_cast<const void *>(cluster_select_kernel), smem))
