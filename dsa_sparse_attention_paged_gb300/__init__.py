@@ -60,6 +60,7 @@ def _load():
         "dsa_paged_mqa_logits": (i32, [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, i32, P,
                                        i64, P, P, i64, i32, P, sz, P]),
         "dsa_coarse_hist_topk": (i32, [P, i64, P, i32, i32, i32, P, i32, i32, P, P, P, sz, P]),
+        "dsa_coarse_hist_topk_launches": (i32, [i64, i32]),
         "dsa_block_amax8": (i32, [P, i64, P, i32, i32, i32, P, i64, P, sz, P]),
         "dsa_sort_candidate_blocks": (i32, [P, i32, P, i32, i32, P, i64, i32, P, P, P, sz, P]),
         "dsa_sparse_mqa_logits": (i32, [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, i32, P,
@@ -269,6 +270,14 @@ def fp16_order_keys(x, out=None, stream=None):
 def wait_timeout_selftest(limit_cycles: int, ws, stream=None):
     _check(lib.dsa_wait_timeout_selftest(ctypes.c_uint64(limit_cycles), ws.ptr, ws.nbytes,
                                          _stream(stream)), "wait_timeout_selftest")
+
+
+def coarse_hist_topk_launches(stride, has_histogram):
+    """Kernel launches one coarse_hist_topk call makes on rows of ``stride``."""
+    n = lib.dsa_coarse_hist_topk_launches(int(stride), 1 if has_histogram else 0)
+    if n < 0:
+        raise ValueError(f"coarse_hist_topk_launches: invalid stride {stride}")
+    return n
 
 
 def coarse_hist_topk_noalloc(logits, context_lens, next_n, k, histogram=None,

@@ -315,6 +315,11 @@ int32_t dsa_coarse_hist_topk(const float *logits, int64_t stride, const int32_t 
   return run_topk(c, static_cast<cudaStream_t>(stream));
 }
 
+int32_t dsa_coarse_hist_topk_launches(int64_t stride, int32_t has_histogram) {
+  if (stride < 1) return -DSA_ERR_INVALID_ARG;
+  return topk_launch_count(stride, has_histogram != 0, true);
+}
+
 int32_t dsa_block_amax8(const float *logits, int64_t stride, const int32_t *context_lens,
                         int32_t next_n, int32_t R, int32_t skip_if_blocks_le, float *amax,
                         int64_t amax_stride, void *workspace, size_t ws_bytes, void *stream) {

@@ -37,7 +37,6 @@ __global__ void __launch_bounds__(kAmaxThreads)
     amax8_kernel(const float *logits, int64_t stride, const int32_t *ctx, int next_n,
                  int skip_le, float *amax, int64_t amax_stride, uint32_t *status) {
   pdl_wait();  // predecessor grids complete before any global access
-  pdl_launch_dependents();
   const int r = blockIdx.y;
   int64_t n = live_len(ctx, next_n, r);
   if (n > stride) {
@@ -100,7 +99,6 @@ __global__ void __launch_bounds__(kSortThreads)
                        const int32_t *page_table, int64_t pt_stride, int page_size,
                        int32_t *phys, int32_t *valid_lens, uint32_t *status) {
   pdl_wait();  // predecessor grids complete before any global access
-  pdl_launch_dependents();
   __shared__ uint32_t bm[kMaxBitmapWords];
   __shared__ int sm_scan[kSortThreads / 32 + 1];
   __shared__ long long sm_live[kSortThreads / 32];

@@ -57,6 +57,8 @@ struct TopkCall {
   bool allow_cluster = true; // rows up to 131072 may take the cluster kernel
 };
 dsa_status_t run_topk(const TopkCall &c, cudaStream_t st);
+// kernel launches run_topk makes for rows of `stride` scores
+int32_t topk_launch_count(int64_t stride, bool has_histogram, bool allow_cluster);
 
 struct Fp16TopkCall {
   const uint16_t *scores;

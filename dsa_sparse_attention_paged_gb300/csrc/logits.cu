@@ -293,7 +293,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const LogitsArgs a) {
   pdl_wait();  // predecessor grids complete before any global access
-  pdl_launch_dependents();
   constexpr int N = 32 * NN;
   constexpr uint32_t IDESC = idesc_e4m3_f32(128, N);
   constexpr int HS = hist_slots_per_group(NN);

@@ -390,7 +390,6 @@ __global__ void __launch_bounds__(kSelThreads)
     hist_build_kernel(const float *logits, int64_t stride, const int32_t *ctx, int next_n,
                       int len_div, int64_t chunk, int32_t *hist, uint32_t *status) {
   pdl_wait();  // predecessor grids complete before any global access
-  pdl_launch_dependents();
   __shared__ int h[DSA_NUM_BINS];
   const int r = blockIdx.y;
   for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kSelThreads) h[i] = 0;
@@ -467,7 +466,6 @@ __device__ void threshold_from_hist(const int32_t *h, int need, int *sm_scan, in
 template <int LEVEL>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
   pdl_wait();  // predecessor grids complete before any global access
-  pdl_launch_dependents();
   extern __shared__ unsigned long long sm_dyn[];  // fine hist (pass) / candidates (refine)
   __shared__ int sm_h[256];
   __shared__ int sm_scan[kSelWarps + 1];
@@ -793,7 +791,6 @@ __device__ __forceinline__ void cl_fetch(int *local, const int32_t *row_ws, int 
 
 __global__ void __launch_bounds__(kClThreads, 2) cluster_select_kernel(const ClArgs a) {
   pdl_wait();  // predecessor grids complete before any global access
-  pdl_launch_dependents();
   extern __shared__ __align__(16) unsigned char cl_raw[];
   ClSmem &sm = *reinterpret_cast<ClSmem *>(cl_raw);
   __shared__ int sm_h[256];
@@ -1040,7 +1037,6 @@ __global__ void __launch_bounds__(kRowThreads)
     row_topk_kernel(const float *logits, int64_t stride, const int32_t *ctx, int next_n,
                     int len_div, int k, int32_t *out, uint32_t *status) {
   pdl_wait();  // predecessor grids complete before any global access
-  pdl_launch_dependents();
   extern __shared__ uint32_t keys[];  // [kSmemRow]
   __shared__ int h[256];
   __shared__ int sm_scan[kRowWarps + 1];
@@ -1121,7 +1117,6 @@ __global__ void __launch_bounds__(kSelThreads)
     topk_fp16_kernel(const uint16_t *scores, int64_t stride, const int32_t *valid_lens, int k,
                      const int32_t *table, int kb, int32_t *out, uint32_t *status) {
   pdl_wait();  // predecessor grids complete before any global access
-  pdl_launch_dependents();
   __shared__ uint32_t keys2[kF16MaxRow / 2];  // two 16-bit keys per word
   __shared__ int h[DSA_NUM_BINS];
   __shared__ int sm_scan[kSelWarps + 1];
@@ -1265,6 +1260,12 @@ __global__ void __launch_bounds__(kSelThreads)
 }
 
 }  // namespace
+
+int32_t topk_launch_count(int64_t stride, bool has_histogram, bool allow_cluster) {
+  if (allow_cluster && stride <= kClRow) return 1;
+  if (!has_histogram && stride <= kSmemRow) return 1;
+  return has_histogram ? 2 : 3;
+}
 
 dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
   char *ws = static_cast<char *>(c.workspace);

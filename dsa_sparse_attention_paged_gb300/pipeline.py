@@ -6,9 +6,10 @@ step's device buffers and the workspace, and each ``step`` runs
 
   source layer   paged MQA logits + fused coarse histogram + fused
                  block maxima over 8 scores                        (1 launch)
-                 histogram-driven exact top-k (resets the hist)   (2 launches)
-  level one      top-kb of the block maxima                        (1 launch,
-                 3 when a row has more than 16384 blocks)
+                 histogram-driven exact top-k (resets the hist)   (1 launch for
+                 rows up to 131072 scores, else 2)
+  level one      top-kb of the block maxima                        (1 launch for
+                 rows up to 131072 blocks, else 3)
                  sort_candidate_blocks -> table, phys, valid lens   (1 launch)
   consumer       sparse MQA logits over the table, FP16 output      (1 launch)
                  FP16 top-k with the fused table transform          (1 launch)
@@ -21,8 +22,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (OUT_F16, Workspace, coarse_hist_topk, paged_mqa_logits, sort_candidate_blocks,
-               sparse_mqa_logits, topk_fp16)
+from . import (OUT_F16, Workspace, coarse_hist_topk, coarse_hist_topk_launches, paged_mqa_logits,
+               sort_candidate_blocks, sparse_mqa_logits, topk_fp16)
 
 
 class DecodePlan:
@@ -52,9 +53,9 @@ class DecodePlan:
     @property
     def launches_per_step(self) -> int:
         """Kernels of this library launched by one step."""
-        n = 1 + 2  # logits (+ histogram, + block maxima), top-k levels 0 and 1
+        n = 1 + coarse_hist_topk_launches(self.stride, True)  # logits (+ hist, maxima), top-k
         if self.two_level:
-            n += (1 if self.amax_stride <= 16384 else 3) + 1 + 1 + 1
+            n += coarse_hist_topk_launches(self.amax_stride, False) + 1 + 1 + 1
         return n
 
     def step(self, q, kv, kscale, weights, page_table, context_lens, events=None):

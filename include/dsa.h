@@ -151,6 +151,10 @@ int32_t dsa_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const fl
  * collects inside its threshold fine bin.  A histogram that does not match
  * the row (stale), or a fine bin still over capacity, falls back to an exact
  * whole-row radix select instead of raising a device error.
+ * Rows of at most 131072 scores (stride <= 131072) take one launch: a cluster
+ * of eight CTAs per row reads the row once into shared memory; it builds the
+ * fine histogram whenever bin T holds more than 512 scores, so at most 512
+ * candidates are usually left to rank.  Longer rows take the multi-CTA passes.
  *
  * Rows: r in [0, R); row r has n_r = ceil_div(context_lens[r / next_n] -
  * (next_n - 1 - r % next_n), len_div) live scores (len_div = 1 for logits
@@ -173,6 +177,14 @@ int32_t dsa_coarse_hist_topk(const float *logits, int64_t stride, const int32_t 
                              int32_t reset_histogram, int32_t k, int32_t *out_idx,
                              int32_t *fallback_flags, void *workspace, size_t ws_bytes,
                              void *stream);
+
+/* Kernel launches one dsa_coarse_hist_topk call makes on rows of `stride`
+ * scores, with (has_histogram != 0) or without a caller histogram: 1 when
+ * stride <= 131072 (one cluster of eight CTAs per row, the row kept in their
+ * shared memory), else 2 with a histogram (pass, refine pass) and 3 without
+ * (histogram build first).  Host only, no device work; -DSA_ERR_INVALID_ARG
+ * for stride < 1. */
+int32_t dsa_coarse_hist_topk_launches(int64_t stride, int32_t has_histogram);
 
 /* ---- top-k without a caller workspace --------------------------------------
  * The pages have no counterpart to this entry point; it exists for callers

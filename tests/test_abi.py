@@ -98,3 +98,16 @@ def test_topk_and_block_argument_checks(lib):
     t = lib.dsa_topk_fp16
     assert t(A16, 4097, A16, 2, 16, None, 0, A16, ws, 4096, None) == 3  # odd stride
     assert t(A16, 4096, A16, 2, 0, None, 0, A16, ws, 4096, None) == 2
+
+
+def test_topk_launch_count_follows_the_dispatch():
+    """Host-only query: one cluster launch up to 131072 scores per row, else
+    the multi-CTA passes (plus the histogram build without a histogram)."""
+    import dsa_sparse_attention_paged_gb300 as D
+    assert D.coarse_hist_topk_launches(1, True) == 1
+    assert D.coarse_hist_topk_launches(131072, True) == 1
+    assert D.coarse_hist_topk_launches(131072, False) == 1
+    assert D.coarse_hist_topk_launches(131073, True) == 2
+    assert D.coarse_hist_topk_launches(1 << 20, False) == 3
+    with pytest.raises(ValueError):
+        D.coarse_hist_topk_launches(0, True)
