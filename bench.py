@@ -323,7 +323,7 @@ def main():
 
     # per-stage split (diagnostic, outside the timed region): events between
     # the stages, so the stages sum to more than a step
-    stages = ["logits", "topk", "publish", "consume"]
+    stages = ["logits", "select", "publish", "consume"]
     Kd = max(1, min(K, 200))
     ev_d = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for n in stages} for _ in range(Kd)]

@@ -33,6 +33,19 @@ _STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
            3: "DSA_ERR_MISALIGNED", 4: "DSA_ERR_CUDA", 5: "DSA_ERR_WORKSPACE"}
 
 
+class TopkProblem(ctypes.Structure):
+    """``dsa_topk_problem``: one problem of ``coarse_hist_topk_batch``."""
+    _fields_ = [("logits", ctypes.c_void_p), ("stride", ctypes.c_int64),
+                ("context_lens", ctypes.c_void_p), ("histogram", ctypes.c_void_p),
+                ("out_idx", ctypes.c_void_p), ("fallback_flags", ctypes.c_void_p),
+                ("next_n", ctypes.c_int32), ("len_div", ctypes.c_int32), ("R", ctypes.c_int32),
+                ("reset_histogram", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+TOPK_BATCH_MAX = 4
+
+
 class DSAError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -61,6 +74,8 @@ def _load():
                                        i64, P, P, i64, i32, P, sz, P]),
         "dsa_coarse_hist_topk": (i32, [P, i64, P, i32, i32, i32, P, i32, i32, P, P, P, sz, P]),
         "dsa_coarse_hist_topk_launches": (i32, [i64, i32]),
+        "dsa_coarse_hist_topk_batch": (i32, [ctypes.POINTER(TopkProblem), i32, P, sz, P]),
+        "dsa_coarse_hist_topk_batch_launches": (i32, [ctypes.POINTER(TopkProblem), i32]),
         "dsa_block_amax8": (i32, [P, i64, P, i32, i32, i32, P, i64, P, sz, P]),
         "dsa_sort_candidate_blocks": (i32, [P, i32, P, i32, i32, P, i64, i32, P, P, P, sz, P]),
         "dsa_sparse_mqa_logits": (i32, [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, i32, P,
@@ -190,6 +205,50 @@ def coarse_hist_topk(logits, context_lens, next_n, k, ws, histogram=None, reset_
         1 if reset_histogram else 0, k, _p(out), _p(fallback_flags), ws.ptr, ws.nbytes,
         _stream(stream)), "coarse_hist_topk")
     return out
+
+
+def _topk_problem(logits, context_lens, next_n, k, histogram=None, reset_histogram=False,
+                  len_div=1, out=None, fallback_flags=None, R=None):
+    _req(logits, torch.float32, "logits")
+    _req(context_lens, torch.int32, "context_lens")
+    R = logits.shape[0] if R is None else R
+    if out is None:
+        out = torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    _req(out, torch.int32, "out")
+    if histogram is not None:
+        _req(histogram, torch.int32, "histogram")
+    if fallback_flags is not None:
+        _req(fallback_flags, torch.int32, "fallback_flags")
+    prob = TopkProblem(logits.data_ptr(), logits.stride(0), context_lens.data_ptr(),
+                       histogram.data_ptr() if histogram is not None else None, out.data_ptr(),
+                       fallback_flags.data_ptr() if fallback_flags is not None else None,
+                       int(next_n), int(len_div), int(R), 1 if reset_histogram else 0, int(k), 0)
+    return prob, out
+
+
+def coarse_hist_topk_batch(problems, ws, stream=None):
+    """Several independent ``coarse_hist_topk`` problems (dicts of its keyword
+    arguments) with one workspace sized for the sum of their rows; one launch
+    when every row stride is at most 131072.  Returns the output tensors."""
+    if len(problems) > TOPK_BATCH_MAX:
+        raise ValueError(f"coarse_hist_topk_batch: at most {TOPK_BATCH_MAX} problems")
+    built = [_topk_problem(**p) for p in problems]
+    arr = (TopkProblem * max(1, len(built)))(*[b[0] for b in built])
+    _check(lib.dsa_coarse_hist_topk_batch(arr, len(built), ws.ptr, ws.nbytes, _stream(stream)),
+           "coarse_hist_topk_batch")
+    return [b[1] for b in built]
+
+
+def coarse_hist_topk_batch_launches(strides_and_hist):
+    """Kernel launches of ``coarse_hist_topk_batch`` for problems given as
+    (row stride, has_histogram, rows) triples."""
+    arr = (TopkProblem * max(1, len(strides_and_hist)))(
+        *[TopkProblem(None, int(s), None, 1 if h else None, None, None, 1, 1, int(r), 0, 1, 0)
+          for s, h, r in strides_and_hist])
+    n = lib.dsa_coarse_hist_topk_batch_launches(arr, len(strides_and_hist))
+    if n < 0:
+        raise ValueError("coarse_hist_topk_batch_launches: invalid problems")
+    return n
 
 
 def block_amax8(logits, context_lens, next_n, ws, skip_if_blocks_le=0, amax=None,

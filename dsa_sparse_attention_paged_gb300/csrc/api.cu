@@ -284,21 +284,18 @@ int32_t dsa_sparse_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const f
   return run_paged_logits(c, static_cast<cudaStream_t>(stream));
 }
 
-int32_t dsa_coarse_hist_topk(const float *logits, int64_t stride, const int32_t *context_lens,
-                             int32_t next_n, int32_t len_div, int32_t R, int32_t *histogram,
-                             int32_t reset_histogram, int32_t k, int32_t *out_idx,
-                             int32_t *fallback_flags, void *workspace, size_t ws_bytes,
-                             void *stream) {
+namespace {
+
+// Arguments of one top-k problem, checked; fills `c` (without the workspace).
+int32_t topk_args(const float *logits, int64_t stride, const int32_t *context_lens,
+                  int32_t next_n, int32_t len_div, int32_t R, int32_t *histogram,
+                  int32_t reset_histogram, int32_t k, int32_t *out_idx, int32_t *fallback_flags,
+                  TopkCall &c) {
   if (R < 0 || next_n < 1 || len_div < 1 || stride < 1) return DSA_ERR_INVALID_ARG;
   if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
   if (!logits || !context_lens || !out_idx) return DSA_ERR_INVALID_ARG;
   if (histogram && !aligned(histogram, 8)) return DSA_ERR_MISALIGNED;
-  if (!workspace) return DSA_ERR_WORKSPACE;
-  if (!aligned(workspace, 256)) return DSA_ERR_MISALIGNED;
-  const int64_t rows = ws_rows_for(ws_bytes);
-  if (rows < R) return DSA_ERR_WORKSPACE;
-  if (R == 0) return DSA_OK;
-  TopkCall c{};
+  c = TopkCall{};
   c.logits = logits;
   c.stride = stride;
   c.context_lens = context_lens;
@@ -310,9 +307,82 @@ int32_t dsa_coarse_hist_topk(const float *logits, int64_t stride, const int32_t 
   c.k = k;
   c.out_idx = out_idx;
   c.fallback_flags = fallback_flags;
+  return DSA_OK;
+}
+
+int32_t topk_problem_args(const dsa_topk_problem &p, TopkCall &c) {
+  return topk_args(p.logits, p.stride, p.context_lens, p.next_n, p.len_div, p.R, p.histogram,
+                   p.reset_histogram, p.k, p.out_idx, p.fallback_flags, c);
+}
+
+}  // namespace
+
+int32_t dsa_coarse_hist_topk(const float *logits, int64_t stride, const int32_t *context_lens,
+                             int32_t next_n, int32_t len_div, int32_t R, int32_t *histogram,
+                             int32_t reset_histogram, int32_t k, int32_t *out_idx,
+                             int32_t *fallback_flags, void *workspace, size_t ws_bytes,
+                             void *stream) {
+  TopkCall c;
+  const int32_t err = topk_args(logits, stride, context_lens, next_n, len_div, R, histogram,
+                                reset_histogram, k, out_idx, fallback_flags, c);
+  if (err != DSA_OK) return err;
+  if (!workspace) return DSA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return DSA_ERR_MISALIGNED;
+  const int64_t rows = ws_rows_for(ws_bytes);
+  if (rows < R) return DSA_ERR_WORKSPACE;
+  if (R == 0) return DSA_OK;
   c.workspace = workspace;
   c.ws_rows = (int32_t)rows;
   return run_topk(c, static_cast<cudaStream_t>(stream));
+}
+
+int32_t dsa_coarse_hist_topk_batch(const dsa_topk_problem *problems, int32_t count,
+                                   void *workspace, size_t ws_bytes, void *stream) {
+  if (count < 0 || (count > 0 && !problems)) return DSA_ERR_INVALID_ARG;
+  if (count > DSA_TOPK_BATCH_MAX) return DSA_ERR_UNSUPPORTED;
+  TopkCall calls[DSA_TOPK_BATCH_MAX];
+  int n = 0;
+  int64_t rows_needed = 0;
+  for (int i = 0; i < count; ++i) {
+    if (problems[i].reserved != 0 || problems[i].R < 0) return DSA_ERR_INVALID_ARG;
+    if (problems[i].R == 0) continue;  // nothing to check or run (pointers may be NULL)
+    TopkCall c;
+    const int32_t err = topk_problem_args(problems[i], c);
+    if (err != DSA_OK) return err;
+    rows_needed += c.R;
+    calls[n++] = c;
+  }
+  if (!workspace) return DSA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return DSA_ERR_MISALIGNED;
+  const int64_t rows = ws_rows_for(ws_bytes);
+  if (rows < rows_needed) return DSA_ERR_WORKSPACE;
+  if (n == 0) return DSA_OK;
+  for (int i = 0; i < n; ++i) {
+    calls[i].workspace = workspace;
+    calls[i].ws_rows = (int32_t)rows;
+  }
+  return run_topk_batch(calls, n, static_cast<cudaStream_t>(stream));
+}
+
+int32_t dsa_coarse_hist_topk_batch_launches(const dsa_topk_problem *problems, int32_t count) {
+  if (count < 0 || (count > 0 && !problems) || count > DSA_TOPK_BATCH_MAX)
+    return -DSA_ERR_INVALID_ARG;
+  TopkCall calls[DSA_TOPK_BATCH_MAX];
+  int n = 0;
+  for (int i = 0; i < count; ++i) {
+    if (problems[i].stride < 1) return -DSA_ERR_INVALID_ARG;
+    if (problems[i].R == 0) continue;
+    calls[n] = TopkCall{};
+    calls[n].stride = problems[i].stride;
+    calls[n].histogram = problems[i].histogram;
+    ++n;
+  }
+  if (n == 0) return 0;
+  if (topk_batchable(calls, n)) return 1;
+  int32_t total = 0;
+  for (int i = 0; i < n; ++i)
+    total += topk_launch_count(calls[i].stride, calls[i].histogram != nullptr, true);
+  return total;
 }
 
 int32_t dsa_coarse_hist_topk_launches(int64_t stride, int32_t has_histogram) {

@@ -96,6 +96,14 @@ __device__ __forceinline__ void dsmem_st64(uint32_t addr, unsigned long long v) 
 }
 // All threads of all CTAs of the cluster meet (shared-memory writes before it
 // are visible to every CTA after it).
+// The two halves of cluster_sync(), for work placed between them: a thread's
+// writes before its arrive are visible to every CTA after that CTA's wait.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");

@@ -59,6 +59,10 @@ struct TopkCall {
 dsa_status_t run_topk(const TopkCall &c, cudaStream_t st);
 // kernel launches run_topk makes for rows of `stride` scores
 int32_t topk_launch_count(int64_t stride, bool has_histogram, bool allow_cluster);
+// several independent calls sharing calls[0]'s workspace (rows laid out one
+// problem after another): one launch when topk_batchable, else in sequence
+bool topk_batchable(const TopkCall *calls, int count);
+dsa_status_t run_topk_batch(const TopkCall *calls, int count, cudaStream_t st);
 
 struct Fp16TopkCall {
   const uint16_t *scores;

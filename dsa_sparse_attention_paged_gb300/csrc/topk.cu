@@ -692,53 +692,69 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
 }
 
 // ---------------------------------------------------------------- cluster select
-// Rows of at most kClRow scores: one cluster of kCl CTAs per row, each CTA
+// One launch selects the rows of up to kClMaxProb independent problems.
+// Long rows (stride > kClChunk): one cluster of kCl CTAs per row, each CTA
 // holding its share of the row as order keys in shared memory (the row is
-// read from memory once).
-//   1. threshold bin T from the caller's histogram, or from one the CTAs
+// read from memory once):
+//   1. threshold bin T from the caller's histogram (worked out while the row
+//      loads, behind an early cluster-barrier arrive), or from one the CTAs
 //      merge in the workspace (global reductions, resolved in L2)
 //   2. the exact key range [loT, hiT] of bin T (coarse bins descend with the
 //      key, so every bin is one key range), found by a warp-parallel search
-//   3. when bin T holds more than kClDirect scores: a fine histogram of bin T
-//      over its exact key range, merged in the workspace the same way, and
+//   3. when bin T holds more than kClDirect scores: a fine histogram over a
+//      window of bin T's key range, merged in the workspace the same way, and
 //      the fine threshold bin S
 //   4. every CTA classifies its scores, reserves its output and candidate
 //      ranges with one atomic per counter on CTA 0, and writes them
 //   5. CTA 0 checks the counts and ranks the candidates (or refines them, or
 //      runs the exact whole-row fallback)
+// Short rows (stride <= kClChunk): each CTA of a cluster takes one row alone
+// (the same steps inside one CTA, no cluster barrier), eight rows a cluster.
 // Every cluster-wide decision is taken from data all CTAs share, so all CTAs
 // pass the same cluster barriers.  The workspace histograms are zero on entry
 // and are cleared again by CTA 0 after the last barrier.
 constexpr int kCl = 8;
 constexpr int kClThreads = 512;
 constexpr int kClVpt = 32;                       // scores per thread
+constexpr int kClVec = kClVpt / 4;               // float4 groups per thread
 constexpr int kClChunk = kClThreads * kClVpt;    // 16384 per CTA
 constexpr int kClRow = kCl * kClChunk;           // 131072
 constexpr int kClDirect = kClThreads;            // candidates ranked directly
-static_assert(kClThreads == kSelThreads, "block scans assume kSelThreads");
+constexpr int kClMaxProb = 4;                    // problems per launch
+constexpr uint32_t kFineWindow = 1u << 26;       // keys one fine histogram spans at most
+static_assert(kClThreads == kSelThreads, "block scans assume kSelThreads threads");
 
 struct ClSmem {
-  uint32_t keys[kClChunk];                // this CTA's scores; CTA 0 refines here
-  int hist[kFineBins];                    // local coarse / fine histogram, then the row's
-  unsigned long long cand[kClDirect];     // CTA 0: the first candidates of the row
-  int ctr[4];                             // CTA 0: emitted, candidates, bin-T count
+  uint4 keys[kClVec * kClThreads];      // keys[q * kClThreads + tid] = slots 4q..4q+3 of tid
+  int hist[kFineBins];                  // local coarse / fine histogram, then the row's
+  unsigned long long cand[kClDirect];   // the row's first candidates (CTA 0 / local CTA)
+  int ctr[4];                           // CTA 0: emitted, candidates, bin-T count
 };
-static_assert(sizeof(uint32_t) * kClChunk >= sizeof(unsigned long long) * DSA_CAND_CAP,
-              "CTA 0 refines the candidates in its key buffer");
+static_assert(sizeof(uint4) * kClVec * kClThreads >= sizeof(unsigned long long) * DSA_CAND_CAP,
+              "the refine reuses the key buffer for the candidates");
 
-struct ClArgs {
+struct ClProb {
   const float *logits;
   int64_t stride;
   const int32_t *ctx;
-  int next_n, len_div;
-  int32_t *hist;  // NULL: the cluster builds it
+  int next_n, len_div, R;
+  int32_t *hist;  // caller's histogram, or NULL
   int reset_hist;
   int k;
   int32_t *out;
   int32_t *flags;
-  unsigned long long *cand;  // [R][DSA_CAND_CAP] workspace
-  int32_t *ws_hist;          // [R][DSA_NUM_BINS] workspace, zero on entry
-  int32_t *ws_fine;          // [R][kFineBins] workspace, zero on entry
+  int ws_row0;    // first workspace row of this problem
+  int local;      // rows of at most kClChunk: one CTA per row
+  int vec;        // rows 16-byte aligned: vector loads
+};
+
+struct ClArgs {
+  ClProb p[kClMaxProb];
+  int cl_begin[kClMaxProb + 1];  // first cluster (blockIdx.y) of each problem
+  int nprob;
+  unsigned long long *cand;  // [workspace rows][DSA_CAND_CAP]
+  int32_t *ws_hist;          // [workspace rows][DSA_NUM_BINS], zero on entry
+  int32_t *ws_fine;          // [workspace rows][kFineBins], zero on entry
   uint32_t *status;
 };
 
@@ -774,6 +790,32 @@ __device__ uint32_t bin_prefix_end(int X) {
   return lo;
 }
 
+// Fine map of bin T: its key range [loT, hiT], or for the two bins wider than
+// kFineWindow keys (|x| >= 223 and |x| below the smallest FP16 step) the
+// window of kFineWindow keys at the end nearer to magnitude 1, spread over
+// kFineBins descending fine bins; keys outside the window clamp to the end
+// bins (the map stays monotone, so the select stays exact).
+__device__ __forceinline__ void cl_fine_window(int T, uint32_t loT, uint32_t hiT, uint32_t &flo,
+                                               int &fshift) {
+  uint32_t span1 = hiT - loT;
+  flo = loT;
+  if (span1 >= kFineWindow) {
+    span1 = kFineWindow - 1;
+    const bool pos = T < 512;
+    const int mag = pos ? 511 - T : T - 512;
+    const bool window_low = (mag == 511) ? pos : !pos;
+    if (!window_low) flo = hiT - span1;
+  }
+  fshift = 0;
+  while ((span1 >> fshift) >= (uint32_t)kFineBins) ++fshift;
+}
+
+__device__ __forceinline__ int cl_fine_idx(uint32_t kk, uint32_t flo, int fshift) {
+  const int64_t off = (int64_t)kk - (int64_t)flo;
+  const int64_t f = off <= 0 ? 0 : min((int64_t)(kFineBins - 1), off >> fshift);
+  return (kFineBins - 1) - (int)f;
+}
+
 // The CTA's local histogram (nb bins) is added into the row's workspace copy.
 __device__ __forceinline__ void cl_flush(const int *local, int32_t *row_ws, int nb) {
   for (int i = threadIdx.x; i < nb; i += kClThreads) {
@@ -789,162 +831,116 @@ __device__ __forceinline__ void cl_fetch(int *local, const int32_t *row_ws, int 
   for (int i = threadIdx.x; i < nb / 4; i += kClThreads) dst[i] = __ldcg(src + i);
 }
 
-__global__ void __launch_bounds__(kClThreads, 2) cluster_select_kernel(const ClArgs a) {
-  pdl_wait();  // predecessor grids complete before any global access
-  extern __shared__ __align__(16) unsigned char cl_raw[];
-  ClSmem &sm = *reinterpret_cast<ClSmem *>(cl_raw);
-  __shared__ int sm_h[256];
-  __shared__ int sm_scan[kSelWarps + 1];
-  __shared__ int sm_misc[16];
-  __shared__ uint32_t sm_key[2];
-  __shared__ unsigned long long sm_u64[2];
-  const uint32_t rank = cluster_ctarank();
-  const int r = blockIdx.y;
-  const int k = a.k;
-  const int warp = threadIdx.x >> 5;
-  const int64_t n = row_len(a.ctx, a.next_n, a.len_div, r, a.stride, a.status);
-  const float *row = a.logits + (int64_t)r * a.stride;
-  int32_t *outr = a.out + (int64_t)r * k;
-  unsigned long long *cr = a.cand + (int64_t)r * DSA_CAND_CAP;
-  int32_t *wh = a.ws_hist + (int64_t)r * DSA_NUM_BINS;
-  int32_t *wf = a.ws_fine + (int64_t)r * kFineBins;
-  // this CTA's share: a multiple of 2048 positions; slot (e, tid) holds
-  // position c0 + e * kClThreads + tid
-  const int64_t chunk = ((n + kCl - 1) / kCl + 2047) / 2048 * 2048;
-  const int64_t c0 = (int64_t)rank * chunk;
-  const int64_t c1 = min(n, c0 + chunk);
-  const int vpt = (int)(chunk / kClThreads);  // slots per thread in use (<= kClVpt)
+// Position of slot (q, j) of this thread: c0 + 4 (q kClThreads + tid) + j.
+__device__ __forceinline__ int64_t cl_pos(int64_t c0, int q, int j) {
+  return c0 + 4 * ((int64_t)q * kClThreads + threadIdx.x) + j;
+}
 
-  {
-    float xv[kClVpt];
+// Loads of the CTA's positions [c0, c1) into registers (NaN past c1).
+__device__ __forceinline__ void cl_issue_loads(const float *row, int64_t c0, int64_t c1, int vq,
+                                               bool vec, float4 (&v)[kClVec]) {
+  const float nanv = __int_as_float(0x7fffffff);
 #pragma unroll
-    for (int e = 0; e < kClVpt; ++e) {
-      const int64_t t = c0 + (int64_t)e * kClThreads + threadIdx.x;
-      xv[e] = (e < vpt && t < c1) ? row[t] : __int_as_float(0x7fffffff);
+  for (int q = 0; q < kClVec; ++q) {
+    float4 x = make_float4(nanv, nanv, nanv, nanv);
+    const int64_t t = cl_pos(c0, q, 0);
+    if (q < vq) {
+      if (vec && t + 3 < c1) {
+        x = __ldg(reinterpret_cast<const float4 *>(row + t));
+      } else {
+        if (t < c1) x.x = __ldg(row + t);
+        if (t + 1 < c1) x.y = __ldg(row + t + 1);
+        if (t + 2 < c1) x.z = __ldg(row + t + 2);
+        if (t + 3 < c1) x.w = __ldg(row + t + 3);
+      }
     }
-    if (!a.hist)
-      for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) sm.hist[i] = 0;
-    if (threadIdx.x < 4) sm.ctr[threadIdx.x] = 0;
+    v[q] = x;
+  }
+}
+
+__device__ __forceinline__ uint32_t key_or_zero(float x) {
+  return isnan(x) ? 0u : f32_order_key(x);
+}
+
+__device__ __forceinline__ void cl_store_keys(const float4 (&v)[kClVec], uint4 *keys) {
 #pragma unroll
-    for (int e = 0; e < kClVpt; ++e)
-      sm.keys[e * kClThreads + threadIdx.x] = isnan(xv[e]) ? 0u : f32_order_key(xv[e]);
-  }
-  __syncthreads();
+  for (int q = 0; q < kClVec; ++q)
+    keys[q * kClThreads + threadIdx.x] = make_uint4(key_or_zero(v[q].x), key_or_zero(v[q].y),
+                                                    key_or_zero(v[q].z), key_or_zero(v[q].w));
+}
 
-  // ---- 1. the row's coarse histogram and its threshold bin
-  if (!a.hist) {
-    for (int e = 0; e < vpt; ++e) {
-      const uint32_t kk = sm.keys[e * kClThreads + threadIdx.x];
-      if (kk) atomicAdd(&sm.hist[coarse_bin_of_key(kk)], 1);
-    }
-    __syncthreads();
-    cl_flush(sm.hist, wh, DSA_NUM_BINS);
-  }
-  cluster_sync();  // merged histogram complete; every CTA's shared state ready
-  if (!a.hist) {
-    cl_fetch(sm.hist, wh, DSA_NUM_BINS);
-    __syncthreads();
-  }
-  threshold_from_hist<DSA_NUM_BINS>(a.hist ? a.hist + (int64_t)r * DSA_NUM_BINS : sm.hist, k,
-                                    sm_scan, sm_misc);
-  const int T = sm_misc[0];
-  const int above = sm_misc[1];
-  const int histT = sm_misc[2];
-  // ---- 2. key range of bin T (empty, loT > hiT, when T is past the last bin)
-  if (warp < 2) {
-    const uint32_t g = bin_prefix_end(T + warp);
-    if ((threadIdx.x & 31) == 0) sm_key[warp] = g;
-  }
-  __syncthreads();
-  const uint32_t hiT = sm_key[0];
-  const uint32_t loT = sm_key[1] + 1;
-  const bool fine = (T < DSA_NUM_BINS) && histT > kClDirect;
-
-  // ---- 3. fine histogram of bin T over its key range, fine threshold bin S
-  int fshift = 0, S = 0, above1 = 0, fineS = 0;
-  if (fine) {
-    const uint32_t span1 = hiT - loT;  // key span - 1; offsets (kk - loT) >> fshift < kFineBins
-    while ((span1 >> fshift) >= (uint32_t)kFineBins) ++fshift;
-    for (int i = threadIdx.x; i < kFineBins; i += kClThreads) sm.hist[i] = 0;
-    __syncthreads();
-    for (int e = 0; e < vpt; ++e) {
-      const uint32_t kk = sm.keys[e * kClThreads + threadIdx.x];
-      if (kk >= loT && kk <= hiT) atomicAdd(&sm.hist[(kFineBins - 1) - (int)((kk - loT) >> fshift)], 1);
-    }
-    __syncthreads();
-    cl_flush(sm.hist, wf, kFineBins);
-    cluster_sync();
-    cl_fetch(sm.hist, wf, kFineBins);
-    __syncthreads();
-    threshold_from_hist<kFineBins>(sm.hist, k - above, sm_scan, sm_misc + 10);
-    S = sm_misc[10];
-    above1 = sm_misc[11];
-    fineS = sm_misc[12];
-  }
-
-  // ---- 4. classify (2 bits per slot: 1 emit, 2 candidate), reserve, write
+// Two bits per slot e = 4q + j: 1 = emit (above the threshold), 2 = candidate.
+// nt counts the slots in bin T.
+__device__ __forceinline__ unsigned long long cl_classify(const uint4 *keys, int vq, uint32_t loT,
+                                                          uint32_t hiT, bool fine, uint32_t flo,
+                                                          int fshift, int S, int &nt) {
   unsigned long long kinds = 0;
-  int ne = 0, nc = 0, nt = 0;
+  nt = 0;
 #pragma unroll
-  for (int e = 0; e < kClVpt; ++e) {
-    if (e >= vpt) break;
-    const uint32_t kk = sm.keys[e * kClThreads + threadIdx.x];
-    uint32_t kd = 0;
-    if (kk > hiT) {
-      kd = 1;
-    } else if (kk >= loT) {
-      ++nt;
-      if (!fine) {
-        kd = 2;
-      } else {
-        const int f = (kFineBins - 1) - (int)((kk - loT) >> fshift);
-        kd = (f < S) ? 1u : (f == S ? 2u : 0u);
-      }
-    }
-    kinds |= (unsigned long long)kd << (2 * e);
-    ne += (kd == 1);
-    nc += (kd == 2);
-  }
-  if (threadIdx.x == 0) sm_misc[4] = 0;
-  int tot;
-  const int ex = block_excl_scan((nc << 16) | ne, sm_scan, &tot);  // per CTA < 2^15 each
-  const int ntw = __reduce_add_sync(0xffffffffu, nt);
-  if ((threadIdx.x & 31) == 0 && ntw) atomicAdd(&sm_misc[4], ntw);
-  __syncthreads();
-  const uint32_t ctr0 = dsmem_map(smem_u32(&sm.ctr[0]), 0);
-  if (threadIdx.x == 0) {
-    sm_misc[5] = (tot & 0xFFFF) ? dsmem_atomic_add(ctr0, tot & 0xFFFF) : 0;
-    sm_misc[6] = (tot >> 16) ? dsmem_atomic_add(ctr0 + 4, tot >> 16) : 0;
-    if (sm_misc[4]) dsmem_red_add(ctr0 + 8, sm_misc[4]);
-  }
-  __syncthreads();
-  if (kinds) {
-    int pe = sm_misc[5] + (ex & 0xFFFF);
-    int pc = sm_misc[6] + (ex >> 16);
-    const uint32_t cand0 = dsmem_map(smem_u32(&sm.cand[0]), 0);
+  for (int q = 0; q < kClVec; ++q) {
+    if (q >= vq) break;
+    const uint4 k4 = keys[q * kClThreads + threadIdx.x];
+    const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-    for (int e = 0; e < kClVpt; ++e) {
-      const uint32_t kd = (uint32_t)(kinds >> (2 * e)) & 3u;
-      if (!kd) continue;
-      const int64_t t = c0 + (int64_t)e * kClThreads + threadIdx.x;
-      if (kd == 1) {
-        if (pe < k) outr[pe] = (int32_t)t;
-        ++pe;
-      } else {
-        const unsigned long long v =
-            ((unsigned long long)sm.keys[e * kClThreads + threadIdx.x] << 32) |
-            (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
-        if (pc < kClDirect) dsmem_st64(cand0 + 8u * pc, v);
-        else if (pc < DSA_CAND_CAP) cr[pc] = v;
-        ++pc;
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t kk = kv[j];
+      uint32_t kd = 0;
+      if (kk > hiT) {
+        kd = 1;
+      } else if (kk >= loT) {
+        ++nt;
+        if (!fine) {
+          kd = 2;
+        } else {
+          const int f = cl_fine_idx(kk, flo, fshift);
+          kd = (f < S) ? 1u : (f == S ? 2u : 0u);
+        }
       }
+      kinds |= (unsigned long long)kd << (2 * (4 * q + j));
     }
   }
-  cluster_sync();  // all emits and candidates are in place; histograms read
-  if (rank != 0) return;  // nothing reads another CTA's shared memory from here on
+  return kinds;
+}
 
-  // ---- 5. CTA 0: check the counts, rank or refine, or fall back
-  const int emitted = sm.ctr[0], ncand = sm.ctr[1], n_binT = sm.ctr[2];
+// Writes this thread's emits (output slots pe, pe+1, ...) and candidates
+// (candidate slots pc, pc+1, ...: the first kClDirect in the shared buffer of
+// CTA 0 or of this CTA, the rest in the workspace).
+__device__ __forceinline__ void cl_write(unsigned long long kinds, const uint4 *keys, int64_t c0,
+                                         int pe, int pc, int k, int32_t *outr, bool remote,
+                                         uint32_t cand_remote, unsigned long long *cand_local,
+                                         unsigned long long *cr) {
+  while (kinds) {
+    const int e = (__ffsll((long long)kinds) - 1) >> 1;
+    const uint32_t kd = (uint32_t)(kinds >> (2 * e)) & 3u;
+    kinds &= ~(3ull << (2 * e));
+    const int q = e >> 2, j = e & 3;
+    const int64_t t = cl_pos(c0, q, j);
+    if (kd == 1) {
+      if (pe < k) outr[pe] = (int32_t)t;
+      ++pe;
+    } else {
+      const uint32_t kk = reinterpret_cast<const uint32_t *>(&keys[q * kClThreads + threadIdx.x])[j];
+      const unsigned long long v = ((unsigned long long)kk << 32) |
+                                   (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
+      if (pc < kClDirect) {
+        if (remote) dsmem_st64(cand_remote + 8u * (uint32_t)pc, v);
+        else cand_local[pc] = v;
+      } else if (pc < DSA_CAND_CAP) {
+        cr[pc] = v;
+      }
+      ++pc;
+    }
+  }
+}
+
+// Last step of a row, run by one CTA once every emit and candidate of the row
+// is in place: check the counts, then rank or refine the candidates, or run
+// the exact whole-row fallback.  Returns the fallback flag.
+__device__ int cl_finish(const float *row, int64_t n, int k, int32_t *outr, int T, int above,
+                         int histT, bool fine, int S, int above1, int fineS, int emitted,
+                         int ncand, int n_binT, const unsigned long long *cand,
+                         const unsigned long long *cr, unsigned long long *scratch, int *sm_h,
+                         int *sm_scan, int *sm_misc, unsigned long long *sm_u64) {
   const bool sane = (T < DSA_NUM_BINS) ? (above >= 0 && above < k && histT >= k - above)
                                        : (above >= 0 && above < k);
   int flag = 0, base_out = 0, m = 0;
@@ -968,30 +964,189 @@ __global__ void __launch_bounds__(kClThreads, 2) cluster_select_kernel(const ClA
       // candidate keys are unique (the column is part of the key): each
       // thread ranks one against all the others
       if (threadIdx.x < ncand) {
-        const unsigned long long v = sm.cand[threadIdx.x];
+        const unsigned long long v = cand[threadIdx.x];
         int rk = 0;
-        for (int j = 0; j < ncand; ++j) rk += sm.cand[j] > v;
+        for (int j = 0; j < ncand; ++j) rk += cand[j] > v;
         if (rk < m) outr[base_out + rk] = (int32_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
       }
     } else {
-      unsigned long long *sc = reinterpret_cast<unsigned long long *>(sm.keys);
       for (int i = threadIdx.x; i < ncand; i += kClThreads)
-        sc[i] = i < kClDirect ? sm.cand[i] : __ldcg(cr + i);
+        scratch[i] = i < kClDirect ? cand[i] : __ldcg(cr + i);
       __syncthreads();
-      refine_candidates(sc, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
+      refine_candidates(scratch, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
     }
   } else {
     __syncthreads();
     block_radix_topk_row(row, n, k, outr, sm_h, sm_scan, sm_misc);
   }
-  if (a.flags && threadIdx.x == 0) a.flags[r] = flag;
+  return flag;
+}
+
+__global__ void __launch_bounds__(kClThreads, 2)
+    cluster_select_kernel(const __grid_constant__ ClArgs a) {
+  pdl_wait();  // predecessor grids complete before any global access
+  extern __shared__ __align__(16) unsigned char cl_raw[];
+  ClSmem &sm = *reinterpret_cast<ClSmem *>(cl_raw);
+  __shared__ int sm_h[256];
+  __shared__ int sm_scan[kSelWarps + 1];
+  __shared__ int sm_misc[16];
+  __shared__ uint32_t sm_key[2];
+  __shared__ unsigned long long sm_u64[2];
+  const uint32_t rank = cluster_ctarank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int y = blockIdx.y;
+  int pi = 0;
+  while (pi + 1 < a.nprob && y >= a.cl_begin[pi + 1]) ++pi;
+  const ClProb &p = a.p[pi];
+  const bool local = p.local != 0;
+  const int r = local ? (y - a.cl_begin[pi]) * kCl + (int)rank : y - a.cl_begin[pi];
+  if (local && r >= p.R) return;  // a local CTA passes no cluster barrier
+  const int k = p.k;
+  const int64_t n = row_len(p.ctx, p.next_n, p.len_div, r, p.stride, a.status);
+  const float *row = p.logits + (int64_t)r * p.stride;
+  int32_t *outr = p.out + (int64_t)r * k;
+  const int64_t wr = (int64_t)p.ws_row0 + r;
+  unsigned long long *cr = a.cand + wr * DSA_CAND_CAP;
+  int32_t *wh = a.ws_hist + wr * DSA_NUM_BINS;
+  int32_t *wf = a.ws_fine + wr * kFineBins;
+  const int32_t *hrow = p.hist ? p.hist + (int64_t)r * DSA_NUM_BINS : nullptr;
+  // this CTA's positions [c0, c1), in groups of 2048 (one float4 per thread)
+  const int64_t chunk = ((local ? n : (n + kCl - 1) / kCl) + 2047) / 2048 * 2048;
+  const int64_t c0 = local ? 0 : (int64_t)rank * chunk;
+  const int64_t c1 = min(n, c0 + chunk);
+  const int vq = (int)(chunk / 2048);  // <= kClVec
+
+  if (threadIdx.x < 4) sm.ctr[threadIdx.x] = 0;
+  float4 v[kClVec];
+  cl_issue_loads(row, c0, c1, vq, p.vec != 0, v);
+
+  // ---- 1, 2. threshold bin T and its key range
+  int T, above, histT;
+  if (hrow) {
+    if (!local) cluster_arrive();  // counters zeroed; the wait comes after the loads
+    threshold_from_hist<DSA_NUM_BINS>(hrow, k, sm_scan, sm_misc);
+    T = sm_misc[0];
+    above = sm_misc[1];
+    histT = sm_misc[2];
+    cl_store_keys(v, sm.keys);
+  } else {
+    for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) sm.hist[i] = 0;
+    cl_store_keys(v, sm.keys);
+    __syncthreads();
+    for (int q = 0; q < vq; ++q) {
+      const uint4 k4 = sm.keys[q * kClThreads + threadIdx.x];
+      const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (kv[j]) atomicAdd(&sm.hist[coarse_bin_of_key(kv[j])], 1);
+    }
+    __syncthreads();
+    if (!local) {
+      cl_flush(sm.hist, wh, DSA_NUM_BINS);
+      cluster_arrive();
+      cluster_wait();
+      cl_fetch(sm.hist, wh, DSA_NUM_BINS);
+      __syncthreads();
+    }
+    threshold_from_hist<DSA_NUM_BINS>(sm.hist, k, sm_scan, sm_misc);
+    T = sm_misc[0];
+    above = sm_misc[1];
+    histT = sm_misc[2];
+  }
+  if (warp < 2) {
+    const uint32_t g = bin_prefix_end(T + warp);
+    if (lane == 0) sm_key[warp] = g;
+  }
+  __syncthreads();
+  const uint32_t hiT = sm_key[0];
+  const uint32_t loT = sm_key[1] + 1;  // loT > hiT: bin T empty (T past the last bin)
+  if (hrow && !local) cluster_wait();  // every CTA's counters are zero from here on
+
+  // ---- 3. fine histogram of bin T, fine threshold bin S
+  const bool fine = (T < DSA_NUM_BINS) && histT > kClDirect;
+  uint32_t flo = 0;
+  int fshift = 0, S = 0, above1 = 0, fineS = 0;
+  if (fine) {
+    cl_fine_window(T, loT, hiT, flo, fshift);
+    for (int i = threadIdx.x; i < kFineBins; i += kClThreads) sm.hist[i] = 0;
+    __syncthreads();
+    for (int q = 0; q < vq; ++q) {
+      const uint4 k4 = sm.keys[q * kClThreads + threadIdx.x];
+      const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (kv[j] >= loT && kv[j] <= hiT) atomicAdd(&sm.hist[cl_fine_idx(kv[j], flo, fshift)], 1);
+    }
+    __syncthreads();
+    if (!local) {
+      cl_flush(sm.hist, wf, kFineBins);
+      cluster_sync();
+      cl_fetch(sm.hist, wf, kFineBins);
+      __syncthreads();
+    }
+    threshold_from_hist<kFineBins>(sm.hist, k - above, sm_scan, sm_misc + 10);
+    S = sm_misc[10];
+    above1 = sm_misc[11];
+    fineS = sm_misc[12];
+  }
+
+  // ---- 4. classify, reserve, write
+  int nt;
+  const unsigned long long kinds = cl_classify(sm.keys, vq, loT, hiT, fine, flo, fshift, S, nt);
+  const int ne = __popcll(kinds & 0x5555555555555555ull);
+  const int nc = __popcll(kinds & 0xAAAAAAAAAAAAAAAAull);
+  if (threadIdx.x == 0) sm_misc[4] = 0;
+  int tot;
+  const int ex = block_excl_scan((nc << 16) | ne, sm_scan, &tot);  // per CTA < 2^15 each
+  const int ntw = __reduce_add_sync(0xffffffffu, nt);
+  if (lane == 0 && ntw) atomicAdd(&sm_misc[4], ntw);
+  __syncthreads();
+  int base_e = 0, base_c = 0;
+  uint32_t cand0 = 0;
+  if (!local) {
+    const uint32_t ctr0 = dsmem_map(smem_u32(&sm.ctr[0]), 0);
+    if (threadIdx.x == 0) {
+      sm_misc[5] = (tot & 0xFFFF) ? dsmem_atomic_add(ctr0, tot & 0xFFFF) : 0;
+      sm_misc[6] = (tot >> 16) ? dsmem_atomic_add(ctr0 + 4, tot >> 16) : 0;
+      if (sm_misc[4]) dsmem_red_add(ctr0 + 8, sm_misc[4]);
+    }
+    __syncthreads();
+    base_e = sm_misc[5];
+    base_c = sm_misc[6];
+    cand0 = dsmem_map(smem_u32(&sm.cand[0]), 0);
+  }
+  if (kinds)
+    cl_write(kinds, sm.keys, c0, base_e + (ex & 0xFFFF), base_c + (ex >> 16), k, outr, !local,
+             cand0, sm.cand, cr);
+  int emitted, ncand, n_binT;
+  if (!local) {
+    cluster_sync();  // all emits and candidates are in place; histograms read
+    if (rank != 0) return;  // nothing reads another CTA's shared memory from here on
+    emitted = sm.ctr[0];
+    ncand = sm.ctr[1];
+    n_binT = sm.ctr[2];
+  } else {
+    __syncthreads();
+    emitted = tot & 0xFFFF;
+    ncand = tot >> 16;
+    n_binT = sm_misc[4];
+  }
+
+  // ---- 5. check, rank or refine, or fall back
+  const int flag = cl_finish(row, n, k, outr, T, above, histT, fine, S, above1, fineS, emitted,
+                             ncand, n_binT, sm.cand, cr,
+                             reinterpret_cast<unsigned long long *>(sm.keys), sm_h, sm_scan,
+                             sm_misc, sm_u64);
+  if (p.flags && threadIdx.x == 0) p.flags[r] = flag;
   // restore the zero workspace histograms; clear the caller's on request
-  if (!a.hist)
-    for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) wh[i] = 0;
-  if (fine)
-    for (int i = threadIdx.x; i < kFineBins; i += kClThreads) wf[i] = 0;
-  if (a.reset_hist && a.hist) {
-    int32_t *hw = a.hist + (int64_t)r * DSA_NUM_BINS;
+  if (!local) {
+    if (!hrow)
+      for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) wh[i] = 0;
+    if (fine)
+      for (int i = threadIdx.x; i < kFineBins; i += kClThreads) wf[i] = 0;
+  }
+  if (p.reset_hist && p.hist) {
+    int32_t *hw = p.hist + (int64_t)r * DSA_NUM_BINS;
     for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) hw[i] = 0;
   }
 }
@@ -1267,6 +1422,89 @@ int32_t topk_launch_count(int64_t stride, bool has_histogram, bool allow_cluster
   return has_histogram ? 2 : 3;
 }
 
+bool topk_batchable(const TopkCall *calls, int count) {
+  if (count < 1 || count > kClMaxProb) return false;
+  for (int i = 0; i < count; ++i)
+    if (!calls[i].allow_cluster || calls[i].stride > kClRow) return false;
+  return true;
+}
+
+namespace {
+
+// One cluster launch for problems whose rows are all at most kClRow long;
+// problem i takes workspace rows from the sum of the earlier problems' R.
+dsa_status_t run_cluster_select(const TopkCall *calls, int count, cudaStream_t st) {
+  char *ws = static_cast<char *>(calls[0].workspace);
+  const int64_t wrows = calls[0].ws_rows;
+  ClArgs ca{};
+  ca.nprob = count;
+  ca.cand = reinterpret_cast<unsigned long long *>(ws + WsLayout::cand_off(wrows));
+  ca.ws_hist = reinterpret_cast<int32_t *>(ws + WsLayout::hist_off(wrows));
+  ca.ws_fine = reinterpret_cast<int32_t *>(ws + WsLayout::fine_off(wrows));
+  ca.status = reinterpret_cast<uint32_t *>(ws + WsLayout::kStatusOff);
+  int64_t row0 = 0, clusters = 0;
+  for (int i = 0; i < count; ++i) {
+    const TopkCall &c = calls[i];
+    ClProb &p = ca.p[i];
+    p.logits = c.logits;
+    p.stride = c.stride;
+    p.ctx = c.context_lens;
+    p.next_n = c.next_n;
+    p.len_div = c.len_div;
+    p.R = c.R;
+    p.hist = c.histogram;
+    p.reset_hist = c.reset_histogram ? 1 : 0;
+    p.k = c.k;
+    p.out = c.out_idx;
+    p.flags = c.fallback_flags;
+    p.ws_row0 = (int)row0;
+    p.local = c.stride <= kClChunk ? 1 : 0;
+    p.vec = ((reinterpret_cast<uintptr_t>(c.logits) & 15) == 0 && c.stride % 4 == 0) ? 1 : 0;
+    ca.cl_begin[i] = (int)clusters;
+    clusters += p.local ? (c.R + kCl - 1) / kCl : c.R;
+    row0 += c.R;
+  }
+  ca.cl_begin[count] = (int)clusters;
+  if (row0 > wrows) return DSA_ERR_WORKSPACE;
+  if (clusters == 0) return DSA_OK;
+  if (clusters > 65535) return DSA_ERR_UNSUPPORTED;
+  const int smem = (int)sizeof(ClSmem);
+  if (!ensure_smem_attr(reinterpret_cast<const void *>(cluster_select_kernel), smem))
+    return DSA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCl, (unsigned)clusters);
+  cfg.blockDim = dim3(kClThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, cluster_select_kernel, ca);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    (void)cudaGetLastError();
+    return DSA_ERR_CUDA;
+  }
+  return DSA_OK;
+}
+
+}  // namespace
+
+dsa_status_t run_topk_batch(const TopkCall *calls, int count, cudaStream_t st) {
+  if (topk_batchable(calls, count)) return run_cluster_select(calls, count, st);
+  for (int i = 0; i < count; ++i) {  // stream order: each call may reuse the workspace rows
+    const dsa_status_t e = run_topk(calls[i], st);
+    if (e != DSA_OK) return e;
+  }
+  return DSA_OK;
+}
+
 dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
   char *ws = static_cast<char *>(c.workspace);
   uint32_t *status = reinterpret_cast<uint32_t *>(ws + WsLayout::kStatusOff);
@@ -1282,48 +1520,7 @@ dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
   while ((c.stride + chunk - 1) / chunk > 65535) chunk *= 2;
   const int64_t nchunks = std::max<int64_t>(1, (c.stride + chunk - 1) / chunk);
   if (nchunks > 65535 || c.R > 65535) return DSA_ERR_UNSUPPORTED;
-  if (c.allow_cluster && c.stride <= kClRow) {
-    // one cluster of kCl CTAs per row, the row held in registers
-    ClArgs ca;
-    ca.logits = c.logits;
-    ca.stride = c.stride;
-    ca.ctx = c.context_lens;
-    ca.next_n = c.next_n;
-    ca.len_div = c.len_div;
-    ca.hist = c.histogram;
-    ca.reset_hist = c.reset_histogram ? 1 : 0;
-    ca.k = c.k;
-    ca.out = c.out_idx;
-    ca.flags = c.fallback_flags;
-    ca.cand = cand;
-    ca.ws_hist = ws_hist;
-    ca.ws_fine = fine;
-    ca.status = status;
-    const int smem = (int)sizeof(ClSmem);
-    if (!ensure_smem_attr(reinterpret_cast<const void *>(cluster_select_kernel), smem))
-      return DSA_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kCl, (unsigned)c.R);
-    cfg.blockDim = dim3(kClThreads);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, cluster_select_kernel, ca);
-    if (e != cudaSuccess) {
-      record_cuda_error(e);
-      (void)cudaGetLastError();
-      return DSA_ERR_CUDA;
-    }
-    return DSA_OK;
-  }
+  if (topk_batchable(&c, 1)) return run_cluster_select(&c, 1, st);
   if (!c.histogram && c.stride <= kSmemRow) {
     // short rows, no histogram: one CTA per row, the row held in shared memory
     const int smem = kSmemRow * 4;

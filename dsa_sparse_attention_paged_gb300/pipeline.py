@@ -6,11 +6,11 @@ step's device buffers and the workspace, and each ``step`` runs
 
   source layer   paged MQA logits + fused coarse histogram + fused
                  block maxima over 8 scores                        (1 launch)
-                 histogram-driven exact top-k (resets the hist)   (1 launch for
-                 rows up to 131072 scores, else 2)
-  level one      top-kb of the block maxima                        (1 launch for
-                 rows up to 131072 blocks, else 3)
-                 sort_candidate_blocks -> table, phys, valid lens   (1 launch)
+                 histogram-driven exact top-k of the logits rows
+                 (resets the hist) and top-kb of the block-maxima
+                 rows, as two problems of one batched select       (1 launch
+                 for rows up to 131072 scores)
+  level one      sort_candidate_blocks -> table, phys, valid lens   (1 launch)
   consumer       sparse MQA logits over the table, FP16 output      (1 launch)
                  FP16 top-k with the fused table transform          (1 launch)
 
@@ -22,7 +22,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (OUT_F16, Workspace, coarse_hist_topk, coarse_hist_topk_launches, paged_mqa_logits,
+from . import (OUT_F16, Workspace, coarse_hist_topk, coarse_hist_topk_batch,
+               coarse_hist_topk_batch_launches, coarse_hist_topk_launches, paged_mqa_logits,
                sort_candidate_blocks, sparse_mqa_logits, topk_fp16)
 
 
@@ -37,7 +38,8 @@ class DecodePlan:
         self.stride = (int(max_context) + 7) // 8 * 8
         dev = torch.device(device)
         R = self.R
-        self.ws = Workspace(R, device=dev)
+        # rows for the logits problem and, two-level, the block-maxima problem
+        self.ws = Workspace(2 * R if two_level else R, device=dev)
         self.logits = torch.empty((R, self.stride), dtype=torch.float32, device=dev)
         self.hist = torch.zeros((R, 1024), dtype=torch.int32, device=dev)
         self.topk_idx = torch.empty((R, k), dtype=torch.int32, device=dev)
@@ -53,10 +55,11 @@ class DecodePlan:
     @property
     def launches_per_step(self) -> int:
         """Kernels of this library launched by one step."""
-        n = 1 + coarse_hist_topk_launches(self.stride, True)  # logits (+ hist, maxima), top-k
-        if self.two_level:
-            n += coarse_hist_topk_launches(self.amax_stride, False) + 1 + 1 + 1
-        return n
+        if not self.two_level:
+            return 1 + coarse_hist_topk_launches(self.stride, True)
+        sel = coarse_hist_topk_batch_launches([(self.stride, True, self.R),
+                                               (self.amax_stride, False, self.R)])
+        return 1 + sel + 1 + 1 + 1
 
     def step(self, q, kv, kscale, weights, page_table, context_lens, events=None):
         """Run one decode step.  ``events`` (optional dict name -> (start, end)
@@ -73,15 +76,20 @@ class DecodePlan:
                          amax=self.amax if self.two_level else None,
                          amax_skip_if_blocks_le=self.kb)
         mark("logits", 1)
-        mark("topk", 0)
-        coarse_hist_topk(self.logits, context_lens, nn, self.k, ws, histogram=self.hist,
-                         reset_histogram=True, out=self.topk_idx)
-        mark("topk", 1)
         if not self.two_level:
+            mark("select", 0)
+            coarse_hist_topk(self.logits, context_lens, nn, self.k, ws, histogram=self.hist,
+                             reset_histogram=True, out=self.topk_idx)
+            mark("select", 1)
             return self.topk_idx, None
+        mark("select", 0)
+        coarse_hist_topk_batch([
+            dict(logits=self.logits, context_lens=context_lens, next_n=nn, k=self.k,
+                 histogram=self.hist, reset_histogram=True, out=self.topk_idx),
+            dict(logits=self.amax, context_lens=context_lens, next_n=nn, k=self.kb, len_div=8,
+                 out=self.block_ids)], ws)
+        mark("select", 1)
         mark("publish", 0)
-        coarse_hist_topk(self.amax, context_lens, nn, self.kb, ws, histogram=None,
-                         len_div=8, out=self.block_ids)
         sort_candidate_blocks(self.block_ids, context_lens, nn, page_table, self.page_size, ws,
                               phys_blocks=self.phys, valid_lens=self.valid_lens)
         mark("publish", 1)

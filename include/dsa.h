@@ -186,6 +186,41 @@ int32_t dsa_coarse_hist_topk(const float *logits, int64_t stride, const int32_t 
  * for stride < 1. */
 int32_t dsa_coarse_hist_topk_launches(int64_t stride, int32_t has_histogram);
 
+/* ---- several top-k problems in one launch --------------------------------
+ * Not a separate operation of the source pages: the decode step's top-2048 of
+ * the logits rows and top-kb of the block-maxima rows ([SG38944]) are
+ * independent, so they can share one launch.  Each problem has exactly the
+ * arguments and results of dsa_coarse_hist_topk; no two problems may write
+ * the same memory.  One workspace serves all of them: it must be sized for
+ * the sum of their R (problem i uses the rows after those of problems
+ * 0..i-1).  When count <= DSA_TOPK_BATCH_MAX and every stride is at most
+ * 131072 the problems run in one launch, otherwise one after another on the
+ * stream.  Problems with R = 0 are skipped unchecked (their pointers may be
+ * NULL); argument errors are reported for the first offending problem before
+ * anything is launched. */
+#define DSA_TOPK_BATCH_MAX 4
+typedef struct dsa_topk_problem {
+  const float *logits;
+  int64_t stride;
+  const int32_t *context_lens;
+  int32_t *histogram;
+  int32_t *out_idx;
+  int32_t *fallback_flags;
+  int32_t next_n;
+  int32_t len_div;
+  int32_t R;
+  int32_t reset_histogram;
+  int32_t k;
+  int32_t reserved;  /* set to 0 */
+} dsa_topk_problem;
+
+int32_t dsa_coarse_hist_topk_batch(const dsa_topk_problem *problems, int32_t count,
+                                   void *workspace, size_t ws_bytes, void *stream);
+
+/* Kernel launches dsa_coarse_hist_topk_batch makes for these problems (host
+ * only, no device work); -DSA_ERR_INVALID_ARG for a bad count or stride. */
+int32_t dsa_coarse_hist_topk_batch_launches(const dsa_topk_problem *problems, int32_t count);
+
 /* ---- top-k without a caller workspace --------------------------------------
  * The pages have no counterpart to this entry point; it exists for callers
  * that cannot allocate device memory at the point where they select -- for

@@ -111,3 +111,19 @@ def test_topk_launch_count_follows_the_dispatch():
     assert D.coarse_hist_topk_launches(1 << 20, False) == 3
     with pytest.raises(ValueError):
         D.coarse_hist_topk_launches(0, True)
+
+
+def test_topk_problem_layout_and_batch_launch_count():
+    """dsa_topk_problem is 72 bytes (six 8-byte fields, six int32); the batch
+    runs in one launch when every row stride is at most 131072."""
+    import ctypes
+    import dsa_sparse_attention_paged_gb300 as D
+    assert ctypes.sizeof(D.TopkProblem) == 72
+    assert D.TopkProblem.next_n.offset == 48
+    n = D.coarse_hist_topk_batch_launches
+    assert n([(131072, True, 32), (16384, False, 32)]) == 1
+    assert n([(200000, True, 2), (16384, False, 2)]) == 2 + 1
+    assert n([(200000, True, 0), (16384, False, 2)]) == 1  # empty problems are skipped
+    assert n([(16384, False, 0)]) == 0
+    with pytest.raises(ValueError):
+        n([(100, True, 1)] * 5)

@@ -1,0 +1,116 @@
+"""The batched select (several independent top-k problems, one launch) and
+the windowed fine histogram of the two widest coarse bins, against the
+oracle's full-sort top-k on the same scores."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from tests.helpers import make, sets_equal, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("B,nn,ctx,ps,dist", [
+    (3, 1, [40000, 9000, 70000], 64, "mixed"),     # logits rows: clusters; maxima: one CTA a row
+    (2, 2, [131072, 20000], 64, "normal"),         # the longest rows a cluster takes
+    (9, 1, [5000] * 4 + [16000] * 5, 64, "unit"),  # short rows only: eight rows a cluster
+])
+def test_logits_and_block_maxima_in_one_launch(B, nn, ctx, ps, dist):
+    import dsa_sparse_attention_paged_gb300 as D
+    case = make(B, nn, ctx, ps, dist, seed=300 + B)
+    d = to_dev(case)
+    R = B * nn
+    stride = (max(ctx) + 7) // 8 * 8
+    ws = D.Workspace(2 * R)
+    logits = torch.full((R, stride), float("nan"), dtype=torch.float32, device="cuda")
+    hist = torch.zeros((R, 1024), dtype=torch.int32, device="cuda")
+    amax = torch.full((R, stride // 8), float("nan"), dtype=torch.float32, device="cuda")
+    D.paged_mqa_logits(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"],
+                       d["context_lens"], nn, ws, logits=logits, histogram=hist, amax=amax)
+    flags = torch.full((2, R), 9, dtype=torch.int32, device="cuda")
+    outs = D.coarse_hist_topk_batch([
+        dict(logits=logits, context_lens=d["context_lens"], next_n=nn, k=2048, histogram=hist,
+             reset_histogram=True, fallback_flags=flags[0]),
+        dict(logits=amax, context_lens=d["context_lens"], next_n=nn, k=512, len_div=8,
+             fallback_flags=flags[1])], ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    rl = O.row_lens(case["context_lens"], nn)
+    L = logits.cpu().numpy()
+    assert sets_equal(outs[0].cpu().numpy(), O.topk(L, rl, 2048))
+    A = amax.cpu().numpy()
+    assert sets_equal(outs[1].cpu().numpy(), O.topk(A, (rl + 7) // 8, 512))
+    assert (flags.cpu().numpy() == 0).all()
+    assert (hist.cpu().numpy() == 0).all()
+    # the workspace is left zeroed: a second batch on it gives the same result
+    hist2 = torch.from_numpy(O.histogram(L, rl)).cuda()
+    again = D.coarse_hist_topk_batch([
+        dict(logits=logits, context_lens=d["context_lens"], next_n=nn, k=2048, histogram=hist2),
+        dict(logits=amax, context_lens=d["context_lens"], next_n=nn, k=512, len_div=8)], ws)
+    torch.cuda.synchronize()
+    assert sets_equal(again[0].cpu().numpy(), outs[0].cpu().numpy())
+    assert sets_equal(again[1].cpu().numpy(), outs[1].cpu().numpy())
+
+
+def test_batch_with_a_long_row_problem_runs_in_sequence_and_skips_empty():
+    import dsa_sparse_attention_paged_gb300 as D
+    rng = np.random.default_rng(5)
+    x1 = rng.normal(0, 4, (2, 150000)).astype(np.float32)   # longer than a cluster's row
+    x2 = rng.normal(0, 4, (3, 3000)).astype(np.float32)
+    ctx1 = torch.full((2,), 150000, dtype=torch.int32, device="cuda")
+    ctx2 = torch.tensor([3000, 17, 2500], dtype=torch.int32, device="cuda")
+    L1, L2 = torch.from_numpy(x1).cuda(), torch.from_numpy(x2).cuda()
+    empty = torch.zeros((0, 64), dtype=torch.float32, device="cuda")
+    ws = D.Workspace(5)
+    o1, o0, o2 = D.coarse_hist_topk_batch([
+        dict(logits=L1, context_lens=ctx1, next_n=1, k=2048),
+        dict(logits=empty, context_lens=ctx2, next_n=1, k=16),
+        dict(logits=L2, context_lens=ctx2, next_n=1, k=100)], ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0 and o0.shape == (0, 16)
+    assert sets_equal(o1.cpu().numpy(), O.topk(x1, np.full(2, 150000), 2048))
+    assert sets_equal(o2.cpu().numpy(), O.topk(x2, np.array([3000, 17, 2500]), 100))
+
+
+def test_batch_rejects_a_small_workspace_before_launching():
+    import dsa_sparse_attention_paged_gb300 as D
+    x = torch.zeros((4, 100), dtype=torch.float32, device="cuda")
+    ctx = torch.full((4,), 100, dtype=torch.int32, device="cuda")
+    ws = D.Workspace(6)
+    with pytest.raises(D.DSAError) as e:
+        D.coarse_hist_topk_batch([dict(logits=x, context_lens=ctx, next_n=1, k=8)] * 2, ws)
+    assert e.value.status == 5
+
+
+@pytest.mark.parametrize("n", [40000, 12000])
+@pytest.mark.parametrize("kind", ["pos_saturating", "neg_saturating", "tiny"])
+def test_widest_bins_use_a_fine_window(kind, n):
+    """Bin T is |x| >= 223 or |x| below the smallest FP16 step, whose key
+    ranges are far wider than the fine histogram: the window at the end nearer
+    to magnitude 1 is resolved, keys beyond it clamp to the end fine bins;
+    the result stays exact (clusters at n = 40000, one CTA at n = 12000)."""
+    import dsa_sparse_attention_paged_gb300 as D
+    R = 3
+    rng = np.random.default_rng(17)
+    x = rng.normal(-50, 1, (R, n)).astype(np.float32)
+    m = 6000
+    if kind == "pos_saturating":
+        x[:, :m] = np.exp(rng.uniform(np.log(223.0), np.log(1e9), (R, m))).astype(np.float32)
+        x[1, :3000] = np.exp(rng.uniform(np.log(1e6), np.log(1e30), 3000)).astype(np.float32)
+    elif kind == "neg_saturating":
+        x = -np.exp(rng.uniform(np.log(223.0), np.log(1e12), (R, n))).astype(np.float32)
+        x[2, :50] = -np.inf
+    else:
+        x[:, :m] = rng.uniform(0, 3.5e-6, (R, m)).astype(np.float32)
+        x[1, :2000] = rng.uniform(0, 1e-30, 2000).astype(np.float32)
+        x[2, :100] = 0.0
+    L = torch.from_numpy(x).cuda()
+    ctx = torch.full((R,), n, dtype=torch.int32, device="cuda")
+    hist = torch.from_numpy(O.histogram(x, np.full(R, n))).cuda()
+    ws = D.Workspace(R)
+    for h in (hist, None):
+        out = D.coarse_hist_topk(L, ctx, 1, 2048, ws, histogram=h)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
+        assert sets_equal(out.cpu().numpy(), O.topk(x, np.full(R, n), 2048)), h is None
