@@ -83,6 +83,7 @@ def _load():
         "dsa_topk_fp16": (i32, [P, i64, P, i32, i32, P, i32, P, P, sz, P]),
         "dsa_coarse_hist_topk_noalloc": (i32, [P, i64, P, i32, i32, i32, P, i32, i32, P, P, P]),
         "dsa_coarse_bins_range": (i32, [u32, i64, P, P]),
+        "dsa_coarse_bin_key_ranges": (i32, [P, P]),
         "dsa_fp16_order_keys": (i32, [P, P, i64, P]),
         "dsa_wait_timeout_selftest": (i32, [u64, P, sz, P]),
     }
@@ -307,6 +308,14 @@ def topk_fp16(scores, valid_lens, k, ws, block_table=None, out=None, stream=None
     _check(lib.dsa_topk_fp16(_p(s), s.stride(0), _p(valid_lens), R, k, _p(block_table), kb,
                              _p(out), ws.ptr, ws.nbytes, _stream(stream)), "topk_fp16")
     return out
+
+
+def coarse_bin_key_ranges(stream=None):
+    """[1025][2] uint32 (as int64): lowest and highest order key of each coarse
+    bin as the select computes them (bin 1024: an empty range)."""
+    out = torch.zeros(2 * 1025, dtype=torch.int32, device="cuda")
+    _check(lib.dsa_coarse_bin_key_ranges(_p(out), _stream(stream)), "coarse_bin_key_ranges")
+    return (out.cpu().to(torch.int64) & 0xFFFFFFFF).view(1025, 2)
 
 
 def coarse_bins_range(start: int, count: int, out=None, stream=None):

@@ -442,6 +442,11 @@ int32_t dsa_topk_fp16(const uint16_t *scores, int64_t stride, const int32_t *val
   return run_topk_fp16(c, static_cast<cudaStream_t>(stream));
 }
 
+int32_t dsa_coarse_bin_key_ranges(uint32_t *out, void *stream) {
+  if (!out) return DSA_ERR_INVALID_ARG;
+  return run_bin_key_ranges(out, static_cast<cudaStream_t>(stream));
+}
+
 int32_t dsa_coarse_bins_range(uint32_t start, int64_t count, int16_t *out, void *stream) {
   if (count < 0 || (count > 0 && !out)) return DSA_ERR_INVALID_ARG;
   return run_bins_range(start, count, out, static_cast<cudaStream_t>(stream));

@@ -86,6 +86,7 @@ dsa_status_t run_sort_blocks(int32_t *ids, int32_t kb, const int32_t *context_le
                              int32_t *valid_lens, uint32_t *status, cudaStream_t st);
 
 dsa_status_t run_bins_range(uint32_t start, int64_t count, int16_t *out, cudaStream_t st);
+dsa_status_t run_bin_key_ranges(uint32_t *out, cudaStream_t st);
 dsa_status_t run_fp16_keys(const uint16_t *in, uint16_t *out, int64_t n, cudaStream_t st);
 dsa_status_t run_wait_selftest(uint64_t limit, uint32_t *status, cudaStream_t st);
 

@@ -721,12 +721,13 @@ constexpr int kClChunk = kClThreads * kClVpt;    // 16384 per CTA
 constexpr int kClRow = kCl * kClChunk;           // 131072
 constexpr int kClDirect = kClThreads;            // candidates ranked directly
 constexpr int kClMaxProb = 4;                    // problems per launch
+constexpr int kClFine = 1024;                    // fine bins
 constexpr uint32_t kFineWindow = 1u << 26;       // keys one fine histogram spans at most
 static_assert(kClThreads == kSelThreads, "block scans assume kSelThreads threads");
 
 struct ClSmem {
   uint4 keys[kClVec * kClThreads];      // keys[q * kClThreads + tid] = slots 4q..4q+3 of tid
-  int hist[kFineBins];                  // local coarse / fine histogram, then the row's
+  int hist[DSA_NUM_BINS];               // local coarse / fine histogram, then the row's
   unsigned long long cand[kClDirect];   // the row's first candidates (CTA 0 / local CTA)
   int ctr[4];                           // CTA 0: emitted, candidates, bin-T count
 };
@@ -766,34 +767,46 @@ __device__ __forceinline__ int coarse_bin_of_key(uint32_t key) {
   return coarse_bin(__uint_as_float(bits));
 }
 
-// Largest non-NaN key whose coarse bin is >= X, kKeyNegInf - 1 if none.  The
-// keys with bin >= X are a prefix of the non-NaN keys because the bin never
-// increases with the value.  Run by one full warp (32-way search, 7 rounds);
-// every lane returns the result.
-__device__ uint32_t bin_prefix_end(int X) {
-  const int lane = threadIdx.x & 31;
-  uint32_t lo = kKeyNegInf - 1, hi = kKeyPosInf;  // answer in [lo, hi]
-  while (hi > lo) {
-    const uint32_t step = (hi - lo + 31) / 32;  // >= 1; lo + 32 step <= hi + 31
-    const uint32_t pt = min(hi, lo + step * (uint32_t)(lane + 1));
-    const unsigned bal = __ballot_sync(0xffffffffu, coarse_bin_of_key(pt) >= X);
-    const int nt = __popc(bal);  // the predicate holds on a prefix of the lanes
-    const uint32_t p_last = __shfl_sync(0xffffffffu, pt, max(nt - 1, 0));
-    const uint32_t p_next = __shfl_sync(0xffffffffu, pt, min(nt, 31));
-    if (nt == 0) {
-      hi = p_last - 1;  // p_last is lane 0's point lo + step
-    } else {
-      lo = p_last;
-      if (nt < 32) hi = p_next - 1;
-    }
+// Smallest magnitude with coarse magnitude code >= m (1 <= m <= 511), from
+// the bin rules: 223 for the saturating code; m - 288 for the unit bins
+// (codes 305..510); for codes 1..304 the midpoint between the FP16 values
+// 64m - 1 and 64m, which round-to-nearest-even sends up to the even 64m.  The
+// midpoint of two FP16 values is exact in FP32.
+__device__ __forceinline__ float code_lo_mag(int m) {
+  if (m == 511) return 223.0f;
+  if (m >= 305) return (float)(m - 288);
+  const float h1 = __half2float(__ushort_as_half((unsigned short)(64 * m - 1)));
+  const float h2 = __half2float(__ushort_as_half((unsigned short)(64 * m)));
+  return 0.5f * (h1 + h2);
+}
+
+// Exact order-key range [loT, hiT] of coarse bin T (bins descend with the
+// value, so every bin is one key range); empty (loT > hiT) for T past the
+// last bin.  Bin T < 512 holds x in [A(m), A(m+1)) with m = 511 - T (x >= 223
+// for m = 511, x >= +0 for m = 0); bin T >= 512 holds x in (-A(m+1), -A(m)]
+// with m = T - 512 (-0 for m = 0, down to -inf for m = 511).
+__device__ __forceinline__ void bin_key_range(int T, uint32_t &loT, uint32_t &hiT) {
+  if (T >= DSA_NUM_BINS) {
+    loT = kKeyNegInf;
+    hiT = kKeyNegInf - 1;
+    return;
   }
-  return lo;
+  const bool pos = T < 512;
+  const int m = pos ? 511 - T : T - 512;
+  const float a0 = m == 0 ? 0.0f : code_lo_mag(m);
+  if (pos) {
+    loT = f32_order_key(a0);
+    hiT = m == 511 ? kKeyPosInf : f32_order_key(code_lo_mag(m + 1)) - 1;
+  } else {
+    hiT = f32_order_key(-a0);
+    loT = m == 511 ? kKeyNegInf : f32_order_key(-code_lo_mag(m + 1)) + 1;
+  }
 }
 
 // Fine map of bin T: its key range [loT, hiT], or for the two bins wider than
 // kFineWindow keys (|x| >= 223 and |x| below the smallest FP16 step) the
 // window of kFineWindow keys at the end nearer to magnitude 1, spread over
-// kFineBins descending fine bins; keys outside the window clamp to the end
+// kClFine descending fine bins; keys outside the window clamp to the end
 // bins (the map stays monotone, so the select stays exact).
 __device__ __forceinline__ void cl_fine_window(int T, uint32_t loT, uint32_t hiT, uint32_t &flo,
                                                int &fshift) {
@@ -807,13 +820,13 @@ __device__ __forceinline__ void cl_fine_window(int T, uint32_t loT, uint32_t hiT
     if (!window_low) flo = hiT - span1;
   }
   fshift = 0;
-  while ((span1 >> fshift) >= (uint32_t)kFineBins) ++fshift;
+  while ((span1 >> fshift) >= (uint32_t)kClFine) ++fshift;
 }
 
 __device__ __forceinline__ int cl_fine_idx(uint32_t kk, uint32_t flo, int fshift) {
   const int64_t off = (int64_t)kk - (int64_t)flo;
-  const int64_t f = off <= 0 ? 0 : min((int64_t)(kFineBins - 1), off >> fshift);
-  return (kFineBins - 1) - (int)f;
+  const int64_t f = off <= 0 ? 0 : min((int64_t)(kClFine - 1), off >> fshift);
+  return (kClFine - 1) - (int)f;
 }
 
 // The CTA's local histogram (nb bins) is added into the row's workspace copy.
@@ -936,22 +949,24 @@ __device__ __forceinline__ void cl_write(unsigned long long kinds, const uint4 *
 // Last step of a row, run by one CTA once every emit and candidate of the row
 // is in place: check the counts, then rank or refine the candidates, or run
 // the exact whole-row fallback.  Returns the fallback flag.
-__device__ int cl_finish(const float *row, int64_t n, int k, int32_t *outr, int T, int above,
-                         int histT, bool fine, int S, int above1, int fineS, int emitted,
-                         int ncand, int n_binT, const unsigned long long *cand,
+__device__ int cl_finish(const float *row, int64_t n, int k, int32_t *outr, bool take_all, int T,
+                         int above, int histT, bool fine, int S, int above1, int fineS,
+                         int emitted, int ncand, int n_binT, const unsigned long long *cand,
                          const unsigned long long *cr, unsigned long long *scratch, int *sm_h,
                          int *sm_scan, int *sm_misc, unsigned long long *sm_u64) {
   const bool sane = (T < DSA_NUM_BINS) ? (above >= 0 && above < k && histT >= k - above)
                                        : (above >= 0 && above < k);
   int flag = 0, base_out = 0, m = 0;
-  if (!sane) {
+  if (take_all) {
+    m = 0;  // every non-NaN score is emitted; the rest is padding
+  } else if (!sane) {
     flag = 1;
   } else if (!fine) {
     if (emitted != above || (T < DSA_NUM_BINS && ncand != histT)) flag = 1;
     base_out = above;
     m = (T < DSA_NUM_BINS) ? k - above : 0;
   } else {
-    const bool sane1 = S < kFineBins && above1 >= 0 && above1 < k - above;
+    const bool sane1 = S < kClFine && above1 >= 0 && above1 < k - above;
     if (!sane1 || n_binT != histT || emitted != above + above1 || ncand != fineS) flag = 1;
     else if (ncand > DSA_CAND_CAP) flag = 2;
     base_out = above + above1;
@@ -990,7 +1005,6 @@ __global__ void __launch_bounds__(kClThreads, 2)
   __shared__ int sm_h[256];
   __shared__ int sm_scan[kSelWarps + 1];
   __shared__ int sm_misc[16];
-  __shared__ uint32_t sm_key[2];
   __shared__ unsigned long long sm_u64[2];
   const uint32_t rank = cluster_ctarank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1020,14 +1034,23 @@ __global__ void __launch_bounds__(kClThreads, 2)
   float4 v[kClVec];
   cl_issue_loads(row, c0, c1, vq, p.vec != 0, v);
 
-  // ---- 1, 2. threshold bin T and its key range
+  // ---- 1, 2. threshold bin T and its key range (rows of at most k scores
+  // take every non-NaN score: T past the last bin)
+  const bool take_all = n <= k;
+  const bool early = hrow || take_all;  // T known without the row's own histogram
   int T, above, histT;
-  if (hrow) {
+  if (early) {
     if (!local) cluster_arrive();  // counters zeroed; the wait comes after the loads
-    threshold_from_hist<DSA_NUM_BINS>(hrow, k, sm_scan, sm_misc);
-    T = sm_misc[0];
-    above = sm_misc[1];
-    histT = sm_misc[2];
+    if (take_all) {
+      T = DSA_NUM_BINS;
+      above = 0;
+      histT = 0;
+    } else {
+      threshold_from_hist<DSA_NUM_BINS>(hrow, k, sm_scan, sm_misc);
+      T = sm_misc[0];
+      above = sm_misc[1];
+      histT = sm_misc[2];
+    }
     cl_store_keys(v, sm.keys);
   } else {
     for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) sm.hist[i] = 0;
@@ -1053,14 +1076,9 @@ __global__ void __launch_bounds__(kClThreads, 2)
     above = sm_misc[1];
     histT = sm_misc[2];
   }
-  if (warp < 2) {
-    const uint32_t g = bin_prefix_end(T + warp);
-    if (lane == 0) sm_key[warp] = g;
-  }
-  __syncthreads();
-  const uint32_t hiT = sm_key[0];
-  const uint32_t loT = sm_key[1] + 1;  // loT > hiT: bin T empty (T past the last bin)
-  if (hrow && !local) cluster_wait();  // every CTA's counters are zero from here on
+  uint32_t loT, hiT;  // loT > hiT: bin T empty (T past the last bin)
+  bin_key_range(T, loT, hiT);
+  if (early && !local) cluster_wait();  // every CTA's counters are zero from here on
 
   // ---- 3. fine histogram of bin T, fine threshold bin S
   const bool fine = (T < DSA_NUM_BINS) && histT > kClDirect;
@@ -1068,7 +1086,7 @@ __global__ void __launch_bounds__(kClThreads, 2)
   int fshift = 0, S = 0, above1 = 0, fineS = 0;
   if (fine) {
     cl_fine_window(T, loT, hiT, flo, fshift);
-    for (int i = threadIdx.x; i < kFineBins; i += kClThreads) sm.hist[i] = 0;
+    for (int i = threadIdx.x; i < kClFine; i += kClThreads) sm.hist[i] = 0;
     __syncthreads();
     for (int q = 0; q < vq; ++q) {
       const uint4 k4 = sm.keys[q * kClThreads + threadIdx.x];
@@ -1079,12 +1097,12 @@ __global__ void __launch_bounds__(kClThreads, 2)
     }
     __syncthreads();
     if (!local) {
-      cl_flush(sm.hist, wf, kFineBins);
+      cl_flush(sm.hist, wf, kClFine);
       cluster_sync();
-      cl_fetch(sm.hist, wf, kFineBins);
+      cl_fetch(sm.hist, wf, kClFine);
       __syncthreads();
     }
-    threshold_from_hist<kFineBins>(sm.hist, k - above, sm_scan, sm_misc + 10);
+    threshold_from_hist<kClFine>(sm.hist, k - above, sm_scan, sm_misc + 10);
     S = sm_misc[10];
     above1 = sm_misc[11];
     fineS = sm_misc[12];
@@ -1133,17 +1151,17 @@ __global__ void __launch_bounds__(kClThreads, 2)
   }
 
   // ---- 5. check, rank or refine, or fall back
-  const int flag = cl_finish(row, n, k, outr, T, above, histT, fine, S, above1, fineS, emitted,
-                             ncand, n_binT, sm.cand, cr,
+  const int flag = cl_finish(row, n, k, outr, take_all, T, above, histT, fine, S, above1, fineS,
+                             emitted, ncand, n_binT, sm.cand, cr,
                              reinterpret_cast<unsigned long long *>(sm.keys), sm_h, sm_scan,
                              sm_misc, sm_u64);
   if (p.flags && threadIdx.x == 0) p.flags[r] = flag;
   // restore the zero workspace histograms; clear the caller's on request
   if (!local) {
-    if (!hrow)
+    if (!early)
       for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) wh[i] = 0;
     if (fine)
-      for (int i = threadIdx.x; i < kFineBins; i += kClThreads) wf[i] = 0;
+      for (int i = threadIdx.x; i < kClFine; i += kClThreads) wf[i] = 0;
   }
   if (p.reset_hist && p.hist) {
     int32_t *hw = p.hist + (int64_t)r * DSA_NUM_BINS;
@@ -1495,6 +1513,27 @@ dsa_status_t run_cluster_select(const TopkCall *calls, int count, cudaStream_t s
 }
 
 }  // namespace
+
+namespace {
+__global__ void bin_key_ranges_kernel(uint32_t *out) {
+  const int T = blockIdx.x * blockDim.x + threadIdx.x;
+  if (T > DSA_NUM_BINS) return;
+  uint32_t lo, hi;
+  bin_key_range(T, lo, hi);
+  out[2 * T] = lo;
+  out[2 * T + 1] = hi;
+}
+}  // namespace
+
+dsa_status_t run_bin_key_ranges(uint32_t *out, cudaStream_t st) {
+  bin_key_ranges_kernel<<<(DSA_NUM_BINS + 1 + 255) / 256, 256, 0, st>>>(out);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return DSA_ERR_CUDA;
+  }
+  return DSA_OK;
+}
 
 dsa_status_t run_topk_batch(const TopkCall *calls, int count, cudaStream_t st) {
   if (topk_batchable(calls, count)) return run_cluster_select(calls, count, st);

@@ -325,8 +325,13 @@ int32_t dsa_topk_fp16(const uint16_t *scores, int64_t stride, const int32_t *val
  *   n even, both arrays device-resident.
  * dsa_wait_timeout_selftest: launches a kernel whose only wait is on a
  *   barrier nothing arrives on, bounded by `limit_cycles`; the kernel records
- *   DSA_DEV_TIMEOUT in the workspace status word and returns. */
+ *   DSA_DEV_TIMEOUT in the workspace status word and returns.
+ * dsa_coarse_bin_key_ranges: out[2T], out[2T+1] = the lowest and highest
+ *   FP32 order key (unsigned compare == value compare) of coarse bin T, for
+ *   T = 0..1024 (T = 1024: an empty range, low > high), as the select kernel
+ *   computes them in closed form; out is a device array of 2050 uint32. */
 int32_t dsa_coarse_bins_range(uint32_t start, int64_t count, int16_t *out, void *stream);
+int32_t dsa_coarse_bin_key_ranges(uint32_t *out, void *stream);
 int32_t dsa_fp16_order_keys(const uint16_t *in, uint16_t *out, int64_t n, void *stream);
 int32_t dsa_wait_timeout_selftest(uint64_t limit_cycles, void *workspace, size_t ws_bytes,
                                   void *stream);

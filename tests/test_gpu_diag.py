@@ -59,3 +59,27 @@ def test_bounded_wait_times_out_and_reports():
     # the context is still usable
     x = torch.arange(10, device="cuda").sum().item()
     assert x == 45
+
+
+def test_closed_form_bin_key_ranges_match_the_oracle_bins():
+    """The select's closed-form key range of every coarse bin: both ends are
+    in the bin by the oracle's coarse_bin, the keys just outside are not, and
+    the ranges tile the non-NaN keys from +inf (bin 0) down to -inf."""
+    import dsa_sparse_attention_paged_gb300 as D
+    from oracle import oracle as O
+    kr = D.coarse_bin_key_ranges().numpy().astype(np.uint64)
+    lo, hi = kr[:1024, 0], kr[:1024, 1]
+    assert kr[1024, 0] > kr[1024, 1]  # past the last bin: empty
+
+    def bins_of_keys(keys):
+        keys = np.asarray(keys, dtype=np.uint64).astype(np.uint32)
+        bits = np.where(keys & 0x80000000, keys ^ 0x80000000, ~keys).astype(np.uint32)
+        return O.coarse_bins(bits.view(np.float32))
+
+    T = np.arange(1024)
+    assert (bins_of_keys(lo) == T).all() and (bins_of_keys(hi) == T).all()
+    assert (lo <= hi).all()
+    assert hi[0] == 0xFF800000 and lo[1023] == 0x007FFFFF      # +inf and -inf
+    assert (lo[:-1] == hi[1:] + 1).all()                      # no gap, no overlap
+    inner_below = lo[:-1] - 1                                 # the keys just below
+    assert (bins_of_keys(inner_below) == T[:-1] + 1).all()
