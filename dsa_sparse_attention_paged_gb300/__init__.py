@@ -38,9 +38,10 @@ class TopkProblem(ctypes.Structure):
     _fields_ = [("logits", ctypes.c_void_p), ("stride", ctypes.c_int64),
                 ("context_lens", ctypes.c_void_p), ("histogram", ctypes.c_void_p),
                 ("out_idx", ctypes.c_void_p), ("fallback_flags", ctypes.c_void_p),
+                ("block_out_idx", ctypes.c_void_p), ("block_fallback_flags", ctypes.c_void_p),
                 ("next_n", ctypes.c_int32), ("len_div", ctypes.c_int32), ("R", ctypes.c_int32),
                 ("reset_histogram", ctypes.c_int32), ("k", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("block_k", ctypes.c_int32)]
 
 
 TOPK_BATCH_MAX = 4
@@ -209,7 +210,8 @@ def coarse_hist_topk(logits, context_lens, next_n, k, ws, histogram=None, reset_
 
 
 def _topk_problem(logits, context_lens, next_n, k, histogram=None, reset_histogram=False,
-                  len_div=1, out=None, fallback_flags=None, R=None):
+                  len_div=1, out=None, fallback_flags=None, R=None, block_k=0, block_out=None,
+                  block_fallback_flags=None):
     _req(logits, torch.float32, "logits")
     _req(context_lens, torch.int32, "context_lens")
     R = logits.shape[0] if R is None else R
@@ -220,17 +222,29 @@ def _topk_problem(logits, context_lens, next_n, k, histogram=None, reset_histogr
         _req(histogram, torch.int32, "histogram")
     if fallback_flags is not None:
         _req(fallback_flags, torch.int32, "fallback_flags")
+    if block_k and block_out is None:
+        block_out = torch.empty((R, block_k), dtype=torch.int32, device=logits.device)
+    if block_out is not None:
+        _req(block_out, torch.int32, "block_out")
+    if block_fallback_flags is not None:
+        _req(block_fallback_flags, torch.int32, "block_fallback_flags")
     prob = TopkProblem(logits.data_ptr(), logits.stride(0), context_lens.data_ptr(),
                        histogram.data_ptr() if histogram is not None else None, out.data_ptr(),
                        fallback_flags.data_ptr() if fallback_flags is not None else None,
-                       int(next_n), int(len_div), int(R), 1 if reset_histogram else 0, int(k), 0)
-    return prob, out
+                       block_out.data_ptr() if block_out is not None else None,
+                       block_fallback_flags.data_ptr() if block_fallback_flags is not None
+                       else None,
+                       int(next_n), int(len_div), int(R), 1 if reset_histogram else 0, int(k),
+                       int(block_k))
+    return prob, ((out, block_out) if block_k else out)
 
 
 def coarse_hist_topk_batch(problems, ws, stream=None):
     """Several independent ``coarse_hist_topk`` problems (dicts of its keyword
-    arguments) with one workspace sized for the sum of their rows; one launch
-    when every row stride is at most 131072.  Returns the output tensors."""
+    arguments, plus ``block_k`` / ``block_out`` / ``block_fallback_flags`` for
+    the fused top block maxima) with one workspace sized for the sum of their
+    rows; one launch when every row stride is at most 131072.  Returns per
+    problem its output tensor, or (output, block output) with block_k."""
     if len(problems) > TOPK_BATCH_MAX:
         raise ValueError(f"coarse_hist_topk_batch: at most {TOPK_BATCH_MAX} problems")
     built = [_topk_problem(**p) for p in problems]
@@ -244,8 +258,8 @@ def coarse_hist_topk_batch_launches(strides_and_hist):
     """Kernel launches of ``coarse_hist_topk_batch`` for problems given as
     (row stride, has_histogram, rows) triples."""
     arr = (TopkProblem * max(1, len(strides_and_hist)))(
-        *[TopkProblem(None, int(s), None, 1 if h else None, None, None, 1, 1, int(r), 0, 1, 0)
-          for s, h, r in strides_and_hist])
+        *[TopkProblem(None, int(s), None, 1 if h else None, None, None, None, None, 1, 1, int(r),
+                      0, 1, 0) for s, h, r in strides_and_hist])
     n = lib.dsa_coarse_hist_topk_batch_launches(arr, len(strides_and_hist))
     if n < 0:
         raise ValueError("coarse_hist_topk_batch_launches: invalid problems")

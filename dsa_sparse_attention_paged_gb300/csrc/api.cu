@@ -343,15 +343,26 @@ int32_t dsa_coarse_hist_topk_batch(const dsa_topk_problem *problems, int32_t cou
   TopkCall calls[DSA_TOPK_BATCH_MAX];
   int n = 0;
   int64_t rows_needed = 0;
+  bool blocks = false;
   for (int i = 0; i < count; ++i) {
-    if (problems[i].reserved != 0 || problems[i].R < 0) return DSA_ERR_INVALID_ARG;
-    if (problems[i].R == 0) continue;  // nothing to check or run (pointers may be NULL)
+    const dsa_topk_problem &pb = problems[i];
+    if (pb.R < 0 || pb.block_k < 0) return DSA_ERR_INVALID_ARG;
+    if (pb.R == 0) continue;  // nothing to check or run (pointers may be NULL)
     TopkCall c;
-    const int32_t err = topk_problem_args(problems[i], c);
+    const int32_t err = topk_problem_args(pb, c);
     if (err != DSA_OK) return err;
+    if (pb.block_k > 0) {
+      if (!pb.block_out_idx) return DSA_ERR_INVALID_ARG;
+      if (pb.block_k > DSA_MAX_TOPK || pb.len_div != 1) return DSA_ERR_UNSUPPORTED;
+      c.block_out = pb.block_out_idx;
+      c.block_flags = pb.block_fallback_flags;
+      c.block_k = pb.block_k;
+      blocks = true;
+    }
     rows_needed += c.R;
     calls[n++] = c;
   }
+  if (blocks && !topk_batchable(calls, n)) return DSA_ERR_UNSUPPORTED;
   if (!workspace) return DSA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return DSA_ERR_MISALIGNED;
   const int64_t rows = ws_rows_for(ws_bytes);

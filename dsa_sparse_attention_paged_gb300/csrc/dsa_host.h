@@ -52,6 +52,9 @@ struct TopkCall {
   int32_t k;
   int32_t *out_idx;
   int32_t *fallback_flags;
+  int32_t *block_out = nullptr;    // also the top block_k block maxima per row (one launch only)
+  int32_t *block_flags = nullptr;
+  int32_t block_k = 0;
   void *workspace;
   int32_t ws_rows;           // rows the workspace was sized for
   bool allow_cluster = true; // rows up to 131072 may take the cluster kernel

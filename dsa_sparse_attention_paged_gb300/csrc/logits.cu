@@ -559,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane_base = 32 * quarter;
     const int tok = g * kSubTok + lane_base + lane;   // token within the stage
     const int gtid = ((warp - 2) & 3) * 32 + lane;    // 0..127 within the group
+    const uint64_t out_pol = policy_evict_last();
     int *grp_hist = hist_s + g * HS * NN * DSA_NUM_BINS;
     int *my_hist = grp_hist + (HS == 4 ? quarter : 0) * NN * DSA_NUM_BINS;
     TileIter<SPARSE> it;
@@ -683,7 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (t == a.out_stride) set_status(a.status, DSA_DEV_BOUNDS);
           }
           if (t < n_rj) {
-            reinterpret_cast<float *>(a.out)[(int64_t)(row_base + j) * a.out_stride + t] = acc[j];
+            // kept in L2 for the select that reads the row next (the K stream
+            // around it is marked evict-first)
+            st_f32_hint(reinterpret_cast<float *>(a.out) + (int64_t)(row_base + j) * a.out_stride + t,
+                        acc[j], out_pol);
             if (HIST) {
               const int bin = coarse_bin(acc[j]);
               if (bin >= 0) atomicAdd(&my_hist[j * DSA_NUM_BINS + bin], 1);

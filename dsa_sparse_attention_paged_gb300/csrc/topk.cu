@@ -284,7 +284,7 @@ __device__ void adaptive_threshold(const K *keys, int n, int m, int *h, K *red, 
 
 // Exact top-m of n unique 64-bit keys (candidates: value order key << 32 |
 // inverted column), emitted as columns to out[0..m).
-__device__ void refine_candidates(const unsigned long long *sc, int n, int m, int32_t *out,
+__device__ __noinline__ void refine_candidates(const unsigned long long *sc, int n, int m, int32_t *out,
                                   int *sm_h, int *sm_misc, unsigned long long *sm_u64) {
   unsigned long long thr;
   int n_gt, need_eq;
@@ -304,12 +304,14 @@ __device__ void refine_candidates(const unsigned long long *sc, int n, int m, in
   __syncthreads();
 }
 
-// Exact top-k of one FP32 row by MSB radix select over 32-bit order keys, run
-// by the whole block.  Ties at the threshold key go to the lowest columns
+// Exact top-k of n elements by MSB radix select over their 32-bit order keys,
+// run by the whole block; key_at(i) is element i's key, 0 for an element that
+// never takes part.  Ties at the threshold key go to the lowest indices
 // (ordered scan).  Writes all k outputs (-1 padded).
-__device__ void block_radix_topk_row(const float *row, int64_t n, int k, int32_t *out,
-                                     int *sm_h /*256*/, int *sm_scan /*kSelWarps+1*/,
-                                     int *sm_misc /*8*/) {
+template <class KeyAt>
+__device__ __noinline__ void block_radix_topk(KeyAt key_at, int64_t n, int k, int32_t *out,
+                                 int *sm_h /*256*/, int *sm_scan /*kSelWarps+1*/,
+                                 int *sm_misc /*8*/) {
   uint32_t prefix = 0, mask = 0;
   int need = k;
   bool early = false;
@@ -317,9 +319,8 @@ __device__ void block_radix_topk_row(const float *row, int64_t n, int k, int32_t
     for (int i = threadIdx.x; i < 256; i += kSelThreads) sm_h[i] = 0;
     __syncthreads();
     for (int64_t t = threadIdx.x; t < n; t += kSelThreads) {
-      const float x = row[t];
-      if (isnan(x)) continue;
-      const uint32_t key = f32_order_key(x);
+      const uint32_t key = key_at(t);
+      if (key == 0) continue;
       if ((key & mask) == prefix) atomicAdd(&sm_h[(key >> shift) & 255], 1);
     }
     __syncthreads();
@@ -357,9 +358,8 @@ __device__ void block_radix_topk_row(const float *row, int64_t n, int k, int32_t
       const int64_t t = base + threadIdx.x * 4 + e;
       eqf[e] = false;
       if (t >= n) continue;
-      const float x = row[t];
-      if (isnan(x)) continue;
-      const uint32_t key = f32_order_key(x);
+      const uint32_t key = key_at(t);
+      if (key == 0) continue;
       const bool sel = early ? (key >= prefix) : (key > prefix);
       if (sel) {
         const int p = atomicAdd(&sm_misc[2], 1);
@@ -384,6 +384,15 @@ __device__ void block_radix_topk_row(const float *row, int64_t n, int k, int32_t
   const int written = early ? sm_misc[2] : k;
   for (int i = written + threadIdx.x; i < k; i += kSelThreads) out[i] = -1;
   __syncthreads();
+}
+
+// Exact top-k of one FP32 row (NaN never taken; ties to the lower column).
+__device__ void block_radix_topk_row(const float *row, int64_t n, int k, int32_t *out,
+                                     int *sm_h, int *sm_scan, int *sm_misc) {
+  block_radix_topk([row](int64_t t) -> uint32_t {
+    const float x = row[t];
+    return isnan(x) ? 0u : f32_order_key(x);
+  }, n, k, out, sm_h, sm_scan, sm_misc);
 }
 
 __global__ void __launch_bounds__(kSelThreads)
@@ -417,7 +426,7 @@ __global__ void __launch_bounds__(kSelThreads)
 // holds fewer than `need`, and (nb, -1, 0) when no bin qualifies (a corrupt
 // histogram).
 template <int NB>
-__device__ void threshold_from_hist(const int32_t *h, int need, int *sm_scan, int *sm_misc) {
+__device__ __noinline__ void threshold_from_hist(const int32_t *h, int need, int *sm_scan, int *sm_misc) {
   constexpr int PER = NB / kSelThreads;
   int c[PER];
   int sum = 0;
@@ -719,17 +728,27 @@ constexpr int kClVpt = 32;                       // scores per thread
 constexpr int kClVec = kClVpt / 4;               // float4 groups per thread
 constexpr int kClChunk = kClThreads * kClVpt;    // 16384 per CTA
 constexpr int kClRow = kCl * kClChunk;           // 131072
-constexpr int kClDirect = kClThreads;            // candidates ranked directly
+constexpr int kClDirect = kClThreads;            // candidates kept in shared memory
+constexpr int kClRank = 64;                      // candidates ranked pairwise
 constexpr int kClMaxProb = 4;                    // problems per launch
 constexpr int kClFine = 1024;                    // fine bins
 constexpr uint32_t kFineWindow = 1u << 26;       // keys one fine histogram spans at most
 static_assert(kClThreads == kSelThreads, "block scans assume kSelThreads threads");
 
+constexpr int kClBlk = kClChunk / 8;             // block maxima per CTA
+constexpr int kClCandHalf = DSA_CAND_CAP / 2;    // candidate slots per select with block output
+
 struct ClSmem {
   uint4 keys[kClVec * kClThreads];      // keys[q * kClThreads + tid] = slots 4q..4q+3 of tid
   int hist[DSA_NUM_BINS];               // local coarse / fine histogram, then the row's
   unsigned long long cand[kClDirect];   // the row's first candidates (CTA 0 / local CTA)
-  int ctr[4];                           // CTA 0: emitted, candidates, bin-T count
+  uint32_t bkey[kClBlk];                // block maxima keys of this CTA's positions
+  int bhist[DSA_NUM_BINS];              // local / merged histogram of the block maxima
+  unsigned long long bcand[kClDirect];  // block select: first candidates (CTA 1 / local CTA)
+  int ctr[8];                           // CTA 0: emitted, candidates, bin-T count; CTA 1: same
+                                        // for the block select (ctr[4..6])
+  uint32_t bmm[8];                      // (~min, max) of the maxima in each wide bin
+  uint32_t red[4];                      // range reductions
 };
 static_assert(sizeof(uint4) * kClVec * kClThreads >= sizeof(unsigned long long) * DSA_CAND_CAP,
               "the refine reuses the key buffer for the candidates");
@@ -744,6 +763,9 @@ struct ClProb {
   int k;
   int32_t *out;
   int32_t *flags;
+  int32_t *bout;  // block output [R][bk], or NULL (bk = 0)
+  int32_t *bflags;
+  int bk;
   int ws_row0;    // first workspace row of this problem
   int local;      // rows of at most kClChunk: one CTA per row
   int vec;        // rows 16-byte aligned: vector loads
@@ -803,30 +825,75 @@ __device__ __forceinline__ void bin_key_range(int T, uint32_t &loT, uint32_t &hi
   }
 }
 
-// Fine map of bin T: its key range [loT, hiT], or for the two bins wider than
-// kFineWindow keys (|x| >= 223 and |x| below the smallest FP16 step) the
-// window of kFineWindow keys at the end nearer to magnitude 1, spread over
-// kClFine descending fine bins; keys outside the window clamp to the end
-// bins (the map stays monotone, so the select stays exact).
-__device__ __forceinline__ void cl_fine_window(int T, uint32_t loT, uint32_t hiT, uint32_t &flo,
-                                               int &fshift) {
+// Fine map of bin T: its key range [loT, hiT] spread over kClFine descending
+// fine bins -- or, for the four bins wider than kFineWindow keys (|x| >= 223
+// and |x| below the smallest FP16 step, each sign), the range [dmin, dmax] the
+// row's scores in the bin actually take (dmax = 0: not known, the end of the
+// bin nearer to magnitude 1 is used).  Keys outside the map clamp to the end
+// bins, so the map stays monotone and the select exact.
+__device__ __forceinline__ void cl_fine_window(int T, uint32_t loT, uint32_t hiT, uint32_t dmin,
+                                               uint32_t dmax, uint32_t &flo, int &fshift) {
   uint32_t span1 = hiT - loT;
   flo = loT;
   if (span1 >= kFineWindow) {
-    span1 = kFineWindow - 1;
-    const bool pos = T < 512;
-    const int mag = pos ? 511 - T : T - 512;
-    const bool window_low = (mag == 511) ? pos : !pos;
-    if (!window_low) flo = hiT - span1;
+    if (dmax != 0 && dmin <= dmax) {
+      flo = dmin;
+      span1 = dmax - dmin;
+    } else {
+      span1 = kFineWindow - 1;
+      const bool pos = T < 512;
+      const int mag = pos ? 511 - T : T - 512;
+      const bool window_low = (mag == 511) ? pos : !pos;
+      if (!window_low) flo = hiT - span1;
+    }
   }
   fshift = 0;
   while ((span1 >> fshift) >= (uint32_t)kClFine) ++fshift;
 }
 
+// Index of the wide coarse bins (0: x >= 223, 1: +tiny, 2: -tiny, 3: x <= -223).
+__device__ __forceinline__ int wide_bin_idx(int T) {
+  return T == 0 ? 0 : T == 511 ? 1 : T == 512 ? 2 : T == 1023 ? 3 : -1;
+}
+
+// Workspace slots (inside the row's fine-histogram area) where every CTA of a
+// cluster publishes the key range its scores take in a wide bin: (~min, max),
+// both 0 when none; CTA r writes only its own slots.
+constexpr int kSlotD = 3 * kClFine;      // score select: 2 per CTA
+constexpr int kSlotB = kSlotD + 2 * kCl; // block select: 8 per CTA (4 wide bins)
+static_assert(kSlotB + 8 * kCl <= kFineBins, "slots fit the row's fine area");
+
+// (~min, max) of this CTA's keys inside [lo, hi] into red[0], red[1] (0 when
+// none); every thread calls it; ends with a __syncthreads.
+__device__ __noinline__ void cl_range_in(const uint4 *keys, int vq, uint32_t lo, uint32_t hi, uint32_t *red) {
+  if (threadIdx.x == 0) {
+    red[0] = 0;
+    red[1] = 0;
+  }
+  __syncthreads();
+  uint32_t nmin = 0, mx = 0;
+  for (int q = 0; q < vq; ++q) {
+    const uint4 k4 = keys[q * kClThreads + threadIdx.x];
+    const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (kv[j] >= lo && kv[j] <= hi) {
+        nmin = max(nmin, ~kv[j]);
+        mx = max(mx, kv[j]);
+      }
+  }
+  nmin = __reduce_max_sync(0xffffffffu, nmin);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if ((threadIdx.x & 31) == 0 && mx) {
+    atomicMax(&red[0], nmin);
+    atomicMax(&red[1], mx);
+  }
+  __syncthreads();
+}
+
 __device__ __forceinline__ int cl_fine_idx(uint32_t kk, uint32_t flo, int fshift) {
-  const int64_t off = (int64_t)kk - (int64_t)flo;
-  const int64_t f = off <= 0 ? 0 : min((int64_t)(kClFine - 1), off >> fshift);
-  return (kClFine - 1) - (int)f;
+  const uint32_t off = kk > flo ? kk - flo : 0u;
+  return (kClFine - 1) - (int)min((uint32_t)(kClFine - 1), off >> fshift);
 }
 
 // The CTA's local histogram (nb bins) is added into the row's workspace copy.
@@ -849,30 +916,37 @@ __device__ __forceinline__ int64_t cl_pos(int64_t c0, int q, int j) {
   return c0 + 4 * ((int64_t)q * kClThreads + threadIdx.x) + j;
 }
 
-// Loads of the CTA's positions [c0, c1) into registers (NaN past c1).
+// Loads of the CTA's positions [c0, c1) into registers (NaN past c1); read
+// once, so the lines are marked evict-first.  Positions of a cluster row are
+// below 2^31.
 __device__ __forceinline__ void cl_issue_loads(const float *row, int64_t c0, int64_t c1, int vq,
                                                bool vec, float4 (&v)[kClVec]) {
   const float nanv = __int_as_float(0x7fffffff);
+  const uint64_t pol = policy_evict_first();
+  const int t0 = (int)c0 + 4 * (int)threadIdx.x, e1 = (int)c1;
 #pragma unroll
   for (int q = 0; q < kClVec; ++q) {
     float4 x = make_float4(nanv, nanv, nanv, nanv);
-    const int64_t t = cl_pos(c0, q, 0);
+    const int t = t0 + 4 * q * kClThreads;
     if (q < vq) {
-      if (vec && t + 3 < c1) {
-        x = __ldg(reinterpret_cast<const float4 *>(row + t));
+      if (vec && t + 3 < e1) {
+        x = ld_f4_hint(row + t, pol);
       } else {
-        if (t < c1) x.x = __ldg(row + t);
-        if (t + 1 < c1) x.y = __ldg(row + t + 1);
-        if (t + 2 < c1) x.z = __ldg(row + t + 2);
-        if (t + 3 < c1) x.w = __ldg(row + t + 3);
+        if (t < e1) x.x = __ldg(row + t);
+        if (t + 1 < e1) x.y = __ldg(row + t + 1);
+        if (t + 2 < e1) x.z = __ldg(row + t + 2);
+        if (t + 3 < e1) x.w = __ldg(row + t + 3);
       }
     }
     v[q] = x;
   }
 }
 
+// Order key, 0 for NaN (branch-free).
 __device__ __forceinline__ uint32_t key_or_zero(float x) {
-  return isnan(x) ? 0u : f32_order_key(x);
+  const uint32_t u = __float_as_uint(x);
+  const uint32_t k = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+  return isnan(x) ? 0u : k;
 }
 
 __device__ __forceinline__ void cl_store_keys(const float4 (&v)[kClVec], uint4 *keys) {
@@ -882,34 +956,37 @@ __device__ __forceinline__ void cl_store_keys(const float4 (&v)[kClVec], uint4 *
                                                     key_or_zero(v[q].z), key_or_zero(v[q].w));
 }
 
-// Two bits per slot e = 4q + j: 1 = emit (above the threshold), 2 = candidate.
-// nt counts the slots in bin T.
-__device__ __forceinline__ unsigned long long cl_classify(const uint4 *keys, int vq, uint32_t loT,
-                                                          uint32_t hiT, bool fine, uint32_t flo,
-                                                          int fshift, int S, int &nt) {
+// Key range [C, E] of fine bin S of bin T under cl_fine_idx's clamped map
+// (fine bins descend): the keys of the bin are exactly C <= key <= E, and the
+// keys of the fine bins above it (and of the coarse bins above T) are > E.
+__device__ __forceinline__ void fine_bin_keys(uint32_t loT, uint32_t hiT, uint32_t flo, int fshift,
+                                              int S, uint32_t &C, uint32_t &E) {
+  const int g = (kClFine - 1) - S;  // ascending offset index
+  int64_t c = (g == 0) ? (int64_t)loT : (int64_t)flo + ((int64_t)g << fshift);
+  int64_t e = (g == kClFine - 1) ? (int64_t)hiT : (int64_t)flo + ((int64_t)(g + 1) << fshift) - 1;
+  c = max(c, (int64_t)loT);
+  e = min(e, (int64_t)hiT);
+  C = (uint32_t)c;
+  E = (uint32_t)e;
+}
+
+// One slot's kind: 1 = emit (key > E), 2 = candidate (C <= key <= E), else 0.
+// Key 0 (NaN, padding) is never either: E >= key(-inf) - 1 > 0, C > 0.
+__device__ __forceinline__ uint32_t cl_kind(uint32_t k, uint32_t C, uint32_t E) {
+  return (uint32_t)(k > E) | ((uint32_t)(k >= C && k <= E) << 1);
+}
+
+// Two bits per slot e = 4q + j.
+__device__ __forceinline__ unsigned long long cl_classify(const uint4 *keys, int vq, uint32_t C,
+                                                          uint32_t E) {
   unsigned long long kinds = 0;
-  nt = 0;
 #pragma unroll
   for (int q = 0; q < kClVec; ++q) {
-    if (q >= vq) break;
-    const uint4 k4 = keys[q * kClThreads + threadIdx.x];
-    const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t kk = kv[j];
-      uint32_t kd = 0;
-      if (kk > hiT) {
-        kd = 1;
-      } else if (kk >= loT) {
-        ++nt;
-        if (!fine) {
-          kd = 2;
-        } else {
-          const int f = cl_fine_idx(kk, flo, fshift);
-          kd = (f < S) ? 1u : (f == S ? 2u : 0u);
-        }
-      }
-      kinds |= (unsigned long long)kd << (2 * (4 * q + j));
+    if (q < vq) {
+      const uint4 k4 = keys[q * kClThreads + threadIdx.x];
+      const uint32_t w = cl_kind(k4.x, C, E) | (cl_kind(k4.y, C, E) << 2) |
+                         (cl_kind(k4.z, C, E) << 4) | (cl_kind(k4.w, C, E) << 6);
+      kinds |= (unsigned long long)w << (8 * q);
     }
   }
   return kinds;
@@ -919,9 +996,9 @@ __device__ __forceinline__ unsigned long long cl_classify(const uint4 *keys, int
 // (candidate slots pc, pc+1, ...: the first kClDirect in the shared buffer of
 // CTA 0 or of this CTA, the rest in the workspace).
 __device__ __forceinline__ void cl_write(unsigned long long kinds, const uint4 *keys, int64_t c0,
-                                         int pe, int pc, int k, int32_t *outr, bool remote,
-                                         uint32_t cand_remote, unsigned long long *cand_local,
-                                         unsigned long long *cr) {
+                                         int pe, int pc, int k, int cap, int32_t *outr,
+                                         bool remote, uint32_t cand_remote,
+                                         unsigned long long *cand_local, unsigned long long *cr) {
   while (kinds) {
     const int e = (__ffsll((long long)kinds) - 1) >> 1;
     const uint32_t kd = (uint32_t)(kinds >> (2 * e)) & 3u;
@@ -938,7 +1015,7 @@ __device__ __forceinline__ void cl_write(unsigned long long kinds, const uint4 *
       if (pc < kClDirect) {
         if (remote) dsmem_st64(cand_remote + 8u * (uint32_t)pc, v);
         else cand_local[pc] = v;
-      } else if (pc < DSA_CAND_CAP) {
+      } else if (pc < cap) {
         cr[pc] = v;
       }
       ++pc;
@@ -949,11 +1026,31 @@ __device__ __forceinline__ void cl_write(unsigned long long kinds, const uint4 *
 // Last step of a row, run by one CTA once every emit and candidate of the row
 // is in place: check the counts, then rank or refine the candidates, or run
 // the exact whole-row fallback.  Returns the fallback flag.
-__device__ int cl_finish(const float *row, int64_t n, int k, int32_t *outr, bool take_all, int T,
-                         int above, int histT, bool fine, int S, int above1, int fineS,
-                         int emitted, int ncand, int n_binT, const unsigned long long *cand,
-                         const unsigned long long *cr, unsigned long long *scratch, int *sm_h,
-                         int *sm_scan, int *sm_misc, unsigned long long *sm_u64) {
+// Order key of the maximum of block b (scores 8b .. 8b+7) of a row of n
+// scores: NaN scores do not count, a block with no other score has key 0
+// (never selected), and the newest block (the last one) counts as +inf.
+__device__ __forceinline__ uint32_t block_max_key(const float *row, int64_t n, int64_t b) {
+  if (b == (n + 7) / 8 - 1) return kKeyPosInf;
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int64_t t = 8 * b + j;
+    if (t < n) {
+      const float x = row[t];
+      if (!isnan(x)) m = max(m, f32_order_key(x));
+    }
+  }
+  return m;
+}
+
+// Elements are the row's scores, or (maxima) the maxima of its blocks of 8
+// scores: n elements, n_scores scores; `cap` candidate slots.
+__device__ __noinline__ int cl_finish(const float *row, int64_t n, bool maxima, int64_t n_scores, int k,
+                         int32_t *outr, bool take_all, int T, int above, int histT, bool fine,
+                         int S, int above1, int fineS, int emitted, int ncand, int cap,
+                         const unsigned long long *cand, const unsigned long long *cr,
+                         unsigned long long *scratch, int *sm_h, int *sm_scan, int *sm_misc,
+                         unsigned long long *sm_u64) {
   const bool sane = (T < DSA_NUM_BINS) ? (above >= 0 && above < k && histT >= k - above)
                                        : (above >= 0 && above < k);
   int flag = 0, base_out = 0, m = 0;
@@ -967,17 +1064,21 @@ __device__ int cl_finish(const float *row, int64_t n, int k, int32_t *outr, bool
     m = (T < DSA_NUM_BINS) ? k - above : 0;
   } else {
     const bool sane1 = S < kClFine && above1 >= 0 && above1 < k - above;
-    if (!sane1 || n_binT != histT || emitted != above + above1 || ncand != fineS) flag = 1;
-    else if (ncand > DSA_CAND_CAP) flag = 2;
+    // emitted = above + above1 < k and ncand = fineS >= k - emitted make the
+    // result exact whatever the histogram said about bin T's total
+    if (!sane1 || emitted != above + above1 || ncand != fineS) flag = 1;
+    else if (ncand > cap) flag = 2;
     base_out = above + above1;
     m = k - base_out;
   }
   if (flag == 0) {
     if (m <= 0) {
       for (int i = emitted + threadIdx.x; i < k; i += kClThreads) outr[i] = -1;
+    } else if (ncand > kClRank && ncand <= kClDirect) {
+      refine_candidates(cand, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
     } else if (ncand <= kClDirect) {
       // candidate keys are unique (the column is part of the key): each
-      // thread ranks one against all the others
+      // thread ranks one against all the others (quadratic: few candidates)
       if (threadIdx.x < ncand) {
         const unsigned long long v = cand[threadIdx.x];
         int rk = 0;
@@ -990,6 +1091,10 @@ __device__ int cl_finish(const float *row, int64_t n, int k, int32_t *outr, bool
       __syncthreads();
       refine_candidates(scratch, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
     }
+  } else if (maxima) {
+    __syncthreads();
+    block_radix_topk([row, n_scores](int64_t b) { return block_max_key(row, n_scores, b); }, n, k,
+                     outr, sm_h, sm_scan, sm_misc);
   } else {
     __syncthreads();
     block_radix_topk_row(row, n, k, outr, sm_h, sm_scan, sm_misc);
@@ -1004,10 +1109,10 @@ __global__ void __launch_bounds__(kClThreads, 2)
   ClSmem &sm = *reinterpret_cast<ClSmem *>(cl_raw);
   __shared__ int sm_h[256];
   __shared__ int sm_scan[kSelWarps + 1];
-  __shared__ int sm_misc[16];
+  __shared__ int sm_misc[32];  // [0..2] T, [8..10] S, [16..18] Tb, [24..26] Sb, counters
   __shared__ unsigned long long sm_u64[2];
   const uint32_t rank = cluster_ctarank();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
   const int y = blockIdx.y;
   int pi = 0;
   while (pi + 1 < a.nprob && y >= a.cl_begin[pi + 1]) ++pi;
@@ -1023,39 +1128,47 @@ __global__ void __launch_bounds__(kClThreads, 2)
   unsigned long long *cr = a.cand + wr * DSA_CAND_CAP;
   int32_t *wh = a.ws_hist + wr * DSA_NUM_BINS;
   int32_t *wf = a.ws_fine + wr * kFineBins;
+  int32_t *wbh = wf + kClFine;       // the row's block-maxima histogram (workspace)
+  int32_t *wbf = wf + 2 * kClFine;   // its fine histogram
   const int32_t *hrow = p.hist ? p.hist + (int64_t)r * DSA_NUM_BINS : nullptr;
   // this CTA's positions [c0, c1), in groups of 2048 (one float4 per thread)
   const int64_t chunk = ((local ? n : (n + kCl - 1) / kCl) + 2047) / 2048 * 2048;
   const int64_t c0 = local ? 0 : (int64_t)rank * chunk;
   const int64_t c1 = min(n, c0 + chunk);
   const int vq = (int)(chunk / 2048);  // <= kClVec
+  const bool blk = p.bk > 0;           // block select alongside the score select
+  const int bk = p.bk;
+  const int dcap = blk ? kClCandHalf : DSA_CAND_CAP;  // candidate slots of the score select
+  const int64_t nbk = (n + 7) / 8;     // blocks of the row
+  const int64_t b0 = c0 / 8;           // this CTA's first block
 
-  if (threadIdx.x < 4) sm.ctr[threadIdx.x] = 0;
+  if (threadIdx.x < 8) sm.ctr[threadIdx.x] = 0;
+  if (threadIdx.x < 8) sm.bmm[threadIdx.x] = 0;
+  for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) {
+    sm.hist[i] = 0;
+    sm.bhist[i] = 0;
+  }
   float4 v[kClVec];
   cl_issue_loads(row, c0, c1, vq, p.vec != 0, v);
 
-  // ---- 1, 2. threshold bin T and its key range (rows of at most k scores
-  // take every non-NaN score: T past the last bin)
+  // ---- 1. threshold bin T from the caller's histogram, while the row loads
+  // (rows of at most k scores take every non-NaN score: T past the last bin)
   const bool take_all = n <= k;
   const bool early = hrow || take_all;  // T known without the row's own histogram
-  int T, above, histT;
-  if (early) {
-    if (!local) cluster_arrive();  // counters zeroed; the wait comes after the loads
-    if (take_all) {
-      T = DSA_NUM_BINS;
-      above = 0;
-      histT = 0;
-    } else {
-      threshold_from_hist<DSA_NUM_BINS>(hrow, k, sm_scan, sm_misc);
-      T = sm_misc[0];
-      above = sm_misc[1];
-      histT = sm_misc[2];
-    }
-    cl_store_keys(v, sm.keys);
-  } else {
-    for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) sm.hist[i] = 0;
-    cl_store_keys(v, sm.keys);
-    __syncthreads();
+  int T = DSA_NUM_BINS, above = 0, histT = 0;
+  if (early && !take_all) {
+    threshold_from_hist<DSA_NUM_BINS>(hrow, k, sm_scan, sm_misc);
+    T = sm_misc[0];
+    above = sm_misc[1];
+    histT = sm_misc[2];
+  }
+  cl_store_keys(v, sm.keys);
+  __syncthreads();
+
+  // ---- 2. local histograms: the scores' (when T is not known yet) and the
+  // block maxima's (a block of 8 scores is two threads' slots), with the key
+  // range each wide bin's maxima take
+  if (!early) {
     for (int q = 0; q < vq; ++q) {
       const uint4 k4 = sm.keys[q * kClThreads + threadIdx.x];
       const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
@@ -1063,11 +1176,59 @@ __global__ void __launch_bounds__(kClThreads, 2)
       for (int j = 0; j < 4; ++j)
         if (kv[j]) atomicAdd(&sm.hist[coarse_bin_of_key(kv[j])], 1);
     }
-    __syncthreads();
+  }
+  if (blk) {
+#pragma unroll 1
+    for (int q = 0; q < kClVec; ++q) {
+      const uint4 k4 = sm.keys[q * kClThreads + threadIdx.x];
+      uint32_t mk = max(max(k4.x, k4.y), max(k4.z, k4.w));
+      mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, 1));
+      const int lb = q * (kClThreads / 2) + (threadIdx.x >> 1);
+      const int b = (int)b0 + lb;           // blocks of a cluster row are below 2^28
+      if (q >= vq || b >= (int)nbk) mk = 0;    // slots past this CTA's positions, blocks past the row
+      else if (b == (int)nbk - 1) mk = kKeyPosInf;  // the newest block is always chosen
+      if ((threadIdx.x & 1) == 0) {
+        sm.bkey[lb] = mk;
+        if (mk) {
+          const int bb = coarse_bin_of_key(mk);
+          atomicAdd(&sm.bhist[bb], 1);
+          const int wi = wide_bin_idx(bb);
+          if (wi >= 0) {
+            atomicMax(&sm.bmm[2 * wi], ~mk);
+            atomicMax(&sm.bmm[2 * wi + 1], mk);
+          }
+        }
+      }
+    }
+  }
+  uint32_t loT = 0, hiT = 0;  // loT > hiT: bin T empty (T past the last bin)
+  bool fine = false, wide = false;
+  if (early) {
+    bin_key_range(T, loT, hiT);
+    fine = (T < DSA_NUM_BINS) && histT > kClDirect;
+    wide = fine && (hiT - loT) >= kFineWindow;
+    if (wide) cl_range_in(sm.keys, vq, loT, hiT, sm.red);
+  }
+  __syncthreads();
+  if (!local) {
+    // publish into the workspace, then the first cluster barrier (it also
+    // makes every CTA's counters safe to reach)
+    if (!early) cl_flush(sm.hist, wh, DSA_NUM_BINS);
+    if (blk) {
+      cl_flush(sm.bhist, wbh, DSA_NUM_BINS);
+      if (threadIdx.x < 8) wf[kSlotB + 8 * rank + threadIdx.x] = sm.bmm[threadIdx.x];
+    }
+    if (wide && threadIdx.x == 0) {
+      wf[kSlotD + 2 * rank] = sm.red[0];
+      wf[kSlotD + 2 * rank + 1] = sm.red[1];
+    }
+    cluster_arrive();
+    cluster_wait();
+  }
+
+  // ---- 3. the score select's T when the row built its own histogram
+  if (!early) {
     if (!local) {
-      cl_flush(sm.hist, wh, DSA_NUM_BINS);
-      cluster_arrive();
-      cluster_wait();
       cl_fetch(sm.hist, wh, DSA_NUM_BINS);
       __syncthreads();
     }
@@ -1075,97 +1236,231 @@ __global__ void __launch_bounds__(kClThreads, 2)
     T = sm_misc[0];
     above = sm_misc[1];
     histT = sm_misc[2];
+    bin_key_range(T, loT, hiT);
+    fine = (T < DSA_NUM_BINS) && histT > kClDirect;
+    wide = fine && (hiT - loT) >= kFineWindow;
+    if (wide) {
+      cl_range_in(sm.keys, vq, loT, hiT, sm.red);
+      if (!local) {
+        if (threadIdx.x == 0) {
+          wf[kSlotD + 2 * rank] = sm.red[0];
+          wf[kSlotD + 2 * rank + 1] = sm.red[1];
+        }
+        cluster_sync();
+      }
+    }
   }
-  uint32_t loT, hiT;  // loT > hiT: bin T empty (T past the last bin)
-  bin_key_range(T, loT, hiT);
-  if (early && !local) cluster_wait();  // every CTA's counters are zero from here on
+  // ---- 4. the block select's threshold Tb and key ranges of wide bins
+  const bool btake = nbk <= bk;
+  int Tb = DSA_NUM_BINS, aboveb = 0, histTb = 0;
+  if (blk) {
+    if (!local) {
+      cl_fetch(sm.bhist, wbh, DSA_NUM_BINS);
+      __syncthreads();
+    }
+    if (!btake) {
+      threshold_from_hist<DSA_NUM_BINS>(sm.bhist, bk, sm_scan, sm_misc + 16);
+      Tb = sm_misc[16];
+      aboveb = sm_misc[17];
+      histTb = sm_misc[18];
+    }
+  }
+  uint32_t bloT, bhiT;
+  bin_key_range(Tb, bloT, bhiT);
+  const bool bfine = blk && (Tb < DSA_NUM_BINS) && histTb > kClDirect;
+  const int bwi = bfine ? wide_bin_idx(Tb) : -1;
+  if (threadIdx.x == 0) {
+    if (wide && !local) {
+      uint32_t nm = 0, mx = 0;
+      for (int c = 0; c < kCl; ++c) {
+        nm = max(nm, (uint32_t)__ldcg(&wf[kSlotD + 2 * c]));
+        mx = max(mx, (uint32_t)__ldcg(&wf[kSlotD + 2 * c + 1]));
+      }
+      sm.red[0] = nm;
+      sm.red[1] = mx;
+    }
+    if (bwi >= 0) {
+      uint32_t nm = sm.bmm[2 * bwi], mx = sm.bmm[2 * bwi + 1];
+      if (!local) {
+        nm = 0;
+        mx = 0;
+        for (int c = 0; c < kCl; ++c) {
+          nm = max(nm, (uint32_t)__ldcg(&wf[kSlotB + 8 * c + 2 * bwi]));
+          mx = max(mx, (uint32_t)__ldcg(&wf[kSlotB + 8 * c + 2 * bwi + 1]));
+        }
+      }
+      sm.red[2] = nm;
+      sm.red[3] = mx;
+    }
+  }
+  __syncthreads();
 
-  // ---- 3. fine histogram of bin T, fine threshold bin S
-  const bool fine = (T < DSA_NUM_BINS) && histT > kClDirect;
-  uint32_t flo = 0;
+  // ---- 5. fine histograms of bin T and bin Tb (one barrier for both)
+  uint32_t flo = 0, bflo = 0;
   int fshift = 0, S = 0, above1 = 0, fineS = 0;
-  if (fine) {
-    cl_fine_window(T, loT, hiT, flo, fshift);
-    for (int i = threadIdx.x; i < kClFine; i += kClThreads) sm.hist[i] = 0;
+  int bfs = 0, Sb = 0, above1b = 0, fineSb = 0;
+  if (fine || bfine) {
+    if (fine) {
+      cl_fine_window(T, loT, hiT, wide ? ~sm.red[0] : 0u, wide ? sm.red[1] : 0u, flo, fshift);
+      for (int i = threadIdx.x; i < kClFine; i += kClThreads) sm.hist[i] = 0;
+    }
+    if (bfine) {
+      cl_fine_window(Tb, bloT, bhiT, bwi >= 0 ? ~sm.red[2] : 0u, bwi >= 0 ? sm.red[3] : 0u, bflo,
+                     bfs);
+      for (int i = threadIdx.x; i < kClFine; i += kClThreads) sm.bhist[i] = 0;
+    }
     __syncthreads();
-    for (int q = 0; q < vq; ++q) {
-      const uint4 k4 = sm.keys[q * kClThreads + threadIdx.x];
-      const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
+    if (fine) {
+      for (int q = 0; q < vq; ++q) {
+        const uint4 k4 = sm.keys[q * kClThreads + threadIdx.x];
+        const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (kv[j] >= loT && kv[j] <= hiT) atomicAdd(&sm.hist[cl_fine_idx(kv[j], flo, fshift)], 1);
+        for (int j = 0; j < 4; ++j)
+          if (kv[j] >= loT && kv[j] <= hiT)
+            atomicAdd(&sm.hist[cl_fine_idx(kv[j], flo, fshift)], 1);
+      }
+    }
+    if (bfine) {
+      for (int i = threadIdx.x; i < kClBlk; i += kClThreads) {
+        const uint32_t mk = sm.bkey[i];
+        if (mk >= bloT && mk <= bhiT) atomicAdd(&sm.bhist[cl_fine_idx(mk, bflo, bfs)], 1);
+      }
     }
     __syncthreads();
     if (!local) {
-      cl_flush(sm.hist, wf, kClFine);
+      if (fine) cl_flush(sm.hist, wf, kClFine);
+      if (bfine) cl_flush(sm.bhist, wbf, kClFine);
       cluster_sync();
-      cl_fetch(sm.hist, wf, kClFine);
+      if (fine) cl_fetch(sm.hist, wf, kClFine);
+      if (bfine) cl_fetch(sm.bhist, wbf, kClFine);
       __syncthreads();
     }
-    threshold_from_hist<kClFine>(sm.hist, k - above, sm_scan, sm_misc + 10);
-    S = sm_misc[10];
-    above1 = sm_misc[11];
-    fineS = sm_misc[12];
+    if (fine) {
+      threshold_from_hist<kClFine>(sm.hist, k - above, sm_scan, sm_misc + 8);
+      S = sm_misc[8];
+      above1 = sm_misc[9];
+      fineS = sm_misc[10];
+    }
+    if (bfine) {
+      threshold_from_hist<kClFine>(sm.bhist, bk - aboveb, sm_scan, sm_misc + 24);
+      Sb = sm_misc[24];
+      above1b = sm_misc[25];
+      fineSb = sm_misc[26];
+    }
   }
 
-  // ---- 4. classify, reserve, write
-  int nt;
-  const unsigned long long kinds = cl_classify(sm.keys, vq, loT, hiT, fine, flo, fshift, S, nt);
+  // ---- 6. classify both selects, reserve output and candidate ranges
+  // (score select on CTA 0, block select on CTA 1), write.  Emit: key > E;
+  // candidate: C <= key <= E (bin T, or its fine bin S)
+  uint32_t C = loT, E = hiT, CB = bloT, EB = bhiT;
+  if (fine) fine_bin_keys(loT, hiT, flo, fshift, S, C, E);
+  if (bfine) fine_bin_keys(bloT, bhiT, bflo, bfs, Sb, CB, EB);
+  const unsigned long long kinds = cl_classify(sm.keys, vq, C, E);
   const int ne = __popcll(kinds & 0x5555555555555555ull);
   const int nc = __popcll(kinds & 0xAAAAAAAAAAAAAAAAull);
-  if (threadIdx.x == 0) sm_misc[4] = 0;
-  int tot;
+  constexpr int kBPer = kClBlk / kClThreads;  // maxima per thread: index tid + e * kClThreads
+  uint32_t bkinds = 0;
+  if (blk) {
+#pragma unroll
+    for (int e = 0; e < kBPer; ++e)
+      bkinds |= cl_kind(sm.bkey[threadIdx.x + e * kClThreads], CB, EB) << (2 * e);
+  }
+  const int bne = __popc(bkinds & 0x55u), bnc = __popc(bkinds & 0xAAu);
+  int tot, btot = 0, bex = 0;
   const int ex = block_excl_scan((nc << 16) | ne, sm_scan, &tot);  // per CTA < 2^15 each
-  const int ntw = __reduce_add_sync(0xffffffffu, nt);
-  if (lane == 0 && ntw) atomicAdd(&sm_misc[4], ntw);
-  __syncthreads();
-  int base_e = 0, base_c = 0;
-  uint32_t cand0 = 0;
+  if (blk) bex = block_excl_scan((bnc << 16) | bne, sm_scan, &btot);
+  int base_e = 0, base_c = 0, bbe = 0, bbc = 0;
+  uint32_t cand0 = 0, bcand1 = 0;
   if (!local) {
     const uint32_t ctr0 = dsmem_map(smem_u32(&sm.ctr[0]), 0);
+    const uint32_t bctr = dsmem_map(smem_u32(&sm.ctr[4]), 1);
     if (threadIdx.x == 0) {
-      sm_misc[5] = (tot & 0xFFFF) ? dsmem_atomic_add(ctr0, tot & 0xFFFF) : 0;
-      sm_misc[6] = (tot >> 16) ? dsmem_atomic_add(ctr0 + 4, tot >> 16) : 0;
-      if (sm_misc[4]) dsmem_red_add(ctr0 + 8, sm_misc[4]);
+      const int e0 = (tot & 0xFFFF) ? dsmem_atomic_add(ctr0, tot & 0xFFFF) : 0;
+      const int e1 = (tot >> 16) ? dsmem_atomic_add(ctr0 + 4, tot >> 16) : 0;
+      const int e2 = (btot & 0xFFFF) ? dsmem_atomic_add(bctr, btot & 0xFFFF) : 0;
+      const int e3 = (btot >> 16) ? dsmem_atomic_add(bctr + 4, btot >> 16) : 0;
+      sm_misc[5] = e0;
+      sm_misc[6] = e1;
+      sm_misc[21] = e2;
+      sm_misc[22] = e3;
     }
     __syncthreads();
     base_e = sm_misc[5];
     base_c = sm_misc[6];
+    bbe = sm_misc[21];
+    bbc = sm_misc[22];
     cand0 = dsmem_map(smem_u32(&sm.cand[0]), 0);
+    bcand1 = dsmem_map(smem_u32(&sm.bcand[0]), 1);
   }
   if (kinds)
-    cl_write(kinds, sm.keys, c0, base_e + (ex & 0xFFFF), base_c + (ex >> 16), k, outr, !local,
-             cand0, sm.cand, cr);
-  int emitted, ncand, n_binT;
-  if (!local) {
-    cluster_sync();  // all emits and candidates are in place; histograms read
-    if (rank != 0) return;  // nothing reads another CTA's shared memory from here on
-    emitted = sm.ctr[0];
-    ncand = sm.ctr[1];
-    n_binT = sm.ctr[2];
-  } else {
-    __syncthreads();
-    emitted = tot & 0xFFFF;
-    ncand = tot >> 16;
-    n_binT = sm_misc[4];
+    cl_write(kinds, sm.keys, c0, base_e + (ex & 0xFFFF), base_c + (ex >> 16), k, dcap, outr,
+             !local, cand0, sm.cand, cr);
+  int32_t *boutr = blk ? p.bout + (int64_t)r * bk : nullptr;
+  unsigned long long *crb = cr + kClCandHalf;
+  if (bkinds) {
+    int pe = bbe + (bex & 0xFFFF), pc = bbc + (bex >> 16);
+#pragma unroll
+    for (int e = 0; e < kBPer; ++e) {
+      const uint32_t kd = (bkinds >> (2 * e)) & 3u;
+      if (!kd) continue;
+      const int idx = threadIdx.x + e * kClThreads;
+      const int64_t b = b0 + idx;
+      if (kd == 1) {
+        if (pe < bk) boutr[pe] = (int32_t)b;
+        ++pe;
+      } else {
+        const unsigned long long cv = ((unsigned long long)sm.bkey[idx] << 32) |
+                                      (unsigned long long)(0xFFFFFFFFu - (uint32_t)b);
+        if (pc < kClDirect) {
+          if (!local) dsmem_st64(bcand1 + 8u * (uint32_t)pc, cv);
+          else sm.bcand[pc] = cv;
+        } else if (pc < kClCandHalf) {
+          crb[pc] = cv;
+        }
+        ++pc;
+      }
+    }
   }
+  if (!local) cluster_sync();  // all emits and candidates are in place; histograms read
+  else __syncthreads();
 
-  // ---- 5. check, rank or refine, or fall back
-  const int flag = cl_finish(row, n, k, outr, take_all, T, above, histT, fine, S, above1, fineS,
-                             emitted, ncand, n_binT, sm.cand, cr,
-                             reinterpret_cast<unsigned long long *>(sm.keys), sm_h, sm_scan,
-                             sm_misc, sm_u64);
-  if (p.flags && threadIdx.x == 0) p.flags[r] = flag;
-  // restore the zero workspace histograms; clear the caller's on request
-  if (!local) {
-    if (!early)
-      for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) wh[i] = 0;
-    if (fine)
-      for (int i = threadIdx.x; i < kClFine; i += kClThreads) wf[i] = 0;
+  // ---- 7. check, rank or refine, or fall back: the score select on CTA 0
+  // (the local CTA), the block select on CTA 1 (the local CTA, after)
+  unsigned long long *scratch = reinterpret_cast<unsigned long long *>(sm.keys);
+  if (local || rank == 0) {
+    const int emitted = local ? (tot & 0xFFFF) : sm.ctr[0];
+    const int ncand = local ? (tot >> 16) : sm.ctr[1];
+    const int flag = cl_finish(row, n, false, n, k, outr, take_all, T, above, histT, fine, S,
+                               above1, fineS, emitted, ncand, dcap, sm.cand, cr, scratch, sm_h,
+                               sm_scan, sm_misc, sm_u64);
+    if (p.flags && threadIdx.x == 0) p.flags[r] = flag;
+    // restore the zero workspace histograms; clear the caller's on request
+    if (!local) {
+      if (!early)
+        for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) wh[i] = 0;
+      if (fine)
+        for (int i = threadIdx.x; i < kClFine; i += kClThreads) wf[i] = 0;
+      if (wide && threadIdx.x < 2 * kCl) wf[kSlotD + threadIdx.x] = 0;
+    }
+    if (p.reset_hist && p.hist) {
+      int32_t *hw = p.hist + (int64_t)r * DSA_NUM_BINS;
+      for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) hw[i] = 0;
+    }
   }
-  if (p.reset_hist && p.hist) {
-    int32_t *hw = p.hist + (int64_t)r * DSA_NUM_BINS;
-    for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) hw[i] = 0;
+  if (blk && (local || rank == 1)) {
+    __syncthreads();  // the local CTA: the score select's finish is done with the scratch
+    const int emitted = local ? (btot & 0xFFFF) : sm.ctr[4];
+    const int ncand = local ? (btot >> 16) : sm.ctr[5];
+    const int flag = cl_finish(row, nbk, true, n, bk, boutr, btake, Tb, aboveb, histTb, bfine, Sb,
+                               above1b, fineSb, emitted, ncand, kClCandHalf, sm.bcand, crb,
+                               scratch, sm_h, sm_scan, sm_misc, sm_u64);
+    if (p.bflags && threadIdx.x == 0) p.bflags[r] = flag;
+    if (!local) {
+      for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) wbh[i] = 0;
+      if (bfine)
+        for (int i = threadIdx.x; i < kClFine; i += kClThreads) wbf[i] = 0;
+      if (threadIdx.x < 8 * kCl) wf[kSlotB + threadIdx.x] = 0;
+    }
   }
 }
 
@@ -1475,6 +1770,9 @@ dsa_status_t run_cluster_select(const TopkCall *calls, int count, cudaStream_t s
     p.k = c.k;
     p.out = c.out_idx;
     p.flags = c.fallback_flags;
+    p.bout = c.block_out;
+    p.bflags = c.block_flags;
+    p.bk = c.block_out ? c.block_k : 0;
     p.ws_row0 = (int)row0;
     p.local = c.stride <= kClChunk ? 1 : 0;
     p.vec = ((reinterpret_cast<uintptr_t>(c.logits) & 15) == 0 && c.stride % 4 == 0) ? 1 : 0;

@@ -4,12 +4,14 @@
 cross-referenced SGLang commit 7e252c5): it is built once per shape, owns the
 step's device buffers and the workspace, and each ``step`` runs
 
-  source layer   paged MQA logits + fused coarse histogram + fused
-                 block maxima over 8 scores                        (1 launch)
+  source layer   paged MQA logits + fused coarse histogram          (1 launch)
                  histogram-driven exact top-k of the logits rows
-                 (resets the hist) and top-kb of the block-maxima
-                 rows, as two problems of one batched select       (1 launch
-                 for rows up to 131072 scores)
+                 (resets the hist) and, in the same launch, top-kb
+                 of their block maxima over 8 scores (amax8 +
+                 top-kb fused into the select)                     (1 launch
+                 for rows up to 131072 scores; longer rows: block
+                 maxima fused into the logits pass and a second
+                 problem of the batched select instead)
   level one      sort_candidate_blocks -> table, phys, valid lens   (1 launch)
   consumer       sparse MQA logits over the table, FP16 output      (1 launch)
                  FP16 top-k with the fused table transform          (1 launch)
@@ -38,14 +40,19 @@ class DecodePlan:
         self.stride = (int(max_context) + 7) // 8 * 8
         dev = torch.device(device)
         R = self.R
-        # rows for the logits problem and, two-level, the block-maxima problem
-        self.ws = Workspace(2 * R if two_level else R, device=dev)
+        # block maxima selected inside the logits-row select (rows a cluster
+        # takes), else written by the logits pass and selected as a second problem
+        self.fused_blocks = two_level and coarse_hist_topk_batch_launches(
+            [(self.stride, True, R)]) == 1
+        self.ws = Workspace(2 * R if two_level and not self.fused_blocks else R, device=dev)
         self.logits = torch.empty((R, self.stride), dtype=torch.float32, device=dev)
         self.hist = torch.zeros((R, 1024), dtype=torch.int32, device=dev)
         self.topk_idx = torch.empty((R, k), dtype=torch.int32, device=dev)
+        self.amax = None
         if two_level:
             self.amax_stride = (self.stride + 7) // 8
-            self.amax = torch.empty((R, self.amax_stride), dtype=torch.float32, device=dev)
+            self.amax = (None if self.fused_blocks else
+                         torch.empty((R, self.amax_stride), dtype=torch.float32, device=dev))
             self.block_ids = torch.empty((R, kb), dtype=torch.int32, device=dev)
             self.phys = torch.empty((R, kb), dtype=torch.int32, device=dev)
             self.valid_lens = torch.empty((R,), dtype=torch.int32, device=dev)
@@ -57,8 +64,11 @@ class DecodePlan:
         """Kernels of this library launched by one step."""
         if not self.two_level:
             return 1 + coarse_hist_topk_launches(self.stride, True)
-        sel = coarse_hist_topk_batch_launches([(self.stride, True, self.R),
-                                               (self.amax_stride, False, self.R)])
+        if self.fused_blocks:
+            sel = coarse_hist_topk_batch_launches([(self.stride, True, self.R)])
+        else:
+            sel = coarse_hist_topk_batch_launches([(self.stride, True, self.R),
+                                                   (self.amax_stride, False, self.R)])
         return 1 + sel + 1 + 1 + 1
 
     def step(self, q, kv, kscale, weights, page_table, context_lens, events=None):
@@ -72,8 +82,7 @@ class DecodePlan:
 
         mark("logits", 0)
         paged_mqa_logits(q, kv, kscale, weights, page_table, context_lens, nn, ws,
-                         logits=self.logits, histogram=self.hist,
-                         amax=self.amax if self.two_level else None,
+                         logits=self.logits, histogram=self.hist, amax=self.amax,
                          amax_skip_if_blocks_le=self.kb)
         mark("logits", 1)
         if not self.two_level:
@@ -83,11 +92,14 @@ class DecodePlan:
             mark("select", 1)
             return self.topk_idx, None
         mark("select", 0)
-        coarse_hist_topk_batch([
-            dict(logits=self.logits, context_lens=context_lens, next_n=nn, k=self.k,
-                 histogram=self.hist, reset_histogram=True, out=self.topk_idx),
-            dict(logits=self.amax, context_lens=context_lens, next_n=nn, k=self.kb, len_div=8,
-                 out=self.block_ids)], ws)
+        dense = dict(logits=self.logits, context_lens=context_lens, next_n=nn, k=self.k,
+                     histogram=self.hist, reset_histogram=True, out=self.topk_idx)
+        if self.fused_blocks:
+            coarse_hist_topk_batch([dict(dense, block_k=self.kb, block_out=self.block_ids)], ws)
+        else:
+            coarse_hist_topk_batch([dense, dict(
+                logits=self.amax, context_lens=context_lens, next_n=nn, k=self.kb, len_div=8,
+                out=self.block_ids)], ws)
         mark("select", 1)
         mark("publish", 0)
         sort_candidate_blocks(self.block_ids, context_lens, nn, page_table, self.page_size, ws,

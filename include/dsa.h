@@ -197,7 +197,21 @@ int32_t dsa_coarse_hist_topk_launches(int64_t stride, int32_t has_histogram);
  * 131072 the problems run in one launch, otherwise one after another on the
  * stream.  Problems with R = 0 are skipped unchecked (their pointers may be
  * NULL); argument errors are reported for the first offending problem before
- * anything is launched. */
+ * anything is launched.
+ *
+ * Block output (block_k > 0, rows of scores: len_div = 1, stride <= 131072):
+ * the same launch also selects, per row, the block_k blocks of 8 consecutive
+ * scores with the largest block maxima -- exactly what dsa_block_amax8 (no
+ * skipped rows) followed by dsa_coarse_hist_topk with len_div = 8 and k =
+ * block_k returns ([SG38944] amax8_varlen + top-kb over the maxima): the
+ * maximum ignores NaN scores, a block of NaN only is never selected, the
+ * newest block (the one holding the row's last live score) counts as +inf,
+ * ties go to the lower block.  The maxima are taken from the scores the
+ * select already holds, never written to memory.
+ *   block_out_idx         [R][block_k] int32 block ids, -1 padded, any order
+ *   block_fallback_flags  NULL or [R] int32, as fallback_flags
+ * With a block output each select keeps at most DSA_CAND_CAP / 2 candidates
+ * before its exact fallback. */
 #define DSA_TOPK_BATCH_MAX 4
 typedef struct dsa_topk_problem {
   const float *logits;
@@ -206,12 +220,14 @@ typedef struct dsa_topk_problem {
   int32_t *histogram;
   int32_t *out_idx;
   int32_t *fallback_flags;
+  int32_t *block_out_idx;         /* NULL unless block_k > 0 */
+  int32_t *block_fallback_flags;  /* NULL or [R] */
   int32_t next_n;
   int32_t len_div;
   int32_t R;
   int32_t reset_histogram;
   int32_t k;
-  int32_t reserved;  /* set to 0 */
+  int32_t block_k;                /* 0: no block output */
 } dsa_topk_problem;
 
 int32_t dsa_coarse_hist_topk_batch(const dsa_topk_problem *problems, int32_t count,

@@ -114,12 +114,12 @@ def test_topk_launch_count_follows_the_dispatch():
 
 
 def test_topk_problem_layout_and_batch_launch_count():
-    """dsa_topk_problem is 72 bytes (six 8-byte fields, six int32); the batch
+    """dsa_topk_problem is 88 bytes (eight 8-byte fields, six int32); the batch
     runs in one launch when every row stride is at most 131072."""
     import ctypes
     import dsa_sparse_attention_paged_gb300 as D
-    assert ctypes.sizeof(D.TopkProblem) == 72
-    assert D.TopkProblem.next_n.offset == 48
+    assert ctypes.sizeof(D.TopkProblem) == 88
+    assert D.TopkProblem.next_n.offset == 64 and D.TopkProblem.block_k.offset == 84
     n = D.coarse_hist_topk_batch_launches
     assert n([(131072, True, 32), (16384, False, 32)]) == 1
     assert n([(200000, True, 2), (16384, False, 2)]) == 2 + 1
@@ -127,3 +127,30 @@ def test_topk_problem_layout_and_batch_launch_count():
     assert n([(16384, False, 0)]) == 0
     with pytest.raises(ValueError):
         n([(100, True, 1)] * 5)
+
+
+def test_batch_block_output_argument_checks(lib):
+    """Block outputs need an output pointer, block_k <= 2048, rows of scores
+    (len_div 1) and rows a cluster takes (stride <= 131072); all refused
+    before anything is launched."""
+    import ctypes
+    import dsa_sparse_attention_paged_gb300 as D
+
+    def prob(**kw):
+        f = dict(logits=0x10000, stride=4096, context_lens=0x10000, histogram=None,
+                 out_idx=0x10000, fallback_flags=None, block_out_idx=0x10000,
+                 block_fallback_flags=None, next_n=1, len_div=1, R=2, reset_histogram=0,
+                 k=64, block_k=16)
+        f.update(kw)
+        return D.TopkProblem(**f)
+
+    def call(*ps):
+        arr = (D.TopkProblem * len(ps))(*ps)
+        return lib.dsa_coarse_hist_topk_batch(arr, len(ps), ctypes.c_void_p(0x20000), 1 << 30,
+                                              None)
+    assert call(prob(block_out_idx=None)) == 1
+    assert call(prob(block_k=-1)) == 1
+    assert call(prob(block_k=4096)) == 2
+    assert call(prob(len_div=8)) == 2
+    assert call(prob(stride=200000)) == 2
+    assert call(prob(stride=1000), prob(stride=200000, block_k=0, block_out_idx=None)) == 2

@@ -59,14 +59,16 @@ def test_full_size_workload(name):
     # dense top-2048
     assert sets_equal(dense_idx.cpu().numpy(), O.topk(Lm, rl, 2048))
 
-    # two-level chain
-    A = plan.amax.cpu().numpy()
+    # two-level chain: block maxima of the GPU's own logits (selected inside
+    # the select when rows fit a cluster, else written by the logits pass)
     kb = plan.kb
     nb = (rl + 7) // 8
-    refA = O.block_amax8(Lm, rl, skip_le=kb, amax_stride=plan.amax_stride, fill=0.0)
-    for r in range(R):
-        if nb[r] > kb:
-            np.testing.assert_array_equal(A[r, :nb[r]], refA[r, :nb[r]])
+    A = O.block_amax8(Lm, rl, skip_le=kb, amax_stride=plan.amax_stride, fill=0.0)
+    if plan.amax is not None:
+        Ag = plan.amax.cpu().numpy()
+        for r in range(R):
+            if nb[r] > kb:
+                np.testing.assert_array_equal(Ag[r, :nb[r]], A[r, :nb[r]])
     rtr = np.arange(R, dtype=np.int32) // nn
     t_ref, p_ref, v_ref = O.block_table(A, rl, rtr, kb, case["page_table"], ps)
     np.testing.assert_array_equal(plan.block_ids.cpu().numpy(), t_ref)

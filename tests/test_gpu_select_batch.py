@@ -114,3 +114,78 @@ def test_widest_bins_use_a_fine_window(kind, n):
         torch.cuda.synchronize()
         assert ws.status() == 0
         assert sets_equal(out.cpu().numpy(), O.topk(x, np.full(R, n), 2048)), h is None
+
+
+def _block_ref(L, rl, kb):
+    nb = (rl + 7) // 8
+    A = O.block_amax8(L, rl, skip_le=0, amax_stride=(L.shape[1] + 7) // 8)
+    return O.topk(A, nb, kb)
+
+
+@pytest.mark.parametrize("B,nn,ctx,ps,dist,kb", [
+    (3, 1, [40000, 9000, 70000], 64, "mixed", 512),  # clusters, ragged last blocks
+    (2, 2, [131072, 20001], 64, "normal", 512),      # the longest rows a cluster takes
+    (9, 1, [5000] * 4 + [16000] * 5, 64, "unit", 512),  # one CTA a row
+    (2, 3, [3000, 100000], 128, "fine", 2048),       # block_k = k, short rows take all
+    (3, 1, [7, 4097, 0], 64, "normal", 16),          # tiny and empty rows
+])
+def test_fused_block_maxima_select(B, nn, ctx, ps, dist, kb):
+    """Top-kb of the block maxima chosen in the same launch as the top-2048
+    of the scores: the same sets as block_amax8 + top-k over the maxima."""
+    import dsa_sparse_attention_paged_gb300 as D
+    case = make(B, nn, ctx, ps, dist, seed=400 + B + kb)
+    d = to_dev(case)
+    R = B * nn
+    stride = (max(ctx) + 7) // 8 * 8 or 8
+    ws = D.Workspace(R)
+    logits = torch.full((R, stride), float("nan"), dtype=torch.float32, device="cuda")
+    hist = torch.zeros((R, 1024), dtype=torch.int32, device="cuda")
+    D.paged_mqa_logits(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"],
+                       d["context_lens"], nn, ws, logits=logits, histogram=hist)
+    flags = torch.full((2, R), 9, dtype=torch.int32, device="cuda")
+    (out, bout), = D.coarse_hist_topk_batch([
+        dict(logits=logits, context_lens=d["context_lens"], next_n=nn, k=2048, histogram=hist,
+             reset_histogram=True, fallback_flags=flags[0], block_k=kb,
+             block_fallback_flags=flags[1])], ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    rl = O.row_lens(case["context_lens"], nn)
+    L = logits.cpu().numpy()
+    assert sets_equal(out.cpu().numpy(), O.topk(L, rl, 2048))
+    assert sets_equal(bout.cpu().numpy(), _block_ref(L, rl, kb))
+    assert (flags.cpu().numpy() == 0).all(), flags
+
+
+@pytest.mark.parametrize("n", [60000, 12000])
+@pytest.mark.parametrize("kind", ["nan_blocks", "tied_maxima", "wide_bin"])
+def test_fused_block_select_edge_cases(kind, n):
+    """All-NaN blocks are never chosen; thousands of equal maxima overflow the
+    candidate slots and take the exact fallback (ties to the lower block);
+    maxima spread over the saturating bin use the fine window."""
+    import dsa_sparse_attention_paged_gb300 as D
+    R = 3
+    rng = np.random.default_rng(23)
+    x = rng.normal(0, 2, (R, n)).astype(np.float32)
+    if kind == "nan_blocks":
+        x[:, : n // 2] = np.nan
+        x[1, 8 * 100: 8 * 101 - 3] = 5.0     # a block with a few NaN still counts
+    elif kind == "tied_maxima":
+        x[:, :] = rng.normal(-5, 1, (R, n)).astype(np.float32)
+        x[:, ::8] = 1.0                      # every block has the same maximum
+    else:
+        x[:, ::3] = np.exp(rng.uniform(np.log(223.0), np.log(1e7), (R, (n + 2) // 3)))
+    L = torch.from_numpy(x).cuda()
+    ctx = torch.tensor([n, n - 5, n // 3], dtype=torch.int32, device="cuda")
+    hist = torch.from_numpy(O.histogram(x, ctx.cpu().numpy())).cuda()
+    ws = D.Workspace(R)
+    bflags = torch.full((R,), 9, dtype=torch.int32, device="cuda")
+    (out, bout), = D.coarse_hist_topk_batch([
+        dict(logits=L, context_lens=ctx, next_n=1, k=2048, histogram=hist, block_k=512,
+             block_fallback_flags=bflags)], ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    rl = ctx.cpu().numpy().astype(np.int64)
+    assert sets_equal(out.cpu().numpy(), O.topk(x, rl, 2048))
+    assert sets_equal(bout.cpu().numpy(), _block_ref(x, rl, 512))
+    f = bflags.cpu().numpy()
+    assert set(f.tolist()) <= ({0, 2} if kind == "tied_maxima" else {0}), f
