@@ -80,7 +80,7 @@ def _load():
         "dsa_block_amax8": (i32, [P, i64, P, i32, i32, i32, P, i64, P, sz, P]),
         "dsa_sort_candidate_blocks": (i32, [P, i32, P, i32, i32, P, i64, i32, P, P, P, sz, P]),
         "dsa_sparse_mqa_logits": (i32, [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, i32, P,
-                                        i32, P, i32, i64, P, sz, P]),
+                                        i32, P, P, P, i32, i64, P, sz, P]),
         "dsa_topk_fp16": (i32, [P, i64, P, i32, i32, P, i32, P, P, sz, P]),
         "dsa_coarse_hist_topk_noalloc": (i32, [P, i64, P, i32, i32, i32, P, i32, i32, P, P, P]),
         "dsa_coarse_bins_range": (i32, [u32, i64, P, P]),
@@ -294,7 +294,11 @@ def sort_candidate_blocks(block_ids, context_lens, next_n, page_table, page_size
 
 
 def sparse_mqa_logits(q, kv_pages, kscale, weights, page_table, context_lens, next_n,
-                      block_table, ws, out=None, out_dtype=OUT_F32, stream=None):
+                      block_table, ws, out=None, out_dtype=OUT_F32, phys_blocks=None,
+                      valid_lens=None, stream=None):
+    """Sparse logits over the block table; with ``phys_blocks`` and
+    ``valid_lens`` from ``sort_candidate_blocks`` the page-table reads are
+    skipped (same results)."""
     q, kv_pages = _u8(q), _u8(kv_pages)
     R, H, D = q.shape
     P, ps, _ = kv_pages.shape
@@ -304,10 +308,14 @@ def sparse_mqa_logits(q, kv_pages, kscale, weights, page_table, context_lens, ne
         dt = torch.float32 if out_dtype == OUT_F32 else torch.float16
         out = torch.empty((R, kb * 8), dtype=dt, device=q.device)
     _req(block_table, torch.int32, "block_table")
+    for t, nm in ((phys_blocks, "phys_blocks"), (valid_lens, "valid_lens")):
+        if t is not None:
+            _req(t, torch.int32, nm)
     _check(lib.dsa_sparse_mqa_logits(
         _p(q), _p(kv_pages), _p(kscale), _p(weights), _p(page_table), page_table.stride(0),
-        _p(context_lens), B, next_n, H, D, ps, P, _p(block_table), kb, _p(out), out_dtype,
-        out.stride(0), ws.ptr, ws.nbytes, _stream(stream)), "sparse_mqa_logits")
+        _p(context_lens), B, next_n, H, D, ps, P, _p(block_table), kb, _p(phys_blocks),
+        _p(valid_lens), _p(out), out_dtype, out.stride(0), ws.ptr, ws.nbytes, _stream(stream)),
+        "sparse_mqa_logits")
     return out
 
 

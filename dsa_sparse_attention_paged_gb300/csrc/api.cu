@@ -246,13 +246,15 @@ int32_t dsa_sparse_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const f
                               int64_t page_table_stride, const int32_t *context_lens, int32_t B,
                               int32_t next_n, int32_t num_heads, int32_t head_dim,
                               int32_t page_size, int32_t num_pages, const int32_t *block_table,
-                              int32_t kb, void *out, int32_t out_dtype, int64_t out_stride,
-                              void *workspace, size_t ws_bytes, void *stream) {
+                              int32_t kb, const int32_t *phys_blocks, const int32_t *valid_lens,
+                              void *out, int32_t out_dtype, int64_t out_stride, void *workspace,
+                              size_t ws_bytes, void *stream) {
   int32_t e = check_paged_common(q, kv_pages, kscale, weights, page_table, page_table_stride,
                                  context_lens, B, next_n, num_heads, head_dim, page_size,
                                  num_pages, workspace, ws_bytes);
   if (e != DSA_OK) return e;
   if (!block_table || !out) return DSA_ERR_INVALID_ARG;
+  if ((phys_blocks == nullptr) != (valid_lens == nullptr)) return DSA_ERR_INVALID_ARG;
   if (kb < 16 || kb % 16 != 0) return DSA_ERR_UNSUPPORTED;
   if (out_dtype != DSA_OUT_F32 && out_dtype != DSA_OUT_F16) return DSA_ERR_INVALID_ARG;
   if (out_stride < (int64_t)kb * 8) return DSA_ERR_INVALID_ARG;
@@ -279,6 +281,8 @@ int32_t dsa_sparse_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const f
   c.out_f16 = (out_dtype == DSA_OUT_F16);
   c.block_table = block_table;
   c.kb = kb;
+  c.phys = phys_blocks;
+  c.valid_lens = valid_lens;
   c.status = status_word(workspace);
   c.wait_limit = kDefaultWaitLimit;
   return run_paged_logits(c, static_cast<cudaStream_t>(stream));

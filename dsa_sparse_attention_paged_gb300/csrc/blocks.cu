@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kSortThreads)
                        const int32_t *page_table, int64_t pt_stride, int page_size,
                        int32_t *phys, int32_t *valid_lens, uint32_t *status) {
   pdl_wait();  // predecessor grids complete before any global access
+  pdl_release_dependents();  // one CTA per row: the sparse logits set up on the idle SMs
   __shared__ uint32_t bm[kMaxBitmapWords];
   __shared__ int sm_scan[kSortThreads / 32 + 1];
   __shared__ long long sm_live[kSortThreads / 32];

@@ -57,12 +57,18 @@ __device__ __forceinline__ uint32_t lane_id() {
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start while its predecessor on the stream finishes.
 // pdl_wait() blocks until every predecessor grid has completed and its memory
-// is visible; each kernel calls it before touching global memory.  No kernel
-// releases its dependents early (griddepcontrol.launch_dependents): CTAs of
-// the next grid that became resident while a grid was still running slowed
-// that grid down by more than the launch latency they hid, so dependents
-// launch as the running grid's CTAs exit.
+// is visible; each kernel calls it before touching memory a predecessor
+// writes.  Kernels do not release their dependents early as a rule
+// (griddepcontrol.launch_dependents): CTAs of the next grid that became
+// resident while a large grid was still running slowed that grid down by more
+// than the launch latency they hid, so dependents launch as the running
+// grid's CTAs exit.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// The one exception: a small grid whose successor can set itself up on the
+// SMs the small grid leaves idle releases it at once (sort -> sparse logits).
+__device__ __forceinline__ void pdl_release_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- clusters
 // Distributed shared memory: map a shared address of this CTA to the same

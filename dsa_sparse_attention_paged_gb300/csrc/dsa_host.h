@@ -35,6 +35,8 @@ struct LogitsCall {
   bool out_f16;
   const int32_t *block_table;
   int32_t kb;
+  const int32_t *phys = nullptr;        // sparse: physical blocks of the table, or NULL
+  const int32_t *valid_lens = nullptr;  // sparse, with phys: live prefix length per row
   uint32_t *status;
   long long wait_limit;
 };

@@ -65,6 +65,8 @@ struct LogitsArgs {
   int32_t sparse_tpu;   // sparse: stages per row (ceil(kb / 32))
   const int32_t *block_table;
   int32_t kb;
+  const int32_t *phys;        // sparse: physical blocks (pool slot / 8) of the table, or NULL
+  const int32_t *valid_lens;  // sparse, with phys: live positions form the prefix [0, len)
   void *out;
   int64_t out_stride;
   int32_t *histogram;
@@ -80,14 +82,17 @@ struct LogitsArgs {
 };
 
 struct SmemPlan {
-  int kst, q, ks, w, hist, bar, misc, total;
+  int kst, q, ks, w, hist, bar, misc, sptab, total;
 };
+
+constexpr int kSpTab = 32;  // sparse: stages whose K rows the producer holds in shared memory
 
 // Histogram slots per epilogue warpgroup: one per warp at next_n = 1, one
 // shared by the group's four warps otherwise (shared memory goes to stages).
 __host__ __device__ constexpr int hist_slots_per_group(int nn) { return nn == 1 ? 4 : 1; }
 
-__host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, int stages, int nacc, int nks) {
+__host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, bool sparse, int stages, int nacc,
+                                              int nks) {
   SmemPlan p;
   int off = 0;
   p.kst = off;
@@ -105,6 +110,8 @@ __host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, int stages, int
   off += (2 * stages + 2 * nks + 4 + 2 * nacc + 3) * 8;
   p.misc = off;
   off += 64 + 2 * 32 * 4;  // flags/schedule + the producer's two row tables
+  p.sptab = off;
+  off += sparse ? kSpTab * 32 * 4 : 0;
   p.total = off + 1024;  // slack to align the base to 1024 bytes
   return p;
 }
@@ -292,7 +299,9 @@ template <int NN, bool SPARSE, bool OUT_F16, bool HIST>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const LogitsArgs a) {
-  pdl_wait();  // predecessor grids complete before any global access
+  // the dense pass waits for its predecessors at once; the sparse pass sets up
+  // (barriers, schedule, TMEM, tensor maps: nothing a predecessor writes) first
+  if (!SPARSE) pdl_wait();
   constexpr int N = 32 * NN;
   constexpr uint32_t IDESC = idesc_e4m3_f32(128, N);
   constexpr int HS = hist_slots_per_group(NN);
@@ -303,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = a.num_stages;
   const int A = a.num_acc;
   const int KS = a.num_ks;
-  const SmemPlan P = smem_plan(NN, HIST, S, A, KS);
+  const SmemPlan P = smem_plan(NN, HIST, SPARSE, S, A, KS);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -373,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (SPARSE) pdl_wait();  // the block table, physical blocks and live lengths are ready
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl ctl{abort_flag, a.status, a.wait_limit};
 
@@ -397,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (SPARSE) {
         const int blk = g0.i * 32 + my_sl;
         if (blk >= a.kb) return kNone;
-        return __ldg(&a.block_table[(int64_t)g0.u * a.kb + blk]);
+        return __ldg(&(a.phys ? a.phys : a.block_table)[(int64_t)g0.u * a.kb + blk]);
       }
       const int64_t p = (int64_t)g0.i * ppt + my_sl;
       if (p * a.page_size >= eff_ctx(a, g0.u)) return kNone;
@@ -406,6 +416,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // physical row of a slot (or -1 when nothing is loaded)
     auto to_row = [&](int raw, int unit) -> int {
       if (raw == kNone || unit < 0) return -1;
+      if (SPARSE && a.phys) {
+        // physical block: its 8 rows of the pool directly (no page-table read)
+        if (raw == INT32_MAX || raw < 0) return -1;
+        if ((int64_t)raw * 8 + 8 > (int64_t)a.num_pages * a.page_size) {
+          set_status(a.status, DSA_DEV_BOUNDS);
+          return -1;
+        }
+        return raw * 8;
+      }
       if (SPARSE) {
         const int b = unit / a.req_next_n;
         const int j = unit - b * a.req_next_n;
@@ -429,7 +448,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol = policy_evict_first();
     const int blk_rows = SPARSE ? 8 : a.page_size;
     int nxt_unit;
-    int nxt = fetch(git, 0, nxt_unit);
+    // sparse with physical blocks: the K rows of the next kSpTab stages sit in
+    // a shared table, refilled with one round of loads every kSpTab stages
+    const bool sptab = SPARSE && a.phys != nullptr;
+    int *sp_tab = reinterpret_cast<int *>(smem + P.sptab);
+    int tab_i = 0;
+    int nxt = sptab ? kNone : fetch(git, 0, nxt_unit);
     int cur_row = -1;
     int prev_u = -1, unit_ord = -1;
     long long issued = 0;
@@ -442,13 +466,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (long long n = 0; n < count && ok; ++n, it.next(a), rs.next(), rk.next(),
                    o = (o + 1 == tpg) ? 0 : o + 1) {
       const int u = it.u;
-      if (o == 0) {
-        cur_row = to_row(nxt, nxt_unit);
-        for (int k = 0; k < tpg; ++k) git.next(a);
-        nxt = fetch(git, n + tpg, nxt_unit);
+      int row;
+      if (sptab) {
+        if (tab_i == 0) {
+          // flattened stage g = (row, tile) in closed form, so the loads of
+          // eight stages are in flight together
+          const long long gbase = (long long)u_start * a.sparse_tpu + i_start + n;
+          for (int j0 = 0; j0 < kSpTab && n + j0 < count; j0 += 8) {
+            int raw[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              raw[jj] = kNone;
+              if (n + j0 + jj < count) {
+                const long long g = gbase + j0 + jj;
+                const int uu = (int)(g / a.sparse_tpu);
+                const int blk = (int)(g - (long long)uu * a.sparse_tpu) * 32 + lane;
+                if (blk < a.kb) raw[jj] = __ldg(&a.phys[(int64_t)uu * a.kb + blk]);
+              }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) sp_tab[(j0 + jj) * 32 + lane] = to_row(raw[jj], 0);
+          }
+          __syncwarp();
+        }
+        row = sp_tab[tab_i * 32 + lane];
+        tab_i = (tab_i + 1 == kSpTab) ? 0 : tab_i + 1;
+      } else {
+        if (o == 0) {
+          cur_row = to_row(nxt, nxt_unit);
+          for (int k = 0; k < tpg; ++k) git.next(a);
+          nxt = fetch(git, n + tpg, nxt_unit);
+        }
+        row = __shfl_sync(0xffffffffu, cur_row, (o * ppt + my_sl) & 31);
+        if (lane >= ppt) row = -1;
       }
-      int row = __shfl_sync(0xffffffffu, cur_row, (o * ppt + my_sl) & 31);
-      if (lane >= ppt) row = -1;
       if (u != prev_u) {
         ++unit_ord;
         prev_u = u;
@@ -618,7 +669,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++unit_ord;
         prev_u = u;
         qb = unit_ord & 1;
-        if (SPARSE) {
+        if (SPARSE && a.valid_lens) {
+          n_row = __ldg(&a.valid_lens[u]);  // live positions of the sparse row
+        } else if (SPARSE) {
           const int b = u / a.req_next_n;
           const int j = u - b * a.req_next_n;
           n_row = eff_ctx(a, b) - (a.req_next_n - 1 - j);
@@ -633,7 +686,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kx = rk.idx;
       const int64_t pos = (int64_t)i * kStageTok + tok;
       int32_t blk = INT32_MAX;
-      if (SPARSE && pos < (int64_t)a.kb * 8) blk = __ldg(&a.block_table[(int64_t)u * a.kb + pos / 8]);
+      if (SPARSE && !a.valid_lens && pos < (int64_t)a.kb * 8)
+        blk = __ldg(&a.block_table[(int64_t)u * a.kb + pos / 8]);
       if (!(ok = ewait(KSF(kx), rk.ph))) break;
       const float ks = ks_s[kx * kStageTok + tok];
       __syncwarp();
@@ -666,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (SPARSE) {
         if (pos < (int64_t)a.kb * 8) {
           const int64_t t = (int64_t)blk * 8 + (pos & 7);
-          const bool live = blk != INT32_MAX && blk >= 0 && t < n_row;
+          const bool live = a.valid_lens ? pos < n_row : (blk != INT32_MAX && blk >= 0 && t < n_row);
           const float val = live ? acc[0] : -INFINITY;
           if (OUT_F16) {
             reinterpret_cast<__half *>(a.out)[(int64_t)u * a.out_stride + pos] = __float2half_rn(val);
@@ -739,7 +793,7 @@ struct LaunchPlan {
   int stages, nacc, nks, cols, smem;
 };
 
-inline LaunchPlan plan_for(int nn, bool hist) {
+inline LaunchPlan plan_for(int nn, bool hist, bool sparse) {
   LaunchPlan L;
   const int N = 32 * nn;
   L.nacc = std::min(4, 512 / (2 * N));  // TMEM pairs (two 128-lane sub-tiles each)
@@ -747,10 +801,10 @@ inline LaunchPlan plan_for(int nn, bool hist) {
   while (L.cols < 2 * L.nacc * N) L.cols <<= 1;
   L.stages = kMaxStages;
   while (L.stages > 2 &&
-         smem_plan(nn, hist, L.stages, L.nacc, L.stages + L.nacc + 2).total > kSmemLimit)
+         smem_plan(nn, hist, sparse, L.stages, L.nacc, L.stages + L.nacc + 2).total > kSmemLimit)
     --L.stages;
   L.nks = L.stages + L.nacc + 2;
-  L.smem = smem_plan(nn, hist, L.stages, L.nacc, L.nks).total;
+  L.smem = smem_plan(nn, hist, sparse, L.stages, L.nacc, L.nks).total;
   return L;
 }
 
@@ -758,7 +812,7 @@ template <int NN, bool SPARSE, bool OUT_F16, bool HIST>
 dsa_status_t launch_one(const CUtensorMap &tk, const CUtensorMap &tq, const LogitsArgs &a0,
                         int grid, cudaStream_t st) {
   LogitsArgs a = a0;
-  const LaunchPlan L = plan_for(NN, HIST);
+  const LaunchPlan L = plan_for(NN, HIST, SPARSE);
   a.num_acc = L.nacc;
   a.num_ks = L.nks;
   a.tmem_cols = (uint32_t)L.cols;
@@ -770,7 +824,7 @@ dsa_status_t launch_one(const CUtensorMap &tk, const CUtensorMap &tq, const Logi
 
 }  // namespace
 
-int logits_stages_for(int next_n, bool hist) { return plan_for(next_n, hist).stages; }
+int logits_stages_for(int next_n, bool hist) { return plan_for(next_n, hist, false).stages; }
 
 dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   CUtensorMap tk, tq;
@@ -793,6 +847,8 @@ dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   a.num_pages = c.num_pages;
   a.block_table = c.block_table;
   a.kb = c.kb;
+  a.phys = c.sparse ? c.phys : nullptr;
+  a.valid_lens = c.sparse ? c.valid_lens : nullptr;
   a.out = c.out;
   a.out_stride = c.out_stride;
   a.histogram = c.histogram;

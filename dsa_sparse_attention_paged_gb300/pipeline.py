@@ -107,7 +107,8 @@ class DecodePlan:
         mark("publish", 1)
         mark("consume", 0)
         sparse_mqa_logits(q, kv, kscale, weights, page_table, context_lens, nn,
-                          self.block_ids, ws, out=self.sparse, out_dtype=OUT_F16)
+                          self.block_ids, ws, out=self.sparse, out_dtype=OUT_F16,
+                          phys_blocks=self.phys, valid_lens=self.valid_lens)
         topk_fp16(self.sparse, self.valid_lens, self.k, ws, block_table=self.block_ids,
                   out=self.sparse_idx)
         mark("consume", 1)

@@ -307,14 +307,20 @@ int32_t dsa_sort_candidate_blocks(int32_t *block_ids, int32_t kb, const int32_t 
  * dsa_paged_mqa_logits; kb % 16 == 0.
  *   out        [R][out_stride] float (DSA_OUT_F32) or FP16 bits (DSA_OUT_F16,
  *              round-to-nearest-even of the float logit, [VL52696] "Why":
- *              the logits kernel writes FP16 directly), out_stride >= kb*8 */
+ *              the logits kernel writes FP16 directly), out_stride >= kb*8
+ *   phys_blocks, valid_lens  both NULL, or both the outputs of
+ *              dsa_sort_candidate_blocks for this table: the K rows are then
+ *              read straight from the physical blocks (no page-table read
+ *              per block) and position i is live iff i < valid_lens[r] (the
+ *              table's live positions form a prefix); same results. */
 int32_t dsa_sparse_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const float *kscale,
                               const float *weights, const int32_t *page_table,
                               int64_t page_table_stride, const int32_t *context_lens, int32_t B,
                               int32_t next_n, int32_t num_heads, int32_t head_dim,
                               int32_t page_size, int32_t num_pages, const int32_t *block_table,
-                              int32_t kb, void *out, int32_t out_dtype, int64_t out_stride,
-                              void *workspace, size_t ws_bytes, void *stream);
+                              int32_t kb, const int32_t *phys_blocks, const int32_t *valid_lens,
+                              void *out, int32_t out_dtype, int64_t out_stride, void *workspace,
+                              size_t ws_bytes, void *stream);
 
 /* ---- top-k over FP16 scores ---------------------------------------------
  * [VL52696] "Why": select on the packed FP16 score bits directly (both halves

@@ -57,6 +57,25 @@ def paged(lib, **kw):
                                     a["ws"], a["wsb"], a["st"])
 
 
+def sparse(lib, **kw):
+    a = dict(q=A16, kv=A16, ks=A16, w=A16, pt=A16, pts=4, ctx=A16, B=2, nn=1, H=32, D=128,
+             ps=64, P=10, bt=A16, kb=64, phys=None, vl=None, out=A16, dt=0, ostride=512,
+             ws=ctypes.c_void_p(0x20000), wsb=4096, st=None)
+    a.update(kw)
+    return lib.dsa_sparse_mqa_logits(a["q"], a["kv"], a["ks"], a["w"], a["pt"], a["pts"],
+                                     a["ctx"], a["B"], a["nn"], a["H"], a["D"], a["ps"], a["P"],
+                                     a["bt"], a["kb"], a["phys"], a["vl"], a["out"], a["dt"],
+                                     a["ostride"], a["ws"], a["wsb"], a["st"])
+
+
+def test_sparse_logits_argument_checks(lib):
+    assert sparse(lib, phys=A16) == 1          # physical blocks without live lengths
+    assert sparse(lib, vl=A16) == 1
+    assert sparse(lib, kb=40) == 2
+    assert sparse(lib, ostride=100) == 1
+    assert sparse(lib, bt=None) == 1
+
+
 def test_paged_logits_argument_checks(lib):
     assert paged(lib, nn=5) == 2
     assert paged(lib, nn=0) == 2
@@ -91,10 +110,10 @@ def test_topk_and_block_argument_checks(lib):
     assert h(A16, 8192, A16, 1, 2, A16, 4, 64, None, None, ws, 4096, None) == 2
     assert h(A16, 512, A16, 1, 2, A16, 4, 12, None, None, ws, 4096, None) == 2
     s = lib.dsa_sparse_mqa_logits
-    assert s(A16, A16, A16, A16, A16, 4, A16, 2, 1, 32, 128, 64, 10, A16, 500, A16, 0, 4000,
-             ws, 4096, None) == 2  # kb not a multiple of 16
-    assert s(A16, A16, A16, A16, A16, 4, A16, 2, 1, 32, 128, 64, 10, A16, 512, A16, 0, 100,
-             ws, 4096, None) == 1  # out_stride < kb * 8
+    assert s(A16, A16, A16, A16, A16, 4, A16, 2, 1, 32, 128, 64, 10, A16, 500, None, None, A16,
+             0, 4000, ws, 4096, None) == 2  # kb not a multiple of 16
+    assert s(A16, A16, A16, A16, A16, 4, A16, 2, 1, 32, 128, 64, 10, A16, 512, None, None, A16,
+             0, 100, ws, 4096, None) == 1  # out_stride < kb * 8
     t = lib.dsa_topk_fp16
     assert t(A16, 4097, A16, 2, 16, None, 0, A16, ws, 4096, None) == 3  # odd stride
     assert t(A16, 4096, A16, 2, 0, None, 0, A16, ws, 4096, None) == 2

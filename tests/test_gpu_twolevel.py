@@ -89,6 +89,15 @@ def test_two_level_chain(ctx, kb, ps, nn):
         assert (~masked[r, :v_ref[r]]).all() and masked[r, v_ref[r]:].all()
     # FP16 output is the RN-even rounding of the FP32 one
     np.testing.assert_array_equal(sp16.cpu().numpy().view(np.uint16), O.fp16_rn_array(SP))
+    # reading the K rows through the sort's physical blocks and live lengths
+    # gives bitwise the same scores, FP32 and FP16
+    for dt, ref in ((D.OUT_F32, sp), (D.OUT_F16, sp16)):
+        via = D.sparse_mqa_logits(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"],
+                                  d["context_lens"], nn, ids, ws, out_dtype=dt,
+                                  phys_blocks=phys, valid_lens=vl)
+        torch.cuda.synchronize()
+        assert torch.equal(via.view(torch.int16 if dt == D.OUT_F16 else torch.int32),
+                           ref.view(torch.int16 if dt == D.OUT_F16 else torch.int32))
 
     # FP16 top-2048 with the fused table transform, on the GPU's own FP16 scores
     k = 2048
