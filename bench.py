@@ -332,6 +332,19 @@ def main():
     torch.cuda.synchronize()
     stage_us = {n: 1e3 * statistics.mean(e[n][0].elapsed_time(e[n][1]) for e in ev_d)
                 for n in stages}
+    # the same step replayed from a CUDA graph (diagnostic, untimed region):
+    # what host launch overhead costs the eager step
+    plan.capture(*inputs)
+    Kg = max(1, min(K, 200))
+    gs, ge = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    plan.replay()
+    torch.cuda.synchronize()
+    gs.record()
+    for _ in range(Kg):
+        plan.replay()
+    ge.record()
+    torch.cuda.synchronize()
+    graph_us = 1e3 * gs.elapsed_time(ge) / Kg
 
     if rank != 0:
         if dist is not None:
@@ -361,6 +374,7 @@ def main():
         "logits_us": 1e3 * lg_ms,
         "stage_us": stage_us,
         "stage_note": "stages timed in a separate loop with events between them",
+        "graph_us_per_step": graph_us,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": "logits_kernel<next_n=1, histogram>",

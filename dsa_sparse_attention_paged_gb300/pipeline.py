@@ -113,3 +113,26 @@ class DecodePlan:
                   out=self.sparse_idx)
         mark("consume", 1)
         return self.topk_idx, self.sparse_idx
+
+    def capture(self, q, kv, kscale, weights, page_table, context_lens, stream=None):
+        """Capture one step into a CUDA graph (after one eager step that sets
+        the kernels' launch attributes).  Every grid depends only on the plan's
+        shape (B, next_n, the maximum stride, kb), and every kernel reads the
+        context lengths from device memory, so the graph stays valid when the
+        caller rewrites ``context_lens`` (within the maximum), ``q``,
+        ``weights``, ``page_table`` or the cache contents in place: ``replay()``
+        then runs the step on the new values.  Returns the graph."""
+        self.step(q, kv, kscale, weights, page_table, context_lens)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            out = self.step(q, kv, kscale, weights, page_table, context_lens)
+        self.graph = g
+        self.graph_out = out
+        return g
+
+    def replay(self):
+        """Run the captured step (see ``capture``); returns its outputs."""
+        self.graph.replay()
+        return self.graph_out
+
