@@ -42,6 +42,9 @@
  *       length of a sparse row counts the live tokens of the chosen blocks.
  *   R9  Sparse positions that are padding or past the row's live length are
  *       -inf in the output.
+ *   R10 The BF16 sibling of the FP16 select (the next step the pages point
+ *       to, [VL52696] "Why" for FP16): bfloat16 rounding is round-to-nearest-
+ *       even, NaN never selected, the same order and tie rule as FP16.
  */
 #include <math.h>
 #include <stdint.h>
@@ -115,6 +118,47 @@ uint16_t o_fp16_rn_bits(float x)
     }
     if (e + 15 >= 31) return (uint16_t)(sign | 0x7C00u);
     return (uint16_t)(sign | (uint16_t)(((e + 15) << 10) | ((int)q - 1024)));
+}
+
+/* bfloat16 (1 sign, 8 exponent bits with bias 127, 7 mantissa bits; the top
+ * half of a binary32), round-to-nearest-even from the value, as the FP16
+ * conversion above (the BF16 sibling of the FP16 select, NEXT-3).          */
+uint16_t o_bf16_rn_bits(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    if (isnan(x)) return (uint16_t)(sign | 0x7FC0u);
+    if (isinf(x)) return (uint16_t)(sign | 0x7F80u);
+    double a = fabs((double)x);
+    if (a < ldexp(1.0, -126)) {
+        /* subnormal range: quantum 2^-133 */
+        double q = o_round_half_even(a * ldexp(1.0, 133));
+        return (uint16_t)(sign | (uint16_t)q);  /* q == 128 is the smallest normal */
+    }
+    int E;
+    (void)frexp(a, &E);          /* a = f * 2^E, f in [0.5, 1) */
+    int e = E - 1;               /* a in [2^e, 2^(e+1))        */
+    double q = o_round_half_even(a * ldexp(1.0, 7 - e));    /* in [128, 256] */
+    if (q >= 256.0) {
+        q = 128.0;
+        e += 1;
+    }
+    if (e + 127 >= 255) return (uint16_t)(sign | 0x7F80u);
+    return (uint16_t)(sign | (uint16_t)(((e + 127) << 7) | ((int)q - 128)));
+}
+
+/* bfloat16 pattern -> double, from the definition. */
+double o_bf16_bits_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 255;
+    int m = h & 127;
+    double mag;
+    if (e == 255) mag = (m == 0) ? INFINITY : NAN;
+    else if (e == 0) mag = ldexp((double)m, -133);
+    else mag = ldexp(1.0 + (double)m / 128.0, e - 127);
+    return sign ? -mag : mag;
 }
 
 /* binary16 pattern -> double, from the definition (used by the FP16 select). */
@@ -398,11 +442,13 @@ void o_sparse_logits(const uint8_t *q, const uint8_t *kv, const float *kscale,
  * table[r][i/8]*8 + i%8 when a table is given, else the position i.        */
 static uint32_t o_f16_order_key(uint16_t h)
 {
+    /* sign-magnitude 16-bit formats (FP16 and BF16 alike) order by this key */
     return (h & 0x8000u) ? (uint32_t)(~h & 0xFFFFu) : (uint32_t)(h | 0x8000u);
 }
 
-void o_topk_fp16(const uint16_t *scores, int64_t stride, const int32_t *valid_len, int R,
-                 int64_t k, const int32_t *table, int kb, int32_t *out /* [R][k] */)
+static void o_topk_16(const uint16_t *scores, int64_t stride, const int32_t *valid_len, int R,
+                      int64_t k, const int32_t *table, int kb, int32_t *out,
+                      double (*decode)(uint16_t))
 {
     for (int r = 0; r < R; ++r) {
         int64_t n = valid_len[r];
@@ -410,7 +456,7 @@ void o_topk_fp16(const uint16_t *scores, int64_t stride, const int32_t *valid_le
         int64_t cnt = 0;
         for (int64_t i = 0; i < n; ++i) {
             uint16_t h = scores[(int64_t)r * stride + i];
-            if (isnan(o_fp16_bits_to_double(h))) continue;
+            if (isnan(decode(h))) continue;
             buf[cnt].key = o_f16_order_key(h);
             buf[cnt].col = i;
             ++cnt;
@@ -428,6 +474,19 @@ void o_topk_fp16(const uint16_t *scores, int64_t stride, const int32_t *valid_le
         }
         free(buf);
     }
+}
+
+void o_topk_fp16(const uint16_t *scores, int64_t stride, const int32_t *valid_len, int R,
+                 int64_t k, const int32_t *table, int kb, int32_t *out /* [R][k] */)
+{
+    o_topk_16(scores, stride, valid_len, R, k, table, kb, out, o_fp16_bits_to_double);
+}
+
+/* The same selection over BF16 scores. */
+void o_topk_bf16(const uint16_t *scores, int64_t stride, const int32_t *valid_len, int R,
+                 int64_t k, const int32_t *table, int kb, int32_t *out /* [R][k] */)
+{
+    o_topk_16(scores, stride, valid_len, R, k, table, kb, out, o_bf16_bits_to_double);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -461,4 +520,19 @@ void o_coarse_bins(const float *x, int64_t n, int16_t *out)
 void o_fp16_rn_array(const float *x, int64_t n, uint16_t *out)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = o_fp16_rn_bits(x[i]);
+}
+
+void o_bf16_rn_array(const float *x, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = o_bf16_rn_bits(x[i]);
+}
+
+void o_bf16_rn_sweep(uint64_t start, uint64_t count, uint16_t *out)
+{
+    for (uint64_t i = 0; i < count; ++i) {
+        uint32_t u = (uint32_t)(start + i);
+        float x;
+        memcpy(&x, &u, 4);
+        out[i] = o_bf16_rn_bits(x);
+    }
 }

@@ -72,6 +72,13 @@ def _load():
     lib.o_coarse_bin_sweep.argtypes = [ctypes.c_uint64, ctypes.c_uint64, P]
     lib.o_coarse_bins.argtypes = [P, i64, P]
     lib.o_fp16_rn_array.argtypes = [P, i64, P]
+    lib.o_bf16_rn_bits.restype = ctypes.c_uint16
+    lib.o_bf16_rn_bits.argtypes = [ctypes.c_float]
+    lib.o_bf16_bits_to_double.restype = ctypes.c_double
+    lib.o_bf16_bits_to_double.argtypes = [ctypes.c_uint16]
+    lib.o_bf16_rn_array.argtypes = [P, i64, P]
+    lib.o_bf16_rn_sweep.argtypes = [ctypes.c_uint64, ctypes.c_uint64, P]
+    lib.o_topk_bf16.argtypes = [P, i64, P, i32, i64, P, i32, P]
     _lib = lib
     return lib
 
@@ -100,6 +107,28 @@ def fp16_rn_bits(x: float) -> int:
 
 def fp16_bits_to_double(h: int) -> float:
     return float(_load().o_fp16_bits_to_double(ctypes.c_uint16(h)))
+
+
+def bf16_rn_bits(x: float) -> int:
+    return int(_load().o_bf16_rn_bits(ctypes.c_float(x)))
+
+
+def bf16_bits_to_double(h: int) -> float:
+    return float(_load().o_bf16_bits_to_double(ctypes.c_uint16(h)))
+
+
+def bf16_rn_sweep(start: int, count: int) -> np.ndarray:
+    out = np.empty(count, dtype=np.uint16)
+    _load().o_bf16_rn_sweep(ctypes.c_uint64(start), ctypes.c_uint64(count), _ptr(out))
+    return out
+
+
+def bf16_rn_array(x: np.ndarray) -> np.ndarray:
+    """bfloat16 round-to-nearest-even bit patterns of a float32 array."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().o_bf16_rn_array(_ptr(x), x.size, _ptr(out))
+    return out
 
 
 def coarse_bin(x: float) -> int:
@@ -258,4 +287,19 @@ def topk_fp16(scores_u16, valid_len, k, table=None) -> np.ndarray:
     else:
         tp, kb = ctypes.c_void_p(0), 0
     _load().o_topk_fp16(_ptr(s), s.shape[1], _ptr(vl), R, k, tp, kb, _ptr(out))
+    return out
+
+
+
+def topk_bf16(scores_u16, valid_len, k, table=None) -> np.ndarray:
+    s = _c(scores_u16, np.uint16)
+    vl = _c(valid_len, np.int32)
+    R = s.shape[0]
+    out = np.empty((R, k), np.int32)
+    if table is not None:
+        table = _c(table, np.int32)
+        tp, kb = _ptr(table), table.shape[1]
+    else:
+        tp, kb = ctypes.c_void_p(0), 0
+    _load().o_topk_bf16(_ptr(s), s.shape[1], _ptr(vl), R, k, tp, kb, _ptr(out))
     return out

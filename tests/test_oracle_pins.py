@@ -63,6 +63,42 @@ def test_fp16_rn_matches_numpy_cast_on_all_2pow32_patterns():
     assert bad == 0
 
 
+def _bf16_chunk(args):
+    start, count = args
+    import torch as T
+    from oracle import oracle as O2
+    got = O2.bf16_rn_sweep(start, count)
+    u = np.arange(start, start + count, dtype=np.uint64).astype(np.uint32)
+    x = u.view(np.float32)
+    ref = T.from_numpy(x).to(T.bfloat16).view(T.int16).numpy().view(np.uint16)
+    isn = np.isnan(x)
+    bad = (got != ref) & ~isn
+    gh = got[isn]
+    bad_nan = ~(((gh & 0x7F80) == 0x7F80) & ((gh & 0x7F) != 0))
+    return int(bad.sum()) + int(bad_nan.sum())
+
+
+def test_bf16_rn_matches_torch_cast_on_all_2pow32_patterns():
+    """Exhaustive: the oracle's bfloat16 round-to-nearest-even conversion
+    (computed from the value) equals torch's float32->bfloat16 cast for every
+    float32 bit pattern (NaN stays NaN)."""
+    chunk = 1 << 26
+    jobs = [(s, chunk) for s in range(0, 1 << 32, chunk)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(min(8, os.cpu_count() or 1)) as pool:
+        bad = sum(pool.map(_bf16_chunk, jobs))
+    assert bad == 0
+
+
+def test_bf16_decode_matches_torch_for_all_65536_codes():
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    dec = np.array([O.bf16_bits_to_double(int(c)) for c in range(65536)])
+    np.testing.assert_array_equal(np.isnan(dec), np.isnan(ref))
+    ok = ~np.isnan(dec)
+    np.testing.assert_array_equal(dec[ok], ref[ok])
+
+
 # ---------------------------------------------------------------- O3: bins
 
 def _golden_bins():
@@ -439,6 +475,34 @@ def test_fp16_order_matches_numpy_over_all_65536_encodings():
     np.testing.assert_array_equal(np.isnan(dec), np.isnan(vals[::17].astype(np.float64)))
     ok = ~np.isnan(dec)
     np.testing.assert_array_equal(dec[ok], vals[::17].astype(np.float64)[ok])
+
+
+def test_bf16_order_matches_torch_over_all_65536_encodings():
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nonnan = ~np.isnan(vals)
+    k = int(nonnan.sum())
+    out = O.topk_bf16(codes[None, :], np.array([65536], np.int32), k)[0]
+    assert np.all(np.diff(vals[out]) <= 0)  # non-increasing values
+    assert sorted(out.tolist()) == np.nonzero(nonnan)[0].tolist()  # every non-NaN once
+    assert out.tolist().index(0x0000) < out.tolist().index(0x8000)  # +0 above -0
+    # a BF16 NaN is not an FP16 NaN (and the other way round): the formats'
+    # own rules decide
+    assert 0x7C01 in out.tolist() and 0x7F81 not in out.tolist()
+
+
+def test_bf16_topk_ties_to_lower_position_and_table_mapping():
+    one5 = int(torch.tensor([1.5]).to(torch.bfloat16).view(torch.int16).item()) & 0xFFFF
+    two = int(torch.tensor([2.0]).to(torch.bfloat16).view(torch.int16).item()) & 0xFFFF
+    s = np.full((1, 40), one5, np.uint16)
+    s[0, 33] = two
+    s[0, 5] = 0x7FC0  # NaN
+    table = np.array([[4, 9, 13, 20, 21]], np.int32)
+    out = O.topk_bf16(s, np.array([37], np.int32), 5, table)[0]
+    pos = [33, 0, 1, 2, 3]
+    assert out.tolist() == [table[0, p // 8] * 8 + p % 8 for p in pos]
+    out = O.topk_bf16(s, np.array([7], np.int32), 8)[0]
+    assert out.tolist() == [0, 1, 2, 3, 4, 6, -1, -1]
 
 
 def test_fp16_topk_ties_to_lower_position_and_table_mapping():
