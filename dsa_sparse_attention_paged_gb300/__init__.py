@@ -24,6 +24,7 @@ MAX_TOPK = 2048
 CAND_CAP = 8192
 OUT_F32 = 0
 OUT_F16 = 1
+OUT_BF16 = 2
 DEV_TIMEOUT = 0x1
 DEV_BOUNDS = 0x2
 INT32_MAX = 2**31 - 1
@@ -82,10 +83,12 @@ def _load():
         "dsa_sparse_mqa_logits": (i32, [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, i32, P,
                                         i32, P, P, P, i32, i64, P, sz, P]),
         "dsa_topk_fp16": (i32, [P, i64, P, i32, i32, P, i32, P, P, sz, P]),
+        "dsa_topk_bf16": (i32, [P, i64, P, i32, i32, P, i32, P, P, sz, P]),
         "dsa_coarse_hist_topk_noalloc": (i32, [P, i64, P, i32, i32, i32, P, i32, i32, P, P, P]),
         "dsa_coarse_bins_range": (i32, [u32, i64, P, P]),
         "dsa_coarse_bin_key_ranges": (i32, [P, P]),
         "dsa_fp16_order_keys": (i32, [P, P, i64, P]),
+        "dsa_bf16_order_keys": (i32, [P, P, i64, P]),
         "dsa_wait_timeout_selftest": (i32, [u64, P, sz, P]),
     }
     for name, (res, args) in sig.items():
@@ -305,7 +308,7 @@ def sparse_mqa_logits(q, kv_pages, kscale, weights, page_table, context_lens, ne
     B = context_lens.shape[0]
     kb = block_table.shape[1]
     if out is None:
-        dt = torch.float32 if out_dtype == OUT_F32 else torch.float16
+        dt = {OUT_F32: torch.float32, OUT_F16: torch.float16, OUT_BF16: torch.bfloat16}[out_dtype]
         out = torch.empty((R, kb * 8), dtype=dt, device=q.device)
     _req(block_table, torch.int32, "block_table")
     for t, nm in ((phys_blocks, "phys_blocks"), (valid_lens, "valid_lens")):
@@ -332,6 +335,19 @@ def topk_fp16(scores, valid_lens, k, ws, block_table=None, out=None, stream=None
     return out
 
 
+def topk_bf16(scores, valid_lens, k, ws, block_table=None, out=None, stream=None):
+    """Top-k over BF16 scores (torch.bfloat16 or raw uint16 bits)."""
+    s = scores.view(torch.uint16) if scores.dtype == torch.bfloat16 else scores
+    _req(s, torch.uint16, "scores")
+    R = s.shape[0]
+    if out is None:
+        out = torch.empty((R, k), dtype=torch.int32, device=s.device)
+    kb = 0 if block_table is None else block_table.shape[1]
+    _check(lib.dsa_topk_bf16(_p(s), s.stride(0), _p(valid_lens), R, k, _p(block_table), kb,
+                             _p(out), ws.ptr, ws.nbytes, _stream(stream)), "topk_bf16")
+    return out
+
+
 def coarse_bin_key_ranges(stream=None):
     """[1025][2] uint32 (as int64): lowest and highest order key of each coarse
     bin as the select computes them (bin 1024: an empty range)."""
@@ -354,6 +370,15 @@ def fp16_order_keys(x, out=None, stream=None):
         out = torch.empty_like(s)
     _check(lib.dsa_fp16_order_keys(_p(s), _p(out), s.numel(), _stream(stream)),
            "fp16_order_keys")
+    return out
+
+
+def bf16_order_keys(x, out=None, stream=None):
+    s = x.view(torch.uint16) if x.dtype == torch.bfloat16 else x
+    if out is None:
+        out = torch.empty_like(s)
+    _check(lib.dsa_bf16_order_keys(_p(s), _p(out), s.numel(), _stream(stream)),
+           "bf16_order_keys")
     return out
 
 

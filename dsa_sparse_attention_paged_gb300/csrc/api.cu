@@ -233,7 +233,7 @@ int32_t dsa_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const fl
   c.amax_stride = amax_stride;
   c.amax_skip = amax_skip_if_blocks_le;
   c.sparse = false;
-  c.out_f16 = false;
+  c.out_fmt = DSA_OUT_F32;
   c.block_table = nullptr;
   c.kb = 0;
   c.status = status_word(workspace);
@@ -256,7 +256,8 @@ int32_t dsa_sparse_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const f
   if (!block_table || !out) return DSA_ERR_INVALID_ARG;
   if ((phys_blocks == nullptr) != (valid_lens == nullptr)) return DSA_ERR_INVALID_ARG;
   if (kb < 16 || kb % 16 != 0) return DSA_ERR_UNSUPPORTED;
-  if (out_dtype != DSA_OUT_F32 && out_dtype != DSA_OUT_F16) return DSA_ERR_INVALID_ARG;
+  if (out_dtype != DSA_OUT_F32 && out_dtype != DSA_OUT_F16 && out_dtype != DSA_OUT_BF16)
+    return DSA_ERR_INVALID_ARG;
   if (out_stride < (int64_t)kb * 8) return DSA_ERR_INVALID_ARG;
   if (B == 0) return DSA_OK;
   LogitsCall c{};
@@ -278,7 +279,7 @@ int32_t dsa_sparse_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const f
   c.amax_stride = 0;
   c.amax_skip = 0;
   c.sparse = true;
-  c.out_f16 = (out_dtype == DSA_OUT_F16);
+  c.out_fmt = out_dtype;
   c.block_table = block_table;
   c.kb = kb;
   c.phys = phys_blocks;
@@ -457,6 +458,30 @@ int32_t dsa_topk_fp16(const uint16_t *scores, int64_t stride, const int32_t *val
   return run_topk_fp16(c, static_cast<cudaStream_t>(stream));
 }
 
+int32_t dsa_topk_bf16(const uint16_t *scores, int64_t stride, const int32_t *valid_lens,
+                      int32_t R, int32_t k, const int32_t *block_table, int32_t kb,
+                      int32_t *out_idx, void *workspace, size_t ws_bytes, void *stream) {
+  if (R < 0 || stride < 2) return DSA_ERR_INVALID_ARG;
+  if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (!scores || !valid_lens || !out_idx) return DSA_ERR_INVALID_ARG;
+  if (stride % 2 != 0 || !aligned(scores, 4)) return DSA_ERR_MISALIGNED;
+  if (block_table && kb < 1) return DSA_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < WsLayout::kHeader) return DSA_ERR_WORKSPACE;
+  if (R == 0) return DSA_OK;
+  Fp16TopkCall c{};
+  c.scores = scores;
+  c.stride = stride;
+  c.valid_lens = valid_lens;
+  c.R = R;
+  c.k = k;
+  c.block_table = block_table;
+  c.kb = kb;
+  c.out_idx = out_idx;
+  c.status = status_word(workspace);
+  c.bf16 = true;
+  return run_topk_fp16(c, static_cast<cudaStream_t>(stream));
+}
+
 int32_t dsa_coarse_bin_key_ranges(uint32_t *out, void *stream) {
   if (!out) return DSA_ERR_INVALID_ARG;
   return run_bin_key_ranges(out, static_cast<cudaStream_t>(stream));
@@ -472,6 +497,13 @@ int32_t dsa_fp16_order_keys(const uint16_t *in, uint16_t *out, int64_t n, void *
   if (n > 0 && (!in || !out)) return DSA_ERR_INVALID_ARG;
   if (!aligned(in, 4) || !aligned(out, 4)) return DSA_ERR_MISALIGNED;
   return run_fp16_keys(in, out, n, static_cast<cudaStream_t>(stream));
+}
+
+int32_t dsa_bf16_order_keys(const uint16_t *in, uint16_t *out, int64_t n, void *stream) {
+  if (n < 0 || n % 2 != 0) return DSA_ERR_INVALID_ARG;
+  if (n > 0 && (!in || !out)) return DSA_ERR_INVALID_ARG;
+  if (!aligned(in, 4) || !aligned(out, 4)) return DSA_ERR_MISALIGNED;
+  return run_bf16_keys(in, out, n, static_cast<cudaStream_t>(stream));
 }
 
 int32_t dsa_wait_timeout_selftest(uint64_t limit_cycles, void *workspace, size_t ws_bytes,

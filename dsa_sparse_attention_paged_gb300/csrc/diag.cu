@@ -23,6 +23,12 @@ __global__ void fp16_keys_kernel(const uint32_t *in, uint32_t *out, int64_t nw) 
     out[i] = f16x2_order_keys(in[i]);
 }
 
+__global__ void bf16_keys_kernel(const uint32_t *in, uint32_t *out, int64_t nw) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nw;
+       i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = bf16x2_order_keys(in[i]);
+}
+
 // One thread waits on a barrier that expects one arrival nobody makes.
 __global__ void wait_selftest_kernel(long long limit, uint32_t *status) {
   __shared__ __align__(8) uint64_t bar;
@@ -54,6 +60,15 @@ dsa_status_t run_fp16_keys(const uint16_t *in, uint16_t *out, int64_t n, cudaStr
   const int sms = num_sms();
   if (sms <= 0) return DSA_ERR_CUDA;
   fp16_keys_kernel<<<sms * 4, 256, 0, st>>>(reinterpret_cast<const uint32_t *>(in),
+                                             reinterpret_cast<uint32_t *>(out), n / 2);
+  return check_launch();
+}
+
+dsa_status_t run_bf16_keys(const uint16_t *in, uint16_t *out, int64_t n, cudaStream_t st) {
+  if (n <= 0) return DSA_OK;
+  const int sms = num_sms();
+  if (sms <= 0) return DSA_ERR_CUDA;
+  bf16_keys_kernel<<<sms * 4, 256, 0, st>>>(reinterpret_cast<const uint32_t *>(in),
                                              reinterpret_cast<uint32_t *>(out), n / 2);
   return check_launch();
 }

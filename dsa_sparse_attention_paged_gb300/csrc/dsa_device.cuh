@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -361,13 +362,23 @@ __device__ __forceinline__ uint32_t f32_order_key(float x) {
 // "Why": both packed halves are transformed with one 32-bit operation).  A
 // set sign bit flips all 16 bits, a clear one flips only the sign bit.  NaN
 // halves become key 0, below every non-NaN key (-inf has key 0x03FF).
-__device__ __forceinline__ uint32_t f16x2_order_keys(uint32_t w) {
+template <uint32_t kNanAdd>
+__device__ __forceinline__ uint32_t x16x2_order_keys(uint32_t w) {
   const uint32_t sign = (w >> 15) & 0x00010001u;
   uint32_t k = w ^ ((sign * 0x7FFFu) | 0x80008000u);
-  // |h| > 0x7C00 (NaN) iff (h & 0x7FFF) + 0x03FF carries into bit 15
-  const uint32_t nan_bits = ((w & 0x7FFF7FFFu) + 0x03FF03FFu) & 0x80008000u;
+  // NaN (magnitude above the infinity pattern) iff (h & 0x7FFF) + kNanAdd
+  // carries into bit 15: kNanAdd = 0x03FF for FP16 (inf 0x7C00), 0x007F for
+  // BF16 (inf 0x7F80)
+  const uint32_t nan_bits = ((w & 0x7FFF7FFFu) + (kNanAdd * 0x00010001u)) & 0x80008000u;
   const uint32_t nan_mask = (nan_bits >> 15) * 0xFFFFu;
   return k & ~nan_mask;
+}
+__device__ __forceinline__ uint32_t f16x2_order_keys(uint32_t w) {
+  return x16x2_order_keys<0x03FFu>(w);
+}
+// The same for two BF16 halves (the same sign-magnitude order).
+__device__ __forceinline__ uint32_t bf16x2_order_keys(uint32_t w) {
+  return x16x2_order_keys<0x007Fu>(w);
 }
 
 }  // namespace dsa

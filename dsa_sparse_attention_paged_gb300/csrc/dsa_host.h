@@ -32,7 +32,7 @@ struct LogitsCall {
   int64_t amax_stride;
   int32_t amax_skip;
   bool sparse;
-  bool out_f16;
+  int32_t out_fmt;      // DSA_OUT_F32 / F16 / BF16 (sparse only)
   const int32_t *block_table;
   int32_t kb;
   const int32_t *phys = nullptr;        // sparse: physical blocks of the table, or NULL
@@ -78,6 +78,7 @@ struct Fp16TopkCall {
   int32_t kb;
   int32_t *out_idx;
   uint32_t *status;
+  bool bf16 = false;  // BF16 scores instead of FP16
 };
 dsa_status_t run_topk_fp16(const Fp16TopkCall &c, cudaStream_t st);
 
@@ -91,6 +92,7 @@ dsa_status_t run_sort_blocks(int32_t *ids, int32_t kb, const int32_t *context_le
                              int32_t *valid_lens, uint32_t *status, cudaStream_t st);
 
 dsa_status_t run_bins_range(uint32_t start, int64_t count, int16_t *out, cudaStream_t st);
+dsa_status_t run_bf16_keys(const uint16_t *in, uint16_t *out, int64_t n, cudaStream_t st);
 dsa_status_t run_bin_key_ranges(uint32_t *out, cudaStream_t st);
 dsa_status_t run_fp16_keys(const uint16_t *in, uint16_t *out, int64_t n, cudaStream_t st);
 dsa_status_t run_wait_selftest(uint64_t limit, uint32_t *status, cudaStream_t st);

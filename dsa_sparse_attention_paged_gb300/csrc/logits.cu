@@ -295,7 +295,7 @@ __device__ __forceinline__ float head_sum(const uint32_t (&v)[32], float ks, con
   return (c0 + c1) + (c2 + c3);
 }
 
-template <int NN, bool SPARSE, bool OUT_F16, bool HIST>
+template <int NN, bool SPARSE, int OUT, bool HIST>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const LogitsArgs a) {
@@ -722,8 +722,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t t = (int64_t)blk * 8 + (pos & 7);
           const bool live = a.valid_lens ? pos < n_row : (blk != INT32_MAX && blk >= 0 && t < n_row);
           const float val = live ? acc[0] : -INFINITY;
-          if (OUT_F16) {
+          if (OUT == DSA_OUT_F16) {
             reinterpret_cast<__half *>(a.out)[(int64_t)u * a.out_stride + pos] = __float2half_rn(val);
+          } else if (OUT == DSA_OUT_BF16) {
+            reinterpret_cast<__nv_bfloat16 *>(a.out)[(int64_t)u * a.out_stride + pos] =
+                __float2bfloat16_rn(val);
           } else {
             reinterpret_cast<float *>(a.out)[(int64_t)u * a.out_stride + pos] = val;
           }
@@ -808,7 +811,7 @@ inline LaunchPlan plan_for(int nn, bool hist, bool sparse) {
   return L;
 }
 
-template <int NN, bool SPARSE, bool OUT_F16, bool HIST>
+template <int NN, bool SPARSE, int OUT, bool HIST>
 dsa_status_t launch_one(const CUtensorMap &tk, const CUtensorMap &tq, const LogitsArgs &a0,
                         int grid, cudaStream_t st) {
   LogitsArgs a = a0;
@@ -817,7 +820,7 @@ dsa_status_t launch_one(const CUtensorMap &tk, const CUtensorMap &tq, const Logi
   a.num_ks = L.nks;
   a.tmem_cols = (uint32_t)L.cols;
   a.num_stages = L.stages;
-  auto kfn = logits_kernel<NN, SPARSE, OUT_F16, HIST>;
+  auto kfn = logits_kernel<NN, SPARSE, OUT, HIST>;
   if (!ensure_smem_attr(reinterpret_cast<const void *>(kfn), L.smem)) return DSA_ERR_CUDA;
   return launch_pdl(kfn, dim3(grid), dim3(kThreads), (size_t)L.smem, st, tk, tq, a);
 }
@@ -864,8 +867,10 @@ dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
     a.sparse_tpu = (c.kb + 31) / 32;
     const long long tiles = (long long)a.num_units * a.sparse_tpu;
     const int grid = (int)std::max<long long>(1, std::min<long long>(sms, tiles));
-    if (c.out_f16) return launch_one<1, true, true, false>(tk, tq, a, grid, st);
-    return launch_one<1, true, false, false>(tk, tq, a, grid, st);
+    if (c.out_fmt == DSA_OUT_F16) return launch_one<1, true, DSA_OUT_F16, false>(tk, tq, a, grid, st);
+    if (c.out_fmt == DSA_OUT_BF16)
+      return launch_one<1, true, DSA_OUT_BF16, false>(tk, tq, a, grid, st);
+    return launch_one<1, true, DSA_OUT_F32, false>(tk, tq, a, grid, st);
   }
   a.num_units = c.B;
   a.sparse_tpu = 0;
@@ -873,17 +878,17 @@ dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   const bool h = c.histogram != nullptr;
   switch (c.next_n) {
     case 1:
-      return h ? launch_one<1, false, false, true>(tk, tq, a, grid, st)
-               : launch_one<1, false, false, false>(tk, tq, a, grid, st);
+      return h ? launch_one<1, false, DSA_OUT_F32, true>(tk, tq, a, grid, st)
+               : launch_one<1, false, DSA_OUT_F32, false>(tk, tq, a, grid, st);
     case 2:
-      return h ? launch_one<2, false, false, true>(tk, tq, a, grid, st)
-               : launch_one<2, false, false, false>(tk, tq, a, grid, st);
+      return h ? launch_one<2, false, DSA_OUT_F32, true>(tk, tq, a, grid, st)
+               : launch_one<2, false, DSA_OUT_F32, false>(tk, tq, a, grid, st);
     case 3:
-      return h ? launch_one<3, false, false, true>(tk, tq, a, grid, st)
-               : launch_one<3, false, false, false>(tk, tq, a, grid, st);
+      return h ? launch_one<3, false, DSA_OUT_F32, true>(tk, tq, a, grid, st)
+               : launch_one<3, false, DSA_OUT_F32, false>(tk, tq, a, grid, st);
     case 4:
-      return h ? launch_one<4, false, false, true>(tk, tq, a, grid, st)
-               : launch_one<4, false, false, false>(tk, tq, a, grid, st);
+      return h ? launch_one<4, false, DSA_OUT_F32, true>(tk, tq, a, grid, st)
+               : launch_one<4, false, DSA_OUT_F32, false>(tk, tq, a, grid, st);
     default:
       return DSA_ERR_UNSUPPORTED;
   }

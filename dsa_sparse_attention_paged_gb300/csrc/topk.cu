@@ -1581,6 +1581,7 @@ __global__ void __launch_bounds__(kRowThreads)
 // ---------------------------------------------------------------- FP16 select
 constexpr int kF16MaxRow = 16384;
 
+template <bool BF16>
 __global__ void __launch_bounds__(kSelThreads)
     topk_fp16_kernel(const uint16_t *scores, int64_t stride, const int32_t *valid_lens, int k,
                      const int32_t *table, int kb, int32_t *out, uint32_t *status) {
@@ -1616,7 +1617,7 @@ __global__ void __launch_bounds__(kSelThreads)
 #pragma unroll
     for (int e = 0; e < WR; ++e) {
       const int w = (rd * WR + e) * kSelThreads + threadIdx.x;
-      uint32_t kk = (w < nw) ? f16x2_order_keys(wv[e]) : 0u;
+      uint32_t kk = (w < nw) ? (BF16 ? bf16x2_order_keys(wv[e]) : f16x2_order_keys(wv[e])) : 0u;
       if (2 * w + 1 >= n) kk &= 0x0000FFFFu;
       keys2[w] = kk;
       const uint32_t lo = kk & 0xFFFFu, hi = kk >> 16;
@@ -1908,7 +1909,8 @@ dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
 }
 
 dsa_status_t run_topk_fp16(const Fp16TopkCall &c, cudaStream_t st) {
-  return launch_pdl(topk_fp16_kernel, dim3(c.R), dim3(kSelThreads), 0, st, c.scores, c.stride,
+  return launch_pdl(c.bf16 ? topk_fp16_kernel<true> : topk_fp16_kernel<false>, dim3(c.R),
+                    dim3(kSelThreads), 0, st, c.scores, c.stride,
                     c.valid_lens, c.k, c.block_table, c.kb, c.out_idx, c.status);
 }
 

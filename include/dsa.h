@@ -75,6 +75,7 @@ typedef enum {
                                  SGLang commit 7e252c5)                        */
 #define DSA_OUT_F32 0
 #define DSA_OUT_F16 1
+#define DSA_OUT_BF16 2
 
 /* Human-readable name of a dsa_status_t (static storage). */
 const char *dsa_status_string(int32_t status);
@@ -307,7 +308,9 @@ int32_t dsa_sort_candidate_blocks(int32_t *block_ids, int32_t kb, const int32_t 
  * dsa_paged_mqa_logits; kb % 16 == 0.
  *   out        [R][out_stride] float (DSA_OUT_F32) or FP16 bits (DSA_OUT_F16,
  *              round-to-nearest-even of the float logit, [VL52696] "Why":
- *              the logits kernel writes FP16 directly), out_stride >= kb*8
+ *              the logits kernel writes FP16 directly) or BF16 bits
+ *              (DSA_OUT_BF16, round-to-nearest-even, the BF16 sibling),
+ *              out_stride >= kb*8
  *   phys_blocks, valid_lens  both NULL, or both the outputs of
  *              dsa_sort_candidate_blocks for this table: the K rows are then
  *              read straight from the physical blocks (no page-table read
@@ -338,13 +341,22 @@ int32_t dsa_topk_fp16(const uint16_t *scores, int64_t stride, const int32_t *val
                       int32_t R, int32_t k, const int32_t *block_table, int32_t kb,
                       int32_t *out_idx, void *workspace, size_t ws_bytes, void *stream);
 
+/* The same select over BF16 scores (the BF16 sibling of the FP16 packed
+ * select; [SG38944]'s topk_bf16_small with its fused page-table transform):
+ * NaN (BF16 exponent field all ones, mantissa not 0) never selected, order by
+ * the BF16 value, ties to the lower position; arguments as dsa_topk_fp16. */
+int32_t dsa_topk_bf16(const uint16_t *scores, int64_t stride, const int32_t *valid_lens,
+                      int32_t R, int32_t k, const int32_t *block_table, int32_t kb,
+                      int32_t *out_idx, void *workspace, size_t ws_bytes, void *stream);
+
 /* ---- diagnostics (same device functions as the kernels above) ------------
  * dsa_coarse_bins_range: out[i] = coarse bin of the float whose bit pattern is
  *   start + i (-1 for NaN), for i < count; out is int16 on the device.  Used
  *   to sweep all 2^32 patterns against an independent reference.
  * dsa_fp16_order_keys: out[i] = 16-bit order key of the FP16 pattern in[i]
  *   computed two halves per 32-bit word, as the FP16 select does (NaN -> 0);
- *   n even, both arrays device-resident.
+ *   n even, both arrays device-resident.  dsa_bf16_order_keys: the same for
+ *   BF16 patterns, as the BF16 select does.
  * dsa_wait_timeout_selftest: launches a kernel whose only wait is on a
  *   barrier nothing arrives on, bounded by `limit_cycles`; the kernel records
  *   DSA_DEV_TIMEOUT in the workspace status word and returns.
@@ -355,6 +367,7 @@ int32_t dsa_topk_fp16(const uint16_t *scores, int64_t stride, const int32_t *val
 int32_t dsa_coarse_bins_range(uint32_t start, int64_t count, int16_t *out, void *stream);
 int32_t dsa_coarse_bin_key_ranges(uint32_t *out, void *stream);
 int32_t dsa_fp16_order_keys(const uint16_t *in, uint16_t *out, int64_t n, void *stream);
+int32_t dsa_bf16_order_keys(const uint16_t *in, uint16_t *out, int64_t n, void *stream);
 int32_t dsa_wait_timeout_selftest(uint64_t limit_cycles, void *workspace, size_t ws_bytes,
                                   void *stream);
 

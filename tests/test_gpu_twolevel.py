@@ -106,6 +106,17 @@ def test_two_level_chain(ctx, kb, ps, nn):
     ref_top = O.topk_fp16(sp16.cpu().numpy().view(np.uint16), v_ref, k, t_ref)
     assert sets_equal(top.cpu().numpy(), ref_top)
 
+    # the BF16 sibling: RN-even of the FP32 scores, and its select
+    spb = D.sparse_mqa_logits(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"],
+                              d["context_lens"], nn, ids, ws, out_dtype=D.OUT_BF16,
+                              phys_blocks=phys, valid_lens=vl)
+    torch.cuda.synchronize()
+    SB = spb.view(torch.int16).cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(SB, O.bf16_rn_array(SP))
+    topb = D.topk_bf16(spb, vl, k, ws, block_table=ids)
+    torch.cuda.synchronize()
+    assert sets_equal(topb.cpu().numpy(), O.topk_bf16(SB, v_ref, k, t_ref))
+
 
 def test_fp16_topk_ties_nan_and_positions():
     import dsa_sparse_attention_paged_gb300 as D
@@ -142,3 +153,41 @@ def test_fp16_order_keys_all_65536_encodings():
     # +0 above -0
     assert keys[0x0000] > keys[0x8000]
     assert (kk > 0).all()
+
+
+def test_bf16_topk_ties_nan_and_positions():
+    import dsa_sparse_attention_paged_gb300 as D
+    rng = np.random.default_rng(4)
+    R, n = 4, 6000
+    vals = torch.from_numpy(rng.normal(0, 4, (R, n)).astype(np.float32))
+    vals[0, :] = 1.0                       # all ties
+    vals[1, ::3] = float("nan")
+    vals[2, :50] = float("inf")
+    vals[2, 50:60] = -float("inf")
+    vals[3, 100:200] = -0.0
+    bits = vals.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+    bits[1, 1::7] = 0x7F81                 # a NaN pattern that is no NaN in FP16
+    s = torch.from_numpy(bits).cuda()
+    ws = D.Workspace(R)
+    for vl_list, k in (([n, n, n, n], 2048), ([5999, 17, 2048, 1], 2048), ([n, 4001, 3, 0], 1)):
+        vl = torch.tensor(vl_list, dtype=torch.int32, device="cuda")
+        out = D.topk_bf16(s, vl, k, ws)
+        torch.cuda.synchronize()
+        ref = O.topk_bf16(bits, np.array(vl_list, np.int32), k)
+        assert sets_equal(out.cpu().numpy(), ref), (vl_list, k)
+
+
+def test_bf16_order_keys_all_65536_encodings():
+    import dsa_sparse_attention_paged_gb300 as D
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    keys = D.bf16_order_keys(torch.from_numpy(codes.copy()).cuda()).cpu().numpy()
+    vals = np.array([O.bf16_bits_to_double(int(c)) for c in codes])
+    nan = np.isnan(vals)
+    assert (keys[nan] == 0).all()
+    kk = keys[~nan].astype(np.int64)
+    v = vals[~nan]
+    assert len(np.unique(kk)) == kk.size  # one key per encoding
+    order = np.argsort(kk)
+    assert np.all(np.diff(v[order]) >= 0)  # keys ascend with the value
+    assert kk[np.nonzero(codes[~nan] == 0x8000)[0][0]] < kk[np.nonzero(codes[~nan] == 0)[0][0]]
+
