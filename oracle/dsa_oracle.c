@@ -42,9 +42,10 @@
  *       length of a sparse row counts the live tokens of the chosen blocks.
  *   R9  Sparse positions that are padding or past the row's live length are
  *       -inf in the output.
- *   R10 The BF16 sibling of the FP16 select (the next step the pages point
+ *   R14 The BF16 sibling of the FP16 select (the next step the pages point
  *       to, [VL52696] "Why" for FP16): bfloat16 rounding is round-to-nearest-
  *       even, NaN never selected, the same order and tie rule as FP16.
+ *   (R10-R13 concern the CUDA path's contracts, not this file's arithmetic.)
  */
 #include <math.h>
 #include <stdint.h>
