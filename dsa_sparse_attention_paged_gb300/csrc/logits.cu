@@ -20,7 +20,8 @@
 //   warp 1      allocates TMEM and issues tcgen05.mma (one thread): per stage
 //               two sub-tiles D[128 tokens x 32*next_n] = K[128 x 128] .
 //               Q[32*next_n x 128]^T, FP8 x FP8 -> FP32, into a TMEM pair
-//   warps 2..9  epilogue, two warpgroups, one per 128-token sub-tile: each
+//   warps 2..   epilogue, one warpgroup per 128-token sub-tile (two per
+//               sub-tile at next_n > 1, taking alternate stages): each
 //               thread owns one TMEM lane = one token, loads its 32 head dots
 //               per row, applies kscale, ReLU and the head weights in
 //               registers, stores the logit (coalesced across the warp) and
@@ -46,8 +47,13 @@ constexpr int kStageK = kStageTok * 128;     // bytes of K per stage
 constexpr int kSubK = kSubTok * 128;
 constexpr int kStageKs = kStageTok * 4;      // bytes of kscale per stage
 constexpr int kMaxStages = 8;
-constexpr int kThreads = 320;                // producer, MMA, 2 x 4 epilogue warps
-constexpr int kEpiWarps = 8;
+// Epilogue warps: two warpgroups (one per 128-token sub-tile) at next_n = 1;
+// four at next_n > 1, where the epilogue carries next_n rows per token: the
+// two groups of a sub-tile take alternate stages.  Eight warps consume each
+// stage either way.
+__host__ __device__ constexpr int epi_warps(int nn) { return nn == 1 ? 8 : 16; }
+__host__ __device__ constexpr int threads_for(int nn) { return 64 + 32 * epi_warps(nn); }
+constexpr int kStageEpiWarps = 8;
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in per CTA
 
 struct LogitsArgs {
@@ -296,7 +302,7 @@ __device__ __forceinline__ float head_sum(const uint32_t (&v)[32], float ks, con
 }
 
 template <int NN, bool SPARSE, int OUT, bool HIST>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(NN), 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const LogitsArgs a) {
   // the dense pass waits for its predecessors at once; the sparse pass sets up
@@ -305,6 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int N = 32 * NN;
   constexpr uint32_t IDESC = idesc_e4m3_f32(128, N);
   constexpr int HS = hist_slots_per_group(NN);
+  constexpr int EW = epi_warps(NN);
+  constexpr int NPAR = EW / kStageEpiWarps;  // groups sharing a sub-tile (alternate stages)
+  constexpr int kThr = threads_for(NN);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -346,25 +355,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int k = 0; k < KS; ++k) {
       mbar_init(KSF(k), 1);
-      mbar_init(KSE(k), kEpiWarps);
+      mbar_init(KSE(k), kStageEpiWarps);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(QFULL(q), 1);
-      mbar_init(QEMPTY(q), 1 + kEpiWarps);
+      mbar_init(QEMPTY(q), 1 + EW);
     }
     for (int x = 0; x < A; ++x) {
       mbar_init(AFULL(x), 1);
-      mbar_init(AEMPTY(x), kEpiWarps);
+      mbar_init(AEMPTY(x), kStageEpiWarps);
     }
     mbar_init(DRAIN, 1);
-    mbar_init(GSYNC(0), 4);
-    mbar_init(GSYNC(1), 4);
+    mbar_init(GSYNC(0), 4 * NPAR);
+    mbar_init(GSYNC(1), 4 * NPAR);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) compute_sched<SPARSE>(a, &sched[0], &sched[1], sched_cnt);
   if (HIST) {
-    for (int i = threadIdx.x; i < 2 * HS * NN * DSA_NUM_BINS; i += kThreads) hist_s[i] = 0;
+    for (int i = threadIdx.x; i < 2 * HS * NN * DSA_NUM_BINS; i += kThr) hist_s[i] = 0;
   }
   __syncthreads();
   const long long count = *sched_cnt;
@@ -603,13 +612,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    // warpgroup g takes sub-tile g of every stage; warp w reads TMEM lanes
-    // 32*(w%4) .. +31, i.e. one token per thread
-    const int g = (warp - 2) >> 2;
+    // warpgroup gi takes sub-tile g = gi % 2 of the stages of parity gi / 2
+    // (every stage at next_n = 1); warp w reads TMEM lanes 32*(w%4) .. +31,
+    // i.e. one token per thread.  Every warp walks every stage for the
+    // bookkeeping (unit changes, histogram flushes, Q release).
+    const int gi = (warp - 2) >> 2;
+    const int g = gi & 1;        // sub-tile
+    const int par = gi >> 1;     // stage parity (0 when NPAR == 1)
     const int quarter = warp & 3;
     const int lane_base = 32 * quarter;
     const int tok = g * kSubTok + lane_base + lane;   // token within the stage
-    const int gtid = ((warp - 2) & 3) * 32 + lane;    // 0..127 within the group
+    const int gtid = par * 128 + ((warp - 2) & 3) * 32 + lane;  // within the sub-tile's warps
     const uint64_t out_pol = policy_evict_last();
     int *grp_hist = hist_s + g * HS * NN * DSA_NUM_BINS;
     int *my_hist = grp_hist + (HS == 4 ? quarter : 0) * NN * DSA_NUM_BINS;
@@ -637,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto flush = [&](int rb) -> bool {
       if (!group_sync()) return false;
       for (int j = 0; j < NN; ++j) {
-        for (int p = gtid; p < DSA_NUM_BINS / 2; p += 128) {
+        for (int p = gtid; p < DSA_NUM_BINS / 2; p += 128 * NPAR) {
           uint32_t c0 = 0, c1 = 0;
 #pragma unroll
           for (int w = 0; w < HS; ++w) {
@@ -682,6 +695,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!(ok = ewait(QFULL(qb), (unit_ord >> 1) & 1))) break;
       }
+      const bool mine = NPAR == 1 || ((int)(n & 1) == par);
+      if (mine) {
       const int x = ra.idx;
       const int kx = rk.idx;
       const int64_t pos = (int64_t)i * kStageTok + tok;
@@ -694,14 +709,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(KSE(kx));
       if (!(ok = ewait(AFULL(x), ra.ph))) break;
       tc_fence_after();
-      // head dots leave TMEM in batches of up to two rows (one wait per
-      // batch, bounded register use); the accumulator goes back to the MMA
-      // as soon as the last batch is in registers
+      // head dots leave TMEM in batches of up to two rows, one row with 16
+      // epilogue warps (one wait per batch; 576 threads leave 96 registers
+      // a thread); the accumulator goes back to the MMA as soon as the last
+      // batch is in registers
       float acc[NN];
       const uint32_t tcol = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)((2 * x + g) * N);
+      constexpr int kB = NN == 1 ? 1 : (EW == 8 ? 2 : 1);
 #pragma unroll
-      for (int j0 = 0; j0 < NN; j0 += 2) {
-        constexpr int kB = 2;
+      for (int j0 = 0; j0 < NN; j0 += kB) {
         uint32_t v[kB][32];
 #pragma unroll
         for (int jj = 0; jj < kB; ++jj)
@@ -774,6 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      }  // mine
       if (i == it.tiles - 1 || n == count - 1) {
         __syncwarp();
         if (lane == 0) mbar_arrive(QEMPTY(qb));
@@ -822,7 +839,7 @@ dsa_status_t launch_one(const CUtensorMap &tk, const CUtensorMap &tq, const Logi
   a.num_stages = L.stages;
   auto kfn = logits_kernel<NN, SPARSE, OUT, HIST>;
   if (!ensure_smem_attr(reinterpret_cast<const void *>(kfn), L.smem)) return DSA_ERR_CUDA;
-  return launch_pdl(kfn, dim3(grid), dim3(kThreads), (size_t)L.smem, st, tk, tq, a);
+  return launch_pdl(kfn, dim3(grid), dim3(threads_for(NN)), (size_t)L.smem, st, tk, tq, a);
 }
 
 }  // namespace
