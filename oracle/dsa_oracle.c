@@ -45,6 +45,9 @@
  *   R14 The BF16 sibling of the FP16 select (the next step the pages point
  *       to, [VL52696] "Why" for FP16): bfloat16 rounding is round-to-nearest-
  *       even, NaN never selected, the same order and tie rule as FP16.
+ *   R15 Row pairing of the sparse pass: rows 2m and 2m+1 of a request form
+ *       one unit (an odd last row is alone) whose pass walks the ascending
+ *       union of the two tables; each row's scores keep its own positions.
  *   (R10-R13 concern the CUDA path's contracts, not this file's arithmetic.)
  */
 #include <math.h>
@@ -432,6 +435,59 @@ void o_sparse_logits(const uint8_t *q, const uint8_t *kv, const float *kscale,
                                        (double)kscale[slot], weights + (int64_t)r * H, H, D, tab);
             }
             out[(int64_t)r * out_stride + i] = v;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* O9: row pairing of the sparse pass ([SG38944] commit text on DeepGEMM's
+ * sparse schedule: two consecutive rows of one request share one KV pass,
+ * each keeping its own block list and output layout, on a shared page-table
+ * row).  Reading R15: within a request, rows 2m and 2m+1 form a unit and an
+ * odd last row is a unit of its own; a unit's pass walks the ascending union
+ * of its rows' tables.  Union entry e holds the physical block and, for each
+ * row, its position in that row's table plus one (0: the row does not hold
+ * the block).  The union is a plain two-pointer merge of the two ascending
+ * tables (INT32_MAX ends a table).  Units: B * ceil(next_n / 2); each output
+ * row has 2*kb slots, padded with INT32_MAX (phys) and 0 (positions).        */
+void o_pair_union(const int32_t *table, const int32_t *phys, int R, int next_n, int kb,
+                  int32_t *uphys, int32_t *upos, int32_t *ulen)
+{
+    int upr = (next_n + 1) / 2;
+    int U = (R / next_n) * upr;
+    for (int u = 0; u < U; ++u) {
+        int b = u / upr, m = u % upr;
+        int ra = b * next_n + 2 * m;
+        int rb = (2 * m + 1 < next_n) ? ra + 1 : -1;
+        const int32_t *ta = table + (int64_t)ra * kb, *pa = phys + (int64_t)ra * kb;
+        const int32_t *tb = rb >= 0 ? table + (int64_t)rb * kb : NULL;
+        const int32_t *pb = rb >= 0 ? phys + (int64_t)rb * kb : NULL;
+        int na = 0, nb = 0;
+        while (na < kb && ta[na] != O_INT32_MAX) ++na;
+        while (tb && nb < kb && tb[nb] != O_INT32_MAX) ++nb;
+        int i = 0, j = 0, e = 0;
+        int32_t *up = uphys + (int64_t)u * 2 * kb, *uq = upos + (int64_t)u * 2 * kb;
+        while (i < na || j < nb) {
+            if (j >= nb || (i < na && ta[i] < tb[j])) {
+                up[e] = pa[i];
+                uq[e] = i + 1;
+                ++i;
+            } else if (i >= na || tb[j] < ta[i]) {
+                up[e] = pb[j];
+                uq[e] = (j + 1) << 16;
+                ++j;
+            } else {
+                up[e] = pa[i];
+                uq[e] = (i + 1) | ((j + 1) << 16);
+                ++i;
+                ++j;
+            }
+            ++e;
+        }
+        ulen[u] = e;
+        for (; e < 2 * kb; ++e) {
+            up[e] = O_INT32_MAX;
+            uq[e] = 0;
         }
     }
 }

@@ -79,6 +79,7 @@ def _load():
     lib.o_bf16_rn_array.argtypes = [P, i64, P]
     lib.o_bf16_rn_sweep.argtypes = [ctypes.c_uint64, ctypes.c_uint64, P]
     lib.o_topk_bf16.argtypes = [P, i64, P, i32, i64, P, i32, P]
+    lib.o_pair_union.argtypes = [P, P, i32, i32, i32, P, P, P]
     _lib = lib
     return lib
 
@@ -274,6 +275,20 @@ def sparse_logits(q, kv, kscale, weights, page_table, row_lens_, row_to_req, pag
                             page_table.shape[1], _ptr(rl), _ptr(rtr), R, H, D, page_size,
                             _ptr(table), kb, _ptr(out), out.shape[1])
     return out
+
+
+def pair_union(table, phys, next_n):
+    """Row pairing of the sparse pass: (union_phys [U][2kb], union_pos
+    [U][2kb], union_len [U]) for U = requests * ceil(next_n / 2) units."""
+    table = _c(table, np.int32)
+    phys = _c(phys, np.int32)
+    R, kb = table.shape
+    U = (R // next_n) * ((next_n + 1) // 2)
+    up = np.empty((U, 2 * kb), np.int32)
+    uq = np.empty((U, 2 * kb), np.int32)
+    ul = np.empty(U, np.int32)
+    _load().o_pair_union(_ptr(table), _ptr(phys), R, next_n, kb, _ptr(up), _ptr(uq), _ptr(ul))
+    return up, uq, ul
 
 
 def topk_fp16(scores_u16, valid_len, k, table=None) -> np.ndarray:

@@ -514,3 +514,78 @@ def test_fp16_topk_ties_to_lower_position_and_table_mapping():
     assert out.tolist() == [table[0, p // 8] * 8 + p % 8 for p in pos]
     out = O.topk_fp16(s, np.array([3], np.int32), 5)[0]
     assert out.tolist() == [0, 1, 2, -1, -1]
+
+
+IMAX = 2**31 - 1
+
+
+def _pad(ids, kb):
+    return list(ids) + [IMAX] * (kb - len(ids))
+
+
+def test_pair_union_worked_example():
+    """Two rows of one request, tables [1 4 7] and [2 4 9 11] (kb = 4): the
+    union is [1 2 4 7 9 11]; block 4 is held by both rows (A at 1, B at 1)."""
+    kb = 4
+    table = np.array([_pad([1, 4, 7], kb), _pad([2, 4, 9, 11], kb)], np.int32)
+    phys = np.where(table == IMAX, IMAX, table + 100).astype(np.int32)
+    up, uq, ul = O.pair_union(table, phys, 2)
+    assert ul.tolist() == [6]
+    assert up[0, :6].tolist() == [101, 102, 104, 107, 109, 111]
+    pos_a = (uq[0, :6] & 0xFFFF) - 1
+    pos_b = (uq[0, :6] >> 16) - 1
+    assert pos_a.tolist() == [0, -1, 1, 2, -1, -1]
+    assert pos_b.tolist() == [-1, 0, 1, -1, 2, 3]
+    assert (up[0, 6:] == IMAX).all() and (uq[0, 6:] == 0).all()
+
+
+@pytest.mark.parametrize("next_n", [1, 2, 3, 4, 5])
+def test_pair_union_brute_force_by_sets(next_n):
+    """Against Python sets on random tiny tables: units are rows (2m, 2m+1) of
+    a request, an odd last row alone; every union entry is a block of one of
+    the two rows, in ascending order, with each row's own table position."""
+    rng = np.random.default_rng(7 + next_n)
+    B, kb = 3, 6
+    R = B * next_n
+    table = np.full((R, kb), IMAX, np.int32)
+    for r in range(R):
+        n = int(rng.integers(0, kb + 1))
+        table[r, :n] = np.sort(rng.choice(14, size=n, replace=False))
+    phys = np.where(table == IMAX, IMAX, 1000 + 3 * table + (np.arange(R)[:, None] // next_n))
+    phys = phys.astype(np.int32)
+    up, uq, ul = O.pair_union(table, phys, next_n)
+    upr = (next_n + 1) // 2
+    assert up.shape == (B * upr, 2 * kb)
+    for u in range(B * upr):
+        b, m = divmod(u, upr)
+        ra = b * next_n + 2 * m
+        rows = [ra] + ([ra + 1] if 2 * m + 1 < next_n else [])
+        lists = [[int(x) for x in table[r] if x != IMAX] for r in rows]
+        want = sorted(set().union(*map(set, lists)))
+        assert ul[u] == len(want)
+        for e, blk in enumerate(want):
+            assert up[u, e] == 1000 + 3 * blk + b
+            for j, lst in enumerate(lists):
+                got = int((uq[u, e] >> (16 * j)) & 0xFFFF) - 1
+                assert got == (lst.index(blk) if blk in lst else -1)
+            if len(rows) == 1:
+                assert uq[u, e] >> 16 == 0
+        assert (up[u, len(want):] == IMAX).all() and (uq[u, len(want):] == 0).all()
+
+
+def test_pair_union_covers_each_row_position_once():
+    """Invariant: over a unit's union, each row's positions 0..n-1 appear
+    exactly once (the pass writes every live slot of both rows once)."""
+    rng = np.random.default_rng(11)
+    kb, R = 64, 8
+    table = np.full((R, kb), IMAX, np.int32)
+    for r in range(R):
+        n = int(rng.integers(kb // 2, kb + 1))
+        table[r, :n] = np.sort(rng.choice(200, size=n, replace=False))
+    up, uq, ul = O.pair_union(table, table, 4)
+    for u in range(len(ul)):
+        for j in range(2):
+            r = (u // 2) * 4 + 2 * (u % 2) + j
+            n = int((table[r] != IMAX).sum())
+            pos = ((uq[u, :ul[u]] >> (16 * j)) & 0xFFFF).astype(np.int64) - 1
+            assert sorted(pos[pos >= 0].tolist()) == list(range(n))
