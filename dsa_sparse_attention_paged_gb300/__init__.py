@@ -82,6 +82,11 @@ def _load():
         "dsa_sort_candidate_blocks": (i32, [P, i32, P, i32, i32, P, i64, i32, P, P, P, sz, P]),
         "dsa_sparse_mqa_logits": (i32, [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, i32, P,
                                         i32, P, P, P, i32, i64, P, sz, P]),
+        "dsa_pair_units": (i32, [i32, i32]),
+        "dsa_sort_candidate_blocks_paired": (i32, [P, i32, P, i32, i32, P, i64, i32, P, P, P, P,
+                                                   P, P, sz, P]),
+        "dsa_sparse_mqa_logits_paired": (i32, [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32,
+                                               i32, i32, P, P, P, P, P, i32, i64, P, sz, P]),
         "dsa_topk_fp16": (i32, [P, i64, P, i32, i32, P, i32, P, P, sz, P]),
         "dsa_topk_bf16": (i32, [P, i64, P, i32, i32, P, i32, P, P, sz, P]),
         "dsa_coarse_hist_topk_noalloc": (i32, [P, i64, P, i32, i32, i32, P, i32, i32, P, P, P]),
@@ -319,6 +324,59 @@ def sparse_mqa_logits(q, kv_pages, kscale, weights, page_table, context_lens, ne
         _p(context_lens), B, next_n, H, D, ps, P, _p(block_table), kb, _p(phys_blocks),
         _p(valid_lens), _p(out), out_dtype, out.stride(0), ws.ptr, ws.nbytes, _stream(stream)),
         "sparse_mqa_logits")
+    return out
+
+
+def pair_units(B: int, next_n: int) -> int:
+    """Units of the paired sparse pass: B * ceil(next_n / 2)."""
+    return int(lib.dsa_pair_units(B, next_n))
+
+
+def sort_candidate_blocks_paired(block_ids, context_lens, next_n, page_table, page_size, ws,
+                                 valid_lens, union, phys_blocks=None, stream=None):
+    """``sort_candidate_blocks`` for every row (in place, same tables) plus the
+    union of each unit's two tables.  ``union`` is (union_phys [U][2kb],
+    union_pos [U][2kb], union_len [U]) int32, filled; returns it."""
+    _req(block_ids, torch.int32, "block_ids")
+    R, kb = block_ids.shape
+    B = context_lens.shape[0]
+    uphys, upos, ulen = union
+    U = pair_units(B, next_n)
+    for t, nm, shp in ((uphys, "union_phys", (U, 2 * kb)), (upos, "union_pos", (U, 2 * kb)),
+                       (ulen, "union_len", (U,)), (valid_lens, "valid_lens", (R,))):
+        _req(t, torch.int32, nm)
+        if tuple(t.shape) != shp or not t.is_contiguous():
+            raise ValueError(f"{nm}: expected a contiguous {shp} tensor")
+    if phys_blocks is not None:
+        _req(phys_blocks, torch.int32, "phys_blocks")
+    _check(lib.dsa_sort_candidate_blocks_paired(
+        _p(block_ids), kb, _p(context_lens), next_n, B, _p(page_table), page_table.stride(0),
+        page_size, _p(phys_blocks), _p(valid_lens), _p(uphys), _p(upos), _p(ulen), ws.ptr,
+        ws.nbytes, _stream(stream)), "sort_candidate_blocks_paired")
+    return union
+
+
+def sparse_mqa_logits_paired(q, kv_pages, kscale, weights, page_table, context_lens, next_n,
+                             kb, union, valid_lens, ws, out=None, out_dtype=OUT_F32,
+                             stream=None):
+    """Sparse logits of every row, two rows of a request per K pass (bitwise
+    the output of ``sparse_mqa_logits`` with physical blocks)."""
+    q, kv_pages = _u8(q), _u8(kv_pages)
+    R, H, D = q.shape
+    P, ps, _ = kv_pages.shape
+    B = context_lens.shape[0]
+    uphys, upos, ulen = union
+    if out is None:
+        dt = {OUT_F32: torch.float32, OUT_F16: torch.float16, OUT_BF16: torch.bfloat16}[out_dtype]
+        out = torch.empty((R, kb * 8), dtype=dt, device=q.device)
+    for t, nm in ((uphys, "union_phys"), (upos, "union_pos"), (ulen, "union_len"),
+                  (valid_lens, "valid_lens")):
+        _req(t, torch.int32, nm)
+    _check(lib.dsa_sparse_mqa_logits_paired(
+        _p(q), _p(kv_pages), _p(kscale), _p(weights), _p(page_table), page_table.stride(0),
+        _p(context_lens), B, next_n, H, D, ps, P, kb, _p(uphys), _p(upos), _p(ulen),
+        _p(valid_lens), _p(out), out_dtype, out.stride(0), ws.ptr, ws.nbytes, _stream(stream)),
+        "sparse_mqa_logits_paired")
     return out
 
 

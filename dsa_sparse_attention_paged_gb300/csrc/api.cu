@@ -435,6 +435,78 @@ int32_t dsa_sort_candidate_blocks(int32_t *block_ids, int32_t kb, const int32_t 
                          static_cast<cudaStream_t>(stream));
 }
 
+int32_t dsa_pair_units(int32_t B, int32_t next_n) {
+  if (B < 0 || next_n < 1) return 0;
+  return B * ((next_n + 1) / 2);
+}
+
+int32_t dsa_sort_candidate_blocks_paired(int32_t *block_ids, int32_t kb,
+                                         const int32_t *context_lens, int32_t next_n, int32_t B,
+                                         const int32_t *page_table, int64_t page_table_stride,
+                                         int32_t page_size, int32_t *phys_blocks,
+                                         int32_t *valid_lens, int32_t *union_phys,
+                                         int32_t *union_pos, int32_t *union_len,
+                                         void *workspace, size_t ws_bytes, void *stream) {
+  if (B < 0 || next_n < 1 || kb < 1) return DSA_ERR_INVALID_ARG;
+  if (kb > 4096) return DSA_ERR_UNSUPPORTED;
+  if (!block_ids || !context_lens || !page_table || page_table_stride < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (!valid_lens || !union_phys || !union_pos || !union_len) return DSA_ERR_INVALID_ARG;
+  if (page_size < 8 || page_size % 8 != 0) return DSA_ERR_UNSUPPORTED;
+  if (!workspace || ws_bytes < WsLayout::kHeader) return DSA_ERR_WORKSPACE;
+  if (B == 0) return DSA_OK;
+  return run_sort_pair_blocks(block_ids, kb, context_lens, next_n, B, page_table,
+                              page_table_stride, page_size, phys_blocks, valid_lens, union_phys,
+                              union_pos, union_len, status_word(workspace),
+                              static_cast<cudaStream_t>(stream));
+}
+
+int32_t dsa_sparse_mqa_logits_paired(const uint8_t *q, const uint8_t *kv_pages,
+                                     const float *kscale, const float *weights,
+                                     const int32_t *page_table, int64_t page_table_stride,
+                                     const int32_t *context_lens, int32_t B, int32_t next_n,
+                                     int32_t num_heads, int32_t head_dim, int32_t page_size,
+                                     int32_t num_pages, int32_t kb, const int32_t *union_phys,
+                                     const int32_t *union_pos, const int32_t *union_len,
+                                     const int32_t *valid_lens, void *out, int32_t out_dtype,
+                                     int64_t out_stride, void *workspace, size_t ws_bytes,
+                                     void *stream) {
+  int32_t e = check_paged_common(q, kv_pages, kscale, weights, page_table, page_table_stride,
+                                 context_lens, B, next_n, num_heads, head_dim, page_size,
+                                 num_pages, workspace, ws_bytes);
+  if (e != DSA_OK) return e;
+  if (!union_phys || !union_pos || !union_len || !valid_lens || !out) return DSA_ERR_INVALID_ARG;
+  if (kb < 16 || kb % 16 != 0 || kb > 4096) return DSA_ERR_UNSUPPORTED;
+  if (out_dtype != DSA_OUT_F32 && out_dtype != DSA_OUT_F16 && out_dtype != DSA_OUT_BF16)
+    return DSA_ERR_INVALID_ARG;
+  if (out_stride < (int64_t)kb * 8) return DSA_ERR_INVALID_ARG;
+  if (B == 0) return DSA_OK;
+  LogitsCall c{};
+  c.q = q;
+  c.kv = kv_pages;
+  c.kscale = kscale;
+  c.weights = weights;
+  c.page_table = page_table;
+  c.pt_stride = page_table_stride;
+  c.context_lens = context_lens;
+  c.B = B;
+  c.next_n = next_n;
+  c.page_size = page_size;
+  c.num_pages = num_pages;
+  c.out = out;
+  c.out_stride = out_stride;
+  c.sparse = true;
+  c.out_fmt = out_dtype;
+  c.kb = kb;
+  c.valid_lens = valid_lens;
+  c.union_phys = union_phys;
+  c.union_pos = union_pos;
+  c.union_len = union_len;
+  c.status = status_word(workspace);
+  c.wait_limit = kDefaultWaitLimit;
+  return run_paged_logits(c, static_cast<cudaStream_t>(stream));
+}
+
 int32_t dsa_topk_fp16(const uint16_t *scores, int64_t stride, const int32_t *valid_lens,
                       int32_t R, int32_t k, const int32_t *block_table, int32_t kb,
                       int32_t *out_idx, void *workspace, size_t ws_bytes, void *stream) {

@@ -37,6 +37,11 @@ struct LogitsCall {
   int32_t kb;
   const int32_t *phys = nullptr;        // sparse: physical blocks of the table, or NULL
   const int32_t *valid_lens = nullptr;  // sparse, with phys: live prefix length per row
+  // sparse, paired rows: units of two rows of one request walk the union of
+  // their tables (physical block, per-row position + 1, union length)
+  const int32_t *union_phys = nullptr;
+  const int32_t *union_pos = nullptr;
+  const int32_t *union_len = nullptr;
   uint32_t *status;
   long long wait_limit;
 };
@@ -90,6 +95,12 @@ dsa_status_t run_sort_blocks(int32_t *ids, int32_t kb, const int32_t *context_le
                              int32_t next_n, int32_t R, const int32_t *page_table,
                              int64_t pt_stride, int32_t page_size, int32_t *phys,
                              int32_t *valid_lens, uint32_t *status, cudaStream_t st);
+
+dsa_status_t run_sort_pair_blocks(int32_t *ids, int32_t kb, const int32_t *context_lens,
+                                  int32_t next_n, int32_t B, const int32_t *page_table,
+                                  int64_t pt_stride, int32_t page_size, int32_t *phys,
+                                  int32_t *valid_lens, int32_t *union_phys, int32_t *union_pos,
+                                  int32_t *union_len, uint32_t *status, cudaStream_t st);
 
 dsa_status_t run_bins_range(uint32_t start, int64_t count, int16_t *out, cudaStream_t st);
 dsa_status_t run_bf16_keys(const uint16_t *in, uint16_t *out, int64_t n, cudaStream_t st);

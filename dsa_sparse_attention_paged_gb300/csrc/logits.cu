@@ -73,6 +73,13 @@ struct LogitsArgs {
   int32_t kb;
   const int32_t *phys;        // sparse: physical blocks (pool slot / 8) of the table, or NULL
   const int32_t *valid_lens;  // sparse, with phys: live positions form the prefix [0, len)
+  // sparse, paired rows (next_n = 2 instantiation): unit u is rows 2m, 2m+1
+  // of request u / upr (an odd last row alone); `phys` is then the union of
+  // their tables, `upos` per union entry (pos_a + 1) | (pos_b + 1) << 16
+  const int32_t *upos;
+  const int32_t *ulen;        // union entries per unit, or NULL (unpaired)
+  int32_t upr;                // units per request: ceil(next_n / 2)
+  int32_t tab_stride;         // entries per unit in `phys`: kb, or 2 kb paired
   void *out;
   int64_t out_stride;
   int32_t *histogram;
@@ -132,7 +139,13 @@ __device__ __forceinline__ int64_t eff_ctx(const LogitsArgs &a, int b) {
 
 template <bool SPARSE>
 __device__ __forceinline__ int unit_tiles(const LogitsArgs &a, int u) {
-  if (SPARSE) return a.sparse_tpu;
+  if (SPARSE) {
+    if (!a.ulen) return a.sparse_tpu;
+    // paired: the union, and at least kb entries so that every padding
+    // position of both rows' outputs is visited once
+    const int n = min(max(__ldg(&a.ulen[u]), a.kb), a.tab_stride);
+    return (n + 31) / 32;
+  }
   return static_cast<int>((eff_ctx(a, u) + kStageTok - 1) / kStageTok);
 }
 
@@ -199,13 +212,14 @@ template <bool SPARSE>
 __device__ void compute_sched(const LogitsArgs &a, int *out_u0, int *out_i0, long long *out_cnt) {
   const int lane = threadIdx.x & 31;
   long long T = 0;
-  if (SPARSE) {
+  const bool fixed = SPARSE && !a.ulen;  // same stage count for every unit
+  if (fixed) {
     T = (long long)a.num_units * a.sparse_tpu;
   } else {
     for (int base = 0; base < a.num_units; base += 32) {
       const int b = base + lane;
-      int t = (b < a.num_units) ? unit_tiles<false>(a, b) : 0;
-      if (b < a.num_units && a.context_lens[b] > a.pt_stride * a.page_size)
+      int t = (b < a.num_units) ? unit_tiles<SPARSE>(a, b) : 0;
+      if (!SPARSE && b < a.num_units && a.context_lens[b] > a.pt_stride * a.page_size)
         set_status(a.status, DSA_DEV_BOUNDS);
       T += __shfl_sync(0xffffffffu, warp_incl_scan(t), 31);
     }
@@ -214,14 +228,14 @@ __device__ void compute_sched(const LogitsArgs &a, int *out_u0, int *out_i0, lon
   const long long g1 = (long long)(blockIdx.x + 1) * T / gridDim.x;
   int u0 = a.num_units, i0 = 0;
   if (g1 > g0) {
-    if (SPARSE) {
+    if (fixed) {
       u0 = (int)(g0 / a.sparse_tpu);
       i0 = (int)(g0 % a.sparse_tpu);
     } else {
       long long acc = 0;
       for (int base = 0; base < a.num_units; base += 32) {
         const int b = base + lane;
-        const int t = (b < a.num_units) ? unit_tiles<false>(a, b) : 0;
+        const int t = (b < a.num_units) ? unit_tiles<SPARSE>(a, b) : 0;
         const int incl = warp_incl_scan(t);
         const int tot = __shfl_sync(0xffffffffu, incl, 31);
         if (g0 < acc + tot) {
@@ -307,7 +321,10 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
                   const LogitsArgs a) {
   // the dense pass waits for its predecessors at once; the sparse pass sets up
   // (barriers, schedule, TMEM, tensor maps: nothing a predecessor writes) first
-  if (!SPARSE) pdl_wait();
+  // dense, and paired sparse (whose schedule reads the union lengths): the
+  // predecessor's outputs are needed from the start
+  constexpr bool kWaitFirst = !SPARSE || NN > 1;
+  if (kWaitFirst) pdl_wait();
   constexpr int N = 32 * NN;
   constexpr uint32_t IDESC = idesc_e4m3_f32(128, N);
   constexpr int HS = hist_slots_per_group(NN);
@@ -391,7 +408,7 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (SPARSE) pdl_wait();  // the block table, physical blocks and live lengths are ready
+  if (!kWaitFirst) pdl_wait();  // the block table, physical blocks and live lengths are ready
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl ctl{abort_flag, a.status, a.wait_limit};
 
@@ -415,8 +432,8 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
       unit = g0.u;
       if (SPARSE) {
         const int blk = g0.i * 32 + my_sl;
-        if (blk >= a.kb) return kNone;
-        return __ldg(&(a.phys ? a.phys : a.block_table)[(int64_t)g0.u * a.kb + blk]);
+        if (blk >= a.tab_stride) return kNone;
+        return __ldg(&(a.phys ? a.phys : a.block_table)[(int64_t)g0.u * a.tab_stride + blk]);
       }
       const int64_t p = (int64_t)g0.i * ppt + my_sl;
       if (p * a.page_size >= eff_ctx(a, g0.u)) return kNone;
@@ -480,17 +497,28 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
         if (tab_i == 0) {
           // flattened stage g = (row, tile) in closed form, so the loads of
           // eight stages are in flight together
+          // (paired: stage counts differ per unit, so a copy of the
+          // iterator walks the next stages instead)
           const long long gbase = (long long)u_start * a.sparse_tpu + i_start + n;
+          TileIter<SPARSE> wt = it;
           for (int j0 = 0; j0 < kSpTab && n + j0 < count; j0 += 8) {
             int raw[8];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
               raw[jj] = kNone;
               if (n + j0 + jj < count) {
-                const long long g = gbase + j0 + jj;
-                const int uu = (int)(g / a.sparse_tpu);
-                const int blk = (int)(g - (long long)uu * a.sparse_tpu) * 32 + lane;
-                if (blk < a.kb) raw[jj] = __ldg(&a.phys[(int64_t)uu * a.kb + blk]);
+                int uu, ti;
+                if (NN == 1) {
+                  const long long g = gbase + j0 + jj;
+                  uu = (int)(g / a.sparse_tpu);
+                  ti = (int)(g - (long long)uu * a.sparse_tpu);
+                } else {
+                  uu = wt.u;
+                  ti = wt.i;
+                  wt.next(a);
+                }
+                const int blk = ti * 32 + lane;
+                if (blk < a.tab_stride) raw[jj] = __ldg(&a.phys[(int64_t)uu * a.tab_stride + blk]);
               }
             }
 #pragma unroll
@@ -513,13 +541,21 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
         ++unit_ord;
         prev_u = u;
         const int qb = unit_ord & 1;
-        const int qrow0 = SPARSE ? u * 32 : u * N;
+        int qrow0 = SPARSE ? u * 32 : u * N;
+        int nw = N;  // head weights loaded
+        if (SPARSE && NN == 2) {
+          // paired unit: rows 2m, 2m+1 of its request; an odd last row loads
+          // its own weights only (the Q tile's second half is not used)
+          const int b = u / a.upr, m2 = 2 * (u - b * a.upr);
+          qrow0 = (b * a.req_next_n + m2) * 32;
+          if (m2 + 1 >= a.req_next_n) nw = 32;
+        }
         if (lane == 0) {
           ok = mbar_wait(QEMPTY(qb), ((unit_ord >> 1) & 1) ^ 1, ctl);
           if (ok) {
-            mbar_arrive_expect_tx(QFULL(qb), N * 128 + N * 4);
+            mbar_arrive_expect_tx(QFULL(qb), N * 128 + nw * 4);
             tma_load_2d(qst + qb * (N * 128), &tm_q, QFULL(qb), 0, qrow0);
-            bulk_load(smem_u32(w_s + qb * N), a.weights + (int64_t)qrow0, N * 4, QFULL(qb));
+            bulk_load(smem_u32(w_s + qb * N), a.weights + (int64_t)qrow0, nw * 4, QFULL(qb));
             ++q_issued;
           }
         }
@@ -633,6 +669,29 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
     int64_t ctx_b = 0, n_row = 0;
     int row_base = 0;
     bool ok = true;
+    // paired unit: its rows, their live lengths and the union length
+    int row_a = 0, row_b = -1, nu = 0;
+    int64_t v_a = 0, v_b = 0;
+    // one sparse score, in the output format
+    auto sp_store = [&](int64_t row, int64_t p, float val) {
+      if (OUT == DSA_OUT_F16) {
+        reinterpret_cast<__half *>(a.out)[row * a.out_stride + p] = __float2half_rn(val);
+      } else if (OUT == DSA_OUT_BF16) {
+        reinterpret_cast<__nv_bfloat16 *>(a.out)[row * a.out_stride + p] = __float2bfloat16_rn(val);
+      } else {
+        reinterpret_cast<float *>(a.out)[row * a.out_stride + p] = val;
+      }
+    };
+    // a paired row's share of a union position: its own table slot p_tab
+    // (live below its valid length, -inf past it), and the padding slots
+    // [blocks * 8, kb * 8) of its output, which the union walk visits once
+    auto pair_store = [&](int row, int p_tab, int64_t pos, int64_t v, float val) {
+      if (p_tab >= 0 && p_tab < a.kb) {
+        const int64_t p = (int64_t)p_tab * 8 + (pos & 7);
+        sp_store(row, p, p < v ? val : -INFINITY);
+      }
+      if (pos >= ((v + 7) >> 3) * 8 && pos < (int64_t)a.kb * 8) sp_store(row, pos, -INFINITY);
+    };
 
     auto ewait = [&](uint32_t bar, uint32_t parity) -> bool {
       const bool r = mbar_wait(bar, parity, ctl);
@@ -682,7 +741,14 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
         ++unit_ord;
         prev_u = u;
         qb = unit_ord & 1;
-        if (SPARSE && a.valid_lens) {
+        if (SPARSE && NN == 2) {
+          const int b = u / a.upr, m2 = 2 * (u - b * a.upr);
+          row_a = b * a.req_next_n + m2;
+          row_b = (m2 + 1 < a.req_next_n) ? row_a + 1 : -1;
+          nu = min(__ldg(&a.ulen[u]), a.tab_stride);
+          v_a = __ldg(&a.valid_lens[row_a]);
+          v_b = row_b >= 0 ? __ldg(&a.valid_lens[row_b]) : 0;
+        } else if (SPARSE && a.valid_lens) {
           n_row = __ldg(&a.valid_lens[u]);  // live positions of the sparse row
         } else if (SPARSE) {
           const int b = u / a.req_next_n;
@@ -701,7 +767,10 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
       const int kx = rk.idx;
       const int64_t pos = (int64_t)i * kStageTok + tok;
       int32_t blk = INT32_MAX;
-      if (SPARSE && !a.valid_lens && pos < (int64_t)a.kb * 8)
+      uint32_t pw = 0;  // paired: the union entry's two table positions
+      if (SPARSE && NN == 2 && (pos >> 3) < nu)
+        pw = (uint32_t)__ldg(&a.upos[(int64_t)u * a.tab_stride + (pos >> 3)]);
+      if (SPARSE && NN == 1 && !a.valid_lens && pos < (int64_t)a.kb * 8)
         blk = __ldg(&a.block_table[(int64_t)u * a.kb + pos / 8]);
       if (!(ok = ewait(KSF(kx), rk.ph))) break;
       const float ks = ks_s[kx * kStageTok + tok];
@@ -733,19 +802,14 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
           if (j0 + jj < NN) acc[j0 + jj] = head_sum(v[jj], ks, w_s + qb * N + (j0 + jj) * 32);
       }
 
-      if (SPARSE) {
+      if (SPARSE && NN == 2) {
+        pair_store(row_a, (int)(pw & 0xffffu) - 1, pos, v_a, acc[0]);
+        if (row_b >= 0) pair_store(row_b, (int)(pw >> 16) - 1, pos, v_b, acc[NN - 1]);
+      } else if (SPARSE) {
         if (pos < (int64_t)a.kb * 8) {
           const int64_t t = (int64_t)blk * 8 + (pos & 7);
           const bool live = a.valid_lens ? pos < n_row : (blk != INT32_MAX && blk >= 0 && t < n_row);
-          const float val = live ? acc[0] : -INFINITY;
-          if (OUT == DSA_OUT_F16) {
-            reinterpret_cast<__half *>(a.out)[(int64_t)u * a.out_stride + pos] = __float2half_rn(val);
-          } else if (OUT == DSA_OUT_BF16) {
-            reinterpret_cast<__nv_bfloat16 *>(a.out)[(int64_t)u * a.out_stride + pos] =
-                __float2bfloat16_rn(val);
-          } else {
-            reinterpret_cast<float *>(a.out)[(int64_t)u * a.out_stride + pos] = val;
-          }
+          sp_store(u, pos, live ? acc[0] : -INFINITY);
         }
       } else {
         const int64_t t = pos;
@@ -851,7 +915,7 @@ dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   dsa_status_t e = make_tmap_rows128(&tk, c.kv, (uint64_t)c.num_pages * c.page_size,
                                      c.sparse ? 8 : c.page_size);
   if (e != DSA_OK) return e;
-  const int nn = c.sparse ? 1 : c.next_n;
+  const int nn = c.sparse ? (c.union_len ? 2 : 1) : c.next_n;
   e = make_tmap_rows128(&tq, c.q, (uint64_t)c.B * c.next_n * 32, 32 * nn);
   if (e != DSA_OK) return e;
   LogitsArgs a{};
@@ -869,6 +933,16 @@ dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   a.kb = c.kb;
   a.phys = c.sparse ? c.phys : nullptr;
   a.valid_lens = c.sparse ? c.valid_lens : nullptr;
+  a.tab_stride = c.kb;
+  a.upr = 1;
+  const bool paired = c.sparse && c.union_len != nullptr;
+  if (paired) {
+    a.phys = c.union_phys;
+    a.upos = c.union_pos;
+    a.ulen = c.union_len;
+    a.tab_stride = 2 * c.kb;
+    a.upr = (c.next_n + 1) / 2;
+  }
   a.out = c.out;
   a.out_stride = c.out_stride;
   a.histogram = c.histogram;
@@ -879,6 +953,17 @@ dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   a.wait_limit = c.wait_limit;
   const int sms = num_sms();
   if (sms <= 0) return DSA_ERR_CUDA;
+  if (paired) {
+    // stage counts per unit come from the union lengths on the device
+    a.num_units = c.B * a.upr;
+    a.sparse_tpu = (c.kb + 31) / 32;
+    const long long tiles = (long long)a.num_units * 2 * a.sparse_tpu;
+    const int grid = (int)std::max<long long>(1, std::min<long long>(sms, tiles));
+    if (c.out_fmt == DSA_OUT_F16) return launch_one<2, true, DSA_OUT_F16, false>(tk, tq, a, grid, st);
+    if (c.out_fmt == DSA_OUT_BF16)
+      return launch_one<2, true, DSA_OUT_BF16, false>(tk, tq, a, grid, st);
+    return launch_one<2, true, DSA_OUT_F32, false>(tk, tq, a, grid, st);
+  }
   if (c.sparse) {
     a.num_units = c.B * c.next_n;
     a.sparse_tpu = (c.kb + 31) / 32;

@@ -13,7 +13,10 @@ step's device buffers and the workspace, and each ``step`` runs
                  maxima fused into the logits pass and a second
                  problem of the batched select instead)
   level one      sort_candidate_blocks -> table, phys, valid lens   (1 launch)
+                 (pair_rows: the paired sort, which also emits the
+                 union of each two-row unit's tables)
   consumer       sparse MQA logits over the table, FP16 output      (1 launch)
+                 (pair_rows: two rows of a request per K pass)
                  FP16 top-k with the fused table transform          (1 launch)
 
 following SGLang PR #38944 ("What this enables": the source layer publishes an
@@ -26,14 +29,20 @@ import torch
 
 from . import (OUT_F16, Workspace, coarse_hist_topk, coarse_hist_topk_batch,
                coarse_hist_topk_batch_launches, coarse_hist_topk_launches, paged_mqa_logits,
-               sort_candidate_blocks, sparse_mqa_logits, topk_fp16)
+               pair_units, sort_candidate_blocks, sort_candidate_blocks_paired,
+               sparse_mqa_logits, sparse_mqa_logits_paired, topk_fp16)
 
 
 class DecodePlan:
 
     def __init__(self, B, next_n, max_context, page_size, k=2048, kb=512, two_level=True,
-                 device="cuda"):
+                 pair_rows=False, device="cuda"):
+        """``pair_rows`` scores two rows of a request per K pass in the sparse
+        step (same results, bitwise).  It pays when the two rows' tables share
+        most blocks (draft rows of one request); on independent rows the union
+        is twice a table and the unpaired pass is faster."""
         self.B, self.next_n, self.page_size = B, next_n, page_size
+        self.pair_rows = bool(pair_rows) and next_n > 1
         self.R = B * next_n
         self.k, self.kb, self.two_level = k, kb, two_level
         # row stride padded to 8 floats: 32-byte aligned rows for the vector loads
@@ -58,6 +67,12 @@ class DecodePlan:
             self.valid_lens = torch.empty((R,), dtype=torch.int32, device=dev)
             self.sparse = torch.empty((R, kb * 8), dtype=torch.float16, device=dev)
             self.sparse_idx = torch.empty((R, k), dtype=torch.int32, device=dev)
+            self.union = None
+            if self.pair_rows:
+                U = pair_units(B, next_n)
+                self.union = (torch.empty((U, 2 * kb), dtype=torch.int32, device=dev),
+                              torch.empty((U, 2 * kb), dtype=torch.int32, device=dev),
+                              torch.empty((U,), dtype=torch.int32, device=dev))
 
     @property
     def launches_per_step(self) -> int:
@@ -102,13 +117,23 @@ class DecodePlan:
                 out=self.block_ids)], ws)
         mark("select", 1)
         mark("publish", 0)
-        sort_candidate_blocks(self.block_ids, context_lens, nn, page_table, self.page_size, ws,
-                              phys_blocks=self.phys, valid_lens=self.valid_lens)
+        if self.union is not None:
+            sort_candidate_blocks_paired(self.block_ids, context_lens, nn, page_table,
+                                         self.page_size, ws, self.valid_lens, self.union,
+                                         phys_blocks=self.phys)
+        else:
+            sort_candidate_blocks(self.block_ids, context_lens, nn, page_table, self.page_size,
+                                  ws, phys_blocks=self.phys, valid_lens=self.valid_lens)
         mark("publish", 1)
         mark("consume", 0)
-        sparse_mqa_logits(q, kv, kscale, weights, page_table, context_lens, nn,
-                          self.block_ids, ws, out=self.sparse, out_dtype=OUT_F16,
-                          phys_blocks=self.phys, valid_lens=self.valid_lens)
+        if self.union is not None:
+            sparse_mqa_logits_paired(q, kv, kscale, weights, page_table, context_lens, nn,
+                                     self.kb, self.union, self.valid_lens, ws, out=self.sparse,
+                                     out_dtype=OUT_F16)
+        else:
+            sparse_mqa_logits(q, kv, kscale, weights, page_table, context_lens, nn,
+                              self.block_ids, ws, out=self.sparse, out_dtype=OUT_F16,
+                              phys_blocks=self.phys, valid_lens=self.valid_lens)
         topk_fp16(self.sparse, self.valid_lens, self.k, ws, block_table=self.block_ids,
                   out=self.sparse_idx)
         mark("consume", 1)

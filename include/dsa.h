@@ -325,6 +325,52 @@ int32_t dsa_sparse_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const f
                               void *out, int32_t out_dtype, int64_t out_stride, void *workspace,
                               size_t ws_bytes, void *stream);
 
+/* ---- row pairing of the sparse pass ---------------------------------------
+ * [SG38944] commit text on DeepGEMM's sparse schedule: two consecutive rows
+ * of one request share one KV pass, each keeping its own block list and
+ * output layout (the rows share their page-table row).  Units: within each
+ * request, rows 2m and 2m+1 form unit b * ceil(next_n / 2) + m; an odd last
+ * row is a unit of its own.  U = B * ceil(next_n / 2) = dsa_pair_units().
+ *
+ * dsa_sort_candidate_blocks_paired: everything dsa_sort_candidate_blocks
+ * does for the B * next_n rows (the same tables, physical blocks and live
+ * lengths, bit for bit; valid_lens is required here), in one launch of U
+ * CTAs, plus per unit the ascending union of its rows' tables:
+ *   union_phys [U][2*kb]  physical block of union entry e (pool slot / 8),
+ *                         INT32_MAX past the union
+ *   union_pos  [U][2*kb]  (pos_a + 1) | (pos_b + 1) << 16: the entry's position
+ *                         in each row's table, 0 where the row does not hold
+ *                         the block; 0 past the union
+ *   union_len  [U]        entries in the union
+ * All caller-owned device buffers; kb <= 4096; page_size % 8 == 0. */
+int32_t dsa_pair_units(int32_t B, int32_t next_n);
+int32_t dsa_sort_candidate_blocks_paired(int32_t *block_ids, int32_t kb,
+                                         const int32_t *context_lens, int32_t next_n, int32_t B,
+                                         const int32_t *page_table, int64_t page_table_stride,
+                                         int32_t page_size, int32_t *phys_blocks,
+                                         int32_t *valid_lens, int32_t *union_phys,
+                                         int32_t *union_pos, int32_t *union_len,
+                                         void *workspace, size_t ws_bytes, void *stream);
+
+/* dsa_sparse_mqa_logits_paired: the same output as dsa_sparse_mqa_logits
+ * with phys_blocks and valid_lens (bitwise), computed per unit: each union
+ * entry's K rows are read once and scored for both rows of the unit in one
+ * tcgen05 MMA with N = 64 (both rows' 32 heads); a row's score goes to its
+ * own table position, and its positions past its table (padding) get -inf.
+ * union_* and valid_lens come from dsa_sort_candidate_blocks_paired for the
+ * same tables.  Other arguments as dsa_sparse_mqa_logits (kb % 16 == 0,
+ * out_stride >= kb*8). */
+int32_t dsa_sparse_mqa_logits_paired(const uint8_t *q, const uint8_t *kv_pages,
+                                     const float *kscale, const float *weights,
+                                     const int32_t *page_table, int64_t page_table_stride,
+                                     const int32_t *context_lens, int32_t B, int32_t next_n,
+                                     int32_t num_heads, int32_t head_dim, int32_t page_size,
+                                     int32_t num_pages, int32_t kb, const int32_t *union_phys,
+                                     const int32_t *union_pos, const int32_t *union_len,
+                                     const int32_t *valid_lens, void *out, int32_t out_dtype,
+                                     int64_t out_stride, void *workspace, size_t ws_bytes,
+                                     void *stream);
+
 /* ---- top-k over FP16 scores ---------------------------------------------
  * [VL52696] "Why": select on the packed FP16 score bits directly (both halves
  * of a 32-bit word are turned into order keys with one 32-bit operation), a

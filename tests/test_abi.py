@@ -173,3 +173,39 @@ def test_batch_block_output_argument_checks(lib):
     assert call(prob(len_div=8)) == 2
     assert call(prob(stride=200000)) == 2
     assert call(prob(stride=1000), prob(stride=200000, block_k=0, block_out_idx=None)) == 2
+
+
+def test_paired_sort_and_sparse_argument_checks(lib):
+    """The paired calls need the union buffers and live lengths; kb as for
+    the unpaired calls; all refused before anything is launched."""
+    ws = ctypes.c_void_p(0x20000)
+    assert lib.dsa_pair_units(5, 4) == 10 and lib.dsa_pair_units(5, 3) == 10
+    assert lib.dsa_pair_units(2, 1) == 2 and lib.dsa_pair_units(-1, 2) == 0
+    h = lib.dsa_sort_candidate_blocks_paired
+    ok = dict(ids=A16, kb=64, ctx=A16, nn=2, B=2, pt=A16, pts=4, ps=64, phys=None, vl=A16,
+              up=A16, uq=A16, ul=A16)
+
+    def sort(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return h(a["ids"], a["kb"], a["ctx"], a["nn"], a["B"], a["pt"], a["pts"], a["ps"],
+                 a["phys"], a["vl"], a["up"], a["uq"], a["ul"], ws, 4096, None)
+    assert sort(vl=None) == 1
+    assert sort(up=None) == 1
+    assert sort(ul=None) == 1
+    assert sort(kb=8192) == 2
+    assert sort(ps=12) == 2
+    assert sort(B=0) == 0
+
+    s = lib.dsa_sparse_mqa_logits_paired
+
+    def sp(**kw):
+        a = dict(kb=64, up=A16, uq=A16, ul=A16, vl=A16, ostride=512, nn=2)
+        a.update(kw)
+        return s(A16, A16, A16, A16, A16, 4, A16, 2, a["nn"], 32, 128, 64, 10, a["kb"], a["up"],
+                 a["uq"], a["ul"], a["vl"], A16, 0, a["ostride"], ws, 4096, None)
+    assert sp(vl=None) == 1
+    assert sp(uq=None) == 1
+    assert sp(kb=40) == 2
+    assert sp(ostride=100) == 1
+    assert sp(nn=5) == 2

@@ -21,7 +21,8 @@ def test_full_size_workload(name):
     case = S.generate(w)
     d = to_dev(case)
     nn, ps = w.next_n, w.page_size
-    plan = DecodePlan(w.B, nn, max(w.context_lens), ps, k=2048, kb=512, two_level=True)
+    plan = DecodePlan(w.B, nn, max(w.context_lens), ps, k=2048, kb=512, two_level=True,
+                      pair_rows=nn > 1)
     dense_idx, sparse_idx = plan.step(d["q"], d["kv"], d["kscale"], d["weights"],
                                       d["page_table"], d["context_lens"])
     torch.cuda.synchronize()
@@ -74,6 +75,9 @@ def test_full_size_workload(name):
     np.testing.assert_array_equal(plan.block_ids.cpu().numpy(), t_ref)
     np.testing.assert_array_equal(plan.phys.cpu().numpy(), p_ref)
     np.testing.assert_array_equal(plan.valid_lens.cpu().numpy(), v_ref)
+    if plan.union is not None:  # next_n > 1: two rows of a request per K pass
+        for got, want in zip(plan.union, O.pair_union(t_ref, p_ref, nn)):
+            np.testing.assert_array_equal(got.cpu().numpy(), want)
     SP16 = plan.sparse.cpu().numpy().view(np.uint16)
     pos = np.arange(kb * 8)
     for r in range(R):

@@ -12,14 +12,15 @@ from tests.helpers import sets_equal, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def test_graph_replay_follows_inputs_rewritten_in_place():
+@pytest.mark.parametrize("pair_rows", [False, True])
+def test_graph_replay_follows_inputs_rewritten_in_place(pair_rows):
     from dsa_sparse_attention_paged_gb300.pipeline import DecodePlan
     # pages for 20000 keys in every request; each replay picks its own lengths
     a = S.generate(S.Workload("graph a", 3, 2, [20000] * 3, 64, "mixed", 91))
     b = S.generate(S.Workload("graph b", 3, 2, [20000] * 3, 64, "normal", 92))
     d = to_dev(a)
     d["context_lens"].copy_(torch.tensor([20000, 9000, 3000], dtype=torch.int32))
-    plan = DecodePlan(3, 2, 20000, 64, k=2048, kb=256)
+    plan = DecodePlan(3, 2, 20000, 64, k=2048, kb=256, pair_rows=pair_rows)
     plan.capture(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"], d["context_lens"])
 
     def replay_and_compare():
