@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
       mbar_init(EMPTY(s), 1);
     }
     for (int k = 0; k < KS; ++k) {
-      mbar_init(KSF(k), 1);
+      mbar_init(KSF(k), SPARSE ? 32 : 1);  // sparse: one cp.async arrival per producer lane
       mbar_init(KSE(k), kStageEpiWarps);
     }
     for (int q = 0; q < 2; ++q) {
@@ -570,18 +570,36 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
       const uint32_t nload = (uint32_t)__popc(__ballot_sync(0xffffffffu, row >= 0));
       if (lane == 0) {
         mbar_arrive_expect_tx(FULL(s), nload * (uint32_t)(blk_rows * 128));
-        mbar_arrive_expect_tx(KSF(kx), nload * (uint32_t)(blk_rows * 4));
+        if (!SPARSE) mbar_arrive_expect_tx(KSF(kx), nload * (uint32_t)(blk_rows * 4));
       }
       __syncwarp();
-      if (row >= 0) {
+      if (row >= 0)
         tma_load_2d_hint(kst + s * kStageK + lane * blk_rows * 128, &tm_k, FULL(s), 0, row, pol);
+      if (SPARSE) {
+        // kscale of the 32 blocks (32 bytes each) by 16-byte cp.async, two
+        // per lane, each lane's completion arriving on KSF by itself: a bulk
+        // copy per block would add a second operation per block on the SM's
+        // TMA unit, which bounds the sparse pass (about 40 ns per operation)
+        const uint32_t sdst = smem_u32(ks_s + kx * kStageTok);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = 16 * h + (lane >> 1), half = lane & 1;
+          const int rj = __shfl_sync(0xffffffffu, row, j);
+          if (rj >= 0)
+            cp_async16_hint(sdst + (uint32_t)((j * 8 + half * 4) * 4),
+                            a.kscale + (int64_t)rj + half * 4, pol);
+        }
+        cp_async_arrive_noinc(KSF(kx));
+      } else if (row >= 0) {
         bulk_load(smem_u32(ks_s + kx * kStageTok + lane * blk_rows), a.kscale + (int64_t)row,
                   blk_rows * 4, KSF(kx));
       }
       ++issued;
     }
+    if (SPARSE) cp_async_wait_all();  // this warp's kscale copies land before it moves on
     if (!ok && lane == 0) {
-      // drain our own copies still in flight before the CTA exits
+      // drain our own TMA copies still in flight before the CTA exits (the
+      // sparse pass's kscale cp.async copies were waited for above)
       const long long lim = a.wait_limit;
       Ring ds = rs, dk = rk;
       ds.idx = (int)(issued % S);
@@ -594,7 +612,7 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
         ds.prev(back, i2, p2);
         mbar_wait_drain(FULL(i2), p2, lim);
       }
-      for (int back = 1; back <= KS && back <= issued; ++back) {
+      for (int back = 1; !SPARSE && back <= KS && back <= issued; ++back) {
         int i2;
         uint32_t p2;
         dk.prev(back, i2, p2);
