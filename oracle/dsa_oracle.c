@@ -45,6 +45,8 @@
  *   R14 The BF16 sibling of the FP16 select (the next step the pages point
  *       to, [VL52696] "Why" for FP16): bfloat16 rounding is round-to-nearest-
  *       even, NaN never selected, the same order and tie rule as FP16.
+ *   R16 MXFP4 index keys: 128 E2M1 codes two per byte (even dimension in
+ *       the low nibble) plus 4 UE8M0 block exponents per token (68 bytes).
  *   R15 Row pairing of the sparse pass: rows 2m and 2m+1 of a request form
  *       one unit (an odd last row is alone) whose pass walks the ascending
  *       union of the two tables; each row's scores keep its own positions.
@@ -488,6 +490,79 @@ void o_pair_union(const int32_t *table, const int32_t *phys, int R, int next_n, 
         for (; e < 2 * kb; ++e) {
             up[e] = O_INT32_MAX;
             uq[e] = 0;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* O10: MXFP4 index keys.  The pages point to a block-scaled E2M1 index-K
+ * cache as the next format: [SG38944] (the Hopper prefill commit text:
+ * decode block-scaled E2M1 index keys directly to E4M3), [VL52696] ("Why"
+ * and the MXFP4 indexer-cache tests: the packed 68-byte cache layout), and
+ * [DG94] "What this adds" (the fused histogram is specified for FP8 "non-MX"
+ * only).  Reading R16: a token's key is 128 E2M1 codes packed two per byte
+ * (dimension 2i in the low nibble of byte i, 2i+1 in the high nibble: 64
+ * bytes) plus 4 UE8M0 block exponents (block b covers dimensions 32b ..
+ * 32b+31: 4 bytes) -- 68 bytes; k[d] = E2M1(code[d]) * 2^(e[d / 32] - 127),
+ * with no per-token kscale.  E2M1: sign bit 3, exponent bits 2..1 with bias 1,
+ * mantissa bit 0, exponent field 0 subnormal (m * 0.5), no inf or NaN.
+ * UE8M0: 2^(e - 127), e = 255 is NaN.  Queries stay FP8 E4M3.              */
+double o_e2m1(uint8_t c)
+{
+    int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+double o_ue8m0(uint8_t e)
+{
+    return e == 255 ? NAN : ldexp(1.0, (int)e - 127);
+}
+
+/* one logit with an MXFP4 key (the O2 formula with kscale = 1); the per-head
+ * dot is exact in double while a token's block exponents lie within about 40
+ * binades of each other */
+static double o_logit_one_mx(const uint8_t *q_row /* [H][D] */, const uint8_t *k_codes /* [D/2] */,
+                             const uint8_t *k_exp /* [D/32] */, const float *w_row, int H, int D,
+                             const double *tab)
+{
+    double acc = 0.0;
+    for (int h = 0; h < H; ++h) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) {
+            uint8_t byte = k_codes[d / 2];
+            uint8_t code = (d % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+            double k = o_e2m1(code) * o_ue8m0(k_exp[d / 32]);
+            dot += tab[q_row[h * D + d]] * k;
+        }
+        double v = dot;
+        if (!(v > 0.0)) v = 0.0;                     /* ReLU (R2) */
+        acc += (double)w_row[h] * v;
+    }
+    return acc;
+}
+
+/* dense logits over an MXFP4 paged cache: k_codes [slots][D/2], k_exp
+ * [slots][D/32], slots = num_pages * page_size; same rows and gather as O2,
+ * live columns written only */
+void o_paged_mqa_logits_mx(const uint8_t *q, const uint8_t *k_codes, const uint8_t *k_exp,
+                           const float *weights, const int32_t *page_table, int64_t pt_stride,
+                           const int32_t *context_lens, int B, int next_n, int H, int D,
+                           int page_size, float *out, int64_t out_stride)
+{
+    double tab[256];
+    o_e4m3_table(tab);
+    for (int b = 0; b < B; ++b) {
+        for (int j = 0; j < next_n; ++j) {
+            int r = b * next_n + j;
+            int64_t n = (int64_t)context_lens[b] - (next_n - 1 - j);
+            for (int64_t t = 0; t < n && t < out_stride; ++t) {
+                int64_t slot = o_slot_of(page_table, pt_stride, b, t, page_size);
+                out[(int64_t)r * out_stride + t] =
+                    (float)o_logit_one_mx(q + (int64_t)r * H * D, k_codes + slot * (D / 2),
+                                          k_exp + slot * (D / 32), weights + (int64_t)r * H, H,
+                                          D, tab);
+            }
         }
     }
 }

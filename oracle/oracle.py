@@ -80,6 +80,12 @@ def _load():
     lib.o_bf16_rn_sweep.argtypes = [ctypes.c_uint64, ctypes.c_uint64, P]
     lib.o_topk_bf16.argtypes = [P, i64, P, i32, i64, P, i32, P]
     lib.o_pair_union.argtypes = [P, P, i32, i32, i32, P, P, P]
+    lib.o_e2m1.restype = ctypes.c_double
+    lib.o_e2m1.argtypes = [ctypes.c_uint8]
+    lib.o_ue8m0.restype = ctypes.c_double
+    lib.o_ue8m0.argtypes = [ctypes.c_uint8]
+    lib.o_paged_mqa_logits_mx.argtypes = [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, P,
+                                          i64]
     _lib = lib
     return lib
 
@@ -192,6 +198,39 @@ def paged_mqa_logits(q, kv, kscale, weights, page_table, context_lens, next_n,
     _load().o_paged_mqa_logits(_ptr(q), _ptr(kv), _ptr(kscale), _ptr(weights),
                                _ptr(page_table), page_table.shape[1], _ptr(context_lens),
                                B, next_n, H, D, page_size, _ptr(out), out.shape[1])
+    return out
+
+
+def e2m1(code: int) -> float:
+    """Value of a 4-bit E2M1 code (MXFP4 element)."""
+    return _load().o_e2m1(code)
+
+
+def ue8m0(e: int) -> float:
+    """Value of an 8-bit UE8M0 block exponent."""
+    return _load().o_ue8m0(e)
+
+
+def paged_mqa_logits_mx(q, k_codes, k_exp, weights, page_table, context_lens, next_n,
+                        page_size, logits_stride=None, fill=np.nan) -> np.ndarray:
+    """Dense logits over an MXFP4 paged key cache: k_codes [P][page][D/2]
+    (two E2M1 codes per byte, even dimension low), k_exp [P][page][D/32]
+    (UE8M0); [R][stride] float32, dead columns keep ``fill``."""
+    q = _c(q, np.uint8)
+    k_codes = _c(k_codes, np.uint8)
+    k_exp = _c(k_exp, np.uint8)
+    weights = _c(weights, np.float32)
+    page_table = _c(page_table, np.int32)
+    context_lens = _c(context_lens, np.int32)
+    B = context_lens.shape[0]
+    R, H, D = q.shape
+    assert R == B * next_n and k_codes.shape[-1] * 2 == D and k_exp.shape[-1] * 32 == D
+    if logits_stride is None:
+        logits_stride = int(context_lens.max()) if B else 0
+    out = np.full((R, max(logits_stride, 1)), fill, dtype=np.float32)
+    _load().o_paged_mqa_logits_mx(_ptr(q), _ptr(k_codes), _ptr(k_exp), _ptr(weights),
+                                  _ptr(page_table), page_table.shape[1], _ptr(context_lens), B,
+                                  next_n, H, D, page_size, _ptr(out), out.shape[1])
     return out
 
 

@@ -589,3 +589,100 @@ def test_pair_union_covers_each_row_position_once():
             n = int((table[r] != IMAX).sum())
             pos = ((uq[u, :ul[u]] >> (16 * j)) & 0xFFFF).astype(np.int64) - 1
             assert sorted(pos[pos >= 0].tolist()) == list(range(n))
+
+
+def test_ue8m0_matches_torch_for_all_256_codes():
+    """UE8M0 block exponents against torch's float8_e8m0fnu decode: 2^(e-127),
+    255 is NaN."""
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = np.array([O.ue8m0(e) for e in range(256)])
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[ok], ref[ok])
+
+
+def test_e2m1_matches_torch_e4m3_through_the_exponent_rebias():
+    """Every E2M1 code decodes to the E4M3 value with the same sign, the
+    exponent field moved from bias 1 to bias 7 and the mantissa bit on top
+    (the subnormal 0.5 becomes the normal 2^-1): the direct E2M1 -> E4M3
+    unpacking the pages name, checked against torch's E4M3 decode."""
+    def rebias(c):
+        s, e, m = c >> 3, (c >> 1) & 3, c & 1
+        if e == 0:
+            bits = 0 if m == 0 else (6 << 3)
+        else:
+            bits = ((e + 6) << 3) | (m << 2)
+        return (s << 7) | bits
+    e4 = torch.tensor([rebias(c) for c in range(16)], dtype=torch.uint8)
+    ref = e4.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([O.e2m1(c) for c in range(16)])
+    np.testing.assert_array_equal(got, ref)
+    np.testing.assert_array_equal(np.signbit(got), np.signbit(ref))
+    assert got.max() == 6.0 and sorted(set(np.abs(got)))[1] == 0.5  # largest, smallest step
+
+
+def _pack_mx(vals, exps):
+    """[slots][128] E2M1 codes -> [slots][64] bytes (even dimension in the low
+    nibble) and [slots][4] block exponents (already codes)."""
+    codes = np.asarray(vals, np.uint8)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8), np.asarray(exps, np.uint8)
+
+
+def test_mx_logits_closed_form_uniform_keys():
+    """q = 1 everywhere, every key element 1.0 (code 2) with all four block
+    exponents e_t: logit = sum_h w_h * 128 * 2^(e_t - 127)."""
+    B, nn, ps, H, D = 2, 1, 64, 32, 128
+    ctx = [150, 77]
+    P, pt = _case(B, nn, ctx, ps, seed=5)
+    rng = np.random.default_rng(2)
+    e_slot = rng.integers(120, 135, size=P * ps)
+    codes, exps = _pack_mx(np.full((P * ps, D), 2), np.repeat(e_slot[:, None], 4, axis=1))
+    q = np.full((B * nn, H, D), E4M3_ONE, np.uint8)
+    w = rng.normal(0, 1, (B * nn, H)).astype(np.float32)
+    L = O.paged_mqa_logits_mx(q, codes.reshape(P, ps, 64), exps.reshape(P, ps, 4), w, pt,
+                              np.array(ctx, np.int32), nn, ps)
+    for b in range(B):
+        for t in range(ctx[b]):
+            slot = pt[b, t // ps] * ps + t % ps
+            v = 128.0 * 2.0 ** (int(e_slot[slot]) - 127)
+            assert L[b, t] == np.float32(sum(float(x) * v for x in w[b]))
+        assert np.isnan(L[b, ctx[b]:]).all()
+
+
+def test_mx_logits_nibble_order_and_block_exponents():
+    """q[r,h] one-hot at d_h = (9h + 5r) % 128 (even and odd dimensions, all
+    four blocks); key element d of logical token t has code c(t, d) in
+    1..15 and block b of token t exponent 125 + (t + b) % 5.  Then
+    dot_h = E2M1(c(t, d_h)) * 2^(e(t, d_h / 32) - 127): a swapped nibble, a
+    wrong block index or a wrong page gather changes the result."""
+    B, nn, ps, H, D = 2, 2, 64, 32, 128
+    ctx = [140, 99]
+    P, pt = _case(B, nn, ctx, ps, seed=9)
+    val = np.zeros((P * ps, D), np.uint8)
+    ex = np.full((P * ps, 4), 127, np.uint8)
+    code = lambda t, d: 1 + (3 * t + 7 * d) % 15
+    for slot, (b, t) in _slot_to_token(pt, ps, B, ctx).items():
+        val[slot] = [code(t, d) for d in range(D)]
+        ex[slot] = [125 + (t + k) % 5 for k in range(4)]
+    codes, exps = _pack_mx(val, ex)
+    R = B * nn
+    q = np.full((R, H, D), E4M3[0.0], np.uint8)
+    s = np.array([[[1.0, 2.0, -1.0, 0.5][(h + r) % 4] for h in range(H)] for r in range(R)])
+    for r in range(R):
+        for h in range(H):
+            q[r, h, (9 * h + 5 * r) % D] = E4M3[s[r, h]]
+    w = np.array([[(h % 5) - 2 + 0.25 * r for h in range(H)] for r in range(R)], np.float32)
+    L = O.paged_mqa_logits_mx(q, codes.reshape(P, ps, 64), exps.reshape(P, ps, 4), w, pt,
+                              np.array(ctx, np.int32), nn, ps)
+    mag = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for r in range(R):
+        b, j = divmod(r, nn)
+        for t in range(ctx[b] - (nn - 1 - j)):
+            acc = 0.0
+            for h in range(H):
+                d = (9 * h + 5 * r) % D
+                c = code(t, d)
+                k = (-1 if c & 8 else 1) * mag[c & 7] * 2.0 ** ((t + d // 32) % 5 - 2)
+                acc += float(w[r, h]) * max(s[r, h] * k, 0.0)
+            assert L[r, t] == np.float32(acc), (r, t)
