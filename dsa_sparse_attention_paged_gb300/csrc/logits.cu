@@ -52,7 +52,10 @@ constexpr int kMaxStages = 8;
 // two groups of a sub-tile take alternate stages.  Eight warps consume each
 // stage either way.
 __host__ __device__ constexpr int epi_warps(int nn) { return nn == 1 ? 8 : 16; }
-__host__ __device__ constexpr int threads_for(int nn) { return 64 + 32 * epi_warps(nn); }
+// The sparse pass adds a second producer warp (after the epilogue warps).
+__host__ __device__ constexpr int threads_for(int nn, bool sparse) {
+  return 64 + 32 * epi_warps(nn) + (sparse ? 32 : 0);
+}
 constexpr int kStageEpiWarps = 8;
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in per CTA
 
@@ -135,6 +138,17 @@ __device__ __forceinline__ int64_t eff_ctx(const LogitsArgs &a, int b) {
   if (c < 0) c = 0;
   if (c > cap) c = cap;
   return c;
+}
+
+// Pool row of physical block `raw` (pool slot / 8), or -1 for padding; an id
+// past the pool is flagged and skipped.
+__device__ __forceinline__ int phys_block_row(const LogitsArgs &a, int raw) {
+  if (raw == INT32_MAX || raw < 0) return -1;
+  if ((int64_t)raw * 8 + 8 > (int64_t)a.num_pages * a.page_size) {
+    set_status(a.status, DSA_DEV_BOUNDS);
+    return -1;
+  }
+  return raw * 8;
 }
 
 template <bool SPARSE>
@@ -316,7 +330,7 @@ __device__ __forceinline__ float head_sum(const uint32_t (&v)[32], float ks, con
 }
 
 template <int NN, bool SPARSE, int OUT, bool HIST>
-__global__ void __launch_bounds__(threads_for(NN), 1)
+__global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const LogitsArgs a) {
   // the dense pass waits for its predecessors at once; the sparse pass sets up
@@ -330,7 +344,7 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
   constexpr int HS = hist_slots_per_group(NN);
   constexpr int EW = epi_warps(NN);
   constexpr int NPAR = EW / kStageEpiWarps;  // groups sharing a sub-tile (alternate stages)
-  constexpr int kThr = threads_for(NN);
+  constexpr int kThr = threads_for(NN, SPARSE);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -442,15 +456,7 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
     // physical row of a slot (or -1 when nothing is loaded)
     auto to_row = [&](int raw, int unit) -> int {
       if (raw == kNone || unit < 0) return -1;
-      if (SPARSE && a.phys) {
-        // physical block: its 8 rows of the pool directly (no page-table read)
-        if (raw == INT32_MAX || raw < 0) return -1;
-        if ((int64_t)raw * 8 + 8 > (int64_t)a.num_pages * a.page_size) {
-          set_status(a.status, DSA_DEV_BOUNDS);
-          return -1;
-        }
-        return raw * 8;
-      }
+      if (SPARSE && a.phys) return phys_block_row(a, raw);  // no page-table read
       if (SPARSE) {
         const int b = unit / a.req_next_n;
         const int j = unit - b * a.req_next_n;
@@ -573,7 +579,8 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
         if (!SPARSE) mbar_arrive_expect_tx(KSF(kx), nload * (uint32_t)(blk_rows * 4));
       }
       __syncwarp();
-      if (row >= 0)
+      // sparse with physical blocks: blocks 16..31 go to the second producer
+      if (row >= 0 && !(sptab && lane >= 16))
         tma_load_2d_hint(kst + s * kStageK + lane * blk_rows * 128, &tm_k, FULL(s), 0, row, pol);
       if (SPARSE) {
         // kscale of the 32 blocks (32 bytes each) by 16-byte cp.async, two
@@ -661,6 +668,76 @@ __global__ void __launch_bounds__(threads_for(NN), 1)
       if (!ok && mmas > 0) {
         mma_commit(DRAIN);
         mbar_wait_drain(DRAIN, 0, a.wait_limit);
+      }
+    }
+    __syncwarp();
+  } else if (SPARSE && warp == 2 + EW) {
+    // ------------------------------------------------------------ second producer
+    // sparse with physical blocks: the K gathers of blocks 16..31 of every
+    // stage (lanes 16..31); warp 0 issues blocks 0..15, the kscale and the
+    // barrier accounting.  One TMA operation per 1 KiB block holds the
+    // issuing warp for about 80 cycles, so two warps share a stage's issue.
+    if (a.phys != nullptr) {
+      TileIter<SPARSE> it;
+      it.init(a, u_start, i_start);
+      const uint64_t pol = policy_evict_first();
+      int rq[8];  // this lane's block rows for the next stages, oldest first
+      int avail = 0;
+      bool ok = true;
+      Ring rs;
+      rs.init(S);
+      long long issued = 0;
+      for (long long n = 0; n < count && ok; ++n, it.next(a), rs.next()) {
+        if (avail == 0) {
+          const long long gbase = (long long)u_start * a.sparse_tpu + i_start + n;
+          TileIter<SPARSE> wt = it;
+          int raw[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            raw[jj] = INT32_MAX;
+            if (n + jj < count) {
+              int uu, ti;
+              if (NN == 1) {
+                const long long g = gbase + jj;
+                uu = (int)(g / a.sparse_tpu);
+                ti = (int)(g - (long long)uu * a.sparse_tpu);
+              } else {
+                uu = wt.u;
+                ti = wt.i;
+                wt.next(a);
+              }
+              const int blk = ti * 32 + lane;
+              if (lane >= 16 && blk < a.tab_stride)
+                raw[jj] = __ldg(&a.phys[(int64_t)uu * a.tab_stride + blk]);
+            }
+          }
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) rq[jj] = phys_block_row(a, raw[jj]);
+          avail = 8;
+        }
+        const int row = rq[0];
+#pragma unroll
+        for (int k = 0; k < 7; ++k) rq[k] = rq[k + 1];
+        --avail;
+        const int s = rs.idx;
+        if (lane == 0) ok = mbar_wait(EMPTY(s), rs.ph ^ 1, ctl);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (row >= 0)
+          tma_load_2d_hint(kst + s * kStageK + lane * 8 * 128, &tm_k, FULL(s), 0, row, pol);
+        ++issued;
+      }
+      if (!ok && lane == 0) {
+        // drain this warp's own copies still in flight
+        Ring ds = rs;
+        ds.idx = (int)(issued % S);
+        ds.ph = (uint32_t)((issued / S) & 1);
+        for (int back = 1; back <= S && back <= issued; ++back) {
+          int i2;
+          uint32_t p2;
+          ds.prev(back, i2, p2);
+          mbar_wait_drain(FULL(i2), p2, a.wait_limit);
+        }
       }
     }
     __syncwarp();
@@ -921,7 +998,7 @@ dsa_status_t launch_one(const CUtensorMap &tk, const CUtensorMap &tq, const Logi
   a.num_stages = L.stages;
   auto kfn = logits_kernel<NN, SPARSE, OUT, HIST>;
   if (!ensure_smem_attr(reinterpret_cast<const void *>(kfn), L.smem)) return DSA_ERR_CUDA;
-  return launch_pdl(kfn, dim3(grid), dim3(threads_for(NN)), (size_t)L.smem, st, tk, tq, a);
+  return launch_pdl(kfn, dim3(grid), dim3(threads_for(NN, SPARSE)), (size_t)L.smem, st, tk, tq, a);
 }
 
 }  // namespace
