@@ -209,20 +209,14 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared through the LSU path; with
-// src_bytes = 0 the destination is zero-filled and global memory is not read.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-
 // Arrive on `bar` once all cp.async copies issued so far by this thread have
 // landed (the barrier's expected count must include this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// 16-byte cp.async with an L2 cache policy.
+// 16-byte asynchronous copy global -> shared through the LSU path, with an
+// L2 cache policy.
 __device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void *src, uint64_t policy) {
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                "l"(policy)

@@ -10,13 +10,16 @@
 // [SG38944] SGLang PR #38944 "What this enables": the sparse logits score only
 // the published 8-token blocks.
 //
-// One persistent CTA per SM, ten warps, over a ring of 256-token stages
-// (32 KiB of K, 1 KiB of kscale each):
+// One persistent CTA per SM over a ring of 256-token stages (32 KiB of K,
+// 1 KiB of kscale each); 10 warps at next_n = 1, 18 at next_n > 1, one more
+// in the sparse pass:
 //   warp 0      producer: gathers the stage's K pages (or 8-token blocks)
 //               through the page table with one multi-lane TMA instruction,
-//               the matching kscale with one multi-lane bulk copy, and each
-//               request's Q tile and head weights into one of two buffers;
-//               page-table entries are read one group of stages ahead
+//               the matching kscale with one multi-lane bulk copy (sparse:
+//               16-byte cp.async), and each request's Q tile and head weights
+//               into one of two buffers; page-table entries are read one
+//               group of stages ahead.  In the sparse pass a second producer
+//               warp (the last one) issues half of each stage's block gathers.
 //   warp 1      allocates TMEM and issues tcgen05.mma (one thread): per stage
 //               two sub-tiles D[128 tokens x 32*next_n] = K[128 x 128] .
 //               Q[32*next_n x 128]^T, FP8 x FP8 -> FP32, into a TMEM pair
