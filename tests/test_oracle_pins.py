@@ -686,3 +686,30 @@ def test_mx_logits_nibble_order_and_block_exponents():
                 k = (-1 if c & 8 else 1) * mag[c & 7] * 2.0 ** ((t + d // 32) % 5 - 2)
                 acc += float(w[r, h]) * max(s[r, h] * k, 0.0)
             assert L[r, t] == np.float32(acc), (r, t)
+
+
+def test_mx_logits_equal_fp8_logits_when_block_exponents_agree():
+    """A key whose four block exponents equal e is the E4M3 key of the same
+    elements (E2M1 -> E4M3 by the exponent rebias) with kscale 2^(e - 127);
+    both oracles are exact in double up to the final rounding, so the MXFP4
+    logits equal the FP8 logits bit for bit (ties O10 to the pinned O2)."""
+    def rebias(c):
+        s, e, m = c >> 3, (c >> 1) & 3, c & 1
+        return (s << 7) | ((6 << 3) if (e == 0 and m) else 0 if e == 0 else ((e + 6) << 3) | (m << 2))
+    B, nn, ps, H, D = 2, 2, 64, 32, 128
+    ctx = [300, 170]
+    P, pt = _case(B, nn, ctx, ps, seed=21)
+    rng = np.random.default_rng(21)
+    val = rng.integers(0, 16, size=(P * ps, D))
+    e_slot = rng.integers(118, 136, size=P * ps)
+    codes, exps = _pack_mx(val, np.repeat(e_slot[:, None], 4, axis=1))
+    kv = np.vectorize(rebias)(val).astype(np.uint8).reshape(P, ps, D)
+    kscale = np.ldexp(1.0, e_slot - 127).astype(np.float32).reshape(P, ps)
+    finite = [c for c in range(256) if (c & 0x7F) != 0x7F]
+    q = rng.choice(finite, size=(B * nn, H, D)).astype(np.uint8)
+    w = rng.normal(0, 1, (B * nn, H)).astype(np.float32)
+    c = np.array(ctx, np.int32)
+    L_mx = O.paged_mqa_logits_mx(q, codes.reshape(P, ps, 64), exps.reshape(P, ps, 4), w, pt, c,
+                                 nn, ps)
+    L_f8 = O.paged_mqa_logits(q, kv, kscale, w, pt, c, nn, ps)
+    np.testing.assert_array_equal(L_mx.view(np.uint32), L_f8.view(np.uint32))
