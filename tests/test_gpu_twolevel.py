@@ -248,6 +248,8 @@ def _host_tables(ids, rl, nn, kb, page_table, ps):
     ([20003, 700, 40000], 256, 128, 3),
     ([12000, 5001], 512, 64, 4),
     ([3000, 2100], 16, 64, 4),
+    ([0, 2, 9, 5000], 16, 64, 4),     # empty request, rows with no or few keys
+    ([3000, 20000], 64, 128, 1),      # every unit a lone row
 ])
 def test_paired_sparse_pass(ctx, kb, ps, nn):
     """Row pairing: the paired sort gives the unpaired sort's tables bit for
