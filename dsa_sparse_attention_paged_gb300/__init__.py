@@ -369,9 +369,12 @@ def sparse_mqa_logits_paired(q, kv_pages, kscale, weights, page_table, context_l
     if out is None:
         dt = {OUT_F32: torch.float32, OUT_F16: torch.float16, OUT_BF16: torch.bfloat16}[out_dtype]
         out = torch.empty((R, kb * 8), dtype=dt, device=q.device)
-    for t, nm in ((uphys, "union_phys"), (upos, "union_pos"), (ulen, "union_len"),
-                  (valid_lens, "valid_lens")):
+    U = pair_units(B, next_n)
+    for t, nm, shp in ((uphys, "union_phys", (U, 2 * kb)), (upos, "union_pos", (U, 2 * kb)),
+                       (ulen, "union_len", (U,)), (valid_lens, "valid_lens", (R,))):
         _req(t, torch.int32, nm)
+        if tuple(t.shape) != shp or not t.is_contiguous():
+            raise ValueError(f"{nm}: expected a contiguous {shp} tensor")
     _check(lib.dsa_sparse_mqa_logits_paired(
         _p(q), _p(kv_pages), _p(kscale), _p(weights), _p(page_table), page_table.stride(0),
         _p(context_lens), B, next_n, H, D, ps, P, kb, _p(uphys), _p(upos), _p(ulen),
