@@ -567,6 +567,24 @@ void o_paged_mqa_logits_mx(const uint8_t *q, const uint8_t *k_codes, const uint8
     }
 }
 
+/* MXFP4 logits at an explicit list of (row, column) pairs (full-size sampled
+ * checks); row r belongs to request r / next_n. */
+void o_logits_at_mx(const uint8_t *q, const uint8_t *k_codes, const uint8_t *k_exp,
+                    const float *weights, const int32_t *page_table, int64_t pt_stride,
+                    int next_n, int H, int D, int page_size, const int64_t *rows,
+                    const int64_t *cols, int64_t n, float *out)
+{
+    double tab[256];
+    o_e4m3_table(tab);
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t r = rows[i];
+        int b = (int)(r / next_n);
+        int64_t slot = o_slot_of(page_table, pt_stride, b, cols[i], page_size);
+        out[i] = (float)o_logit_one_mx(q + r * H * D, k_codes + slot * (D / 2),
+                                       k_exp + slot * (D / 32), weights + r * H, H, D, tab);
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* O8: top-k over FP16 scores ([VL52696] "Why": select on FP16 score bits).
  * Positions i < valid_len[r] take part unless NaN; order by the FP16 value,

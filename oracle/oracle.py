@@ -86,6 +86,7 @@ def _load():
     lib.o_ue8m0.argtypes = [ctypes.c_uint8]
     lib.o_paged_mqa_logits_mx.argtypes = [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, P,
                                           i64]
+    lib.o_logits_at_mx.argtypes = [P, P, P, P, P, i64, i32, i32, i32, i32, P, P, i64, P]
     _lib = lib
     return lib
 
@@ -231,6 +232,24 @@ def paged_mqa_logits_mx(q, k_codes, k_exp, weights, page_table, context_lens, ne
     _load().o_paged_mqa_logits_mx(_ptr(q), _ptr(k_codes), _ptr(k_exp), _ptr(weights),
                                   _ptr(page_table), page_table.shape[1], _ptr(context_lens), B,
                                   next_n, H, D, page_size, _ptr(out), out.shape[1])
+    return out
+
+
+def logits_at_mx(q, k_codes, k_exp, weights, page_table, next_n, page_size, rows,
+                 cols) -> np.ndarray:
+    """MXFP4-key logits at (rows[i], cols[i]) pairs, one by one."""
+    q = _c(q, np.uint8)
+    k_codes = _c(k_codes, np.uint8)
+    k_exp = _c(k_exp, np.uint8)
+    weights = _c(weights, np.float32)
+    page_table = _c(page_table, np.int32)
+    rows = _c(rows, np.int64)
+    cols = _c(cols, np.int64)
+    R, H, D = q.shape
+    out = np.empty(rows.shape[0], np.float32)
+    _load().o_logits_at_mx(_ptr(q), _ptr(k_codes), _ptr(k_exp), _ptr(weights),
+                           _ptr(page_table), page_table.shape[1], next_n, H, D, page_size,
+                           _ptr(rows), _ptr(cols), rows.shape[0], _ptr(out))
     return out
 
 

@@ -12,6 +12,9 @@ Layouts (all C-contiguous numpy arrays):
   weights      f32    [R][H]        per-row head weights
   page_table   int32  [B][maxp]     logical page -> physical page, -1 past the end
   context_lens int32  [B]           keys of the request's last token
+  with key_format "mxfp4" also:
+  k_codes      uint8  [P][ps][D/2]  E2M1 codes, two per byte (even dimension low)
+  k_exp        uint8  [P][ps][D/32] UE8M0 exponents, one per 32 dimensions
 
 The five named workloads follow the pages' shapes (DeepGEMM PR #94 "Producer
 cost" cells; SGLang PR #38944 two-level path at bs=8, 128K with 128-slot
@@ -23,6 +26,10 @@ pages), with seed 20260000 + index.  Score distributions:
   intexact q, K in {-2..2} (mostly 0), kscale in {0.5, 1}, w in {+-0.5, +-1, +-2}:
            every partial sum is exactly representable, so any summation
            order gives the same float (bitwise comparisons are meaningful)
+MXFP4 keys (key_format "mxfp4"): uniform E2M1 codes and block exponents
+uniform in [125, 129] (scales of 1/4 .. 4, where block maxima of unit-variance
+keys put them), drawn after every other input so the FP8 inputs of a seed stay
+the same.
 """
 from __future__ import annotations
 
@@ -50,6 +57,7 @@ class Workload:
     D: int = D_DEFAULT
     spare_pages: int = 3  # unreferenced pool pages, so a wrong gather shows
     extra: dict = field(default_factory=dict)
+    key_format: str = "fp8"  # or "mxfp4": also draw E2M1 codes + UE8M0 exponents
 
     @property
     def R(self) -> int:
@@ -143,10 +151,19 @@ def generate(w: Workload) -> dict:
             weights *= 8.0
         elif w.dist != "normal":
             raise ValueError(w.dist)
-    return dict(q=np.ascontiguousarray(q), kv=np.ascontiguousarray(kv),
-                kscale=np.ascontiguousarray(kscale), weights=np.ascontiguousarray(weights),
-                page_table=page_table, context_lens=ctx, next_n=nn, page_size=ps,
-                num_pages=P, H=H, D=D)
+    out = dict(q=np.ascontiguousarray(q), kv=np.ascontiguousarray(kv),
+               kscale=np.ascontiguousarray(kscale), weights=np.ascontiguousarray(weights),
+               page_table=page_table, context_lens=ctx, next_n=nn, page_size=ps,
+               num_pages=P, H=H, D=D)
+    if w.key_format == "mxfp4":
+        nib = torch.randint(0, 16, (P, ps, D), generator=g, dtype=torch.int32).numpy()
+        out["k_codes"] = np.ascontiguousarray((nib[..., 0::2] | (nib[..., 1::2] << 4))
+                                              .astype(np.uint8))
+        out["k_exp"] = torch.randint(125, 130, (P, ps, D // 32), generator=g,
+                                     dtype=torch.int32).numpy().astype(np.uint8)
+    elif w.key_format != "fp8":
+        raise ValueError(w.key_format)
+    return out
 
 
 def random_logits(R, n, seed, dist="normal", stride=None) -> np.ndarray:

@@ -713,3 +713,25 @@ def test_mx_logits_equal_fp8_logits_when_block_exponents_agree():
                                  nn, ps)
     L_f8 = O.paged_mqa_logits(q, kv, kscale, w, pt, c, nn, ps)
     np.testing.assert_array_equal(L_mx.view(np.uint32), L_f8.view(np.uint32))
+
+
+def test_mx_logits_at_matches_dense_mx_logits():
+    """The sampled MXFP4 logits (used for full-size checks) equal the dense
+    ones at the same (row, column), on a seeded MXFP4 workload."""
+    import synthetic as S
+    w = S.Workload("mx small", 3, 2, [700, 65, 1300], 64, "normal", 77, key_format="mxfp4")
+    c = S.generate(w)
+    L = O.paged_mqa_logits_mx(c["q"], c["k_codes"], c["k_exp"], c["weights"], c["page_table"],
+                              c["context_lens"], 2, 64)
+    rl = O.row_lens(c["context_lens"], 2)
+    rng = np.random.default_rng(3)
+    rows = rng.integers(0, 6, 500)
+    cols = (rng.random(500) * rl[rows]).astype(np.int64)
+    got = O.logits_at_mx(c["q"], c["k_codes"], c["k_exp"], c["weights"], c["page_table"], 2, 64,
+                         rows, cols)
+    np.testing.assert_array_equal(got, L[rows, cols])
+    assert c["k_codes"].shape == (c["num_pages"], 64, 64) and c["k_exp"].shape[-1] == 4
+    # the FP8 inputs of the seed do not move when MXFP4 keys are drawn too
+    f8 = S.generate(S.Workload("mx small", 3, 2, [700, 65, 1300], 64, "normal", 77))
+    for k in ("q", "kv", "kscale", "weights", "page_table"):
+        np.testing.assert_array_equal(f8[k], c[k])
