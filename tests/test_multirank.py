@@ -51,3 +51,29 @@ def test_whole_job_rate_is_weak_scaling():
     assert bench.whole_job_rate(1000, 1, 10, 2.0) == 5000.0
     assert bench.whole_job_rate(1000, 4, 10, 2.0) == 20000.0
     assert bench.max_over_ranks(3.5, None, "cpu") == 3.5
+
+
+def test_reference_arm_prints_the_contract_line():
+    """bench.py --impl reference (the oracle on the host cores) prints one JSON
+    line with the contract's keys, its e2e equal to its own value with no
+    host-device copies, and a cpu_baseline describing the run."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    p = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
+                       timeout=600, cwd=root)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [ln for ln in p.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["n_gpus"] == 1
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert "workload" in d["config"]
