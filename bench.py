@@ -32,6 +32,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "indexer decode keys scored/s and HBM GB/s (% of peak); top-2048 rows/s"
 KEY_BYTES = 132  # 128 FP8 bytes of K + 4 bytes of kscale per key
+NOMINAL_GBS = 8000.0  # the ~8 TB/s nominal HBM3e figure the target is stated against
+PER_WORKLOADS = ("c0", "c1", "c3", "c3u", "c4")
 
 
 def parse():
@@ -43,6 +45,8 @@ def parse():
     p.add_argument("--workload", default="c2")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0)
+    p.add_argument("--no-per-workload", action="store_true",
+                   help="skip the per-workload table (c0, c1, c3, c3u, c4)")
     return p.parse_args()
 
 
@@ -78,16 +82,14 @@ def peaks():
 
 
 def traffic_record(kernel_src):
-    """Per-launch DRAM bytes of the logits kernel from the committed ncu summary,
-    valid only while the kernel source is unchanged (sha256 recorded there)."""
-    path = os.path.join(ROOT, "profiles", "logits_fused_hist_c2.md")
+    """Per-launch DRAM bytes of the logits kernel from the committed ncu record
+    (profiles/logits_fused_hist_c2.json), valid only while the kernel source
+    is unchanged (its sha256 is stored beside the number); None otherwise."""
+    path = os.path.join(ROOT, "profiles", "logits_fused_hist_c2.json")
     try:
         sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-        rec = {}
-        for line in open(path):
-            if ":" in line and line.strip().startswith("- "):
-                k, v = line.strip()[2:].split(":", 1)
-                rec[k.strip()] = v.strip().strip("`")
+        with open(path) as f:
+            rec = json.load(f)
         if rec.get("source_sha256") == sha:
             return float(rec["dram_bytes_per_launch"])
     except Exception:
@@ -201,6 +203,67 @@ def run_reference(args, ws_, rank):
             "e2e": {"value": v, "unit": "keys/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def measure_workload(name, dev, steps=200, warmup=5):
+    """Per-workload timings of the same step (outside the headline's timed
+    region): the logits launch alone (CUDA events around it), the eager step
+    (events around the whole step only) and the CUDA-graph replay."""
+    import torch
+    import synthetic as S
+    from dsa_sparse_attention_paged_gb300.pipeline import DecodePlan
+    w = S.named(name)
+    case = S.generate(w)
+    nn = w.next_n
+    d = {k: (torch.from_numpy(v).to(dev) if isinstance(v, np.ndarray) else v)
+         for k, v in case.items()}
+    plan = DecodePlan(w.B, nn, max(w.context_lens), w.page_size, k=2048, kb=512,
+                      two_level=True, device=dev)
+    inputs = (d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"], d["context_lens"])
+    ctx = np.asarray(w.context_lens, dtype=np.int64)
+    keys = int((ctx[:, None] - (nn - 1 - np.arange(nn))[None, :]).sum())
+    kv_bytes = int(ctx.sum()) * KEY_BYTES
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    for _ in range(warmup):
+        plan.step(*inputs)
+    torch.cuda.synchronize()
+    steps_ev = [ev() for _ in range(steps)]
+    for a, b in steps_ev:
+        a.record()
+        plan.step(*inputs)
+        b.record()
+    torch.cuda.synchronize()
+    step_us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in steps_ev)
+    lg_ev = [{"logits": ev()} for _ in range(steps)]
+    for e in lg_ev:
+        plan.step(*inputs, events=e)
+    torch.cuda.synchronize()
+    lg_us = 1e3 * statistics.median(e["logits"][0].elapsed_time(e["logits"][1]) for e in lg_ev)
+    plan.capture(*inputs)
+    plan.replay()
+    torch.cuda.synchronize()
+    gs, ge = ev()
+    gs.record()
+    for _ in range(steps):
+        plan.replay()
+    ge.record()
+    torch.cuda.synchronize()
+    graph_us = 1e3 * gs.elapsed_time(ge) / steps
+    if plan.ws.status() != 0:
+        raise RuntimeError(f"{name}: device status {plan.ws.status():#x}")
+    peak, kind = peaks()
+    gbs = kv_bytes / (lg_us * 1e-6) / 1e9
+    out = {"workload": w.name, "keys_per_step": keys, "kstream_bytes": kv_bytes,
+           "logits_us": lg_us, "kstream_gbs": gbs, "frac_of_measured_peak": gbs / peak,
+           "frac_of_8tbs_nominal": gbs / NOMINAL_GBS, "step_us_eager": step_us,
+           "step_us_graph": graph_us, "keys_per_s_eager": keys / (step_us * 1e-6),
+           "keys_per_s_graph": keys / (graph_us * 1e-6)}
+    del plan, d
+    torch.cuda.empty_cache()
+    return out
 
 
 def cpu_baseline(case, w, budget):
@@ -359,6 +422,11 @@ def main():
     cb = None
     if not args.no_cpu_baseline:
         cb = cpu_baseline(case, w, args.cpu_budget)
+    per_workload = None
+    if not args.no_per_workload:
+        per_workload = {nm: measure_workload(nm, dev) for nm in PER_WORKLOADS
+                        if nm != args.workload}
+    kstream_gbs = kv_bytes / (lg_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -370,6 +438,9 @@ def main():
                    "l2": (f"not flushed: inputs larger than L2 (each step streams "
                           f"{kv_bytes / 1e6:.0f} MB of K cache and scales, L2 129 MB)")},
         "hbm_gbs_logits": achieved,
+        "kstream_gbs": kstream_gbs,
+        "kstream_frac_of_measured_peak": kstream_gbs / peak,
+        "kstream_frac_of_8tbs_nominal": kstream_gbs / NOMINAL_GBS,
         "top2048_rows_per_s": world * 2 * w.R * K / t_total,
         "logits_us": 1e3 * lg_ms,
         "stage_us": stage_us,
@@ -387,6 +458,7 @@ def main():
                 "ms_per_step": 1e3 * e2e_s / Ke, "steps": Ke},
         "gpu_launches": plan.launches_per_step * K,
         "clocks": clocks,
+        "per_workload": per_workload,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

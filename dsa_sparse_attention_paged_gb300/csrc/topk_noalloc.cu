@@ -4,8 +4,9 @@
 //
 // The scratch is a file-scope __device__ array laid out exactly like a caller
 // workspace sized for DSA_NOALLOC_MAX_ROWS rows; the regular select launcher
-// runs on it unchanged.  Every GPU that loads the library keeps this array
-// until the process exits.
+// runs on it unchanged, so rows of at most 131072 scores take the one-launch
+// cluster select and longer rows the multi-CTA select, as with a workspace.
+// Every GPU that loads the library keeps this array until the process exits.
 #include <mutex>
 
 #include "dsa_device.cuh"
@@ -35,9 +36,13 @@ void *g_scratch_addr[kMaxDevices] = {};
 void *scratch_on_current_device(dsa_status_t *err) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  if (e != cudaSuccess) {
     record_cuda_error(e);
     *err = DSA_ERR_CUDA;
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {  // beyond the address table: not a CUDA failure
+    *err = DSA_ERR_UNSUPPORTED;
     return nullptr;
   }
   std::lock_guard<std::mutex> lk(g_mu);
@@ -77,9 +82,13 @@ extern "C" int32_t dsa_coarse_hist_topk_noalloc(const float *logits, int64_t str
   void *ws = scratch_on_current_device(&err);
   if (!ws) return err;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The array keeps whatever the previous call left: clear the status word,
-  // the counters and both histograms of the rows this call uses (the
-  // candidate buffer needs no clearing).
+  // The array keeps whatever the previous call left.  The kernels leave the
+  // counters and histograms they use at zero when they finish, but a call
+  // that never ran to the end (a wait that ran out, a launch that failed
+  // after an earlier kernel of the call) would leave them dirty for every
+  // later caller of the shared array.  So each call clears the status word,
+  // the counters and both histograms of the rows it uses itself (three small
+  // memsets, ~1.3 MB at 64 rows; the candidate buffer needs no clearing).
   char *base = static_cast<char *>(ws);
   const int64_t rows = DSA_NOALLOC_MAX_ROWS;
   cudaError_t e = cudaMemsetAsync(base, 0, WsLayout::counters_off() + (size_t)R * 16, st);
@@ -105,6 +114,5 @@ extern "C" int32_t dsa_coarse_hist_topk_noalloc(const float *logits, int64_t str
   c.fallback_flags = fallback_flags;
   c.workspace = ws;
   c.ws_rows = DSA_NOALLOC_MAX_ROWS;
-  c.allow_cluster = false;  // the scratch-based kernels, whatever the row length
   return run_topk(c, st);
 }

@@ -23,7 +23,9 @@
  *     says otherwise; the library never frees or retains them past the call.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream).  The library allocates no device memory: scratch space comes
- *     from a caller-owned workspace sized by dsa_workspace_size().
+ *     from a caller-owned workspace sized by dsa_workspace_size().  The one
+ *     exception is dsa_coarse_hist_topk_noalloc, whose scratch is a static
+ *     device array of the library (about 5.3 MB per GPU that loads it).
  *   - Host-side argument checks run before anything is launched and return a
  *     status synchronously; nothing is launched when the status is not DSA_OK.
  *   - Problems only the device can see (a page id outside the pool, a context
@@ -256,7 +258,8 @@ int32_t dsa_coarse_hist_topk_batch_launches(const dsa_topk_problem *problems, in
  *     (cudaGetSymbolAddress) with that device current; make this first call
  *     before any stream capture.
  *   - Every call shares the one array and clears the parts that must start at
- *     zero itself.  Calls whose kernels overlap on the GPU (other streams,
+ *     zero itself (the kernels leave them at zero too, but a call that did
+ *     not run to the end would otherwise leave them dirty for the next).  Calls whose kernels overlap on the GPU (other streams,
  *     other host threads) race on it and give wrong results: serialise them.
  *   - Device-side anomaly bits of this variant stay in the library's array and
  *     are not reported; fallback_flags still reports per-row fallbacks. */

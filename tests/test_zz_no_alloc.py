@@ -76,3 +76,54 @@ def test_noalloc_rejects_rows_beyond_its_maximum():
         ctypes.c_void_p(x.data_ptr()), 64, ctypes.c_void_p(c.data_ptr()), 1, 1, n, None, 0, 8,
         ctypes.c_void_p(o.data_ptr()), None, None)
     assert st == 2  # DSA_ERR_UNSUPPORTED
+
+
+def _overcap_rows(R, n, rng):
+    """Rows whose threshold bin holds more than the candidate capacity: many
+    equal scores (the exact whole-row fallback, flag 2), many distinct scores
+    inside one coarse bin (the fine histogram, flag 0), plain rows, short
+    rows (k or fewer scores: every score taken)."""
+    x = rng.uniform(-60.0, 0.0, (R, n)).astype(np.float32)
+    for r in range(R):
+        big = rng.permutation(n)[:1000 + 100 * r]
+        x[r, big] = rng.uniform(100.0, 200.0, big.size).astype(np.float32)
+        rest = np.setdiff1d(np.arange(n), big)
+        pos = rng.permutation(rest)[:20000]
+        if r % 3 == 0:
+            x[r, pos] = 5.0                                    # one key: ties
+        elif r % 3 == 1:
+            x[r, pos] = rng.uniform(5.0, 5.2, pos.size).astype(np.float32)  # one coarse bin
+    return x
+
+
+def test_noalloc_over_capacity_bins_then_fewer_rows():
+    import dsa_sparse_attention_paged_gb300 as D
+    from oracle import oracle as O
+    rng = np.random.default_rng(99)
+    R, n, k = 8, 40000, 2048
+    x = _overcap_rows(R, n, rng)
+    ctx_h = np.array([40000, 40000, 40000, 30000, 2000, 40000, 35000, 1], np.int32)
+    hist_h = O.histogram(x, ctx_h.astype(np.int64))
+    ref = O.topk(x, ctx_h.astype(np.int64), k)
+    L = torch.from_numpy(x).cuda()
+    ctx = torch.from_numpy(ctx_h).cuda()
+    hist = torch.from_numpy(hist_h).cuda()
+    ws = D.Workspace(R)
+    wflags = torch.full((R,), -1, dtype=torch.int32, device="cuda")
+    wout = D.coarse_hist_topk(L, ctx, 1, k, ws, histogram=hist, fallback_flags=wflags)
+    torch.cuda.synchronize()
+    wf = wflags.cpu().numpy()
+    assert (wf[[0, 3, 6]] == 2).all() and (wf[[1, 4, 7]] == 0).all(), wf
+    np.testing.assert_array_equal(_sorted(wout), np.sort(ref, axis=1))
+    for rows in (R, 2):  # a call on fewer rows after one on more: stale rows stay out
+        flags = torch.full((R,), -1, dtype=torch.int32, device="cuda")
+        out = torch.full((R, k), -7, dtype=torch.int32, device="cuda")
+        D.coarse_hist_topk_noalloc(L, ctx, 1, k, histogram=hist, out=out, fallback_flags=flags,
+                                   R=rows)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(flags.cpu().numpy()[:rows], wf[:rows])
+        assert (flags.cpu().numpy()[rows:] == -1).all()
+        np.testing.assert_array_equal(_sorted(out[:rows]), np.sort(ref[:rows], axis=1))
+        assert (out[rows:].cpu().numpy() == -7).all()
+        # the caller's histogram is read, not changed, without reset_histogram
+        np.testing.assert_array_equal(hist.cpu().numpy(), hist_h)
