@@ -706,17 +706,27 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
 // holding its share of the row as order keys in shared memory (the row is
 // read from memory once):
 //   1. threshold bin T from the caller's histogram (worked out while the row
-//      loads, behind an early cluster-barrier arrive), or from one the CTAs
-//      merge in the workspace (global reductions, resolved in L2)
+//      loads), or from one the CTAs merge in the workspace (global
+//      reductions, resolved in L2, one cluster barrier)
 //   2. the exact key range [loT, hiT] of bin T (coarse bins descend with the
-//      key, so every bin is one key range), found by a warp-parallel search
+//      key, so every bin is one key range), in closed form
 //   3. when bin T holds more than kClDirect scores: a fine histogram over a
 //      window of bin T's key range, merged in the workspace the same way, and
 //      the fine threshold bin S
-//   4. every CTA classifies its scores, reserves its output and candidate
-//      ranges with one atomic per counter on CTA 0, and writes them
+//   4. every CTA classifies its scores against the emit threshold E (emit:
+//      key > E; candidate: C <= key <= E), reserves output and candidate
+//      ranges with one DSMEM atomic per warp on CTA 0, and writes them
 //   5. CTA 0 checks the counts and ranks the candidates (or refines them, or
 //      runs the exact whole-row fallback)
+// With a block output the top-bk blocks of 8 scores by block maximum come out
+// of the same pass without a histogram of the maxima: a block whose maximum
+// is above E holds an emitted score, and every block at or below E ranks
+// below every block above it, so when at least bk blocks (the newest one
+// counted as +inf) lie above E, the top bk of the row are the top bk of those
+// -- at most k blocks, collected in CTA 1's shared memory and selected
+// exactly there.  Rows with fewer such blocks (scores crowded into few
+// blocks) take the exact whole-row select over every block maximum, also on
+// CTA 1.
 // Short rows (stride <= kClChunk): each CTA of a cluster takes one row alone
 // (the same steps inside one CTA, no cluster barrier), eight rows a cluster.
 // Every cluster-wide decision is taken from data all CTAs share, so all CTAs
@@ -736,22 +746,26 @@ constexpr uint32_t kFineWindow = 1u << 26;       // keys one fine histogram span
 static_assert(kClThreads == kSelThreads, "block scans assume kSelThreads threads");
 
 constexpr int kClBlk = kClChunk / 8;             // block maxima per CTA
-constexpr int kClCandHalf = DSA_CAND_CAP / 2;    // candidate slots per select with block output
+constexpr int kClBPer = kClBlk / kClThreads;     // block maxima per thread
+constexpr int kBSel = DSA_MAX_TOPK;              // block candidates kept (blocks above E)
+constexpr int kClGroups = 4;                     // bulk-copy groups of a CTA's scores
+constexpr int kClGroupVec = kClVec / kClGroups;  // float4 slots per thread in a group
 
 struct ClSmem {
   uint4 keys[kClVec * kClThreads];      // keys[q * kClThreads + tid] = slots 4q..4q+3 of tid
   int hist[DSA_NUM_BINS];               // local coarse / fine histogram, then the row's
   unsigned long long cand[kClDirect];   // the row's first candidates (CTA 0 / local CTA)
   uint32_t bkey[kClBlk];                // block maxima keys of this CTA's positions
-  int bhist[DSA_NUM_BINS];              // local / merged histogram of the block maxima
-  unsigned long long bcand[kClDirect];  // block select: first candidates (CTA 1 / local CTA)
-  int ctr[8];                           // CTA 0: emitted, candidates, bin-T count; CTA 1: same
-                                        // for the block select (ctr[4..6])
-  uint32_t bmm[8];                      // (~min, max) of the maxima in each wide bin
-  uint32_t red[4];                      // range reductions
+  unsigned long long bsel[kBSel];       // block candidates (CTA 1 / local CTA)
+  int fmerge[kClFine];                  // CTA 0: the cluster's fine histogram of bin T
+  unsigned long long ctr;               // CTA 0: emitted | candidates << 32
+  int bctr;                             // CTA 1: block candidates (or emitted blocks)
+  unsigned long long bar[1 + kClGroups];  // bulk copies landed: histogram row, score groups
 };
 static_assert(sizeof(uint4) * kClVec * kClThreads >= sizeof(unsigned long long) * DSA_CAND_CAP,
               "the refine reuses the key buffer for the candidates");
+static_assert(sizeof(uint4) * kClVec * kClThreads >= sizeof(uint32_t) * (kClRow / 8),
+              "the whole-row block select keeps every block maximum in the key buffer");
 
 struct ClProb {
   const float *logits;
@@ -851,46 +865,6 @@ __device__ __forceinline__ void cl_fine_window(int T, uint32_t loT, uint32_t hiT
   while ((span1 >> fshift) >= (uint32_t)kClFine) ++fshift;
 }
 
-// Index of the wide coarse bins (0: x >= 223, 1: +tiny, 2: -tiny, 3: x <= -223).
-__device__ __forceinline__ int wide_bin_idx(int T) {
-  return T == 0 ? 0 : T == 511 ? 1 : T == 512 ? 2 : T == 1023 ? 3 : -1;
-}
-
-// Workspace slots (inside the row's fine-histogram area) where every CTA of a
-// cluster publishes the key range its scores take in a wide bin: (~min, max),
-// both 0 when none; CTA r writes only its own slots.
-constexpr int kSlotD = 3 * kClFine;      // score select: 2 per CTA
-constexpr int kSlotB = kSlotD + 2 * kCl; // block select: 8 per CTA (4 wide bins)
-static_assert(kSlotB + 8 * kCl <= kFineBins, "slots fit the row's fine area");
-
-// (~min, max) of this CTA's keys inside [lo, hi] into red[0], red[1] (0 when
-// none); every thread calls it; ends with a __syncthreads.
-__device__ __noinline__ void cl_range_in(const uint4 *keys, int vq, uint32_t lo, uint32_t hi, uint32_t *red) {
-  if (threadIdx.x == 0) {
-    red[0] = 0;
-    red[1] = 0;
-  }
-  __syncthreads();
-  uint32_t nmin = 0, mx = 0;
-  for (int q = 0; q < vq; ++q) {
-    const uint4 k4 = keys[q * kClThreads + threadIdx.x];
-    const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (kv[j] >= lo && kv[j] <= hi) {
-        nmin = max(nmin, ~kv[j]);
-        mx = max(mx, kv[j]);
-      }
-  }
-  nmin = __reduce_max_sync(0xffffffffu, nmin);
-  mx = __reduce_max_sync(0xffffffffu, mx);
-  if ((threadIdx.x & 31) == 0 && mx) {
-    atomicMax(&red[0], nmin);
-    atomicMax(&red[1], mx);
-  }
-  __syncthreads();
-}
-
 __device__ __forceinline__ int cl_fine_idx(uint32_t kk, uint32_t flo, int fshift) {
   const uint32_t off = kk > flo ? kk - flo : 0u;
   return (kClFine - 1) - (int)min((uint32_t)(kClFine - 1), off >> fshift);
@@ -947,13 +921,6 @@ __device__ __forceinline__ uint32_t key_or_zero(float x) {
   const uint32_t u = __float_as_uint(x);
   const uint32_t k = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
   return isnan(x) ? 0u : k;
-}
-
-__device__ __forceinline__ void cl_store_keys(const float4 (&v)[kClVec], uint4 *keys) {
-#pragma unroll
-  for (int q = 0; q < kClVec; ++q)
-    keys[q * kClThreads + threadIdx.x] = make_uint4(key_or_zero(v[q].x), key_or_zero(v[q].y),
-                                                    key_or_zero(v[q].z), key_or_zero(v[q].w));
 }
 
 // Key range [C, E] of fine bin S of bin T under cl_fine_idx's clamped map
@@ -1023,34 +990,104 @@ __device__ __forceinline__ void cl_write(unsigned long long kinds, const uint4 *
   }
 }
 
-// Last step of a row, run by one CTA once every emit and candidate of the row
-// is in place: check the counts, then rank or refine the candidates, or run
-// the exact whole-row fallback.  Returns the fallback flag.
-// Order key of the maximum of block b (scores 8b .. 8b+7) of a row of n
-// scores: NaN scores do not count, a block with no other score has key 0
-// (never selected), and the newest block (the last one) counts as +inf.
-__device__ __forceinline__ uint32_t block_max_key(const float *row, int64_t n, int64_t b) {
-  if (b == (n + 7) / 8 - 1) return kKeyPosInf;
-  uint32_t m = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int64_t t = 8 * b + j;
-    if (t < n) {
-      const float x = row[t];
-      if (!isnan(x)) m = max(m, f32_order_key(x));
+// Exact top-m of the n unique items it[0..n) (order key << 32 | ~id, so
+// equal keys rank by lower id), written as ids to out[0..m) in any order;
+// every item's key lies in [lo, hi] and n >= m.  Level by level a 1024-bin
+// histogram of the keys still in play -- the coarse score bins at the first
+// level when `coarse`, else an even split of [lo, hi] -- gives the threshold
+// bin: items above it are emitted, the bin's items stay in play with [lo, hi]
+// narrowed to the bin.  A threshold bin of at most kClRank items (or the one
+// left after the third level) is ranked pairwise.  Run by the whole block;
+// scratch: h[1024], two item buffers of n (not aliasing `it`).
+__device__ __noinline__ void local_hist_select(const unsigned long long *it, int n, int m,
+                                               int32_t *out, bool coarse, uint32_t lo, uint32_t hi,
+                                               int *h, unsigned long long *bufA,
+                                               unsigned long long *bufB, int *sm_scan,
+                                               int *sm_misc) {
+  const unsigned long long *src = it;
+  int ns = n, base = 0, need = m;
+  for (int level = 0;; ++level) {
+    int shift = 0;
+    if (!coarse)
+      while (((hi - lo) >> shift) >= (uint32_t)kClFine) ++shift;
+    for (int i = threadIdx.x; i < kClFine; i += kClThreads) h[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < ns; i += kClThreads) {
+      const uint32_t k32 = (uint32_t)(src[i] >> 32);
+      if (k32 >= lo && k32 <= hi)
+        atomicAdd(&h[coarse ? coarse_bin_of_key(k32) : cl_fine_idx(k32, lo, shift)], 1);
     }
+    __syncthreads();
+    threshold_from_hist<kClFine>(h, need, sm_scan, sm_misc);
+    const int T = sm_misc[0];
+    uint32_t C, E;
+    if (T >= kClFine) {  // fewer than `need` in play (inconsistent input): take them all
+      C = lo;
+      E = hi;
+    } else if (coarse) {
+      bin_key_range(T, C, E);
+      C = max(C, lo);
+      E = min(E, hi);
+    } else {
+      fine_bin_keys(lo, hi, lo, shift, T, C, E);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      sm_misc[4] = 0;
+      sm_misc[5] = 0;
+    }
+    __syncthreads();
+    // emit the items above the threshold bin, gather those in it
+    unsigned long long *dst = (level & 1) ? bufB : bufA;
+    for (int i = threadIdx.x; i < ns; i += kClThreads) {
+      const unsigned long long v = src[i];
+      const uint32_t k32 = (uint32_t)(v >> 32);
+      if (k32 > E && k32 <= hi) {
+        const int p = base + atomicAdd(&sm_misc[4], 1);
+        if (p < m) out[p] = (int32_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
+      } else if (k32 >= C && k32 <= E) {
+        dst[atomicAdd(&sm_misc[5], 1)] = v;
+      }
+    }
+    __syncthreads();
+    const int emitted = sm_misc[4], inbin = sm_misc[5];
+    base += emitted;
+    need -= emitted;
+    __syncthreads();
+    if (T >= kClFine) need = min(need, inbin);
+    if (need <= 0) break;
+    if (inbin <= kClRank || level == 2 || T >= kClFine || C == E) {
+      // unique keys: each item's rank is the number of larger items
+      for (int i = threadIdx.x; i < inbin; i += kClThreads) {
+        const unsigned long long v = dst[i];
+        int rk = 0;
+        for (int j = 0; j < inbin; ++j) rk += dst[j] > v;
+        if (rk < need) out[base + rk] = (int32_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
+      }
+      __syncthreads();
+      break;
+    }
+    src = dst;
+    ns = inbin;
+    lo = C;
+    hi = E;
+    coarse = false;
   }
-  return m;
 }
 
-// Elements are the row's scores, or (maxima) the maxima of its blocks of 8
-// scores: n elements, n_scores scores; `cap` candidate slots.
-__device__ __noinline__ int cl_finish(const float *row, int64_t n, bool maxima, int64_t n_scores, int k,
-                         int32_t *outr, bool take_all, int T, int above, int histT, bool fine,
-                         int S, int above1, int fineS, int emitted, int ncand, int cap,
-                         const unsigned long long *cand, const unsigned long long *cr,
-                         unsigned long long *scratch, int *sm_h, int *sm_scan, int *sm_misc,
-                         unsigned long long *sm_u64) {
+// Last step of the score select, run by one CTA once every emit and
+// candidate of the row is in place: check the counts, then rank or refine
+// the candidates, or run the exact whole-row fallback.  Returns the fallback
+// flag (0 histogram path, 1 stale histogram, 2 over capacity).
+// The candidates' keys lie in [C, E] (bin T, or its fine bin S).
+__device__ __noinline__ int cl_finish(const float *row, int64_t n, int k, int32_t *outr,
+                                      bool take_all, int T, int above, int histT, bool fine,
+                                      int S, int above1, int fineS, int emitted, int ncand,
+                                      int cap, uint32_t C, uint32_t E,
+                                      const unsigned long long *cand,
+                                      const unsigned long long *cr, unsigned long long *scratch,
+                                      int *hist, int *sm_h, int *sm_scan, int *sm_misc,
+                                      unsigned long long *sm_u64) {
   const bool sane = (T < DSA_NUM_BINS) ? (above >= 0 && above < k && histT >= k - above)
                                        : (above >= 0 && above < k);
   int flag = 0, base_out = 0, m = 0;
@@ -1074,9 +1111,7 @@ __device__ __noinline__ int cl_finish(const float *row, int64_t n, bool maxima, 
   if (flag == 0) {
     if (m <= 0) {
       for (int i = emitted + threadIdx.x; i < k; i += kClThreads) outr[i] = -1;
-    } else if (ncand > kClRank && ncand <= kClDirect) {
-      refine_candidates(cand, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
-    } else if (ncand <= kClDirect) {
+    } else if (ncand <= kClRank) {
       // candidate keys are unique (the column is part of the key): each
       // thread ranks one against all the others (quadratic: few candidates)
       if (threadIdx.x < ncand) {
@@ -1085,16 +1120,19 @@ __device__ __noinline__ int cl_finish(const float *row, int64_t n, bool maxima, 
         for (int j = 0; j < ncand; ++j) rk += cand[j] > v;
         if (rk < m) outr[base_out + rk] = (int32_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
       }
+    } else if (ncand <= kClDirect) {
+      local_hist_select(cand, ncand, m, outr + base_out, false, C, E, hist, scratch,
+                        scratch + kClDirect, sm_scan, sm_misc);
     } else {
       for (int i = threadIdx.x; i < ncand; i += kClThreads)
         scratch[i] = i < kClDirect ? cand[i] : __ldcg(cr + i);
       __syncthreads();
-      refine_candidates(scratch, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
+      if (3 * ncand <= DSA_CAND_CAP)
+        local_hist_select(scratch, ncand, m, outr + base_out, false, C, E, hist, scratch + ncand,
+                          scratch + 2 * ncand, sm_scan, sm_misc);
+      else
+        refine_candidates(scratch, ncand, m, outr + base_out, sm_h, sm_misc, sm_u64);
     }
-  } else if (maxima) {
-    __syncthreads();
-    block_radix_topk([row, n_scores](int64_t b) { return block_max_key(row, n_scores, b); }, n, k,
-                     outr, sm_h, sm_scan, sm_misc);
   } else {
     __syncthreads();
     block_radix_topk_row(row, n, k, outr, sm_h, sm_scan, sm_misc);
@@ -1102,14 +1140,126 @@ __device__ __noinline__ int cl_finish(const float *row, int64_t n, bool maxima, 
   return flag;
 }
 
+// Order key of the maximum of a block of 8 scores: NaN scores do not count,
+// a block with no other score has key 0 (never selected).
+__device__ __forceinline__ uint32_t max_key8(float4 a, float4 b) {
+  return max(max(max(key_or_zero(a.x), key_or_zero(a.y)), max(key_or_zero(a.z), key_or_zero(a.w))),
+             max(max(key_or_zero(b.x), key_or_zero(b.y)), max(key_or_zero(b.z), key_or_zero(b.w))));
+}
+
+// Last step of the block select, run by one CTA: nbc block candidates (every
+// block whose maximum is above the score select's E, as (key << 32 | ~block))
+// are in bsel.  With at least bk of them the top bk are among them: the
+// blocks at +inf (the newest one at least) are taken first, the others by
+// local_hist_select over the key range they span.  Otherwise every block
+// maximum of the row is recomputed into the key buffer `tab` and the exact
+// whole-row select runs over them.  Returns the fallback flag (2: more
+// candidates than bsel holds).
+__device__ __noinline__ int cl_block_finish(const float *row, int64_t n, bool vec, int bk,
+                                            int32_t *boutr, bool btake, int nbc,
+                                            const unsigned long long *bsel, uint32_t *tab,
+                                            int *hist, int *sm_h, int *sm_scan, int *sm_misc) {
+  const int64_t nbk = (n + 7) / 8;
+  if (btake) {  // every block with a valid maximum was emitted directly
+    for (int i = nbc + threadIdx.x; i < bk; i += kClThreads) boutr[i] = -1;
+    return 0;
+  }
+  if (nbc >= bk && nbc <= kBSel) {
+    // key range of the finite maxima; the blocks at +inf are counted
+    if (threadIdx.x == 0) {
+      sm_misc[4] = -1;  // min (as unsigned)
+      sm_misc[5] = 0;   // max
+      sm_misc[6] = 0;           // blocks at +inf
+    }
+    __syncthreads();
+    uint32_t lo = 0xFFFFFFFFu, hi = 0;
+    int ninf = 0;
+    for (int i = threadIdx.x; i < nbc; i += kClThreads) {
+      const uint32_t k32 = (uint32_t)(bsel[i] >> 32);
+      if (k32 >= kKeyPosInf) {
+        ++ninf;
+      } else {
+        lo = min(lo, k32);
+        hi = max(hi, k32);
+      }
+    }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    ninf = __reduce_add_sync(0xffffffffu, ninf);
+    if ((threadIdx.x & 31) == 0) {
+      atomicMin(reinterpret_cast<unsigned int *>(&sm_misc[4]), lo);
+      atomicMax(reinterpret_cast<unsigned int *>(&sm_misc[5]), hi);
+      atomicAdd(&sm_misc[6], ninf);
+    }
+    __syncthreads();
+    lo = (uint32_t)sm_misc[4];
+    hi = (uint32_t)sm_misc[5];
+    ninf = sm_misc[6];
+    __syncthreads();
+    if (ninf < bk) {
+      // the blocks at +inf, in any order, then the rest
+      if (threadIdx.x == 0) sm_misc[7] = 0;
+      __syncthreads();
+      for (int i = threadIdx.x; i < nbc; i += kClThreads) {
+        const unsigned long long v = bsel[i];
+        if ((uint32_t)(v >> 32) >= kKeyPosInf)
+          boutr[atomicAdd(&sm_misc[7], 1)] = (int32_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
+      }
+      __syncthreads();
+      unsigned long long *buf = reinterpret_cast<unsigned long long *>(tab);
+      local_hist_select(bsel, nbc, bk - ninf, boutr + ninf, false, lo, hi, hist, buf,
+                        buf + kBSel, sm_scan, sm_misc);
+      return 0;
+    }
+  }
+  for (int64_t b = threadIdx.x; b < nbk; b += kClThreads) {
+    uint32_t mk;
+    if (b == nbk - 1) {
+      mk = kKeyPosInf;  // the newest block is always chosen
+    } else if (vec) {   // a whole block of live scores, 32-byte aligned
+      mk = max_key8(__ldcg(reinterpret_cast<const float4 *>(row + 8 * b)),
+                    __ldcg(reinterpret_cast<const float4 *>(row + 8 * b + 4)));
+    } else {
+      mk = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mk = max(mk, key_or_zero(__ldcg(row + 8 * b + j)));
+    }
+    tab[b] = mk;
+  }
+  __syncthreads();
+  block_radix_topk([tab](int64_t b) { return tab[b]; }, nbk, bk, boutr, sm_h, sm_scan, sm_misc);
+  return nbc > kBSel ? 2 : 0;
+}
+
+// Bounded wait for phase 0 of `bar` (a CTA's bulk copies).  A wait that runs
+// out records DSA_DEV_TIMEOUT and waits once more, bounded again: the copies
+// must land before the CTA reads or leaves its shared memory.
+__device__ __forceinline__ void cl_wait_copies(uint32_t bar, uint32_t *status) {
+  if (mbar_try_wait(bar, 0)) return;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, 0)) {
+    if (clock64() - t0 > kDefaultWaitLimit) {
+      set_status(status, DSA_DEV_TIMEOUT);
+      mbar_wait_drain(bar, 0, kDefaultWaitLimit);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ unsigned long long dsmem_atomic_add64(uint32_t addr, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.shared::cluster.add.u64 %0, [%1], %2;" : "=l"(old) : "r"(addr), "l"(v)
+               : "memory");
+  return old;
+}
+
 __global__ void __launch_bounds__(kClThreads, 2)
     cluster_select_kernel(const __grid_constant__ ClArgs a) {
-  pdl_wait();  // predecessor grids complete before any global access
   extern __shared__ __align__(16) unsigned char cl_raw[];
   ClSmem &sm = *reinterpret_cast<ClSmem *>(cl_raw);
   __shared__ int sm_h[256];
   __shared__ int sm_scan[kSelWarps + 1];
-  __shared__ int sm_misc[32];  // [0..2] T, [8..10] S, [16..18] Tb, [24..26] Sb, counters
+  __shared__ int sm_misc[32];  // [0..2] T, [8..10] S
   __shared__ unsigned long long sm_u64[2];
   const uint32_t rank = cluster_ctarank();
   const int lane = threadIdx.x & 31;
@@ -1121,54 +1271,158 @@ __global__ void __launch_bounds__(kClThreads, 2)
   const int r = local ? (y - a.cl_begin[pi]) * kCl + (int)rank : y - a.cl_begin[pi];
   if (local && r >= p.R) return;  // a local CTA passes no cluster barrier
   const int k = p.k;
-  const int64_t n = row_len(p.ctx, p.next_n, p.len_div, r, p.stride, a.status);
   const float *row = p.logits + (int64_t)r * p.stride;
   int32_t *outr = p.out + (int64_t)r * k;
   const int64_t wr = (int64_t)p.ws_row0 + r;
   unsigned long long *cr = a.cand + wr * DSA_CAND_CAP;
   int32_t *wh = a.ws_hist + wr * DSA_NUM_BINS;
-  int32_t *wf = a.ws_fine + wr * kFineBins;
-  int32_t *wbh = wf + kClFine;       // the row's block-maxima histogram (workspace)
-  int32_t *wbf = wf + 2 * kClFine;   // its fine histogram
   const int32_t *hrow = p.hist ? p.hist + (int64_t)r * DSA_NUM_BINS : nullptr;
-  // this CTA's positions [c0, c1), in groups of 2048 (one float4 per thread)
-  const int64_t chunk = ((local ? n : (n + kCl - 1) / kCl) + 2047) / 2048 * 2048;
-  const int64_t c0 = local ? 0 : (int64_t)rank * chunk;
-  const int64_t c1 = min(n, c0 + chunk);
-  const int vq = (int)(chunk / 2048);  // <= kClVec
-  const bool blk = p.bk > 0;           // block select alongside the score select
+  const bool blk = p.bk > 0;  // block select alongside the score select
   const int bk = p.bk;
-  const int dcap = blk ? kClCandHalf : DSA_CAND_CAP;  // candidate slots of the score select
-  const int64_t nbk = (n + 7) / 8;     // blocks of the row
+  // this CTA's positions: [c0, c0 + chunk) of the row's stride, in groups of
+  // 2048 (one float4 per thread); cut by the stride, so the copies can start
+  // before the row's live length is read
+  const int64_t chunk = ((local ? p.stride : (p.stride + kCl - 1) / kCl) + 2047) / 2048 * 2048;
+  const int64_t c0 = local ? 0 : (int64_t)rank * chunk;
+  const int vq = (int)(chunk / 2048);  // <= kClVec
   const int64_t b0 = c0 / 8;           // this CTA's first block
+  // 16-byte aligned rows come into shared memory by bulk copies (the key
+  // buffer takes the CTA's scores as they lie, then they become keys in
+  // place); the caller's histogram row likewise when it is 16-byte aligned
+  const bool bulk = p.vec != 0;
+  const bool hbulk = hrow && ((reinterpret_cast<uintptr_t>(hrow) & 15) == 0);
+  const int64_t cend = min(p.stride, c0 + chunk);
+  const int64_t rbytes = (bulk && cend > c0) ? (cend - c0) * 4 : 0;  // multiple of 16
+  // the scores come in kClGroups groups (group g: the float4 slots q of
+  // kClGroupVec * g .. of every thread, 16 KB of consecutive scores), each on
+  // its own barrier, so keys are made from one group while the next lands
+  const uint32_t bar_h = smem_u32(&sm.bar[0]);
+  auto bar_g = [&](int g) { return smem_u32(&sm.bar[1 + g]); };
+  constexpr int64_t kGroupBytes = (int64_t)kClGroupVec * kClThreads * 16;
 
-  if (threadIdx.x < 8) sm.ctr[threadIdx.x] = 0;
-  if (threadIdx.x < 8) sm.bmm[threadIdx.x] = 0;
-  for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) {
-    sm.hist[i] = 0;
-    sm.bhist[i] = 0;
+  // ---- set-up that reads no global memory, ahead of the predecessor's end
+  if (threadIdx.x == 0) {
+    sm.ctr = 0;
+    sm.bctr = 0;
+    for (int i = 0; i <= kClGroups; ++i) mbar_init(smem_u32(&sm.bar[i]), 1);
+    fence_mbar_init();
   }
+  if (!hrow)
+    for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) sm.hist[i] = 0;
+  for (int i = threadIdx.x; i < kClFine; i += kClThreads) sm.fmerge[i] = 0;
+  __syncthreads();
+  // cluster barrier A: every CTA's counters and merge buffer are zeroed; it is
+  // waited for just before the first remote access
+  if (!local) cluster_arrive();
+  bool pending = !local;
+  auto wait_pending = [&]() {
+    if (pending) {
+      cluster_wait();
+      pending = false;
+    }
+  };
+
+  pdl_wait();  // predecessor grids complete before any global access
+  if ((bulk || hbulk) && threadIdx.x < 32) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_h, hbulk ? DSA_NUM_BINS * 4 : 0);
+      if (hbulk) bulk_load(smem_u32(sm.hist), hrow, DSA_NUM_BINS * 4, bar_h);
+    }
+    if (lane <= kClGroups && lane > 0) {
+      const int64_t gb = rbytes - (lane - 1) * kGroupBytes;
+      mbar_arrive_expect_tx(bar_g(lane - 1), (uint32_t)(gb <= 0 ? 0 : min(gb, kGroupBytes)));
+    }
+    __syncwarp();
+    const uint64_t pol = policy_evict_first();
+    const uint32_t kdst = smem_u32(sm.keys);
+    const char *src = reinterpret_cast<const char *>(row + c0);
+    for (int64_t off = (int64_t)lane * 4096; off < rbytes; off += 32 * 4096)
+      bulk_load_hint(kdst + (uint32_t)off, src + off, (uint32_t)min((int64_t)4096, rbytes - off),
+                     bar_g((int)(off / kGroupBytes)), pol);
+  }
+  const int64_t n = row_len(p.ctx, p.next_n, p.len_div, r, p.stride, a.status);
+  const int64_t c1 = min(n, c0 + chunk);
+  const int64_t nrow = c1 > c0 ? c1 - c0 : 0;  // this CTA's live scores
+  const int64_t nbk = (n + 7) / 8;             // blocks of the row
+  const bool btake = nbk <= bk;                // every block is taken
+  const bool take_all = n <= k;
+  const bool early = hrow || take_all;  // T known without the row's own histogram
   float4 v[kClVec];
-  cl_issue_loads(row, c0, c1, vq, p.vec != 0, v);
+  if (!bulk) cl_issue_loads(row, c0, c1, vq, false, v);
 
   // ---- 1. threshold bin T from the caller's histogram, while the row loads
   // (rows of at most k scores take every non-NaN score: T past the last bin)
-  const bool take_all = n <= k;
-  const bool early = hrow || take_all;  // T known without the row's own histogram
   int T = DSA_NUM_BINS, above = 0, histT = 0;
+  if (hbulk) cl_wait_copies(bar_h, a.status);  // every copy lands before the CTA moves on
   if (early && !take_all) {
-    threshold_from_hist<DSA_NUM_BINS>(hrow, k, sm_scan, sm_misc);
+    threshold_from_hist<DSA_NUM_BINS>(hbulk ? sm.hist : hrow, k, sm_scan, sm_misc);
     T = sm_misc[0];
     above = sm_misc[1];
     histT = sm_misc[2];
   }
-  cl_store_keys(v, sm.keys);
+  // keys into shared memory, and the block maxima (a block of 8 scores is
+  // two neighbouring threads' slots; the newest block counts as +inf)
+  const float nanv = __int_as_float(0x7fffffff);
+#pragma unroll
+  for (int q = 0; q < kClVec; ++q) {
+    const int i = q * kClThreads + threadIdx.x;
+    float4 x = v[q];
+    if (bulk) {
+      if (q % kClGroupVec == 0) cl_wait_copies(bar_g(q / kClGroupVec), a.status);
+      const int64_t t = 4 * (int64_t)i;  // chunk offset of the slot's first score
+      if (q < vq && t < nrow) {
+        x = reinterpret_cast<const float4 *>(sm.keys)[i];
+        if (t + 4 > nrow) {  // the row ends inside this slot
+          if (t + 1 >= nrow) x.y = nanv;
+          if (t + 2 >= nrow) x.z = nanv;
+          x.w = nanv;
+        }
+      } else {
+        x = make_float4(nanv, nanv, nanv, nanv);
+      }
+    }
+    const uint4 kk = make_uint4(key_or_zero(x.x), key_or_zero(x.y), key_or_zero(x.z),
+                                key_or_zero(x.w));
+    sm.keys[i] = kk;
+    if (blk) {
+      uint32_t mk = max(max(kk.x, kk.y), max(kk.z, kk.w));
+      mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, 1));
+      const int lb = q * (kClThreads / 2) + (threadIdx.x >> 1);
+      const int64_t b = b0 + lb;
+      if (q >= vq || b >= nbk) mk = 0;          // slots past this CTA's positions or the row
+      else if (b == nbk - 1) mk = kKeyPosInf;   // the newest block is always chosen
+      if ((threadIdx.x & 1) == 0) sm.bkey[lb] = mk;
+    }
+  }
   __syncthreads();
-
-  // ---- 2. local histograms: the scores' (when T is not known yet) and the
-  // block maxima's (a block of 8 scores is two threads' slots), with the key
-  // range each wide bin's maxima take
-  if (!early) {
+  uint32_t loT = 0, hiT = 0;  // loT > hiT: bin T empty (T past the last bin)
+  bool fine = false;
+  uint32_t flo = 0;
+  int fshift = 0;
+  // this CTA's fine histogram of bin T into sm.hist: an even split of the
+  // bin's key range, or for the four bins wider than kFineWindow keys a
+  // window of that many keys at the end nearer to magnitude 1 (keys outside
+  // clamp to the end bins)
+  auto fine_local = [&]() {
+    cl_fine_window(T, loT, hiT, 0u, 0u, flo, fshift);
+    for (int i = threadIdx.x; i < kClFine; i += kClThreads) sm.hist[i] = 0;
+    __syncthreads();
+    for (int q = 0; q < vq; ++q) {
+      const uint4 k4 = sm.keys[q * kClThreads + threadIdx.x];
+      const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (kv[j] >= loT && kv[j] <= hiT) atomicAdd(&sm.hist[cl_fine_idx(kv[j], flo, fshift)], 1);
+    }
+    __syncthreads();
+  };
+  if (early) {
+    bin_key_range(T, loT, hiT);
+    fine = (T < DSA_NUM_BINS) && histT > kClDirect;
+    if (fine) fine_local();
+  } else {
+    // ---- 2. the row's own coarse histogram (no histogram given): local,
+    // then merged in the workspace behind one cluster barrier
     for (int q = 0; q < vq; ++q) {
       const uint4 k4 = sm.keys[q * kClThreads + threadIdx.x];
       const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
@@ -1176,59 +1430,11 @@ __global__ void __launch_bounds__(kClThreads, 2)
       for (int j = 0; j < 4; ++j)
         if (kv[j]) atomicAdd(&sm.hist[coarse_bin_of_key(kv[j])], 1);
     }
-  }
-  if (blk) {
-#pragma unroll 1
-    for (int q = 0; q < kClVec; ++q) {
-      const uint4 k4 = sm.keys[q * kClThreads + threadIdx.x];
-      uint32_t mk = max(max(k4.x, k4.y), max(k4.z, k4.w));
-      mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, 1));
-      const int lb = q * (kClThreads / 2) + (threadIdx.x >> 1);
-      const int b = (int)b0 + lb;           // blocks of a cluster row are below 2^28
-      if (q >= vq || b >= (int)nbk) mk = 0;    // slots past this CTA's positions, blocks past the row
-      else if (b == (int)nbk - 1) mk = kKeyPosInf;  // the newest block is always chosen
-      if ((threadIdx.x & 1) == 0) {
-        sm.bkey[lb] = mk;
-        if (mk) {
-          const int bb = coarse_bin_of_key(mk);
-          atomicAdd(&sm.bhist[bb], 1);
-          const int wi = wide_bin_idx(bb);
-          if (wi >= 0) {
-            atomicMax(&sm.bmm[2 * wi], ~mk);
-            atomicMax(&sm.bmm[2 * wi + 1], mk);
-          }
-        }
-      }
-    }
-  }
-  uint32_t loT = 0, hiT = 0;  // loT > hiT: bin T empty (T past the last bin)
-  bool fine = false, wide = false;
-  if (early) {
-    bin_key_range(T, loT, hiT);
-    fine = (T < DSA_NUM_BINS) && histT > kClDirect;
-    wide = fine && (hiT - loT) >= kFineWindow;
-    if (wide) cl_range_in(sm.keys, vq, loT, hiT, sm.red);
-  }
-  __syncthreads();
-  if (!local) {
-    // publish into the workspace, then the first cluster barrier (it also
-    // makes every CTA's counters safe to reach)
-    if (!early) cl_flush(sm.hist, wh, DSA_NUM_BINS);
-    if (blk) {
-      cl_flush(sm.bhist, wbh, DSA_NUM_BINS);
-      if (threadIdx.x < 8) wf[kSlotB + 8 * rank + threadIdx.x] = sm.bmm[threadIdx.x];
-    }
-    if (wide && threadIdx.x == 0) {
-      wf[kSlotD + 2 * rank] = sm.red[0];
-      wf[kSlotD + 2 * rank + 1] = sm.red[1];
-    }
-    cluster_arrive();
-    cluster_wait();
-  }
-
-  // ---- 3. the score select's T when the row built its own histogram
-  if (!early) {
+    __syncthreads();
     if (!local) {
+      cl_flush(sm.hist, wh, DSA_NUM_BINS);
+      wait_pending();
+      cluster_sync();
       cl_fetch(sm.hist, wh, DSA_NUM_BINS);
       __syncthreads();
     }
@@ -1238,210 +1444,116 @@ __global__ void __launch_bounds__(kClThreads, 2)
     histT = sm_misc[2];
     bin_key_range(T, loT, hiT);
     fine = (T < DSA_NUM_BINS) && histT > kClDirect;
-    wide = fine && (hiT - loT) >= kFineWindow;
-    if (wide) {
-      cl_range_in(sm.keys, vq, loT, hiT, sm.red);
-      if (!local) {
-        if (threadIdx.x == 0) {
-          wf[kSlotD + 2 * rank] = sm.red[0];
-          wf[kSlotD + 2 * rank + 1] = sm.red[1];
-        }
-        cluster_sync();
-      }
-    }
+    if (fine) fine_local();
   }
-  // ---- 4. the block select's threshold Tb and key ranges of wide bins
-  const bool btake = nbk <= bk;
-  int Tb = DSA_NUM_BINS, aboveb = 0, histTb = 0;
-  if (blk) {
-    if (!local) {
-      cl_fetch(sm.bhist, wbh, DSA_NUM_BINS);
-      __syncthreads();
-    }
-    if (!btake) {
-      threshold_from_hist<DSA_NUM_BINS>(sm.bhist, bk, sm_scan, sm_misc + 16);
-      Tb = sm_misc[16];
-      aboveb = sm_misc[17];
-      histTb = sm_misc[18];
-    }
-  }
-  uint32_t bloT, bhiT;
-  bin_key_range(Tb, bloT, bhiT);
-  const bool bfine = blk && (Tb < DSA_NUM_BINS) && histTb > kClDirect;
-  const int bwi = bfine ? wide_bin_idx(Tb) : -1;
-  if (threadIdx.x == 0) {
-    if (wide && !local) {
-      uint32_t nm = 0, mx = 0;
-      for (int c = 0; c < kCl; ++c) {
-        nm = max(nm, (uint32_t)__ldcg(&wf[kSlotD + 2 * c]));
-        mx = max(mx, (uint32_t)__ldcg(&wf[kSlotD + 2 * c + 1]));
-      }
-      sm.red[0] = nm;
-      sm.red[1] = mx;
-    }
-    if (bwi >= 0) {
-      uint32_t nm = sm.bmm[2 * bwi], mx = sm.bmm[2 * bwi + 1];
-      if (!local) {
-        nm = 0;
-        mx = 0;
-        for (int c = 0; c < kCl; ++c) {
-          nm = max(nm, (uint32_t)__ldcg(&wf[kSlotB + 8 * c + 2 * bwi]));
-          mx = max(mx, (uint32_t)__ldcg(&wf[kSlotB + 8 * c + 2 * bwi + 1]));
-        }
-      }
-      sm.red[2] = nm;
-      sm.red[3] = mx;
-    }
-  }
-  __syncthreads();
 
-  // ---- 5. fine histograms of bin T and bin Tb (one barrier for both)
-  uint32_t flo = 0, bflo = 0;
-  int fshift = 0, S = 0, above1 = 0, fineS = 0;
-  int bfs = 0, Sb = 0, above1b = 0, fineSb = 0;
-  if (fine || bfine) {
-    if (fine) {
-      cl_fine_window(T, loT, hiT, wide ? ~sm.red[0] : 0u, wide ? sm.red[1] : 0u, flo, fshift);
-      for (int i = threadIdx.x; i < kClFine; i += kClThreads) sm.hist[i] = 0;
-    }
-    if (bfine) {
-      cl_fine_window(Tb, bloT, bhiT, bwi >= 0 ? ~sm.red[2] : 0u, bwi >= 0 ? sm.red[3] : 0u, bflo,
-                     bfs);
-      for (int i = threadIdx.x; i < kClFine; i += kClThreads) sm.bhist[i] = 0;
-    }
-    __syncthreads();
-    if (fine) {
-      for (int q = 0; q < vq; ++q) {
-        const uint4 k4 = sm.keys[q * kClThreads + threadIdx.x];
-        const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (kv[j] >= loT && kv[j] <= hiT)
-            atomicAdd(&sm.hist[cl_fine_idx(kv[j], flo, fshift)], 1);
-      }
-    }
-    if (bfine) {
-      for (int i = threadIdx.x; i < kClBlk; i += kClThreads) {
-        const uint32_t mk = sm.bkey[i];
-        if (mk >= bloT && mk <= bhiT) atomicAdd(&sm.bhist[cl_fine_idx(mk, bflo, bfs)], 1);
-      }
-    }
-    __syncthreads();
+  // ---- 3. the fine threshold bin S of bin T: the CTAs' fine histograms are
+  // added into CTA 0's merge buffer and read back from there
+  int S = 0, above1 = 0, fineS = 0;
+  uint32_t C = loT, E = hiT;
+  if (fine) {
     if (!local) {
-      if (fine) cl_flush(sm.hist, wf, kClFine);
-      if (bfine) cl_flush(sm.bhist, wbf, kClFine);
+      wait_pending();
+      const uint32_t fm0 = dsmem_map(smem_u32(&sm.fmerge[0]), 0);
+      for (int i = threadIdx.x; i < kClFine; i += kClThreads) {
+        const int c = sm.hist[i];
+        if (c) dsmem_red_add(fm0 + 4u * (uint32_t)i, c);
+      }
       cluster_sync();
-      if (fine) cl_fetch(sm.hist, wf, kClFine);
-      if (bfine) cl_fetch(sm.bhist, wbf, kClFine);
+      for (int i = threadIdx.x; i < kClFine / 4; i += kClThreads)
+        reinterpret_cast<int4 *>(sm.hist)[i] = dsmem_ld4(fm0 + 16u * (uint32_t)i);
       __syncthreads();
     }
-    if (fine) {
-      threshold_from_hist<kClFine>(sm.hist, k - above, sm_scan, sm_misc + 8);
-      S = sm_misc[8];
-      above1 = sm_misc[9];
-      fineS = sm_misc[10];
-    }
-    if (bfine) {
-      threshold_from_hist<kClFine>(sm.bhist, bk - aboveb, sm_scan, sm_misc + 24);
-      Sb = sm_misc[24];
-      above1b = sm_misc[25];
-      fineSb = sm_misc[26];
-    }
+    threshold_from_hist<kClFine>(sm.hist, k - above, sm_scan, sm_misc + 8);
+    S = sm_misc[8];
+    above1 = sm_misc[9];
+    fineS = sm_misc[10];
+    fine_bin_keys(loT, hiT, flo, fshift, S, C, E);
   }
 
-  // ---- 6. classify both selects, reserve output and candidate ranges
-  // (score select on CTA 0, block select on CTA 1), write.  Emit: key > E;
-  // candidate: C <= key <= E (bin T, or its fine bin S)
-  uint32_t C = loT, E = hiT, CB = bloT, EB = bhiT;
-  if (fine) fine_bin_keys(loT, hiT, flo, fshift, S, C, E);
-  if (bfine) fine_bin_keys(bloT, bhiT, bflo, bfs, Sb, CB, EB);
+  // ---- 4. classify, reserve output and candidate ranges (scores on CTA 0,
+  // blocks on CTA 1) with one atomic per warp, write.  Scores: emit when
+  // key > E, candidate when C <= key <= E.  Blocks: with bk or fewer blocks in
+  // the row every block with a valid maximum is emitted; otherwise every
+  // block whose maximum is above E is a candidate.
   const unsigned long long kinds = cl_classify(sm.keys, vq, C, E);
   const int ne = __popcll(kinds & 0x5555555555555555ull);
   const int nc = __popcll(kinds & 0xAAAAAAAAAAAAAAAAull);
-  constexpr int kBPer = kClBlk / kClThreads;  // maxima per thread: index tid + e * kClThreads
-  uint32_t bkinds = 0;
+  const uint32_t EB = btake ? kKeyNegInf - 1 : E;
+  uint32_t bmask = 0;
   if (blk) {
 #pragma unroll
-    for (int e = 0; e < kBPer; ++e)
-      bkinds |= cl_kind(sm.bkey[threadIdx.x + e * kClThreads], CB, EB) << (2 * e);
+    for (int e = 0; e < kClBPer; ++e)
+      bmask |= (uint32_t)(sm.bkey[threadIdx.x + e * kClThreads] > EB) << e;
   }
-  const int bne = __popc(bkinds & 0x55u), bnc = __popc(bkinds & 0xAAu);
-  int tot, btot = 0, bex = 0;
-  const int ex = block_excl_scan((nc << 16) | ne, sm_scan, &tot);  // per CTA < 2^15 each
-  if (blk) bex = block_excl_scan((bnc << 16) | bne, sm_scan, &btot);
-  int base_e = 0, base_c = 0, bbe = 0, bbc = 0;
-  uint32_t cand0 = 0, bcand1 = 0;
-  if (!local) {
-    const uint32_t ctr0 = dsmem_map(smem_u32(&sm.ctr[0]), 0);
-    const uint32_t bctr = dsmem_map(smem_u32(&sm.ctr[4]), 1);
-    if (threadIdx.x == 0) {
-      const int e0 = (tot & 0xFFFF) ? dsmem_atomic_add(ctr0, tot & 0xFFFF) : 0;
-      const int e1 = (tot >> 16) ? dsmem_atomic_add(ctr0 + 4, tot >> 16) : 0;
-      const int e2 = (btot & 0xFFFF) ? dsmem_atomic_add(bctr, btot & 0xFFFF) : 0;
-      const int e3 = (btot >> 16) ? dsmem_atomic_add(bctr + 4, btot >> 16) : 0;
-      sm_misc[5] = e0;
-      sm_misc[6] = e1;
-      sm_misc[21] = e2;
-      sm_misc[22] = e3;
-    }
-    __syncthreads();
-    base_e = sm_misc[5];
-    base_c = sm_misc[6];
-    bbe = sm_misc[21];
-    bbc = sm_misc[22];
-    cand0 = dsmem_map(smem_u32(&sm.cand[0]), 0);
-    bcand1 = dsmem_map(smem_u32(&sm.bcand[0]), 1);
-  }
-  if (kinds)
-    cl_write(kinds, sm.keys, c0, base_e + (ex & 0xFFFF), base_c + (ex >> 16), k, dcap, outr,
-             !local, cand0, sm.cand, cr);
-  int32_t *boutr = blk ? p.bout + (int64_t)r * bk : nullptr;
-  unsigned long long *crb = cr + kClCandHalf;
-  if (bkinds) {
-    int pe = bbe + (bex & 0xFFFF), pc = bbc + (bex >> 16);
+  const int nb = __popc(bmask);
+  // warp-inclusive scans of the three counts (ne, nc <= 32; nb <= kClBPer)
+  int ie = ne, ic = nc, ib = nb;
 #pragma unroll
-    for (int e = 0; e < kBPer; ++e) {
-      const uint32_t kd = (bkinds >> (2 * e)) & 3u;
-      if (!kd) continue;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x1 = __shfl_up_sync(0xffffffffu, ie, o);
+    const int x2 = __shfl_up_sync(0xffffffffu, ic, o);
+    const int x3 = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) {
+      ie += x1;
+      ic += x2;
+      ib += x3;
+    }
+  }
+  wait_pending();  // every CTA's counters are zeroed before the first remote atomic
+  int we = 0, wc = 0, wb = 0;  // this warp's bases
+  if (lane == 31) {
+    const unsigned long long add = (unsigned long long)ie | ((unsigned long long)ic << 32);
+    if (add) {
+      const unsigned long long old =
+          local ? atomicAdd(&sm.ctr, add) : dsmem_atomic_add64(dsmem_map(smem_u32(&sm.ctr), 0), add);
+      we = (int)(old & 0xFFFFFFFFull);
+      wc = (int)(old >> 32);
+    }
+    if (ib) wb = local ? atomicAdd(&sm.bctr, ib) : dsmem_atomic_add(dsmem_map(smem_u32(&sm.bctr), 1), ib);
+  }
+  we = __shfl_sync(0xffffffffu, we, 31) + ie - ne;
+  wc = __shfl_sync(0xffffffffu, wc, 31) + ic - nc;
+  wb = __shfl_sync(0xffffffffu, wb, 31) + ib - nb;
+  const uint32_t cand0 = local ? 0u : dsmem_map(smem_u32(&sm.cand[0]), 0);
+  if (kinds)
+    cl_write(kinds, sm.keys, c0, we, wc, k, DSA_CAND_CAP, outr, !local, cand0, sm.cand, cr);
+  int32_t *boutr = blk ? p.bout + (int64_t)r * bk : nullptr;
+  if (bmask) {
+    const uint32_t bsel1 = local ? 0u : dsmem_map(smem_u32(&sm.bsel[0]), 1);
+    int pb = wb;
+#pragma unroll
+    for (int e = 0; e < kClBPer; ++e) {
+      if (!((bmask >> e) & 1u)) continue;
       const int idx = threadIdx.x + e * kClThreads;
       const int64_t b = b0 + idx;
-      if (kd == 1) {
-        if (pe < bk) boutr[pe] = (int32_t)b;
-        ++pe;
-      } else {
+      if (btake) {
+        if (pb < bk) boutr[pb] = (int32_t)b;
+      } else if (pb < kBSel) {
         const unsigned long long cv = ((unsigned long long)sm.bkey[idx] << 32) |
                                       (unsigned long long)(0xFFFFFFFFu - (uint32_t)b);
-        if (pc < kClDirect) {
-          if (!local) dsmem_st64(bcand1 + 8u * (uint32_t)pc, cv);
-          else sm.bcand[pc] = cv;
-        } else if (pc < kClCandHalf) {
-          crb[pc] = cv;
-        }
-        ++pc;
+        if (local) sm.bsel[pb] = cv;
+        else dsmem_st64(bsel1 + 8u * (uint32_t)pb, cv);
       }
+      ++pb;
     }
   }
-  if (!local) cluster_sync();  // all emits and candidates are in place; histograms read
+  if (!local) cluster_sync();  // all emits and candidates are in place
   else __syncthreads();
 
-  // ---- 7. check, rank or refine, or fall back: the score select on CTA 0
+  // ---- 5. check, rank or refine, or fall back: the score select on CTA 0
   // (the local CTA), the block select on CTA 1 (the local CTA, after)
   unsigned long long *scratch = reinterpret_cast<unsigned long long *>(sm.keys);
   if (local || rank == 0) {
-    const int emitted = local ? (tot & 0xFFFF) : sm.ctr[0];
-    const int ncand = local ? (tot >> 16) : sm.ctr[1];
-    const int flag = cl_finish(row, n, false, n, k, outr, take_all, T, above, histT, fine, S,
-                               above1, fineS, emitted, ncand, dcap, sm.cand, cr, scratch, sm_h,
-                               sm_scan, sm_misc, sm_u64);
+    const int emitted = (int)(sm.ctr & 0xFFFFFFFFull);
+    const int ncand = (int)(sm.ctr >> 32);
+    const int flag = cl_finish(row, n, k, outr, take_all, T, above, histT, fine, S, above1, fineS,
+                               emitted, ncand, DSA_CAND_CAP, C, E, sm.cand, cr, scratch, sm.hist,
+                               sm_h, sm_scan, sm_misc, sm_u64);
     if (p.flags && threadIdx.x == 0) p.flags[r] = flag;
-    // restore the zero workspace histograms; clear the caller's on request
-    if (!local) {
-      if (!early)
-        for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) wh[i] = 0;
-      if (fine)
-        for (int i = threadIdx.x; i < kClFine; i += kClThreads) wf[i] = 0;
-      if (wide && threadIdx.x < 2 * kCl) wf[kSlotD + threadIdx.x] = 0;
-    }
+    // restore the zero workspace histogram; clear the caller's on request
+    if (!local && !early)
+      for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) wh[i] = 0;
     if (p.reset_hist && p.hist) {
       int32_t *hw = p.hist + (int64_t)r * DSA_NUM_BINS;
       for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) hw[i] = 0;
@@ -1449,18 +1561,10 @@ __global__ void __launch_bounds__(kClThreads, 2)
   }
   if (blk && (local || rank == 1)) {
     __syncthreads();  // the local CTA: the score select's finish is done with the scratch
-    const int emitted = local ? (btot & 0xFFFF) : sm.ctr[4];
-    const int ncand = local ? (btot >> 16) : sm.ctr[5];
-    const int flag = cl_finish(row, nbk, true, n, bk, boutr, btake, Tb, aboveb, histTb, bfine, Sb,
-                               above1b, fineSb, emitted, ncand, kClCandHalf, sm.bcand, crb,
-                               scratch, sm_h, sm_scan, sm_misc, sm_u64);
+    const int flag = cl_block_finish(row, n, p.vec != 0, bk, boutr, btake, sm.bctr, sm.bsel,
+                                     reinterpret_cast<uint32_t *>(sm.keys), sm.hist, sm_h, sm_scan,
+                                     sm_misc);
     if (p.bflags && threadIdx.x == 0) p.bflags[r] = flag;
-    if (!local) {
-      for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) wbh[i] = 0;
-      if (bfine)
-        for (int i = threadIdx.x; i < kClFine; i += kClThreads) wbf[i] = 0;
-      if (threadIdx.x < 8 * kCl) wf[kSlotB + threadIdx.x] = 0;
-    }
   }
 }
 
@@ -1511,7 +1615,6 @@ __global__ void __launch_bounds__(kRowThreads)
   __shared__ int sm_misc[8];
   __shared__ uint32_t sm_red[2];
   const int r = blockIdx.x;
-  const int lane = threadIdx.x & 31;
   int64_t n = row_len(ctx, next_n, len_div, r, stride, status);
   if (n > kSmemRow) {
     if (threadIdx.x == 0) set_status(status, DSA_DEV_BOUNDS);

@@ -210,11 +210,16 @@ int32_t dsa_coarse_hist_topk_launches(int64_t stride, int32_t has_histogram);
  * maximum ignores NaN scores, a block of NaN only is never selected, the
  * newest block (the one holding the row's last live score) counts as +inf,
  * ties go to the lower block.  The maxima are taken from the scores the
- * select already holds, never written to memory.
+ * select already holds, never written to memory.  No histogram of the
+ * maxima is needed: every block whose maximum lies above the score select's
+ * emit threshold holds an emitted score, so when at least block_k blocks
+ * (the newest one included) lie above it, the top block_k are selected
+ * exactly among those (at most k of them); otherwise the exact select runs
+ * over every block maximum of the row.
  *   block_out_idx         [R][block_k] int32 block ids, -1 padded, any order
- *   block_fallback_flags  NULL or [R] int32, as fallback_flags
- * With a block output each select keeps at most DSA_CAND_CAP / 2 candidates
- * before its exact fallback. */
+ *   block_fallback_flags  NULL or [R] int32: 0, or 2 when more blocks lay
+ *                         above the threshold than k (an inconsistent
+ *                         histogram) and the whole-row select ran */
 #define DSA_TOPK_BATCH_MAX 4
 typedef struct dsa_topk_problem {
   const float *logits;
