@@ -207,8 +207,9 @@ def run_reference(args, ws_, rank):
 
 def measure_workload(name, dev, steps=200, warmup=5):
     """Per-workload timings of the same step (outside the headline's timed
-    region): the logits launch alone (CUDA events around it), the eager step
-    (events around the whole step only) and the CUDA-graph replay."""
+    region): the logits launch alone (a CUDA graph of back-to-back launches),
+    the eager step (events around the whole step only) and the CUDA-graph
+    replay of the step."""
     import torch
     import synthetic as S
     from dsa_sparse_attention_paged_gb300.pipeline import DecodePlan
@@ -237,11 +238,33 @@ def measure_workload(name, dev, steps=200, warmup=5):
         b.record()
     torch.cuda.synchronize()
     step_us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in steps_ev)
-    lg_ev = [{"logits": ev()} for _ in range(steps)]
-    for e in lg_ev:
-        plan.step(*inputs, events=e)
+    # the logits launch alone, from a CUDA graph of back-to-back launches (an
+    # eager launch of a few-microsecond kernel would time the host's launch)
+    import dsa_sparse_attention_paged_gb300 as D
+    hist = torch.zeros((w.R, 1024), dtype=torch.int32, device=dev)
+    reps = 20
+
+    def logits_only():
+        D.paged_mqa_logits(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"],
+                           d["context_lens"], nn, plan.ws, logits=plan.logits, histogram=hist)
+
+    logits_only()
     torch.cuda.synchronize()
-    lg_us = 1e3 * statistics.median(e["logits"][0].elapsed_time(e["logits"][1]) for e in lg_ev)
+    gl = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gl):
+        for _ in range(reps):
+            logits_only()
+    gl.replay()
+    torch.cuda.synchronize()
+    lg = []
+    for _ in range(10):
+        a, b = ev()
+        a.record()
+        gl.replay()
+        b.record()
+        torch.cuda.synchronize()
+        lg.append(a.elapsed_time(b) / reps)
+    lg_us = 1e3 * statistics.median(lg)
     plan.capture(*inputs)
     plan.replay()
     torch.cuda.synchronize()
@@ -264,6 +287,56 @@ def measure_workload(name, dev, steps=200, warmup=5):
     del plan, d
     torch.cuda.empty_cache()
     return out
+
+
+MX_KEY_BYTES = 68  # 64 bytes of E2M1 codes + 4 UE8M0 block exponents per key
+
+
+def measure_mx_logits(case, w, d, dev, steps=200, warmup=5):
+    """The MXFP4-key logits launch (with the fused histogram) at this
+    workload's shape and page pool: seeded E2M1 codes and exponents, launches
+    back to back (the 68-byte-a-key stream is larger than L2), CUDA events."""
+    import torch
+    import dsa_sparse_attention_paged_gb300 as D
+    g = torch.Generator().manual_seed(w.seed + 1000)
+    P, ps = case["num_pages"], w.page_size
+    codes = torch.randint(0, 256, (P, ps, 64), generator=g, dtype=torch.uint8).to(dev)
+    exps = torch.randint(125, 130, (P, ps, 4), generator=g, dtype=torch.uint8).to(dev)
+    nn = w.next_n
+    ctx = np.asarray(w.context_lens, dtype=np.int64)
+    stride = (int(ctx.max()) + 7) // 8 * 8
+    ws = D.Workspace(w.R, device=dev)
+    logits = torch.empty((w.R, stride), dtype=torch.float32, device=dev)
+    hist = torch.zeros((w.R, 1024), dtype=torch.int32, device=dev)
+
+    def launch():
+        D.paged_mqa_logits_mx(d["q"], codes, exps, d["weights"], d["page_table"],
+                              d["context_lens"], nn, ws, logits=logits, histogram=hist)
+
+    for _ in range(warmup):
+        launch()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        a.record()
+        launch()
+        b.record()
+    torch.cuda.synchronize()
+    if ws.status() != 0:
+        raise RuntimeError(f"MXFP4 logits: device status {ws.status():#x}")
+    us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in ev)
+    keys = int(ctx.sum())
+    kbytes = keys * MX_KEY_BYTES
+    peak, kind = peaks()
+    gbs = kbytes / (us * 1e-6) / 1e9
+    del codes, exps, logits, hist
+    torch.cuda.empty_cache()
+    return {"kernel": f"logits_kernel<next_n={nn}, MXFP4 keys, histogram>",
+            "logits_us": us, "kstream_bytes": kbytes, "key_bytes": MX_KEY_BYTES,
+            "kstream_gbs": gbs, "frac_of_measured_peak": gbs / peak,
+            "frac_of_8tbs_nominal": gbs / NOMINAL_GBS,
+            "keys_per_s": keys * nn / (us * 1e-6)}
 
 
 def cpu_baseline(case, w, budget):
@@ -422,6 +495,7 @@ def main():
     cb = None
     if not args.no_cpu_baseline:
         cb = cpu_baseline(case, w, args.cpu_budget)
+    mx = measure_mx_logits(case, w, d, dev)
     per_workload = None
     if not args.no_per_workload:
         per_workload = {nm: measure_workload(nm, dev) for nm in PER_WORKLOADS
@@ -458,6 +532,7 @@ def main():
                 "ms_per_step": 1e3 * e2e_s / Ke, "steps": Ke},
         "gpu_launches": plan.launches_per_step * K,
         "clocks": clocks,
+        "mxfp4_logits": mx,
         "per_workload": per_workload,
     }
     print(json.dumps(line), flush=True)

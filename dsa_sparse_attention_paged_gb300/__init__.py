@@ -74,6 +74,8 @@ def _load():
         "dsa_read_device_status": (i32, [P, P, ctypes.POINTER(u32)]),
         "dsa_paged_mqa_logits": (i32, [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, i32, P,
                                        i64, P, P, i64, i32, P, sz, P]),
+        "dsa_paged_mqa_logits_mx": (i32, [P, P, P, P, P, i64, P, i32, i32, i32, i32, i32, i32,
+                                          P, i64, P, P, sz, P]),
         "dsa_coarse_hist_topk": (i32, [P, i64, P, i32, i32, i32, P, i32, i32, P, P, P, sz, P]),
         "dsa_coarse_hist_topk_launches": (i32, [i64, i32]),
         "dsa_coarse_hist_topk_batch": (i32, [ctypes.POINTER(TopkProblem), i32, P, sz, P]),
@@ -194,6 +196,40 @@ def paged_mqa_logits(q, kv_pages, kscale, weights, page_table, context_lens, nex
         _p(context_lens), B, next_n, H, D, ps, P, _p(logits), logits.stride(0), _p(histogram),
         _p(amax), amax.stride(0) if amax is not None else 0, int(amax_skip_if_blocks_le),
         ws.ptr, ws.nbytes, _stream(stream)), "paged_mqa_logits")
+    return logits
+
+
+def paged_mqa_logits_mx(q, k_codes, k_exp, weights, page_table, context_lens, next_n, ws,
+                        logits=None, logits_stride=None, histogram=None, stream=None):
+    """Dense logits over an MXFP4 index-K cache: k_codes [P][ps][64] uint8
+    (two E2M1 codes per byte, even dimension in the low nibble), k_exp
+    [P][ps][4] uint8 (UE8M0, one per 32 dimensions).  Same outputs as
+    paged_mqa_logits (dead columns untouched, optional histogram)."""
+    q, k_codes, k_exp = _u8(q), _u8(k_codes), _u8(k_exp)
+    _req(q, torch.uint8, "q")
+    _req(k_codes, torch.uint8, "k_codes")
+    _req(k_exp, torch.uint8, "k_exp")
+    _req(weights, torch.float32, "weights")
+    _req(page_table, torch.int32, "page_table")
+    _req(context_lens, torch.int32, "context_lens")
+    R, H, D = q.shape
+    P, ps, Dh = k_codes.shape
+    B = context_lens.shape[0]
+    if R != B * next_n or 2 * Dh != D or tuple(k_exp.shape) != (P, ps, D // 32):
+        raise ValueError("shape mismatch between q, k_codes, k_exp and context_lens")
+    if logits is None:
+        if logits_stride is None:
+            raise ValueError("give logits or logits_stride")
+        logits = torch.empty((R, int(logits_stride)), dtype=torch.float32, device=q.device)
+    _req(logits, torch.float32, "logits")
+    if histogram is not None:
+        _req(histogram, torch.int32, "histogram")
+    for t in (q, k_codes, k_exp, weights, page_table, context_lens):
+        assert t.is_contiguous()
+    _check(lib.dsa_paged_mqa_logits_mx(
+        _p(q), _p(k_codes), _p(k_exp), _p(weights), _p(page_table), page_table.stride(0),
+        _p(context_lens), B, next_n, H, D, ps, P, _p(logits), logits.stride(0), _p(histogram),
+        ws.ptr, ws.nbytes, _stream(stream)), "paged_mqa_logits_mx")
     return logits
 
 

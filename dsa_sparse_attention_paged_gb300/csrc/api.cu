@@ -126,6 +126,25 @@ dsa_status_t make_tmap_rows128(CUtensorMap *map, const void *base, uint64_t rows
   return DSA_OK;
 }
 
+dsa_status_t make_tmap_rows_e2m1(CUtensorMap *map, const void *base, uint64_t rows,
+                                 uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return DSA_ERR_CUDA;
+  const cuuint64_t dims[2] = {128, rows};  // in 4-bit elements
+  const cuuint64_t strides[1] = {64};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void *>(base),
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_cuda_error = static_cast<int32_t>(r);
+    return DSA_ERR_CUDA;
+  }
+  return DSA_OK;
+}
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -238,6 +257,45 @@ int32_t dsa_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const fl
   c.kb = 0;
   c.status = status_word(workspace);
   c.wait_limit = kDefaultWaitLimit;
+  return run_paged_logits(c, static_cast<cudaStream_t>(stream));
+}
+
+int32_t dsa_paged_mqa_logits_mx(const uint8_t *q, const uint8_t *k_codes, const uint8_t *k_exp,
+                                const float *weights, const int32_t *page_table,
+                                int64_t page_table_stride, const int32_t *context_lens, int32_t B,
+                                int32_t next_n, int32_t num_heads, int32_t head_dim,
+                                int32_t page_size, int32_t num_pages, float *logits,
+                                int64_t logits_stride, int32_t *histogram, void *workspace,
+                                size_t ws_bytes, void *stream) {
+  int32_t e = check_paged_common(q, k_codes, reinterpret_cast<const float *>(k_exp), weights,
+                                 page_table, page_table_stride, context_lens, B, next_n,
+                                 num_heads, head_dim, page_size, num_pages, workspace, ws_bytes);
+  if (e != DSA_OK) return e;
+  if (!aligned(k_codes, 32)) return DSA_ERR_MISALIGNED;
+  if (!logits || logits_stride < 1) return DSA_ERR_INVALID_ARG;
+  if (histogram && !aligned(histogram, 8)) return DSA_ERR_MISALIGNED;
+  if (B == 0) return DSA_OK;
+  LogitsCall c{};
+  c.q = q;
+  c.kv = k_codes;
+  c.kscale = reinterpret_cast<const float *>(k_exp);  // 4 bytes a token, like kscale
+  c.weights = weights;
+  c.page_table = page_table;
+  c.pt_stride = page_table_stride;
+  c.context_lens = context_lens;
+  c.B = B;
+  c.next_n = next_n;
+  c.page_size = page_size;
+  c.num_pages = num_pages;
+  c.out = logits;
+  c.out_stride = logits_stride;
+  c.histogram = histogram;
+  c.amax = nullptr;
+  c.sparse = false;
+  c.out_fmt = DSA_OUT_F32;
+  c.status = status_word(workspace);
+  c.wait_limit = kDefaultWaitLimit;
+  c.mx = true;
   return run_paged_logits(c, static_cast<cudaStream_t>(stream));
 }
 

@@ -320,6 +320,69 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
          ((uint32_t)(M >> 4) << 24);
 }
 
+// D[tmem] (+)= (A[smem] * sA) * (B[smem] * sB)^T with block scale factors:
+// A E2M1 (MXFP4 keys, one UE8M0 exponent per 32 K-elements), B E4M3, FP32
+// accumulate; the scale factors are read from TMEM (sfa / sfb columns), the
+// byte within each 32-bit cell chosen by the scale-factor ids of `idesc`.
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], "
+      "[%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Instruction descriptor of the block-scaled kind::mxf8f6f4 MMA: A = E2M1,
+// B = E4M3, both K-major, D = FP32, N >> 3 at bit 17, UE8M0 scale factors
+// (bit 23), M >> 4 at bit 24, the A scale-factor byte id at bits 29-30 and
+// the B one at bits 4-5.
+__host__ __device__ constexpr uint32_t idesc_mx_e2m1_e4m3(int M, int N, int a_sf_id, int b_sf_id) {
+  return ((uint32_t)b_sf_id << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) |
+         (1u << 23) | ((uint32_t)(M >> 4) << 24) | ((uint32_t)a_sf_id << 29);
+}
+
+// Copy a 32-row x 16-byte shared-memory matrix into 32 TMEM lanes x 4 columns,
+// repeated in all four lane quarters (issued by one thread, ordered before the
+// MMAs it issues after it).
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// 32 lanes x 4 columns of 32-bit data from registers: thread i of the warp
+// writes columns taddr .. taddr + 3 of TMEM lane (warp's lane base + i).
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2,
+                                         uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v0), "r"(v1), "r"(v2), "r"(v3)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Generic-proxy shared-memory writes become visible to the async proxy
+// (tcgen05.cp / TMA reads) issued after this fence.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a plain (no swizzle) K-major operand:
+// core matrices of 8 rows x 16 bytes stored contiguously, `sbo` bytes between
+// 8-row groups, `lbo` bytes between core matrices along K.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(lbo >> 4) << 16;
+  d |= (uint64_t)(sbo >> 4) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version (sm_100 family); swizzle none
+  return d;
+}
+
 // Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
 // layout TMA writes (rows of 128 bytes, 8-row groups 1024 bytes apart).
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {

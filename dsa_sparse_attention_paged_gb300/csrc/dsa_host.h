@@ -44,10 +44,13 @@ struct LogitsCall {
   const int32_t *union_len = nullptr;
   uint32_t *status;
   long long wait_limit;
+  // MXFP4 keys: kv = E2M1 codes [slots][64] (two per byte, even dimension in
+  // the low nibble), kscale = the UE8M0 exponents [slots][4] (dense only)
+  bool mx = false;
 };
 
 dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st);
-int logits_stages_for(int next_n, bool hist);
+int logits_stages_for(int next_n, bool hist, bool mx = false);
 
 struct TopkCall {
   const float *logits;
@@ -138,6 +141,11 @@ dsa_status_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t 
 // --- utilities (api.cu) ---
 dsa_status_t make_tmap_rows128(CUtensorMap *map, const void *base, uint64_t rows,
                                uint32_t box_rows);
+// Rows of 128 E2M1 codes packed two per byte (64 bytes), copied into shared
+// memory unpacked to the 128-byte rows of an 8-bit operand (each 16 codes in
+// the first 8 bytes of a 16-byte chunk), 128-byte swizzle; base 32-byte aligned.
+dsa_status_t make_tmap_rows_e2m1(CUtensorMap *map, const void *base, uint64_t rows,
+                                 uint32_t box_rows);
 int num_sms();
 bool ensure_smem_attr(const void *fn, int bytes);
 dsa_status_t check_launch();

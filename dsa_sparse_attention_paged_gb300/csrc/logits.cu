@@ -101,7 +101,7 @@ struct LogitsArgs {
 };
 
 struct SmemPlan {
-  int kst, q, ks, w, hist, bar, misc, sptab, total;
+  int kst, q, ks, w, hist, bar, misc, sptab, sfst, total;
 };
 
 constexpr int kSpTab = 32;  // sparse: stages whose K rows the producer holds in shared memory
@@ -110,8 +110,12 @@ constexpr int kSpTab = 32;  // sparse: stages whose K rows the producer holds in
 // shared by the group's four warps otherwise (shared memory goes to stages).
 __host__ __device__ constexpr int hist_slots_per_group(int nn) { return nn == 1 ? 4 : 1; }
 
+// MXFP4 keys: per K stage, the block exponents of its two sub-tiles as the
+// 32-row x 16-byte tables the scale-factor copy into TMEM reads (2 x 512 B).
+constexpr int kSfStage = 1024;
+
 __host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, bool sparse, int stages, int nacc,
-                                              int nks) {
+                                              int nks, bool mx = false) {
   SmemPlan p;
   int off = 0;
   p.kst = off;
@@ -131,6 +135,9 @@ __host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, bool sparse, in
   off += 64 + 2 * 32 * 4;  // flags/schedule + the producer's two row tables
   p.sptab = off;
   off += sparse ? kSpTab * 32 * 4 : 0;
+  off = (off + 127) & ~127;
+  p.sfst = off;
+  off += mx ? stages * kSfStage : 0;
   p.total = off + 1024;  // slack to align the base to 1024 bytes
   return p;
 }
@@ -332,10 +339,14 @@ __device__ __forceinline__ float head_sum(const uint32_t (&v)[32], float ks, con
   return (c0 + c1) + (c2 + c3);
 }
 
-template <int NN, bool SPARSE, int OUT, bool HIST>
+// MX: the keys are MXFP4 (E2M1 codes through a 4-bit unpacking tensor map,
+// one UE8M0 exponent per 32 dimensions in place of kscale), multiplied by
+// the block-scaled MMA; dense logits only.
+template <int NN, bool SPARSE, int OUT, bool HIST, bool MX = false>
 __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const LogitsArgs a) {
+  static_assert(!(MX && SPARSE), "MXFP4 keys: dense logits only");
   // the dense pass waits for its predecessors at once; the sparse pass sets up
   // (barriers, schedule, TMEM, tensor maps: nothing a predecessor writes) first
   // dense, and paired sparse (whose schedule reads the union lengths): the
@@ -355,7 +366,7 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
   const int S = a.num_stages;
   const int A = a.num_acc;
   const int KS = a.num_ks;
-  const SmemPlan P = smem_plan(NN, HIST, SPARSE, S, A, KS);
+  const SmemPlan P = smem_plan(NN, HIST, SPARSE, S, A, KS, MX);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -389,7 +400,7 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
     }
     for (int k = 0; k < KS; ++k) {
       mbar_init(KSF(k), SPARSE ? 32 : 1);  // sparse: one cp.async arrival per producer lane
-      mbar_init(KSE(k), kStageEpiWarps);
+      mbar_init(KSE(k), MX ? 1 : kStageEpiWarps);  // MX: the MMA warp reads the exponents
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(QFULL(q), 1);
@@ -427,6 +438,22 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
   tc_fence_after();
   if (!kWaitFirst) pdl_wait();  // the block table, physical blocks and live lengths are ready
   const uint32_t tmem_base = *tmem_slot;
+  // MX TMEM beyond the accumulators: the A scale factors of the two
+  // sub-tiles (4 columns each, rewritten every stage in issue order with the
+  // MMAs), then the B scale factors, all 2^0 (UE8M0 127): queries are plain E4M3
+  const uint32_t sfa0 = tmem_base + 2u * (uint32_t)A * (uint32_t)N;
+  const uint32_t sfb = sfa0 + 64u;
+  if (MX) {
+    if (warp >= 2 && warp < 6) {  // one warp per TMEM lane quarter
+      const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
+      tmem_st4(sfb + lq, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      tmem_st4(sfb + lq + 4u, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
   const WaitCtl ctl{abort_flag, a.status, a.wait_limit};
 
   if (warp == 0) {
@@ -578,7 +605,8 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
       if (!ok) break;
       const uint32_t nload = (uint32_t)__popc(__ballot_sync(0xffffffffu, row >= 0));
       if (lane == 0) {
-        mbar_arrive_expect_tx(FULL(s), nload * (uint32_t)(blk_rows * 128));
+        // MX: the 4-bit unpacking copy counts the 64 packed bytes of a row
+        mbar_arrive_expect_tx(FULL(s), nload * (uint32_t)(blk_rows * (MX ? 64 : 128)));
         if (!SPARSE) mbar_arrive_expect_tx(KSF(kx), nload * (uint32_t)(blk_rows * 4));
       }
       __syncwarp();
@@ -631,6 +659,78 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
       for (int k2 = (q_issued > 2 ? q_issued - 2 : 0); k2 < q_issued; ++k2)
         mbar_wait_drain(QFULL(k2 & 1), (uint32_t)((k2 >> 1) & 1), lim);
     }
+  } else if (warp == 1 && MX) {
+    // ------------------------------------------------------------ MMA issuer, MXFP4 keys
+    // The whole warp turns the stage's 256 token exponent words (token order,
+    // byte j = exponent of dimensions 32j .. 32j+31) into the two tables the
+    // scale-factor copy reads: row i of sub-tile h holds the words of tokens
+    // i, i+32, i+64, i+96 of the sub-tile, which lands token m's exponents in
+    // TMEM lane m, column m / 32 of the sub-tile's A scale factors; the MMA
+    // for dimensions 32kk .. 32kk+31 takes byte kk.  Lane 0 waits and issues.
+    TileIter<SPARSE> it;
+    it.init(a, u_start, i_start);
+    int prev_u = -1, unit_ord = -1, qb = 0;
+    bool ok = true;
+    long long mmas = 0;
+    Ring rs, ra, rk;
+    rs.init(S);
+    ra.init(A);
+    rk.init(KS);
+    const uint32_t *kraw = reinterpret_cast<const uint32_t *>(ks_s);
+    for (long long n = 0; n < count; ++n, it.next(a), rs.next(), ra.next(), rk.next()) {
+      if (it.u != prev_u) {
+        ++unit_ord;
+        prev_u = it.u;
+        qb = unit_ord & 1;
+        if (lane == 0) ok = mbar_wait(QFULL(qb), (unit_ord >> 1) & 1, ctl);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+      const int s = rs.idx;
+      const int x = ra.idx;
+      const int kx = rk.idx;
+      if (lane == 0)
+        ok = mbar_wait(AEMPTY(x), ra.ph ^ 1, ctl) && mbar_wait(FULL(s), rs.ph, ctl) &&
+             mbar_wait(KSF(kx), rk.ph, ctl);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      uint8_t *stg = smem + P.sfst + s * kSfStage;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t *src = kraw + kx * kStageTok + h * kSubTok + lane;
+        *reinterpret_cast<uint4 *>(stg + h * 512 + 16 * lane) =
+            make_uint4(src[0], src[32], src[64], src[96]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(KSE(kx));  // the exponents of this ring slot are read
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tmem_cp_32x128b_x4(sfa0 + 32u * h, sdesc_plain(smem_u32(stg + h * 512), 128, 128));
+        const uint64_t bd = sdesc_sw128(qst + qb * (N * 128));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t d = tmem_base + (uint32_t)((2 * x + h) * N);
+          const uint64_t ad = sdesc_sw128(kst + s * kStageK + h * kSubK);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // K = 128 E2M1 = 4 steps of 32 (one exponent each)
+            mma_mx(d, ad + 2 * kk, bd + 2 * kk, idesc_mx_e2m1_e4m3(128, N, kk, kk), sfa0 + 32u * h,
+                   sfb, kk > 0 ? 1u : 0u);
+        }
+        ++mmas;
+        mma_commit(EMPTY(s));
+        mma_commit(AFULL(x));
+        if (it.i == it.tiles - 1 || n == count - 1) mma_commit(QEMPTY(qb));
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0 && mmas > 0) {
+      mma_commit(DRAIN);
+      mbar_wait_drain(DRAIN, 0, a.wait_limit);
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -870,10 +970,13 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
         pw = (uint32_t)__ldg(&a.upos[(int64_t)u * a.tab_stride + (pos >> 3)]);
       if (SPARSE && NN == 1 && !a.valid_lens && pos < (int64_t)a.kb * 8)
         blk = __ldg(&a.block_table[(int64_t)u * a.kb + pos / 8]);
-      if (!(ok = ewait(KSF(kx), rk.ph))) break;
-      const float ks = ks_s[kx * kStageTok + tok];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(KSE(kx));
+      float ks = 1.0f;  // MX: the block exponents were applied by the MMA
+      if (!MX) {
+        if (!(ok = ewait(KSF(kx), rk.ph))) break;
+        ks = ks_s[kx * kStageTok + tok];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(KSE(kx));
+      }
       if (!(ok = ewait(AFULL(x), ra.ph))) break;
       tc_fence_after();
       // head dots leave TMEM in batches of up to two rows, one row with 16
@@ -975,43 +1078,52 @@ struct LaunchPlan {
   int stages, nacc, nks, cols, smem;
 };
 
-inline LaunchPlan plan_for(int nn, bool hist, bool sparse) {
+inline LaunchPlan plan_for(int nn, bool hist, bool sparse, bool mx = false) {
   LaunchPlan L;
   const int N = 32 * nn;
-  L.nacc = std::min(4, 512 / (2 * N));  // TMEM pairs (two 128-lane sub-tiles each)
+  // TMEM pairs (two 128-lane sub-tiles each); MX keeps 96 columns after the
+  // pairs for the scale factors (two A regions and the B region, 32 apart)
+  L.nacc = std::min(4, 512 / (2 * N));
+  if (mx)
+    while (L.nacc > 1 && 2 * L.nacc * N + 96 > 512) --L.nacc;
   L.cols = 32;
-  while (L.cols < 2 * L.nacc * N) L.cols <<= 1;
+  while (L.cols < 2 * L.nacc * N + (mx ? 96 : 0)) L.cols <<= 1;
   L.stages = kMaxStages;
   while (L.stages > 2 &&
-         smem_plan(nn, hist, sparse, L.stages, L.nacc, L.stages + L.nacc + 2).total > kSmemLimit)
+         smem_plan(nn, hist, sparse, L.stages, L.nacc, L.stages + L.nacc + 2, mx).total > kSmemLimit)
     --L.stages;
   L.nks = L.stages + L.nacc + 2;
-  L.smem = smem_plan(nn, hist, sparse, L.stages, L.nacc, L.nks).total;
+  L.smem = smem_plan(nn, hist, sparse, L.stages, L.nacc, L.nks, mx).total;
   return L;
 }
 
-template <int NN, bool SPARSE, int OUT, bool HIST>
+template <int NN, bool SPARSE, int OUT, bool HIST, bool MX = false>
 dsa_status_t launch_one(const CUtensorMap &tk, const CUtensorMap &tq, const LogitsArgs &a0,
                         int grid, cudaStream_t st) {
   LogitsArgs a = a0;
-  const LaunchPlan L = plan_for(NN, HIST, SPARSE);
+  const LaunchPlan L = plan_for(NN, HIST, SPARSE, MX);
   a.num_acc = L.nacc;
   a.num_ks = L.nks;
   a.tmem_cols = (uint32_t)L.cols;
   a.num_stages = L.stages;
-  auto kfn = logits_kernel<NN, SPARSE, OUT, HIST>;
+  auto kfn = logits_kernel<NN, SPARSE, OUT, HIST, MX>;
   if (!ensure_smem_attr(reinterpret_cast<const void *>(kfn), L.smem)) return DSA_ERR_CUDA;
   return launch_pdl(kfn, dim3(grid), dim3(threads_for(NN, SPARSE)), (size_t)L.smem, st, tk, tq, a);
 }
 
 }  // namespace
 
-int logits_stages_for(int next_n, bool hist) { return plan_for(next_n, hist, false).stages; }
+int logits_stages_for(int next_n, bool hist, bool mx) {
+  return plan_for(next_n, hist, false, mx).stages;
+}
 
 dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   CUtensorMap tk, tq;
-  dsa_status_t e = make_tmap_rows128(&tk, c.kv, (uint64_t)c.num_pages * c.page_size,
-                                     c.sparse ? 8 : c.page_size);
+  if (c.mx && c.sparse) return DSA_ERR_UNSUPPORTED;
+  dsa_status_t e = c.mx ? make_tmap_rows_e2m1(&tk, c.kv, (uint64_t)c.num_pages * c.page_size,
+                                               c.page_size)
+                        : make_tmap_rows128(&tk, c.kv, (uint64_t)c.num_pages * c.page_size,
+                                            c.sparse ? 8 : c.page_size);
   if (e != DSA_OK) return e;
   const int nn = c.sparse ? (c.union_len ? 2 : 1) : c.next_n;
   e = make_tmap_rows128(&tq, c.q, (uint64_t)c.B * c.next_n * 32, 32 * nn);
@@ -1076,6 +1188,24 @@ dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   a.sparse_tpu = 0;
   const int grid = sms;
   const bool h = c.histogram != nullptr;
+  if (c.mx) {
+    switch (c.next_n) {
+      case 1:
+        return h ? launch_one<1, false, DSA_OUT_F32, true, true>(tk, tq, a, grid, st)
+                 : launch_one<1, false, DSA_OUT_F32, false, true>(tk, tq, a, grid, st);
+      case 2:
+        return h ? launch_one<2, false, DSA_OUT_F32, true, true>(tk, tq, a, grid, st)
+                 : launch_one<2, false, DSA_OUT_F32, false, true>(tk, tq, a, grid, st);
+      case 3:
+        return h ? launch_one<3, false, DSA_OUT_F32, true, true>(tk, tq, a, grid, st)
+                 : launch_one<3, false, DSA_OUT_F32, false, true>(tk, tq, a, grid, st);
+      case 4:
+        return h ? launch_one<4, false, DSA_OUT_F32, true, true>(tk, tq, a, grid, st)
+                 : launch_one<4, false, DSA_OUT_F32, false, true>(tk, tq, a, grid, st);
+      default:
+        return DSA_ERR_UNSUPPORTED;
+    }
+  }
   switch (c.next_n) {
     case 1:
       return h ? launch_one<1, false, DSA_OUT_F32, true>(tk, tq, a, grid, st)

@@ -144,6 +144,32 @@ int32_t dsa_paged_mqa_logits(const uint8_t *q, const uint8_t *kv_pages, const fl
                              int64_t amax_stride, int32_t amax_skip_if_blocks_le,
                              void *workspace, size_t ws_bytes, void *stream);
 
+/* ---- paged MQA logits over an MXFP4 index-K cache ------------------------
+ * The next index-key format the pages point to: [SG38944] (Hopper prefill
+ * commit text: block-scaled E2M1 index keys decoded to E4M3) and [VL52696]
+ * ("Why"; the MXFP4 indexer-cache tests with a packed 68-byte layout).  Per
+ * token: 128 E2M1 codes packed two per byte, dimension 2i in the low nibble
+ * of byte i (64 bytes), and 4 UE8M0 block exponents, exponent j covering
+ * dimensions 32j .. 32j+31 (4 bytes); k[d] = E2M1(code) * 2^(e[d / 32] - 127)
+ * and no per-token kscale.  The logits are those of dsa_paged_mqa_logits
+ * with that key and kscale = 1:
+ *   logits[r][t] = sum_h w[r][h] * ReLU(q[r][h] . k[t])  for t < n_r,
+ * computed on the block-scaled tensor-core MMA (E2M1 x E4M3, the exponents
+ * applied per 32-dimension block as scale factors).
+ *   k_codes  [num_pages][page_size][64] uint8, 32-byte aligned
+ *   k_exp    [num_pages][page_size][4] uint8, 16-byte aligned
+ * Every other argument, layout, the fused histogram and the error behaviour
+ * are those of dsa_paged_mqa_logits (no block-maxima output).  The pages
+ * restrict their fused histogram to FP8 keys; here the histogram is taken in
+ * the same epilogue for either key format. */
+int32_t dsa_paged_mqa_logits_mx(const uint8_t *q, const uint8_t *k_codes, const uint8_t *k_exp,
+                                const float *weights, const int32_t *page_table,
+                                int64_t page_table_stride, const int32_t *context_lens, int32_t B,
+                                int32_t next_n, int32_t num_heads, int32_t head_dim,
+                                int32_t page_size, int32_t num_pages, float *logits,
+                                int64_t logits_stride, int32_t *histogram, void *workspace,
+                                size_t ws_bytes, void *stream);
+
 /* ---- histogram-driven exact top-k ---------------------------------------
  * SGLang commit 7e252c5 (select.cuh, cross-referenced from [DG94]): per row,
  * find the threshold bin T from the coarse histogram (the bins above T hold

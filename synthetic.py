@@ -156,11 +156,12 @@ def generate(w: Workload) -> dict:
                page_table=page_table, context_lens=ctx, next_n=nn, page_size=ps,
                num_pages=P, H=H, D=D)
     if w.key_format == "mxfp4":
-        nib = torch.randint(0, 16, (P, ps, D), generator=g, dtype=torch.int32).numpy()
-        out["k_codes"] = np.ascontiguousarray((nib[..., 0::2] | (nib[..., 1::2] << 4))
-                                              .astype(np.uint8))
+        # uniform bytes are uniform pairs of E2M1 codes (drawn packed: a
+        # 128K-token cache holds 2^29 codes)
+        out["k_codes"] = torch.randint(0, 256, (P, ps, D // 2), generator=g,
+                                       dtype=torch.uint8).numpy()
         out["k_exp"] = torch.randint(125, 130, (P, ps, D // 32), generator=g,
-                                     dtype=torch.int32).numpy().astype(np.uint8)
+                                     dtype=torch.uint8).numpy()
     elif w.key_format != "fp8":
         raise ValueError(w.key_format)
     return out

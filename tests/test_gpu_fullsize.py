@@ -1,8 +1,12 @@
 """Full-size parity on the five named workloads, in the launch configuration
-the bench times (DecodePlan): logits on sampled (row, column) pairs against
-the oracle one by one; histograms, top-k sets, block tables and the FP16
-select exactly, on the GPU's own logits; sparse logits bitwise against the
-dense logits at the chosen positions."""
+the bench times (DecodePlan): every live logit against the oracle (one
+request per task of a process pool); histograms, top-k sets, block tables
+and the FP16 select exactly, on the GPU's own logits; sparse logits bitwise
+against the dense logits at the chosen positions.  MXFP4 keys at the
+largest workload's shape: sampled logits against the oracle one by one."""
+import multiprocessing as mp
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -13,9 +17,39 @@ from tests.helpers import assert_close, sets_equal, to_dev
 
 pytestmark = pytest.mark.gpu
 
+_CASE_KEYS = ("q", "kv", "kscale", "weights", "page_table", "context_lens")
+
+
+def _oracle_request_logits(args):
+    """One request's dense logits [next_n][stride] from the case saved in
+    `folder` (memory-mapped, so the workers share one copy)."""
+    folder, b, nn, ps, stride = args
+    c = {k: np.load(os.path.join(folder, k + ".npy"), mmap_mode="r") for k in _CASE_KEYS}
+    return b, O.paged_mqa_logits(c["q"][b * nn:(b + 1) * nn], c["kv"], c["kscale"],
+                                 c["weights"][b * nn:(b + 1) * nn], c["page_table"][b:b + 1],
+                                 c["context_lens"][b:b + 1], nn, ps, logits_stride=stride)
+
+
+@pytest.fixture(scope="module")
+def oracle_pool():
+    ctx = mp.get_context("spawn")  # no fork after the GPU is in use
+    with ctx.Pool(min(16, os.cpu_count() or 1)) as pool:
+        yield pool
+
+
+def _oracle_logits_all(case, nn, ps, stride, folder, pool):
+    for k in _CASE_KEYS:
+        np.save(os.path.join(folder, k + ".npy"), np.ascontiguousarray(case[k]))
+    B = len(case["context_lens"])
+    ref = np.full((B * nn, stride), np.nan, np.float32)
+    for b, Lb in pool.imap_unordered(_oracle_request_logits,
+                                      [(folder, b, nn, ps, stride) for b in range(B)]):
+        ref[b * nn:(b + 1) * nn] = Lb
+    return ref
+
 
 @pytest.mark.parametrize("name", ["c0", "c1", "c2", "c3", "c3u", "c4"])
-def test_full_size_workload(name):
+def test_full_size_workload(name, oracle_pool, tmp_path):
     from dsa_sparse_attention_paged_gb300.pipeline import DecodePlan
     w = S.named(name)
     case = S.generate(w)
@@ -31,15 +65,10 @@ def test_full_size_workload(name):
     rl = O.row_lens(case["context_lens"], nn)
     L = plan.logits.cpu().numpy()
 
-    # logits: 8192 sampled live positions (plus every row's first and last column)
-    rng = np.random.default_rng(1)
-    rows = rng.integers(0, R, 8192)
-    cols = (rng.random(8192) * rl[rows]).astype(np.int64)
-    rows = np.concatenate([rows, np.arange(R), np.arange(R)])
-    cols = np.concatenate([cols, np.zeros(R, np.int64), rl - 1])
-    ref = O.logits_at(case["q"], case["kv"], case["kscale"], case["weights"],
-                      case["page_table"], nn, ps, rows, cols)
-    assert_close(L[rows, cols], ref, f"{name} logits")
+    # logits: every live position against the oracle
+    ref = _oracle_logits_all(case, nn, ps, plan.stride, str(tmp_path), oracle_pool)
+    live = np.arange(plan.stride)[None, :] < rl[:, None]
+    assert_close(L[live], ref[live], f"{name} logits")
 
     # histogram of the GPU's own logits (the plan's top-k reset it, so rerun)
     hist = torch.zeros((R, 1024), dtype=torch.int32, device="cuda")
@@ -86,3 +115,36 @@ def test_full_size_workload(name):
         np.testing.assert_array_equal(SP16[r, :n_live], O.fp16_rn_array(L[r, tok[:n_live]]))
         assert (SP16[r, n_live:] == 0xFC00).all()
     assert sets_equal(sparse_idx.cpu().numpy(), O.topk_fp16(SP16, v_ref, 2048, t_ref))
+
+
+def test_full_size_mxfp4_keys_largest_shape():
+    """MXFP4 keys at B=32, L=131072 (page 64): the launch the bench times for
+    the MXFP4 key stream; 8192 sampled live logits plus every row's first and
+    last column against the oracle, and the fused histogram on the GPU's own
+    logits."""
+    import dsa_sparse_attention_paged_gb300 as D
+    w = S.named("c2")
+    case = S.generate(w)
+    g = torch.Generator().manual_seed(w.seed + 1000)
+    P = case["num_pages"]
+    codes = torch.randint(0, 256, (P, w.page_size, 64), generator=g, dtype=torch.uint8)
+    exps = torch.randint(125, 130, (P, w.page_size, 4), generator=g, dtype=torch.uint8)
+    d = to_dev(case)
+    R, stride = w.R, 131072
+    ws = D.Workspace(R)
+    hist = torch.zeros((R, 1024), dtype=torch.int32, device="cuda")
+    L = D.paged_mqa_logits_mx(d["q"], codes.cuda(), exps.cuda(), d["weights"], d["page_table"],
+                              d["context_lens"], 1, ws, logits_stride=stride, histogram=hist)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    L = L.cpu().numpy()
+    rl = O.row_lens(case["context_lens"], 1)
+    rng = np.random.default_rng(2)
+    rows = rng.integers(0, R, 8192)
+    cols = (rng.random(8192) * rl[rows]).astype(np.int64)
+    rows = np.concatenate([rows, np.arange(R), np.arange(R)])
+    cols = np.concatenate([cols, np.zeros(R, np.int64), rl - 1])
+    ref = O.logits_at_mx(case["q"], codes.numpy(), exps.numpy(), case["weights"],
+                         case["page_table"], 1, w.page_size, rows, cols)
+    assert_close(L[rows, cols], ref, "MXFP4 logits")
+    np.testing.assert_array_equal(hist.cpu().numpy(), O.histogram(L, rl))
