@@ -42,7 +42,9 @@ class TopkProblem(ctypes.Structure):
                 ("block_out_idx", ctypes.c_void_p), ("block_fallback_flags", ctypes.c_void_p),
                 ("next_n", ctypes.c_int32), ("len_div", ctypes.c_int32), ("R", ctypes.c_int32),
                 ("reset_histogram", ctypes.c_int32), ("k", ctypes.c_int32),
-                ("block_k", ctypes.c_int32)]
+                ("block_k", ctypes.c_int32), ("block_page_table", ctypes.c_void_p),
+                ("block_page_table_stride", ctypes.c_int64), ("block_page_size", ctypes.c_int32),
+                ("block_phys", ctypes.c_void_p), ("block_valid_lens", ctypes.c_void_p)]
 
 
 TOPK_BATCH_MAX = 4
@@ -255,7 +257,8 @@ def coarse_hist_topk(logits, context_lens, next_n, k, ws, histogram=None, reset_
 
 def _topk_problem(logits, context_lens, next_n, k, histogram=None, reset_histogram=False,
                   len_div=1, out=None, fallback_flags=None, R=None, block_k=0, block_out=None,
-                  block_fallback_flags=None):
+                  block_fallback_flags=None, block_page_table=None, block_page_size=0,
+                  block_phys=None, block_valid_lens=None):
     _req(logits, torch.float32, "logits")
     _req(context_lens, torch.int32, "context_lens")
     R = logits.shape[0] if R is None else R
@@ -280,13 +283,26 @@ def _topk_problem(logits, context_lens, next_n, k, histogram=None, reset_histogr
                        else None,
                        int(next_n), int(len_div), int(R), 1 if reset_histogram else 0, int(k),
                        int(block_k))
+    if block_page_table is not None:
+        _req(block_page_table, torch.int32, "block_page_table")
+        prob.block_page_table = block_page_table.data_ptr()
+        prob.block_page_table_stride = block_page_table.stride(0)
+        prob.block_page_size = int(block_page_size)
+        if block_phys is not None:
+            _req(block_phys, torch.int32, "block_phys")
+            prob.block_phys = block_phys.data_ptr()
+        if block_valid_lens is not None:
+            _req(block_valid_lens, torch.int32, "block_valid_lens")
+            prob.block_valid_lens = block_valid_lens.data_ptr()
     return prob, ((out, block_out) if block_k else out)
 
 
 def coarse_hist_topk_batch(problems, ws, stream=None):
     """Several independent ``coarse_hist_topk`` problems (dicts of its keyword
     arguments, plus ``block_k`` / ``block_out`` / ``block_fallback_flags`` for
-    the fused top block maxima) with one workspace sized for the sum of their
+    the fused top block maxima, and ``block_page_table`` / ``block_page_size``
+    / ``block_phys`` / ``block_valid_lens`` to have the block output written
+    as the sorted block table) with one workspace sized for the sum of their
     rows; one launch when every row stride is at most 131072.  Returns per
     problem its output tensor, or (output, block output) with block_k."""
     if len(problems) > TOPK_BATCH_MAX:

@@ -421,6 +421,17 @@ int32_t dsa_coarse_hist_topk_batch(const dsa_topk_problem *problems, int32_t cou
       c.block_flags = pb.block_fallback_flags;
       c.block_k = pb.block_k;
       blocks = true;
+      if (pb.block_page_table) {
+        if (pb.block_page_size != 64 && pb.block_page_size != 128) return DSA_ERR_UNSUPPORTED;
+        if (pb.block_page_table_stride < 1) return DSA_ERR_INVALID_ARG;
+        c.block_pt = pb.block_page_table;
+        c.block_pt_stride = pb.block_page_table_stride;
+        c.block_ps = pb.block_page_size;
+        c.block_phys = pb.block_phys;
+        c.block_valid = pb.block_valid_lens;
+      }
+    } else if (pb.block_page_table) {
+      return DSA_ERR_INVALID_ARG;
     }
     rows_needed += c.R;
     calls[n++] = c;

@@ -65,6 +65,13 @@ struct TopkCall {
   int32_t *block_out = nullptr;    // also the top block_k block maxima per row (one launch only)
   int32_t *block_flags = nullptr;
   int32_t block_k = 0;
+  // block output written as the sorted block table (with physical blocks and
+  // live lengths) when block_pt is set
+  const int32_t *block_pt = nullptr;
+  int64_t block_pt_stride = 0;
+  int32_t block_ps = 0;
+  int32_t *block_phys = nullptr;
+  int32_t *block_valid = nullptr;
   void *workspace;
   int32_t ws_rows;           // rows the workspace was sized for
   bool allow_cluster = true; // rows up to 131072 may take the cluster kernel

@@ -108,7 +108,13 @@ constexpr int kSpTab = 32;  // sparse: stages whose K rows the producer holds in
 
 // Histogram slots per epilogue warpgroup: one per warp at next_n = 1, one
 // shared by the group's four warps otherwise (shared memory goes to stages).
+// A slot holds 16-bit counts, two bins to a 32-bit word (bin 2p in the low
+// half of word p), and is flushed on every change of request and at least
+// every kHistFlushStages stages, so no count reaches 2^16: a slot counts at
+// most 128 tokens a stage.
 __host__ __device__ constexpr int hist_slots_per_group(int nn) { return nn == 1 ? 4 : 1; }
+constexpr int kHistWords = DSA_NUM_BINS / 2;  // 32-bit words of one slot row
+constexpr int kHistFlushStages = 256;
 
 // MXFP4 keys: per K stage, the block exponents of its two sub-tiles as the
 // 32-row x 16-byte tables the scale-factor copy into TMEM reads (2 x 512 B).
@@ -127,7 +133,7 @@ __host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, bool sparse, in
   p.w = off;
   off += 2 * nn * 32 * 4;
   p.hist = off;
-  off += hist ? 2 * hist_slots_per_group(nn) * nn * DSA_NUM_BINS * 4 : 0;
+  off += hist ? 2 * hist_slots_per_group(nn) * nn * kHistWords * 4 : 0;
   off = (off + 7) & ~7;
   p.bar = off;
   off += (2 * stages + 2 * nks + 4 + 2 * nacc + 3) * 8;
@@ -342,6 +348,42 @@ __device__ __forceinline__ float head_sum(const uint32_t (&v)[32], float ks, con
 // MX: the keys are MXFP4 (E2M1 codes through a 4-bit unpacking tensor map,
 // one UE8M0 exponent per 32 dimensions in place of kscale), multiplied by
 // the block-scaled MMA; dense logits only.
+// head_sum in two calls of 16 heads each (heads 16p .. 16p+15 for p = 0, 1,
+// in that order): the same chains in the same order, so the same float.
+__device__ __forceinline__ void head_sum_part(const uint32_t (&v)[16], float ks, const float *w,
+                                              uint64_t &a01, uint64_t &a23) {
+  if (ks >= 0.0f && ks <= 3.4028234e38f) {
+#pragma unroll
+    for (int h = 0; h < 16; h += 4) {
+      const float4 wv = *reinterpret_cast<const float4 *>(w + h);
+      a01 = fma2(pk2(wv.x, wv.y),
+                 pk2(fmaxf(__uint_as_float(v[h + 0]), 0.0f), fmaxf(__uint_as_float(v[h + 1]), 0.0f)),
+                 a01);
+      a23 = fma2(pk2(wv.z, wv.w),
+                 pk2(fmaxf(__uint_as_float(v[h + 2]), 0.0f), fmaxf(__uint_as_float(v[h + 3]), 0.0f)),
+                 a23);
+    }
+    return;
+  }
+  const uint64_t ks2 = pk2(ks, ks);
+#pragma unroll
+  for (int h = 0; h < 16; h += 4) {
+    const float4 wv = *reinterpret_cast<const float4 *>(w + h);
+    float p0, p1, p2, p3;
+    upk2(mul2(pk2(__uint_as_float(v[h + 0]), __uint_as_float(v[h + 1])), ks2), p0, p1);
+    upk2(mul2(pk2(__uint_as_float(v[h + 2]), __uint_as_float(v[h + 3])), ks2), p2, p3);
+    a01 = fma2(pk2(wv.x, wv.y), pk2(fmaxf(p0, 0.0f), fmaxf(p1, 0.0f)), a01);
+    a23 = fma2(pk2(wv.z, wv.w), pk2(fmaxf(p2, 0.0f), fmaxf(p3, 0.0f)), a23);
+  }
+}
+__device__ __forceinline__ float head_sum_finish(float ks, uint64_t a01, uint64_t a23) {
+  float c0, c1, c2, c3;
+  upk2(a01, c0, c1);
+  upk2(a23, c2, c3);
+  const float s = (c0 + c1) + (c2 + c3);
+  return (ks >= 0.0f && ks <= 3.4028234e38f) ? ks * s : s;
+}
+
 template <int NN, bool SPARSE, int OUT, bool HIST, bool MX = false>
 __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
@@ -374,7 +416,7 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
   const uint32_t qst = smem_u32(smem + P.q);
   float *ks_s = reinterpret_cast<float *>(smem + P.ks);
   float *w_s = reinterpret_cast<float *>(smem + P.w);
-  int *hist_s = reinterpret_cast<int *>(smem + P.hist);
+  uint32_t *hist_s = reinterpret_cast<uint32_t *>(smem + P.hist);
   const uint32_t bar0 = smem_u32(smem + P.bar);
   // barrier map
   auto FULL = [&](int s) { return bar0 + 8u * s; };                       // K landed
@@ -418,7 +460,7 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
   }
   if (warp == 0) compute_sched<SPARSE>(a, &sched[0], &sched[1], sched_cnt);
   if (HIST) {
-    for (int i = threadIdx.x; i < 2 * HS * NN * DSA_NUM_BINS; i += kThr) hist_s[i] = 0;
+    for (int i = threadIdx.x; i < 2 * HS * NN * kHistWords; i += kThr) hist_s[i] = 0;
   }
   __syncthreads();
   const long long count = *sched_cnt;
@@ -858,8 +900,8 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
     const int tok = g * kSubTok + lane_base + lane;   // token within the stage
     const int gtid = par * 128 + ((warp - 2) & 3) * 32 + lane;  // within the sub-tile's warps
     const uint64_t out_pol = policy_evict_last();
-    int *grp_hist = hist_s + g * HS * NN * DSA_NUM_BINS;
-    int *my_hist = grp_hist + (HS == 4 ? quarter : 0) * NN * DSA_NUM_BINS;
+    uint32_t *grp_hist = hist_s + g * HS * NN * kHistWords;
+    uint32_t *my_hist = grp_hist + (HS == 4 ? quarter : 0) * NN * kHistWords;
     TileIter<SPARSE> it;
     it.init(a, u_start, i_start);
     int prev_u = -1, unit_ord = -1, qb = 0;
@@ -902,20 +944,19 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
       gsync_ph ^= 1;
       return r;
     };
-    // add this group's counts for the finished request to the global
+    // add this group's counts of the current request to the global
     // histogram (packed 64-bit atomics on bin pairs) and clear its slots
     auto flush = [&](int rb) -> bool {
       if (!group_sync()) return false;
       for (int j = 0; j < NN; ++j) {
-        for (int p = gtid; p < DSA_NUM_BINS / 2; p += 128 * NPAR) {
+        for (int p = gtid; p < kHistWords; p += 128 * NPAR) {
           uint32_t c0 = 0, c1 = 0;
 #pragma unroll
           for (int w = 0; w < HS; ++w) {
-            int *sl = grp_hist + (w * NN + j) * DSA_NUM_BINS + 2 * p;
-            c0 += sl[0];
-            c1 += sl[1];
-            sl[0] = 0;
-            sl[1] = 0;
+            uint32_t *sl = grp_hist + (w * NN + j) * kHistWords + p;
+            c0 += *sl & 0xFFFFu;
+            c1 += *sl >> 16;
+            *sl = 0;
           }
           if (c0 | c1) {
             unsigned long long *gp = reinterpret_cast<unsigned long long *>(
@@ -930,12 +971,18 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
     Ring ra, rk;
     ra.init(A);
     rk.init(KS);
+    int since_flush = 0;  // stages counted into the slots since their last flush
     for (long long n = 0; n < count; ++n, it.next(a), ra.next(), rk.next()) {
       const int u = it.u, i = it.i;
+      if (HIST && u == prev_u && ++since_flush >= kHistFlushStages) {
+        if (!(ok = flush(row_base))) break;  // every warp of the group walks every stage
+        since_flush = 0;
+      }
       if (u != prev_u) {
         if (HIST && prev_u >= 0) {
           if (!(ok = flush(row_base))) break;
         }
+        since_flush = 0;
         ++unit_ord;
         prev_u = u;
         qb = unit_ord & 1;
@@ -979,13 +1026,34 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
       }
       if (!(ok = ewait(AFULL(x), ra.ph))) break;
       tc_fence_after();
-      // head dots leave TMEM in batches of up to two rows, one row with 16
-      // epilogue warps (one wait per batch; 576 threads leave 96 registers
-      // a thread); the accumulator goes back to the MMA as soon as the last
-      // batch is in registers
+      // head dots leave TMEM in batches of up to two rows; with 16 epilogue
+      // warps (576 threads leave 96 registers a thread) in half rows of 16
+      // heads, the load of the next half in flight while one is summed.  The
+      // accumulator goes back to the MMA as soon as the last load is in.
       float acc[NN];
       const uint32_t tcol = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)((2 * x + g) * N);
       constexpr int kB = NN == 1 ? 1 : (EW == 8 ? 2 : 1);
+      if constexpr (EW == 16) {
+        const float *wq = w_s + qb * N;
+        uint32_t hv[2][16];
+        uint64_t c01 = 0, c23 = 0;
+        tmem_ld16(tcol, hv[0]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int step = 0; step < 2 * NN; ++step) {  // row step / 2, heads 16 (step % 2) ..
+          if (step + 1 < 2 * NN) {
+            tmem_ld16(tcol + (uint32_t)((step + 1) * 16), hv[(step + 1) & 1]);
+          } else {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(AEMPTY(x));
+          }
+          if ((step & 1) == 0) c01 = c23 = pk2(0.0f, 0.0f);
+          head_sum_part(hv[step & 1], ks, wq + 16 * step, c01, c23);
+          if (step & 1) acc[step >> 1] = head_sum_finish(ks, c01, c23);
+          if (step + 1 < 2 * NN) tmem_ld_wait();
+        }
+      } else {
 #pragma unroll
       for (int j0 = 0; j0 < NN; j0 += kB) {
         uint32_t v[kB][32];
@@ -1001,6 +1069,7 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
 #pragma unroll
         for (int jj = 0; jj < kB; ++jj)
           if (j0 + jj < NN) acc[j0 + jj] = head_sum(v[jj], ks, w_s + qb * N + (j0 + jj) * 32);
+      }
       }
 
       if (SPARSE && NN == 2) {
@@ -1028,7 +1097,7 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
                         acc[j], out_pol);
             if (HIST) {
               const int bin = coarse_bin(acc[j]);
-              if (bin >= 0) atomicAdd(&my_hist[j * DSA_NUM_BINS + bin], 1);
+              if (bin >= 0) atomicAdd(&my_hist[j * kHistWords + (bin >> 1)], 1u << (16 * (bin & 1)));
             }
           }
           if (a.amax != nullptr) {

@@ -766,6 +766,7 @@ static_assert(sizeof(uint4) * kClVec * kClThreads >= sizeof(unsigned long long) 
               "the refine reuses the key buffer for the candidates");
 static_assert(sizeof(uint4) * kClVec * kClThreads >= sizeof(uint32_t) * (kClRow / 8),
               "the whole-row block select keeps every block maximum in the key buffer");
+static_assert(kClBlk >= DSA_MAX_TOPK, "the block-key buffer holds the chosen block ids");
 
 struct ClProb {
   const float *logits;
@@ -783,6 +784,12 @@ struct ClProb {
   int ws_row0;    // first workspace row of this problem
   int local;      // rows of at most kClChunk: one CTA per row
   int vec;        // rows 16-byte aligned: vector loads
+  // block output as the sorted block table, or bpt = NULL
+  const int32_t *bpt;
+  int64_t bpt_stride;
+  int bps;
+  int32_t *bphys;
+  int32_t *bvalid;
 };
 
 struct ClArgs {
@@ -1145,6 +1152,81 @@ __device__ __noinline__ int cl_finish(const float *row, int64_t n, int k, int32_
 __device__ __forceinline__ uint32_t max_key8(float4 a, float4 b) {
   return max(max(max(key_or_zero(a.x), key_or_zero(a.y)), max(key_or_zero(a.z), key_or_zero(a.w))),
              max(max(key_or_zero(b.x), key_or_zero(b.y)), max(key_or_zero(b.z), key_or_zero(b.w))));
+}
+
+// The selected block ids of a row (ids[0..bk), any order, -1 padding) become
+// the sorted block table out[0..bk) -- ascending, INT32_MAX padded -- with the
+// physical block of each (pool slot / 8 through the request's page-table row)
+// and the row's live length (the chosen blocks hold a prefix of the live
+// positions: the newest, partial block is the largest id), by a counting
+// sort over a bitmap of the row's nbk blocks ([SG38944]
+// sort_candidate_blocks).  A row of at most bk blocks takes the identity
+// table 0 .. nbk-1, whatever was selected.  Every thread calls it; bm holds
+// nbk bits.
+__device__ __noinline__ void cl_sort_table(const int32_t *ids, int32_t *out, int bk, int64_t n,
+                                           int64_t nbk,
+                                           const int32_t *pt_row, int ps, int32_t *phys,
+                                           int32_t *valid, uint32_t *bm, int *sm_scan,
+                                           long long *sm_live) {
+  auto phys_of = [&](int64_t id) -> int32_t {
+    const int64_t tok = id * 8;
+    const int64_t pg = __ldg(&pt_row[tok / ps]);
+    return (int32_t)((pg * ps + tok % ps) / 8);
+  };
+  if (nbk <= bk) {
+    for (int i = threadIdx.x; i < bk; i += kClThreads) {
+      out[i] = i < nbk ? i : INT32_MAX;
+      if (phys) phys[i] = i < nbk ? phys_of(i) : INT32_MAX;
+    }
+    if (valid && threadIdx.x == 0) *valid = (int32_t)n;
+    __syncthreads();
+    return;
+  }
+  const int W = (int)((nbk + 31) / 32);
+  for (int w = threadIdx.x; w < W; w += kClThreads) bm[w] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < bk; i += kClThreads) {
+    const int32_t id = ids[i];
+    if (id >= 0 && id < nbk) atomicOr(&bm[id >> 5], 1u << (id & 31));
+  }
+  __syncthreads();
+  const int per = (W + kClThreads - 1) / kClThreads;
+  const int w0 = threadIdx.x * per, w1 = min(W, w0 + per);
+  int c = 0;
+  for (int w = w0; w < w1; ++w) c += __popc(bm[w]);
+  int total;
+  int pos = block_excl_scan(c, sm_scan, &total);
+  long long live = 0;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t m = bm[w];
+    while (m) {
+      const int bit = __ffs(m) - 1;
+      m &= m - 1;
+      const int64_t id = (int64_t)w * 32 + bit;
+      if (pos < bk) {
+        out[pos] = (int32_t)id;
+        if (phys) phys[pos] = phys_of(id);
+      }
+      ++pos;
+      const int64_t in_blk = n - id * 8;
+      live += in_blk < 8 ? in_blk : 8;
+    }
+  }
+  for (int i = total + threadIdx.x; i < bk; i += kClThreads) {
+    out[i] = INT32_MAX;
+    if (phys) phys[i] = INT32_MAX;
+  }
+  if (valid) {
+    live = __reduce_add_sync(0xffffffffu, (unsigned)live);
+    if ((threadIdx.x & 31) == 0) sm_live[threadIdx.x >> 5] = live;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      long long s2 = 0;
+      for (int i = 0; i < kClThreads / 32; ++i) s2 += sm_live[i];
+      *valid = (int32_t)s2;
+    }
+  }
+  __syncthreads();
 }
 
 // Last step of the block select, run by one CTA: nbc block candidates (every
@@ -1542,7 +1624,10 @@ __global__ void __launch_bounds__(kClThreads, 2)
   else __syncthreads();
 
   // ---- 5. check, rank or refine, or fall back: the score select on CTA 0
-  // (the local CTA), the block select on CTA 1 (the local CTA, after)
+  // (the local CTA), the block select on CTA 1 (the local CTA, after).  The
+  // next kernel (the sparse logits over the block table) may set itself up
+  // on the SMs the other CTAs leave; it waits for this grid before reading.
+  pdl_release_dependents();
   unsigned long long *scratch = reinterpret_cast<unsigned long long *>(sm.keys);
   if (local || rank == 0) {
     const int emitted = (int)(sm.ctr & 0xFFFFFFFFull);
@@ -1561,10 +1646,21 @@ __global__ void __launch_bounds__(kClThreads, 2)
   }
   if (blk && (local || rank == 1)) {
     __syncthreads();  // the local CTA: the score select's finish is done with the scratch
-    const int flag = cl_block_finish(row, n, p.vec != 0, bk, boutr, btake, sm.bctr, sm.bsel,
+    // with a table to write, the chosen ids go to this CTA's block-key buffer
+    // (free after the last cluster barrier) and are sorted from there
+    int32_t *ids = p.bpt ? reinterpret_cast<int32_t *>(sm.bkey) : boutr;
+    const int flag = cl_block_finish(row, n, p.vec != 0, bk, ids, btake, sm.bctr, sm.bsel,
                                      reinterpret_cast<uint32_t *>(sm.keys), sm.hist, sm_h, sm_scan,
                                      sm_misc);
     if (p.bflags && threadIdx.x == 0) p.bflags[r] = flag;
+    if (p.bpt) {
+      __syncthreads();  // the block ids are in place
+      __shared__ long long sm_live[kClThreads / 32];
+      cl_sort_table(ids, boutr, bk, n, nbk, p.bpt + (int64_t)(r / p.next_n) * p.bpt_stride, p.bps,
+                    p.bphys ? p.bphys + (int64_t)r * bk : nullptr,
+                    p.bvalid ? p.bvalid + r : nullptr, reinterpret_cast<uint32_t *>(sm.hist),
+                    sm_scan, sm_live);
+    }
   }
 }
 
@@ -1879,6 +1975,11 @@ dsa_status_t run_cluster_select(const TopkCall *calls, int count, cudaStream_t s
     p.bk = c.block_out ? c.block_k : 0;
     p.ws_row0 = (int)row0;
     p.local = c.stride <= kClChunk ? 1 : 0;
+    p.bpt = c.block_out ? c.block_pt : nullptr;
+    p.bpt_stride = c.block_pt_stride;
+    p.bps = c.block_ps;
+    p.bphys = c.block_phys;
+    p.bvalid = c.block_valid;
     p.vec = ((reinterpret_cast<uintptr_t>(c.logits) & 15) == 0 && c.stride % 4 == 0) ? 1 : 0;
     ca.cl_begin[i] = (int)clusters;
     clusters += p.local ? (c.R + kCl - 1) / kCl : c.R;

@@ -12,8 +12,9 @@ step's device buffers and the workspace, and each ``step`` runs
                  for rows up to 131072 scores; longer rows: block
                  maxima fused into the logits pass and a second
                  problem of the batched select instead)
-  level one      sort_candidate_blocks -> table, phys, valid lens   (1 launch)
-                 (pair_rows: the paired sort, which also emits the
+  level one      sort_candidate_blocks -> table, phys, valid lens   (inside the
+                 select launch for rows a cluster takes; else 1 launch;
+                 pair_rows: the paired sort, which also emits the
                  union of each two-row unit's tables)
   consumer       sparse MQA logits over the table, FP16 output      (1 launch)
                  (pair_rows: two rows of a request per K pass)
@@ -84,7 +85,14 @@ class DecodePlan:
         else:
             sel = coarse_hist_topk_batch_launches([(self.stride, True, self.R),
                                                    (self.amax_stride, False, self.R)])
-        return 1 + sel + 1 + 1 + 1
+        sort = 0 if self.fused_table else 1
+        return 1 + sel + sort + 1 + 1
+
+    @property
+    def fused_table(self) -> bool:
+        """The sorted block table comes out of the select launch (rows a
+        cluster takes, unpaired rows): no separate sort launch."""
+        return self.two_level and self.fused_blocks and self.union is None
 
     def step(self, q, kv, kscale, weights, page_table, context_lens, events=None):
         """Run one decode step.  ``events`` (optional dict name -> (start, end)
@@ -109,7 +117,12 @@ class DecodePlan:
         mark("select", 0)
         dense = dict(logits=self.logits, context_lens=context_lens, next_n=nn, k=self.k,
                      histogram=self.hist, reset_histogram=True, out=self.topk_idx)
-        if self.fused_blocks:
+        if self.fused_table:
+            coarse_hist_topk_batch([dict(dense, block_k=self.kb, block_out=self.block_ids,
+                                         block_page_table=page_table,
+                                         block_page_size=self.page_size, block_phys=self.phys,
+                                         block_valid_lens=self.valid_lens)], ws)
+        elif self.fused_blocks:
             coarse_hist_topk_batch([dict(dense, block_k=self.kb, block_out=self.block_ids)], ws)
         else:
             coarse_hist_topk_batch([dense, dict(
@@ -117,7 +130,9 @@ class DecodePlan:
                 out=self.block_ids)], ws)
         mark("select", 1)
         mark("publish", 0)
-        if self.union is not None:
+        if self.fused_table:
+            pass  # the select launch wrote the sorted table, physical blocks, live lengths
+        elif self.union is not None:
             sort_candidate_blocks_paired(self.block_ids, context_lens, nn, page_table,
                                          self.page_size, ws, self.valid_lens, self.union,
                                          phys_blocks=self.phys)

@@ -262,6 +262,17 @@ typedef struct dsa_topk_problem {
   int32_t reset_histogram;
   int32_t k;
   int32_t block_k;                /* 0: no block output */
+  /* NULL, or the block output becomes the sorted block table of
+   * [SG38944] sort_candidate_blocks in the same launch: exactly what
+   * dsa_sort_candidate_blocks (row_to_req NULL, next_n as above) writes for
+   * these block ids -- ascending, INT32_MAX padded, the identity table for
+   * rows of at most block_k blocks -- with its physical blocks and live
+   * lengths (either may be NULL) */
+  const int32_t *block_page_table;  /* [B][block_page_table_stride] */
+  int64_t block_page_table_stride;
+  int32_t block_page_size;          /* 64 or 128 */
+  int32_t *block_phys;              /* NULL or [R][block_k] */
+  int32_t *block_valid_lens;        /* NULL or [R] */
 } dsa_topk_problem;
 
 int32_t dsa_coarse_hist_topk_batch(const dsa_topk_problem *problems, int32_t count,

@@ -137,8 +137,12 @@ def test_topk_problem_layout_and_batch_launch_count():
     runs in one launch when every row stride is at most 131072."""
     import ctypes
     import dsa_sparse_attention_paged_gb300 as D
-    assert ctypes.sizeof(D.TopkProblem) == 88
+    assert ctypes.sizeof(D.TopkProblem) == 128
     assert D.TopkProblem.next_n.offset == 64 and D.TopkProblem.block_k.offset == 84
+    assert D.TopkProblem.block_page_table.offset == 88
+    assert D.TopkProblem.block_page_table_stride.offset == 96
+    assert D.TopkProblem.block_page_size.offset == 104
+    assert D.TopkProblem.block_phys.offset == 112 and D.TopkProblem.block_valid_lens.offset == 120
     n = D.coarse_hist_topk_batch_launches
     assert n([(131072, True, 32), (16384, False, 32)]) == 1
     assert n([(200000, True, 2), (16384, False, 2)]) == 2 + 1

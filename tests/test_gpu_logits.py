@@ -139,3 +139,29 @@ def test_fused_block_maxima_equal_block_amax8(B, nn, ctx, ps, skip):
     L = np.where(live, logits.cpu().numpy(), np.nan).astype(np.float32)
     ref = O.block_amax8(L, rl, skip_le=skip, amax_stride=stride // 8, fill=-3.0)
     np.testing.assert_array_equal(fused.cpu().numpy(), ref)
+
+
+def test_histogram_counts_past_16_bits_per_slot():
+    """One request of 80M keys (a 64-page pool referenced over and over): with
+    q = 0 every score is +0, all in bin 511, so every histogram slot of every
+    CTA counts far beyond 2^16 tokens of one bin; the periodic flush keeps the
+    16-bit slot counts exact and the global count is the key count."""
+    import dsa_sparse_attention_paged_gb300 as D
+    n, ps, pool = 80_000_000, 64, 64
+    npg = (n + ps - 1) // ps
+    pt = (torch.arange(npg, dtype=torch.int32, device="cuda") % pool).reshape(1, npg)
+    q = torch.zeros((1, 32, 128), dtype=torch.uint8, device="cuda")
+    g = torch.Generator().manual_seed(12)
+    kv = torch.randint(0, 256, (pool, ps, 128), generator=g, dtype=torch.uint8).cuda()
+    kv[(kv & 0x7F) == 0x7F] = 0  # no NaN codes
+    ks = torch.ones((pool, ps), dtype=torch.float32, device="cuda")
+    w = torch.ones((1, 32), dtype=torch.float32, device="cuda")
+    ctx = torch.tensor([n], dtype=torch.int32, device="cuda")
+    hist = torch.zeros((1, 1024), dtype=torch.int32, device="cuda")
+    ws = D.Workspace(1)
+    L = D.paged_mqa_logits(q, kv, ks, w, pt, ctx, 1, ws, logits_stride=n, histogram=hist)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert bool((L == 0).all())
+    h = hist.cpu().numpy()[0]
+    assert h[511] == n and h.sum() == n

@@ -189,3 +189,55 @@ def test_fused_block_select_edge_cases(kind, n):
     assert sets_equal(bout.cpu().numpy(), _block_ref(x, rl, 512))
     f = bflags.cpu().numpy()
     assert set(f.tolist()) <= ({0, 2} if kind == "tied_maxima" else {0}), f
+
+
+@pytest.mark.parametrize("B,nn,ctx,ps", [
+    (3, 1, [40000, 3000, 131072], 64),   # a short row takes the identity table
+    (2, 2, [70001, 9000], 128),
+    (4, 1, [16000, 20000, 4097, 100000], 64),
+])
+def test_select_writes_sorted_block_table(B, nn, ctx, ps):
+    """The block output written as the sorted block table in the select
+    launch equals the separate sort_candidate_blocks of the same ids: table,
+    physical blocks and live lengths, bitwise; NaN-only blocks in a short row
+    still take their identity slot."""
+    import dsa_sparse_attention_paged_gb300 as D
+    case = make(B, nn, ctx, ps, "normal", seed=800 + B)
+    d = to_dev(case)
+    R = B * nn
+    kb = 512
+    stride = (max(ctx) + 7) // 8 * 8
+    ws = D.Workspace(R)
+    logits = torch.full((R, stride), float("nan"), dtype=torch.float32, device="cuda")
+    hist = torch.zeros((R, 1024), dtype=torch.int32, device="cuda")
+    D.paged_mqa_logits(d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"],
+                       d["context_lens"], nn, ws, logits=logits, histogram=hist)
+    rl = O.row_lens(case["context_lens"], nn)
+    short = int(np.argmin(rl))
+    logits[short, 8:40] = float("nan")  # NaN-only blocks 1..4 of the shortest row
+    hist2 = torch.from_numpy(O.histogram(logits.cpu().numpy(), rl)).cuda()
+    outs = []
+    for fused in (False, True):
+        table = torch.full((R, kb), -5, dtype=torch.int32, device="cuda")
+        phys = torch.full((R, kb), -5, dtype=torch.int32, device="cuda")
+        vlen = torch.full((R,), -5, dtype=torch.int32, device="cuda")
+        extra = dict(block_page_table=d["page_table"], block_page_size=ps, block_phys=phys,
+                     block_valid_lens=vlen) if fused else {}
+        D.coarse_hist_topk_batch([dict(logits=logits, context_lens=d["context_lens"], next_n=nn,
+                                       k=2048, histogram=hist2.clone(), block_k=kb,
+                                       block_out=table, **extra)], ws)
+        if not fused:
+            D.sort_candidate_blocks(table, d["context_lens"], nn, d["page_table"], ps, ws,
+                                    phys_blocks=phys, valid_lens=vlen)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
+        outs.append([t.cpu().numpy() for t in (table, phys, vlen)])
+    for a, b in zip(*outs):
+        np.testing.assert_array_equal(a, b)
+    A = O.block_amax8(logits.cpu().numpy(), rl, skip_le=kb, amax_stride=(stride + 7) // 8,
+                      fill=0.0)
+    t_ref, p_ref, v_ref = O.block_table(A, rl, np.arange(R, dtype=np.int32) // nn, kb,
+                                        case["page_table"], ps)
+    np.testing.assert_array_equal(outs[1][0], t_ref)
+    np.testing.assert_array_equal(outs[1][1], p_ref)
+    np.testing.assert_array_equal(outs[1][2], v_ref)
