@@ -47,6 +47,9 @@ def parse():
     p.add_argument("--cpu-budget", type=float, default=12.0)
     p.add_argument("--no-per-workload", action="store_true",
                    help="skip the per-workload table (c0, c1, c3, c3u, c4)")
+    p.add_argument("--no-mx", action="store_true", help="skip the MXFP4-key logits timing")
+    p.add_argument("--mx-only", action="store_true",
+                   help="only the MXFP4-key logits launch (warm-up + steps), one JSON object")
     return p.parse_args()
 
 
@@ -377,6 +380,10 @@ def main():
     nn, ps = w.next_n, w.page_size
     d = {k: (torch.from_numpy(v).to(dev) if isinstance(v, np.ndarray) else v)
          for k, v in case.items()}
+    if args.mx_only:
+        print(json.dumps(measure_mx_logits(case, w, d, dev, steps=max(1, args.steps),
+                                           warmup=args.warmup)), flush=True)
+        return
     plan = DecodePlan(w.B, nn, max(w.context_lens), ps, k=2048, kb=512, two_level=True,
                       device=dev)
     inputs = (d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"], d["context_lens"])
@@ -495,7 +502,7 @@ def main():
     cb = None
     if not args.no_cpu_baseline:
         cb = cpu_baseline(case, w, args.cpu_budget)
-    mx = measure_mx_logits(case, w, d, dev)
+    mx = None if args.no_mx else measure_mx_logits(case, w, d, dev)
     per_workload = None
     if not args.no_per_workload:
         per_workload = {nm: measure_workload(nm, dev) for nm in PER_WORKLOADS
