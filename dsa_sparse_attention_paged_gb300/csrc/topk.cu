@@ -1778,53 +1778,70 @@ __global__ void __launch_bounds__(kRowThreads)
 }
 
 // ---------------------------------------------------------------- FP16 select
+// [VL52696] "Why": top-k over packed 16-bit scores.  Each thread owns a
+// contiguous run of words (two scores each) in registers: one pass builds the
+// 10-bit coarse histogram of the order keys, a block scan finds the threshold
+// bin, a second pass over the run refines the remaining 6 bits inside it (a
+// warp finds the digit), and one block scan of packed counts gives every
+// thread its output slots -- the keys above the threshold anywhere, the keys
+// equal to it in position order (ties to the lower position).
 constexpr int kF16MaxRow = 16384;
 
-template <bool BF16>
-__global__ void __launch_bounds__(kSelThreads)
+// WPT: words a thread holds (rows of up to 2 * WPT * kSelThreads scores)
+template <bool BF16, int WPT>
+__global__ void __launch_bounds__(kSelThreads, 1)
     topk_fp16_kernel(const uint16_t *scores, int64_t stride, const int32_t *valid_lens, int k,
                      const int32_t *table, int kb, int32_t *out, uint32_t *status) {
   pdl_wait();  // predecessor grids complete before any global access
-  __shared__ uint32_t keys2[kF16MaxRow / 2];  // two 16-bit keys per word
   __shared__ int h[DSA_NUM_BINS];
   __shared__ int sm_scan[kSelWarps + 1];
   __shared__ int sm_misc[8];
   const int r = blockIdx.x;
+  const int lane = threadIdx.x & 31;
   int64_t n = valid_lens[r];
   if (n < 0) n = 0;
-  if (n > kF16MaxRow || n > stride) {
+  constexpr int kMaxRow = 2 * WPT * kSelThreads;
+  if (n > kMaxRow || n > stride) {
     if (threadIdx.x == 0) set_status(status, DSA_DEV_BOUNDS);
-    n = min((int64_t)kF16MaxRow, stride);
+    n = min((int64_t)kMaxRow, stride);
   }
   const uint32_t *row = reinterpret_cast<const uint32_t *>(scores + (int64_t)r * stride);
   const int nw = (int)((n + 1) / 2);
+  // this thread's words [w0, w0 + wpt), wpt a multiple of 4 (16-byte loads)
+  const int wpt = ((nw + kSelThreads - 1) / kSelThreads + 3) & ~3;
+  const int w0 = threadIdx.x * wpt;
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
   for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kSelThreads) h[i] = 0;
-  __syncthreads();
-  // keys, with positions >= n masked to the invalid key 0 (all loads issued
-  // first); coarse histogram
-  // words are handled in rounds of 4 per thread (all 4 loads in flight);
-  // the round count depends only on the row, so every lane runs it
-  constexpr int WR = 4;
-  const int rounds = (nw + WR * kSelThreads - 1) / (WR * kSelThreads);
-  for (int rd = 0; rd < rounds; ++rd) {
-    uint32_t wv[WR];
+  uint32_t kv[WPT];  // order keys, two per word; 0 = no score
 #pragma unroll
-    for (int e = 0; e < WR; ++e) {
-      const int w = (rd * WR + e) * kSelThreads + threadIdx.x;
-      wv[e] = (w < nw) ? row[w] : 0u;
+  for (int q = 0; q < WPT / 4; ++q) {
+    const int w = w0 + 4 * q;
+    uint32_t x[4] = {0u, 0u, 0u, 0u};
+    if (4 * q < wpt) {
+      if (vec && w + 3 < nw) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(row + w));
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (w + e < nw) x[e] = __ldg(row + w + e);
+      }
     }
 #pragma unroll
-    for (int e = 0; e < WR; ++e) {
-      const int w = (rd * WR + e) * kSelThreads + threadIdx.x;
-      uint32_t kk = (w < nw) ? (BF16 ? bf16x2_order_keys(wv[e]) : f16x2_order_keys(wv[e])) : 0u;
-      if (2 * w + 1 >= n) kk &= 0x0000FFFFu;
-      keys2[w] = kk;
-      const uint32_t lo = kk & 0xFFFFu, hi = kk >> 16;
-      if (lo) atomicAdd(&h[lo >> 6], 1);
-      if (hi) atomicAdd(&h[hi >> 6], 1);
+    for (int e = 0; e < 4; ++e) {
+      uint32_t kk = (4 * q < wpt && w + e < nw)
+                        ? (BF16 ? bf16x2_order_keys(x[e]) : f16x2_order_keys(x[e])) : 0u;
+      if (2 * (w + e) + 1 >= n) kk &= 0x0000FFFFu;  // the odd position past the row
+      kv[4 * q + e] = kk;
     }
   }
-  const int nw_r = rounds * WR * kSelThreads;  // words written above (zero past the row)
+  __syncthreads();  // h zeroed
+#pragma unroll
+  for (int e = 0; e < WPT; ++e) {
+    const uint32_t lo = kv[e] & 0xFFFFu, hi = kv[e] >> 16;
+    if (lo) atomicAdd(&h[lo >> 6], 1);
+    if (hi) atomicAdd(&h[hi >> 6], 1);
+  }
   __syncthreads();
   // threshold among 1024 coarse bins, searching from the top (bin 1023)
   {
@@ -1849,81 +1866,79 @@ __global__ void __launch_bounds__(kSelThreads)
   }
   const int T10 = sm_misc[0];
   int above = sm_misc[1];
-  uint32_t thr = 0;   // exact 16-bit threshold key
-  int need = 0;       // entries equal to thr still to take
-  bool take_all = (T10 < 0);
+  const bool take_all = (T10 < 0);
+  uint32_t thr = 0;  // exact 16-bit threshold key
   if (!take_all) {
-    // refine the remaining 6 bits inside bin T10
+    // the remaining 6 bits inside bin T10
     if (threadIdx.x < 64) h[threadIdx.x] = 0;
     __syncthreads();
-    for (int w0 = 0; w0 < nw_r; w0 += kSelThreads) {
-      const uint32_t kk = keys2[w0 + threadIdx.x];  // 0 past the row
-      const uint32_t lo = kk & 0xFFFFu, hi = kk >> 16;
+#pragma unroll
+    for (int e = 0; e < WPT; ++e) {
+      const uint32_t lo = kv[e] & 0xFFFFu, hi = kv[e] >> 16;
       if (lo && (int)(lo >> 6) == T10) atomicAdd(&h[lo & 63], 1);
       if (hi && (int)(hi >> 6) == T10) atomicAdd(&h[hi & 63], 1);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int acc = above;
-      sm_misc[2] = 0;
-      sm_misc[3] = above;
-      for (int d = 63; d >= 0; --d) {
-        if (acc + h[d] >= k) {
-          sm_misc[2] = d;
-          sm_misc[3] = acc;
-          break;
-        }
-        acc += h[d];
+    if (threadIdx.x < 32) {
+      // lane l holds digits 63-2l and 62-2l (descending)
+      const int d0 = 63 - 2 * lane;
+      const int a0 = h[d0], a1 = h[d0 - 1];
+      int incl = a0 + a1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int ex = incl - a0 - a1;
+      const unsigned m = __ballot_sync(0xffffffffu, above + incl >= k);
+      const int l = m ? __ffs(m) - 1 : 31;
+      if (lane == l) {
+        const bool first = above + ex + a0 >= k;
+        sm_misc[2] = first ? d0 : d0 - 1;
+        sm_misc[3] = above + (first ? ex : ex + a0);
       }
     }
     __syncthreads();
     thr = ((uint32_t)T10 << 6) | (uint32_t)sm_misc[2];
     above = sm_misc[3];
-    need = k - above;
   }
-  if (threadIdx.x == 0) sm_misc[4] = 0;
-  __syncthreads();
+  const int need = take_all ? 0 : k - above;
+  // one scan of (keys above thr, keys equal to thr) per thread, in position order
+  int nsel = 0, neq = 0;
+#pragma unroll
+  for (int e = 0; e < WPT; ++e) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const uint32_t key = hh ? (kv[e] >> 16) : (kv[e] & 0xFFFFu);
+      if (!key) continue;
+      if (take_all || key > thr) ++nsel;
+      else if (key == thr) ++neq;
+    }
+  }
+  int tot;
+  const int ex = block_excl_scan(nsel | (neq << 16), sm_scan, &tot);
+  int ps = ex & 0xFFFF, pq = ex >> 16;
   int32_t *outr = out + (int64_t)r * k;
   auto emit_col = [&](int p) -> int32_t {
     return table ? (int32_t)(table[(int64_t)r * kb + p / 8] * 8 + (p & 7)) : (int32_t)p;
   };
-  // emission: keys above thr anywhere; keys equal to thr by position order
-  int eq_base = 0;
-  for (int base = 0; base < nw; base += kSelThreads * 2) {
-    int eqc = 0;
-    bool eqf[4];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int w = base + threadIdx.x * 2 + e;
-      const uint32_t kk = (w < nw) ? keys2[w] : 0u;
+  for (int e = 0; e < WPT; ++e) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t key = hh ? (kk >> 16) : (kk & 0xFFFFu);
-        eqf[2 * e + hh] = false;
-        if (!key) continue;
-        const bool sel = take_all ? true : key > thr;
-        if (sel) {
-          const int p = atomicAdd(&sm_misc[4], 1);
-          if (p < k) outr[p] = emit_col(2 * w + hh);
-        } else if (!take_all && key == thr) {
-          eqf[2 * e + hh] = true;
-          ++eqc;
-        }
+    for (int hh = 0; hh < 2; ++hh) {
+      const uint32_t key = hh ? (kv[e] >> 16) : (kv[e] & 0xFFFFu);
+      if (!key) continue;
+      const int pos = 2 * (w0 + e) + hh;
+      if (take_all || key > thr) {
+        if (ps < k) outr[ps] = emit_col(pos);
+        ++ps;
+      } else if (key == thr) {
+        if (pq < need) outr[above + pq] = emit_col(pos);
+        ++pq;
       }
     }
-    int tot;
-    const int ex = block_excl_scan(eqc, sm_scan, &tot);
-    int rank = eq_base + ex;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (!eqf[q]) continue;
-      if (rank < need) outr[above + rank] = emit_col(2 * (base + threadIdx.x * 2 + q / 2) + (q & 1));
-      ++rank;
-    }
-    eq_base += tot;
   }
-  __syncthreads();
-  const int written = take_all ? sm_misc[4] : k;
+  const int written = take_all ? (tot & 0xFFFF) : k;
   for (int i = written + threadIdx.x; i < k; i += kSelThreads) outr[i] = -1;
 }
 
@@ -2113,9 +2128,12 @@ dsa_status_t run_topk(const TopkCall &c, cudaStream_t st) {
 }
 
 dsa_status_t run_topk_fp16(const Fp16TopkCall &c, cudaStream_t st) {
-  return launch_pdl(c.bf16 ? topk_fp16_kernel<true> : topk_fp16_kernel<false>, dim3(c.R),
-                    dim3(kSelThreads), 0, st, c.scores, c.stride,
-                    c.valid_lens, c.k, c.block_table, c.kb, c.out_idx, c.status);
+  // words a thread holds: the fewest that cover a row of `stride` scores
+  auto fn = c.bf16 ? topk_fp16_kernel<true, 16> : topk_fp16_kernel<false, 16>;
+  if (c.stride <= 2 * 4 * kSelThreads) fn = c.bf16 ? topk_fp16_kernel<true, 4> : topk_fp16_kernel<false, 4>;
+  else if (c.stride <= 2 * 8 * kSelThreads) fn = c.bf16 ? topk_fp16_kernel<true, 8> : topk_fp16_kernel<false, 8>;
+  return launch_pdl(fn, dim3(c.R), dim3(kSelThreads), 0, st, c.scores, c.stride, c.valid_lens,
+                    c.k, c.block_table, c.kb, c.out_idx, c.status);
 }
 
 }  // namespace dsa
