@@ -176,3 +176,105 @@ class DecodePlan:
         self.graph.replay()
         return self.graph_out
 
+
+class HostStepPipeline:
+    """Decode steps fed from and returned to host memory, with the copies of
+    one step overlapped with the kernels of its neighbours.
+
+    Two ``DecodePlan``s and two device copies of the per-step inputs (q,
+    weights, context lengths, page table) alternate between steps.  ``submit``
+    queues three things on three streams:
+
+      input stream    host-to-device copy of the step's inputs into the idle
+                      set, once the step that last read that set has finished
+      compute stream  the step (``DecodePlan.step``), once its inputs are in
+                      and the step that last wrote its plan's outputs has had
+                      them copied out
+      output stream   device-to-host copy of both index sets, once the step
+                      has finished
+
+    so step i+1's inputs travel while step i computes, and step i's results
+    travel while step i+1 computes.  The K cache (``kv``, ``kscale``) is
+    resident device state that both plans read.  Host tensors must be pinned
+    and stay untouched until the step's ``wait``; the kernels and the results
+    are those of ``DecodePlan.step``."""
+
+    def __init__(self, B, next_n, max_context, page_size, kv, kscale, k=2048, kb=512,
+                 device="cuda"):
+        dev = torch.device(device)
+        self.plans = [DecodePlan(B, next_n, max_context, page_size, k=k, kb=kb, two_level=True,
+                                 device=dev) for _ in range(2)]
+        self.kv, self.kscale = kv, kscale
+        self.inputs = [None, None]
+        self.s_in = torch.cuda.Stream(device=dev)
+        self.s_compute = torch.cuda.Stream(device=dev)
+        self.s_out = torch.cuda.Stream(device=dev)
+        self.step_done = [None, None]   # per set: the last step that used it finished
+        self.out_done = [None, None]    # per set: that step's outputs reached the host
+        self.pending = {}               # step index -> out_done event
+        self.n = 0
+        # the plans' buffers were zeroed on the caller's stream
+        ready = torch.cuda.Event()
+        ready.record(torch.cuda.current_stream(dev))
+        self.start_after(ready)
+
+    @property
+    def launches_per_step(self) -> int:
+        return self.plans[0].launches_per_step
+
+    def start_after(self, event):
+        """Make every later submit wait for ``event`` (e.g. a timing mark)."""
+        for st in (self.s_in, self.s_compute, self.s_out):
+            st.wait_event(event)
+
+    def record_all(self):
+        """An event on each stream, after everything submitted so far."""
+        evs = []
+        for st in (self.s_in, self.s_compute, self.s_out):
+            e = torch.cuda.Event()
+            e.record(st)
+            evs.append(e)
+        return evs
+
+    def submit(self, q, weights, context_lens, page_table, out_dense, out_sparse):
+        """Queue one step on pinned host tensors; returns the step index."""
+        i, s = self.n, self.n % 2
+        plan = self.plans[s]
+        dev = plan.logits.device
+        host_in = (q, weights, context_lens, page_table)
+        if self.inputs[s] is None:
+            self.inputs[s] = [torch.empty(t.shape, dtype=t.dtype, device=dev) for t in host_in]
+        dq, dw, dc, dp = self.inputs[s]
+        with torch.cuda.stream(self.s_in):
+            if self.step_done[s] is not None:
+                self.s_in.wait_event(self.step_done[s])
+            for d, h in zip(self.inputs[s], host_in):
+                d.copy_(h, non_blocking=True)
+            in_ready = torch.cuda.Event()
+            in_ready.record(self.s_in)
+        with torch.cuda.stream(self.s_compute):
+            self.s_compute.wait_event(in_ready)
+            if self.out_done[s] is not None:
+                self.s_compute.wait_event(self.out_done[s])
+            dense, sparse = plan.step(dq, self.kv, self.kscale, dw, dp, dc)
+            done = torch.cuda.Event()
+            done.record(self.s_compute)
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(done)
+            out_dense.copy_(dense, non_blocking=True)
+            out_sparse.copy_(sparse, non_blocking=True)
+            oe = torch.cuda.Event()
+            oe.record(self.s_out)
+        self.step_done[s], self.out_done[s] = done, oe
+        self.pending[i] = oe
+        self.n += 1
+        return i
+
+    def wait(self, i):
+        """Block until step i's host outputs are written."""
+        self.pending.pop(i).synchronize()
+
+    def synchronize(self):
+        for st in (self.s_in, self.s_compute, self.s_out):
+            st.synchronize()
+        self.pending.clear()

@@ -43,3 +43,39 @@ def test_graph_replay_follows_inputs_rewritten_in_place(pair_rows):
     d["q"].copy_(torch.from_numpy(b["q"]))
     d["weights"].copy_(torch.from_numpy(b["weights"]))
     replay_and_compare()
+
+
+def test_host_pipeline_matches_eager_steps():
+    """Overlapped host-to-host steps (two plans, three streams): every step's
+    host outputs equal an eager step on the same inputs, with steps on
+    different lengths, queries and weights in flight together."""
+    from dsa_sparse_attention_paged_gb300.pipeline import DecodePlan, HostStepPipeline
+    cases = [S.generate(S.Workload("pipe %d" % i, 3, 2, [20000] * 3, 64, dist, 300 + i))
+             for i, dist in enumerate(("mixed", "normal", "mixed"))]
+    lens = ([20000, 9000, 3000], [7000, 20000, 100], [15000, 15000, 15000])
+    d = to_dev(cases[0])  # the K cache is the first case's; pages cover 20000 keys
+    pipe = HostStepPipeline(3, 2, 20000, 64, d["kv"], d["kscale"], k=2048, kb=256)
+    host_in, outs = [], []
+    for c, L in zip(cases, lens):
+        host_in.append({"q": torch.from_numpy(c["q"]).pin_memory(),
+                        "weights": torch.from_numpy(c["weights"]).pin_memory(),
+                        "context_lens": torch.tensor(L, dtype=torch.int32).pin_memory(),
+                        "page_table": torch.from_numpy(cases[0]["page_table"]).pin_memory()})
+    order = [0, 1, 2, 1, 0, 2]
+    for j in order:
+        h = host_in[j]
+        o = (torch.full((6, 2048), -5, dtype=torch.int32).pin_memory(),
+             torch.full((6, 2048), -5, dtype=torch.int32).pin_memory())
+        outs.append(o)
+        pipe.submit(h["q"], h["weights"], h["context_lens"], h["page_table"], *o)
+    pipe.synchronize()
+    for p in pipe.plans:
+        assert p.ws.status() == 0
+    plan = DecodePlan(3, 2, 20000, 64, k=2048, kb=256)
+    for j, o in zip(order, outs):
+        h = host_in[j]
+        dense, sparse = plan.step(h["q"].cuda(), d["kv"], d["kscale"], h["weights"].cuda(),
+                                  h["page_table"].cuda(), h["context_lens"].cuda())
+        torch.cuda.synchronize()
+        assert sets_equal(o[0].numpy(), dense.cpu().numpy())
+        assert sets_equal(o[1].numpy(), sparse.cpu().numpy())
