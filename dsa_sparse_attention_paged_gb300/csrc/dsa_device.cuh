@@ -109,6 +109,9 @@ __device__ __forceinline__ int4 dsmem_ld4(uint32_t addr) {
 __device__ __forceinline__ void dsmem_st64(uint32_t addr, unsigned long long v) {
   asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
 }
+__device__ __forceinline__ void dsmem_st32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 // All threads of all CTAs of the cluster meet (shared-memory writes before it
 // are visible to every CTA after it).
 // The two halves of cluster_sync(), for work placed between them: a thread's

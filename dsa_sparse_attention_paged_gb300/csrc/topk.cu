@@ -1082,6 +1082,67 @@ __device__ __noinline__ void local_hist_select(const unsigned long long *it, int
   }
 }
 
+// The m-th largest (1 <= m <= n) of the n unique items it[0..n) whose keys
+// lie in [lo, hi] (items outside the range are ignored; at least m lie in
+// it).  Level by level a 1024-bin histogram over an even split of [lo, hi]
+// gives the bin holding the m-th item, and the range narrows to that bin; a
+// bin of at most kClRank items, one key wide, or left after the third level
+// is ranked pairwise.  Run by the whole block; every thread gets the item.
+// Scratch: h[1024], two item buffers of n (not aliasing `it`).
+__device__ __noinline__ unsigned long long local_hist_kth(const unsigned long long *it, int n,
+                                                          int m, uint32_t lo, uint32_t hi, int *h,
+                                                          unsigned long long *bufA,
+                                                          unsigned long long *bufB, int *sm_scan,
+                                                          int *sm_misc,
+                                                          unsigned long long *sm_res) {
+  const unsigned long long *src = it;
+  int ns = n, need = m;
+  if (threadIdx.x == 0) *sm_res = 0;
+  for (int level = 0;; ++level) {
+    int shift = 0;
+    while (((hi - lo) >> shift) >= (uint32_t)kClFine) ++shift;
+    for (int i = threadIdx.x; i < kClFine; i += kClThreads) h[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < ns; i += kClThreads) {
+      const uint32_t k32 = (uint32_t)(src[i] >> 32);
+      if (k32 >= lo && k32 <= hi) atomicAdd(&h[cl_fine_idx(k32, lo, shift)], 1);
+    }
+    __syncthreads();
+    threshold_from_hist<kClFine>(h, need, sm_scan, sm_misc);
+    const int T = sm_misc[0];
+    const int above = sm_misc[1];
+    if (T >= kClFine) return 0ull;  // fewer than m in play: not a valid input
+    uint32_t C, E;
+    fine_bin_keys(lo, hi, lo, shift, T, C, E);
+    need -= above;
+    if (threadIdx.x == 0) sm_misc[5] = 0;
+    __syncthreads();
+    unsigned long long *dst = (level & 1) ? bufB : bufA;
+    for (int i = threadIdx.x; i < ns; i += kClThreads) {
+      const unsigned long long v = src[i];
+      const uint32_t k32 = (uint32_t)(v >> 32);
+      if (k32 >= C && k32 <= E) dst[atomicAdd(&sm_misc[5], 1)] = v;
+    }
+    __syncthreads();
+    const int inbin = sm_misc[5];
+    if (inbin <= kClRank || level == 2 || C == E) {
+      // unique items: the one with exactly need - 1 larger items in the bin
+      for (int i = threadIdx.x; i < inbin; i += kClThreads) {
+        const unsigned long long v = dst[i];
+        int rk = 0;
+        for (int j = 0; j < inbin; ++j) rk += dst[j] > v;
+        if (rk == need - 1) *sm_res = v;
+      }
+      __syncthreads();
+      return *sm_res;
+    }
+    src = dst;
+    ns = inbin;
+    lo = C;
+    hi = E;
+  }
+}
+
 // Last step of the score select, run by one CTA once every emit and
 // candidate of the row is in place: check the counts, then rank or refine
 // the candidates, or run the exact whole-row fallback.  Returns the fallback
@@ -1313,6 +1374,180 @@ __device__ __noinline__ int cl_block_finish(const float *row, int64_t n, bool ve
   return nbc > kBSel ? 2 : 0;
 }
 
+// Block-candidate histogram of a cluster row whose block output is the sorted
+// table: bins of 2^kBShift keys (1/512 of a binade) above the score select's
+// E, descending, the last 2 binades' worth clamped into bin 0 with +inf.
+constexpr int kBShift = 14;
+// Warp groups of a cluster row: 8 CTAs x 16 warps, 128 blocks (4 a thread) each.
+constexpr int kWGroups = kCl * kSelWarps;
+
+// CTA 1 of a cluster row whose block output is the sorted block table.  When
+// the row has more than bk blocks and bk to kBSel block candidates (every
+// block whose maximum key is above the score select's E: the top bk blocks
+// are among them), the table is the bk blocks whose item (key << 32 | ~block)
+// is at least V, the bk-th largest candidate item.  The candidates' histogram
+// bh (built by every CTA as it stored them) gives V's bin; the candidates
+// above that bin are counted, the bin's own are ranked (pairwise, or by
+// local_hist_kth when many), and V is the item of rank bk - above.  Every
+// CTA's blocks are one contiguous range of the row and each of its warps
+// covers 128 consecutive blocks, so this CTA counts the chosen blocks of each
+// warp group, and stores V and the warp groups' exclusive offsets into every
+// CTA's shared memory (tab_addr: V; woff_addr: kSelWarps offsets), with the
+// row's live length.  V = 0 everywhere: this CTA builds the table alone.
+__device__ __noinline__ void cl_block_publish(int64_t n, int bk, bool btake, int nbc,
+                                              const unsigned long long *bsel, const int *bh,
+                                              uint32_t base, int nloc, unsigned long long *buf,
+                                              int *hist, int *sm_h, int *sm_scan, int *sm_misc,
+                                              unsigned long long *sm_res, uint32_t tab_addr,
+                                              uint32_t woff_addr, int32_t *valid,
+                                              int32_t *bflag) {
+  unsigned long long vstar = 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  auto wgroup = [&](int64_t b) { return (int)(b / nloc) * kSelWarps + (int)((b % nloc) >> 7); };
+  auto live_of = [&](int64_t b) { const int64_t t = n - 8 * b; return t < 8 ? (int)t : 8; };
+  if (!btake && nbc >= bk && nbc <= kBSel) {
+    for (int i = threadIdx.x; i <= kWGroups; i += kClThreads) sm_h[i] = 0;  // + live length
+    if (threadIdx.x == 0) {
+      sm_misc[5] = 0;
+      *sm_res = 0;
+    }
+    threshold_from_hist<kClFine>(bh, bk, sm_scan, sm_misc);
+    const int Tb = sm_misc[0];
+    const int need = bk - sm_misc[1];  // 1 .. the bin's count
+    if (Tb < kClFine) {
+      int live = 0;
+      // the items of a warp mostly come from one warp group: one shared
+      // atomic per distinct group
+      for (int i0 = 0; i0 < nbc; i0 += kClThreads) {
+        const int i = i0 + (int)threadIdx.x;
+        const unsigned long long v = i < nbc ? bsel[i] : 0ull;
+        const int bin = i < nbc ? cl_fine_idx((uint32_t)(v >> 32), base, kBShift) : kClFine;
+        const int64_t b = (int64_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
+        const bool up = bin < Tb;
+        const unsigned act = __ballot_sync(0xffffffffu, up);
+        if (up) {
+          const int wg = wgroup(b);
+          const unsigned peers = __match_any_sync(act, wg);
+          if (lane == __ffs(peers) - 1) atomicAdd(&sm_h[wg], __popc(peers));
+          live += live_of(b);
+        } else if (bin == Tb) {
+          buf[atomicAdd(&sm_misc[5], 1)] = v;
+        }
+      }
+      __syncthreads();
+      const int ni = sm_misc[5];
+      if (ni <= kClRank) {
+        if ((int)threadIdx.x < ni) {
+          const unsigned long long v = buf[threadIdx.x];
+          int rk = 0;
+          for (int j = 0; j < ni; ++j) rk += buf[j] > v;
+          if (rk < need) {
+            const int64_t b = (int64_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
+            atomicAdd(&sm_h[wgroup(b)], 1);
+            live += live_of(b);
+          }
+          if (rk == need - 1) *sm_res = v;
+        }
+        __syncthreads();
+      } else {
+        const uint32_t g = (uint32_t)((kClFine - 1) - Tb);
+        const uint32_t lo = base + (g << kBShift);
+        const uint32_t hi = Tb == 0 ? 0xFFFFFFFFu : lo + (1u << kBShift) - 1u;
+        const unsigned long long vk = local_hist_kth(buf, ni, need, lo, hi, hist, buf + kBSel,
+                                                     buf + 2 * kBSel, sm_scan, sm_misc, sm_res);
+        for (int i = threadIdx.x; i < ni; i += kClThreads) {
+          const unsigned long long v = buf[i];
+          if (vk && v >= vk) {
+            const int64_t b = (int64_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
+            atomicAdd(&sm_h[wgroup(b)], 1);
+            live += live_of(b);
+          }
+        }
+      }
+      live = (int)__reduce_add_sync(0xffffffffu, (unsigned)live);
+      if (lane == 0 && live) atomicAdd(&sm_h[kWGroups], live);
+      __syncthreads();
+      vstar = *sm_res;
+      // exclusive offsets of the warp groups in block order (warp 0, four a lane)
+      if (vstar && warp == 0) {
+        int c[kWGroups / 32], sum = 0;
+#pragma unroll
+        for (int j = 0; j < kWGroups / 32; ++j) {
+          c[j] = sm_h[lane * (kWGroups / 32) + j];
+          sum += c[j];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int x = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += x;
+        }
+        int off = incl - sum;
+#pragma unroll
+        for (int j = 0; j < kWGroups / 32; ++j) {
+          sm_h[lane * (kWGroups / 32) + j] = off;
+          off += c[j];
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (vstar) {
+    if (threadIdx.x < kWGroups)
+      dsmem_st32(dsmem_map(woff_addr + 4u * (threadIdx.x % kSelWarps), threadIdx.x / kSelWarps),
+                 sm_h[threadIdx.x]);
+    if (threadIdx.x == 0) {
+      if (valid) *valid = sm_h[kWGroups];
+      if (bflag) *bflag = 0;
+    }
+  }
+  if (threadIdx.x < kCl) dsmem_st64(dsmem_map(tab_addr, threadIdx.x), vstar);
+}
+
+// This CTA's slice of the sorted block table: of its blocks b0 + 4t .. b0 +
+// 4t + 3 (thread t; keys in bkey) those whose item is at least V, ascending,
+// from the warp's table offset woff[warp], with their physical blocks (pool
+// slot / 8 through the request's page-table row; pg0 is the page of the
+// thread's first block when page_size is a multiple of 32, so all four of its
+// blocks lie in that page).  No block barrier: warp scans only.
+__device__ __forceinline__ void cl_table_slice(const uint32_t *bkey, int nloc, int64_t b0,
+                                               unsigned long long vstar, const int *woff,
+                                               int32_t *out, int32_t *phys, const int32_t *pt_row,
+                                               int ps, int32_t pg0) {
+  const int lane = threadIdx.x & 31;
+  uint4 k4 = make_uint4(0u, 0u, 0u, 0u);
+  if (4 * (int)threadIdx.x < nloc) k4 = reinterpret_cast<const uint4 *>(bkey)[threadIdx.x];
+  const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
+  const int64_t bb = b0 + 4 * (int64_t)threadIdx.x;
+  uint32_t sel = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const unsigned long long item = ((unsigned long long)kv[j] << 32) |
+                                    (unsigned long long)(0xFFFFFFFFu - (uint32_t)(bb + j));
+    sel |= (uint32_t)(kv[j] != 0u && item >= vstar) << j;
+  }
+  const int c = __popc(sel);
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  int pos = woff[threadIdx.x >> 5] + incl - c;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (!((sel >> j) & 1u)) continue;
+    const int64_t b = bb + j;
+    out[pos] = (int32_t)b;
+    if (phys) {
+      const int64_t tok = b * 8;
+      const int64_t pg = (ps % 32 == 0) ? (int64_t)pg0 : (int64_t)__ldg(&pt_row[tok / ps]);
+      phys[pos] = (int32_t)((pg * ps + tok % ps) / 8);
+    }
+    ++pos;
+  }
+}
+
 // Bounded wait for phase 0 of `bar` (a CTA's bulk copies).  A wait that runs
 // out records DSA_DEV_TIMEOUT and waits once more, bounded again: the copies
 // must land before the CTA reads or leaves its shared memory.
@@ -1333,6 +1568,63 @@ __device__ __forceinline__ unsigned long long dsmem_atomic_add64(uint32_t addr, 
   asm volatile("atom.shared::cluster.add.u64 %0, [%1], %2;" : "=l"(old) : "r"(addr), "l"(v)
                : "memory");
   return old;
+}
+
+// The sorted block table of a cluster row, written by the whole cluster when
+// its fast case holds: CTA 1 publishes the threshold item V and the warp
+// groups' offsets (cl_block_publish), and after a cluster barrier each CTA
+// writes its slice.  Returns false (V = 0) when CTA 1 must build the table
+// alone.  Every CTA of the cluster calls it; `base` is the score select's
+// E + 1, the bottom of the block-candidate histogram (CTA 1's sm.fmerge).
+__device__ __noinline__ bool cl_table_cluster(const ClProb &p, int r, int64_t n, uint32_t rank,
+                                              uint32_t base, ClSmem &sm, int *sm_h, int *sm_scan,
+                                              int *sm_misc, unsigned long long *sm_u64) {
+  __shared__ unsigned long long sm_tab;  // V
+  __shared__ int sm_woff[kSelWarps];     // this CTA's warps' first table positions
+  const int bk = p.bk;
+  const int nloc = (int)((((p.stride + kCl - 1) / kCl) + 2047) / 2048 * 256);  // blocks a CTA
+  const int64_t bs0 = (int64_t)rank * nloc;
+  const int32_t *pt_row = p.bpt + (int64_t)(r / p.next_n) * p.bpt_stride;
+  if (rank == 1)
+    cl_block_publish(n, bk, (n + 7) / 8 <= bk, sm.bctr, sm.bsel, sm.fmerge, base, nloc,
+                     reinterpret_cast<unsigned long long *>(sm.keys), sm.hist, sm_h, sm_scan,
+                     sm_misc, sm_u64, smem_u32(&sm_tab), smem_u32(&sm_woff[0]),
+                     p.bvalid ? p.bvalid + r : nullptr, p.bflags ? p.bflags + r : nullptr);
+  int32_t pg0 = 0;  // the page of this thread's first block, read ahead of the barrier
+  const int64_t bt = bs0 + 4 * (int64_t)threadIdx.x;
+  if (p.bphys && p.bps % 32 == 0 && 4 * (int)threadIdx.x < nloc && bt * 8 < n)
+    pg0 = __ldg(&pt_row[bt * 8 / p.bps]);
+  cluster_sync();  // every CTA's V and offsets are in place
+  const unsigned long long vstar = sm_tab;
+  if (!vstar) return false;
+  cl_table_slice(sm.bkey, nloc, bs0, vstar, sm_woff, p.bout + (int64_t)r * bk,
+                 p.bphys ? p.bphys + (int64_t)r * bk : nullptr, pt_row, p.bps, pg0);
+  return true;
+}
+
+// The block select and table of one row by this CTA alone: the top bk
+// blocks by cl_block_finish, then (with a table to write) the counting sort
+// of cl_sort_table over the chosen ids, which go to the block-key buffer
+// (free after the last cluster barrier).
+__device__ __noinline__ void cl_block_general(const ClProb &p, int r, int64_t n, ClSmem &sm,
+                                              int *sm_h, int *sm_scan, int *sm_misc) {
+  const int bk = p.bk;
+  const int64_t nbk = (n + 7) / 8;
+  int32_t *boutr = p.bout + (int64_t)r * bk;
+  int32_t *ids = p.bpt ? reinterpret_cast<int32_t *>(sm.bkey) : boutr;
+  const int flag = cl_block_finish(p.logits + (int64_t)r * p.stride, n, p.vec != 0, bk, ids,
+                                   nbk <= bk, sm.bctr, sm.bsel,
+                                   reinterpret_cast<uint32_t *>(sm.keys), sm.hist, sm_h, sm_scan,
+                                   sm_misc);
+  if (p.bflags && threadIdx.x == 0) p.bflags[r] = flag;
+  if (p.bpt) {
+    __syncthreads();  // the block ids are in place
+    __shared__ long long sm_live[kClThreads / 32];
+    cl_sort_table(ids, boutr, bk, n, nbk, p.bpt + (int64_t)(r / p.next_n) * p.bpt_stride, p.bps,
+                  p.bphys ? p.bphys + (int64_t)r * bk : nullptr,
+                  p.bvalid ? p.bvalid + r : nullptr, reinterpret_cast<uint32_t *>(sm.hist),
+                  sm_scan, sm_live);
+  }
 }
 
 __global__ void __launch_bounds__(kClThreads, 2)
@@ -1391,7 +1683,13 @@ __global__ void __launch_bounds__(kClThreads, 2)
   }
   if (!hrow)
     for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) sm.hist[i] = 0;
-  for (int i = threadIdx.x; i < kClFine; i += kClThreads) sm.fmerge[i] = 0;
+  // this CTA's fine histogram of bin T lives in the candidate buffer until the
+  // fine merge (CTA 0's candidates arrive only after that merge's barrier)
+  int *const fh = reinterpret_cast<int *>(sm.cand);
+  for (int i = threadIdx.x; i < kClFine; i += kClThreads) {
+    sm.fmerge[i] = 0;
+    fh[i] = 0;
+  }
   __syncthreads();
   // cluster barrier A: every CTA's counters and merge buffer are zeroed; it is
   // waited for just before the first remote access
@@ -1445,24 +1743,8 @@ __global__ void __launch_bounds__(kClThreads, 2)
   // keys into shared memory, and the block maxima (a block of 8 scores is
   // two neighbouring threads' slots; the newest block counts as +inf)
   const float nanv = __int_as_float(0x7fffffff);
-#pragma unroll
-  for (int q = 0; q < kClVec; ++q) {
+  auto convert = [&](int q, float4 x) {
     const int i = q * kClThreads + threadIdx.x;
-    float4 x = v[q];
-    if (bulk) {
-      if (q % kClGroupVec == 0) cl_wait_copies(bar_g(q / kClGroupVec), a.status);
-      const int64_t t = 4 * (int64_t)i;  // chunk offset of the slot's first score
-      if (q < vq && t < nrow) {
-        x = reinterpret_cast<const float4 *>(sm.keys)[i];
-        if (t + 4 > nrow) {  // the row ends inside this slot
-          if (t + 1 >= nrow) x.y = nanv;
-          if (t + 2 >= nrow) x.z = nanv;
-          x.w = nanv;
-        }
-      } else {
-        x = make_float4(nanv, nanv, nanv, nanv);
-      }
-    }
     const uint4 kk = make_uint4(key_or_zero(x.x), key_or_zero(x.y), key_or_zero(x.z),
                                 key_or_zero(x.w));
     sm.keys[i] = kk;
@@ -1475,26 +1757,45 @@ __global__ void __launch_bounds__(kClThreads, 2)
       else if (b == nbk - 1) mk = kKeyPosInf;   // the newest block is always chosen
       if ((threadIdx.x & 1) == 0) sm.bkey[lb] = mk;
     }
+  };
+  if (bulk) {
+#pragma unroll
+    for (int q = 0; q < kClVec; ++q) {
+      if (q % kClGroupVec == 0) cl_wait_copies(bar_g(q / kClGroupVec), a.status);
+      const int i = q * kClThreads + threadIdx.x;
+      const int64_t t = 4 * (int64_t)i;  // chunk offset of the slot's first score
+      float4 x = make_float4(nanv, nanv, nanv, nanv);
+      if (q < vq && t < nrow) {
+        x = reinterpret_cast<const float4 *>(sm.keys)[i];
+        if (t + 4 > nrow) {  // the row ends inside this slot
+          if (t + 1 >= nrow) x.y = nanv;
+          if (t + 2 >= nrow) x.z = nanv;
+          x.w = nanv;
+        }
+      }
+      convert(q, x);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < kClVec; ++q) convert(q, v[q]);
   }
   __syncthreads();
   uint32_t loT = 0, hiT = 0;  // loT > hiT: bin T empty (T past the last bin)
   bool fine = false;
   uint32_t flo = 0;
   int fshift = 0;
-  // this CTA's fine histogram of bin T into sm.hist: an even split of the
-  // bin's key range, or for the four bins wider than kFineWindow keys a
+  // this CTA's fine histogram of bin T into fh (still zero): an even split of
+  // the bin's key range, or for the four bins wider than kFineWindow keys a
   // window of that many keys at the end nearer to magnitude 1 (keys outside
   // clamp to the end bins)
   auto fine_local = [&]() {
     cl_fine_window(T, loT, hiT, 0u, 0u, flo, fshift);
-    for (int i = threadIdx.x; i < kClFine; i += kClThreads) sm.hist[i] = 0;
-    __syncthreads();
     for (int q = 0; q < vq; ++q) {
       const uint4 k4 = sm.keys[q * kClThreads + threadIdx.x];
       const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        if (kv[j] >= loT && kv[j] <= hiT) atomicAdd(&sm.hist[cl_fine_idx(kv[j], flo, fshift)], 1);
+        if (kv[j] >= loT && kv[j] <= hiT) atomicAdd(&fh[cl_fine_idx(kv[j], flo, fshift)], 1);
     }
     __syncthreads();
   };
@@ -1538,7 +1839,7 @@ __global__ void __launch_bounds__(kClThreads, 2)
       wait_pending();
       const uint32_t fm0 = dsmem_map(smem_u32(&sm.fmerge[0]), 0);
       for (int i = threadIdx.x; i < kClFine; i += kClThreads) {
-        const int c = sm.hist[i];
+        const int c = fh[i];
         if (c) dsmem_red_add(fm0 + 4u * (uint32_t)i, c);
       }
       cluster_sync();
@@ -1546,7 +1847,7 @@ __global__ void __launch_bounds__(kClThreads, 2)
         reinterpret_cast<int4 *>(sm.hist)[i] = dsmem_ld4(fm0 + 16u * (uint32_t)i);
       __syncthreads();
     }
-    threshold_from_hist<kClFine>(sm.hist, k - above, sm_scan, sm_misc + 8);
+    threshold_from_hist<kClFine>(local ? fh : sm.hist, k - above, sm_scan, sm_misc + 8);
     S = sm_misc[8];
     above1 = sm_misc[9];
     fineS = sm_misc[10];
@@ -1603,6 +1904,8 @@ __global__ void __launch_bounds__(kClThreads, 2)
   int32_t *boutr = blk ? p.bout + (int64_t)r * bk : nullptr;
   if (bmask) {
     const uint32_t bsel1 = local ? 0u : dsmem_map(smem_u32(&sm.bsel[0]), 1);
+    // a sorted table written by the cluster: the candidates' histogram on CTA 1
+    const uint32_t bh1 = (p.bpt && !local && !btake) ? dsmem_map(smem_u32(&sm.fmerge[0]), 1) : 0u;
     int pb = wb;
 #pragma unroll
     for (int e = 0; e < kClBPer; ++e) {
@@ -1616,6 +1919,7 @@ __global__ void __launch_bounds__(kClThreads, 2)
                                       (unsigned long long)(0xFFFFFFFFu - (uint32_t)b);
         if (local) sm.bsel[pb] = cv;
         else dsmem_st64(bsel1 + 8u * (uint32_t)pb, cv);
+        if (bh1) dsmem_red_add(bh1 + 4u * (uint32_t)cl_fine_idx(sm.bkey[idx], E + 1u, kBShift), 1);
       }
       ++pb;
     }
@@ -1644,23 +1948,14 @@ __global__ void __launch_bounds__(kClThreads, 2)
       for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kClThreads) hw[i] = 0;
     }
   }
+  // ---- 6. the sorted block table: CTA 1 works out the chosen blocks'
+  // threshold item and every CTA's slice offset, then each CTA writes its
+  // slice; in the general case (V = 0) CTA 1 selects and sorts alone
+  const bool dtab = blk && p.bpt && !local;
+  if (dtab && cl_table_cluster(p, r, n, rank, E + 1u, sm, sm_h, sm_scan, sm_misc, sm_u64)) return;
   if (blk && (local || rank == 1)) {
     __syncthreads();  // the local CTA: the score select's finish is done with the scratch
-    // with a table to write, the chosen ids go to this CTA's block-key buffer
-    // (free after the last cluster barrier) and are sorted from there
-    int32_t *ids = p.bpt ? reinterpret_cast<int32_t *>(sm.bkey) : boutr;
-    const int flag = cl_block_finish(row, n, p.vec != 0, bk, ids, btake, sm.bctr, sm.bsel,
-                                     reinterpret_cast<uint32_t *>(sm.keys), sm.hist, sm_h, sm_scan,
-                                     sm_misc);
-    if (p.bflags && threadIdx.x == 0) p.bflags[r] = flag;
-    if (p.bpt) {
-      __syncthreads();  // the block ids are in place
-      __shared__ long long sm_live[kClThreads / 32];
-      cl_sort_table(ids, boutr, bk, n, nbk, p.bpt + (int64_t)(r / p.next_n) * p.bpt_stride, p.bps,
-                    p.bphys ? p.bphys + (int64_t)r * bk : nullptr,
-                    p.bvalid ? p.bvalid + r : nullptr, reinterpret_cast<uint32_t *>(sm.hist),
-                    sm_scan, sm_live);
-    }
+    cl_block_general(p, r, n, sm, sm_h, sm_scan, sm_misc);
   }
 }
 
@@ -1785,7 +2080,6 @@ __global__ void __launch_bounds__(kRowThreads)
 // warp finds the digit), and one block scan of packed counts gives every
 // thread its output slots -- the keys above the threshold anywhere, the keys
 // equal to it in position order (ties to the lower position).
-constexpr int kF16MaxRow = 16384;
 
 // WPT: words a thread holds (rows of up to 2 * WPT * kSelThreads scores)
 template <bool BF16, int WPT>

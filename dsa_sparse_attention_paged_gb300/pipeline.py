@@ -178,40 +178,35 @@ class DecodePlan:
 
 
 class HostStepPipeline:
-    """Decode steps fed from and returned to host memory, with the copies of
-    one step overlapped with the kernels of its neighbours.
+    """Decode steps fed from and returned to pinned host memory, two in
+    flight: while one step computes, the next one's inputs travel in and the
+    previous one's results travel out.
 
-    Two ``DecodePlan``s and two device copies of the per-step inputs (q,
-    weights, context lengths, page table) alternate between steps.  ``submit``
-    queues three things on three streams:
-
-      input stream    host-to-device copy of the step's inputs into the idle
-                      set, once the step that last read that set has finished
-      compute stream  the step (``DecodePlan.step``), once its inputs are in
-                      and the step that last wrote its plan's outputs has had
-                      them copied out
-      output stream   device-to-host copy of both index sets, once the step
-                      has finished
-
-    so step i+1's inputs travel while step i computes, and step i's results
-    travel while step i+1 computes.  The K cache (``kv``, ``kscale``) is
-    resident device state that both plans read.  Host tensors must be pinned
-    and stay untouched until the step's ``wait``; the kernels and the results
-    are those of ``DecodePlan.step``."""
+    Two slots alternate, each with its own ``DecodePlan``, device copy of the
+    per-step inputs (q, weights, context lengths, page table) and stream.  A
+    slot's step -- the host-to-device copies, the plan's kernels and the
+    device-to-host copies of both index sets -- is captured once as a CUDA
+    graph (its first submit runs the step eagerly and captures it), so a
+    submit is one graph launch.  A graph holds the addresses of the host
+    tensors it was captured with: pass each slot the same pinned tensors on
+    every submit and rewrite their contents in place (a slot given other
+    tensors is captured again).  The K cache (``kv``, ``kscale``) is resident
+    device state that both slots read.  Host inputs may be rewritten, and host
+    outputs read, once ``wait(i)`` for the slot's last step has returned.  The
+    kernels and the results are those of ``DecodePlan.step``."""
 
     def __init__(self, B, next_n, max_context, page_size, kv, kscale, k=2048, kb=512,
                  device="cuda"):
         dev = torch.device(device)
+        self.device = dev
         self.plans = [DecodePlan(B, next_n, max_context, page_size, k=k, kb=kb, two_level=True,
                                  device=dev) for _ in range(2)]
         self.kv, self.kscale = kv, kscale
+        self.streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
         self.inputs = [None, None]
-        self.s_in = torch.cuda.Stream(device=dev)
-        self.s_compute = torch.cuda.Stream(device=dev)
-        self.s_out = torch.cuda.Stream(device=dev)
-        self.step_done = [None, None]   # per set: the last step that used it finished
-        self.out_done = [None, None]    # per set: that step's outputs reached the host
-        self.pending = {}               # step index -> out_done event
+        self.graphs = [None, None]
+        self.bound = [None, None]   # host tensor addresses each slot's graph holds
+        self.pending = {}           # step index -> event after its host outputs
         self.n = 0
         # the plans' buffers were zeroed on the caller's stream
         ready = torch.cuda.Event()
@@ -224,49 +219,51 @@ class HostStepPipeline:
 
     def start_after(self, event):
         """Make every later submit wait for ``event`` (e.g. a timing mark)."""
-        for st in (self.s_in, self.s_compute, self.s_out):
+        for st in self.streams:
             st.wait_event(event)
 
     def record_all(self):
-        """An event on each stream, after everything submitted so far."""
+        """An event on each slot's stream, after everything submitted so far."""
         evs = []
-        for st in (self.s_in, self.s_compute, self.s_out):
+        for st in self.streams:
             e = torch.cuda.Event()
             e.record(st)
             evs.append(e)
         return evs
 
+    def _run(self, s, host):
+        plan, (dq, dw, dc, dp) = self.plans[s], self.inputs[s]
+        for d, h in zip((dq, dw, dc, dp), host[:4]):
+            d.copy_(h, non_blocking=True)
+        dense, sparse = plan.step(dq, self.kv, self.kscale, dw, dp, dc)
+        host[4].copy_(dense, non_blocking=True)
+        host[5].copy_(sparse, non_blocking=True)
+
     def submit(self, q, weights, context_lens, page_table, out_dense, out_sparse):
         """Queue one step on pinned host tensors; returns the step index."""
         i, s = self.n, self.n % 2
-        plan = self.plans[s]
-        dev = plan.logits.device
-        host_in = (q, weights, context_lens, page_table)
-        if self.inputs[s] is None:
-            self.inputs[s] = [torch.empty(t.shape, dtype=t.dtype, device=dev) for t in host_in]
-        dq, dw, dc, dp = self.inputs[s]
-        with torch.cuda.stream(self.s_in):
-            if self.step_done[s] is not None:
-                self.s_in.wait_event(self.step_done[s])
-            for d, h in zip(self.inputs[s], host_in):
-                d.copy_(h, non_blocking=True)
-            in_ready = torch.cuda.Event()
-            in_ready.record(self.s_in)
-        with torch.cuda.stream(self.s_compute):
-            self.s_compute.wait_event(in_ready)
-            if self.out_done[s] is not None:
-                self.s_compute.wait_event(self.out_done[s])
-            dense, sparse = plan.step(dq, self.kv, self.kscale, dw, dp, dc)
-            done = torch.cuda.Event()
-            done.record(self.s_compute)
-        with torch.cuda.stream(self.s_out):
-            self.s_out.wait_event(done)
-            out_dense.copy_(dense, non_blocking=True)
-            out_sparse.copy_(sparse, non_blocking=True)
-            oe = torch.cuda.Event()
-            oe.record(self.s_out)
-        self.step_done[s], self.out_done[s] = done, oe
-        self.pending[i] = oe
+        host = (q, weights, context_lens, page_table, out_dense, out_sparse)
+        if not all(t.is_pinned() for t in host):
+            raise ValueError("HostStepPipeline needs pinned host tensors")
+        st = self.streams[s]
+        key = tuple((t.data_ptr(), tuple(t.shape), t.dtype) for t in host)
+        if self.bound[s] != key:
+            if self.inputs[s] is None:
+                self.inputs[s] = [torch.empty(t.shape, dtype=t.dtype, device=self.device)
+                                  for t in host[:4]]
+            with torch.cuda.stream(st):
+                self._run(s, host)  # this step, eagerly (sets the kernels' attributes)
+            st.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                self._run(s, host)
+            self.graphs[s], self.bound[s] = g, key
+        else:
+            with torch.cuda.stream(st):
+                self.graphs[s].replay()
+        ev = torch.cuda.Event()
+        ev.record(st)
+        self.pending[i] = ev
         self.n += 1
         return i
 
@@ -275,6 +272,6 @@ class HostStepPipeline:
         self.pending.pop(i).synchronize()
 
     def synchronize(self):
-        for st in (self.s_in, self.s_compute, self.s_out):
+        for st in self.streams:
             st.synchronize()
         self.pending.clear()

@@ -46,36 +46,51 @@ def test_graph_replay_follows_inputs_rewritten_in_place(pair_rows):
 
 
 def test_host_pipeline_matches_eager_steps():
-    """Overlapped host-to-host steps (two plans, three streams): every step's
-    host outputs equal an eager step on the same inputs, with steps on
-    different lengths, queries and weights in flight together."""
+    """Host-to-host steps two in flight (two slots, each a captured graph of
+    copies + kernels + copies): every step's host outputs equal an eager step
+    on the same inputs.  Each slot keeps its pinned buffers; their contents
+    change between steps (lengths, queries, weights), so the later steps are
+    graph replays over rewritten host memory."""
     from dsa_sparse_attention_paged_gb300.pipeline import DecodePlan, HostStepPipeline
     cases = [S.generate(S.Workload("pipe %d" % i, 3, 2, [20000] * 3, 64, dist, 300 + i))
              for i, dist in enumerate(("mixed", "normal", "mixed"))]
     lens = ([20000, 9000, 3000], [7000, 20000, 100], [15000, 15000, 15000])
     d = to_dev(cases[0])  # the K cache is the first case's; pages cover 20000 keys
     pipe = HostStepPipeline(3, 2, 20000, 64, d["kv"], d["kscale"], k=2048, kb=256)
-    host_in, outs = [], []
-    for c, L in zip(cases, lens):
-        host_in.append({"q": torch.from_numpy(c["q"]).pin_memory(),
-                        "weights": torch.from_numpy(c["weights"]).pin_memory(),
-                        "context_lens": torch.tensor(L, dtype=torch.int32).pin_memory(),
-                        "page_table": torch.from_numpy(cases[0]["page_table"]).pin_memory()})
-    order = [0, 1, 2, 1, 0, 2]
-    for j in order:
-        h = host_in[j]
-        o = (torch.full((6, 2048), -5, dtype=torch.int32).pin_memory(),
-             torch.full((6, 2048), -5, dtype=torch.int32).pin_memory())
-        outs.append(o)
-        pipe.submit(h["q"], h["weights"], h["context_lens"], h["page_table"], *o)
+    c0 = cases[0]
+    slots = [({"q": torch.empty(c0["q"].shape, dtype=torch.uint8).pin_memory(),
+               "weights": torch.empty(c0["weights"].shape, dtype=torch.float32).pin_memory(),
+               "context_lens": torch.empty((3,), dtype=torch.int32).pin_memory(),
+               "page_table": torch.from_numpy(c0["page_table"]).pin_memory()},
+              (torch.empty((6, 2048), dtype=torch.int32).pin_memory(),
+               torch.empty((6, 2048), dtype=torch.int32).pin_memory())) for _ in range(2)]
+    plan = DecodePlan(3, 2, 20000, 64, k=2048, kb=256)
+
+    def expect(j):
+        c = cases[j]
+        dense, sparse = plan.step(torch.from_numpy(c["q"]).cuda(), d["kv"], d["kscale"],
+                                  torch.from_numpy(c["weights"]).cuda(), d["page_table"],
+                                  torch.tensor(lens[j], dtype=torch.int32, device="cuda"))
+        torch.cuda.synchronize()
+        return dense.cpu().numpy(), sparse.cpu().numpy()
+
+    order = [0, 1, 2, 1, 0, 2, 2, 0]
+    for i, j in enumerate(order):
+        hin, hout = slots[i % 2]
+        if i >= 2:  # the slot's previous step: outputs final, inputs free
+            pipe.wait(i - 2)
+            e_dense, e_sparse = expect(order[i - 2])
+            assert sets_equal(hout[0].numpy(), e_dense)
+            assert sets_equal(hout[1].numpy(), e_sparse)
+        hin["q"].copy_(torch.from_numpy(cases[j]["q"]))
+        hin["weights"].copy_(torch.from_numpy(cases[j]["weights"]))
+        hin["context_lens"].copy_(torch.tensor(lens[j], dtype=torch.int32))
+        pipe.submit(hin["q"], hin["weights"], hin["context_lens"], hin["page_table"], *hout)
     pipe.synchronize()
     for p in pipe.plans:
         assert p.ws.status() == 0
-    plan = DecodePlan(3, 2, 20000, 64, k=2048, kb=256)
-    for j, o in zip(order, outs):
-        h = host_in[j]
-        dense, sparse = plan.step(h["q"].cuda(), d["kv"], d["kscale"], h["weights"].cuda(),
-                                  h["page_table"].cuda(), h["context_lens"].cuda())
-        torch.cuda.synchronize()
-        assert sets_equal(o[0].numpy(), dense.cpu().numpy())
-        assert sets_equal(o[1].numpy(), sparse.cpu().numpy())
+    for i in (len(order) - 2, len(order) - 1):
+        e_dense, e_sparse = expect(order[i])
+        hout = slots[i % 2][1]
+        assert sets_equal(hout[0].numpy(), e_dense)
+        assert sets_equal(hout[1].numpy(), e_sparse)

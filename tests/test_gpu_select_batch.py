@@ -156,12 +156,17 @@ def test_fused_block_maxima_select(B, nn, ctx, ps, dist, kb):
     assert (flags.cpu().numpy() == 0).all(), flags
 
 
+@pytest.mark.parametrize("table", [False, True])
 @pytest.mark.parametrize("n", [60000, 12000])
-@pytest.mark.parametrize("kind", ["nan_blocks", "tied_maxima", "wide_bin"])
-def test_fused_block_select_edge_cases(kind, n):
+@pytest.mark.parametrize("kind", ["nan_blocks", "tied_maxima", "wide_bin", "inf_blocks",
+                                  "plain"])
+def test_fused_block_select_edge_cases(kind, n, table):
     """All-NaN blocks are never chosen; thousands of equal maxima overflow the
     candidate slots and take the exact fallback (ties to the lower block);
-    maxima spread over the saturating bin use the fine window."""
+    maxima spread over the saturating bin use the fine window; more blocks at
+    +inf than the table holds take the lowest of them.  With `table` the
+    block output is the sorted block table (written by the whole cluster in
+    the plain case), checked with its physical blocks and live lengths."""
     import dsa_sparse_attention_paged_gb300 as D
     R = 3
     rng = np.random.default_rng(23)
@@ -172,23 +177,48 @@ def test_fused_block_select_edge_cases(kind, n):
     elif kind == "tied_maxima":
         x[:, :] = rng.normal(-5, 1, (R, n)).astype(np.float32)
         x[:, ::8] = 1.0                      # every block has the same maximum
-    else:
+    elif kind == "wide_bin":
         x[:, ::3] = np.exp(rng.uniform(np.log(223.0), np.log(1e7), (R, (n + 2) // 3)))
+    elif kind == "inf_blocks":
+        x[:, 8 * 37: 8 * 37 + 8 * 700: 8] = np.inf  # 700 blocks at +inf (rows of 12000: fewer)
     L = torch.from_numpy(x).cuda()
     ctx = torch.tensor([n, n - 5, n // 3], dtype=torch.int32, device="cuda")
     hist = torch.from_numpy(O.histogram(x, ctx.cpu().numpy())).cuda()
     ws = D.Workspace(R)
     bflags = torch.full((R,), 9, dtype=torch.int32, device="cuda")
+    ps = 64
+    extra = {}
+    if table:
+        # each row its own request; pages of a request a permutation of a pool
+        npg = (n + ps - 1) // ps
+        pt_h = np.stack([rng.permutation(R * npg)[:npg] for _ in range(R)]).astype(np.int32)
+        phys = torch.full((R, 512), -5, dtype=torch.int32, device="cuda")
+        vlen = torch.full((R,), -5, dtype=torch.int32, device="cuda")
+        extra = dict(block_page_table=torch.from_numpy(pt_h).cuda(), block_page_size=ps,
+                     block_phys=phys, block_valid_lens=vlen)
     (out, bout), = D.coarse_hist_topk_batch([
         dict(logits=L, context_lens=ctx, next_n=1, k=2048, histogram=hist, block_k=512,
-             block_fallback_flags=bflags)], ws)
+             block_fallback_flags=bflags, **extra)], ws)
     torch.cuda.synchronize()
     assert ws.status() == 0
     rl = ctx.cpu().numpy().astype(np.int64)
     assert sets_equal(out.cpu().numpy(), O.topk(x, rl, 2048))
-    assert sets_equal(bout.cpu().numpy(), _block_ref(x, rl, 512))
+    ids, ref = bout.cpu().numpy(), _block_ref(x, rl, 512)
+    if table:
+        # the table pads with INT32_MAX, and a row of at most 512 blocks takes
+        # the identity table (checked against the oracle's table below)
+        ids = np.where(ids == np.iinfo(np.int32).max, -1, ids)
+        big = (rl + 7) // 8 > 512
+        ids, ref = ids[big], ref[big]
+    assert sets_equal(ids, ref)
     f = bflags.cpu().numpy()
     assert set(f.tolist()) <= ({0, 2} if kind == "tied_maxima" else {0}), f
+    if table:
+        A = O.block_amax8(x, rl, skip_le=512, amax_stride=(n + 7) // 8, fill=0.0)
+        t_ref, p_ref, v_ref = O.block_table(A, rl, np.arange(R, dtype=np.int32), 512, pt_h, ps)
+        np.testing.assert_array_equal(bout.cpu().numpy(), t_ref)
+        np.testing.assert_array_equal(phys.cpu().numpy(), p_ref)
+        np.testing.assert_array_equal(vlen.cpu().numpy(), v_ref)
 
 
 @pytest.mark.parametrize("B,nn,ctx,ps", [
