@@ -410,8 +410,9 @@ def main():
     K = args.steps
     ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(K)]
+    every = max(1, min(LOGITS_EVERY, K // 4))  # at least four bracketed launches
     ev_k = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for n in names} if i % LOGITS_EVERY == 0 or K < LOGITS_EVERY else None
+             for n in names} if i % every == 0 else None
             for i in range(K)]
     uuid = None
     try:
