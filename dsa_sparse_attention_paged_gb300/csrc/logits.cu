@@ -37,6 +37,8 @@
 // by counters (no division per stage).
 #include <algorithm>
 
+#include <type_traits>
+
 #include "dsa_device.cuh"
 #include "dsa_host.h"
 
@@ -350,9 +352,15 @@ __device__ __forceinline__ float head_sum(const uint32_t (&v)[32], float ks, con
 // the block-scaled MMA; dense logits only.
 // head_sum in two calls of 16 heads each (heads 16p .. 16p+15 for p = 0, 1,
 // in that order): the same chains in the same order, so the same float.
-__device__ __forceinline__ void head_sum_part(const uint32_t (&v)[16], float ks, const float *w,
-                                              uint64_t &a01, uint64_t &a23) {
-  if (ks >= 0.0f && ks <= 3.4028234e38f) {
+// ALLOK (chosen per warp by the caller): every lane's kscale is finite and
+// >= 0, so the sum is taken without it and the caller applies it.  Otherwise
+// each lane takes its own case by selects, not branches (the warp's TMEM
+// loads around this call need it converged): a lane whose kscale qualifies
+// (`ksok`) still sums without it, the others apply it term by term.
+template <bool ALLOK>
+__device__ __forceinline__ void head_sum_part(const uint32_t (&v)[16], float ks, bool ksok,
+                                              const float *w, uint64_t &a01, uint64_t &a23) {
+  if (ALLOK) {
 #pragma unroll
     for (int h = 0; h < 16; h += 4) {
       const float4 wv = *reinterpret_cast<const float4 *>(w + h);
@@ -372,16 +380,13 @@ __device__ __forceinline__ void head_sum_part(const uint32_t (&v)[16], float ks,
     float p0, p1, p2, p3;
     upk2(mul2(pk2(__uint_as_float(v[h + 0]), __uint_as_float(v[h + 1])), ks2), p0, p1);
     upk2(mul2(pk2(__uint_as_float(v[h + 2]), __uint_as_float(v[h + 3])), ks2), p2, p3);
+    p0 = ksok ? __uint_as_float(v[h + 0]) : p0;
+    p1 = ksok ? __uint_as_float(v[h + 1]) : p1;
+    p2 = ksok ? __uint_as_float(v[h + 2]) : p2;
+    p3 = ksok ? __uint_as_float(v[h + 3]) : p3;
     a01 = fma2(pk2(wv.x, wv.y), pk2(fmaxf(p0, 0.0f), fmaxf(p1, 0.0f)), a01);
     a23 = fma2(pk2(wv.z, wv.w), pk2(fmaxf(p2, 0.0f), fmaxf(p3, 0.0f)), a23);
   }
-}
-__device__ __forceinline__ float head_sum_finish(float ks, uint64_t a01, uint64_t a23) {
-  float c0, c1, c2, c3;
-  upk2(a01, c0, c1);
-  upk2(a23, c2, c3);
-  const float s = (c0 + c1) + (c2 + c3);
-  return (ks >= 0.0f && ks <= 3.4028234e38f) ? ks * s : s;
 }
 
 template <int NN, bool SPARSE, int OUT, bool HIST, bool MX = false>
@@ -865,11 +870,19 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
         for (int k = 0; k < 7; ++k) rq[k] = rq[k + 1];
         --avail;
         const int s = rs.idx;
-        if (lane == 0) ok = mbar_wait(EMPTY(s), rs.ph ^ 1, ctl);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        if (row >= 0)
-          tma_load_2d_hint(kst + s * kStageK + lane * 8 * 128, &tm_k, FULL(s), 0, row, pol);
+        // Wait for the slot only in a stage this warp loads into.  A stage
+        // whose blocks 16..31 are all padding completes without this warp
+        // (warp 0 arms its barrier for the other blocks alone), so the MMA
+        // may release the slot before this warp gets there, and a wait on it
+        // would then be for a phase already past.  A stage this warp loads
+        // into cannot complete without it, so that wait is never behind.
+        if (__ballot_sync(0xffffffffu, row >= 0) != 0) {
+          if (lane == 0) ok = mbar_wait(EMPTY(s), rs.ph ^ 1, ctl);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          if (row >= 0)
+            tma_load_2d_hint(kst + s * kStageK + lane * 8 * 128, &tm_k, FULL(s), 0, row, pol);
+        }
         ++issued;
       }
       if (!ok && lane == 0) {
@@ -1039,20 +1052,34 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
         uint64_t c01 = 0, c23 = 0;
         tmem_ld16(tcol, hv[0]);
         tmem_ld_wait();
+        const bool ksok = ks >= 0.0f && ks <= 3.4028234e38f;
+        // one unrolled pass per case, chosen per warp (the TMEM loads in it
+        // need the whole warp; padding tokens may carry any kscale)
+        auto run = [&](auto allok_tag) {
+          constexpr bool ALLOK = decltype(allok_tag)::value;
 #pragma unroll
-        for (int step = 0; step < 2 * NN; ++step) {  // row step / 2, heads 16 (step % 2) ..
-          if (step + 1 < 2 * NN) {
-            tmem_ld16(tcol + (uint32_t)((step + 1) * 16), hv[(step + 1) & 1]);
-          } else {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(AEMPTY(x));
+          for (int step = 0; step < 2 * NN; ++step) {  // row step / 2, heads 16 (step % 2) ..
+            if (step + 1 < 2 * NN) {
+              tmem_ld16(tcol + (uint32_t)((step + 1) * 16), hv[(step + 1) & 1]);
+            } else {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(AEMPTY(x));
+            }
+            if ((step & 1) == 0) c01 = c23 = pk2(0.0f, 0.0f);
+            head_sum_part<ALLOK>(hv[step & 1], ks, ksok, wq + 16 * step, c01, c23);
+            if (step & 1) {
+              float c0, c1, c2, c3;
+              upk2(c01, c0, c1);
+              upk2(c23, c2, c3);
+              const float sm = (c0 + c1) + (c2 + c3);
+              acc[step >> 1] = (ALLOK || ksok) ? ks * sm : sm;
+            }
+            if (step + 1 < 2 * NN) tmem_ld_wait();
           }
-          if ((step & 1) == 0) c01 = c23 = pk2(0.0f, 0.0f);
-          head_sum_part(hv[step & 1], ks, wq + 16 * step, c01, c23);
-          if (step & 1) acc[step >> 1] = head_sum_finish(ks, c01, c23);
-          if (step + 1 < 2 * NN) tmem_ld_wait();
-        }
+        };
+        if (__all_sync(0xffffffffu, ksok)) run(std::true_type{});
+        else run(std::false_type{});
       } else {
 #pragma unroll
       for (int j0 = 0; j0 < NN; j0 += kB) {
@@ -1083,18 +1110,16 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
         }
       } else {
         const int64_t t = pos;
+        if (t == a.out_stride && ctx_b > a.out_stride) set_status(a.status, DSA_DEV_BOUNDS);
+        float *const op = reinterpret_cast<float *>(a.out) + (int64_t)row_base * a.out_stride + t;
+        const bool in_stride = t < a.out_stride;
 #pragma unroll
         for (int j = 0; j < NN; ++j) {
-          int64_t n_rj = ctx_b - (NN - 1 - j);
-          if (n_rj > a.out_stride) {
-            n_rj = a.out_stride;
-            if (t == a.out_stride) set_status(a.status, DSA_DEV_BOUNDS);
-          }
-          if (t < n_rj) {
+          const int64_t n_rj = ctx_b - (NN - 1 - j);
+          if (in_stride && t < n_rj) {
             // kept in L2 for the select that reads the row next (the K stream
             // around it is marked evict-first)
-            st_f32_hint(reinterpret_cast<float *>(a.out) + (int64_t)(row_base + j) * a.out_stride + t,
-                        acc[j], out_pol);
+            st_f32_hint(op + j * a.out_stride, acc[j], out_pol);
             if (HIST) {
               const int bin = coarse_bin(acc[j]);
               if (bin >= 0) atomicAdd(&my_hist[j * kHistWords + (bin >> 1)], 1u << (16 * (bin & 1)));
