@@ -243,11 +243,11 @@ class HostStepPipeline:
         """Queue one step on pinned host tensors; returns the step index."""
         i, s = self.n, self.n % 2
         host = (q, weights, context_lens, page_table, out_dense, out_sparse)
-        if not all(t.is_pinned() for t in host):
-            raise ValueError("HostStepPipeline needs pinned host tensors")
         st = self.streams[s]
         key = tuple((t.data_ptr(), tuple(t.shape), t.dtype) for t in host)
         if self.bound[s] != key:
+            if not all(t.is_pinned() for t in host):
+                raise ValueError("HostStepPipeline needs pinned host tensors")
             if self.inputs[s] is None:
                 self.inputs[s] = [torch.empty(t.shape, dtype=t.dtype, device=self.device)
                                   for t in host[:4]]
