@@ -57,9 +57,10 @@ constexpr int kMaxStages = 8;
 // two groups of a sub-tile take alternate stages.  Eight warps consume each
 // stage either way.
 __host__ __device__ constexpr int epi_warps(int nn) { return nn == 1 ? 8 : 16; }
-// The sparse pass adds a second producer warp (after the epilogue warps).
-__host__ __device__ constexpr int threads_for(int nn, bool sparse) {
-  return 64 + 32 * epi_warps(nn) + (sparse ? 32 : 0);
+// The sparse pass adds a second producer warp (after the epilogue warps), the
+// MXFP4 pass a scale-factor warp in the same place.
+__host__ __device__ constexpr int threads_for(int nn, bool sparse, bool mx = false) {
+  return 64 + 32 * epi_warps(nn) + ((sparse || mx) ? 32 : 0);
 }
 constexpr int kStageEpiWarps = 8;
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in per CTA
@@ -138,7 +139,7 @@ __host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, bool sparse, in
   off += hist ? 2 * hist_slots_per_group(nn) * nn * kHistWords * 4 : 0;
   off = (off + 7) & ~7;
   p.bar = off;
-  off += (2 * stages + 2 * nks + 4 + 2 * nacc + 3) * 8;
+  off += (2 * stages + 2 * nks + 4 + 2 * nacc + 3 + (mx ? stages : 0)) * 8;
   p.misc = off;
   off += 64 + 2 * 32 * 4;  // flags/schedule + the producer's two row tables
   p.sptab = off;
@@ -390,7 +391,7 @@ __device__ __forceinline__ void head_sum_part(const uint32_t (&v)[16], float ks,
 }
 
 template <int NN, bool SPARSE, int OUT, bool HIST, bool MX = false>
-__global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
+__global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const LogitsArgs a) {
   static_assert(!(MX && SPARSE), "MXFP4 keys: dense logits only");
@@ -405,7 +406,7 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
   constexpr int HS = hist_slots_per_group(NN);
   constexpr int EW = epi_warps(NN);
   constexpr int NPAR = EW / kStageEpiWarps;  // groups sharing a sub-tile (alternate stages)
-  constexpr int kThr = threads_for(NN, SPARSE);
+  constexpr int kThr = threads_for(NN, SPARSE, MX);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -435,6 +436,7 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
   auto AEMPTY = [&](int x) { return qb0 + 8u * (4 + A + x); };
   const uint32_t DRAIN = qb0 + 8u * (4 + 2 * A);
   auto GSYNC = [&](int g) { return qb0 + 8u * (5 + 2 * A + g); };
+  auto SFR = [&](int s) { return qb0 + 8u * (7 + 2 * A + s); };  // MX: scale factors staged
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P.misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P.misc + 4);
   int *sched = reinterpret_cast<int *>(smem + P.misc + 16);
@@ -447,7 +449,7 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
     }
     for (int k = 0; k < KS; ++k) {
       mbar_init(KSF(k), SPARSE ? 32 : 1);  // sparse: one cp.async arrival per producer lane
-      mbar_init(KSE(k), MX ? 1 : kStageEpiWarps);  // MX: the MMA warp reads the exponents
+      mbar_init(KSE(k), MX ? 1 : kStageEpiWarps);  // MX: the scale-factor warp reads the exponents
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(QFULL(q), 1);
@@ -458,6 +460,8 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
       mbar_init(AEMPTY(x), kStageEpiWarps);
     }
     mbar_init(DRAIN, 1);
+    if (MX)
+      for (int s = 0; s < S; ++s) mbar_init(SFR(s), 1);
     mbar_init(GSYNC(0), 4 * NPAR);
     mbar_init(GSYNC(1), 4 * NPAR);
     *abort_flag = 0;
@@ -708,51 +712,33 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
     }
   } else if (warp == 1 && MX) {
     // ------------------------------------------------------------ MMA issuer, MXFP4 keys
-    // The whole warp turns the stage's 256 token exponent words (token order,
-    // byte j = exponent of dimensions 32j .. 32j+31) into the two tables the
-    // scale-factor copy reads: row i of sub-tile h holds the words of tokens
-    // i, i+32, i+64, i+96 of the sub-tile, which lands token m's exponents in
-    // TMEM lane m, column m / 32 of the sub-tile's A scale factors; the MMA
-    // for dimensions 32kk .. 32kk+31 takes byte kk.  Lane 0 waits and issues.
-    TileIter<SPARSE> it;
-    it.init(a, u_start, i_start);
-    int prev_u = -1, unit_ord = -1, qb = 0;
-    bool ok = true;
-    long long mmas = 0;
-    Ring rs, ra, rk;
-    rs.init(S);
-    ra.init(A);
-    rk.init(KS);
-    const uint32_t *kraw = reinterpret_cast<const uint32_t *>(ks_s);
-    for (long long n = 0; n < count; ++n, it.next(a), rs.next(), ra.next(), rk.next()) {
-      if (it.u != prev_u) {
-        ++unit_ord;
-        prev_u = it.u;
-        qb = unit_ord & 1;
-        if (lane == 0) ok = mbar_wait(QFULL(qb), (unit_ord >> 1) & 1, ctl);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-      }
-      const int s = rs.idx;
-      const int x = ra.idx;
-      const int kx = rk.idx;
-      if (lane == 0)
-        ok = mbar_wait(AEMPTY(x), ra.ph ^ 1, ctl) && mbar_wait(FULL(s), rs.ph, ctl) &&
-             mbar_wait(KSF(kx), rk.ph, ctl);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
-      uint8_t *stg = smem + P.sfst + s * kSfStage;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t *src = kraw + kx * kStageTok + h * kSubTok + lane;
-        *reinterpret_cast<uint4 *>(stg + h * 512 + 16 * lane) =
-            make_uint4(src[0], src[32], src[64], src[96]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(KSE(kx));  // the exponents of this ring slot are read
+    // Per stage: the scale-factor warp's two staged tables go to the sub-tiles'
+    // A scale-factor columns of TMEM (tcgen05.cp, in issue order with the
+    // MMAs that read them), then four block-scaled MMAs a sub-tile, the MMA
+    // for dimensions 32kk .. 32kk+31 taking exponent byte kk.
+    if (lane == 0) {
+      TileIter<SPARSE> it;
+      it.init(a, u_start, i_start);
+      int prev_u = -1, unit_ord = -1, qb = 0;
+      bool ok = true;
+      long long mmas = 0;
+      Ring rs, ra;
+      rs.init(S);
+      ra.init(A);
+      for (long long n = 0; n < count; ++n, it.next(a), rs.next(), ra.next()) {
+        if (it.u != prev_u) {
+          ++unit_ord;
+          prev_u = it.u;
+          qb = unit_ord & 1;
+          if (!(ok = mbar_wait(QFULL(qb), (unit_ord >> 1) & 1, ctl))) break;
+        }
+        const int s = rs.idx;
+        const int x = ra.idx;
+        if (!(ok = mbar_wait(AEMPTY(x), ra.ph ^ 1, ctl) && mbar_wait(FULL(s), rs.ph, ctl) &&
+                   mbar_wait(SFR(s), rs.ph, ctl)))
+          break;
         tc_fence_after();
+        const uint8_t *stg = smem + P.sfst + s * kSfStage;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
           tmem_cp_32x128b_x4(sfa0 + 32u * h, sdesc_plain(smem_u32(stg + h * 512), 128, 128));
@@ -771,11 +757,47 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE), 1)
         mma_commit(AFULL(x));
         if (it.i == it.tiles - 1 || n == count - 1) mma_commit(QEMPTY(qb));
       }
-      __syncwarp();
+      if (!ok && mmas > 0) {
+        mma_commit(DRAIN);
+        mbar_wait_drain(DRAIN, 0, a.wait_limit);
+      }
     }
-    if (!ok && lane == 0 && mmas > 0) {
-      mma_commit(DRAIN);
-      mbar_wait_drain(DRAIN, 0, a.wait_limit);
+    __syncwarp();
+  } else if (MX && warp == 2 + EW) {
+    // ------------------------------------------------------------ scale-factor warp, MXFP4 keys
+    // Turns each stage's 256 token exponent words (token order, byte j = the
+    // exponent of dimensions 32j .. 32j+31) into the two tables the
+    // scale-factor copy reads: row i of sub-tile h holds the words of tokens
+    // i, i+32, i+64, i+96 of the sub-tile, which lands token m's exponents in
+    // TMEM lane m, column m / 32 of the sub-tile's A scale factors.  Running
+    // ahead of the MMA warp, it keeps these loads, stores and the proxy fence
+    // off the MMA's per-stage path.  The stage's table slot is free once its
+    // exponents have landed: the producer copied them only after the slot's
+    // previous MMAs (and the scale-factor copy before them) had completed.
+    const uint32_t *kraw = reinterpret_cast<const uint32_t *>(ks_s);
+    bool ok = true;
+    Ring rs, rk;
+    rs.init(S);
+    rk.init(KS);
+    for (long long n = 0; n < count; ++n, rs.next(), rk.next()) {
+      const int s = rs.idx;
+      const int kx = rk.idx;
+      if (lane == 0) ok = mbar_wait(KSF(kx), rk.ph, ctl);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      uint8_t *stg = smem + P.sfst + s * kSfStage;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t *src = kraw + kx * kStageTok + h * kSubTok + lane;
+        *reinterpret_cast<uint4 *>(stg + h * 512 + 16 * lane) =
+            make_uint4(src[0], src[32], src[64], src[96]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(KSE(kx));  // the exponents of this ring slot are read
+        mbar_arrive(SFR(s));   // the stage's tables are staged
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -1202,7 +1224,7 @@ dsa_status_t launch_one(const CUtensorMap &tk, const CUtensorMap &tq, const Logi
   a.num_stages = L.stages;
   auto kfn = logits_kernel<NN, SPARSE, OUT, HIST, MX>;
   if (!ensure_smem_attr(reinterpret_cast<const void *>(kfn), L.smem)) return DSA_ERR_CUDA;
-  return launch_pdl(kfn, dim3(grid), dim3(threads_for(NN, SPARSE)), (size_t)L.smem, st, tk, tq, a);
+  return launch_pdl(kfn, dim3(grid), dim3(threads_for(NN, SPARSE, MX)), (size_t)L.smem, st, tk, tq, a);
 }
 
 }  // namespace
