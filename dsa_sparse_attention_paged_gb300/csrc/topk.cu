@@ -1394,7 +1394,7 @@ constexpr int kWGroups = kCl * kSelWarps;
 // warp group, and stores V and the warp groups' exclusive offsets into every
 // CTA's shared memory (tab_addr: V; woff_addr: kSelWarps offsets), with the
 // row's live length.  V = 0 everywhere: this CTA builds the table alone.
-__device__ __noinline__ void cl_block_publish(int64_t n, int bk, bool btake, int nbc,
+__device__ __forceinline__ void cl_block_publish(int64_t n, int bk, bool btake, int nbc,
                                               const unsigned long long *bsel, const int *bh,
                                               uint32_t base, int nloc, unsigned long long *buf,
                                               int *hist, int *sm_h, int *sm_scan, int *sm_misc,
@@ -1403,7 +1403,15 @@ __device__ __noinline__ void cl_block_publish(int64_t n, int bk, bool btake, int
                                               int32_t *bflag) {
   unsigned long long vstar = 0;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  auto wgroup = [&](int64_t b) { return (int)(b / nloc) * kSelWarps + (int)((b % nloc) >> 7); };
+  // warp group of block b: its CTA c = b / nloc (b < kCl * nloc = 8 nloc, so
+  // c by three compares, not a division), then its 128-block run in the CTA
+  auto wgroup = [&](int64_t b64) {
+    const int b = (int)b64;
+    int c = b >= 4 * nloc ? 4 : 0;  // kCl = 8: three halving steps
+    c += b >= (c + 2) * nloc ? 2 : 0;
+    c += b >= (c + 1) * nloc ? 1 : 0;
+    return c * kSelWarps + ((b - c * nloc) >> 7);
+  };
   auto live_of = [&](int64_t b) { const int64_t t = n - 8 * b; return t < 8 ? (int)t : 8; };
   if (!btake && nbc >= bk && nbc <= kBSel) {
     for (int i = threadIdx.x; i <= kWGroups; i += kClThreads) sm_h[i] = 0;  // + live length
