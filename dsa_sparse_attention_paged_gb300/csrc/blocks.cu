@@ -120,10 +120,15 @@ __global__ void __launch_bounds__(kSortThreads)
     nb = (int64_t)kMaxBitmapWords * 32;
   }
   int32_t *idr = ids + (int64_t)r * kb;
+  // (tokens below 2^31: context lengths are int32; a power-of-two page size
+  // takes shifts instead of a division per block)
+  const bool pow2 = (page_size & (page_size - 1)) == 0;
+  const int lg = __ffs(page_size) - 1;
   auto phys_of = [&](int64_t id) -> int32_t {
-    const int64_t tok = id * 8;
-    const int64_t pg = page_table[(int64_t)b * pt_stride + tok / page_size];
-    return (int32_t)((pg * page_size + tok % page_size) / 8);
+    const int tok = (int)(id * 8);
+    const int pi = pow2 ? tok >> lg : tok / page_size;
+    const int64_t pg = page_table[(int64_t)b * pt_stride + pi];
+    return (int32_t)((pg * page_size + (tok - pi * page_size)) >> 3);
   };
   long long live = 0;
   if (nb <= kb) {
@@ -257,10 +262,15 @@ __global__ void __launch_bounds__(kSortThreads)
     }
   }
   __syncthreads();
+  // (tokens below 2^31: context lengths are int32; a power-of-two page size
+  // takes shifts instead of a division per block)
+  const bool pow2 = (page_size & (page_size - 1)) == 0;
+  const int lg = __ffs(page_size) - 1;
   auto phys_of = [&](int64_t id) -> int32_t {
-    const int64_t tok = id * 8;
-    const int64_t pg = page_table[(int64_t)b * pt_stride + tok / page_size];
-    return (int32_t)((pg * page_size + tok % page_size) / 8);
+    const int tok = (int)(id * 8);
+    const int pi = pow2 ? tok >> lg : tok / page_size;
+    const int64_t pg = page_table[(int64_t)b * pt_stride + pi];
+    return (int32_t)((pg * page_size + (tok - pi * page_size)) >> 3);
   };
   const int per = (W + kSortThreads - 1) / kSortThreads;
   const int w0 = threadIdx.x * per, w1 = min(W, w0 + per);

@@ -1229,10 +1229,13 @@ __device__ __noinline__ void cl_sort_table(const int32_t *ids, int32_t *out, int
                                            const int32_t *pt_row, int ps, int32_t *phys,
                                            int32_t *valid, uint32_t *bm, int *sm_scan,
                                            long long *sm_live) {
+  const bool pow2 = (ps & (ps - 1)) == 0;
+  const int lg = __ffs(ps) - 1;
   auto phys_of = [&](int64_t id) -> int32_t {
-    const int64_t tok = id * 8;
-    const int64_t pg = __ldg(&pt_row[tok / ps]);
-    return (int32_t)((pg * ps + tok % ps) / 8);
+    const int tok = (int)id * 8;  // blocks of a cluster row: below 2^14
+    const int pi = pow2 ? tok >> lg : tok / ps;
+    const int64_t pg = __ldg(&pt_row[pi]);
+    return (int32_t)((pg * ps + (tok - pi * ps)) >> 3);
   };
   if (nbk <= bk) {
     for (int i = threadIdx.x; i < bk; i += kClThreads) {
@@ -1542,15 +1545,19 @@ __device__ __forceinline__ void cl_table_slice(const uint32_t *bkey, int nloc, i
     if (lane >= o) incl += x;
   }
   int pos = woff[threadIdx.x >> 5] + incl - c;
+  const bool pow2 = (ps & (ps - 1)) == 0;  // page sizes are powers of two in practice
+  const int lg = __ffs(ps) - 1;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     if (!((sel >> j) & 1u)) continue;
-    const int64_t b = bb + j;
-    out[pos] = (int32_t)b;
+    const int b = (int)(bb + j);  // blocks of a cluster row: below 2^14
+    out[pos] = b;
     if (phys) {
-      const int64_t tok = b * 8;
-      const int64_t pg = (ps % 32 == 0) ? (int64_t)pg0 : (int64_t)__ldg(&pt_row[tok / ps]);
-      phys[pos] = (int32_t)((pg * ps + tok % ps) / 8);
+      const int tok = b * 8;
+      const int pi = pow2 ? tok >> lg : tok / ps;  // page of the block, slot within it
+      const int in_pg = tok - pi * ps;
+      const int64_t pg = (ps % 32 == 0) ? (int64_t)pg0 : (int64_t)__ldg(&pt_row[pi]);
+      phys[pos] = (int32_t)((pg * ps + in_pg) >> 3);
     }
     ++pos;
   }
@@ -1601,7 +1608,7 @@ __device__ __noinline__ bool cl_table_cluster(const ClProb &p, int r, int64_t n,
   int32_t pg0 = 0;  // the page of this thread's first block, read ahead of the barrier
   const int64_t bt = bs0 + 4 * (int64_t)threadIdx.x;
   if (p.bphys && p.bps % 32 == 0 && 4 * (int)threadIdx.x < nloc && bt * 8 < n)
-    pg0 = __ldg(&pt_row[bt * 8 / p.bps]);
+    pg0 = __ldg(&pt_row[(int)(bt * 8) / p.bps]);
   cluster_sync();  // every CTA's V and offsets are in place
   const unsigned long long vstar = sm_tab;
   if (!vstar) return false;
