@@ -595,10 +595,10 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
               raw[jj] = kNone;
               if (n + j0 + jj < count) {
                 int uu, ti;
-                if (NN == 1) {
-                  const long long g = gbase + j0 + jj;
-                  uu = (int)(g / a.sparse_tpu);
-                  ti = (int)(g - (long long)uu * a.sparse_tpu);
+                if (NN == 1) {  // stage numbers fit 32 bits: rows x (kb / 32)
+                  const int g = (int)(gbase + j0 + jj);
+                  uu = g / a.sparse_tpu;
+                  ti = g - uu * a.sparse_tpu;
                 } else {
                   uu = wt.u;
                   ti = wt.i;
@@ -870,9 +870,9 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
             if (n + jj < count) {
               int uu, ti;
               if (NN == 1) {
-                const long long g = gbase + jj;
-                uu = (int)(g / a.sparse_tpu);
-                ti = (int)(g - (long long)uu * a.sparse_tpu);
+                const int g = (int)(gbase + jj);
+                uu = g / a.sparse_tpu;
+                ti = g - uu * a.sparse_tpu;
               } else {
                 uu = wt.u;
                 ti = wt.i;
