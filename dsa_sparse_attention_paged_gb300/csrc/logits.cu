@@ -257,13 +257,21 @@ __device__ void compute_sched(const LogitsArgs &a, int *out_u0, int *out_i0, lon
       T += __shfl_sync(0xffffffffu, warp_incl_scan(t), 31);
     }
   }
-  const long long g0 = (long long)blockIdx.x * T / gridDim.x;
-  const long long g1 = (long long)(blockIdx.x + 1) * T / gridDim.x;
+  // (32-bit divisions when the products fit: a 64-bit one is a long
+  // software sequence on the start of every CTA)
+  long long g0, g1;
+  if (T * gridDim.x < (1ll << 31)) {
+    g0 = (int)(blockIdx.x * (unsigned)T) / (int)gridDim.x;
+    g1 = (int)((blockIdx.x + 1) * (unsigned)T) / (int)gridDim.x;
+  } else {
+    g0 = (long long)blockIdx.x * T / gridDim.x;
+    g1 = (long long)(blockIdx.x + 1) * T / gridDim.x;
+  }
   int u0 = a.num_units, i0 = 0;
   if (g1 > g0) {
     if (fixed) {
-      u0 = (int)(g0 / a.sparse_tpu);
-      i0 = (int)(g0 % a.sparse_tpu);
+      u0 = g0 < (1ll << 31) ? (int)g0 / a.sparse_tpu : (int)(g0 / a.sparse_tpu);
+      i0 = (int)(g0 - (long long)u0 * a.sparse_tpu);
     } else {
       long long acc = 0;
       for (int base = 0; base < a.num_units; base += 32) {

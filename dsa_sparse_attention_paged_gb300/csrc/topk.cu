@@ -32,7 +32,7 @@ __device__ __forceinline__ int64_t row_len(const int32_t *ctx, int next_n, int l
                                            int64_t stride, uint32_t *status) {
   int64_t n = (int64_t)ctx[r / next_n] - (next_n - 1 - r % next_n);
   if (n < 0) n = 0;
-  n = (n + len_div - 1) / len_div;
+  if (len_div > 1) n = (n + len_div - 1) / len_div;
   if (n > stride) {
     if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, DSA_DEV_BOUNDS);
     n = stride;
