@@ -300,8 +300,10 @@ LOGITS_EVERY = 8  # steps per event-bracketed logits launch in the timed loop
 
 def measure_mx_logits(case, w, d, dev, steps=200, warmup=5):
     """The MXFP4-key logits launch (with the fused histogram) at this
-    workload's shape and page pool: seeded E2M1 codes and exponents, launches
-    back to back (the 68-byte-a-key stream is larger than L2), CUDA events."""
+    workload's shape and page pool: seeded E2M1 codes and exponents, timed
+    like the per-workload logits: a CUDA graph of 20 launches back to back
+    (the 68-byte-a-key stream is larger than L2), CUDA events around its
+    replays."""
     import torch
     import dsa_sparse_attention_paged_gb300 as D
     g = torch.Generator().manual_seed(w.seed + 1000)
@@ -322,16 +324,22 @@ def measure_mx_logits(case, w, d, dev, steps=200, warmup=5):
     for _ in range(warmup):
         launch()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
-    for a, b in ev:
-        a.record()
-        launch()
-        b.record()
+    gl = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gl):
+        for _ in range(20):
+            launch()
+    gl.replay()
+    torch.cuda.synchronize()
+    reps = max(1, min(10, steps // 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        gl.replay()
+    e1.record()
     torch.cuda.synchronize()
     if ws.status() != 0:
         raise RuntimeError(f"MXFP4 logits: device status {ws.status():#x}")
-    us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in ev)
+    us = 1e3 * e0.elapsed_time(e1) / (20 * reps)
     keys = int(ctx.sum())
     kbytes = keys * MX_KEY_BYTES
     peak, kind = peaks()
