@@ -12,7 +12,7 @@ the >= 70 % HBM target of the logits kernel is stated on.  Inputs are resident
 in HBM and larger than L2: each step streams the whole K cache (554 MB at
 this size) through the 129 MB L2 with an evict-first policy, so no step finds
 the previous step's K lines; L2 is not flushed between steps.  The timed
-loop replays the step's CUDA graph (DecodePlan.capture / replay), every 8th
+loop replays the step's CUDA graph (DecodePlan.capture / replay), every 16th
 step run eagerly with events around the dense logits launch for the roofline.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the plain CPU
@@ -295,7 +295,7 @@ def measure_workload(name, dev, steps=200, warmup=5):
 
 
 MX_KEY_BYTES = 68  # 64 bytes of E2M1 codes + 4 UE8M0 block exponents per key
-LOGITS_EVERY = 8  # steps per event-bracketed logits launch in the timed loop
+LOGITS_EVERY = 16  # steps per event-bracketed logits launch in the timed loop
 
 
 def measure_mx_logits(case, w, d, dev, steps=200, warmup=5):
