@@ -782,7 +782,9 @@ struct ClProb {
   int32_t *bflags;
   int bk;
   int ws_row0;    // first workspace row of this problem
-  int local;      // rows of at most kClChunk: one CTA per row
+  int local;      // 1: rows of at most kClChunk, one CTA per row; 2: rows of at
+                  // most kClRow / 2, two rows per cluster (four CTAs each); 0:
+                  // one row per cluster
   int vec;        // rows 16-byte aligned: vector loads
   // block output as the sorted block table, or bpt = NULL
   const int32_t *bpt;
@@ -1399,8 +1401,9 @@ constexpr int kWGroups = kCl * kSelWarps;
 // row's live length.  V = 0 everywhere: this CTA builds the table alone.
 __device__ __forceinline__ void cl_block_publish(int64_t n, int bk, bool btake, int nbc,
                                               const unsigned long long *bsel, const int *bh,
-                                              uint32_t base, int nloc, unsigned long long *buf,
-                                              int *hist, int *sm_h, int *sm_scan, int *sm_misc,
+                                              uint32_t base, int nloc, int ncl, uint32_t rbase,
+                                              unsigned long long *buf, int *hist, int *sm_h,
+                                              int *sm_scan, int *sm_misc,
                                               unsigned long long *sm_res, uint32_t tab_addr,
                                               uint32_t woff_addr, int32_t *valid,
                                               int32_t *bflag) {
@@ -1504,15 +1507,16 @@ __device__ __forceinline__ void cl_block_publish(int64_t n, int bk, bool btake, 
     }
   }
   if (vstar) {
-    if (threadIdx.x < kWGroups)
-      dsmem_st32(dsmem_map(woff_addr + 4u * (threadIdx.x % kSelWarps), threadIdx.x / kSelWarps),
+    if ((int)threadIdx.x < ncl * kSelWarps)  // the row's CTAs (rbase .. rbase + ncl - 1)
+      dsmem_st32(dsmem_map(woff_addr + 4u * (threadIdx.x % kSelWarps),
+                           rbase + threadIdx.x / kSelWarps),
                  sm_h[threadIdx.x]);
     if (threadIdx.x == 0) {
       if (valid) *valid = sm_h[kWGroups];
       if (bflag) *bflag = 0;
     }
   }
-  if (threadIdx.x < kCl) dsmem_st64(dsmem_map(tab_addr, threadIdx.x), vstar);
+  if ((int)threadIdx.x < ncl) dsmem_st64(dsmem_map(tab_addr, rbase + threadIdx.x), vstar);
 }
 
 // This CTA's slice of the sorted block table: of its blocks b0 + 4t .. b0 +
@@ -1591,18 +1595,18 @@ __device__ __forceinline__ unsigned long long dsmem_atomic_add64(uint32_t addr, 
 // writes its slice.  Returns false (V = 0) when CTA 1 must build the table
 // alone.  Every CTA of the cluster calls it; `base` is the score select's
 // E + 1, the bottom of the block-candidate histogram (CTA 1's sm.fmerge).
-__device__ __noinline__ bool cl_table_cluster(const ClProb &p, int r, int64_t n, uint32_t rank,
-                                              uint32_t base, ClSmem &sm, int *sm_h, int *sm_scan,
-                                              int *sm_misc, unsigned long long *sm_u64) {
+__device__ __noinline__ bool cl_table_cluster(const ClProb &p, int r, int64_t n, uint32_t rsub,
+                                              uint32_t rbase, int ncl, int nloc, uint32_t base,
+                                              ClSmem &sm, int *sm_h, int *sm_scan, int *sm_misc,
+                                              unsigned long long *sm_u64) {
   __shared__ unsigned long long sm_tab;  // V
   __shared__ int sm_woff[kSelWarps];     // this CTA's warps' first table positions
   const int bk = p.bk;
-  const int nloc = (int)((((p.stride + kCl - 1) / kCl) + 2047) / 2048 * 256);  // blocks a CTA
-  const int64_t bs0 = (int64_t)rank * nloc;
+  const int64_t bs0 = (int64_t)rsub * nloc;  // nloc: blocks a CTA
   const int32_t *pt_row = p.bpt + (int64_t)(r / p.next_n) * p.bpt_stride;
-  if (rank == 1)
-    cl_block_publish(n, bk, (n + 7) / 8 <= bk, sm.bctr, sm.bsel, sm.fmerge, base, nloc,
-                     reinterpret_cast<unsigned long long *>(sm.keys), sm.hist, sm_h, sm_scan,
+  if (rsub == 1)
+    cl_block_publish(n, bk, (n + 7) / 8 <= bk, sm.bctr, sm.bsel, sm.fmerge, base, nloc, ncl,
+                     rbase, reinterpret_cast<unsigned long long *>(sm.keys), sm.hist, sm_h, sm_scan,
                      sm_misc, sm_u64, smem_u32(&sm_tab), smem_u32(&sm_woff[0]),
                      p.bvalid ? p.bvalid + r : nullptr, p.bflags ? p.bflags + r : nullptr);
   int32_t pg0 = 0;  // the page of this thread's first block, read ahead of the barrier
@@ -1656,8 +1660,15 @@ __global__ void __launch_bounds__(kClThreads, 2)
   int pi = 0;
   while (pi + 1 < a.nprob && y >= a.cl_begin[pi + 1]) ++pi;
   const ClProb &p = a.p[pi];
-  const bool local = p.local != 0;
-  const int r = local ? (y - a.cl_begin[pi]) * kCl + (int)rank : y - a.cl_begin[pi];
+  const bool local = p.local == 1;
+  // two rows a cluster: CTAs 0-3 take one, 4-7 the other; every CTA still
+  // passes every cluster barrier, so the rows' barrier sequences are the same
+  const bool pairm = p.local == 2;
+  const uint32_t rsub = pairm ? (rank & 3u) : rank;  // CTA of the row
+  const uint32_t rbase = pairm ? (rank & 4u) : 0u;   // the row's first CTA
+  const int ncl = pairm ? kCl / 2 : kCl;             // CTAs of the row
+  const int r = local ? (y - a.cl_begin[pi]) * kCl + (int)rank
+                      : pairm ? (y - a.cl_begin[pi]) * 2 + (int)(rank >> 2) : y - a.cl_begin[pi];
   if (local && r >= p.R) return;  // a local CTA passes no cluster barrier
   const int k = p.k;
   const float *row = p.logits + (int64_t)r * p.stride;
@@ -1671,8 +1682,8 @@ __global__ void __launch_bounds__(kClThreads, 2)
   // this CTA's positions: [c0, c0 + chunk) of the row's stride, in groups of
   // 2048 (one float4 per thread); cut by the stride, so the copies can start
   // before the row's live length is read
-  const int64_t chunk = ((local ? p.stride : (p.stride + kCl - 1) / kCl) + 2047) / 2048 * 2048;
-  const int64_t c0 = local ? 0 : (int64_t)rank * chunk;
+  const int64_t chunk = ((local ? p.stride : (p.stride + ncl - 1) / ncl) + 2047) / 2048 * 2048;
+  const int64_t c0 = local ? 0 : (int64_t)rsub * chunk;
   const int vq = (int)(chunk / 2048);  // <= kClVec
   const int64_t b0 = c0 / 8;           // this CTA's first block
   // 16-byte aligned rows come into shared memory by bulk copies (the key
@@ -1741,7 +1752,9 @@ __global__ void __launch_bounds__(kClThreads, 2)
   const int64_t nbk = (n + 7) / 8;             // blocks of the row
   const bool btake = nbk <= bk;                // every block is taken
   const bool take_all = n <= k;
-  const bool early = hrow || take_all;  // T known without the row's own histogram
+  // T known without the row's own histogram (two rows a cluster: a row of k
+  // or fewer scores builds it too, so both rows pass the same barriers)
+  const bool early = hrow || (take_all && !pairm);
   float4 v[kClVec];
   if (!bulk) cl_issue_loads(row, c0, c1, vq, false, v);
 
@@ -1840,6 +1853,10 @@ __global__ void __launch_bounds__(kClThreads, 2)
     T = sm_misc[0];
     above = sm_misc[1];
     histT = sm_misc[2];
+    if (take_all) {  // every non-NaN score is taken: T past the last bin
+      T = DSA_NUM_BINS;
+      above = histT = 0;
+    }
     bin_key_range(T, loT, hiT);
     fine = (T < DSA_NUM_BINS) && histT > kClDirect;
     if (fine) fine_local();
@@ -1849,24 +1866,28 @@ __global__ void __launch_bounds__(kClThreads, 2)
   // added into CTA 0's merge buffer and read back from there
   int S = 0, above1 = 0, fineS = 0;
   uint32_t C = loT, E = hiT;
-  if (fine) {
+  if (fine || pairm) {  // two rows a cluster: both rows pass this barrier
     if (!local) {
       wait_pending();
-      const uint32_t fm0 = dsmem_map(smem_u32(&sm.fmerge[0]), 0);
-      for (int i = threadIdx.x; i < kClFine; i += kClThreads) {
-        const int c = fh[i];
-        if (c) dsmem_red_add(fm0 + 4u * (uint32_t)i, c);
-      }
+      const uint32_t fm0 = dsmem_map(smem_u32(&sm.fmerge[0]), rbase);
+      if (fine)
+        for (int i = threadIdx.x; i < kClFine; i += kClThreads) {
+          const int c = fh[i];
+          if (c) dsmem_red_add(fm0 + 4u * (uint32_t)i, c);
+        }
       cluster_sync();
-      for (int i = threadIdx.x; i < kClFine / 4; i += kClThreads)
-        reinterpret_cast<int4 *>(sm.hist)[i] = dsmem_ld4(fm0 + 16u * (uint32_t)i);
+      if (fine)
+        for (int i = threadIdx.x; i < kClFine / 4; i += kClThreads)
+          reinterpret_cast<int4 *>(sm.hist)[i] = dsmem_ld4(fm0 + 16u * (uint32_t)i);
       __syncthreads();
     }
-    threshold_from_hist<kClFine>(local ? fh : sm.hist, k - above, sm_scan, sm_misc + 8);
-    S = sm_misc[8];
-    above1 = sm_misc[9];
-    fineS = sm_misc[10];
-    fine_bin_keys(loT, hiT, flo, fshift, S, C, E);
+    if (fine) {
+      threshold_from_hist<kClFine>(local ? fh : sm.hist, k - above, sm_scan, sm_misc + 8);
+      S = sm_misc[8];
+      above1 = sm_misc[9];
+      fineS = sm_misc[10];
+      fine_bin_keys(loT, hiT, flo, fshift, S, C, E);
+    }
   }
 
   // ---- 4. classify, reserve output and candidate ranges (scores on CTA 0,
@@ -1904,23 +1925,27 @@ __global__ void __launch_bounds__(kClThreads, 2)
     const unsigned long long add = (unsigned long long)ie | ((unsigned long long)ic << 32);
     if (add) {
       const unsigned long long old =
-          local ? atomicAdd(&sm.ctr, add) : dsmem_atomic_add64(dsmem_map(smem_u32(&sm.ctr), 0), add);
+          local ? atomicAdd(&sm.ctr, add)
+                : dsmem_atomic_add64(dsmem_map(smem_u32(&sm.ctr), rbase), add);
       we = (int)(old & 0xFFFFFFFFull);
       wc = (int)(old >> 32);
     }
-    if (ib) wb = local ? atomicAdd(&sm.bctr, ib) : dsmem_atomic_add(dsmem_map(smem_u32(&sm.bctr), 1), ib);
+    if (ib)
+      wb = local ? atomicAdd(&sm.bctr, ib)
+                 : dsmem_atomic_add(dsmem_map(smem_u32(&sm.bctr), rbase + 1u), ib);
   }
   we = __shfl_sync(0xffffffffu, we, 31) + ie - ne;
   wc = __shfl_sync(0xffffffffu, wc, 31) + ic - nc;
   wb = __shfl_sync(0xffffffffu, wb, 31) + ib - nb;
-  const uint32_t cand0 = local ? 0u : dsmem_map(smem_u32(&sm.cand[0]), 0);
+  const uint32_t cand0 = local ? 0u : dsmem_map(smem_u32(&sm.cand[0]), rbase);
   if (kinds)
     cl_write(kinds, sm.keys, c0, we, wc, k, DSA_CAND_CAP, outr, !local, cand0, sm.cand, cr);
   int32_t *boutr = blk ? p.bout + (int64_t)r * bk : nullptr;
   if (bmask) {
-    const uint32_t bsel1 = local ? 0u : dsmem_map(smem_u32(&sm.bsel[0]), 1);
+    const uint32_t bsel1 = local ? 0u : dsmem_map(smem_u32(&sm.bsel[0]), rbase + 1u);
     // a sorted table written by the cluster: the candidates' histogram on CTA 1
-    const uint32_t bh1 = (p.bpt && !local && !btake) ? dsmem_map(smem_u32(&sm.fmerge[0]), 1) : 0u;
+    const uint32_t bh1 =
+        (p.bpt && !local && !btake) ? dsmem_map(smem_u32(&sm.fmerge[0]), rbase + 1u) : 0u;
     int pb = wb;
 #pragma unroll
     for (int e = 0; e < kClBPer; ++e) {
@@ -1948,7 +1973,7 @@ __global__ void __launch_bounds__(kClThreads, 2)
   // on the SMs the other CTAs leave; it waits for this grid before reading.
   pdl_release_dependents();
   unsigned long long *scratch = reinterpret_cast<unsigned long long *>(sm.keys);
-  if (local || rank == 0) {
+  if (local || rsub == 0) {
     const int emitted = (int)(sm.ctr & 0xFFFFFFFFull);
     const int ncand = (int)(sm.ctr >> 32);
     const int flag = cl_finish(row, n, k, outr, take_all, T, above, histT, fine, S, above1, fineS,
@@ -1967,8 +1992,10 @@ __global__ void __launch_bounds__(kClThreads, 2)
   // threshold item and every CTA's slice offset, then each CTA writes its
   // slice; in the general case (V = 0) CTA 1 selects and sorts alone
   const bool dtab = blk && p.bpt && !local;
-  if (dtab && cl_table_cluster(p, r, n, rank, E + 1u, sm, sm_h, sm_scan, sm_misc, sm_u64)) return;
-  if (blk && (local || rank == 1)) {
+  if (dtab && cl_table_cluster(p, r, n, rsub, rbase, ncl, (int)(chunk / 8), E + 1u, sm, sm_h,
+                               sm_scan, sm_misc, sm_u64))
+    return;
+  if (blk && (local || rsub == 1)) {
     __syncthreads();  // the local CTA: the score select's finish is done with the scratch
     cl_block_general(p, r, n, sm, sm_h, sm_scan, sm_misc);
   }
@@ -2279,6 +2306,21 @@ dsa_status_t run_cluster_select(const TopkCall *calls, int count, cudaStream_t s
   ca.ws_hist = reinterpret_cast<int32_t *>(ws + WsLayout::hist_off(wrows));
   ca.ws_fine = reinterpret_cast<int32_t *>(ws + WsLayout::fine_off(wrows));
   ca.status = reinterpret_cast<uint32_t *>(ws + WsLayout::kStatusOff);
+  // More row clusters than one wave of two CTAs an SM holds: rows of at most
+  // kClRow / 2 scores (an even count of them) go two to a cluster.
+  int64_t row_clusters = 0;
+  for (int i = 0; i < count; ++i)
+    if (calls[i].stride > kClChunk) row_clusters += calls[i].R;
+  static int sm_count = 0;
+  if (sm_count == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      sm_count = n;
+    else
+      sm_count = 152;
+  }
+  const bool pair_rows = row_clusters * kCl > 2 * (int64_t)sm_count;
   int64_t row0 = 0, clusters = 0;
   for (int i = 0; i < count; ++i) {
     const TopkCall &c = calls[i];
@@ -2298,7 +2340,8 @@ dsa_status_t run_cluster_select(const TopkCall *calls, int count, cudaStream_t s
     p.bflags = c.block_flags;
     p.bk = c.block_out ? c.block_k : 0;
     p.ws_row0 = (int)row0;
-    p.local = c.stride <= kClChunk ? 1 : 0;
+    p.local = c.stride <= kClChunk ? 1
+              : (pair_rows && c.stride <= kClRow / 2 && c.R % 2 == 0) ? 2 : 0;
     p.bpt = c.block_out ? c.block_pt : nullptr;
     p.bpt_stride = c.block_pt_stride;
     p.bps = c.block_ps;
@@ -2306,7 +2349,7 @@ dsa_status_t run_cluster_select(const TopkCall *calls, int count, cudaStream_t s
     p.bvalid = c.block_valid;
     p.vec = ((reinterpret_cast<uintptr_t>(c.logits) & 15) == 0 && c.stride % 4 == 0) ? 1 : 0;
     ca.cl_begin[i] = (int)clusters;
-    clusters += p.local ? (c.R + kCl - 1) / kCl : c.R;
+    clusters += p.local == 1 ? (c.R + kCl - 1) / kCl : p.local == 2 ? c.R / 2 : c.R;
     row0 += c.R;
   }
   ca.cl_begin[count] = (int)clusters;

@@ -271,3 +271,53 @@ def test_select_writes_sorted_block_table(B, nn, ctx, ps):
     np.testing.assert_array_equal(outs[1][0], t_ref)
     np.testing.assert_array_equal(outs[1][1], p_ref)
     np.testing.assert_array_equal(outs[1][2], v_ref)
+
+
+@pytest.mark.parametrize("R", [48, 47])
+@pytest.mark.parametrize("given_hist", [True, False])
+def test_two_rows_a_cluster(R, given_hist):
+    """More rows of at most 65536 scores than one wave of row clusters holds
+    (more than 38 on 152 SMs): an even count goes two rows to a cluster, four
+    CTAs each, an odd count one row a cluster.  The row mix puts the two rows
+    of a cluster on different paths: a row of k or fewer scores beside a full
+    one, an empty row, rows that end inside the first CTA's slice, rows whose
+    threshold bin needs the fine histogram.  Top-k sets, the sorted block
+    table, its physical blocks and live lengths against the oracle; the
+    workspace is left zeroed (a second run gives the same result)."""
+    import dsa_sparse_attention_paged_gb300 as D
+    rng = np.random.default_rng(900 + R + 2 * given_hist)
+    n, ps, kb = 65536, 64, 512
+    x = rng.normal(0, 2, (R, n)).astype(np.float32)
+    narrow = np.arange(1, R, 4)  # one coarse bin holds almost the whole row
+    x[narrow] = (1.0 + rng.uniform(0.0, 0.06, (len(narrow), n))).astype(np.float32)
+    lens = rng.integers(16385, n + 1, R)
+    lens[[0, 2, 3, 5, 6, 7, 9, 10]] = [n, 2048, 0, 100, 2049, 16000, n - 3, 4096]
+    lens[R - 1] = 12001
+    ctx = torch.from_numpy(lens.astype(np.int32)).cuda()
+    L = torch.from_numpy(x).cuda()
+    npg = n // ps
+    pt_h = np.stack([rng.permutation(2 * npg)[:npg] for _ in range(R)]).astype(np.int32)
+    ws = D.Workspace(R)
+    res = []
+    for _ in range(2):
+        table = torch.full((R, kb), -5, dtype=torch.int32, device="cuda")
+        phys = torch.full((R, kb), -5, dtype=torch.int32, device="cuda")
+        vlen = torch.full((R,), -5, dtype=torch.int32, device="cuda")
+        hist = torch.from_numpy(O.histogram(x, lens)).cuda() if given_hist else None
+        ((out, _),) = D.coarse_hist_topk_batch([
+            dict(logits=L, context_lens=ctx, next_n=1, k=2048, histogram=hist, block_k=kb,
+                 block_out=table, block_page_table=torch.from_numpy(pt_h).cuda(),
+                 block_page_size=ps, block_phys=phys, block_valid_lens=vlen)], ws)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
+        res.append([t.cpu().numpy() for t in (out, table, phys, vlen)])
+    rl = lens.astype(np.int64)
+    assert sets_equal(res[0][0], O.topk(x, rl, 2048))
+    A = O.block_amax8(x, rl, skip_le=kb, amax_stride=n // 8, fill=0.0)
+    t_ref, p_ref, v_ref = O.block_table(A, rl, np.arange(R, dtype=np.int32), kb, pt_h, ps)
+    np.testing.assert_array_equal(res[0][1], t_ref)
+    np.testing.assert_array_equal(res[0][2], p_ref)
+    np.testing.assert_array_equal(res[0][3], v_ref)
+    assert sets_equal(res[1][0], res[0][0])
+    for a, b in zip(res[0][1:], res[1][1:]):
+        np.testing.assert_array_equal(a, b)
