@@ -89,6 +89,9 @@ struct LogitsArgs {
   const int32_t *ulen;        // union entries per unit, or NULL (unpaired)
   int32_t upr;                // units per request: ceil(next_n / 2)
   int32_t tab_stride;         // entries per unit in `phys`: kb, or 2 kb paired
+  // unpaired, kb a multiple of 32, `phys` 16-byte aligned: the entries of
+  // flattened stage g are phys[32 g .. 32 g + 31], read by 16-byte loads
+  int32_t phys_vec;
   void *out;
   int64_t out_stride;
   int32_t *histogram;
@@ -142,6 +145,7 @@ __host__ __device__ inline SmemPlan smem_plan(int nn, bool hist, bool sparse, in
   off += (2 * stages + 2 * nks + 4 + 2 * nacc + 3 + (mx ? stages : 0)) * 8;
   p.misc = off;
   off += 64 + 2 * 32 * 4;  // flags/schedule + the producer's two row tables
+  off = (off + 15) & ~15;  // 16-byte stores into the sparse row table
   p.sptab = off;
   off += sparse ? kSpTab * 32 * 4 : 0;
   off = (off + 127) & ~127;
@@ -596,7 +600,21 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
           // iterator walks the next stages instead)
           const long long gbase = (long long)u_start * a.sparse_tpu + i_start + n;
           TileIter<SPARSE> wt = it;
-          for (int j0 = 0; j0 < kSpTab && n + j0 < count; j0 += 8) {
+          if (NN == 1 && a.phys_vec) {
+            // the next nst stages' entries are one contiguous run: eight
+            // 16-byte loads a stage, converted in place (the row table's
+            // layout, stage-major, is the run's own)
+            const int nq = 8 * (int)min((long long)kSpTab, count - n);
+            const int4 *src = reinterpret_cast<const int4 *>(a.phys + gbase * 32);
+            int4 *dst = reinterpret_cast<int4 *>(sp_tab);
+#pragma unroll 2
+            for (int q = lane; q < nq; q += 32) {
+              const int4 v = __ldg(src + q);
+              dst[q] = make_int4(phys_block_row(a, v.x), phys_block_row(a, v.y),
+                                 phys_block_row(a, v.z), phys_block_row(a, v.w));
+            }
+          }
+          for (int j0 = 0; !(NN == 1 && a.phys_vec) && j0 < kSpTab && n + j0 < count; j0 += 8) {
             int raw[8];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
@@ -868,7 +886,26 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
       rs.init(S);
       long long issued = 0;
       for (long long n = 0; n < count && ok; ++n, it.next(a), rs.next()) {
-        if (avail == 0) {
+        if (avail == 0 && NN == 1 && a.phys_vec) {
+          // one 16-byte load a lane: lane l holds blocks 16 + 4 (l % 4) ..
+          // + 3 of stage l / 4 of the next eight; each lane 16..31 takes its
+          // block of every stage from the lane holding it
+          const long long gbase = (long long)u_start * a.sparse_tpu + i_start + n;
+          int4 v = make_int4(INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX);
+          if (n + (lane >> 2) < count)
+            v = __ldg(reinterpret_cast<const int4 *>(a.phys + (gbase + (lane >> 2)) * 32 + 16) +
+                      (lane & 3));
+          const int src0 = (lane - 16) >> 2, e = lane & 3;
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int sl = (4 * jj + src0) & 31;
+            const int x = __shfl_sync(0xffffffffu, v.x, sl), y = __shfl_sync(0xffffffffu, v.y, sl);
+            const int z = __shfl_sync(0xffffffffu, v.z, sl), w = __shfl_sync(0xffffffffu, v.w, sl);
+            const int r = e == 0 ? x : e == 1 ? y : e == 2 ? z : w;
+            rq[jj] = phys_block_row(a, lane >= 16 ? r : INT32_MAX);
+          }
+          avail = 8;
+        } else if (avail == 0) {
           const long long gbase = (long long)u_start * a.sparse_tpu + i_start + n;
           TileIter<SPARSE> wt = it;
           int raw[8];
@@ -1268,6 +1305,7 @@ dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   a.phys = c.sparse ? c.phys : nullptr;
   a.valid_lens = c.sparse ? c.valid_lens : nullptr;
   a.tab_stride = c.kb;
+  a.phys_vec = 0;
   a.upr = 1;
   const bool paired = c.sparse && c.union_len != nullptr;
   if (paired) {
@@ -1301,6 +1339,7 @@ dsa_status_t run_paged_logits(const LogitsCall &c, cudaStream_t st) {
   if (c.sparse) {
     a.num_units = c.B * c.next_n;
     a.sparse_tpu = (c.kb + 31) / 32;
+    a.phys_vec = (a.phys && c.kb % 32 == 0 && (reinterpret_cast<uintptr_t>(a.phys) & 15) == 0) ? 1 : 0;
     const long long tiles = (long long)a.num_units * a.sparse_tpu;
     const int grid = (int)std::max<long long>(1, std::min<long long>(sms, tiles));
     if (c.out_fmt == DSA_OUT_F16) return launch_one<1, true, DSA_OUT_F16, false>(tk, tq, a, grid, st);
