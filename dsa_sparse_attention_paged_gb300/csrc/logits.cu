@@ -57,10 +57,11 @@ constexpr int kMaxStages = 8;
 // two groups of a sub-tile take alternate stages.  Eight warps consume each
 // stage either way.
 __host__ __device__ constexpr int epi_warps(int nn) { return nn == 1 ? 8 : 16; }
-// The sparse pass adds a second producer warp (after the epilogue warps), the
-// MXFP4 pass a scale-factor warp in the same place.
+// One more warp after the epilogue warps: a second producer (the sparse
+// pass; dense FP8 keys at next_n = 1) or, with MXFP4 keys, the scale-factor
+// warp.
 __host__ __device__ constexpr int threads_for(int nn, bool sparse, bool mx = false) {
-  return 64 + 32 * epi_warps(nn) + ((sparse || mx) ? 32 : 0);
+  return 64 + 32 * epi_warps(nn) + ((sparse || mx || nn == 1) ? 32 : 0);
 }
 constexpr int kStageEpiWarps = 8;
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in per CTA
@@ -519,8 +520,20 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
   }
   const WaitCtl ctl{abort_flag, a.status, a.wait_limit};
 
-  if (warp == 0) {
+  // FP8 dense keys at next_n = 1 in pages of 64 tokens (four page copies a
+  // stage): two producer warps take alternate stages, warp 0 also loading Q
+  // and the weights.  One warp issuing every stage's copies caps the gather
+  // below what the memory delivers (measured: two warps gather random 8 KiB
+  // pages about 8 % faster).  With pages of 128 tokens (two copies a stage)
+  // or next_n > 1 (the epilogue bounds the pass) one producer does it all.
+  constexpr bool kTwoProd = !SPARSE && !MX && NN == 1;
+  const int nprod = (kTwoProd && a.page_size == 64) ? 2 : 1;
+  if (warp == 0 || (kTwoProd && warp == 2 + EW)) {
     // ------------------------------------------------------------ producer
+    // (the second producer warp is idle when one producer does it all)
+    const int role = warp == 0 ? 0 : 1;
+    const bool idle = role == 1 && nprod == 1;
+    auto mine = [&](long long m) { return nprod == 1 || (int)(m & 1) == role; };
     // ppt load slots per stage (4 or 2 pages, or 32 blocks of 8 tokens), one
     // per lane; tpg = 32 / ppt stages per prefetch group.  Each lane reads its
     // slot's table entry one group ahead of use.
@@ -581,14 +594,14 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
     int nxt = sptab ? kNone : fetch(git, 0, nxt_unit);
     int cur_row = -1;
     int prev_u = -1, unit_ord = -1;
-    long long issued = 0;
+    long long n_done = 0;  // stages walked; this warp's among them were issued
     int q_issued = 0;
     bool ok = true;
     Ring rs, rk;
     rs.init(S);
     rk.init(KS);
     int o = 0;
-    for (long long n = 0; n < count && ok; ++n, it.next(a), rs.next(), rk.next(),
+    for (long long n = 0; n < count && ok && !idle; ++n, it.next(a), rs.next(), rk.next(),
                    o = (o + 1 == tpg) ? 0 : o + 1) {
       const int u = it.u;
       int row;
@@ -650,7 +663,7 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
         row = __shfl_sync(0xffffffffu, cur_row, (o * ppt + my_sl) & 31);
         if (lane >= ppt) row = -1;
       }
-      if (u != prev_u) {
+      if (role == 0 && u != prev_u) {
         ++unit_ord;
         prev_u = u;
         const int qb = unit_ord & 1;
@@ -674,6 +687,10 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
+      }
+      if (!mine(n)) {  // the other producer's stage
+        n_done = n + 1;
+        continue;
       }
       const int s = rs.idx;
       const int kx = rk.idx;
@@ -709,30 +726,18 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
         bulk_load(smem_u32(ks_s + kx * kStageTok + lane * blk_rows), a.kscale + (int64_t)row,
                   blk_rows * 4, KSF(kx));
       }
-      ++issued;
+      n_done = n + 1;
     }
     if (SPARSE) cp_async_wait_all();  // this warp's kscale copies land before it moves on
     if (!ok && lane == 0) {
       // drain our own TMA copies still in flight before the CTA exits (the
       // sparse pass's kscale cp.async copies were waited for above)
+      // (stage m sits in K slot m % S, phase (m / S) & 1; kscale likewise)
       const long long lim = a.wait_limit;
-      Ring ds = rs, dk = rk;
-      ds.idx = (int)(issued % S);
-      ds.ph = (uint32_t)((issued / S) & 1);
-      dk.idx = (int)(issued % KS);
-      dk.ph = (uint32_t)((issued / KS) & 1);
-      for (int back = 1; back <= S && back <= issued; ++back) {
-        int i2;
-        uint32_t p2;
-        ds.prev(back, i2, p2);
-        mbar_wait_drain(FULL(i2), p2, lim);
-      }
-      for (int back = 1; !SPARSE && back <= KS && back <= issued; ++back) {
-        int i2;
-        uint32_t p2;
-        dk.prev(back, i2, p2);
-        mbar_wait_drain(KSF(i2), p2, lim);
-      }
+      for (long long m = n_done > S ? n_done - S : 0; m < n_done; ++m)
+        if (mine(m)) mbar_wait_drain(FULL((int)(m % S)), (uint32_t)((m / S) & 1), lim);
+      for (long long m = n_done > KS ? n_done - KS : 0; !SPARSE && m < n_done; ++m)
+        if (mine(m)) mbar_wait_drain(KSF((int)(m % KS)), (uint32_t)((m / KS) & 1), lim);
       for (int k2 = (q_issued > 2 ? q_issued - 2 : 0); k2 < q_issued; ++k2)
         mbar_wait_drain(QFULL(k2 & 1), (uint32_t)((k2 >> 1) & 1), lim);
     }
