@@ -2148,6 +2148,15 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   const int w0 = threadIdx.x * wpt;
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
   for (int i = threadIdx.x; i < DSA_NUM_BINS; i += kSelThreads) h[i] = 0;
+  // this thread's positions [2 w0, 2 w0 + 2 wpt) are whole blocks of 8 (wpt a
+  // multiple of 4): their table entries, read once here instead of once per
+  // emitted position
+  int32_t tab[WPT / 4];
+#pragma unroll
+  for (int q = 0; q < WPT / 4; ++q) {
+    const int b = (2 * w0) / 8 + q;
+    tab[q] = (table && 4 * q < wpt && b < kb) ? __ldg(&table[(int64_t)r * kb + b]) : 0;
+  }
   uint32_t kv[WPT];  // order keys, two per word; 0 = no score
 #pragma unroll
   for (int q = 0; q < WPT / 4; ++q) {
@@ -2255,8 +2264,9 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   const int ex = block_excl_scan(nsel | (neq << 16), sm_scan, &tot);
   int ps = ex & 0xFFFF, pq = ex >> 16;
   int32_t *outr = out + (int64_t)r * k;
-  auto emit_col = [&](int p) -> int32_t {
-    return table ? (int32_t)(table[(int64_t)r * kb + p / 8] * 8 + (p & 7)) : (int32_t)p;
+  // position p = 2 (w0 + e) + hh lies in this thread's block e / 4
+  auto emit_col = [&](int e, int p) -> int32_t {
+    return table ? (int32_t)(tab[e / 4] * 8 + (p & 7)) : (int32_t)p;
   };
 #pragma unroll
   for (int e = 0; e < WPT; ++e) {
@@ -2266,10 +2276,10 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       if (!key) continue;
       const int pos = 2 * (w0 + e) + hh;
       if (take_all || key > thr) {
-        if (ps < k) outr[ps] = emit_col(pos);
+        if (ps < k) outr[ps] = emit_col(e, pos);
         ++ps;
       } else if (key == thr) {
-        if (pq < need) outr[above + pq] = emit_col(pos);
+        if (pq < need) outr[above + pq] = emit_col(e, pos);
         ++pq;
       }
     }
