@@ -50,6 +50,21 @@ class TopkProblem(ctypes.Structure):
 TOPK_BATCH_MAX = 4
 
 
+class DecodeStepArgs(ctypes.Structure):
+    """``dsa_decode_step_args``: the buffers and sizes of one decode step."""
+    _fields_ = [("q", ctypes.c_void_p), ("kv_pages", ctypes.c_void_p),
+                ("kscale", ctypes.c_void_p), ("weights", ctypes.c_void_p),
+                ("page_table", ctypes.c_void_p), ("page_table_stride", ctypes.c_int64),
+                ("context_lens", ctypes.c_void_p), ("B", ctypes.c_int32),
+                ("next_n", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("k", ctypes.c_int32), ("kb", ctypes.c_int32),
+                ("logits", ctypes.c_void_p), ("logits_stride", ctypes.c_int64),
+                ("histogram", ctypes.c_void_p), ("topk_idx", ctypes.c_void_p),
+                ("block_ids", ctypes.c_void_p), ("phys_blocks", ctypes.c_void_p),
+                ("valid_lens", ctypes.c_void_p), ("sparse_scores", ctypes.c_void_p),
+                ("sparse_idx", ctypes.c_void_p)]
+
+
 class DSAError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -99,6 +114,7 @@ def _load():
         "dsa_fp16_order_keys": (i32, [P, P, i64, P]),
         "dsa_bf16_order_keys": (i32, [P, P, i64, P]),
         "dsa_wait_timeout_selftest": (i32, [u64, P, sz, P]),
+        "dsa_decode_step": (i32, [ctypes.POINTER(DecodeStepArgs), P, sz, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -199,6 +215,52 @@ def paged_mqa_logits(q, kv_pages, kscale, weights, page_table, context_lens, nex
         _p(amax), amax.stride(0) if amax is not None else 0, int(amax_skip_if_blocks_le),
         ws.ptr, ws.nbytes, _stream(stream)), "paged_mqa_logits")
     return logits
+
+
+def decode_step_args(q, kv_pages, kscale, weights, page_table, context_lens, next_n, k, kb,
+                     logits, histogram, topk_idx, block_ids, phys_blocks, valid_lens,
+                     sparse_scores, sparse_idx) -> DecodeStepArgs:
+    """Checked argument block of ``decode_step`` (build it once and reuse it
+    while the tensors stay the same: it holds their addresses)."""
+    q, kv_pages = _u8(q), _u8(kv_pages)
+    for t, dt, nm in ((q, torch.uint8, "q"), (kv_pages, torch.uint8, "kv_pages"),
+                      (kscale, torch.float32, "kscale"), (weights, torch.float32, "weights"),
+                      (page_table, torch.int32, "page_table"),
+                      (context_lens, torch.int32, "context_lens"),
+                      (logits, torch.float32, "logits"), (histogram, torch.int32, "histogram"),
+                      (topk_idx, torch.int32, "topk_idx"), (block_ids, torch.int32, "block_ids"),
+                      (phys_blocks, torch.int32, "phys_blocks"),
+                      (valid_lens, torch.int32, "valid_lens"),
+                      (sparse_scores, torch.float16, "sparse_scores"),
+                      (sparse_idx, torch.int32, "sparse_idx")):
+        _req(t, dt, nm)
+    for t in (q, kv_pages, kscale, weights, page_table, context_lens, histogram, topk_idx,
+              block_ids, phys_blocks, valid_lens, sparse_scores, sparse_idx):
+        assert t.is_contiguous()
+    R, H, D = q.shape
+    P, ps, D2 = kv_pages.shape
+    B = context_lens.shape[0]
+    if R != B * next_n or D2 != D or H != 32 or D != 128:
+        raise ValueError("shape mismatch between q, kv_pages and context_lens")
+    if (tuple(histogram.shape) != (R, NUM_BINS) or tuple(topk_idx.shape) != (R, k)
+            or tuple(block_ids.shape) != (R, kb) or tuple(phys_blocks.shape) != (R, kb)
+            or tuple(valid_lens.shape) != (R,) or tuple(sparse_scores.shape) != (R, kb * 8)
+            or tuple(sparse_idx.shape) != (R, k) or logits.shape[0] != R):
+        raise ValueError("output shapes do not match B * next_n rows, k and kb")
+    return DecodeStepArgs(
+        q.data_ptr(), kv_pages.data_ptr(), kscale.data_ptr(), weights.data_ptr(),
+        page_table.data_ptr(), page_table.stride(0), context_lens.data_ptr(), B, next_n, ps, P,
+        k, kb, logits.data_ptr(), logits.stride(0), histogram.data_ptr(), topk_idx.data_ptr(),
+        block_ids.data_ptr(), phys_blocks.data_ptr(), valid_lens.data_ptr(),
+        sparse_scores.data_ptr(), sparse_idx.data_ptr())
+
+
+def decode_step(args: DecodeStepArgs, ws, stream=None):
+    """The whole two-level decode step in one library call (``dsa_decode_step``:
+    dense logits + histogram, select with the sorted block table, sparse FP16
+    logits, FP16 top-k), on the argument block from ``decode_step_args``."""
+    _check(lib.dsa_decode_step(ctypes.byref(args), ws.ptr, ws.nbytes, _stream(stream)),
+           "decode_step")
 
 
 def paged_mqa_logits_mx(q, k_codes, k_exp, weights, page_table, context_lens, next_n, ws,

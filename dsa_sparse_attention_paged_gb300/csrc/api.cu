@@ -647,6 +647,51 @@ int32_t dsa_bf16_order_keys(const uint16_t *in, uint16_t *out, int64_t n, void *
   return run_bf16_keys(in, out, n, static_cast<cudaStream_t>(stream));
 }
 
+int32_t dsa_decode_step(const dsa_decode_step_args *args, void *workspace, size_t ws_bytes,
+                        void *stream) {
+  if (!args) return DSA_ERR_INVALID_ARG;
+  const dsa_decode_step_args &a = *args;
+  if (a.B < 0 || a.next_n < 1 || a.kb < 1 || a.k < 1 || a.logits_stride < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (a.B == 0) return DSA_OK;
+  const int32_t R = a.B * a.next_n;
+  dsa_topk_problem p{};
+  p.logits = a.logits;
+  p.stride = a.logits_stride;
+  p.context_lens = a.context_lens;
+  p.histogram = a.histogram;
+  p.out_idx = a.topk_idx;
+  p.block_out_idx = a.block_ids;
+  p.next_n = a.next_n;
+  p.len_div = 1;
+  p.R = R;
+  p.reset_histogram = 1;
+  p.k = a.k;
+  p.block_k = a.kb;
+  p.block_page_table = a.page_table;
+  p.block_page_table_stride = a.page_table_stride;
+  p.block_page_size = a.page_size;
+  p.block_phys = a.phys_blocks;
+  p.block_valid_lens = a.valid_lens;
+  // rows a single cluster launch takes (the select writes the table itself)
+  if (dsa_coarse_hist_topk_batch_launches(&p, 1) != 1) return DSA_ERR_UNSUPPORTED;
+  int32_t e = dsa_paged_mqa_logits(a.q, a.kv_pages, a.kscale, a.weights, a.page_table,
+                                   a.page_table_stride, a.context_lens, a.B, a.next_n, 32, 128,
+                                   a.page_size, a.num_pages, a.logits, a.logits_stride,
+                                   a.histogram, nullptr, 0, a.kb, workspace, ws_bytes, stream);
+  if (e != DSA_OK) return e;
+  e = dsa_coarse_hist_topk_batch(&p, 1, workspace, ws_bytes, stream);
+  if (e != DSA_OK) return e;
+  e = dsa_sparse_mqa_logits(a.q, a.kv_pages, a.kscale, a.weights, a.page_table,
+                            a.page_table_stride, a.context_lens, a.B, a.next_n, 32, 128,
+                            a.page_size, a.num_pages, a.block_ids, a.kb, a.phys_blocks,
+                            a.valid_lens, a.sparse_scores, DSA_OUT_F16, (int64_t)a.kb * 8,
+                            workspace, ws_bytes, stream);
+  if (e != DSA_OK) return e;
+  return dsa_topk_fp16(a.sparse_scores, (int64_t)a.kb * 8, a.valid_lens, R, a.k, a.block_ids,
+                       a.kb, a.sparse_idx, workspace, ws_bytes, stream);
+}
+
 int32_t dsa_wait_timeout_selftest(uint64_t limit_cycles, void *workspace, size_t ws_bytes,
                                   void *stream) {
   if (!workspace || ws_bytes < WsLayout::kHeader) return DSA_ERR_WORKSPACE;

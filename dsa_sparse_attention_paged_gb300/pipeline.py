@@ -28,7 +28,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (OUT_F16, Workspace, coarse_hist_topk, coarse_hist_topk_batch,
+from . import (OUT_F16, Workspace, coarse_hist_topk, coarse_hist_topk_batch, decode_step,
+               decode_step_args,
                coarse_hist_topk_batch_launches, coarse_hist_topk_launches, paged_mqa_logits,
                pair_units, sort_candidate_blocks, sort_candidate_blocks_paired,
                sparse_mqa_logits, sparse_mqa_logits_paired, topk_fp16)
@@ -96,8 +97,22 @@ class DecodePlan:
 
     def step(self, q, kv, kscale, weights, page_table, context_lens, events=None):
         """Run one decode step.  ``events`` (optional dict name -> (start, end)
-        CUDA events) brackets individual launches for per-kernel timing."""
+        CUDA events) brackets individual launches for per-kernel timing.
+        Without events, the plan's usual shape (the table written by the select
+        launch) runs as one library call (``dsa_decode_step``) whose argument
+        block is built once per set of input tensors."""
         nn, ws = self.next_n, self.ws
+        if events is None and self.fused_table:
+            key = tuple((t.data_ptr(), tuple(t.shape), t.dtype)
+                        for t in (q, kv, kscale, weights, page_table, context_lens))
+            if getattr(self, "_step_key", None) != key:
+                self._step_args = decode_step_args(
+                    q, kv, kscale, weights, page_table, context_lens, nn, self.k, self.kb,
+                    self.logits, self.hist, self.topk_idx, self.block_ids, self.phys,
+                    self.valid_lens, self.sparse, self.sparse_idx)
+                self._step_key = key
+            decode_step(self._step_args, ws)
+            return self.topk_idx, self.sparse_idx
 
         def mark(name, i):
             if events is not None and name in events:

@@ -440,6 +440,58 @@ int32_t dsa_topk_bf16(const uint16_t *scores, int64_t stride, const int32_t *val
                       int32_t R, int32_t k, const int32_t *block_table, int32_t kb,
                       int32_t *out_idx, void *workspace, size_t ws_bytes, void *stream);
 
+/* ---- one whole decode step ------------------------------------------------
+ * The two-level step of [SG38944] "What this enables" / "Structure" with the
+ * fused histogram of [DG94] "What this adds", as one host call: the dense
+ * logits with the coarse histogram, then one select launch for the
+ * top-k of every row, its top-kb blocks and their sorted table with physical
+ * blocks and live lengths (the histogram cleared for the next step), the
+ * sparse logits over those blocks in FP16, and the FP16 top-k with the table
+ * transform -- exactly the calls dsa_paged_mqa_logits,
+ * dsa_coarse_hist_topk_batch (block_k = kb, block_page_table given),
+ * dsa_sparse_mqa_logits (DSA_OUT_F16) and dsa_topk_fp16 make, each with its
+ * own argument checks, on one stream.  It spares a caller that launches
+ * eagerly the per-call overhead of four bindings; the results are bitwise
+ * those of the four calls.
+ *   logits        [R][logits_stride] float, R = B * next_n; logits_stride at
+ *                 most 131072 (longer rows: DSA_ERR_UNSUPPORTED -- make the
+ *                 separate calls, whose select takes them in several launches)
+ *   histogram     [R][1024] int32, zero on entry, cleared again by the select
+ *   topk_idx      [R][k] top-k columns of the dense logits
+ *   block_ids     [R][kb] the sorted block table; phys_blocks [R][kb];
+ *                 valid_lens [R]
+ *   sparse_scores [R][kb * 8] FP16 bits; sparse_idx [R][k] the top-k of the
+ *                 sparse scores as logical columns
+ * All buffers are the caller's; the workspace is sized for R rows.  Returns
+ * the first failing call's status (the launches before it are queued). */
+typedef struct dsa_decode_step_args {
+  const uint8_t *q;
+  const uint8_t *kv_pages;
+  const float *kscale;
+  const float *weights;
+  const int32_t *page_table;
+  int64_t page_table_stride;
+  const int32_t *context_lens;
+  int32_t B;
+  int32_t next_n;
+  int32_t page_size;
+  int32_t num_pages;
+  int32_t k;
+  int32_t kb;
+  float *logits;
+  int64_t logits_stride;
+  int32_t *histogram;
+  int32_t *topk_idx;
+  int32_t *block_ids;
+  int32_t *phys_blocks;
+  int32_t *valid_lens;
+  uint16_t *sparse_scores;
+  int32_t *sparse_idx;
+} dsa_decode_step_args;
+
+int32_t dsa_decode_step(const dsa_decode_step_args *args, void *workspace, size_t ws_bytes,
+                        void *stream);
+
 /* ---- diagnostics (same device functions as the kernels above) ------------
  * dsa_coarse_bins_range: out[i] = coarse bin of the float whose bit pattern is
  *   start + i (-1 for NaN), for i < count; out is int16 on the device.  Used

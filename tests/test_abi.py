@@ -213,3 +213,26 @@ def test_paired_sort_and_sparse_argument_checks(lib):
     assert sp(kb=40) == 2
     assert sp(ostride=100) == 1
     assert sp(nn=5) == 2
+
+
+def test_decode_step_rejects_before_launching(lib):
+    """One-call decode step: a missing argument block, bad sizes and rows
+    longer than one cluster launch takes are refused on the host, before any
+    launch (the pointers are never dereferenced)."""
+    import dsa_sparse_attention_paged_gb300 as D
+    ws = ctypes.c_void_p(0x20000)
+    assert lib.dsa_decode_step(None, ws, 4096, None) == 1
+
+    def args(**kw):
+        a = dict(q=0x10000, kv_pages=0x10000, kscale=0x10000, weights=0x10000,
+                 page_table=0x10000, page_table_stride=4, context_lens=0x10000, B=2, next_n=1,
+                 page_size=64, num_pages=10, k=2048, kb=512, logits=0x10000,
+                 logits_stride=131072, histogram=0x10000, topk_idx=0x10000, block_ids=0x10000,
+                 phys_blocks=0x10000, valid_lens=0x10000, sparse_scores=0x10000,
+                 sparse_idx=0x10000)
+        a.update(kw)
+        return D.DecodeStepArgs(**a)
+    assert lib.dsa_decode_step(ctypes.byref(args(kb=0)), ws, 4096, None) == 1
+    assert lib.dsa_decode_step(ctypes.byref(args(next_n=0)), ws, 4096, None) == 1
+    assert lib.dsa_decode_step(ctypes.byref(args(logits_stride=131080)), ws, 4096, None) == 2
+    assert lib.dsa_decode_step(ctypes.byref(args(B=0)), ws, 4096, None) == 0

@@ -94,3 +94,43 @@ def test_host_pipeline_matches_eager_steps():
         hout = slots[i % 2][1]
         assert sets_equal(hout[0].numpy(), e_dense)
         assert sets_equal(hout[1].numpy(), e_sparse)
+
+
+@pytest.mark.parametrize("B,nn,L,ps,kb", [(4, 1, 40000, 64, 512), (3, 2, 20001, 128, 256)])
+def test_one_call_step_equals_separate_calls(B, nn, L, ps, kb):
+    """``dsa_decode_step`` (one library call for the whole step) writes what
+    the four separate calls write: bit for bit the logits, the cleared
+    histogram, the sorted table, physical blocks, live lengths and the FP16
+    sparse scores, and the same two index sets (in any order); a second step
+    on lengths rewritten in place reuses the argument block and follows them."""
+    from dsa_sparse_attention_paged_gb300.pipeline import DecodePlan
+    case = S.generate(S.Workload("one call", B, nn, [L] * B, ps, "mixed", 777 + B))
+    d = to_dev(case)
+    lens2 = torch.tensor([max(1, L - 997 * (i + 1)) for i in range(B)], dtype=torch.int32,
+                         device="cuda")
+    plans = [DecodePlan(B, nn, L, ps, k=2048, kb=kb) for _ in range(2)]
+    assert plans[0].fused_table
+    ctx = d["context_lens"].clone()
+    for it in range(2):
+        if it == 1:
+            ctx.copy_(lens2)  # rewritten in place: the same argument block
+        inp = (d["q"], d["kv"], d["kscale"], d["weights"], d["page_table"], ctx)
+        outs = []
+        for i, plan in enumerate(plans):
+            plan.logits.fill_(float("nan"))
+            plan.step(*inp, events=None if i == 0 else {})  # events: the separate calls
+            torch.cuda.synchronize()
+            assert plan.ws.status() == 0
+            outs.append([t.cpu() for t in (plan.logits, plan.hist, plan.topk_idx, plan.block_ids,
+                                           plan.phys, plan.valid_lens, plan.sparse,
+                                           plan.sparse_idx)])
+        bits = {torch.float32: torch.int32, torch.float16: torch.int16}
+        for i, (a, b) in enumerate(zip(*outs)):
+            if i in (2, 7):  # index sets: their order is unspecified
+                assert sets_equal(a.numpy(), b.numpy())
+            else:
+                assert torch.equal(a.view(bits.get(a.dtype, a.dtype)),
+                                   b.view(bits.get(b.dtype, b.dtype)))
+        rl = O.row_lens(ctx.cpu().numpy(), nn)
+        L_np = outs[0][0].numpy()
+        assert sets_equal(outs[0][2].numpy(), O.topk(L_np, rl, 2048))
