@@ -729,6 +729,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelArgs a) {
 // CTA 1.
 // Short rows (stride <= kClChunk): each CTA of a cluster takes one row alone
 // (the same steps inside one CTA, no cluster barrier), eight rows a cluster.
+// Rows of at most kClRow / 2 scores, when one row a cluster would need more
+// clusters than one wave holds: two rows a cluster, four CTAs each (each half
+// has its own CTA 0 and CTA 1; both halves pass every cluster barrier).
 // Every cluster-wide decision is taken from data all CTAs share, so all CTAs
 // pass the same cluster barriers.  The workspace histograms are zero on entry
 // and are cleared again by CTA 0 after the last barrier.
