@@ -89,10 +89,15 @@ def peaks():
 def traffic_record(kernel_src):
     """Per-launch DRAM bytes of the logits kernel from the committed ncu record
     (profiles/logits_fused_hist_c2.json), valid only while the kernel source
-    is unchanged (its sha256 is stored beside the number); None otherwise."""
+    (the kernel file and the device header it includes) is unchanged: the
+    sha256 of the two, in that order, is stored beside the number; None
+    otherwise."""
     path = os.path.join(ROOT, "profiles", "logits_fused_hist_c2.json")
     try:
-        sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+        h = hashlib.sha256()
+        for src in (kernel_src, os.path.join(os.path.dirname(kernel_src), "dsa_device.cuh")):
+            h.update(open(src, "rb").read())
+        sha = h.hexdigest()
         with open(path) as f:
             rec = json.load(f)
         if rec.get("source_sha256") == sha:

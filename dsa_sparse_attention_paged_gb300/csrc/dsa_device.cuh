@@ -436,17 +436,16 @@ __device__ __forceinline__ void tmem_ld_wait() {
 // 304 + floor(|x|) - 16; |x| < 16 -> FP16-RN(|x|) >> 6.  bin = 511 - m for a
 // clear sign bit, 512 + m otherwise; -1 for NaN.
 __device__ __forceinline__ int coarse_bin(float x) {
-  if (isnan(x)) return -1;
   const float a = fabsf(x);
-  int m;
-  if (a >= 223.0f) {
-    m = 511;
-  } else if (a >= 16.0f) {
-    m = 288 + static_cast<int>(a);  // 304 + floor(a) - 16; a > 0 so truncation is floor
-  } else {
-    m = static_cast<int>(__half_as_ushort(__float2half_rn(a)) >> 6);
-  }
-  return (__float_as_uint(x) >> 31) ? 512 + m : 511 - m;
+  int m = static_cast<int>(__half_as_ushort(__float2half_rn(a)) >> 6);  // |x| < 16
+  // 16 <= |x| < 223: floor(a) as the low bits of a + 2^23 rounded down (an
+  // add instead of a float-to-int conversion; exact below 2^23)
+  const int mu = __float_as_int(__fadd_rd(a, 8388608.0f)) - (0x4B000000 - 288);
+  m = a >= 16.0f ? mu : m;
+  m = a >= 223.0f ? 511 : m;
+  // 511 - m for a clear sign bit, 512 + m for a set one: m ^ 511 or m ^ 512 (m < 512)
+  const int bin = m ^ (511 + static_cast<int>(__float_as_uint(x) >> 31));
+  return isnan(x) ? -1 : bin;
 }
 
 // Ascending order key of an FP32 value: unsigned compare == value compare,
