@@ -992,6 +992,12 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
     int prev_u = -1, unit_ord = -1, qb = 0;
     uint32_t gsync_ph = 0;
     int64_t ctx_b = 0, n_row = 0;
+    // dense: the current request's rows (their first logit) and, per row, the
+    // positions stored: below min(live length, row stride), set per request
+    float *orow = nullptr;
+    uint32_t lim[NN];
+#pragma unroll
+    for (int j = 0; j < NN; ++j) lim[j] = 0;
     int row_base = 0;
     bool ok = true;
     // paired unit: its rows, their live lengths and the union length
@@ -1088,6 +1094,14 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
         } else {
           ctx_b = eff_ctx(a, u);
           row_base = u * NN;
+          orow = reinterpret_cast<float *>(a.out) + (int64_t)row_base * a.out_stride;
+#pragma unroll
+          for (int j = 0; j < NN; ++j) {
+            const int64_t n_rj = ctx_b - (NN - 1 - j);
+            lim[j] = (uint32_t)max((int64_t)0, min(n_rj, a.out_stride));
+          }
+          // a live position past the row stride is flagged, not stored
+          if (lane == 0 && ctx_b > a.out_stride) set_status(a.status, DSA_DEV_BOUNDS);
         }
         if (!(ok = ewait(QFULL(qb), (unit_ord >> 1) & 1))) break;
       }
@@ -1181,17 +1195,13 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
           sp_store(u, pos, live ? acc[0] : -INFINITY);
         }
       } else {
-        const int64_t t = pos;
-        if (t == a.out_stride && ctx_b > a.out_stride) set_status(a.status, DSA_DEV_BOUNDS);
-        float *const op = reinterpret_cast<float *>(a.out) + (int64_t)row_base * a.out_stride + t;
-        const bool in_stride = t < a.out_stride;
+        const uint32_t t32 = (uint32_t)i * kStageTok + (uint32_t)tok;  // position in the row
 #pragma unroll
         for (int j = 0; j < NN; ++j) {
-          const int64_t n_rj = ctx_b - (NN - 1 - j);
-          if (in_stride && t < n_rj) {
+          if (t32 < lim[j]) {
             // kept in L2 for the select that reads the row next (the K stream
             // around it is marked evict-first)
-            st_f32_hint(op + j * a.out_stride, acc[j], out_pol);
+            st_f32_hint(orow + j * a.out_stride + t32, acc[j], out_pol);
             if (HIST) {
               const int bin = coarse_bin(acc[j]);
               if (bin >= 0) atomicAdd(&my_hist[j * kHistWords + (bin >> 1)], 1u << (16 * (bin & 1)));
@@ -1201,6 +1211,8 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
             // block maximum of 8 consecutive scores (8 consecutive lanes), in
             // the value order of the select (-0 below +0, NaN ignored); the
             // newest block is +inf, nothing is written past the block count
+            const int64_t t = pos;
+            const int64_t n_rj = ctx_b - (NN - 1 - j);
             const int64_t nb = n_rj > 0 ? (n_rj + 7) >> 3 : 0;
             uint32_t key = (t < n_rj && !isnan(acc[j])) ? f32_order_key(acc[j]) : 0u;
             key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
