@@ -326,17 +326,17 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
 // as (c0 + c1) + (c2 + c3).  For a finite kscale s >= 0, ReLU(d * s) = s *
 // ReLU(d), so s is applied once to the sum; any other s takes the formula
 // term by term.  Dense and sparse logits share this function, so they are
-// bitwise equal.
-__device__ __forceinline__ float head_sum(const uint32_t (&v)[32], float ks, const float *w) {
+// bitwise equal.  The head weights come in registers (the row's 32, read
+// once per request).
+__device__ __forceinline__ float head_sum(const uint32_t (&v)[32], float ks, const float (&w)[32]) {
   uint64_t a01 = pk2(0.0f, 0.0f), a23 = pk2(0.0f, 0.0f);
   if (ks >= 0.0f && ks <= 3.4028234e38f) {
 #pragma unroll
     for (int h = 0; h < 32; h += 4) {
-      const float4 wv = *reinterpret_cast<const float4 *>(w + h);
-      a01 = fma2(pk2(wv.x, wv.y),
+      a01 = fma2(pk2(w[h + 0], w[h + 1]),
                  pk2(fmaxf(__uint_as_float(v[h + 0]), 0.0f), fmaxf(__uint_as_float(v[h + 1]), 0.0f)),
                  a01);
-      a23 = fma2(pk2(wv.z, wv.w),
+      a23 = fma2(pk2(w[h + 2], w[h + 3]),
                  pk2(fmaxf(__uint_as_float(v[h + 2]), 0.0f), fmaxf(__uint_as_float(v[h + 3]), 0.0f)),
                  a23);
     }
@@ -348,12 +348,11 @@ __device__ __forceinline__ float head_sum(const uint32_t (&v)[32], float ks, con
   const uint64_t ks2 = pk2(ks, ks);
 #pragma unroll
   for (int h = 0; h < 32; h += 4) {
-    const float4 wv = *reinterpret_cast<const float4 *>(w + h);
     float p0, p1, p2, p3;
     upk2(mul2(pk2(__uint_as_float(v[h + 0]), __uint_as_float(v[h + 1])), ks2), p0, p1);
     upk2(mul2(pk2(__uint_as_float(v[h + 2]), __uint_as_float(v[h + 3])), ks2), p2, p3);
-    a01 = fma2(pk2(wv.x, wv.y), pk2(fmaxf(p0, 0.0f), fmaxf(p1, 0.0f)), a01);
-    a23 = fma2(pk2(wv.z, wv.w), pk2(fmaxf(p2, 0.0f), fmaxf(p3, 0.0f)), a23);
+    a01 = fma2(pk2(w[h + 0], w[h + 1]), pk2(fmaxf(p0, 0.0f), fmaxf(p1, 0.0f)), a01);
+    a23 = fma2(pk2(w[h + 2], w[h + 3]), pk2(fmaxf(p2, 0.0f), fmaxf(p3, 0.0f)), a23);
   }
   float c0, c1, c2, c3;
   upk2(a01, c0, c1);
@@ -995,6 +994,7 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
     // dense: the current request's rows (their first logit) and, per row, the
     // positions stored: below min(live length, row stride), set per request
     float *orow = nullptr;
+    float wr[32];  // next_n = 1: the current row's head weights
     uint32_t lim[NN];
 #pragma unroll
     for (int j = 0; j < NN; ++j) lim[j] = 0;
@@ -1104,6 +1104,16 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
           if (lane == 0 && ctx_b > a.out_stride) set_status(a.status, DSA_DEV_BOUNDS);
         }
         if (!(ok = ewait(QFULL(qb), (unit_ord >> 1) & 1))) break;
+        if constexpr (EW == 8) {  // next_n = 1: the row's head weights into registers
+#pragma unroll
+          for (int h = 0; h < 32; h += 4) {
+            const float4 wv = *reinterpret_cast<const float4 *>(w_s + qb * N + h);
+            wr[h + 0] = wv.x;
+            wr[h + 1] = wv.y;
+            wr[h + 2] = wv.z;
+            wr[h + 3] = wv.w;
+          }
+        }
       }
       const bool mine = NPAR == 1 || ((int)(n & 1) == par);
       if (mine) {
@@ -1181,7 +1191,7 @@ __global__ void __launch_bounds__(threads_for(NN, SPARSE, MX), 1)
         }
 #pragma unroll
         for (int jj = 0; jj < kB; ++jj)
-          if (j0 + jj < NN) acc[j0 + jj] = head_sum(v[jj], ks, w_s + qb * N + (j0 + jj) * 32);
+          if (j0 + jj < NN) acc[j0 + jj] = head_sum(v[jj], ks, wr);
       }
       }
 
