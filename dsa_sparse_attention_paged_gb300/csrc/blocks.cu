@@ -171,18 +171,21 @@ __global__ void __launch_bounds__(kSortThreads)
       const int bit = __ffs(m) - 1;
       m &= m - 1;
       const int64_t id = (int64_t)w * 32 + bit;
-      if (pos < kb) {
-        idr[pos] = (int32_t)id;
-        if (phys) phys[(int64_t)r * kb + pos] = phys_of(id);
-      }
+      if (pos < kb) idr[pos] = (int32_t)id;
       ++pos;
       const int64_t in_blk = n - id * 8;
       live += in_blk < 8 ? in_blk : 8;
     }
   }
-  for (int i = total + threadIdx.x; i < kb; i += kSortThreads) {
-    idr[i] = INT32_MAX;
-    if (phys) phys[(int64_t)r * kb + i] = INT32_MAX;
+  for (int i = total + threadIdx.x; i < kb; i += kSortThreads) idr[i] = INT32_MAX;
+  if (phys) {
+    // the physical blocks one table slot a thread, from the sorted ids just
+    // written (visible to the whole block after the barrier), so no
+    // page-table read sits in the serial bitmap walk above
+    __syncthreads();
+    const int nt = min(total, kb);
+    for (int i = threadIdx.x; i < kb; i += kSortThreads)
+      phys[(int64_t)r * kb + i] = i < nt ? phys_of(idr[i]) : INT32_MAX;
   }
   if (valid_lens) {
     long long v = live;
@@ -296,12 +299,10 @@ __global__ void __launch_bounds__(kSortThreads)
       const int bit = __ffs(mk) - 1;
       mk &= mk - 1;
       const int64_t id = (int64_t)w * 32 + bit;
-      const int32_t ph = phys_of(id);
       uint32_t word = 0;
       if ((a >> bit) & 1u) {
         if (pa < kb) {
           ida[pa] = (int32_t)id;
-          if (pha) pha[pa] = ph;
           word |= (uint32_t)(pa + 1);
         }
         ++pa;
@@ -311,7 +312,6 @@ __global__ void __launch_bounds__(kSortThreads)
       if ((c >> bit) & 1u) {
         if (pb < kb) {
           idb[pb] = (int32_t)id;
-          if (phb) phb[pb] = ph;
           word |= (uint32_t)(pb + 1) << 16;
         }
         ++pb;
@@ -319,11 +319,23 @@ __global__ void __launch_bounds__(kSortThreads)
         live[1] += in_blk < 8 ? in_blk : 8;
       }
       if (pu < 2 * kb) {
-        up[pu] = ph;
+        up[pu] = (int32_t)id;  // the block id for now: its physical block below
         uq[pu] = (int32_t)word;
       }
       ++pu;
     }
+  }
+  // the physical blocks one union slot a thread (visible to the whole block
+  // after the barrier), so no page-table read sits in the serial walk above:
+  // the union's own entry, and through its positions each row's
+  __syncthreads();
+  const int nu = min(tot_u, 2 * kb);
+  for (int i = threadIdx.x; i < nu; i += kSortThreads) {
+    const int32_t ph = phys_of(up[i]);
+    up[i] = ph;
+    const uint32_t word = (uint32_t)uq[i];
+    if (pha && (word & 0xFFFFu)) pha[(word & 0xFFFFu) - 1] = ph;
+    if (phb && (word >> 16)) phb[(word >> 16) - 1] = ph;
   }
   for (int j = 0; j < nrow; ++j) {
     int32_t *idr = j == 0 ? ida : idb;

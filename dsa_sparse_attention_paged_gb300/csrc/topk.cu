@@ -742,7 +742,8 @@ constexpr int kClVec = kClVpt / 4;               // float4 groups per thread
 constexpr int kClChunk = kClThreads * kClVpt;    // 16384 per CTA
 constexpr int kClRow = kCl * kClChunk;           // 131072
 constexpr int kClDirect = kClThreads;            // candidates kept in shared memory
-constexpr int kClRank = 64;                      // candidates ranked pairwise
+constexpr int kClRank = 64;                      // items of a histogram level's bin ranked pairwise
+constexpr int kClRankDirect = 256;               // score candidates ranked pairwise before any level
 constexpr int kClMaxProb = 4;                    // problems per launch
 constexpr int kClFine = 1024;                    // fine bins
 constexpr uint32_t kFineWindow = 1u << 26;       // keys one fine histogram spans at most
@@ -1002,6 +1003,14 @@ __device__ __forceinline__ void cl_write(unsigned long long kinds, const uint4 *
   }
 }
 
+// Rank of v among the n unique items a[0..n): the number of larger items
+// (every thread of a rank pass reads the same items: broadcast loads).
+__device__ __forceinline__ int rank_of(const unsigned long long *a, int n, unsigned long long v) {
+  int rk = 0;
+  for (int j = 0; j < n; ++j) rk += a[j] > v;
+  return rk;
+}
+
 // Exact top-m of the n unique items it[0..n) (order key << 32 | ~id, so
 // equal keys rank by lower id), written as ids to out[0..m) in any order;
 // every item's key lies in [lo, hi] and n >= m.  Level by level a 1024-bin
@@ -1072,8 +1081,7 @@ __device__ __noinline__ void local_hist_select(const unsigned long long *it, int
       // unique keys: each item's rank is the number of larger items
       for (int i = threadIdx.x; i < inbin; i += kClThreads) {
         const unsigned long long v = dst[i];
-        int rk = 0;
-        for (int j = 0; j < inbin; ++j) rk += dst[j] > v;
+        const int rk = rank_of(dst, inbin, v);
         if (rk < need) out[base + rk] = (int32_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
       }
       __syncthreads();
@@ -1134,8 +1142,7 @@ __device__ __noinline__ unsigned long long local_hist_kth(const unsigned long lo
       // unique items: the one with exactly need - 1 larger items in the bin
       for (int i = threadIdx.x; i < inbin; i += kClThreads) {
         const unsigned long long v = dst[i];
-        int rk = 0;
-        for (int j = 0; j < inbin; ++j) rk += dst[j] > v;
+        const int rk = rank_of(dst, inbin, v);
         if (rk == need - 1) *sm_res = v;
       }
       __syncthreads();
@@ -1184,13 +1191,14 @@ __device__ __noinline__ int cl_finish(const float *row, int64_t n, int k, int32_
   if (flag == 0) {
     if (m <= 0) {
       for (int i = emitted + threadIdx.x; i < k; i += kClThreads) outr[i] = -1;
-    } else if (ncand <= kClRank) {
+    } else if (ncand <= kClRankDirect) {
       // candidate keys are unique (the column is part of the key): each
-      // thread ranks one against all the others (quadratic: few candidates)
+      // thread ranks one against all the others (quadratic, but one pass:
+      // cheaper than the two or three histogram levels that several hundred
+      // candidates would take from scratch)
       if (threadIdx.x < ncand) {
         const unsigned long long v = cand[threadIdx.x];
-        int rk = 0;
-        for (int j = 0; j < ncand; ++j) rk += cand[j] > v;
+        const int rk = rank_of(cand, ncand, v);
         if (rk < m) outr[base_out + rk] = (int32_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
       }
     } else if (ncand <= kClDirect) {
@@ -1228,8 +1236,11 @@ __device__ __forceinline__ uint32_t max_key8(float4 a, float4 b) {
 // sort over a bitmap of the row's nbk blocks ([SG38944]
 // sort_candidate_blocks).  A row of at most bk blocks takes the identity
 // table 0 .. nbk-1, whatever was selected.  Every thread calls it; bm holds
-// nbk bits.
-__device__ __noinline__ void cl_sort_table(const int32_t *ids, int32_t *out, int bk, int64_t n,
+// nbk bits.  `ids` is shared memory: once the bitmap holds them it takes the
+// sorted ids, whose physical blocks are then looked up one a thread (the
+// bitmap walk itself is serial within a thread's words, so no page-table
+// read sits in it).
+__device__ __noinline__ void cl_sort_table(int32_t *ids, int32_t *out, int bk, int64_t n,
                                            int64_t nbk,
                                            const int32_t *pt_row, int ps, int32_t *phys,
                                            int32_t *valid, uint32_t *bm, int *sm_scan,
@@ -1264,7 +1275,7 @@ __device__ __noinline__ void cl_sort_table(const int32_t *ids, int32_t *out, int
   int c = 0;
   for (int w = w0; w < w1; ++w) c += __popc(bm[w]);
   int total;
-  int pos = block_excl_scan(c, sm_scan, &total);
+  int pos = block_excl_scan(c, sm_scan, &total);  // its barriers order the reads of ids above
   long long live = 0;
   for (int w = w0; w < w1; ++w) {
     uint32_t m = bm[w];
@@ -1274,17 +1285,19 @@ __device__ __noinline__ void cl_sort_table(const int32_t *ids, int32_t *out, int
       const int64_t id = (int64_t)w * 32 + bit;
       if (pos < bk) {
         out[pos] = (int32_t)id;
-        if (phys) phys[pos] = phys_of(id);
+        ids[pos] = (int32_t)id;
       }
       ++pos;
       const int64_t in_blk = n - id * 8;
       live += in_blk < 8 ? in_blk : 8;
     }
   }
-  for (int i = total + threadIdx.x; i < bk; i += kClThreads) {
-    out[i] = INT32_MAX;
-    if (phys) phys[i] = INT32_MAX;
+  if (phys) {
+    __syncthreads();  // the sorted ids are in place
+    const int nt = min(total, bk);
+    for (int i = threadIdx.x; i < bk; i += kClThreads) phys[i] = i < nt ? phys_of(ids[i]) : INT32_MAX;
   }
+  for (int i = total + threadIdx.x; i < bk; i += kClThreads) out[i] = INT32_MAX;
   if (valid) {
     live = __reduce_add_sync(0xffffffffu, (unsigned)live);
     if ((threadIdx.x & 31) == 0) sm_live[threadIdx.x >> 5] = live;
@@ -1456,8 +1469,7 @@ __device__ __forceinline__ void cl_block_publish(int64_t n, int bk, bool btake, 
       if (ni <= kClRank) {
         if ((int)threadIdx.x < ni) {
           const unsigned long long v = buf[threadIdx.x];
-          int rk = 0;
-          for (int j = 0; j < ni; ++j) rk += buf[j] > v;
+          const int rk = rank_of(buf, ni, v);
           if (rk < need) {
             const int64_t b = (int64_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
             atomicAdd(&sm_h[wgroup(b)], 1);
