@@ -106,6 +106,45 @@ def test_threshold_bin_over_capacity_falls_back_to_exact():
     assert (flags.cpu().numpy() == 2).all()
 
 
+@pytest.mark.parametrize("n", [8192, 40000])
+@pytest.mark.parametrize("c", [64, 65, 256, 257, 512])
+def test_threshold_bin_sizes_around_the_rank_limits(n, c):
+    """The threshold bin holds exactly c scores, of which the top 10 are taken
+    (2038 scores lie in higher bins): up to 256 candidates are ranked in one
+    pairwise pass, more by 1024-bin levels; rows of 8192 take the one-CTA
+    select, rows of 40000 the cluster.  Row 0's candidates are distinct, row
+    1's all equal (ties -> lower column)."""
+    import dsa_sparse_attention_paged_gb300 as D
+    k, above = 2048, 2038
+    R = 2
+    rng = np.random.default_rng(1000 + c + n)
+    x = rng.uniform(-50.0, -10.0, (R, n)).astype(np.float32)
+    cand_pos = []
+    for r in range(R):
+        pos = rng.permutation(n)
+        x[r, pos[:above]] = rng.uniform(50.0, 100.0, above).astype(np.float32)
+        cv = rng.uniform(1.001, 1.06, c) if r == 0 else np.full(c, 1.03125)
+        x[r, pos[above:above + c]] = cv.astype(np.float32)
+        cand_pos.append(pos[above:above + c])
+    # the construction: the c candidates share one bin, and it is the bin the
+    # 2048th score falls in
+    for r in range(R):
+        b = O.coarse_bins(x[r, cand_pos[r]])
+        assert (b == b[0]).all()
+        assert (O.coarse_bins(x[r]) == b[0]).sum() == c
+    lens = np.full(R, n)
+    hist = torch.from_numpy(O.histogram(x, lens)).cuda()
+    L = torch.from_numpy(x).cuda()
+    ctx = torch.full((R,), n, dtype=torch.int32, device="cuda")
+    ws = D.Workspace(R)
+    flags = torch.full((R,), 9, dtype=torch.int32, device="cuda")
+    out = D.coarse_hist_topk(L, ctx, 1, k, ws, histogram=hist, fallback_flags=flags)
+    torch.cuda.synchronize()
+    assert sets_equal(out.cpu().numpy(), O.topk(x, lens, k))
+    assert (flags.cpu().numpy() == 0).all(), flags
+    assert ws.status() == 0
+
+
 @pytest.mark.parametrize("lo,hi", [(223.0, 1000.0), (17.0, 17.9), (0.5, 0.53)])
 def test_overflowing_bin_resolved_by_fine_histogram(lo, hi):
     """30000 distinct scores inside one coarse bin (the saturating bin, a unit
